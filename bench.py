@@ -1,0 +1,508 @@
+"""Benchmark of the W2A8 ternary GEMV path on GB300.
+
+Workload: the M=1 GEMV sweep over the BitNet-2B decode shapes of the W2A8
+kernel page (§7.1 table; §一 model shape) -- wqkv 3840x2560 (3 scale
+segments), wo 2560x2560, w13 13824x2560 (2 segments), w2 2560x6912 --
+with i.i.d. ternary weights (P(0) = 0.35), N(0,1) fp32 activation rows and
+bf16 weight scales in [0.5, 2).
+
+One step = one pass of the hot path over one batch of synthetic input:
+  1. bw_quant_act on the step's 64 fp32 activation rows (48 of K=2560,
+     16 of K=6912): per-row absmax to int8 + scale;
+  2. 64 bw_gemv_w2a8 calls: R = 16 replicas x the 4 shapes, each replica a
+     distinct weight buffer (278 MB in total, over twice the 126 MB L2, so
+     every call streams its weights from HBM).
+Each part is captured once as a CUDA graph; CUDA events between the parts
+give the GEMV kernel's own time inside the timed region.
+
+value = packed weight bytes per step / step time (GB/s, all GPUs).
+The reference arm (--impl reference) times the CPU oracle, single-threaded,
+on a bounded sample of the same workload, in the same unit.
+Multi-GPU: replicas only (the path has no exchange step); each rank runs the
+same workload on its own GPU.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import synth  # noqa: E402
+
+METRIC = ("W2A8 ternary GEMV µs/call & weight GB/s vs HBM peak (M=1); "
+          "layer-stack tok/s")
+WORKLOAD = ("M=1 W2A8 GEMV sweep over the BitNet-2B decode shapes: wqkv "
+            "3840x2560, wo 2560x2560, w13 13824x2560, w2 2560x6912")
+SHAPES = ["wqkv", "wo", "w13", "w2"]
+REPLICAS = 16
+FALLBACK_HBM_GBS = 6800.0
+
+
+def parse_args():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=50)
+    p.add_argument("--warmup", type=int, default=5)
+    p.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    p.add_argument("--replicas", type=int, default=REPLICAS)
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--cpu-seconds", type=float, default=12.0,
+                   help="bounded CPU work for the oracle baseline")
+    return p.parse_args()
+
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def algorithmic_bytes(N, K, n_ws):
+    """Packed weights + int8 x + bf16 y + fp32 s + bf16 ws of one call."""
+    return N * K // 4 + K + 2 * N + 4 + 2 * n_ws
+
+
+def weight_bytes(N, K):
+    return N * K // 4
+
+
+def read_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled during the timed
+    region (200 ms period)."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,"
+              "clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.path = os.path.join(ROOT, "gpurun_out",
+                                 f"clocks_rank{index}.csv")
+
+    def start(self):
+        try:
+            os.makedirs(os.path.dirname(self.path), exist_ok=True)
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index),
+                 f"--query-gpu={self.FIELDS}", "--format=csv,noheader",
+                 "-lms", "200"], stdout=self.f, stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [],
+                    "note": "nvidia-smi unavailable"}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.f.close()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown",
+                 "sw_power_cap"]
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1].split()[0]))
+                smax.append(float(parts[2].split()[0]))
+            except ValueError:
+                continue
+            for name, val in zip(names, parts[5:9]):
+                if val.lower().startswith("active"):
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def build_workload(torch, bw, dev, replicas, seed):
+    """Weights (repacked, one buffer per replica), scales, activations."""
+    shapes = {}
+    for si, name in enumerate(SHAPES):
+        N, K, bounds = synth.DECODE_SHAPES[name]
+        canon = synth.canonical_weights(seed + si, N, K)
+        canon_d = torch.from_numpy(canon).to(dev)
+        packed0 = bw.bw_repack(canon_d, N, K)
+        packed = [packed0] + [packed0.clone() for _ in range(replicas - 1)]
+        ws = synth.bf16_uniform(seed + si, len(bounds) - 1)
+        ws_d = torch.from_numpy(ws.view(np.int16)).to(dev).view(torch.bfloat16)
+        shapes[name] = dict(N=N, K=K, bounds=bounds, canon=canon, ws=ws,
+                            packed=packed, ws_d=ws_d)
+    # Activation rows of one step: for every replica and shape, one N(0,1)
+    # row of length K; grouped by K for the quantisation launches.
+    rows = {}
+    for name in SHAPES:
+        K = shapes[name]["K"]
+        rows.setdefault(K, []).append(name)
+    act = {}
+    for K, names in rows.items():
+        count = replicas * len(names)
+        xf = synth.normal_f32(seed + K, count * K).reshape(count, K)
+        act[K] = dict(names=names, xf=xf,
+                      xf_d=torch.from_numpy(xf).to(dev),
+                      q_d=torch.empty((count, K), dtype=torch.int8,
+                                      device=dev),
+                      s_d=torch.empty((count,), dtype=torch.float32,
+                                      device=dev))
+    outs = {name: [torch.empty((1, shapes[name]["N"]), dtype=torch.bfloat16,
+                               device=dev) for _ in range(replicas)]
+            for name in SHAPES}
+    return shapes, act, outs
+
+
+def act_row(act, shapes, name, r):
+    """(q row view, s element view) of replica r of a shape."""
+    K = shapes[name]["K"]
+    a = act[K]
+    idx = r * len(a["names"]) + a["names"].index(name)
+    return a["q_d"][idx:idx + 1], a["s_d"][idx:idx + 1]
+
+
+def check_sample(bw, shapes, act, outs):
+    """Cheap parity check of the bench's own outputs: 64 sampled rows of
+    replica 0 of every shape against the oracle."""
+    import oracle
+    for name in SHAPES:
+        sh = shapes[name]
+        N, K = sh["N"], sh["K"]
+        q_d, s_d = act_row(act, shapes, name, 0)
+        q = q_d.cpu().numpy()
+        s = s_d.cpu().numpy()
+        sel = (synth.u64(1, 77, 64) % np.uint64(N)).astype(np.int64)
+        y = outs[name][0].view(__import__("torch").int16).cpu().numpy() \
+            .view(np.uint16)[0]
+        seg = np.searchsorted(np.asarray(sh["bounds"]), sel, side="right") - 1
+        for i, n in enumerate(sel):
+            ref = oracle.gemv(q, sh["canon"][n:n + 1], s,
+                              sh["ws"][seg[i]:seg[i] + 1], [0, 1], 1, K)[0, 0]
+            g = synth.bf16_bits_to_f32(np.array([y[n]], np.uint16))[0]
+            r_ = synth.bf16_bits_to_f32(np.array([ref], np.uint16))[0]
+            ulp = 2.0 ** (np.floor(np.log2(max(abs(r_), 1e-38))) - 7)
+            if abs(float(g) - float(r_)) > ulp:
+                raise AssertionError(f"bench output mismatch {name} row {n}")
+    return True
+
+
+def run_ours(args):
+    import torch
+    import bit_gemv_bitlinear_gb300 as bw
+
+    rank, world, local = dist_env()
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+
+    R = args.replicas
+    seed = synth.base_seed(1)
+    shapes, act, outs = build_workload(torch, bw, dev, R, seed)
+    stream = torch.cuda.Stream(device=dev)
+
+    def launch_quant():
+        for K, a in act.items():
+            bw.bw_quant_act(a["xf_d"], a["q_d"], a["s_d"], stream=stream)
+
+    def launch_shape(name):
+        sh = shapes[name]
+        for r in range(R):
+            q_d, s_d = act_row(act, shapes, name, r)
+            bw.bw_gemv_w2a8(q_d, sh["packed"][r], s_d, sh["ws_d"],
+                            sh["bounds"], sh["N"], sh["K"], y=outs[name][r],
+                            stream=stream)
+
+    # Capture the parts of a step as CUDA graphs (after an eager warm-up).
+    with torch.cuda.stream(stream):
+        launch_quant()
+        for name in SHAPES:
+            launch_shape(name)
+    stream.synchronize()
+    graphs = {}
+    parts = ["quant"] + SHAPES
+    for part in parts:
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            if part == "quant":
+                launch_quant()
+            else:
+                launch_shape(part)
+        graphs[part] = g
+    torch.cuda.synchronize()
+
+    def step(evs=None):
+        with torch.cuda.stream(stream):
+            if evs is not None:
+                evs[0].record(stream)
+            for i, part in enumerate(parts):
+                graphs[part].replay()
+                if evs is not None:
+                    evs[i + 1].record(stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    check_sample(bw, shapes, act, outs)
+
+    K_steps = args.steps
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(len(parts) + 1)]
+           for _ in range(K_steps)]
+    start = torch.cuda.Event(enable_timing=True)
+    end = torch.cuda.Event(enable_timing=True)
+    sampler = ClockSampler(local)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    sampler.start()
+    time.sleep(0.3)
+    start.record(stream)
+    for k in range(K_steps):
+        step(evs[k])
+    end.record(stream)
+    torch.cuda.synchronize()
+    clocks = sampler.stop()
+    total_ms = start.elapsed_time(end)
+    part_ms = {p: 0.0 for p in parts}
+    for k in range(K_steps):
+        for i, p in enumerate(parts):
+            part_ms[p] += evs[k][i].elapsed_time(evs[k][i + 1])
+    if world > 1:
+        t = torch.tensor([total_ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        total_ms = float(t.item())
+
+    wbytes_step = R * sum(weight_bytes(shapes[n]["N"], shapes[n]["K"])
+                          for n in SHAPES)
+    ms_per_step = total_ms / K_steps
+    value = world * wbytes_step / (ms_per_step * 1e-3) / 1e9
+
+    # Per-shape GEMV figures from the events inside the timed region.
+    per_call = {}
+    alg_total, gemv_ms = 0, 0.0
+    for n in SHAPES:
+        sh = shapes[n]
+        us = part_ms[n] * 1e3 / (K_steps * R)
+        ab = algorithmic_bytes(sh["N"], sh["K"], len(sh["bounds"]) - 1)
+        per_call[n] = {"N": sh["N"], "K": sh["K"], "us_per_call": round(us, 3),
+                       "weight_GBps": round(weight_bytes(sh["N"], sh["K"])
+                                            / (us * 1e3), 1),
+                       "alg_GBps": round(ab / (us * 1e3), 1)}
+        alg_total += ab * R * K_steps
+        gemv_ms += part_ms[n]
+    peak, peak_kind = read_peaks()
+    achieved = alg_total / (gemv_ms * 1e-3) / 1e9
+    gemv_launches = len(SHAPES) * R
+    quant_launches = len(act)
+
+    # End to end: the same step with host buffers -- pinned H2D of the
+    # step's fp32 activation rows, the step, D2H of every output.
+    host_in = {K: torch.from_numpy(a["xf"]).pin_memory()
+               for K, a in act.items()}
+    host_out = {n: [torch.empty_like(o, device="cpu").pin_memory()
+                    for o in outs[n]] for n in SHAPES}
+    h2d = sum(t.numel() * 4 for t in host_in.values())
+    d2h = sum(o.numel() * 2 for n in SHAPES for o in outs[n])
+
+    def e2e_step():
+        with torch.cuda.stream(stream):
+            for K, a in act.items():
+                a["xf_d"].copy_(host_in[K], non_blocking=True)
+            for part in parts:
+                graphs[part].replay()
+            for n in SHAPES:
+                for r in range(R):
+                    host_out[n][r].copy_(outs[n][r], non_blocking=True)
+
+    for _ in range(args.warmup):
+        e2e_step()
+    torch.cuda.synchronize()
+    e_start = torch.cuda.Event(enable_timing=True)
+    e_end = torch.cuda.Event(enable_timing=True)
+    e_start.record(stream)
+    for _ in range(K_steps):
+        e2e_step()
+    e_end.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e_start.elapsed_time(e_end) / K_steps
+    e2e_value = world * wbytes_step / (e2e_ms * 1e-3) / 1e9
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(shapes, act, args.cpu_seconds)
+
+    if rank == 0:
+        line = {
+            "metric": METRIC,
+            "value": round(value, 2),
+            "unit": "GB/s",
+            "n_gpus": world,
+            "steps": K_steps,
+            "warmup": args.warmup,
+            "ms_per_step": round(ms_per_step, 5),
+            "higher_is_better": True,
+            "scaling": "weak",
+            "vs_baseline": None,
+            "dtype": "int8",
+            "data": "synthetic",
+            "config": {
+                "workload": WORKLOAD,
+                "replicas": R,
+                "gemv_calls_per_step": gemv_launches,
+                "weight_bytes_per_step": wbytes_step,
+                "l2": "inputs larger than L2: 16 distinct weight buffers "
+                      "per shape, 278 MB per step vs 126 MB L2",
+                "graphs": "each step part is one CUDA graph replay",
+                "parallelism": "replicas" if world > 1 else "single GPU",
+            },
+            "per_call": per_call,
+            "roofline": {
+                "bound": "hbm",
+                "kernel": "gemv_w2a8_kernel",
+                "achieved": round(achieved, 1),
+                "peak": peak,
+                "peak_kind": peak_kind,
+                "unit": "GB/s",
+                "frac": round(achieved / peak, 4),
+                "traffic": None,
+            },
+            "e2e": {"value": round(e2e_value, 2), "unit": "GB/s",
+                    "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                    "ms_per_step": round(e2e_ms, 5)},
+            "gpu_launches": (gemv_launches + quant_launches) * K_steps,
+            "clocks": clocks,
+        }
+        if cpu is not None:
+            line["cpu_baseline"] = cpu
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+def cpu_baseline(shapes, act, seconds):
+    """The oracle as it stands, single-threaded, on whole steps of the
+    workload restricted to one replica, repeated for a bounded time."""
+    import oracle
+    oracle.build()
+    t0 = time.perf_counter()
+    reps, wbytes = 0, 0
+    while True:
+        for K, a in act.items():
+            oracle.quant_act(a["xf"][: len(a["names"])])
+        for name in SHAPES:
+            sh = shapes[name]
+            K = sh["K"]
+            a = act[K]
+            q, s = oracle.quant_act(a["xf"][a["names"].index(name)])
+            oracle.gemv(q, sh["canon"], s, sh["ws"], sh["bounds"], sh["N"], K)
+            wbytes += weight_bytes(sh["N"], K)
+        reps += 1
+        if time.perf_counter() - t0 >= seconds:
+            break
+    dt = time.perf_counter() - t0
+    return {"value": round(wbytes / dt / 1e9, 4), "unit": "GB/s", "cores": 1,
+            "kind": "oracle",
+            "sample": f"{reps} pass(es) of quant + the 4 decode-shape GEMVs "
+                      f"(one replica), {dt:.1f} s on 1 host core"}
+
+
+def run_reference(args):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return
+    import torch  # noqa: F401  (only for the shared generators' dtype use)
+    seed = synth.base_seed(1)
+    shapes, act = {}, {}
+    for si, name in enumerate(SHAPES):
+        N, K, bounds = synth.DECODE_SHAPES[name]
+        shapes[name] = dict(N=N, K=K, bounds=bounds,
+                            canon=synth.canonical_weights(seed + si, N, K),
+                            ws=synth.bf16_uniform(seed + si, len(bounds) - 1))
+    for name in SHAPES:
+        K = shapes[name]["K"]
+        act.setdefault(K, {"names": []})["names"].append(name)
+    for K, a in act.items():
+        count = len(a["names"])
+        a["xf"] = synth.normal_f32(seed + K, count * K).reshape(count, K)
+
+    import oracle
+    oracle.build()
+
+    def one_step():
+        wb = 0
+        for K, a in act.items():
+            oracle.quant_act(a["xf"])
+        for name in SHAPES:
+            sh = shapes[name]
+            a = act[sh["K"]]
+            q, s = oracle.quant_act(a["xf"][a["names"].index(name)])
+            oracle.gemv(q, sh["canon"], s, sh["ws"], sh["bounds"], sh["N"],
+                        sh["K"])
+            wb += weight_bytes(sh["N"], sh["K"])
+        return wb
+
+    for _ in range(args.warmup):
+        one_step()
+    t0 = time.perf_counter()
+    wb = 0
+    for _ in range(args.steps):
+        wb += one_step()
+    dt = time.perf_counter() - t0
+    value = wb / dt / 1e9
+    sample = (f"each step: quant + the 4 decode-shape GEMVs of one replica "
+              f"(1/{REPLICAS} of a GPU step); {args.steps} steps in "
+              f"{dt:.1f} s on 1 host core")
+    line = {
+        "impl": "reference",
+        "metric": METRIC, "value": round(value, 4), "unit": "GB/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(dt / args.steps * 1e3, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "int8", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "replicas": 1,
+                   "implementation": "CPU oracle (plain C, single thread)"},
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s",
+                         "cores": 1, "kind": "oracle", "sample": sample},
+        "e2e": {"value": round(value, 4), "unit": "GB/s",
+                "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse_args()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

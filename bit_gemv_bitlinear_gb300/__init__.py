@@ -1,0 +1,184 @@
+"""Python binding of libbw, the GB300 (sm_103a) W2A8 ternary GEMV library.
+
+Argument marshalling only: every step of the path runs in the library's CUDA
+kernels, reached through the C ABI of ``include/bw.h``.  PyTorch provides
+device memory and streams.  There is no fallback: if ``libbw.so`` is missing
+the import fails (build it with ``python -m bit_gemv_bitlinear_gb300.build``
+or ``__graft_entry__.build()``).
+
+Function names follow the C ABI: ``bw_quant_act``, ``bw_repack``,
+``bw_unrepack``, ``bw_gemv_w2a8``, ``bw_gemv_w2a8_acc``.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libbw.so")
+
+if not os.path.exists(LIB_PATH):
+    raise ImportError(
+        f"{LIB_PATH} is missing: build the CUDA library first "
+        "(python -m bit_gemv_bitlinear_gb300.build)")
+
+_lib = ctypes.CDLL(LIB_PATH)
+
+BW_OK = 0
+STATUS_NAMES = {0: "BW_OK", 1: "BW_ERR_INVALID_ARG",
+                2: "BW_ERR_UNSUPPORTED_SHAPE", 3: "BW_ERR_MISALIGNED",
+                4: "BW_ERR_BAD_CODE", 5: "BW_ERR_CUDA", 6: "BW_ERR_TIMEOUT"}
+MAX_K, MAX_N, MAX_M, MAX_WS = 65536, 1 << 24, 4096, 8
+
+# Every symbol the C ABI declares (checked by the tests without a GPU).
+EXPORTS = ("bw_status_string", "bw_last_cuda_error", "bw_version",
+           "bw_quant_act", "bw_repack_bytes", "bw_repack", "bw_unrepack",
+           "bw_gemv_w2a8", "bw_gemv_w2a8_acc")
+
+_P = ctypes.c_void_p
+_I = ctypes.c_int
+_SIGS = {
+    "bw_status_string": (ctypes.c_char_p, [_I]),
+    "bw_last_cuda_error": (_I, []),
+    "bw_version": (_I, []),
+    "bw_quant_act": (_I, [_P, _I, _I, _P, _P, _P]),
+    "bw_repack_bytes": (ctypes.c_size_t, [_I, _I]),
+    "bw_repack": (_I, [_P, _I, _I, _P, _P]),
+    "bw_unrepack": (_I, [_P, _I, _I, _P, _P]),
+    "bw_gemv_w2a8": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _P, _P]),
+    "bw_gemv_w2a8_acc": (_I, [_P, _P, _I, _I, _I, _P, _P]),
+}
+for _name, (_res, _args) in _SIGS.items():
+    _fn = getattr(_lib, _name)
+    _fn.restype = _res
+    _fn.argtypes = _args
+
+
+class BwError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        name = STATUS_NAMES.get(status, str(status))
+        extra = ""
+        if name == "BW_ERR_CUDA":
+            extra = f" (cudaError {_lib.bw_last_cuda_error()})"
+        super().__init__(f"{what}: {name}{extra}")
+
+
+def _check(status: int, what: str):
+    if status != BW_OK:
+        raise BwError(status, what)
+
+
+def _stream(stream) -> int:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def _dev(t: torch.Tensor, dtype, name: str) -> int:
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    return t.data_ptr()
+
+
+def version() -> int:
+    return _lib.bw_version()
+
+
+def status_string(status: int) -> str:
+    return _lib.bw_status_string(status).decode()
+
+
+def bw_repack_bytes(N: int, K: int) -> int:
+    return int(_lib.bw_repack_bytes(N, K))
+
+
+def bw_quant_act(x: torch.Tensor, q: torch.Tensor | None = None,
+                 s: torch.Tensor | None = None, stream=None):
+    """fp32 x [M][K] -> (int8 q [M][K], fp32 s [M]); s = 127/absmax."""
+    x2 = x if x.dim() == 2 else x.reshape(1, -1)
+    M, K = x2.shape
+    if q is None:
+        q = torch.empty((M, K), dtype=torch.int8, device=x.device)
+    if s is None:
+        s = torch.empty((M,), dtype=torch.float32, device=x.device)
+    _check(_lib.bw_quant_act(_dev(x2, torch.float32, "x"), M, K,
+                             _dev(q, torch.int8, "q"),
+                             _dev(s, torch.float32, "s"), _stream(stream)),
+           "bw_quant_act")
+    return q, s
+
+
+def bw_repack(canon: torch.Tensor, N: int, K: int,
+              packed: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """Canonical bytes uint8 [N][K/4] -> device layout (synchronising)."""
+    if packed is None:
+        size = bw_repack_bytes(N, K)
+        if size == 0:
+            raise BwError(2, "bw_repack_bytes")
+        packed = torch.empty((size,), dtype=torch.uint8, device=canon.device)
+    _check(_lib.bw_repack(_dev(canon, torch.uint8, "canon"), N, K,
+                          _dev(packed, torch.uint8, "packed"),
+                          _stream(stream)), "bw_repack")
+    return packed
+
+
+def bw_unrepack(packed: torch.Tensor, N: int, K: int,
+                canon: torch.Tensor | None = None, stream=None):
+    if canon is None:
+        canon = torch.empty((N, K // 4), dtype=torch.uint8,
+                            device=packed.device)
+    _check(_lib.bw_unrepack(_dev(packed, torch.uint8, "packed"), N, K,
+                            _dev(canon, torch.uint8, "canon"),
+                            _stream(stream)), "bw_unrepack")
+    return canon
+
+
+def _bounds_array(bounds):
+    arr = (ctypes.c_int * len(bounds))(*[int(b) for b in bounds])
+    return arr
+
+
+def bw_gemv_w2a8(x: torch.Tensor, packed: torch.Tensor, s: torch.Tensor,
+                 ws: torch.Tensor, ws_bounds, N: int, K: int,
+                 y: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """bf16 y [M][N] = bf16((acc / s[m]) * ws[seg(n)]); ws is bf16 [n_ws],
+    ws_bounds a host sequence of n_ws + 1 ints from 0 to N."""
+    x2 = x if x.dim() == 2 else x.reshape(1, -1)
+    M = x2.shape[0]
+    if x2.shape[1] != K:
+        raise ValueError("x has the wrong K")
+    if y is None:
+        y = torch.empty((M, N), dtype=torch.bfloat16, device=x.device)
+    b = _bounds_array(ws_bounds)
+    _check(_lib.bw_gemv_w2a8(
+        _dev(x2, torch.int8, "x"), _dev(packed, torch.uint8, "packed"),
+        _dev(s, torch.float32, "s"), _dev(ws, torch.bfloat16, "ws"),
+        ctypes.cast(b, _P), len(ws_bounds) - 1, M, N, K,
+        _dev(y, torch.bfloat16, "y"), _stream(stream)), "bw_gemv_w2a8")
+    return y
+
+
+def bw_gemv_w2a8_acc(x: torch.Tensor, packed: torch.Tensor, N: int, K: int,
+                     acc: torch.Tensor | None = None,
+                     stream=None) -> torch.Tensor:
+    """Exact int32 acc [M][N] of the same product, no scales."""
+    x2 = x if x.dim() == 2 else x.reshape(1, -1)
+    M = x2.shape[0]
+    if x2.shape[1] != K:
+        raise ValueError("x has the wrong K")
+    if acc is None:
+        acc = torch.empty((M, N), dtype=torch.int32, device=x.device)
+    _check(_lib.bw_gemv_w2a8_acc(
+        _dev(x2, torch.int8, "x"), _dev(packed, torch.uint8, "packed"), M, N,
+        K, _dev(acc, torch.int32, "acc"), _stream(stream)),
+        "bw_gemv_w2a8_acc")
+    return acc

@@ -1,0 +1,68 @@
+// bw_internal.cuh -- declarations shared by the translation units of libbw.
+// Nothing here is visible through the C ABI (include/bw.h).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <stdint.h>
+
+#include "../../include/bw.h"
+
+namespace bw {
+
+// Device layout geometry (see the layout specification in bw.h).
+constexpr int kGroupRows = 8;         // rows per row group
+constexpr int kChunkWeights = 64;     // weights per 16-byte chunk
+constexpr int kChunkBytes = 16;
+constexpr int kGroupChunkBytes = 128; // one chunk of all 8 rows of a group
+
+inline int64_t padded_rows(int N) { return (int64_t(N) + 7) / 8 * 8; }
+inline int chunks_per_row(int K) { return (K + 63) / 64; }
+
+// Weight-scale segments passed by value to the kernels.
+struct WsSegments {
+  int n_ws;
+  int bounds[BW_MAX_WS + 1];
+};
+
+// Arguments of one GEMV launch over an M-tile of at most 4 rows.
+struct GemvArgs {
+  const int8_t *x;        // [mt][x_ld]
+  const uint8_t *w;       // device layout
+  const float *s;         // [mt] (bf16 mode only)
+  const __nv_bfloat16 *ws;
+  void *out;              // bf16 [mt][out_ld] or int32 [mt][out_ld]
+  int K, N;
+  int x_ld, out_ld;
+  int chunks;             // C = Kpad / 64
+  int n_groups;           // Npad / 8
+  int passes;             // K passes of warps*jb quads each
+  int vec_x;              // x rows are 16-byte aligned and K % 16 == 0
+  WsSegments seg;
+};
+
+// Launch configuration chosen by the host dispatcher.
+struct GemvPlan {
+  int mt;      // activation rows per launch (1, 2 or 4)
+  int rg;      // row groups per CTA (1, 2 or 4)
+  int jb;      // chunk quads per warp and pass (1..4)
+  int warps;   // warps per CTA
+  int passes;  // K passes
+  int grid;    // CTAs
+};
+
+GemvPlan plan_gemv(int mt, int N, int K, int num_sms);
+cudaError_t launch_gemv(const GemvPlan &plan, const GemvArgs &args,
+                        bool acc_out, cudaStream_t stream);
+
+cudaError_t launch_quant_act(const float *x, int M, int K, int8_t *q,
+                             float *s, cudaStream_t stream);
+cudaError_t launch_repack(const uint8_t *canon, int N, int K,
+                          uint8_t *packed, unsigned int *bad,
+                          cudaStream_t stream);
+cudaError_t launch_unrepack(const uint8_t *packed, int N, int K,
+                            uint8_t *canon, cudaStream_t stream);
+
+int device_sm_count();
+
+}  // namespace bw

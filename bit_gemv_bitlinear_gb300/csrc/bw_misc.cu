@@ -1,0 +1,133 @@
+// bw_misc.cu -- activation quantisation and weight repacking for sm_103a.
+//
+// Sources: "BitNet GPU 推理框架：从零构建 W2A8 的 2-bit 大模型 CUDA GEMV 内核",
+// §六 item 3 (per-row absmax quantisation s = 127 / max|x|, round, clamp to
+// [-128, 127]) and §5.1/§5.2 (offline packing of the ternary weights; the
+// device layout produced here is specified in bw.h).
+#include "bw_internal.cuh"
+
+namespace bw {
+namespace {
+
+constexpr int kQuantThreads = 256;
+
+// One CTA per activation row.  Pass 1: absmax (max is exact in any order).
+// Pass 2: q = clamp(rint(x * s), -128, 127) with s = 127 / max(absmax, 1e-5),
+// all in IEEE fp32; rintf rounds half to even.
+__global__ void __launch_bounds__(kQuantThreads)
+quant_act_kernel(const float *__restrict__ x, int K, int8_t *__restrict__ q,
+                 float *__restrict__ s) {
+  __shared__ float warp_max[kQuantThreads / 32];
+  const int m = blockIdx.x;
+  const float *xr = x + size_t(m) * K;
+  int8_t *qr = q + size_t(m) * K;
+
+  float amax = 0.0f;
+  for (int k = threadIdx.x; k < K; k += blockDim.x)
+    amax = fmaxf(amax, fabsf(xr[k]));
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1)
+    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+  if ((threadIdx.x & 31) == 0) warp_max[threadIdx.x >> 5] = amax;
+  __syncthreads();
+  amax = 0.0f;
+  for (int w = 0; w < int(blockDim.x >> 5); ++w) amax = fmaxf(amax, warp_max[w]);
+
+  const float scale = 127.0f / fmaxf(amax, 1e-5f);
+  if (threadIdx.x == 0) s[m] = scale;
+  for (int k = threadIdx.x; k < K; k += blockDim.x) {
+    const float v = fminf(fmaxf(rintf(xr[k] * scale), -128.0f), 127.0f);
+    qr[k] = static_cast<int8_t>(static_cast<int>(v));
+  }
+}
+
+// One thread per 16-byte output chunk, enumerated in memory order:
+// idx = ((group * C) + j) * 8 + row_in_group.
+__global__ void repack_kernel(const uint8_t *__restrict__ canon, int N, int K,
+                              int chunks, int64_t total,
+                              uint8_t *__restrict__ packed,
+                              unsigned int *__restrict__ bad) {
+  const int64_t row_bytes = K / 4;
+  for (int64_t idx = blockIdx.x * int64_t(blockDim.x) + threadIdx.x;
+       idx < total; idx += int64_t(gridDim.x) * blockDim.x) {
+    const int64_t r = idx % kGroupRows;
+    const int64_t j = (idx / kGroupRows) % chunks;
+    const int64_t grp = idx / (int64_t(kGroupRows) * chunks);
+    const int64_t n = grp * kGroupRows + r;
+    uint32_t word[4] = {0u, 0u, 0u, 0u};
+    bool bad_code = false;
+    for (int i = 0; i < kChunkWeights; ++i) {
+      const int64_t k = j * kChunkWeights + i;
+      uint32_t code = 1u;  // padding: weight 0
+      if (n < N && k < K) {
+        code = (canon[n * row_bytes + k / 4] >> (2 * (k % 4))) & 3u;
+        bad_code |= code == 3u;
+      }
+      const int t = i / 16, e = i % 16;
+      word[t] |= code << (8 * (e % 4) + 2 * (e / 4));
+    }
+    if (bad_code) atomicOr(bad, 1u);
+    reinterpret_cast<uint4 *>(packed)[idx] =
+        make_uint4(word[0], word[1], word[2], word[3]);
+  }
+}
+
+// One thread per canonical byte.
+__global__ void unrepack_kernel(const uint8_t *__restrict__ packed, int N,
+                                int K, int chunks,
+                                uint8_t *__restrict__ canon) {
+  const int64_t row_bytes = K / 4;
+  const int64_t total = int64_t(N) * row_bytes;
+  for (int64_t idx = blockIdx.x * int64_t(blockDim.x) + threadIdx.x;
+       idx < total; idx += int64_t(gridDim.x) * blockDim.x) {
+    const int64_t n = idx / row_bytes;
+    const int64_t b = idx % row_bytes;
+    uint32_t byte = 0u;
+    for (int t = 0; t < 4; ++t) {
+      const int64_t k = 4 * b + t;
+      const int64_t j = k / kChunkWeights;
+      const int wt = int(k % kChunkWeights) / 16;
+      const int e = int(k % 16);
+      const int64_t off =
+          ((n / kGroupRows) * chunks + j) * kGroupChunkBytes +
+          (n % kGroupRows) * kChunkBytes + wt * 4 + (e % 4);
+      const uint32_t code = (packed[off] >> (2 * (e / 4))) & 3u;
+      byte |= code << (2 * t);
+    }
+    canon[idx] = static_cast<uint8_t>(byte);
+  }
+}
+
+int grid_for(int64_t items, int threads) {
+  const int64_t blocks = (items + threads - 1) / threads;
+  const int64_t cap = int64_t(device_sm_count()) * 16;
+  return int(blocks < cap ? (blocks > 0 ? blocks : 1) : cap);
+}
+
+}  // namespace
+
+cudaError_t launch_quant_act(const float *x, int M, int K, int8_t *q,
+                             float *s, cudaStream_t stream) {
+  quant_act_kernel<<<M, kQuantThreads, 0, stream>>>(x, K, q, s);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_repack(const uint8_t *canon, int N, int K,
+                          uint8_t *packed, unsigned int *bad,
+                          cudaStream_t stream) {
+  const int chunks = chunks_per_row(K);
+  const int64_t total = padded_rows(N) * chunks;
+  repack_kernel<<<grid_for(total, 256), 256, 0, stream>>>(
+      canon, N, K, chunks, total, packed, bad);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_unrepack(const uint8_t *packed, int N, int K,
+                            uint8_t *canon, cudaStream_t stream) {
+  const int64_t total = int64_t(N) * (K / 4);
+  unrepack_kernel<<<grid_for(total, 256), 256, 0, stream>>>(
+      packed, N, K, chunks_per_row(K), canon);
+  return cudaGetLastError();
+}
+
+}  // namespace bw

@@ -1,0 +1,156 @@
+/*
+ * bw.h -- C ABI of libbw, a GB300 (sm_103a) library for the BitNet b1.58
+ * ternary-weight x int8-activation (W2A8) linear layer at decode.
+ *
+ * Sources (page title and section):
+ *   [W2A8] "BitNet GPU 推理框架：从零构建 W2A8 的 2-bit 大模型 CUDA GEMV 内核":
+ *          §2.2 the kernel's C interface (int8 activations, 4:1 packed ternary
+ *          weights, bf16 output, activation scale s, weight scales ws, M, N,
+ *          K, stream); §5.1/§5.2 packing, permutation and word interleave;
+ *          §5.3 dp4a dot product, shuffle reduction and the scale epilogue;
+ *          §六 item 3 the per-row absmax activation quantisation;
+ *          §一 and §4.1 the BitNet-2B decoder layer the stack chains.
+ *   [ESP]  "Յոթ ESP32-S3 տախտակ ... 1,58 բիթանոց լեզվական մոդել", section
+ *          "1,58 բիթ մեկ կշռի համար": ternary weights, four per byte.
+ *
+ * Conventions for every call:
+ *   - Tensor arguments are DEVICE pointers owned by the caller; the library
+ *     never frees them and keeps no reference after the call returns.
+ *   - Calls are asynchronous on `stream` unless their comment says otherwise;
+ *     nothing is synchronised on the GEMV path.
+ *   - Arguments are validated on the host before any launch.  A failed check
+ *     returns a status and launches nothing.  A launch error is returned as
+ *     BW_ERR_CUDA (the CUDA error is then available from cudaGetLastError in
+ *     this library's runtime instance via bw_last_cuda_error()).
+ *   - bf16 values are passed as their 16-bit patterns (the upper half of an
+ *     IEEE fp32 pattern), type bw_bf16; __nv_bfloat16 has the same layout.
+ *   - Matrices are row-major.  Sizes are element counts.
+ *
+ * Canonical weight format (input of bw_repack, output of bw_unrepack):
+ *   N rows of K/4 bytes; weight w[n][k] in {-1, 0, +1} is stored as the code
+ *   c = w + 1 in {0, 1, 2} at bits 2t..2t+1 (t = k mod 4) of byte k/4 of row
+ *   n.  Code 3 is invalid.  K must be a multiple of 4.
+ *
+ * Device weight layout (output of bw_repack, input of the GEMV):
+ *   Rows are padded to Npad = ceil(N/8)*8 and K to Kpad = ceil(K/64)*64
+ *   with code 1 (weight 0).  A 16-byte chunk holds the 64 weights of one row
+ *   with k in [64j, 64j+64) (chunk j).  Its 32-bit word t (bytes 4t..4t+3)
+ *   holds k in [64j+16t, 64j+16t+16); element e = k mod 16 of the word sits
+ *   in byte (e mod 4) at bits 2*(e div 4) -- the [W2A8] §5.2 word interleave
+ *   (field order 0,4,8,12,1,5,9,13,2,6,10,14,3,7,11,15).  Chunks are stored
+ *   by groups of 8 rows: chunk (n, j) starts at byte
+ *       ((n/8) * C + j) * 128 + (n mod 8) * 16,       C = Kpad/64,
+ *   so the 8 rows x Kpad weights of a row group are one contiguous run of
+ *   2*Kpad bytes.  Total size: bw_repack_bytes(N, K) = Npad * Kpad / 4.
+ */
+#ifndef BW_H
+#define BW_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* cudaStream_t without requiring the CUDA headers in the caller. */
+typedef struct CUstream_st *bw_stream_t;
+typedef uint16_t bw_bf16;
+
+typedef enum {
+    BW_OK = 0,
+    BW_ERR_INVALID_ARG = 1,       /* null pointer, negative size, bad bounds */
+    BW_ERR_UNSUPPORTED_SHAPE = 2, /* a size outside the limits below        */
+    BW_ERR_MISALIGNED = 3,        /* a pointer without its required alignment */
+    BW_ERR_BAD_CODE = 4,          /* a canonical weight code equal to 3      */
+    BW_ERR_CUDA = 5,              /* a CUDA runtime call or launch failed    */
+    BW_ERR_TIMEOUT = 6            /* a bounded device-side wait gave up      */
+} bw_status;
+
+/* Limits checked by every call. */
+#define BW_MAX_K 65536      /* reduction length                           */
+#define BW_MAX_N (1 << 24)  /* output rows                                */
+#define BW_MAX_M 4096       /* activation rows of one GEMV call           */
+#define BW_MAX_WS 8         /* weight-scale segments of one GEMV call     */
+
+/* Human-readable name of a status.  Never returns NULL. */
+const char *bw_status_string(bw_status status);
+
+/* The CUDA error code of the last BW_ERR_CUDA returned on this thread
+ * (cudaSuccess = 0 if none). */
+int bw_last_cuda_error(void);
+
+/* Library version, major * 10000 + minor * 100 + patch. */
+int bw_version(void);
+
+/* ------------------------------------------------------------------------
+ * bw_quant_act -- per-row absmax quantisation of activations to int8.
+ * [W2A8] §六 item 3: s = 127 / max|x|, q = round(x * s) clamped to
+ * [-128, 127] (round half to even, as PyTorch's round).  The absmax is
+ * floored at 1e-5 so an all-zero row gives q = 0 (reading: the floor the
+ * page's weight quantiser of §4.2 uses).  fp32 arithmetic throughout.
+ *   x  fp32 [M][K] device, 4-byte aligned; finite values.
+ *   q  int8 [M][K] device (output).
+ *   s  fp32 [M]    device (output): the scale that multiplied x.
+ *   1 <= M <= BW_MAX_M, 1 <= K <= BW_MAX_K.
+ * ---------------------------------------------------------------------- */
+bw_status bw_quant_act(const float *x, int M, int K, int8_t *q, float *s,
+                       bw_stream_t stream);
+
+/* ------------------------------------------------------------------------
+ * bw_repack -- canonical ternary bytes to the device weight layout
+ * (offline, once per weight; [W2A8] §5.1/§5.2 describe the page's own
+ * permutation and interleave, which this layout replaces).
+ *   canon   uint8 [N][K/4] device, canonical format (any alignment).
+ *   packed  uint8 [bw_repack_bytes(N, K)] device, 16-byte aligned (output).
+ *   1 <= N <= BW_MAX_N, 4 <= K <= BW_MAX_K, K % 4 == 0.
+ * Returns BW_ERR_BAD_CODE if any code is 3 (the output is then undefined).
+ * This call allocates a 4-byte status word with cudaMallocAsync on `stream`
+ * and SYNCHRONISES `stream` before returning (it is not for the hot path).
+ * ---------------------------------------------------------------------- */
+size_t bw_repack_bytes(int N, int K);
+bw_status bw_repack(const uint8_t *canon, int N, int K, uint8_t *packed,
+                    bw_stream_t stream);
+
+/* bw_unrepack -- the inverse of bw_repack: device layout to canonical bytes
+ * [N][K/4] (padding is dropped).  Asynchronous; same limits as bw_repack;
+ * packed must be 16-byte aligned. */
+bw_status bw_unrepack(const uint8_t *packed, int N, int K, uint8_t *canon,
+                      bw_stream_t stream);
+
+/* ------------------------------------------------------------------------
+ * bw_gemv_w2a8 -- y = bf16( (acc / s[m]) * ws[seg(n)] ),
+ *                 acc[m][n] = sum_k w[n][k] * x[m][k]  (exact int32).
+ * [W2A8] §2.2 (the interface: int8 x, packed int2 W, bf16 out, s, ws, M,
+ * N, K, stream), §5.3 (int32 dp4a accumulation, bf16 epilogue), §4.2 (one
+ * weight scale per fused sub-projection).  The page's kernel multiplies by
+ * s; with s = 127/absmax (§六 item 3) the dimensionally consistent reading
+ * divides, which is what this call does.  Every fp32 step is IEEE (no fast
+ * math) and there is a single rounding to bf16, to nearest even.
+ *   x          int8 [M][K] device, 4-byte aligned.
+ *   packed     device weight layout from bw_repack(N, K), 16-byte aligned.
+ *   s          fp32 [M] device: activation scales (as bw_quant_act writes).
+ *   ws         bf16 [n_ws] device: weight scales.
+ *   ws_bounds  int [n_ws + 1] HOST: 0 = b[0] < b[1] < ... < b[n_ws] = N;
+ *              row n uses ws[i] for b[i] <= n < b[i+1] (e.g. the fused
+ *              q|k|v projection of BitNet-2B: {0, 2560, 3200, 3840}).
+ *   y          bf16 [M][N] device, 2-byte aligned (output).
+ *   1 <= M <= BW_MAX_M, 1 <= N <= BW_MAX_N, 4 <= K <= BW_MAX_K, K % 4 == 0,
+ *   1 <= n_ws <= BW_MAX_WS.  M <= 15 runs on CUDA cores (int dp4a);
+ *   larger M is processed in row tiles.
+ * ---------------------------------------------------------------------- */
+bw_status bw_gemv_w2a8(const int8_t *x, const uint8_t *packed, const float *s,
+                       const bw_bf16 *ws, const int *ws_bounds, int n_ws,
+                       int M, int N, int K, bw_bf16 *y, bw_stream_t stream);
+
+/* bw_gemv_w2a8_acc -- the exact int32 accumulators acc[M][N] of the same
+ * product, without scales (the page's exact-int32 test of §三).  acc is
+ * int32 [M][N] device, 4-byte aligned.  Same limits as bw_gemv_w2a8. */
+bw_status bw_gemv_w2a8_acc(const int8_t *x, const uint8_t *packed, int M,
+                           int N, int K, int32_t *acc, bw_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* BW_H */

@@ -14,6 +14,7 @@ from __future__ import annotations
 
 import ctypes
 import os
+import platform
 import subprocess
 
 import numpy as np
@@ -31,7 +32,11 @@ class OracleError(RuntimeError):
 
 def build(force: bool = False) -> str:
     """Compile oracle.c into liboracle.so with the host gcc (no CUDA)."""
-    if (not force and os.path.exists(_LIB)
+    stamp_path = _LIB + ".stamp"
+    stamp = platform.machine()
+    same_host = (os.path.exists(stamp_path)
+                 and open(stamp_path).read() == stamp)
+    if (not force and same_host and os.path.exists(_LIB)
             and os.path.getmtime(_LIB) >= os.path.getmtime(_SRC)):
         return _LIB
     tmp = _LIB + f".tmp{os.getpid()}"
@@ -39,6 +44,8 @@ def build(force: bool = False) -> str:
            "-fno-fast-math", "-Wall", "-Wextra", _SRC, "-o", tmp, "-lm"]
     subprocess.run(cmd, check=True)
     os.replace(tmp, _LIB)
+    with open(stamp_path, "w") as f:
+        f.write(stamp)
     return _LIB
 
 

@@ -30,3 +30,9 @@ def read_golden(name):
             if line and not line.startswith("#"):
                 out.append(line)
     return out
+
+
+def build_lib():
+    """Build libbw.so (fast when up to date) and return its path."""
+    import __graft_entry__
+    return __graft_entry__.load_builder().build()

@@ -1,0 +1,149 @@
+"""Host-side checks of the C ABI that need no GPU.
+
+The library must load and export every function that include/bw.h declares,
+and every argument check must reject bad input on the host, before any CUDA
+call, with the documented status.
+"""
+import ctypes
+import os
+import re
+
+import pytest
+
+from conftest import ROOT, build_lib
+
+HEADER = os.path.join(ROOT, "include", "bw.h")
+OK, INVALID, SHAPE, MISALIGNED = 0, 1, 2, 3
+
+
+@pytest.fixture(scope="module")
+def lib():
+    return ctypes.CDLL(build_lib())
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    names = re.findall(r"\b(bw_[a-z0-9_]+)\s*\(", text)
+    return sorted(set(names))
+
+
+def test_header_declares_the_path():
+    names = declared_functions()
+    for required in ("bw_quant_act", "bw_repack", "bw_unrepack",
+                     "bw_gemv_w2a8", "bw_gemv_w2a8_acc", "bw_repack_bytes",
+                     "bw_status_string"):
+        assert required in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    missing = [n for n in declared_functions() if not hasattr(lib, n)]
+    assert not missing, missing
+
+
+def test_binding_names_match_header(lib):
+    import bit_gemv_bitlinear_gb300 as bw
+    assert sorted(bw.EXPORTS) == declared_functions()
+
+
+def test_status_strings_and_version(lib):
+    lib.bw_status_string.restype = ctypes.c_char_p
+    names = [lib.bw_status_string(i).decode() for i in range(7)]
+    assert names == ["BW_OK", "BW_ERR_INVALID_ARG", "BW_ERR_UNSUPPORTED_SHAPE",
+                     "BW_ERR_MISALIGNED", "BW_ERR_BAD_CODE", "BW_ERR_CUDA",
+                     "BW_ERR_TIMEOUT"]
+    assert lib.bw_status_string(99) is not None
+    assert lib.bw_version() >= 100
+
+
+def test_repack_bytes_matches_layout_spec(lib):
+    import oracle
+    lib.bw_repack_bytes.restype = ctypes.c_size_t
+    for N, K in [(1, 4), (8, 64), (5, 68), (2560, 2560), (13824, 2560),
+                 (2560, 6912), (55296, 5120), (1000, 300), (3, 65536)]:
+        assert lib.bw_repack_bytes(N, K) == oracle.layout_bytes(N, K)
+    assert lib.bw_repack_bytes(0, 64) == 0
+    assert lib.bw_repack_bytes(8, 0) == 0
+    assert lib.bw_repack_bytes(8, 65540) == 0
+
+
+P = ctypes.c_void_p
+
+
+def gemv(lib, x, w, s, ws, bounds, n_ws, M, N, K, y):
+    f = lib.bw_gemv_w2a8
+    f.restype = ctypes.c_int
+    f.argtypes = [P, P, P, P, P, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                  ctypes.c_int, P, P]
+    b = None if bounds is None else (ctypes.c_int * len(bounds))(*bounds)
+    return f(x, w, s, ws, ctypes.cast(b, P) if b is not None else None, n_ws,
+             M, N, K, y, None)
+
+
+# Fake, never-dereferenced device addresses with the alignment required.
+A16, A4, A2 = 0x10000, 0x20000, 0x30000
+
+
+def test_gemv_host_validation(lib):
+    good = dict(x=A16, w=A16, s=A4, ws=A2, bounds=[0, 64], n_ws=1, M=1,
+                N=64, K=256, y=A2)
+
+    def call(**kw):
+        a = dict(good)
+        a.update(kw)
+        return gemv(lib, a["x"], a["w"], a["s"], a["ws"], a["bounds"],
+                    a["n_ws"], a["M"], a["N"], a["K"], a["y"])
+
+    assert call(x=None) == INVALID
+    assert call(w=None) == INVALID
+    assert call(y=None) == INVALID
+    assert call(s=None) == INVALID
+    assert call(bounds=None) == INVALID
+    assert call(M=0) == INVALID
+    assert call(N=0) == INVALID
+    assert call(K=0) == INVALID
+    assert call(K=258) == SHAPE            # not a multiple of 4
+    assert call(K=65540) == SHAPE          # above the maximum
+    assert call(M=4097) == SHAPE
+    assert call(bounds=[0, 63]) == INVALID           # does not end at N
+    assert call(bounds=[1, 64]) == INVALID           # does not start at 0
+    assert call(bounds=[0, 32, 32, 64], n_ws=3) == INVALID  # not increasing
+    assert call(bounds=list(range(0, 64, 7)) + [64], n_ws=10) == INVALID
+    assert call(n_ws=0) == INVALID
+    assert call(w=A16 + 4) == MISALIGNED
+    assert call(x=A4 + 1) == MISALIGNED
+    assert call(s=A4 + 2) == MISALIGNED
+    assert call(y=A2 + 1) == MISALIGNED
+    assert call(ws=A2 + 1) == MISALIGNED
+
+
+def test_other_entry_points_host_validation(lib):
+    qa = lib.bw_quant_act
+    qa.argtypes = [P, ctypes.c_int, ctypes.c_int, P, P, P]
+    assert qa(None, 1, 64, A16, A4, None) == INVALID
+    assert qa(A4, 0, 64, A16, A4, None) == INVALID
+    assert qa(A4, 1, 65537, A16, A4, None) == SHAPE
+    assert qa(A4 + 2, 1, 64, A16, A4, None) == MISALIGNED
+    rp = lib.bw_repack
+    rp.argtypes = [P, ctypes.c_int, ctypes.c_int, P, P]
+    assert rp(None, 8, 64, A16, None) == INVALID
+    assert rp(A16, 8, 66, A16, None) == SHAPE
+    assert rp(A16, 8, 64, A16 + 8, None) == MISALIGNED
+    ur = lib.bw_unrepack
+    ur.argtypes = [P, ctypes.c_int, ctypes.c_int, P, P]
+    assert ur(A16 + 8, 8, 64, A16, None) == MISALIGNED
+    assert ur(A16, 0, 64, A16, None) == INVALID
+    ga = lib.bw_gemv_w2a8_acc
+    ga.argtypes = [P, P, ctypes.c_int, ctypes.c_int, ctypes.c_int, P, P]
+    assert ga(A16, A16, 1, 64, 256, A4 + 2, None) == MISALIGNED
+    assert ga(A16, A16, 1, 64, 6, A4, None) == SHAPE
+
+
+def test_product_path_never_touches_the_oracle():
+    """The package and its sources must not reference the oracle."""
+    pkg = os.path.join(ROOT, "bit_gemv_bitlinear_gb300")
+    for dirpath, _, files in os.walk(pkg):
+        for f in files:
+            if f.endswith((".py", ".cu", ".cuh", ".h", ".cpp")):
+                text = open(os.path.join(dirpath, f)).read()
+                assert "oracle" not in text.lower(), f
