@@ -35,7 +35,7 @@ MAX_K, MAX_N, MAX_M, MAX_WS = 65536, 1 << 24, 4096, 8
 # Every symbol the C ABI declares (checked by the tests without a GPU).
 EXPORTS = ("bw_status_string", "bw_last_cuda_error", "bw_version",
            "bw_quant_act", "bw_repack_bytes", "bw_repack", "bw_unrepack",
-           "bw_gemv_w2a8", "bw_gemv_w2a8_acc")
+           "bw_gemv_w2a8", "bw_gemv_w2a8_acc", "bw_repack_noalloc")
 
 _P = ctypes.c_void_p
 _I = ctypes.c_int
@@ -47,6 +47,7 @@ _SIGS = {
     "bw_repack_bytes": (ctypes.c_size_t, [_I, _I]),
     "bw_repack": (_I, [_P, _I, _I, _P, _P]),
     "bw_unrepack": (_I, [_P, _I, _I, _P, _P]),
+    "bw_repack_noalloc": (_I, [_P, _I, _I, _P, _P]),
     "bw_gemv_w2a8": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _P, _P]),
     "bw_gemv_w2a8_acc": (_I, [_P, _P, _I, _I, _I, _P, _P]),
 }
@@ -128,6 +129,18 @@ def bw_repack(canon: torch.Tensor, N: int, K: int,
     _check(_lib.bw_repack(_dev(canon, torch.uint8, "canon"), N, K,
                           _dev(packed, torch.uint8, "packed"),
                           _stream(stream)), "bw_repack")
+    return packed
+
+
+def bw_repack_noalloc(canon: torch.Tensor, N: int, K: int,
+                      packed: torch.Tensor, stream=None) -> torch.Tensor:
+    """bw_repack for callers that may not allocate device memory: the caller
+    supplies `packed` (bw_repack_bytes(N, K) bytes) and the library uses a
+    fixed internal scratch word instead of allocating one (synchronising;
+    overlapping calls race on that word)."""
+    _check(_lib.bw_repack_noalloc(_dev(canon, torch.uint8, "canon"), N, K,
+                                  _dev(packed, torch.uint8, "packed"),
+                                  _stream(stream)), "bw_repack_noalloc")
     return packed
 
 

@@ -104,6 +104,8 @@ int device_sm_count() {
   return g_sm_count[dev];
 }
 
+void record_cuda_error(int err) { g_last_cuda_error = err; }
+
 }  // namespace bw
 
 using namespace bw;

@@ -65,4 +65,7 @@ cudaError_t launch_unrepack(const uint8_t *packed, int N, int K,
 
 int device_sm_count();
 
+// Remembers a CUDA error for bw_last_cuda_error() (calling thread).
+void record_cuda_error(int err);
+
 }  // namespace bw

@@ -112,6 +112,26 @@ size_t bw_repack_bytes(int N, int K);
 bw_status bw_repack(const uint8_t *canon, int N, int K, uint8_t *packed,
                     bw_stream_t stream);
 
+/* bw_repack_noalloc -- bw_repack without any device allocation, for
+ * callers that are not allowed to allocate device memory (for example an
+ * application whose device memory is owned by a host framework's own
+ * allocator, or one running with stream-ordered memory pools disabled).
+ * The pages have no counterpart: this is a library convenience, not part of
+ * the method.  Same arguments, result and limits as bw_repack; sizes beyond
+ * BW_MAX_N or BW_MAX_K are rejected with BW_ERR_UNSUPPORTED_SHAPE.
+ *   Scratch: instead of allocating its 4-byte bad-code flag, the call uses
+ *   a fixed 256-byte array inside the library (every GPU that loads the
+ *   library holds it until the process exits; the repack needs one word of
+ *   it whatever N and K are).  The first call on each device looks up that
+ *   array's device address with the device current; make that first call
+ *   before any stream capture.  Every call shares the array and clears the
+ *   flag before use, so calls that overlap on the GPU (on different streams
+ *   or from different threads) race on it and may report each other's bad
+ *   codes: serialise them.  Calls no cudaMalloc, cudaFree or other
+ *   allocating routine.  SYNCHRONISES `stream` before returning. */
+bw_status bw_repack_noalloc(const uint8_t *canon, int N, int K,
+                            uint8_t *packed, bw_stream_t stream);
+
 /* bw_unrepack -- the inverse of bw_repack: device layout to canonical bytes
  * [N][K/4] (padding is dropped).  Asynchronous; same limits as bw_repack;
  * packed must be 16-byte aligned. */
