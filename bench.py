@@ -12,8 +12,10 @@ One step = one pass of the hot path over one batch of synthetic input:
   2. 64 bw_gemv_w2a8 calls: R = 16 replicas x the 4 shapes, each replica a
      distinct weight buffer (278 MB in total, over twice the 126 MB L2, so
      every call streams its weights from HBM).
-Each part is captured once as a CUDA graph; CUDA events between the parts
-give the GEMV kernel's own time inside the timed region.
+The quantisation and the 64 GEMVs (in decode-layer order, one chain of
+programmatic dependent launches) are each captured once as a CUDA graph;
+CUDA events between the two give the GEMV kernel's own time inside the
+timed region.
 
 value = packed weight bytes per step / step time (GB/s, all GPUs).
 The reference arm (--impl reference) times the CPU oracle, single-threaded,
@@ -51,13 +53,21 @@ FALLBACK_HBM_GBS = 6800.0
 def parse_args():
     p = argparse.ArgumentParser()
     p.add_argument("--gpus", type=int, default=1)
-    p.add_argument("--steps", type=int, default=50)
+    p.add_argument("--steps", type=int, default=2000)
     p.add_argument("--warmup", type=int, default=5)
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
     p.add_argument("--replicas", type=int, default=REPLICAS)
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--cpu-seconds", type=float, default=12.0,
                    help="bounded CPU work for the oracle baseline")
+    p.add_argument("--single", default=None, metavar="N,K[,M]",
+                   help="time one GEMV shape alone over rotating weight "
+                        "buffers (CUDA graph of back-to-back calls)")
+    p.add_argument("--iters", type=int, default=2000)
+    p.add_argument("--rotate", type=int, default=0,
+                   help="--single: weight buffers (0: enough for 4x L2)")
+    p.add_argument("--eager", action="store_true",
+                   help="--single: launch eagerly instead of a CUDA graph")
     return p.parse_args()
 
 
@@ -240,21 +250,31 @@ def run_ours(args):
                             sh["bounds"], sh["N"], sh["K"], y=outs[name][r],
                             stream=stream)
 
-    # Capture the parts of a step as CUDA graphs (after an eager warm-up).
+    def launch_gemvs():
+        """The 64 GEMVs in decode-layer order: replica by replica, wqkv, wo,
+        w13, w2 -- one programmatic-dependent-launch chain."""
+        for r in range(R):
+            for name in SHAPES:
+                sh = shapes[name]
+                q_d, s_d = act_row(act, shapes, name, r)
+                bw.bw_gemv_w2a8(q_d, sh["packed"][r], s_d, sh["ws_d"],
+                                sh["bounds"], sh["N"], sh["K"],
+                                y=outs[name][r], stream=stream)
+
+    # Capture the two parts of a step as CUDA graphs (after an eager warm-up).
     with torch.cuda.stream(stream):
         launch_quant()
-        for name in SHAPES:
-            launch_shape(name)
+        launch_gemvs()
     stream.synchronize()
     graphs = {}
-    parts = ["quant"] + SHAPES
+    parts = ["quant", "gemv"]
     for part in parts:
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g, stream=stream):
             if part == "quant":
                 launch_quant()
             else:
-                launch_shape(part)
+                launch_gemvs()
         graphs[part] = g
     torch.cuda.synchronize()
 
@@ -289,6 +309,7 @@ def run_ours(args):
     end.record(stream)
     torch.cuda.synchronize()
     clocks = sampler.stop()
+    bw.bw_device_error(stream)   # raises if a bounded device wait ran out
     total_ms = start.elapsed_time(end)
     part_ms = {p: 0.0 for p in parts}
     for k in range(K_steps):
@@ -304,21 +325,16 @@ def run_ours(args):
     ms_per_step = total_ms / K_steps
     value = world * wbytes_step / (ms_per_step * 1e-3) / 1e9
 
-    # Per-shape GEMV figures from the events inside the timed region.
-    per_call = {}
-    alg_total, gemv_ms = 0, 0.0
-    for n in SHAPES:
-        sh = shapes[n]
-        us = part_ms[n] * 1e3 / (K_steps * R)
-        ab = algorithmic_bytes(sh["N"], sh["K"], len(sh["bounds"]) - 1)
-        per_call[n] = {"N": sh["N"], "K": sh["K"], "us_per_call": round(us, 3),
-                       "weight_GBps": round(weight_bytes(sh["N"], sh["K"])
-                                            / (us * 1e3), 1),
-                       "alg_GBps": round(ab / (us * 1e3), 1)}
-        alg_total += ab * R * K_steps
-        gemv_ms += part_ms[n]
+    # The GEMV kernel's own time: the events around the GEMV graph of every
+    # timed step.
+    alg_total = K_steps * R * sum(
+        algorithmic_bytes(shapes[n]["N"], shapes[n]["K"],
+                          len(shapes[n]["bounds"]) - 1) for n in SHAPES)
+    gemv_ms = part_ms["gemv"]
     peak, peak_kind = read_peaks()
     achieved = alg_total / (gemv_ms * 1e-3) / 1e9
+    per_call = per_shape_times(torch, bw, shapes, act, outs, R, stream,
+                               reps=max(1, min(50, K_steps)))
     gemv_launches = len(SHAPES) * R
     quant_launches = len(act)
 
@@ -379,7 +395,8 @@ def run_ours(args):
                 "weight_bytes_per_step": wbytes_step,
                 "l2": "inputs larger than L2: 16 distinct weight buffers "
                       "per shape, 278 MB per step vs 126 MB L2",
-                "graphs": "each step part is one CUDA graph replay",
+                "graphs": "per step: one graph of the quantisation launches, "
+                          "one graph of the 64 GEMV launches",
                 "parallelism": "replicas" if world > 1 else "single GPU",
             },
             "per_call": per_call,
@@ -404,6 +421,37 @@ def run_ours(args):
         print(json.dumps(line), flush=True)
     if world > 1:
         torch.distributed.destroy_process_group()
+
+
+def per_shape_times(torch, bw, shapes, act, outs, R, stream, reps=50):
+    """Informational, after the timed region: µs per call of each shape,
+    from a graph of its R calls back to back."""
+    res = {}
+    for name in SHAPES:
+        sh = shapes[name]
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for r in range(R):
+                q_d, s_d = act_row(act, shapes, name, r)
+                bw.bw_gemv_w2a8(q_d, sh["packed"][r], s_d, sh["ws_d"],
+                                sh["bounds"], sh["N"], sh["K"],
+                                y=outs[name][r], stream=stream)
+        with torch.cuda.stream(stream):
+            g.replay()
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            for _ in range(reps):
+                g.replay()
+            e1.record(stream)
+        torch.cuda.synchronize()
+        us = e0.elapsed_time(e1) * 1e3 / (reps * R)
+        ab = algorithmic_bytes(sh["N"], sh["K"], len(sh["bounds"]) - 1)
+        res[name] = {"N": sh["N"], "K": sh["K"], "us_per_call": round(us, 3),
+                     "weight_GBps": round(weight_bytes(sh["N"], sh["K"])
+                                          / (us * 1e3), 1),
+                     "alg_GBps": round(ab / (us * 1e3), 1)}
+    return res
 
 
 def cpu_baseline(shapes, act, seconds):
@@ -496,9 +544,77 @@ def run_reference(args):
     print(json.dumps(line), flush=True)
 
 
+def run_single(args):
+    """One shape over rotating weight buffers; also the command the kernel
+    profiles are taken with."""
+    import torch
+    import bit_gemv_bitlinear_gb300 as bw
+
+    dims = [int(v) for v in args.single.split(",")]
+    N, K = dims[0], dims[1]
+    M = dims[2] if len(dims) > 2 else 1
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    seed = synth.base_seed(2, 1)
+    canon = synth.canonical_weights(seed, N, K)
+    packed0 = bw.bw_repack(torch.from_numpy(canon).to(dev), N, K)
+    wb = weight_bytes(N, K)
+    rot = args.rotate or max(2, -(-4 * 126 * 2**20 // wb))
+    rot = min(rot, max(2, (8 << 30) // max(wb, 1)))
+    packed = [packed0] + [packed0.clone() for _ in range(rot - 1)]
+    xf = torch.from_numpy(synth.normal_f32(seed, M * K).reshape(M, K)).to(dev)
+    q, s_ = bw.bw_quant_act(xf)
+    ws = torch.ones(1, device=dev).to(torch.bfloat16)
+    y = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+    stream = torch.cuda.Stream(device=dev)
+    per_graph = max(rot, min(args.iters, 64))
+
+    def launches():
+        for i in range(per_graph):
+            bw.bw_gemv_w2a8(q, packed[i % rot], s_, ws, [0, N], N, K, y=y,
+                            stream=stream)
+
+    with torch.cuda.stream(stream):
+        launches()
+    stream.synchronize()
+    if args.eager:
+        def run():
+            with torch.cuda.stream(stream):
+                launches()
+    else:
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            launches()
+
+        def run():
+            with torch.cuda.stream(stream):
+                g.replay()
+    for _ in range(3):
+        run()
+    torch.cuda.synchronize()
+    reps = max(1, args.iters // per_graph)
+    start = torch.cuda.Event(enable_timing=True)
+    end = torch.cuda.Event(enable_timing=True)
+    start.record(stream)
+    for _ in range(reps):
+        run()
+    end.record(stream)
+    torch.cuda.synchronize()
+    bw.bw_device_error(stream)
+    us = start.elapsed_time(end) * 1e3 / (reps * per_graph)
+    ab = algorithmic_bytes(N, K, 1) + (M - 1) * (K + 2 * N + 4)
+    print(json.dumps({"single": [N, K, M], "rotate": rot,
+                      "graph": not args.eager, "calls": reps * per_graph,
+                      "us_per_call": round(us, 3),
+                      "weight_GBps": round(wb / (us * 1e3), 1),
+                      "alg_GBps": round(ab / (us * 1e3), 1)}), flush=True)
+
+
 def main():
     args = parse_args()
-    if args.impl == "reference":
+    if args.single:
+        run_single(args)
+    elif args.impl == "reference":
         run_reference(args)
     else:
         run_ours(args)

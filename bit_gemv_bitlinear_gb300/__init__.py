@@ -35,7 +35,8 @@ MAX_K, MAX_N, MAX_M, MAX_WS = 65536, 1 << 24, 4096, 8
 # Every symbol the C ABI declares (checked by the tests without a GPU).
 EXPORTS = ("bw_status_string", "bw_last_cuda_error", "bw_version",
            "bw_quant_act", "bw_repack_bytes", "bw_repack", "bw_unrepack",
-           "bw_gemv_w2a8", "bw_gemv_w2a8_acc", "bw_repack_noalloc")
+           "bw_gemv_w2a8", "bw_gemv_w2a8_acc", "bw_repack_noalloc",
+           "bw_device_error")
 
 _P = ctypes.c_void_p
 _I = ctypes.c_int
@@ -50,6 +51,7 @@ _SIGS = {
     "bw_repack_noalloc": (_I, [_P, _I, _I, _P, _P]),
     "bw_gemv_w2a8": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _P, _P]),
     "bw_gemv_w2a8_acc": (_I, [_P, _P, _I, _I, _I, _P, _P]),
+    "bw_device_error": (_I, [_P, _P]),
 }
 for _name, (_res, _args) in _SIGS.items():
     _fn = getattr(_lib, _name)
@@ -195,3 +197,14 @@ def bw_gemv_w2a8_acc(x: torch.Tensor, packed: torch.Tensor, N: int, K: int,
         K, _dev(acc, torch.int32, "acc"), _stream(stream)),
         "bw_gemv_w2a8_acc")
     return acc
+
+
+def bw_device_error(stream=None) -> int:
+    """Read and clear the device error word (synchronises the stream).
+    Raises BwError(BW_ERR_TIMEOUT) if a bounded device wait ran out."""
+    bits = ctypes.c_uint(0)
+    status = _lib.bw_device_error(ctypes.byref(bits), _stream(stream))
+    if status == 6:
+        raise BwError(status, f"bw_device_error (bits {bits.value:#x})")
+    _check(status, "bw_device_error")
+    return bits.value

@@ -76,12 +76,18 @@ bw_status gemv_common(const int8_t *x, const uint8_t *packed, const float *s,
   while (m0 < M) {
     const int left = M - m0;
     const int mt = left >= 4 ? 4 : (left >= 2 ? 2 : 1);
-    GemvPlan plan = plan_gemv(mt, N, K, sms);
     a.x = x + size_t(m0) * K;
     a.s = acc_out ? nullptr : s + m0;
     a.out = static_cast<char *>(out) + size_t(m0) * N * out_elem;
-    a.passes = plan.passes;
-    cudaError_t e = launch_gemv(plan, a, acc_out, stream);
+    cudaError_t e;
+    TmaPlan tplan;
+    if (plan_gemv_tma(mt, N, K, sms, &tplan)) {
+      e = launch_gemv_tma(tplan, a, mt, acc_out, stream);
+    } else {  // K beyond the shared-memory ring: register-streamed kernel
+      GemvPlan plan = plan_gemv(mt, N, K, sms);
+      a.passes = plan.passes;
+      e = launch_gemv(plan, a, acc_out, stream);
+    }
     if (e != cudaSuccess) return cuda_status(e);
     m0 += mt;
   }
@@ -182,6 +188,14 @@ bw_status bw_gemv_w2a8(const int8_t *x, const uint8_t *packed, const float *s,
                        int M, int N, int K, bw_bf16 *y, bw_stream_t stream) {
   return gemv_common(x, packed, s, ws, ws_bounds, n_ws, M, N, K, y, false,
                      reinterpret_cast<cudaStream_t>(stream));
+}
+
+bw_status bw_device_error(unsigned int *bits, bw_stream_t stream) {
+  if (!bits) return BW_ERR_INVALID_ARG;
+  cudaError_t e =
+      read_device_error(reinterpret_cast<cudaStream_t>(stream), bits);
+  if (e != cudaSuccess) return cuda_status(e);
+  return *bits ? BW_ERR_TIMEOUT : BW_OK;
 }
 
 bw_status bw_gemv_w2a8_acc(const int8_t *x, const uint8_t *packed, int M,

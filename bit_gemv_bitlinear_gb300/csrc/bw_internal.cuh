@@ -51,6 +51,21 @@ struct GemvPlan {
   int grid;    // CTAs
 };
 
+// TMA-streamed GEMV (bw_gemv_tma.cu): a shared-memory ring of `stages`
+// buffers of `groups_per_stage` row groups, `consumers` compute warps and
+// one producer warp.
+struct TmaPlan {
+  int consumers;
+  int groups_per_stage;
+  int stages;
+  int split;  // 1: one row group per stage, K split across all consumers
+};
+bool plan_gemv_tma(int mt, int N, int K, int num_sms, TmaPlan *plan);
+cudaError_t launch_gemv_tma(const TmaPlan &plan, const GemvArgs &args, int mt,
+                            bool acc_out, cudaStream_t stream);
+// Reads and clears the device error word (synchronises `stream`).
+cudaError_t read_device_error(cudaStream_t stream, unsigned int *bits);
+
 GemvPlan plan_gemv(int mt, int N, int K, int num_sms);
 cudaError_t launch_gemv(const GemvPlan &plan, const GemvArgs &args,
                         bool acc_out, cudaStream_t stream);

@@ -11,33 +11,82 @@ namespace {
 
 constexpr int kQuantThreads = 256;
 
+// Block-wide max of a non-negative value (every thread gets the result).
+__device__ __forceinline__ float block_max(float v, float *warp_max) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1)
+    v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  if ((threadIdx.x & 31) == 0) warp_max[threadIdx.x >> 5] = v;
+  __syncthreads();
+  v = 0.0f;
+  for (int w = 0; w < int(blockDim.x >> 5); ++w) v = fmaxf(v, warp_max[w]);
+  return v;
+}
+
+// q = clamp(rint(x * s), -128, 127) in IEEE fp32; rintf rounds half to even.
+__device__ __forceinline__ int8_t quant1(float x, float scale) {
+  return static_cast<int8_t>(
+      static_cast<int>(fminf(fmaxf(rintf(x * scale), -128.0f), 127.0f)));
+}
+
+// Programmatic dependent launch: let the next kernel (a GEMV that only
+// prefetches weights before its own wait) start its prologue now, and wait
+// for the producer of x before reading it (or writing q and s).
+__device__ __forceinline__ void pdl_enter() {
+  asm volatile("griddepcontrol.launch_dependents;");
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
 // One CTA per activation row.  Pass 1: absmax (max is exact in any order).
-// Pass 2: q = clamp(rint(x * s), -128, 127) with s = 127 / max(absmax, 1e-5),
-// all in IEEE fp32; rintf rounds half to even.
+// Pass 2: q = clamp(rint(x * s), -128, 127), s = 127 / max(absmax, 1e-5).
 __global__ void __launch_bounds__(kQuantThreads)
 quant_act_kernel(const float *__restrict__ x, int K, int8_t *__restrict__ q,
                  float *__restrict__ s) {
   __shared__ float warp_max[kQuantThreads / 32];
+  pdl_enter();
   const int m = blockIdx.x;
   const float *xr = x + size_t(m) * K;
   int8_t *qr = q + size_t(m) * K;
-
   float amax = 0.0f;
   for (int k = threadIdx.x; k < K; k += blockDim.x)
     amax = fmaxf(amax, fabsf(xr[k]));
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1)
-    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
-  if ((threadIdx.x & 31) == 0) warp_max[threadIdx.x >> 5] = amax;
-  __syncthreads();
-  amax = 0.0f;
-  for (int w = 0; w < int(blockDim.x >> 5); ++w) amax = fmaxf(amax, warp_max[w]);
-
+  amax = block_max(amax, warp_max);
   const float scale = 127.0f / fmaxf(amax, 1e-5f);
   if (threadIdx.x == 0) s[m] = scale;
-  for (int k = threadIdx.x; k < K; k += blockDim.x) {
-    const float v = fminf(fmaxf(rintf(xr[k] * scale), -128.0f), 127.0f);
-    qr[k] = static_cast<int8_t>(static_cast<int>(v));
+  for (int k = threadIdx.x; k < K; k += blockDim.x) qr[k] = quant1(xr[k], scale);
+}
+
+// The same arithmetic for rows with K % 4 == 0 that start on a 16-byte
+// boundary: V float4 per thread stay in registers between the two passes
+// and q is written 4 bytes at a time.
+template <int V>
+__global__ void __launch_bounds__(kQuantThreads)
+quant_act_vec_kernel(const float *__restrict__ x, int K,
+                     int8_t *__restrict__ q, float *__restrict__ s) {
+  __shared__ float warp_max[kQuantThreads / 32];
+  pdl_enter();
+  const int m = blockIdx.x;
+  const int nv = K / 4;
+  const float4 *xr = reinterpret_cast<const float4 *>(x + size_t(m) * K);
+  char4 *qr = reinterpret_cast<char4 *>(q + size_t(m) * K);
+  float4 v[V];
+  float amax = 0.0f;
+#pragma unroll
+  for (int i = 0; i < V; ++i) {
+    const int idx = threadIdx.x + i * kQuantThreads;
+    v[i] = idx < nv ? xr[idx] : make_float4(0.f, 0.f, 0.f, 0.f);
+    amax = fmaxf(amax, fmaxf(fmaxf(fabsf(v[i].x), fabsf(v[i].y)),
+                             fmaxf(fabsf(v[i].z), fabsf(v[i].w))));
+  }
+  amax = block_max(amax, warp_max);
+  const float scale = 127.0f / fmaxf(amax, 1e-5f);
+  if (threadIdx.x == 0) s[m] = scale;
+#pragma unroll
+  for (int i = 0; i < V; ++i) {
+    const int idx = threadIdx.x + i * kQuantThreads;
+    if (idx < nv)
+      qr[idx] = make_char4(quant1(v[i].x, scale), quant1(v[i].y, scale),
+                           quant1(v[i].z, scale), quant1(v[i].w, scale));
   }
 }
 
@@ -108,8 +157,27 @@ int grid_for(int64_t items, int threads) {
 
 cudaError_t launch_quant_act(const float *x, int M, int K, int8_t *q,
                              float *s, cudaStream_t stream) {
-  quant_act_kernel<<<M, kQuantThreads, 0, stream>>>(x, K, q, s);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(M);
+  cfg.blockDim = dim3(kQuantThreads);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  const bool vec = K % 4 == 0 && reinterpret_cast<uintptr_t>(x) % 16 == 0 &&
+                   reinterpret_cast<uintptr_t>(q) % 4 == 0;
+  const int per_thread = (K / 4 + kQuantThreads - 1) / kQuantThreads;
+  if (vec && per_thread <= 1)
+    return cudaLaunchKernelEx(&cfg, quant_act_vec_kernel<1>, x, K, q, s);
+  if (vec && per_thread <= 2)
+    return cudaLaunchKernelEx(&cfg, quant_act_vec_kernel<2>, x, K, q, s);
+  if (vec && per_thread <= 4)
+    return cudaLaunchKernelEx(&cfg, quant_act_vec_kernel<4>, x, K, q, s);
+  if (vec && per_thread <= 8)
+    return cudaLaunchKernelEx(&cfg, quant_act_vec_kernel<8>, x, K, q, s);
+  return cudaLaunchKernelEx(&cfg, quant_act_kernel, x, K, q, s);
 }
 
 cudaError_t launch_repack(const uint8_t *canon, int N, int K,

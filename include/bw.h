@@ -156,8 +156,15 @@ bw_status bw_unrepack(const uint8_t *packed, int N, int K, uint8_t *canon,
  *              q|k|v projection of BitNet-2B: {0, 2560, 3200, 3840}).
  *   y          bf16 [M][N] device, 2-byte aligned (output).
  *   1 <= M <= BW_MAX_M, 1 <= N <= BW_MAX_N, 4 <= K <= BW_MAX_K, K % 4 == 0,
- *   1 <= n_ws <= BW_MAX_WS.  M <= 15 runs on CUDA cores (int dp4a);
- *   larger M is processed in row tiles.
+ *   1 <= n_ws <= BW_MAX_WS.  Activation rows are processed in tiles of
+ *   4, 2 and 1 on CUDA cores (int dp4a); the weights are streamed once per
+ *   tile.
+ * Ordering: the call is launched with programmatic dependent launch, so it
+ * may start while the preceding work on `stream` is still running.  x, s,
+ * ws and y are touched only after that work has completed; `packed` may be
+ * read earlier.  So `packed` must not be written by work still in flight on
+ * `stream` (weights are static once bw_repack, which synchronises, has
+ * returned; order any later writer with an event or a synchronisation).
  * ---------------------------------------------------------------------- */
 bw_status bw_gemv_w2a8(const int8_t *x, const uint8_t *packed, const float *s,
                        const bw_bf16 *ws, const int *ws_bounds, int n_ws,
@@ -168,6 +175,15 @@ bw_status bw_gemv_w2a8(const int8_t *x, const uint8_t *packed, const float *s,
  * int32 [M][N] device, 4-byte aligned.  Same limits as bw_gemv_w2a8. */
 bw_status bw_gemv_w2a8_acc(const int8_t *x, const uint8_t *packed, int M,
                            int N, int K, int32_t *acc, bw_stream_t stream);
+
+/* bw_device_error -- reads and clears the library's device error word.
+ * Kernels that wait on an mbarrier bound every wait (about one second); a
+ * wait that runs out sets a bit here and the kernel stops early instead of
+ * hanging (bit 1: the producer gave up on a free buffer, bit 2: the producer
+ * gave up on its own copies, bit 4: a consumer gave up on a full buffer).
+ * Returns BW_ERR_TIMEOUT if any bit was set, BW_OK otherwise; *bits receives
+ * the word.  SYNCHRONISES `stream`; not for the hot path. */
+bw_status bw_device_error(unsigned int *bits, bw_stream_t stream);
 
 #ifdef __cplusplus
 }

@@ -70,6 +70,7 @@ def run_case(bw, case, check_y=True, rows=None):
     y = bw.bw_gemv_w2a8(x_d, packed, s_d, bf16_dev(case["ws"]),
                         case["bounds"].tolist(), N, K)
     torch.cuda.synchronize()
+    assert bw.bw_device_error() == 0      # no bounded wait ran out
     _, s_ref = oracle.quant_act(case["xf"])
     assert (s_d.cpu().numpy() == s_ref).all()
     sel = np.arange(N) if rows is None else np.asarray(rows)
