@@ -58,6 +58,10 @@ def parse_args():
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
     p.add_argument("--replicas", type=int, default=REPLICAS)
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--no-stack", action="store_true",
+                   help="skip the layer-stack tok/s measurement")
+    p.add_argument("--stack", action="store_true",
+                   help="only time the 30-layer decode stack (tok/s)")
     p.add_argument("--cpu-seconds", type=float, default=12.0,
                    help="bounded CPU work for the oracle baseline")
     p.add_argument("--single", default=None, metavar="N,K[,M]",
@@ -370,6 +374,10 @@ def run_ours(args):
     e2e_ms = e_start.elapsed_time(e_end) / K_steps
     e2e_value = world * wbytes_step / (e2e_ms * 1e-3) / 1e9
 
+    stack_line = None
+    if not args.no_stack:
+        stack_line = run_stack_timing(torch, bw, dev)
+
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cpu = cpu_baseline(shapes, act, args.cpu_seconds)
@@ -416,11 +424,66 @@ def run_ours(args):
             "gpu_launches": (gemv_launches + quant_launches) * K_steps,
             "clocks": clocks,
         }
+        if stack_line is not None:
+            line["layer_stack"] = stack_line
         if cpu is not None:
             line["cpu_baseline"] = cpu
         print(json.dumps(line), flush=True)
     if world > 1:
         torch.distributed.destroy_process_group()
+
+
+STACK_LAYERS, STACK_STEPS = 30, 256
+
+
+def run_stack_timing(torch, bw, dev, n_layers=STACK_LAYERS,
+                     steps=STACK_STEPS, reps=3):
+    """The BitNet-2B-shaped decode layer stack (dim 2560, ffn 6912, 20/5
+    heads): `steps` independent decode steps through `n_layers` layers.
+    One layer's random ternary weights are generated and copied into
+    n_layers distinct device buffers (521 MB for 30 layers, so every step
+    streams all weights from HBM).  Returns tok/s and the derived figures."""
+    dim, ffn, nh, nkv = 2560, 6912, 20, 5
+    seed = synth.base_seed(4)
+    w = synth.stack_weights(seed, 1, dim, ffn, nh, nkv)
+    L0 = w["layers"][0]
+    base = {}
+    for name in ("wqkv", "wo", "w13", "w2"):
+        canon = L0[name]
+        base[name] = bw.bw_repack(torch.from_numpy(canon).to(dev),
+                                  canon.shape[0], canon.shape[1] * 4)
+    ws = torch.from_numpy(L0["ws"].view(np.int16)).to(dev).view(torch.bfloat16)
+    gam = torch.from_numpy(L0["gammas"]).to(dev)
+    layers = [{k: (v if i == 0 else v.clone()) for k, v in base.items()}
+              | {"ws": ws, "gammas": gam} for i in range(n_layers)]
+    stack = bw.Stack(layers, dim, ffn, nh, nkv, w["eps"])
+    h_in = torch.from_numpy(synth.step_inputs(seed, steps, dim)).to(dev)
+    h_out = torch.empty_like(h_in)
+    stream = torch.cuda.Stream(device=dev)
+    with torch.cuda.stream(stream):
+        stack.run(h_in[:4], h_out[:4], stream=stream)
+    stream.synchronize()
+    best = None
+    for _ in range(reps):
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            e0.record(stream)
+            stack.run(h_in, h_out, stream=stream)
+            e1.record(stream)
+        stream.synchronize()
+        ms = e0.elapsed_time(e1)
+        best = ms if best is None else min(best, ms)
+    bw.bw_device_error(stream)
+    stack.close()
+    layer_bytes = sum(int(base[k].numel()) for k in base)
+    us_tok = best * 1e3 / steps
+    return {"layers": n_layers, "steps": steps, "tok_s": round(steps / (best * 1e-3), 1),
+            "us_per_token": round(us_tok, 2),
+            "weight_bytes_per_token": layer_bytes * n_layers,
+            "weight_GBps": round(layer_bytes * n_layers / (us_tok * 1e3), 1),
+            "launches_per_token": 8 * n_layers + 1,
+            "timing": f"best of {reps} runs of {steps} steps, CUDA events"}
 
 
 def per_shape_times(torch, bw, shapes, act, outs, R, stream, reps=50):
@@ -614,6 +677,13 @@ def main():
     args = parse_args()
     if args.single:
         run_single(args)
+    elif args.stack and args.impl != "reference":
+        import torch
+        import bit_gemv_bitlinear_gb300 as bw
+        dev = torch.device("cuda", 0)
+        torch.cuda.set_device(dev)
+        print(json.dumps({"layer_stack": run_stack_timing(torch, bw, dev)}),
+              flush=True)
     elif args.impl == "reference":
         run_reference(args)
     else:

@@ -36,7 +36,8 @@ MAX_K, MAX_N, MAX_M, MAX_WS = 65536, 1 << 24, 4096, 8
 EXPORTS = ("bw_status_string", "bw_last_cuda_error", "bw_version",
            "bw_quant_act", "bw_repack_bytes", "bw_repack", "bw_unrepack",
            "bw_gemv_w2a8", "bw_gemv_w2a8_acc", "bw_repack_noalloc",
-           "bw_device_error")
+           "bw_device_error", "bw_stack_create", "bw_layer_stack",
+           "bw_stack_destroy")
 
 _P = ctypes.c_void_p
 _I = ctypes.c_int
@@ -52,6 +53,9 @@ _SIGS = {
     "bw_gemv_w2a8": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _P, _P]),
     "bw_gemv_w2a8_acc": (_I, [_P, _P, _I, _I, _I, _P, _P]),
     "bw_device_error": (_I, [_P, _P]),
+    "bw_stack_create": (_I, [_P, _P]),
+    "bw_layer_stack": (_I, [_P, _P, _I, _P, _P, _P]),
+    "bw_stack_destroy": (None, [_P]),
 }
 for _name, (_res, _args) in _SIGS.items():
     _fn = getattr(_lib, _name)
@@ -208,3 +212,72 @@ def bw_device_error(stream=None) -> int:
         raise BwError(status, f"bw_device_error (bits {bits.value:#x})")
     _check(status, "bw_device_error")
     return bits.value
+
+
+class _StackDesc(ctypes.Structure):
+    _fields_ = [("n_layers", _I), ("dim", _I), ("ffn", _I), ("n_heads", _I),
+                ("n_kv_heads", _I), ("eps", ctypes.c_float),
+                ("wqkv", _P), ("wo", _P), ("w13", _P), ("w2", _P),
+                ("ws", _P), ("gammas", _P)]
+
+
+class _StackTrace(ctypes.Structure):
+    _fields_ = [("layer", _I)] + [(n, _P) for n in (
+        "h_in", "q_attn", "s_attn", "qkv", "q_o", "s_o", "o", "h_mid",
+        "q_ffn", "s_ffn", "gu", "q_down", "s_down", "down")]
+
+
+class Stack:
+    """A decoder layer stack (bw_stack_create / bw_layer_stack).
+
+    layers: list of dicts with device tensors 'wqkv', 'wo', 'w13', 'w2'
+    (uint8 device layouts from bw_repack), 'ws' (bf16 [7]) and 'gammas'
+    (fp32 [3 dim + ffn]).  The tensors must outlive the stack."""
+
+    def __init__(self, layers, dim, ffn, n_heads, n_kv_heads, eps=1e-5):
+        self.dim, self.ffn = dim, ffn
+        self.n_heads, self.n_kv_heads = n_heads, n_kv_heads
+        self._keep = layers
+        L = len(layers)
+        arr = lambda key, dt: (_P * L)(*[_dev(l[key], dt, key)
+                                         for l in layers])
+        self._arrays = [arr("wqkv", torch.uint8), arr("wo", torch.uint8),
+                        arr("w13", torch.uint8), arr("w2", torch.uint8),
+                        arr("ws", torch.bfloat16), arr("gammas", torch.float32)]
+        desc = _StackDesc(L, dim, ffn, n_heads, n_kv_heads, eps,
+                          *[ctypes.cast(a, _P) for a in self._arrays])
+        handle = _P()
+        _check(_lib.bw_stack_create(ctypes.byref(desc), ctypes.byref(handle)),
+               "bw_stack_create")
+        self._h = handle
+
+    def run(self, h_in: torch.Tensor, h_out: torch.Tensor | None = None,
+            trace: dict | None = None, stream=None) -> torch.Tensor:
+        """h_in fp32 [steps][dim] -> h_out fp32 [steps][dim].  trace: a dict
+        with 'layer' and device tensors named as bw_stack_trace's fields."""
+        h2 = h_in if h_in.dim() == 2 else h_in.reshape(1, -1)
+        steps = h2.shape[0]
+        if h_out is None:
+            h_out = torch.empty_like(h2)
+        tr_ptr = None
+        if trace is not None:
+            tr = _StackTrace(int(trace["layer"]))
+            for name, _ in _StackTrace._fields_[1:]:
+                t = trace.get(name)
+                setattr(tr, name, t.data_ptr() if t is not None else None)
+            tr_ptr = ctypes.byref(tr)
+        _check(_lib.bw_layer_stack(self._h, _dev(h2, torch.float32, "h_in"),
+                                   steps, _dev(h_out, torch.float32, "h_out"),
+                                   tr_ptr, _stream(stream)), "bw_layer_stack")
+        return h_out
+
+    def close(self):
+        if getattr(self, "_h", None):
+            _lib.bw_stack_destroy(self._h)
+            self._h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass

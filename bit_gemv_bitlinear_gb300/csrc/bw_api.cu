@@ -112,6 +112,13 @@ int device_sm_count() {
 
 void record_cuda_error(int err) { g_last_cuda_error = err; }
 
+bw_status gemv_internal(const int8_t *x, const uint8_t *packed, const float *s,
+                        const bw_bf16 *ws, const int *ws_bounds, int n_ws,
+                        int M, int N, int K, bw_bf16 *y, cudaStream_t stream) {
+  return gemv_common(x, packed, s, ws, ws_bounds, n_ws, M, N, K, y, false,
+                     stream);
+}
+
 }  // namespace bw
 
 using namespace bw;

@@ -83,4 +83,9 @@ int device_sm_count();
 // Remembers a CUDA error for bw_last_cuda_error() (calling thread).
 void record_cuda_error(int err);
 
+// bw_gemv_w2a8 for library-internal callers (same validation and launch).
+bw_status gemv_internal(const int8_t *x, const uint8_t *packed, const float *s,
+                        const bw_bf16 *ws, const int *ws_bounds, int n_ws,
+                        int M, int N, int K, bw_bf16 *y, cudaStream_t stream);
+
 }  // namespace bw

@@ -176,6 +176,87 @@ bw_status bw_gemv_w2a8(const int8_t *x, const uint8_t *packed, const float *s,
 bw_status bw_gemv_w2a8_acc(const int8_t *x, const uint8_t *packed, int M,
                            int N, int K, int32_t *acc, bw_stream_t stream);
 
+/* ------------------------------------------------------------------------
+ * Decoder layer stack: chained M=1 W2A8 GEMVs with the fp32 glue between
+ * them, in the order of the BitNet b1.58 block ([W2A8] §一 model shape,
+ * §4.1 fused projections and the four RMSNorms, §六 item 3 the per-token
+ * quantisation before each GEMV, §六 item 1 decode replayed from a graph):
+ *   h += down(previous layer)
+ *   qkv  = W2A8(quant(rmsnorm(h) * g_attn),            wqkv)   3 scales
+ *   o    = W2A8(quant(rmsnorm(attn(qkv)) * g_attn_sub), wo)     1 scale
+ *   h   += o
+ *   gu   = W2A8(quant(rmsnorm(h) * g_ffn),              w13)    2 scales
+ *   down = W2A8(quant(rmsnorm(relu(gate)^2 * up) * g_ffn_sub), w2) 1 scale
+ * and, after the last layer, h += down.  attn() is attention over a
+ * one-token context: query head i returns the value vector of KV head
+ * i / (n_heads / n_kv_heads) (the softmax of a single score is 1); q and k
+ * are computed but do not change the result.  RMSNorm:
+ * v * (1/sqrt(mean(v^2) + eps)) * gamma, fp32.  The residual stream h is
+ * fp32; GEMV outputs are bf16.
+ * ---------------------------------------------------------------------- */
+typedef struct bw_stack bw_stack;
+
+typedef struct {
+    int n_layers;
+    int dim;          /* model width (multiple of n_heads and of 4, <= 8192) */
+    int ffn;          /* FFN width (multiple of 4, <= 8192)                  */
+    int n_heads;      /* query heads                                         */
+    int n_kv_heads;   /* KV heads (divides n_heads)                          */
+    float eps;        /* RMSNorm epsilon                                     */
+    /* Host arrays of n_layers DEVICE pointers (16-byte aligned), each a
+     * device weight layout written by bw_repack:
+     *   wqkv [(n_heads + 2 n_kv_heads) * dim/n_heads][dim]  (q | k | v rows)
+     *   wo   [dim][dim]
+     *   w13  [2 ffn][dim]                                   (gate | up rows)
+     *   w2   [dim][ffn]                                                    */
+    const uint8_t *const *wqkv;
+    const uint8_t *const *wo;
+    const uint8_t *const *w13;
+    const uint8_t *const *w2;
+    /* Host array of n_layers device pointers to 7 bf16 weight scales:
+     * q, k, v, o, gate, up, down. */
+    const bw_bf16 *const *ws;
+    /* Host array of n_layers device pointers to 3 dim + ffn fp32 gains:
+     * attention_norm, attn_sub_norm, ffn_norm (dim each), ffn_sub_norm. */
+    const float *const *gammas;
+} bw_stack_desc;
+
+/* Optional per-stage record of one layer of the LAST step of a
+ * bw_layer_stack call (device buffers; any pointer may be NULL). */
+typedef struct {
+    int layer;
+    float *h_in;                     /* [dim] layer input (after residual) */
+    int8_t *q_attn; float *s_attn;   /* [dim], [1]                         */
+    bw_bf16 *qkv;                    /* [(n_heads + 2 n_kv) hd]            */
+    int8_t *q_o; float *s_o;         /* [dim], [1]                         */
+    bw_bf16 *o;                      /* [dim]                              */
+    float *h_mid;                    /* [dim] h + o                        */
+    int8_t *q_ffn; float *s_ffn;     /* [dim], [1]                         */
+    bw_bf16 *gu;                     /* [2 ffn]                            */
+    int8_t *q_down; float *s_down;   /* [ffn], [1]                         */
+    bw_bf16 *down;                   /* [dim]                              */
+} bw_stack_trace;
+
+/* Creates a stack: copies the descriptor (the pointer arrays; the weights
+ * stay the caller's and must outlive the stack), allocates its device
+ * scratch (about 4 dim + 5 ffn bytes of activations) with cudaMalloc,
+ * runs one step on zero input and captures one step as a CUDA graph on a
+ * private stream.  Synchronising; call it before any stream capture. */
+bw_status bw_stack_create(const bw_stack_desc *desc, bw_stack **stack);
+
+/* Runs `steps` decode steps: h_out[t] = stack(h_in[t]) (fp32 [steps][dim],
+ * device).  Steps are independent (no KV cache).  Asynchronous on `stream`.
+ * `trace` (may be NULL) records the stages of trace->layer in the last
+ * step.  Calls on the same stack must not overlap (they share its scratch);
+ * use one stack per concurrent stream. */
+bw_status bw_layer_stack(bw_stack *stack, const float *h_in, int steps,
+                         float *h_out, const bw_stack_trace *trace,
+                         bw_stream_t stream);
+
+/* Frees the scratch and the graph (synchronises the device through
+ * cudaFree).  NULL is accepted. */
+void bw_stack_destroy(bw_stack *stack);
+
 /* bw_device_error -- reads and clears the library's device error word.
  * Kernels that wait on an mbarrier bound every wait (about one second); a
  * wait that runs out sets a bit here and the kernel stops early instead of

@@ -147,3 +147,41 @@ def test_product_path_never_touches_the_oracle():
             if f.endswith((".py", ".cu", ".cuh", ".h", ".cpp")):
                 text = open(os.path.join(dirpath, f)).read()
                 assert "oracle" not in text.lower(), f
+
+
+class _Desc(ctypes.Structure):
+    _fields_ = [("n_layers", ctypes.c_int), ("dim", ctypes.c_int),
+                ("ffn", ctypes.c_int), ("n_heads", ctypes.c_int),
+                ("n_kv_heads", ctypes.c_int), ("eps", ctypes.c_float),
+                ("wqkv", P), ("wo", P), ("w13", P), ("w2", P), ("ws", P),
+                ("gammas", P)]
+
+
+def test_stack_create_host_validation(lib):
+    create = lib.bw_stack_create
+    create.argtypes = [P, P]
+    run = lib.bw_layer_stack
+    run.argtypes = [P, P, ctypes.c_int, P, P, P]
+    handle = P()
+    L = 2
+    w16 = (P * L)(A16, A16 + 256)
+    ws = (P * L)(A2, A2 + 64)
+    gam = (P * L)(A4, A4 + 64)
+
+    def make(**kw):
+        base = dict(n_layers=L, dim=256, ffn=512, n_heads=4, n_kv_heads=2,
+                    eps=1e-5, wqkv=ctypes.cast(w16, P), wo=ctypes.cast(w16, P),
+                    w13=ctypes.cast(w16, P), w2=ctypes.cast(w16, P),
+                    ws=ctypes.cast(ws, P), gammas=ctypes.cast(gam, P))
+        base.update(kw)
+        return create(ctypes.byref(_Desc(**base)), ctypes.byref(handle))
+
+    assert create(None, ctypes.byref(handle)) == INVALID
+    assert make(n_layers=0) == INVALID
+    assert make(dim=250) == SHAPE           # not a multiple of n_heads
+    assert make(n_kv_heads=3) == SHAPE      # does not divide n_heads
+    assert make(ffn=8196) == SHAPE          # above the glue limit
+    assert make(wo=None) == INVALID
+    bad = (P * L)(A16, A16 + 8)             # second layer misaligned
+    assert make(w2=ctypes.cast(bad, P)) == MISALIGNED
+    assert run(None, A4, 1, A4, None, None) == INVALID
