@@ -71,6 +71,19 @@ bw_status gemv_common(const int8_t *x, const uint8_t *packed, const float *s,
   a.seg = seg;
   const size_t out_elem = acc_out ? sizeof(int32_t) : sizeof(bw_bf16);
 
+  // Batched activations: tensor cores, tiles of up to 64 rows.
+  if (M >= kMmaMinRows && K <= kMmaMaxK) {
+    for (int m0 = 0; m0 < M; m0 += 64) {
+      const int rows = M - m0 < 64 ? M - m0 : 64;
+      a.x = x + size_t(m0) * K;
+      a.s = acc_out ? nullptr : s + m0;
+      a.out = static_cast<char *>(out) + size_t(m0) * N * out_elem;
+      cudaError_t e = launch_gemv_mma(a, rows, acc_out, stream);
+      if (e != cudaSuccess) return cuda_status(e);
+    }
+    return BW_OK;
+  }
+
   // Activation rows in tiles of 4, then 2, then 1.
   int m0 = 0;
   while (m0 < M) {

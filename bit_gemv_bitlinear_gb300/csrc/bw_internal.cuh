@@ -66,6 +66,13 @@ cudaError_t launch_gemv_tma(const TmaPlan &plan, const GemvArgs &args, int mt,
 // Reads and clears the device error word (synchronises `stream`).
 cudaError_t read_device_error(cudaStream_t stream, unsigned int *bits);
 
+// Tensor-core GEMV for batched activations (bw_gemv_mma.cu): one launch per
+// tile of up to 64 activation rows (`rows` valid rows at args.x).
+constexpr int kMmaMinRows = 8;      // M at or above this uses tensor cores
+constexpr int kMmaMaxK = 16384;     // fp32 partial sums stay below 2^21
+cudaError_t launch_gemv_mma(const GemvArgs &args, int rows, bool acc_out,
+                            cudaStream_t stream);
+
 GemvPlan plan_gemv(int mt, int N, int K, int num_sms);
 cudaError_t launch_gemv(const GemvPlan &plan, const GemvArgs &args,
                         bool acc_out, cudaStream_t stream);

@@ -243,3 +243,19 @@ def test_reproducible_and_stream_ordered(bw):
                              N, K, stream=st)
     st.synchronize()
     assert torch.equal(y1, y2)
+
+
+@pytest.mark.parametrize("M,N,K", [
+    (8, 8, 64), (9, 100, 300), (17, 1000, 1028), (33, 77, 16384),
+    (65, 513, 2560), (128, 2560, 2560), (200, 64, 68), (8, 40, 20000)])
+def test_batched_tensor_core_tiles(bw, M, N, K):
+    """M >= 8 takes the tensor-core path (token tiles of 8..64, padded);
+    K > 16384 goes back to CUDA cores.  int32 exact, bf16 within 1 ulp."""
+    case = synth.gemv_case(M, N, K, synth.base_seed(10, M % 16),
+                           uniform_x=False, bounds=[0, N // 3 + 1, N])
+    q, _ = oracle.quant_act(case["xf"])
+    case["q"] = q
+    # extreme activations in one row: +-128/127 saturate the int8 range
+    case["q"][M // 2, ::3] = -128
+    case["q"][M // 2, 1::3] = 127
+    run_case(bw, case)
