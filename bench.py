@@ -49,6 +49,13 @@ SHAPES = ["wqkv", "wo", "w13", "w2"]
 REPLICAS = 16
 FALLBACK_HBM_GBS = 6800.0
 
+# DRAM bytes (read + write) per launch of the current TMA GEMV kernel,
+# measured with ncu (dram__bytes_read.sum + dram__bytes_write.sum, median of
+# 4 launches; profiles/bench_m1_sweep_launches.md).  Must be re-measured --
+# or set to None -- whenever the GEMV kernel changes.
+MEASURED_DRAM_BYTES = {"wqkv": 2488576, "wo": 1669376, "w13": 8880448,
+                       "w2": 4459136}
+
 
 def parse_args():
     p = argparse.ArgumentParser()
@@ -416,7 +423,12 @@ def run_ours(args):
                 "peak_kind": peak_kind,
                 "unit": "GB/s",
                 "frac": round(achieved / peak, 4),
-                "traffic": None,
+                "traffic": (round(sum(MEASURED_DRAM_BYTES[n] for n in SHAPES)
+                                  / len(SHAPES))
+                            if MEASURED_DRAM_BYTES else None),
+                "traffic_unit": "bytes per GEMV launch (ncu)",
+                "alg_bytes_per_launch": round(alg_total / (K_steps * R
+                                                           * len(SHAPES))),
             },
             "e2e": {"value": round(e2e_value, 2), "unit": "GB/s",
                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,

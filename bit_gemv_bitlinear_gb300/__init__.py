@@ -37,7 +37,7 @@ EXPORTS = ("bw_status_string", "bw_last_cuda_error", "bw_version",
            "bw_quant_act", "bw_repack_bytes", "bw_repack", "bw_unrepack",
            "bw_gemv_w2a8", "bw_gemv_w2a8_acc", "bw_repack_noalloc",
            "bw_device_error", "bw_stack_create", "bw_layer_stack",
-           "bw_stack_destroy")
+           "bw_stack_destroy", "bw_selftest_wait_timeout")
 
 _P = ctypes.c_void_p
 _I = ctypes.c_int
@@ -56,6 +56,7 @@ _SIGS = {
     "bw_stack_create": (_I, [_P, _P]),
     "bw_layer_stack": (_I, [_P, _P, _I, _P, _P, _P]),
     "bw_stack_destroy": (None, [_P]),
+    "bw_selftest_wait_timeout": (_I, [_P, _P]),
 }
 for _name, (_res, _args) in _SIGS.items():
     _fn = getattr(_lib, _name)
@@ -281,3 +282,11 @@ class Stack:
             self.close()
         except Exception:
             pass
+
+
+def bw_selftest_wait_timeout(stream=None) -> tuple[int, int]:
+    """Run the bounded-wait self-test; returns (status, device error bits).
+    The expected result is (6, 8): BW_ERR_TIMEOUT with bit 8."""
+    bits = ctypes.c_uint(0)
+    status = _lib.bw_selftest_wait_timeout(ctypes.byref(bits), _stream(stream))
+    return status, bits.value

@@ -218,6 +218,15 @@ bw_status bw_device_error(unsigned int *bits, bw_stream_t stream) {
   return *bits ? BW_ERR_TIMEOUT : BW_OK;
 }
 
+bw_status bw_selftest_wait_timeout(unsigned int *bits, bw_stream_t stream) {
+  if (!bits) return BW_ERR_INVALID_ARG;
+  cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+  cudaError_t e = launch_selftest_wait(cs);
+  if (e == cudaSuccess) e = read_device_error(cs, bits);
+  if (e != cudaSuccess) return cuda_status(e);
+  return *bits ? BW_ERR_TIMEOUT : BW_OK;
+}
+
 bw_status bw_gemv_w2a8_acc(const int8_t *x, const uint8_t *packed, int M,
                            int N, int K, int32_t *acc, bw_stream_t stream) {
   return gemv_common(x, packed, nullptr, nullptr, nullptr, 0, M, N, K, acc,

@@ -81,13 +81,27 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar,
   return done != 0;
 }
 
-// Wait for the phase of `parity` to complete, for at most about a second.
-__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity) {
+// Wait for the phase of `parity` to complete, for at most `limit` cycles
+// (about a second by default).
+__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity,
+                                          long long limit = kWaitLimitCycles) {
   if (mbar_try_wait(bar, parity)) return true;
   const long long t0 = clock64();
   while (!mbar_try_wait(bar, parity))
-    if (clock64() - t0 > kWaitLimitCycles) return false;
+    if (clock64() - t0 > limit) return false;
   return true;
+}
+
+// Failure-detection self-test: a wait that nothing can complete (the
+// barrier expects two arrivals and gets one) must run out, report bit 8 in
+// the device error word and return, leaving the context usable.
+__global__ void selftest_wait_kernel(long long limit) {
+  __shared__ uint64_t bar;
+  if (threadIdx.x != 0) return;
+  mbar_init(&bar, 2);
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  mbar_arrive(&bar);
+  if (!mbar_wait(&bar, 0u, limit)) atomicOr(&g_device_error, 8u);
 }
 
 __device__ __forceinline__ void bulk_copy_g2s(void *dst, const void *src,
@@ -551,6 +565,15 @@ cudaError_t launch_gemv_tma(const TmaPlan &p, const GemvArgs &a, int mt,
     return acc_out ? launch_tma_instance<4, true>(p, a, stream)
                    : launch_tma_instance<4, false>(p, a, stream);
   return cudaErrorInvalidConfiguration;
+}
+
+cudaError_t launch_selftest_wait(cudaStream_t stream) {
+  int khz = 0;
+  cudaError_t e = cudaDeviceGetAttribute(&khz, cudaDevAttrClockRate, 0);
+  if (e != cudaSuccess) return e;
+  const long long limit = (long long)(khz > 0 ? khz : 2000000) * 10;  // ~10 ms
+  selftest_wait_kernel<<<1, 32, 0, stream>>>(limit);
+  return cudaGetLastError();
 }
 
 cudaError_t read_device_error(cudaStream_t stream, unsigned int *out) {

@@ -63,6 +63,9 @@ struct TmaPlan {
 bool plan_gemv_tma(int mt, int N, int K, int num_sms, TmaPlan *plan);
 cudaError_t launch_gemv_tma(const TmaPlan &plan, const GemvArgs &args, int mt,
                             bool acc_out, cudaStream_t stream);
+// Launches the bounded-wait self-test kernel (sets bit 8 after ~10 ms).
+cudaError_t launch_selftest_wait(cudaStream_t stream);
+
 // Reads and clears the device error word (synchronises `stream`).
 cudaError_t read_device_error(cudaStream_t stream, unsigned int *bits);
 

@@ -266,6 +266,15 @@ void bw_stack_destroy(bw_stack *stack);
  * the word.  SYNCHRONISES `stream`; not for the hot path. */
 bw_status bw_device_error(unsigned int *bits, bw_stream_t stream);
 
+/* bw_selftest_wait_timeout -- failure-detection self-test: launches a
+ * one-thread kernel whose mbarrier wait cannot complete (it expects two
+ * arrivals and receives one) with a limit of about 10 ms.  The wait runs
+ * out, the kernel sets bit 8 of the device error word and returns; this
+ * call then reads and clears the word like bw_device_error and returns
+ * BW_ERR_TIMEOUT (with *bits = 8) -- the expected outcome.  The context
+ * stays usable.  SYNCHRONISES `stream`. */
+bw_status bw_selftest_wait_timeout(unsigned int *bits, bw_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif
