@@ -53,8 +53,7 @@ FALLBACK_HBM_GBS = 6800.0
 # measured with ncu (dram__bytes_read.sum + dram__bytes_write.sum, median of
 # 4 launches; profiles/bench_m1_sweep_launches.md).  Must be re-measured --
 # or set to None -- whenever the GEMV kernel changes.
-MEASURED_DRAM_BYTES = {"wqkv": 2488576, "wo": 1669376, "w13": 8880448,
-                       "w2": 4459136}
+MEASURED_DRAM_BYTES = None
 
 
 def parse_args():
@@ -69,6 +68,10 @@ def parse_args():
                    help="skip the layer-stack tok/s measurement")
     p.add_argument("--stack", action="store_true",
                    help="only time the 30-layer decode stack (tok/s)")
+    p.add_argument("--stack-layers", type=int, default=None,
+                   help="--stack: layers (default 30)")
+    p.add_argument("--stack-steps", type=int, default=None,
+                   help="--stack: decode steps per run (default 256)")
     p.add_argument("--cpu-seconds", type=float, default=12.0,
                    help="bounded CPU work for the oracle baseline")
     p.add_argument("--single", default=None, metavar="N,K[,M]",
@@ -417,7 +420,7 @@ def run_ours(args):
             "per_call": per_call,
             "roofline": {
                 "bound": "hbm",
-                "kernel": "gemv_w2a8_kernel",
+                "kernel": "gemv_w2a8_pipe_kernel",
                 "achieved": round(achieved, 1),
                 "peak": peak,
                 "peak_kind": peak_kind,
@@ -694,7 +697,9 @@ def main():
         import bit_gemv_bitlinear_gb300 as bw
         dev = torch.device("cuda", 0)
         torch.cuda.set_device(dev)
-        print(json.dumps({"layer_stack": run_stack_timing(torch, bw, dev)}),
+        print(json.dumps({"layer_stack": run_stack_timing(
+            torch, bw, dev, args.stack_layers or STACK_LAYERS,
+            args.stack_steps or STACK_STEPS)}),
               flush=True)
     elif args.impl == "reference":
         run_reference(args)

@@ -8,26 +8,26 @@
 // Design for sm_103a:
 //  * The packed weights are the only large operand and each byte is used
 //    once, so they are streamed HBM -> shared memory with 1-D TMA bulk copies
-//    (cp.async.bulk, completion counted in bytes on an mbarrier) into a ring
-//    of `stages` buffers.  One producer lane keeps the ring full; the bytes
-//    in flight per SM are set by the ring size, not by registers or warps.
-//  * A stage is S whole row groups (contiguous in the device layout).
-//    Consumer warps form teams of S warps; team t takes every T-th stage of
-//    the CTA and warp u of the team the u-th row group of it, i.e. a warp
-//    owns all of K for 8 rows: no cross-warp reduction, no CTA barrier in
-//    the loop.
+//    (cp.async.bulk, completion counted in bytes on an mbarrier); the bytes
+//    in flight per SM are set by the shared-memory buffers, not by registers
+//    or warps.
+//  * A CTA owns k consecutive row groups (k as small as the resident CTAs
+//    allow, so every CTA but the last has the same work); its 8 warps split
+//    the CTA's chunks into 8 equal runs and each warp streams its run in
+//    pieces of up to 4 KB through its own 2-slot ring, issuing its own
+//    copies.  Partial row sums meet in shared memory (int32 atomics, exact in
+//    any order); one epilogue per CTA scales and stores the rows.
 //  * Lane (q, r): row r of the group, chunks j = q (mod 4).  One 128-bit
 //    shared load gives 64 codes (a contiguous 512-byte warp access, no bank
 //    conflict); the int8 activations, staged once in shared memory, come as
-//    four 128-bit broadcast loads per chunk.  Decode = one AND per 4 codes
+//    four 128-bit broadcast loads per chunk (conflict-free thanks to a
+//    16-byte pad every two chunks).  Decode = one AND per 4 codes
 //    (unsigned codes c = w + 1 masked in place, unsigned x signed dp4a); the
 //    4^i slot factor and the sum_k x offset are removed once per row.
-//  * A warp keeps its totals for 4 row groups in the 4 lane quarters and
-//    runs one 32-lane epilogue for those 32 rows.
 //  * Every mbarrier wait is bounded (clock64); on time-out the kernel sets
 //    the library's device error word and stops; the host reads it with
-//    bw_device_error().  Before leaving, the producer waits (bounded) for
-//    the copies it issued.
+//    bw_device_error().  Before leaving, the issuing lane waits (bounded)
+//    for the copies it issued.
 //  * Programmatic dependent launch: the first ring fills are issued before
 //    griddepcontrol.wait (the packed weights are static once bw_repack has
 //    returned); activations, scales and outputs are touched after it, and
@@ -113,22 +113,11 @@ __device__ __forceinline__ void bulk_copy_g2s(void *dst, const void *src,
       : "memory");
 }
 
-__device__ __forceinline__ void prefetch_l2(const void *p, uint32_t bytes) {
-  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p),
-               "r"(bytes)
-               : "memory");
-}
-
 __device__ __forceinline__ void pdl_wait() {
   asm volatile("griddepcontrol.wait;" ::: "memory");
 }
 __device__ __forceinline__ void pdl_trigger() {
   asm volatile("griddepcontrol.launch_dependents;");
-}
-
-// Barrier among the consumer warps only (the producer warp never joins).
-__device__ __forceinline__ void consumer_sync(int consumer_threads) {
-  asm volatile("bar.sync 1, %0;" ::"r"(consumer_threads) : "memory");
 }
 
 __device__ __forceinline__ int dp4a_us(uint32_t a, uint32_t b, int c) {
@@ -137,62 +126,91 @@ __device__ __forceinline__ int dp4a_us(uint32_t a, uint32_t b, int c) {
   return d;
 }
 
-// Shared-memory carve-up of one CTA (all offsets 16-byte aligned).
-struct SmemLayout {
-  uint32_t ring, xs, sums, red, bars, total;
-};
-
-// sums: [MT] spare, [consumers][MT] per-warp activation sums, 1 abort flag,
-//       [MT] activation scales s, [BW_MAX_WS] weight scales (as fp32);
-// red: [2][consumers][MT][8] row partials of the K-split mode.
-__host__ __device__ inline SmemLayout smem_layout(int mt, int kpad,
-                                                  uint32_t stage_bytes,
-                                                  int stages, int consumers) {
-  SmemLayout l;
-  l.ring = 0;
-  l.xs = l.ring + stage_bytes * uint32_t(stages);
-  l.sums = l.xs + uint32_t(mt * kpad);
-  const uint32_t sums_bytes =
-      uint32_t((mt + consumers * mt + 1 + mt + BW_MAX_WS) * 4);
-  l.red = (l.sums + sums_bytes + 15) / 16 * 16;
-  const uint32_t red_bytes = uint32_t(2 * consumers * mt * 8 * 4);
-  l.bars = (l.red + red_bytes + 15) / 16 * 16;
-  l.total = l.bars + uint32_t(2 * stages * 8);
-  return l;
+// Activations in shared memory: chunk j (64 int8 values) starts at byte
+// 64 j + 16 floor(j / 2).  A warp reads, in one instruction, the same
+// 16-byte word t of four chunks 4P + q (q = 0..3); with this padding the
+// four words fall in four distinct bank quarters (offsets 32P + {0, 64, 16,
+// 80} + 16t mod 128), so the broadcast load is one wavefront, not two.
+__host__ __device__ inline uint32_t xs_row_bytes(int chunks) {
+  return uint32_t(chunks) * 64u + uint32_t((chunks + 1) / 2) * 16u;
+}
+__device__ __forceinline__ uint32_t xs_chunk_off(int j) {
+  return uint32_t(j) * 64u + uint32_t(j >> 1) * 16u;
 }
 
-// Dot products of one row group held in shared memory, over the chunk quads
-// pq = first, first + step, ...: lane (q, r) takes chunk 4 pq + q of row r.
-// acc[m][i] collects slot i (codes scaled by 4^i) against activation row m.
+// Stages the MT activation rows (zero beyond K) in the padded layout and
+// returns this thread's share of sum_k x[m][k] in part[m].  All loads of a
+// row are independent; K is a multiple of 4.
+template <int MT>
+__device__ __forceinline__ void stage_x(const GemvArgs &a, int8_t *xs,
+                                        uint32_t xrow, int tid, int nthreads,
+                                        int (&part)[MT]) {
+#pragma unroll
+  for (int m = 0; m < MT; ++m) {
+    int p = 0;
+    int8_t *dst = xs + m * xrow;
+    if (a.vec_x) {
+      const uint4 *src =
+          reinterpret_cast<const uint4 *>(a.x + size_t(m) * a.x_ld);
+      for (int v = tid; v < a.chunks * 4; v += nthreads) {
+        uint4 x4 = make_uint4(0u, 0u, 0u, 0u);
+        if (16 * v < a.K) x4 = __ldg(src + v);
+        *reinterpret_cast<uint4 *>(dst + xs_chunk_off(v >> 2) + (v & 3) * 16) =
+            x4;
+        p = dp4a_us(0x01010101u, x4.x, p);
+        p = dp4a_us(0x01010101u, x4.y, p);
+        p = dp4a_us(0x01010101u, x4.z, p);
+        p = dp4a_us(0x01010101u, x4.w, p);
+      }
+    } else {
+      const unsigned int *src =
+          reinterpret_cast<const unsigned int *>(a.x + size_t(m) * a.x_ld);
+      for (int wd = tid; wd < a.chunks * 16; wd += nthreads) {
+        uint32_t v = 0u;
+        if (4 * wd < a.K) v = __ldg(src + wd);
+        *reinterpret_cast<uint32_t *>(dst + xs_chunk_off(wd >> 4) +
+                                      (wd & 15) * 4) = v;
+        p = dp4a_us(0x01010101u, v, p);
+      }
+    }
+    part[m] = p;
+  }
+}
+
+// Dot products of `chunks` consecutive chunks of one row group held in
+// shared memory at wbase, the first being chunk c0 of the row: lane (q, r)
+// takes chunks 4 pq + q of row r.  acc[m][i] collects slot i (codes scaled
+// by 4^i) against activation row m.  The four lanes q of one instruction
+// read x words of four consecutive chunks, conflict-free whatever c0 is.
 template <int MT>
 __device__ __forceinline__ void dot_row_group(const uint8_t *wbase,
-                                              const int8_t *xs, int kpad,
-                                              int chunks, int q, int r,
-                                              int first, int step,
-                                              int (&acc)[MT][4]) {
+                                              const int8_t *xs, uint32_t xrow,
+                                              int c0, int chunks, int q,
+                                              int r, int (&acc)[MT][4]) {
   const int quads = (chunks + 3) / 4;
 #pragma unroll 2
-  for (int pq = first; pq < quads; pq += step) {
+  for (int pq = 0; pq < quads; ++pq) {
     const int j = 4 * pq + q;
     if (j < chunks) {
       const uint4 wv = *reinterpret_cast<const uint4 *>(
           wbase + j * kGroupChunkBytes + r * kChunkBytes);
       const uint32_t wd[4] = {wv.x, wv.y, wv.z, wv.w};
+      const int8_t *xj = xs + xs_chunk_off(c0 + j);
 #pragma unroll
       for (int t = 0; t < 4; ++t) {
-        const uint32_t c0 = wd[t] & 0x03030303u;
-        const uint32_t c1 = wd[t] & 0x0c0c0c0cu;
-        const uint32_t c2 = wd[t] & 0x30303030u;
-        const uint32_t c3 = wd[t] & 0xc0c0c0c0u;
+        const uint32_t c0w = wd[t] & 0x03030303u;
+        const uint32_t c1w = wd[t] & 0x0c0c0c0cu;
+        const uint32_t c2w = wd[t] & 0x30303030u;
+        const uint32_t c3w = wd[t] & 0xc0c0c0c0u;
 #pragma unroll
         for (int m = 0; m < MT; ++m) {
           // activation words 4t..4t+3 of chunk j: k = 64j + 16t + 4i + b
-          const uint4 xv = *reinterpret_cast<const uint4 *>(
-              xs + m * kpad + j * kChunkWeights + 16 * t);
-          acc[m][0] = dp4a_us(c0, xv.x, acc[m][0]);
-          acc[m][1] = dp4a_us(c1, xv.y, acc[m][1]);
-          acc[m][2] = dp4a_us(c2, xv.z, acc[m][2]);
-          acc[m][3] = dp4a_us(c3, xv.w, acc[m][3]);
+          const uint4 xv =
+              *reinterpret_cast<const uint4 *>(xj + m * xrow + 16 * t);
+          acc[m][0] = dp4a_us(c0w, xv.x, acc[m][0]);
+          acc[m][1] = dp4a_us(c1w, xv.y, acc[m][1]);
+          acc[m][2] = dp4a_us(c2w, xv.z, acc[m][2]);
+          acc[m][3] = dp4a_us(c3w, xv.w, acc[m][3]);
         }
       }
     }
@@ -229,328 +247,303 @@ __device__ __forceinline__ void store_row(const GemvArgs &a, int n, int m,
   }
 }
 
+// ---------------------------------------------------------------------------
+// Balanced per-warp pipelines (pipe mode).
+//
+// CTA b owns the k consecutive row groups b k .. b k + k - 1 (the last CTA
+// may own fewer); its 8 warps split the CTA's k C chunks into 8 contiguous,
+// equal runs.  A warp walks its run in pieces of at most `slot_chunks`
+// chunks that never cross a row-group boundary; each piece is one bulk copy
+// into the next slot of the warp's own ring of `slots` slots.  Lane 0 of the
+// warp issues the copies: the first `slots` pieces before
+// griddepcontrol.wait, then piece i + slots into the slot of piece i as soon
+// as the warp has read it, so each warp keeps slots - 1 pieces in flight
+// whatever the other warps do.  When a piece ends a row group or the run, the
+// warp folds its partial sums and adds them (int32, exact in any order) to
+// the CTA's row totals in shared memory; one epilogue per CTA then scales
+// and stores the k * 8 rows.  Every warp has the same amount of work and
+// every CTA but the last the same number of groups, so no tail of the grid
+// runs on a few warps with few bytes in flight.
+struct PipeLayout {
+  uint32_t ring, xs, sums, tot, bars, total;
+};
+
+// sums: [MT] activation scales s, [BW_MAX_WS] weight scales (as fp32),
+// [warps][MT] per-warp activation sums; tot: [k][MT][8] row totals.
+__host__ __device__ inline PipeLayout pipe_layout(int mt, int chunks,
+                                                  int slot_chunks, int slots,
+                                                  int warps, int k) {
+  PipeLayout l;
+  l.ring = 0;
+  l.xs = uint32_t(warps * slots * slot_chunks) * kGroupChunkBytes;
+  l.sums = l.xs + uint32_t(mt) * xs_row_bytes(chunks);
+  const uint32_t sums_bytes = uint32_t((mt + BW_MAX_WS + warps * mt) * 4);
+  l.tot = (l.sums + sums_bytes + 15) / 16 * 16;
+  l.bars = l.tot + uint32_t(k * mt * 8 * 4);
+  l.total = l.bars + uint32_t(warps * slots * 8);
+  return l;
+}
+
+constexpr int kPipeWarps = 8;
+constexpr int kPipeMaxGroupsPerCta = 256;
+constexpr int kPipeMinGroupsPerCta = 2;  // fewer CTAs staging x for small N
+
+// Orders this warp's earlier generic-proxy reads of a slot before the
+// bulk copy (async proxy) that overwrites it.
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// Position in a warp's run: chunk u of the CTA's range = chunk c of the
+// CTA's row group g.
+struct RunCursor {
+  int u, g, c;
+  __device__ __forceinline__ int piece(int ks, int chunks, int end) const {
+    return min(min(ks, chunks - c), end - u);
+  }
+  __device__ __forceinline__ void advance(int len, int chunks) {
+    u += len;
+    c += len;
+    if (c == chunks) {
+      c = 0;
+      ++g;
+    }
+  }
+};
+
 template <int MT, bool ACC_OUT>
-__global__ void __launch_bounds__(288)
-gemv_w2a8_tma_kernel(const GemvArgs a, const TmaPlan p) {
+__global__ void __launch_bounds__(kPipeWarps * 32)
+gemv_w2a8_pipe_kernel(const GemvArgs a, const TmaPlan p) {
   extern __shared__ __align__(128) uint8_t smem[];
-  const int warps = blockDim.x >> 5;
-  const int consumers = warps - 1;
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int S = p.groups_per_stage;
-  const int NS = p.stages;
-  const int kpad = a.chunks * kChunkWeights;
-  const uint32_t group_bytes = uint32_t(a.chunks) * kGroupChunkBytes;
-  const uint32_t stage_bytes = uint32_t(S) * group_bytes;
-  const SmemLayout L = smem_layout(MT, kpad, stage_bytes, NS, consumers);
-  uint8_t *ring = smem + L.ring;
+  const int KS = p.slot_chunks;
+  const int R = p.slots;
+  const int C = a.chunks;
+  const int k = p.groups_per_cta;
+  const uint32_t slot_bytes = uint32_t(KS) * kGroupChunkBytes;
+  const uint32_t xrow = xs_row_bytes(C);
+  const PipeLayout L = pipe_layout(MT, C, KS, R, kPipeWarps, k);
+  uint8_t *ring = smem + L.ring + size_t(warp) * R * slot_bytes;
   int8_t *xs = reinterpret_cast<int8_t *>(smem + L.xs);
-  int *sx_part = reinterpret_cast<int *>(smem + L.sums) + MT;  // [cons][MT]
-  volatile int *abort_flag = sx_part + consumers * MT;
-  float *s_sm = reinterpret_cast<float *>(sx_part + consumers * MT + 1);
+  float *s_sm = reinterpret_cast<float *>(smem + L.sums);
   float *ws_sm = s_sm + MT;
-  int *red = reinterpret_cast<int *>(smem + L.red);
-  uint64_t *full = reinterpret_cast<uint64_t *>(smem + L.bars);
-  uint64_t *empty = full + NS;
+  int *sx_part = reinterpret_cast<int *>(ws_sm + BW_MAX_WS);  // [warps][MT]
+  int *tot = reinterpret_cast<int *>(smem + L.tot);           // [k][MT][8]
+  uint64_t *full = reinterpret_cast<uint64_t *>(smem + L.bars) + warp * R;
 
-  const int n_stages = (a.n_groups + S - 1) / S;
-  const int grid = gridDim.x;
-  const int n_local = (n_stages - int(blockIdx.x) + grid - 1) / grid;
+  const int g_lo = int(blockIdx.x) * k;
+  const int n_g = min(k, a.n_groups - g_lo);
+  const int U = n_g * C;  // chunks of this CTA (k C <= 256 * 384)
+  const int run_lo = U * warp / kPipeWarps;
+  const int run_hi = U * (warp + 1) / kPipeWarps;
+  const uint8_t *wcta = a.w + size_t(g_lo) * C * kGroupChunkBytes;
 
-  if (threadIdx.x == 0) {
-    for (int s = 0; s < NS; ++s) {
-      mbar_init(&full[s], 1);
-      mbar_init(&empty[s], p.split ? 1u : uint32_t(S));
-    }
-    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-  }
-  __syncthreads();  // barriers initialised before any copy or wait
-
-  // The first ring fills start before the dependency on earlier work
-  // resolves: the weights are static once written (bw_repack synchronises
-  // its stream), so only the activations and scales -- which the preceding
-  // kernel may produce -- wait for griddepcontrol.wait.
-  auto fill = [&](int i) {
-    const int s = i % NS;
-    const int g0 = (int(blockIdx.x) + i * grid) * S;
-    const int g1 = min(g0 + S, a.n_groups);
-    const uint32_t bytes = uint32_t(g1 - g0) * group_bytes;
-    mbar_arrive_expect_tx(&full[s], bytes);
-    bulk_copy_g2s(ring + size_t(s) * stage_bytes,
-                  a.w + size_t(g0) * group_bytes, bytes, &full[s]);
+  RunCursor iss;  // next piece to copy (lane 0)
+  iss.u = run_lo;
+  iss.g = run_lo / C;
+  iss.c = run_lo - iss.g * C;
+  RunCursor cur = iss;  // next piece to consume (whole warp)
+  int issued = 0;
+  auto issue_next = [&](int slot) {
+    const int len = iss.piece(KS, C, run_hi);
+    const uint32_t bytes = uint32_t(len) * kGroupChunkBytes;
+    mbar_arrive_expect_tx(&full[slot], bytes);
+    bulk_copy_g2s(ring + size_t(slot) * slot_bytes,
+                  wcta + (size_t(iss.g) * C + iss.c) * kGroupChunkBytes,
+                  bytes, &full[slot]);
+    iss.advance(len, C);
+    ++issued;
   };
-  const int early = NS < n_local ? NS : n_local;
-  if (warp == consumers && lane == 0) {
-    for (int i = 0; i < early; ++i) fill(i);
-    for (int i = early; i < n_local && i < 2 * NS; ++i) {  // next ones: L2
-      const int g0 = (int(blockIdx.x) + i * grid) * S;
-      const int g1 = min(g0 + S, a.n_groups);
-      prefetch_l2(a.w + size_t(g0) * group_bytes,
-                  uint32_t(g1 - g0) * group_bytes);
-    }
+  if (lane == 0) {
+    for (int s = 0; s < R; ++s) mbar_init(&full[s], 1);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    // The weights are static once written (bw_repack synchronises its
+    // stream): the first pieces are requested before the dependency wait.
+    for (int s = 0; s < R && iss.u < run_hi; ++s) issue_next(s);
   }
+  for (int t = threadIdx.x; t < n_g * MT * 8; t += blockDim.x) tot[t] = 0;
   pdl_wait();
 
-  if (warp == consumers) {
-    // ---------------------------------------------------------- producer
-    pdl_trigger();
-    if (lane == 0) {
-      int issued = early;
-      bool ok = true;
-      for (int i = early; i < n_local; ++i) {
-        const int s = i % NS;
-        if (!mbar_wait(&empty[s], uint32_t((i / NS) - 1) & 1u)) {
-          ok = false;
-          break;
-        }
-        fill(i);
-        ++issued;
-      }
-      if (!ok) atomicOr(&g_device_error, 1u);
-      // Every issued copy has landed before this thread leaves (normally
-      // the consumers have already waited for them; after a time-out they
-      // may not have).
-      for (int i = max(0, issued - NS); i < issued; ++i)
-        if (!mbar_wait(&full[i % NS], uint32_t(i / NS) & 1u))
-          atomicOr(&g_device_error, 2u);
-    }
-    return;
-  }
-
-  // ------------------------------------------------------------- consumers
-  const int cthreads = consumers * 32;
-  // Stage the scales, the activations (zero beyond K) and the per-warp
-  // activation sums; all loads are issued before any is used.
   if (!ACC_OUT) {
     if (threadIdx.x < MT) s_sm[threadIdx.x] = a.s[threadIdx.x];
     if (threadIdx.x >= 32 && threadIdx.x < 32 + a.seg.n_ws)
       ws_sm[threadIdx.x - 32] = __bfloat162float(a.ws[threadIdx.x - 32]);
   }
+  int part[MT];
+  stage_x<MT>(a, xs, xrow, threadIdx.x, int(blockDim.x), part);
 #pragma unroll
   for (int m = 0; m < MT; ++m) {
-    int part = 0;
-    if (a.vec_x) {
-      const uint4 *xrow = reinterpret_cast<const uint4 *>(a.x + size_t(m) * a.x_ld);
-      uint4 *dst = reinterpret_cast<uint4 *>(xs + m * kpad);
-      for (int v = threadIdx.x; v < kpad / 16; v += cthreads) {
-        uint4 x4 = make_uint4(0u, 0u, 0u, 0u);
-        if (16 * v < a.K) x4 = __ldg(xrow + v);
-        dst[v] = x4;
-        part = dp4a_us(0x01010101u, x4.x, part);
-        part = dp4a_us(0x01010101u, x4.y, part);
-        part = dp4a_us(0x01010101u, x4.z, part);
-        part = dp4a_us(0x01010101u, x4.w, part);
-      }
-    } else {
-      const unsigned int *xrow =
-          reinterpret_cast<const unsigned int *>(a.x + size_t(m) * a.x_ld);
-      uint32_t *dst = reinterpret_cast<uint32_t *>(xs + m * kpad);
-      for (int wd = threadIdx.x; wd < kpad / 4; wd += cthreads) {
-        uint32_t v = 0u;
-        if (4 * wd < a.K) v = __ldg(xrow + wd);
-        dst[wd] = v;
-        part = dp4a_us(0x01010101u, v, part);
-      }
-    }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1)
-      part += __shfl_xor_sync(0xffffffffu, part, o);
-    if (lane == 0) sx_part[warp * MT + m] = part;
+      part[m] += __shfl_xor_sync(0xffffffffu, part[m], o);
+    if (lane == 0) sx_part[warp * MT + m] = part[m];
   }
-  if (threadIdx.x == 0) *abort_flag = 0;
-  consumer_sync(cthreads);
+  __syncthreads();  // activations staged, totals zeroed, barriers set up
+  pdl_trigger();    // dependents may start their prologue on free SM slots
+
+  const int q = lane >> 3;  // chunk residue (relative to the piece) mod 4
+  const int r = lane & 7;   // row inside the group
+  int acc[MT][4];
+#pragma unroll
+  for (int m = 0; m < MT; ++m)
+#pragma unroll
+    for (int t = 0; t < 4; ++t) acc[m][t] = 0;
+  bool ok = true;
+  int consumed = 0, slot = 0;
+  uint32_t phase = 0;
+  while (cur.u < run_hi) {
+    // warp-uniform outcome before any full-mask shuffle below
+    if (!__all_sync(0xffffffffu, mbar_wait(&full[slot], phase))) {
+      ok = false;
+      break;
+    }
+    const int len = cur.piece(KS, C, run_hi);
+    dot_row_group<MT>(ring + size_t(slot) * slot_bytes, xs, xrow, cur.c, len,
+                      q, r, acc);
+    __syncwarp();
+    if (lane == 0 && iss.u < run_hi) {  // piece consumed + R: this slot
+      fence_proxy_async_smem();
+      issue_next(slot);
+    }
+    const int g = cur.g;
+    cur.advance(len, C);
+    ++consumed;
+    if (cur.c == 0 || cur.u == run_hi) {  // row group or run finished
+#pragma unroll
+      for (int m = 0; m < MT; ++m) {
+        const int v = fold_row(acc[m]);
+        if (q == 0) atomicAdd(&tot[(g * MT + m) * 8 + r], v);
+#pragma unroll
+        for (int t = 0; t < 4; ++t) acc[m][t] = 0;
+      }
+    }
+    if (++slot == R) {
+      slot = 0;
+      phase ^= 1u;
+    }
+  }
+  if (!ok && lane == 0) {
+    atomicOr(&g_device_error, 4u);
+    // copies still in flight land before the CTA may leave
+    for (int i = consumed; i < issued; ++i)
+      if (!mbar_wait(&full[i % R], uint32_t(i / R) & 1u))
+        atomicOr(&g_device_error, 2u);
+  }
+  __syncthreads();  // every partial sum is in `tot`
+
   int sx[MT];  // sum_k x[m][k] over the whole row
 #pragma unroll
   for (int m = 0; m < MT; ++m) {
     sx[m] = 0;
-    for (int w = 0; w < consumers; ++w) sx[m] += sx_part[w * MT + m];
+#pragma unroll
+    for (int w = 0; w < kPipeWarps; ++w) sx[m] += sx_part[w * MT + m];
   }
-  pdl_trigger();  // dependents may start their prologue on free SM slots
-
-  const int q = lane >> 3;  // chunk residue mod 4
-  const int r = lane & 7;   // row inside the group
-
-  if (p.split) {
-    // One row group per stage; consumer warp w takes chunk quads w, w + 8,
-    // ...; row partials meet in shared memory (double-buffered by stage
-    // parity, one consumer barrier per stage).
-    for (int i = 0; i < n_local; ++i) {
-      const int s = i % NS;
-      const bool ok =
-          __all_sync(0xffffffffu, mbar_wait(&full[s], uint32_t(i / NS) & 1u));
-      if (!ok && lane == 0) {
-        atomicOr(&g_device_error, 4u);
-        *abort_flag = 1;
-      }
-      int acc[MT][4];
+  for (int t = threadIdx.x; t < n_g * 8; t += blockDim.x) {
+    const int gl = t >> 3, rr = t & 7;
+    const int n = (g_lo + gl) * kGroupRows + rr;
+    if (n < a.N) {
 #pragma unroll
       for (int m = 0; m < MT; ++m)
-#pragma unroll
-        for (int t = 0; t < 4; ++t) acc[m][t] = 0;
-      if (ok)
-        dot_row_group<MT>(ring + size_t(s) * stage_bytes, xs, kpad, a.chunks,
-                          q, r, warp, consumers, acc);
-      int *rb = red + (i & 1) * (consumers * MT * 8);
-#pragma unroll
-      for (int m = 0; m < MT; ++m) {
-        const int v = fold_row(acc[m]);
-        if (q == 0) rb[(warp * MT + m) * 8 + r] = v;
-      }
-      // every warp reaches this barrier, also after a time-out
-      consumer_sync(cthreads);
-      if (*abort_flag) break;
-      if (threadIdx.x == 0) mbar_arrive(&empty[s]);  // stage fully read
-      if (warp == 0 && lane < 8) {
-        const int n = (int(blockIdx.x) + i * grid) * kGroupRows + lane;
-        if (n < a.N) {
-#pragma unroll
-          for (int m = 0; m < MT; ++m) {
-            int total = -sx[m];
-            for (int w = 0; w < consumers; ++w)
-              total += rb[(w * MT + m) * 8 + lane];
-            store_row<MT, ACC_OUT>(a, n, m, total, s_sm, ws_sm);
-          }
-        }
-      }
+        store_row<MT, ACC_OUT>(a, n, m, tot[(gl * MT + m) * 8 + rr] - sx[m],
+                               s_sm, ws_sm);
     }
-    return;
   }
-
-  // One warp per row group: teams of S warps take every T-th stage.
-  const int teams = consumers / S;
-  const int team = warp / S;
-  const int member = warp % S;
-
-  int my_group = -1;  // row group whose totals this lane keeps
-  int my_tot[MT];
-#pragma unroll
-  for (int m = 0; m < MT; ++m) my_tot[m] = 0;
-  int handled = 0;
-
-  auto epilogue = [&]() {
-    const int n = my_group * kGroupRows + r;
-    if (my_group >= 0 && n < a.N) {
-#pragma unroll
-      for (int m = 0; m < MT; ++m)
-        store_row<MT, ACC_OUT>(a, n, m, my_tot[m], s_sm, ws_sm);
-    }
-    my_group = -1;
-  };
-
-  for (int i = team; i < n_local; i += teams) {
-    const int s = i % NS;
-    // warp-uniform outcome before any full-mask shuffle below
-    if (!__all_sync(0xffffffffu, mbar_wait(&full[s], uint32_t(i / NS) & 1u))) {
-      if (lane == 0) atomicOr(&g_device_error, 4u);
-      break;
-    }
-    const int grp = (int(blockIdx.x) + i * grid) * S + member;
-    int tot[MT];
-#pragma unroll
-    for (int m = 0; m < MT; ++m) tot[m] = 0;
-    if (grp < a.n_groups) {
-      int acc[MT][4];
-#pragma unroll
-      for (int m = 0; m < MT; ++m)
-#pragma unroll
-        for (int t = 0; t < 4; ++t) acc[m][t] = 0;
-      dot_row_group<MT>(
-          ring + size_t(s) * stage_bytes + size_t(member) * group_bytes, xs,
-          kpad, a.chunks, q, r, 0, 1, acc);
-#pragma unroll
-      for (int m = 0; m < MT; ++m) tot[m] = fold_row(acc[m]) - sx[m];
-    }
-    __syncwarp();
-    if (lane == 0) mbar_arrive(&empty[s]);
-    if (q == (handled & 3)) {
-      my_group = grp;
-#pragma unroll
-      for (int m = 0; m < MT; ++m) my_tot[m] = tot[m];
-    }
-    ++handled;
-    if ((handled & 3) == 0) epilogue();
-  }
-  if (handled & 3) epilogue();
 }
 
-template <int MT, bool ACC>
-cudaError_t launch_tma_instance(const TmaPlan &p, const GemvArgs &a,
-                                cudaStream_t stream) {
-  const int kpad = a.chunks * kChunkWeights;
-  const uint32_t stage_bytes =
-      uint32_t(p.groups_per_stage) * uint32_t(a.chunks) * kGroupChunkBytes;
-  const SmemLayout L =
-      smem_layout(MT, kpad, stage_bytes, p.stages, p.consumers);
-  static bool configured[64];  // per device: the opt-in smem attribute
+// Sets the opt-in shared-memory size once per device and returns how many
+// CTAs of `kernel` are resident on the device at once (at least one).
+template <class Kernel>
+cudaError_t resident_ctas(Kernel kernel, bool *configured, int threads,
+                          uint32_t smem, int64_t *resident) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
   if (!configured[dev]) {
-    e = cudaFuncSetAttribute(gemv_w2a8_tma_kernel<MT, ACC>,
+    e = cudaFuncSetAttribute(kernel,
                              cudaFuncAttributeMaxDynamicSharedMemorySize,
                              227 * 1024);
     if (e != cudaSuccess) return e;
     configured[dev] = true;
   }
-  const int threads = (p.consumers + 1) * 32;
   int per_sm = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(
-          &per_sm, gemv_w2a8_tma_kernel<MT, ACC>, threads, L.total) !=
-          cudaSuccess ||
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, threads,
+                                                    smem) != cudaSuccess ||
       per_sm < 1)
     per_sm = 1;
-  const int n_stages =
-      (a.n_groups + p.groups_per_stage - 1) / p.groups_per_stage;
-  const int resident = per_sm * device_sm_count();
-  const int grid = n_stages < resident ? n_stages : resident;
+  *resident = int64_t(per_sm) * device_sm_count();
+  return cudaSuccess;
+}
+
+// Launches `kernel` on `grid` CTAs with programmatic dependent launch.
+template <class Kernel>
+cudaError_t launch_pdl(Kernel kernel, int64_t grid, int threads,
+                       uint32_t smem, const GemvArgs &a, const TmaPlan &p,
+                       cudaStream_t stream) {
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(grid > 0 ? grid : 1);
+  cfg.gridDim = dim3(unsigned(grid > 0 ? grid : 1));
   cfg.blockDim = dim3(threads);
-  cfg.dynamicSmemBytes = L.total;
+  cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, gemv_w2a8_tma_kernel<MT, ACC>, a, p);
+  return cudaLaunchKernelEx(&cfg, kernel, a, p);
+}
+
+template <int MT, bool ACC>
+cudaError_t launch_tma_instance(const TmaPlan &plan, const GemvArgs &a,
+                                cudaStream_t stream) {
+  int64_t resident = 0;
+  // k groups per CTA with k as small as the resident CTAs allow
+  // (at most kPipeMaxGroupsPerCta; beyond that the grid runs in waves), and
+  // slots no longer than a warp's run.
+  static bool configured[64];
+  TmaPlan p = plan;
+  // k from the residency at k = 1, then once more at that k (the row
+  // totals grow with k).
+  int64_t k = 1;
+  for (int pass = 0; pass < 2; ++pass) {
+    const PipeLayout Lk = pipe_layout(MT, a.chunks, p.slot_chunks, p.slots,
+                                      kPipeWarps, int(k));
+    cudaError_t e = resident_ctas(gemv_w2a8_pipe_kernel<MT, ACC>, configured,
+                                  kPipeWarps * 32, Lk.total, &resident);
+    if (e != cudaSuccess) return e;
+    k = (a.n_groups + resident - 1) / resident;
+    if (k > kPipeMaxGroupsPerCta) k = kPipeMaxGroupsPerCta;
+    if (k < kPipeMinGroupsPerCta) k = kPipeMinGroupsPerCta;
+  }
+  const int64_t grid = (a.n_groups + k - 1) / k;
+  const int64_t run = (k * a.chunks + kPipeWarps - 1) / kPipeWarps;
+  if (run < p.slot_chunks) p.slot_chunks = int(run < 1 ? 1 : run);
+  p.groups_per_cta = int(k);
+  const PipeLayout L = pipe_layout(MT, a.chunks, p.slot_chunks, p.slots,
+                                   kPipeWarps, p.groups_per_cta);
+  return launch_pdl(gemv_w2a8_pipe_kernel<MT, ACC>, grid, kPipeWarps * 32,
+                    L.total, a, p, stream);
 }
 
 }  // namespace
 
 bool plan_gemv_tma(int mt, int N, int K, int num_sms, TmaPlan *p) {
-  const int chunks = chunks_per_row(K);
-  const uint32_t group_bytes = uint32_t(chunks) * kGroupChunkBytes;
-  constexpr uint32_t kStageTarget = 24 * 1024;
-  constexpr uint32_t kRingBudget = 96 * 1024;   // two CTAs fit in one SM
-  constexpr uint32_t kSplitBudget = 48 * 1024;  // four CTAs fit in one SM
+  (void)N;
+  (void)num_sms;
   if (mt != 1 && mt != 2 && mt != 4) return false;
-  if (group_bytes > kRingBudget / 2) return false;  // K too long: other path
-  p->consumers = 8;
-  const int64_t groups = padded_rows(N) / kGroupRows;
-  // Few row groups (up to four per SM): split each row group's K across all
-  // consumer warps, so no warp walks a whole row alone and every CTA
-  // finishes its one or two row groups at about the same time.
-  if (groups <= 4 * int64_t(num_sms)) {
-    p->split = 1;
-    p->groups_per_stage = 1;
-    const int stages = int(kSplitBudget / group_bytes);
-    p->stages = stages < 2 ? 2 : (stages > 4 ? 4 : stages);
-    return true;
-  }
-  // Many row groups: one warp per row group, S row groups per stage, with S
-  // small enough that every CTA (about two per SM) still gets eight stages,
-  // one per consumer team at least.
-  p->split = 0;
-  int S = 1;
-  while (S < p->consumers && 2 * S * group_bytes <= kStageTarget &&
-         groups / (2 * S) >= 16 * int64_t(num_sms))
-    S *= 2;
-  p->groups_per_stage = S;
-  const int stages = int(kRingBudget / (uint32_t(S) * group_bytes));
-  p->stages = stages < 2 ? 2 : (stages > 8 ? 8 : stages);
-  return true;
+  // Pieces of up to 4 KB, two slots per warp: 64 KB of ring per 8-warp CTA,
+  // about three CTAs per SM for K <= 8192.
+  p->consumers = kPipeWarps;
+  p->slot_chunks = 32;
+  p->slots = 2;
+  p->groups_per_cta = 0;  // chosen at launch from the resident CTAs
+  // The activations are staged whole: K too long for shared memory goes to
+  // the register-streamed kernel.
+  const PipeLayout L = pipe_layout(mt, chunks_per_row(K), p->slot_chunks,
+                                   p->slots, kPipeWarps,
+                                   kPipeMaxGroupsPerCta);
+  return L.total <= 227u * 1024u;
 }
 
 cudaError_t launch_gemv_tma(const TmaPlan &p, const GemvArgs &a, int mt,

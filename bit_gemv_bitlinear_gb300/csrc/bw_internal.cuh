@@ -51,14 +51,14 @@ struct GemvPlan {
   int grid;    // CTAs
 };
 
-// TMA-streamed GEMV (bw_gemv_tma.cu): a shared-memory ring of `stages`
-// buffers of `groups_per_stage` row groups, `consumers` compute warps and
-// one producer warp.
+// TMA-streamed GEMV (bw_gemv_tma.cu): `groups_per_cta` row groups per CTA
+// of `consumers` warps; each warp streams an equal share of the CTA's chunks
+// through its own ring of `slots` pieces of at most `slot_chunks` chunks.
 struct TmaPlan {
   int consumers;
-  int groups_per_stage;
-  int stages;
-  int split;  // 1: one row group per stage, K split across all consumers
+  int slot_chunks;
+  int slots;
+  int groups_per_cta;
 };
 bool plan_gemv_tma(int mt, int N, int K, int num_sms, TmaPlan *plan);
 cudaError_t launch_gemv_tma(const TmaPlan &plan, const GemvArgs &args, int mt,
