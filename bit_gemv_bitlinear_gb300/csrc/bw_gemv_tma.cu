@@ -20,8 +20,7 @@
 //  * Lane (q, r): row r of the group, chunks j = q (mod 4).  One 128-bit
 //    shared load gives 64 codes (a contiguous 512-byte warp access, no bank
 //    conflict); the int8 activations, staged once in shared memory, come as
-//    four 128-bit broadcast loads per chunk (conflict-free thanks to a
-//    16-byte pad every two chunks).  Decode = one AND per 4 codes
+//    four 128-bit broadcast loads per chunk.  Decode = one AND per 4 codes
 //    (unsigned codes c = w + 1 masked in place, unsigned x signed dp4a); the
 //    4^i slot factor and the sum_k x offset are removed once per row.
 //  * Every mbarrier wait is bounded (clock64); on time-out the kernel sets
@@ -126,19 +125,13 @@ __device__ __forceinline__ int dp4a_us(uint32_t a, uint32_t b, int c) {
   return d;
 }
 
-// Activations in shared memory: chunk j (64 int8 values) starts at byte
-// 64 j + 16 floor(j / 2).  A warp reads, in one instruction, the same
-// 16-byte word t of four chunks 4P + q (q = 0..3); with this padding the
-// four words fall in four distinct bank quarters (offsets 32P + {0, 64, 16,
-// 80} + 16t mod 128), so the broadcast load is one wavefront, not two.
+// Activations in shared memory: row m, chunk j (64 int8 values) at byte
+// m xrow + 64 j, zero beyond K.
 __host__ __device__ inline uint32_t xs_row_bytes(int chunks) {
-  return uint32_t(chunks) * 64u + uint32_t((chunks + 1) / 2) * 16u;
-}
-__device__ __forceinline__ uint32_t xs_chunk_off(int j) {
-  return uint32_t(j) * 64u + uint32_t(j >> 1) * 16u;
+  return uint32_t(chunks) * 64u;
 }
 
-// Stages the MT activation rows (zero beyond K) in the padded layout and
+// Stages the MT activation rows (zero beyond K) in shared memory and
 // returns this thread's share of sum_k x[m][k] in part[m].  All loads of a
 // row are independent; K is a multiple of 4.
 template <int MT>
@@ -155,8 +148,7 @@ __device__ __forceinline__ void stage_x(const GemvArgs &a, int8_t *xs,
       for (int v = tid; v < a.chunks * 4; v += nthreads) {
         uint4 x4 = make_uint4(0u, 0u, 0u, 0u);
         if (16 * v < a.K) x4 = __ldg(src + v);
-        *reinterpret_cast<uint4 *>(dst + xs_chunk_off(v >> 2) + (v & 3) * 16) =
-            x4;
+        reinterpret_cast<uint4 *>(dst)[v] = x4;
         p = dp4a_us(0x01010101u, x4.x, p);
         p = dp4a_us(0x01010101u, x4.y, p);
         p = dp4a_us(0x01010101u, x4.z, p);
@@ -168,8 +160,7 @@ __device__ __forceinline__ void stage_x(const GemvArgs &a, int8_t *xs,
       for (int wd = tid; wd < a.chunks * 16; wd += nthreads) {
         uint32_t v = 0u;
         if (4 * wd < a.K) v = __ldg(src + wd);
-        *reinterpret_cast<uint32_t *>(dst + xs_chunk_off(wd >> 4) +
-                                      (wd & 15) * 4) = v;
+        reinterpret_cast<uint32_t *>(dst)[wd] = v;
         p = dp4a_us(0x01010101u, v, p);
       }
     }
@@ -177,44 +168,51 @@ __device__ __forceinline__ void stage_x(const GemvArgs &a, int8_t *xs,
   }
 }
 
+// Products of one chunk: 16 bytes of packed codes (row r, 64 weights) at
+// wp against the 64 activations of each row m at xp + m xrow.
+template <int MT>
+__device__ __forceinline__ void dot_chunk(const uint8_t *wp, const int8_t *xp,
+                                          uint32_t xrow, int (&acc)[MT][4]) {
+  const uint4 wv = *reinterpret_cast<const uint4 *>(wp);
+  const uint32_t wd[4] = {wv.x, wv.y, wv.z, wv.w};
+#pragma unroll
+  for (int t = 0; t < 4; ++t) {
+    const uint32_t c0w = wd[t] & 0x03030303u;
+    const uint32_t c1w = wd[t] & 0x0c0c0c0cu;
+    const uint32_t c2w = wd[t] & 0x30303030u;
+    const uint32_t c3w = wd[t] & 0xc0c0c0c0u;
+#pragma unroll
+    for (int m = 0; m < MT; ++m) {
+      // activation words 4t..4t+3 of the chunk: k = 64j + 16t + 4i + b
+      const uint4 xv = *reinterpret_cast<const uint4 *>(xp + m * xrow + 16 * t);
+      acc[m][0] = dp4a_us(c0w, xv.x, acc[m][0]);
+      acc[m][1] = dp4a_us(c1w, xv.y, acc[m][1]);
+      acc[m][2] = dp4a_us(c2w, xv.z, acc[m][2]);
+      acc[m][3] = dp4a_us(c3w, xv.w, acc[m][3]);
+    }
+  }
+}
+
 // Dot products of `chunks` consecutive chunks of one row group held in
 // shared memory at wbase, the first being chunk c0 of the row: lane (q, r)
 // takes chunks 4 pq + q of row r.  acc[m][i] collects slot i (codes scaled
-// by 4^i) against activation row m.  The four lanes q of one instruction
-// read x words of four consecutive chunks, conflict-free whatever c0 is.
+// by 4^i) against activation row m.  Two pointers advance by constants;
+// only the last, partial quad is predicated.
 template <int MT>
 __device__ __forceinline__ void dot_row_group(const uint8_t *wbase,
                                               const int8_t *xs, uint32_t xrow,
                                               int c0, int chunks, int q,
                                               int r, int (&acc)[MT][4]) {
-  const int quads = (chunks + 3) / 4;
+  const uint8_t *wp = wbase + q * kGroupChunkBytes + r * kChunkBytes;
+  const int8_t *xp = xs + (c0 + q) * kChunkWeights;
+  const int quads = chunks >> 2;
 #pragma unroll 2
   for (int pq = 0; pq < quads; ++pq) {
-    const int j = 4 * pq + q;
-    if (j < chunks) {
-      const uint4 wv = *reinterpret_cast<const uint4 *>(
-          wbase + j * kGroupChunkBytes + r * kChunkBytes);
-      const uint32_t wd[4] = {wv.x, wv.y, wv.z, wv.w};
-      const int8_t *xj = xs + xs_chunk_off(c0 + j);
-#pragma unroll
-      for (int t = 0; t < 4; ++t) {
-        const uint32_t c0w = wd[t] & 0x03030303u;
-        const uint32_t c1w = wd[t] & 0x0c0c0c0cu;
-        const uint32_t c2w = wd[t] & 0x30303030u;
-        const uint32_t c3w = wd[t] & 0xc0c0c0c0u;
-#pragma unroll
-        for (int m = 0; m < MT; ++m) {
-          // activation words 4t..4t+3 of chunk j: k = 64j + 16t + 4i + b
-          const uint4 xv =
-              *reinterpret_cast<const uint4 *>(xj + m * xrow + 16 * t);
-          acc[m][0] = dp4a_us(c0w, xv.x, acc[m][0]);
-          acc[m][1] = dp4a_us(c1w, xv.y, acc[m][1]);
-          acc[m][2] = dp4a_us(c2w, xv.z, acc[m][2]);
-          acc[m][3] = dp4a_us(c3w, xv.w, acc[m][3]);
-        }
-      }
-    }
+    dot_chunk<MT>(wp, xp, xrow, acc);
+    wp += 4 * kGroupChunkBytes;
+    xp += 4 * kChunkWeights;
   }
+  if (q < (chunks & 3)) dot_chunk<MT>(wp, xp, xrow, acc);
 }
 
 // Remove the slot factors: (((a3/4 + a2)/4 + a1)/4 + a0, exact because a_i is
@@ -508,21 +506,21 @@ cudaError_t launch_tma_instance(const TmaPlan &plan, const GemvArgs &a,
   int64_t k = 1;
   for (int pass = 0; pass < 2; ++pass) {
     const PipeLayout Lk = pipe_layout(MT, a.chunks, p.slot_chunks, p.slots,
-                                      kPipeWarps, int(k));
+                                      p.consumers, int(k));
     cudaError_t e = resident_ctas(gemv_w2a8_pipe_kernel<MT, ACC>, configured,
-                                  kPipeWarps * 32, Lk.total, &resident);
+                                  p.consumers * 32, Lk.total, &resident);
     if (e != cudaSuccess) return e;
     k = (a.n_groups + resident - 1) / resident;
     if (k > kPipeMaxGroupsPerCta) k = kPipeMaxGroupsPerCta;
     if (k < kPipeMinGroupsPerCta) k = kPipeMinGroupsPerCta;
   }
   const int64_t grid = (a.n_groups + k - 1) / k;
-  const int64_t run = (k * a.chunks + kPipeWarps - 1) / kPipeWarps;
+  const int64_t run = (k * a.chunks + p.consumers - 1) / p.consumers;
   if (run < p.slot_chunks) p.slot_chunks = int(run < 1 ? 1 : run);
   p.groups_per_cta = int(k);
   const PipeLayout L = pipe_layout(MT, a.chunks, p.slot_chunks, p.slots,
-                                   kPipeWarps, p.groups_per_cta);
-  return launch_pdl(gemv_w2a8_pipe_kernel<MT, ACC>, grid, kPipeWarps * 32,
+                                   p.consumers, p.groups_per_cta);
+  return launch_pdl(gemv_w2a8_pipe_kernel<MT, ACC>, grid, p.consumers * 32,
                     L.total, a, p, stream);
 }
 
@@ -541,7 +539,7 @@ bool plan_gemv_tma(int mt, int N, int K, int num_sms, TmaPlan *p) {
   // The activations are staged whole: K too long for shared memory goes to
   // the register-streamed kernel.
   const PipeLayout L = pipe_layout(mt, chunks_per_row(K), p->slot_chunks,
-                                   p->slots, kPipeWarps,
+                                   p->slots, p->consumers,
                                    kPipeMaxGroupsPerCta);
   return L.total <= 227u * 1024u;
 }
