@@ -497,7 +497,7 @@ def run_stack_timing(torch, bw, dev, n_layers=STACK_LAYERS,
             "us_per_token": round(us_tok, 2),
             "weight_bytes_per_token": layer_bytes * n_layers,
             "weight_GBps": round(layer_bytes * n_layers / (us_tok * 1e3), 1),
-            "launches_per_token": 8 * n_layers + 1,
+            "launches_per_token": 4 * n_layers,
             "timing": f"best of {reps} runs of {steps} steps, CUDA events"}
 
 

@@ -93,10 +93,9 @@ bw_status gemv_common(const int8_t *x, const uint8_t *packed, const float *s,
     a.s = acc_out ? nullptr : s + m0;
     a.out = static_cast<char *>(out) + size_t(m0) * N * out_elem;
     cudaError_t e;
-    TmaPlan tplan;
-    if (plan_gemv_tma(mt, N, K, sms, &tplan)) {
-      e = launch_gemv_tma(tplan, a, mt, acc_out, stream);
-    } else {  // K beyond the shared-memory ring: register-streamed kernel
+    if (pipe_fits(mt, K)) {
+      e = launch_gemv_pipe(a, mt, acc_out, stream);
+    } else {  // activations too long for shared memory: register-streamed
       GemvPlan plan = plan_gemv(mt, N, K, sms);
       a.passes = plan.passes;
       e = launch_gemv(plan, a, acc_out, stream);

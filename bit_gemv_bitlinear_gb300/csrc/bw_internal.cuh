@@ -51,18 +51,15 @@ struct GemvPlan {
   int grid;    // CTAs
 };
 
-// TMA-streamed GEMV (bw_gemv_tma.cu): `groups_per_cta` row groups per CTA
-// of `consumers` warps; each warp streams an equal share of the CTA's chunks
-// through its own ring of `slots` pieces of at most `slot_chunks` chunks.
-struct TmaPlan {
-  int consumers;
-  int slot_chunks;
-  int slots;
-  int groups_per_cta;
-};
-bool plan_gemv_tma(int mt, int N, int K, int num_sms, TmaPlan *plan);
-cudaError_t launch_gemv_tma(const TmaPlan &plan, const GemvArgs &args, int mt,
-                            bool acc_out, cudaStream_t stream);
+// TMA-streamed GEMV (bw_gemv_tma.cu, kernel in bw_pipe.cuh) for M-tiles of
+// mt = 1, 2 or 4 rows; pipe_fits() is false where the staged activations
+// do not fit in shared memory.
+bool pipe_fits(int mt, int K);
+cudaError_t launch_gemv_pipe(const GemvArgs &args, int mt, bool acc_out,
+                             cudaStream_t stream);
+// Device address of the library's error word on the current device (null
+// if it cannot be resolved).
+unsigned int *device_error_word();
 // Launches the bounded-wait self-test kernel (sets bit 8 after ~10 ms).
 cudaError_t launch_selftest_wait(cudaStream_t stream);
 

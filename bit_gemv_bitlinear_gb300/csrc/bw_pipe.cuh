@@ -1,0 +1,524 @@
+// bw_pipe.cuh -- the TMA-streamed W2A8 GEMV machinery shared by the public
+// GEMV (bw_gemv_tma.cu) and the fused layer stack (bw_stack.cu).
+//
+// Source: "BitNet GPU 推理框架：从零构建 W2A8 的 2-bit 大模型 CUDA GEMV 内核",
+// §5.2 (2-bit decode), §5.3 (dp4a dot product, shuffle reduction, scale
+// epilogue).  The kernel template streams the packed weights; what feeds it
+// (the int8 activations and their scales) and what it writes (bf16 outputs,
+// int32 accumulators, or a residual update) are policies:
+//
+//   Prologue policy, after griddepcontrol.wait, called by every thread:
+//     template <int MT> __device__ void stage(int8_t *xs, uint32_t xrow,
+//         int chunks, float *s_sm, float *red, int (&part)[MT]) const;
+//   stages MT int8 activation rows at xs + m xrow (zero from K up to
+//   64 chunks), their scales in s_sm[m], and returns this thread's share of
+//   sum_k x[m][k] in part[m].  It may use CTA barriers (__syncthreads) and
+//   the 64 floats at `red`.
+//
+//   Epilogue policy:
+//     __device__ void stage_scales(float *ws_sm) const;   (after the wait)
+//     __device__ float prefetch(const PipeArgs &a, int g_lo, int n_g) const;
+//     template <int MT> __device__ void finish(const PipeArgs &a,
+//         const int *tot, const int (&sx)[MT], int g_lo, int n_g,
+//         const float *s_sm, const float *ws_sm, float *red,
+//         float pre) const;
+//   prefetch() runs right after the dependency wait; whatever it returns
+//   reaches finish() of the same thread as `pre` (e.g. a value of the
+//   thread's first output row, loaded early).
+//   finish() is called by every thread once the CTA's row totals are
+//   complete: the exact int32 dot product of output n = 8 G + r (G =
+//   phys_group(a, g_lo + gl)), row m, is tot[(gl MT + m) 8 + r] - sx[m].
+//   It may use CTA barriers and the 64 floats at `red`.
+#pragma once
+
+#include "bw_internal.cuh"
+
+namespace bw {
+namespace pipe {
+
+constexpr long long kWaitLimitCycles = 2000000000LL;  // about one second
+
+__device__ __forceinline__ uint32_t smem_addr(const void *p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)),
+               "r"(count)
+               : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(
+                   smem_addr(bar))
+               : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar,
+                                                      uint32_t bytes) {
+  asm volatile(
+      "mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(
+          smem_addr(bar)),
+      "r"(bytes)
+      : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t *bar,
+                                              uint32_t parity) {
+  uint32_t done;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(done)
+      : "r"(smem_addr(bar)), "r"(parity)
+      : "memory");
+  return done != 0;
+}
+
+// Wait for the phase of `parity` to complete, for at most `limit` cycles
+// (about a second by default).
+__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity,
+                                          long long limit = kWaitLimitCycles) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const long long t0 = clock64();
+  while (!mbar_try_wait(bar, parity))
+    if (clock64() - t0 > limit) return false;
+  return true;
+}
+
+__device__ __forceinline__ void bulk_copy_g2s(void *dst, const void *src,
+                                              uint32_t bytes, uint64_t *bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes "
+      "[%0], [%1], %2, [%3];" ::"r"(smem_addr(dst)),
+      "l"(src), "r"(bytes), "r"(smem_addr(bar))
+      : "memory");
+}
+
+__device__ __forceinline__ void pdl_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+__device__ __forceinline__ void pdl_trigger() {
+  asm volatile("griddepcontrol.launch_dependents;");
+}
+
+__device__ __forceinline__ int dp4a_us(uint32_t a, uint32_t b, int c) {
+  int d;
+  asm("dp4a.u32.s32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+  return d;
+}
+
+// Activations in shared memory: row m, chunk j (64 int8 values) at byte
+// m xrow + 64 j, zero beyond K.
+__host__ __device__ inline uint32_t xs_row_bytes(int chunks) {
+  return uint32_t(chunks) * 64u;
+}
+
+// Products of one chunk: 16 bytes of packed codes (row r, 64 weights) at
+// wp against the 64 activations of each row m at xp + m xrow.
+template <int MT>
+__device__ __forceinline__ void dot_chunk(const uint8_t *wp, const int8_t *xp,
+                                          uint32_t xrow, int (&acc)[MT][4]) {
+  const uint4 wv = *reinterpret_cast<const uint4 *>(wp);
+  const uint32_t wd[4] = {wv.x, wv.y, wv.z, wv.w};
+#pragma unroll
+  for (int t = 0; t < 4; ++t) {
+    const uint32_t c0w = wd[t] & 0x03030303u;
+    const uint32_t c1w = wd[t] & 0x0c0c0c0cu;
+    const uint32_t c2w = wd[t] & 0x30303030u;
+    const uint32_t c3w = wd[t] & 0xc0c0c0c0u;
+#pragma unroll
+    for (int m = 0; m < MT; ++m) {
+      // activation words 4t..4t+3 of the chunk: k = 64j + 16t + 4i + b
+      const uint4 xv = *reinterpret_cast<const uint4 *>(xp + m * xrow + 16 * t);
+      acc[m][0] = dp4a_us(c0w, xv.x, acc[m][0]);
+      acc[m][1] = dp4a_us(c1w, xv.y, acc[m][1]);
+      acc[m][2] = dp4a_us(c2w, xv.z, acc[m][2]);
+      acc[m][3] = dp4a_us(c3w, xv.w, acc[m][3]);
+    }
+  }
+}
+
+// Dot products of `chunks` consecutive chunks of one row group held in
+// shared memory at wbase, the first being chunk c0 of the row: lane (q, r)
+// takes chunks 4 pq + q of row r.  acc[m][i] collects slot i (codes scaled
+// by 4^i) against activation row m.  Two pointers advance by constants;
+// only the last, partial quad is predicated.
+template <int MT>
+__device__ __forceinline__ void dot_row_group(const uint8_t *wbase,
+                                              const int8_t *xs, uint32_t xrow,
+                                              int c0, int chunks, int q,
+                                              int r, int (&acc)[MT][4]) {
+  const uint8_t *wp = wbase + q * kGroupChunkBytes + r * kChunkBytes;
+  const int8_t *xp = xs + (c0 + q) * kChunkWeights;
+  const int quads = chunks >> 2;
+#pragma unroll 2
+  for (int pq = 0; pq < quads; ++pq) {
+    dot_chunk<MT>(wp, xp, xrow, acc);
+    wp += 4 * kGroupChunkBytes;
+    xp += 4 * kChunkWeights;
+  }
+  if (q < (chunks & 3)) dot_chunk<MT>(wp, xp, xrow, acc);
+}
+
+// Remove the slot factors: (((a3/4 + a2)/4 + a1)/4 + a0, exact because a_i is
+// a multiple of 4^i; then sum the 4 chunk lanes of the row.
+__device__ __forceinline__ int fold_row(const int (&a)[4]) {
+  int v = ((((a[3] >> 2) + a[2]) >> 2) + a[1]) >> 2;
+  v += a[0];
+  v += __shfl_xor_sync(0xffffffffu, v, 8);
+  v += __shfl_xor_sync(0xffffffffu, v, 16);
+  return v;
+}
+
+// ---------------------------------------------------------------------------
+// Balanced per-warp pipelines (pipe mode).
+//
+// CTA b owns the k consecutive row groups b k .. b k + k - 1 (the last CTA
+// may own fewer); its 8 warps split the CTA's k C chunks into 8 contiguous,
+// equal runs.  A warp walks its run in pieces of at most `slot_chunks`
+// chunks that never cross a row-group boundary; each piece is one bulk copy
+// into the next slot of the warp's own ring of `slots` slots.  Lane 0 of the
+// warp issues the copies: the first `slots` pieces before
+// griddepcontrol.wait, then piece i + slots into the slot of piece i as soon
+// as the warp has read it, so each warp keeps slots - 1 pieces in flight
+// whatever the other warps do.  When a piece ends a row group or the run, the
+// warp folds its partial sums and adds them (int32, exact in any order) to
+// the CTA's row totals in shared memory; one epilogue per CTA then scales
+// and stores the k * 8 rows.  Every warp has the same amount of work and
+// every CTA but the last the same number of groups, so no tail of the grid
+// runs on a few warps with few bytes in flight.
+struct PipeLayout {
+  uint32_t ring, xs, sums, red, tot, bars, total;
+};
+
+// sums: [MT] activation scales s, [BW_MAX_WS] weight scales (as fp32),
+// [warps][MT] per-warp activation sums; red: 64 floats of prologue
+// reduction scratch; tot: [k][MT][8] row totals.
+__host__ __device__ inline PipeLayout pipe_layout(int mt, int chunks,
+                                                  int slot_chunks, int slots,
+                                                  int warps, int k) {
+  PipeLayout l;
+  l.ring = 0;
+  l.xs = uint32_t(warps * slots * slot_chunks) * kGroupChunkBytes;
+  l.sums = l.xs + uint32_t(mt) * xs_row_bytes(chunks);
+  const uint32_t sums_bytes = uint32_t((mt + BW_MAX_WS + warps * mt) * 4);
+  l.red = (l.sums + sums_bytes + 15) / 16 * 16;
+  l.tot = l.red + 64 * 4;
+  l.bars = l.tot + uint32_t(k * mt * 8 * 4);
+  l.total = l.bars + uint32_t(warps * slots * 8);
+  return l;
+}
+
+constexpr int kPipeWarps = 8;
+constexpr int kPipeMaxGroupsPerCta = 256;
+constexpr int kPipeMinGroupsPerCta = 2;  // fewer CTAs staging x for small N
+
+// Orders this warp's earlier generic-proxy reads of a slot before the
+// bulk copy (async proxy) that overwrites it.
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// Position in a warp's run: chunk u of the CTA's range = chunk c of the
+// CTA's row group g.
+struct RunCursor {
+  int u, g, c;
+  __device__ __forceinline__ int piece(int ks, int chunks, int end) const {
+    return min(min(ks, chunks - c), end - u);
+  }
+  __device__ __forceinline__ void advance(int len, int chunks) {
+    u += len;
+    c += len;
+    if (c == chunks) {
+      c = 0;
+      ++g;
+    }
+  }
+};
+
+// What the kernel streams and how it is split (see launch_pipe).
+struct PipeArgs {
+  const uint8_t *w;     // packed weights, device layout
+  int N;                // output rows
+  int chunks;           // C = ceil(K / 64)
+  int n_groups;         // ceil(N / 8)
+  int slot_chunks;      // chunks per piece (at most)
+  int slots;            // ring slots per warp
+  int groups_per_cta;   // k
+  int pair_half;        // 0, or H: group order 0, H, 1, H + 1, ... (2H groups)
+  unsigned int *err;    // device error word (time-out bits)
+};
+
+// Physical row group of the g-th group in streaming order.  With pair_half
+// H the two halves of the rows are interleaved group by group, so that a
+// CTA owning an even number of consecutive groups holds matching groups of
+// both halves (e.g. gate and up rows of the same features).
+__host__ __device__ __forceinline__ int phys_group(const PipeArgs &a, int g) {
+  return a.pair_half ? (g >> 1) + (g & 1) * a.pair_half : g;
+}
+
+// Sum and maximum over the CTA's 8 warps in one exchange (fixed shuffle
+// tree, then the 8 warp values in order); every thread gets both results.
+// `red` holds 64 floats.
+__device__ __forceinline__ void cta_sum_max(float &sum, float &mx,
+                                            float *red) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    sum += __shfl_xor_sync(0xffffffffu, sum, o);
+    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+  }
+  __syncthreads();
+  if ((threadIdx.x & 31) == 0) {
+    red[threadIdx.x >> 5] = sum;
+    red[32 + (threadIdx.x >> 5)] = mx;
+  }
+  __syncthreads();
+  sum = 0.0f;
+  mx = 0.0f;
+#pragma unroll
+  for (int w = 0; w < kPipeWarps; ++w) {
+    sum += red[w];
+    mx = fmaxf(mx, red[32 + w]);
+  }
+}
+
+// Deterministic reductions over the CTA's 8 warps (fixed shuffle tree, then
+// the 8 warp values in order); `red` holds 32 floats; every thread returns
+// the same value.
+__device__ __forceinline__ float cta_sum(float v, float *red) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  __syncthreads();
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = v;
+  __syncthreads();
+  float t = 0.0f;
+#pragma unroll
+  for (int w = 0; w < kPipeWarps; ++w) t += red[w];
+  return t;
+}
+
+__device__ __forceinline__ float cta_max(float v, float *red) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1)
+    v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  __syncthreads();
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = v;
+  __syncthreads();
+  float t = 0.0f;
+#pragma unroll
+  for (int w = 0; w < kPipeWarps; ++w) t = fmaxf(t, red[w]);
+  return t;
+}
+
+template <int MT, class Pro, class Epi>
+__global__ void __launch_bounds__(kPipeWarps * 32)
+pipe_gemv_kernel(const PipeArgs a, const Pro pro, const Epi epi) {
+  extern __shared__ __align__(128) uint8_t smem[];
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int KS = a.slot_chunks;
+  const int R = a.slots;
+  const int C = a.chunks;
+  const int k = a.groups_per_cta;
+  const uint32_t slot_bytes = uint32_t(KS) * kGroupChunkBytes;
+  const uint32_t xrow = xs_row_bytes(C);
+  const PipeLayout L = pipe_layout(MT, C, KS, R, kPipeWarps, k);
+  uint8_t *ring = smem + L.ring + size_t(warp) * R * slot_bytes;
+  int8_t *xs = reinterpret_cast<int8_t *>(smem + L.xs);
+  float *s_sm = reinterpret_cast<float *>(smem + L.sums);
+  float *ws_sm = s_sm + MT;
+  int *sx_part = reinterpret_cast<int *>(ws_sm + BW_MAX_WS);  // [warps][MT]
+  float *red = reinterpret_cast<float *>(smem + L.red);
+  int *tot = reinterpret_cast<int *>(smem + L.tot);  // [k][MT][8]
+  uint64_t *full = reinterpret_cast<uint64_t *>(smem + L.bars) + warp * R;
+
+  const int g_lo = int(blockIdx.x) * k;
+  const int n_g = max(0, min(k, a.n_groups - g_lo));
+  const int U = n_g * C;  // chunks of this CTA (k C <= 256 * 1024)
+  const int run_lo = U * warp / kPipeWarps;
+  const int run_hi = U * (warp + 1) / kPipeWarps;
+
+  RunCursor iss;  // next piece to copy (lane 0)
+  iss.u = run_lo;
+  iss.g = run_lo / C;
+  iss.c = run_lo - iss.g * C;
+  RunCursor cur = iss;  // next piece to consume (whole warp)
+  int issued = 0;
+  auto issue_next = [&](int slot) {
+    const int len = iss.piece(KS, C, run_hi);
+    const uint32_t bytes = uint32_t(len) * kGroupChunkBytes;
+    mbar_arrive_expect_tx(&full[slot], bytes);
+    const size_t pg = size_t(phys_group(a, g_lo + iss.g));
+    bulk_copy_g2s(ring + size_t(slot) * slot_bytes,
+                  a.w + (pg * C + iss.c) * kGroupChunkBytes, bytes,
+                  &full[slot]);
+    iss.advance(len, C);
+    ++issued;
+  };
+  if (lane == 0) {
+    for (int s = 0; s < R; ++s) mbar_init(&full[s], 1);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    // The weights are static once written (bw_repack synchronises its
+    // stream): the first pieces are requested before the dependency wait.
+    for (int s = 0; s < R && iss.u < run_hi; ++s) issue_next(s);
+  }
+  for (int t = threadIdx.x; t < n_g * MT * 8; t += blockDim.x) tot[t] = 0;
+  pdl_wait();
+
+  epi.stage_scales(ws_sm);
+  const float pre = epi.prefetch(a, g_lo, n_g);
+  int part[MT];
+  pro.template stage<MT>(xs, xrow, C, s_sm, red, part);
+#pragma unroll
+  for (int m = 0; m < MT; ++m) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1)
+      part[m] += __shfl_xor_sync(0xffffffffu, part[m], o);
+    if (lane == 0) sx_part[warp * MT + m] = part[m];
+  }
+  __syncthreads();  // activations staged, totals zeroed, barriers set up
+  pdl_trigger();    // dependents may start their prologue on free SM slots
+
+  const int q = lane >> 3;  // chunk residue (relative to the piece) mod 4
+  const int r = lane & 7;   // row inside the group
+  int acc[MT][4];
+#pragma unroll
+  for (int m = 0; m < MT; ++m)
+#pragma unroll
+    for (int t = 0; t < 4; ++t) acc[m][t] = 0;
+  bool ok = true;
+  int consumed = 0, slot = 0;
+  uint32_t phase = 0;
+  while (cur.u < run_hi) {
+    // warp-uniform outcome before any full-mask shuffle below
+    if (!__all_sync(0xffffffffu, mbar_wait(&full[slot], phase))) {
+      ok = false;
+      break;
+    }
+    const int len = cur.piece(KS, C, run_hi);
+    dot_row_group<MT>(ring + size_t(slot) * slot_bytes, xs, xrow, cur.c, len,
+                      q, r, acc);
+    __syncwarp();
+    if (lane == 0 && iss.u < run_hi) {  // piece consumed + R: this slot
+      fence_proxy_async_smem();
+      issue_next(slot);
+    }
+    const int g = cur.g;
+    cur.advance(len, C);
+    ++consumed;
+    if (cur.c == 0 || cur.u == run_hi) {  // row group or run finished
+#pragma unroll
+      for (int m = 0; m < MT; ++m) {
+        const int v = fold_row(acc[m]);
+        if (q == 0) atomicAdd(&tot[(g * MT + m) * 8 + r], v);
+#pragma unroll
+        for (int t = 0; t < 4; ++t) acc[m][t] = 0;
+      }
+    }
+    if (++slot == R) {
+      slot = 0;
+      phase ^= 1u;
+    }
+  }
+  if (!ok && lane == 0) {
+    atomicOr(a.err, 4u);
+    // copies still in flight land before the CTA may leave
+    for (int i = consumed; i < issued; ++i)
+      if (!mbar_wait(&full[i % R], uint32_t(i / R) & 1u)) atomicOr(a.err, 2u);
+  }
+  __syncthreads();  // every partial sum is in `tot`
+
+  int sx[MT];  // sum_k x[m][k] over the whole row
+#pragma unroll
+  for (int m = 0; m < MT; ++m) {
+    sx[m] = 0;
+#pragma unroll
+    for (int w = 0; w < kPipeWarps; ++w) sx[m] += sx_part[w * MT + m];
+  }
+  epi.template finish<MT>(a, tot, sx, g_lo, n_g, s_sm, ws_sm, red, pre);
+}
+
+// Sets the opt-in shared-memory size once per device and returns how many
+// CTAs of `kernel` are resident on the device at once (at least one).
+template <class Kernel>
+cudaError_t resident_ctas(Kernel kernel, bool *configured, int threads,
+                          uint32_t smem, int64_t *resident) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  if (!configured[dev]) {
+    e = cudaFuncSetAttribute(kernel,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             227 * 1024);
+    if (e != cudaSuccess) return e;
+    configured[dev] = true;
+  }
+  int per_sm = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, threads,
+                                                    smem) != cudaSuccess ||
+      per_sm < 1)
+    per_sm = 1;
+  *resident = int64_t(per_sm) * device_sm_count();
+  return cudaSuccess;
+}
+
+// Pieces of up to 4 KB, two slots per warp: 64 KB of ring per 8-warp CTA,
+// about three CTAs per SM for K <= 8192.
+constexpr int kPipeSlotChunks = 32;
+constexpr int kPipeSlots = 2;
+
+// Shared memory of a launch with k groups per CTA; a launch fits while this
+// is at most 227 KB for k = kPipeMaxGroupsPerCta.
+inline uint32_t pipe_smem_bytes(int mt, int chunks, int slot_chunks, int k) {
+  return pipe_layout(mt, chunks, slot_chunks, kPipeSlots, kPipeWarps, k).total;
+}
+
+// Launches the pipe kernel with programmatic dependent launch: k groups per
+// CTA with k as small as the resident CTAs allow (at least
+// kPipeMinGroupsPerCta, at most kPipeMaxGroupsPerCta; beyond that the grid
+// runs in waves; even with pair_half), and pieces no longer than a warp's
+// run.  Fills in the split fields of `a`; *grid_out (if set) receives the
+// number of CTAs.
+template <int MT, class Pro, class Epi>
+cudaError_t launch_pipe(PipeArgs a, const Pro &pro, const Epi &epi,
+                        cudaStream_t stream, int *grid_out = nullptr) {
+  static bool configured[64];
+  auto kernel = pipe_gemv_kernel<MT, Pro, Epi>;
+  a.slot_chunks = kPipeSlotChunks;
+  a.slots = kPipeSlots;
+  // k from the residency at k = 1, then once more at that k (the row
+  // totals grow with k).
+  int64_t k = 1, resident = 0;
+  for (int pass = 0; pass < 2; ++pass) {
+    cudaError_t e = resident_ctas(
+        kernel, configured, kPipeWarps * 32,
+        pipe_smem_bytes(MT, a.chunks, a.slot_chunks, int(k)), &resident);
+    if (e != cudaSuccess) return e;
+    k = (a.n_groups + resident - 1) / resident;
+    if (k > kPipeMaxGroupsPerCta) k = kPipeMaxGroupsPerCta;
+    if (k < kPipeMinGroupsPerCta) k = kPipeMinGroupsPerCta;
+    if (a.pair_half) k += k & 1;  // whole pairs per CTA
+  }
+  const int64_t grid = (a.n_groups + k - 1) / k;
+  const int64_t run = (k * a.chunks + kPipeWarps - 1) / kPipeWarps;
+  if (run < a.slot_chunks) a.slot_chunks = int(run < 1 ? 1 : run);
+  a.groups_per_cta = int(k);
+  if (grid_out) *grid_out = int(grid);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(unsigned(grid > 0 ? grid : 1));
+  cfg.blockDim = dim3(kPipeWarps * 32);
+  cfg.dynamicSmemBytes = pipe_smem_bytes(MT, a.chunks, a.slot_chunks, int(k));
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, a, pro, epi);
+}
+
+}  // namespace pipe
+}  // namespace bw

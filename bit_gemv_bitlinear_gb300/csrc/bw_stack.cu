@@ -9,180 +9,407 @@
 // quantisation before every W2A8 GEMV), §六 item 1 (decode replayed from a
 // CUDA graph).
 //
-// One layer, M = 1:
-//   h <- h + down(prev layer)            (fused into the first glue kernel)
+// One layer, M = 1 (h is the fp32 residual stream):
 //   (q, s) <- quant(rmsnorm(h) * g_attn)              -> qkv = W2A8(wqkv)
 //   (q, s) <- quant(rmsnorm(attn(qkv)) * g_attn_sub)  -> o   = W2A8(wo)
-//   h <- h + o; (q, s) <- quant(rmsnorm(h) * g_ffn)   -> gu  = W2A8(w13)
+//   h <- h + o
+//   (q, s) <- quant(rmsnorm(h) * g_ffn)               -> gu  = W2A8(w13)
 //   (q, s) <- quant(rmsnorm(relu(gate)^2 up) * g_sub) -> down = W2A8(w2)
+//   h <- h + down
 // attn() is attention over a one-token context: the softmax of one score is
 // 1, so query head h returns the value vector of KV head h / (heads / kv).
 //
-// Each glue step is one single-CTA kernel (1024 threads, up to 8 values
-// per thread kept in registers between the two reductions); the GEMVs are
-// the TMA-streamed kernels.  All launches use programmatic dependent
-// launch, and one decode step is captured once as a CUDA graph.
+// Each GEMV is ONE launch of the pipe GEMV kernel (bw_pipe.cuh); the glue
+// is split between launches so that every value is computed once:
+//  * the epilogue of each launch writes, besides its bf16 output, the fp32
+//    values the NEXT RMSNorm reads (the attention output, h after the
+//    residual add, or the gated product; the wo and w2 epilogues add their
+//    outputs into h, each element once) and, per CTA, the partial sum of
+//    their squares and the partial max of |value * gain|;
+//  * the prologue of the next launch reduces those partials (in the same
+//    fixed order in every CTA) to the RMS factor and the absmax scale, and
+//    quantises the values into its shared-memory activations.
+// w13 streams its row groups in (gate j, up j) pairs so that the CTA that
+// computes gate[f] also holds up[f].  The first GEMV of a step normalises h
+// itself (no earlier launch).  Four launches per layer, all with
+// programmatic dependent launch; one decode step is captured once as a
+// CUDA graph.
 #include <cstdlib>
 #include <new>
 #include <vector>
 
-#include "bw_internal.cuh"
+#include "bw_pipe.cuh"
 
 namespace bw {
 namespace {
 
-constexpr int kGlueThreads = 1024;
-constexpr int kMaxGlueK = 8 * kGlueThreads;
+using namespace pipe;
 
-__device__ __forceinline__ void pdl_enter() {
-  asm volatile("griddepcontrol.launch_dependents;");
-  asm volatile("griddepcontrol.wait;" ::: "memory");
-}
-
-// Deterministic block reductions (fixed shuffle tree, then warp 0).
-__device__ __forceinline__ float block_sum(float v, float *scratch) {
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-  __syncthreads();
-  if ((threadIdx.x & 31) == 0) scratch[threadIdx.x >> 5] = v;
-  __syncthreads();
-  float t = 0.0f;
-  for (int w = 0; w < int(blockDim.x >> 5); ++w) t += scratch[w];
-  return t;
-}
-
-__device__ __forceinline__ float block_max(float v, float *scratch) {
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1)
-    v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
-  __syncthreads();
-  if ((threadIdx.x & 31) == 0) scratch[threadIdx.x >> 5] = v;
-  __syncthreads();
-  float t = 0.0f;
-  for (int w = 0; w < int(blockDim.x >> 5); ++w) t = fmaxf(t, scratch[w]);
-  return t;
-}
+constexpr int kPrologueThreads = kPipeWarps * 32;
+constexpr int kMaxGlueK = 32 * kPrologueThreads;  // 8192: V <= 32 per thread
 
 __device__ __forceinline__ int8_t quant1(float x, float scale) {
   return static_cast<int8_t>(
       static_cast<int>(fminf(fmaxf(rintf(x * scale), -128.0f), 127.0f)));
 }
 
-// Element loaders of the three glue steps.
-struct ResidualLoad {  // x[k] (+ bf16 add[k]), fp32
-  const float *x;
-  const __nv_bfloat16 *add;
-  __device__ float operator()(int k) const {
-    float v = x[k];
-    if (add) v = v + __bfloat162float(add[k]);
-    return v;
-  }
-};
+// Prologue of the first GEMV of a step (h comes from the caller, so no
+// earlier launch has its statistics): v = h[k] for k < K, then
+//   n = (v * (1 / sqrt(mean(v^2) + eps))) * gamma,
+//   s = 127 / max(absmax n, 1e-5),  q = clamp(rint(n * s), -128, 127),
+// all in fp32 with fixed-order CTA reductions.  CTA 0 copies q to trace_q
+// and s to trace_s, each when set.
+template <int V>
+struct NormQuantH {
+  const float *h;
+  const float *gamma;
+  int K;
+  float eps;
+  int8_t *trace_q;
+  float *trace_s;
 
-struct AttnLoad {  // value head of query head k / hd
-  const __nv_bfloat16 *qkv;
-  int v_off, hd, group;
-  __device__ float operator()(int k) const {
-    const int h = k / hd;
-    return __bfloat162float(qkv[v_off + (h / group) * hd + (k - h * hd)]);
-  }
-};
-
-struct Relu2Load {  // relu(gate)^2 * up, exact in fp32 for bf16 inputs
-  const __nv_bfloat16 *gu;
-  int F;
-  __device__ float operator()(int k) const {
-    const float g = __bfloat162float(gu[k]);
-    const float u = __bfloat162float(gu[F + k]);
-    const float r = g > 0.0f ? g : 0.0f;
-    return r * r * u;
-  }
-};
-
-// v = load(k); optionally h_out[k] = v; then
-// n = (v * (1 / sqrt(mean(v^2) + eps))) * gamma, s = 127 / max(absmax n, 1e-5),
-// q = clamp(rint(n * s), -128, 127).  One CTA, fp32.
-template <class Load, int V>
-__global__ void __launch_bounds__(kGlueThreads)
-norm_quant_kernel(Load load, const float *__restrict__ gamma, int K,
-                  float eps, float *h_out, int8_t *__restrict__ q,
-                  float *__restrict__ s) {
-  __shared__ float scratch[32];
-  pdl_enter();
-  float v[V];
-  float ss = 0.0f;
-#pragma unroll
-  for (int i = 0; i < V; ++i) {
-    const int k = threadIdx.x + i * kGlueThreads;
-    v[i] = k < K ? load(k) : 0.0f;
-    ss += v[i] * v[i];
-  }
-  if (h_out) {
+  template <int MT>
+  __device__ __forceinline__ void stage(int8_t *xs, uint32_t xrow, int chunks,
+                                        float *s_sm, float *red,
+                                        int (&part)[MT]) const {
+    static_assert(MT == 1, "the stack runs one token per step");
+    (void)xrow;
+    const int tid = threadIdx.x;
+    float v[V], gm[V];
 #pragma unroll
     for (int i = 0; i < V; ++i) {
-      const int k = threadIdx.x + i * kGlueThreads;
-      if (k < K) h_out[k] = v[i];
+      const int k = tid + i * kPrologueThreads;
+      v[i] = k < K ? h[k] : 0.0f;
+      gm[i] = k < K ? gamma[k] : 0.0f;
     }
-  }
-  ss = block_sum(ss, scratch);
-  const float r = 1.0f / sqrtf(ss / static_cast<float>(K) + eps);
-  float amax = 0.0f;
+    float ss = 0.0f, unused = 0.0f;
 #pragma unroll
-  for (int i = 0; i < V; ++i) {
-    const int k = threadIdx.x + i * kGlueThreads;
-    if (k < K) {
-      v[i] = (v[i] * r) * gamma[k];
+    for (int i = 0; i < V; ++i) ss += v[i] * v[i];
+    cta_sum_max(ss, unused, red);
+    const float r = 1.0f / sqrtf(ss / static_cast<float>(K) + eps);
+    float amax = 0.0f;
+#pragma unroll
+    for (int i = 0; i < V; ++i) {
+      v[i] = (v[i] * r) * gm[i];
       amax = fmaxf(amax, fabsf(v[i]));
     }
-  }
-  amax = block_max(amax, scratch);
-  const float scale = 127.0f / fmaxf(amax, 1e-5f);
-  if (threadIdx.x == 0) *s = scale;
+    float unused2 = 0.0f;
+    cta_sum_max(unused2, amax, red);
+    const float scale = 127.0f / fmaxf(amax, 1e-5f);
+    if (tid == 0) s_sm[0] = scale;
+    const bool tr = trace_q && blockIdx.x == 0;
+    int p = 0;
 #pragma unroll
-  for (int i = 0; i < V; ++i) {
-    const int k = threadIdx.x + i * kGlueThreads;
-    if (k < K) q[k] = quant1(v[i], scale);
+    for (int i = 0; i < V; ++i) {
+      const int k = tid + i * kPrologueThreads;
+      if (k < K) {
+        const int8_t qv = quant1(v[i], scale);
+        xs[k] = qv;
+        p += qv;
+        if (tr) trace_q[k] = qv;
+      }
+    }
+    for (int k = K + tid; k < chunks * kChunkWeights; k += kPrologueThreads)
+      xs[k] = 0;
+    if (trace_s && blockIdx.x == 0 && tid == 0) *trace_s = scale;
+    part[0] = p;
   }
+};
+
+// Prologue of every other GEMV: the previous launch wrote the fp32 values
+// v[K] to normalise and, per CTA, the partial statistics (sum of v^2, max
+// of |v * gamma|) over the values it wrote.  Each warp reduces the P
+// partials in the same fixed order, so every CTA gets the same
+//   r = 1 / sqrt(sum / K + eps),  s = 127 / max(max * r, 1e-5),
+// and quantises q = clamp(rint(((v * gamma) * r) * s)).  Rounding is
+// monotone, so max * r is exactly the largest |(v * gamma) * r|.  Four
+// values per thread and step (16-byte loads, one 32-bit store of codes).
+template <int V4>
+struct NormQuantP {
+  const float *src;     // v [K], 16-byte aligned
+  const float *gamma;   // [K], 16-byte aligned
+  const float2 *part;   // [P]
+  int P, K;
+  float eps;
+  int8_t *trace_q;
+  float *trace_s;
+
+  template <int MT>
+  __device__ __forceinline__ void stage(int8_t *xs, uint32_t xrow, int chunks,
+                                        float *s_sm, float *red,
+                                        int (&part_out)[MT]) const {
+    static_assert(MT == 1, "the stack runs one token per step");
+    (void)xrow;
+    (void)red;
+    const int tid = threadIdx.x, lane = tid & 31;
+    const int groups = K >> 2;  // K is a multiple of 4
+    float4 v[V4], gm[V4];
+#pragma unroll
+    for (int i = 0; i < V4; ++i) {
+      const int g = tid + i * kPrologueThreads;
+      if (g < groups) {
+        v[i] = __ldg(reinterpret_cast<const float4 *>(src) + g);
+        gm[i] = __ldg(reinterpret_cast<const float4 *>(gamma) + g);
+      }
+    }
+    float ss = 0.0f, mx = 0.0f;
+    for (int i = lane; i < P; i += 32) {
+      const float2 pv = part[i];
+      ss += pv.x;
+      mx = fmaxf(mx, pv.y);
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      ss += __shfl_xor_sync(0xffffffffu, ss, o);
+      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+    }
+    const float r = 1.0f / sqrtf(ss / static_cast<float>(K) + eps);
+    const float scale = 127.0f / fmaxf(__fmul_rn(mx, r), 1e-5f);
+    if (tid == 0) s_sm[0] = scale;
+    const bool tr = trace_q && blockIdx.x == 0;
+    uint32_t *xw = reinterpret_cast<uint32_t *>(xs);
+    int p = 0;
+#pragma unroll
+    for (int i = 0; i < V4; ++i) {
+      const int g = tid + i * kPrologueThreads;
+      if (g < groups) {
+        const float e[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
+        const float f[4] = {gm[i].x, gm[i].y, gm[i].z, gm[i].w};
+        uint32_t word = 0;
+#pragma unroll
+        for (int b = 0; b < 4; ++b) {
+          const int8_t qv =
+              quant1(__fmul_rn(__fmul_rn(e[b], f[b]), r), scale);
+          word |= uint32_t(uint8_t(qv)) << (8 * b);
+          if (tr) trace_q[4 * g + b] = qv;
+        }
+        xw[g] = word;
+        p = dp4a_us(0x01010101u, word, p);
+      }
+    }
+    for (int w = groups + tid; w < chunks * (kChunkWeights / 4);
+         w += kPrologueThreads)
+      xw[w] = 0u;
+    if (trace_s && blockIdx.x == 0 && tid == 0) *trace_s = scale;
+    part_out[0] = p;
+  }
+};
+
+// Scaled bf16 output of one row: bf16((acc / s) * ws), IEEE fp32.
+__device__ __forceinline__ __nv_bfloat16 scaled_bf16(int total, float s,
+                                                     float ws) {
+  return __float2bfloat16_rn((static_cast<float>(total) / s) * ws);
 }
 
-// h += down (the residual of the last layer).
-__global__ void __launch_bounds__(kGlueThreads)
-residual_kernel(float *h, const __nv_bfloat16 *down, int n) {
-  pdl_enter();
-  for (int k = threadIdx.x; k < n; k += blockDim.x)
-    h[k] = h[k] + __bfloat162float(down[k]);
+// Writes this CTA's partial statistics (every thread calls it).
+__device__ __forceinline__ void write_partials(float2 *out, float ss, float mx,
+                                               float *red) {
+  if (!out) return;
+  cta_sum_max(ss, mx, red);
+  if (threadIdx.x == 0) out[blockIdx.x] = make_float2(ss, mx);
 }
 
-cudaLaunchConfig_t glue_config(cudaStream_t stream, cudaLaunchAttribute *attr) {
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(1);
-  cfg.blockDim = dim3(kGlueThreads);
-  cfg.stream = stream;
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  return cfg;
+// Epilogue of wqkv: qkv[n] (bf16, scales q | k | v), and for the value rows
+// the one-token attention output attn[h hd + d] = v[kv hd + d] for the
+// `group` query heads h of KV head kv (fp32), with the partial statistics
+// of attn against the attn_sub_norm gains.
+struct EpiQKV {
+  __nv_bfloat16 *qkv;
+  float *attn;
+  const __nv_bfloat16 *ws;
+  WsSegments seg;
+  int v_off, hd, group;
+  const float *gamma_next;
+  float2 *part_out;
+
+  __device__ __forceinline__ void stage_scales(float *ws_sm) const {
+    if (int(threadIdx.x) < seg.n_ws)
+      ws_sm[threadIdx.x] = __bfloat162float(ws[threadIdx.x]);
+  }
+  __device__ __forceinline__ float prefetch(const PipeArgs &, int,
+                                            int) const {
+    return 0.0f;
+  }
+  template <int MT>
+  __device__ __forceinline__ void finish(const PipeArgs &a, const int *tot,
+                                         const int (&sx)[MT], int g_lo,
+                                         int n_g, const float *s_sm,
+                                         const float *ws_sm, float *red,
+                                         float) const {
+    float ss = 0.0f, mx = 0.0f;
+    for (int t = threadIdx.x; t < n_g * 8; t += blockDim.x) {
+      const int gl = t >> 3, rr = t & 7;
+      const int n = (g_lo + gl) * kGroupRows + rr;
+      if (n >= a.N) continue;
+      int sg = 0;
+#pragma unroll
+      for (int i = 1; i < BW_MAX_WS; ++i)
+        if (i < seg.n_ws && n >= seg.bounds[i]) sg = i;
+      const __nv_bfloat16 yv =
+          scaled_bf16(tot[gl * 8 + rr] - sx[0], s_sm[0], ws_sm[sg]);
+      qkv[n] = yv;
+      if (n >= v_off) {
+        const int j = n - v_off;
+        const int kv = j / hd, d = j - kv * hd;
+        const float yf = __bfloat162float(yv);
+        for (int h = kv * group; h < (kv + 1) * group; ++h) {
+          const int pos = h * hd + d;
+          attn[pos] = yf;
+          ss += yf * yf;
+          mx = fmaxf(mx, fabsf(__fmul_rn(yf, gamma_next[pos])));
+        }
+      }
+    }
+    write_partials(part_out, ss, mx, red);
+  }
+};
+
+// Epilogue of wo and w2: y[n] (bf16, one scale) and the residual update
+// h[n] += y[n] (fp32), with the partial statistics of the new h against the
+// gains of the next RMSNorm (none after the last layer).  h[n] of the
+// thread's first row is loaded right after the dependency wait.
+struct EpiResid {
+  __nv_bfloat16 *y;
+  float *h;
+  const __nv_bfloat16 *ws;
+  const float *gamma_next;  // or null
+  float2 *part_out;         // or null
+
+  __device__ __forceinline__ void stage_scales(float *ws_sm) const {
+    if (threadIdx.x == 0) ws_sm[0] = __bfloat162float(ws[0]);
+  }
+  __device__ __forceinline__ float prefetch(const PipeArgs &a, int g_lo,
+                                            int n_g) const {
+    const int t = threadIdx.x;
+    const int n = (g_lo + (t >> 3)) * kGroupRows + (t & 7);
+    return (t < n_g * 8 && n < a.N) ? h[n] : 0.0f;
+  }
+  template <int MT>
+  __device__ __forceinline__ void finish(const PipeArgs &a, const int *tot,
+                                         const int (&sx)[MT], int g_lo,
+                                         int n_g, const float *s_sm,
+                                         const float *ws_sm, float *red,
+                                         float pre) const {
+    float ss = 0.0f, mx = 0.0f;
+    for (int t = threadIdx.x; t < n_g * 8; t += blockDim.x) {
+      const int gl = t >> 3, rr = t & 7;
+      const int n = (g_lo + gl) * kGroupRows + rr;
+      if (n >= a.N) continue;
+      const __nv_bfloat16 yv =
+          scaled_bf16(tot[gl * 8 + rr] - sx[0], s_sm[0], ws_sm[0]);
+      y[n] = yv;
+      const float hv = t == int(threadIdx.x) ? pre : h[n];
+      const float hn = hv + __bfloat162float(yv);
+      h[n] = hn;
+      if (gamma_next) {
+        ss += hn * hn;
+        mx = fmaxf(mx, fabsf(__fmul_rn(hn, gamma_next[n])));
+      }
+    }
+    write_partials(part_out, ss, mx, red);
+  }
+};
+
+// Epilogue of w13, streamed with paired row groups (gate group j, then up
+// group j): gu[f] and gu[F + f] (bf16, scales gate | up), and the gated
+// product g[f] = relu(gate)^2 * up (fp32, exact for bf16 inputs) with its
+// partial statistics against the ffn_sub_norm gains.  F is a multiple of 8.
+struct EpiGate {
+  __nv_bfloat16 *gu;
+  float *gated;
+  const __nv_bfloat16 *ws;
+  int F;
+  const float *gamma_next;
+  float2 *part_out;
+
+  __device__ __forceinline__ void stage_scales(float *ws_sm) const {
+    if (threadIdx.x < 2) ws_sm[threadIdx.x] = __bfloat162float(ws[threadIdx.x]);
+  }
+  __device__ __forceinline__ float prefetch(const PipeArgs &, int,
+                                            int) const {
+    return 0.0f;
+  }
+  template <int MT>
+  __device__ __forceinline__ void finish(const PipeArgs &a, const int *tot,
+                                         const int (&sx)[MT], int g_lo,
+                                         int n_g, const float *s_sm,
+                                         const float *ws_sm, float *red,
+                                         float) const {
+    (void)a;
+    float ss = 0.0f, mx = 0.0f;
+    // g_lo and n_g are even: the CTA holds whole (gate, up) pairs.
+    for (int t = threadIdx.x; t < (n_g >> 1) * 8; t += blockDim.x) {
+      const int jl = t >> 3, rr = t & 7;
+      const int f = ((g_lo >> 1) + jl) * kGroupRows + rr;
+      const __nv_bfloat16 yg =
+          scaled_bf16(tot[(2 * jl) * 8 + rr] - sx[0], s_sm[0], ws_sm[0]);
+      const __nv_bfloat16 yu =
+          scaled_bf16(tot[(2 * jl + 1) * 8 + rr] - sx[0], s_sm[0], ws_sm[1]);
+      gu[f] = yg;
+      gu[F + f] = yu;
+      const float g = __bfloat162float(yg);
+      const float r = g > 0.0f ? g : 0.0f;
+      const float v = __fmul_rn(__fmul_rn(r, r), __bfloat162float(yu));
+      gated[f] = v;
+      ss += v * v;
+      mx = fmaxf(mx, fabsf(__fmul_rn(v, gamma_next[f])));
+    }
+    write_partials(part_out, ss, mx, red);
+  }
+};
+
+// Partial statistics per launch: at most one entry per CTA; a launch has at
+// most n_groups / kPipeMinGroupsPerCta + 1 <= 1025 CTAs for N <= 16384.
+constexpr int kMaxPartials = 2048;
+
+template <class Pro, class Epi>
+cudaError_t launch_one(const uint8_t *w, int N, int K, int pair_half,
+                       const Pro &pro, const Epi &epi, cudaStream_t cs,
+                       int *grid) {
+  PipeArgs a{};
+  a.w = w;
+  a.N = N;
+  a.chunks = chunks_per_row(K);
+  a.n_groups = int(padded_rows(N) / kGroupRows);
+  a.pair_half = pair_half;
+  a.err = device_error_word();
+  if (!a.err) return cudaErrorInvalidSymbol;
+  return launch_pipe<1>(a, pro, epi, cs, grid);
 }
 
-template <class Load>
-cudaError_t launch_norm_quant(const Load &load, const float *gamma, int K,
-                              float eps, float *h_out, int8_t *q, float *s,
-                              cudaStream_t stream) {
-  cudaLaunchAttribute attr[1];
-  cudaLaunchConfig_t cfg = glue_config(stream, attr);
-  const int v = (K + kGlueThreads - 1) / kGlueThreads;
-  if (v <= 1)
-    return cudaLaunchKernelEx(&cfg, norm_quant_kernel<Load, 1>, load, gamma,
-                              K, eps, h_out, q, s);
-  if (v <= 2)
-    return cudaLaunchKernelEx(&cfg, norm_quant_kernel<Load, 2>, load, gamma,
-                              K, eps, h_out, q, s);
-  if (v <= 4)
-    return cudaLaunchKernelEx(&cfg, norm_quant_kernel<Load, 4>, load, gamma,
-                              K, eps, h_out, q, s);
-  return cudaLaunchKernelEx(&cfg, norm_quant_kernel<Load, 8>, load, gamma, K,
-                            eps, h_out, q, s);
+// First GEMV of a step: the prologue normalises h itself.
+template <class Epi>
+cudaError_t launch_first(const uint8_t *w, int N, int K, const float *h,
+                         const float *gamma, float eps, int8_t *tq, float *ts,
+                         const Epi &epi, cudaStream_t cs, int *grid) {
+  if (K <= 8 * kPrologueThreads)
+    return launch_one(w, N, K, 0, NormQuantH<8>{h, gamma, K, eps, tq, ts},
+                      epi, cs, grid);
+  return launch_one(w, N, K, 0, NormQuantH<32>{h, gamma, K, eps, tq, ts},
+                    epi, cs, grid);
+}
+
+// Every other GEMV: the prologue quantises what the previous launch wrote.
+template <class Epi>
+cudaError_t launch_next(const uint8_t *w, int N, int K, int pair_half,
+                        const float *src, const float *gamma,
+                        const float2 *part, int P, float eps, int8_t *tq,
+                        float *ts, const Epi &epi, cudaStream_t cs,
+                        int *grid) {
+  if (K <= 8 * kPrologueThreads)
+    return launch_one(w, N, K, pair_half,
+                      NormQuantP<2>{src, gamma, part, P, K, eps, tq, ts}, epi,
+                      cs, grid);
+  return launch_one(w, N, K, pair_half,
+                    NormQuantP<8>{src, gamma, part, P, K, eps, tq, ts}, epi,
+                    cs, grid);
+}
+
+WsSegments segments(const int *bounds, int n) {
+  WsSegments sg{};
+  sg.n_ws = n;
+  for (int i = 0; i <= n; ++i) sg.bounds[i] = bounds[i];
+  return sg;
 }
 
 }  // namespace
@@ -197,10 +424,10 @@ struct bw_stack {
   std::vector<const float *> gammas;
   int hd, qkv_n, v_off, group;
   // device scratch
-  float *h;
-  int8_t *q;
-  float *s;
-  __nv_bfloat16 *qkv, *o, *gu, *dn;
+  float *h;                           // residual stream [dim]
+  __nv_bfloat16 *qkv, *o, *gu, *dn;   // GEMV outputs
+  float *attn, *gated;                // inputs of attn_sub_norm, ffn_sub_norm
+  float2 *part;                       // [2][kMaxPartials] partial statistics
   cudaGraphExec_t exec;
   bool have_graph;
 };
@@ -228,71 +455,74 @@ cudaError_t trace_copy(void *dst, const void *src, size_t bytes,
 #define BW_TRY_CUDA(expr) BW_TRY(cuda_err(expr))
 
 // One decode step over all layers on fixed buffers: st->h holds the step's
-// input on entry and its output on exit.
+// input on entry and its output on exit.  Each launch's epilogue writes the
+// values the next launch normalises, with per-CTA partial statistics in one
+// of two alternating buffers (a launch reads the previous launch's buffer
+// and writes the other).
 bw_status run_step(bw_stack *st, cudaStream_t cs, const bw_stack_trace *tr) {
   const bw_stack_desc &d = st->d;
   const int dim = d.dim, ffn = d.ffn;
   const int b_qkv[4] = {0, d.n_heads * st->hd,
                         (d.n_heads + d.n_kv_heads) * st->hd, st->qkv_n};
-  const int b_dim[2] = {0, dim};
-  const int b_13[3] = {0, ffn, 2 * ffn};
-  const bw_bf16 *qkv = reinterpret_cast<bw_bf16 *>(st->qkv);
+  const WsSegments seg_qkv = segments(b_qkv, 3);
+  float2 *pin = st->part + kMaxPartials;  // read by the next launch
+  float2 *pout = st->part;                // written by the next launch
+  int P = 0;                              // CTAs of the previous launch
+  int grid = 0;
+  auto flip = [&]() {
+    float2 *t = pin;
+    pin = pout;
+    pout = t;
+    P = grid;
+  };
   for (int l = 0; l < d.n_layers; ++l) {
     const float *g = st->gammas[l];
-    const bw_bf16 *ws = st->ws[l];
+    const __nv_bfloat16 *ws =
+        reinterpret_cast<const __nv_bfloat16 *>(st->ws[l]);
+    const bool last = l == d.n_layers - 1;
     const bool rec = tr && tr->layer == l;
-    // attention_norm(h + down of the previous layer)
-    BW_TRY_CUDA(launch_norm_quant(
-        ResidualLoad{st->h, l ? st->dn : nullptr}, g, dim, d.eps, st->h,
-        st->q, st->s, cs));
+    if (rec) BW_TRY_CUDA(trace_copy(tr->h_in, st->h, dim * 4, cs));
+    // qkv = W2A8(wqkv, quant(attention_norm(h))); attn = value heads
+    const EpiQKV e_qkv{st->qkv, st->attn,    ws,     seg_qkv, st->v_off,
+                       st->hd,  st->group,   g + dim, pout};
+    if (l == 0)
+      BW_TRY_CUDA(launch_first(st->wqkv[l], st->qkv_n, dim, st->h, g, d.eps,
+                               rec ? tr->q_attn : nullptr,
+                               rec ? tr->s_attn : nullptr, e_qkv, cs, &grid));
+    else
+      BW_TRY_CUDA(launch_next(st->wqkv[l], st->qkv_n, dim, 0, st->h, g, pin,
+                              P, d.eps, rec ? tr->q_attn : nullptr,
+                              rec ? tr->s_attn : nullptr, e_qkv, cs, &grid));
+    flip();
+    if (rec) BW_TRY_CUDA(trace_copy(tr->qkv, st->qkv, st->qkv_n * 2, cs));
+    // o = W2A8(wo, quant(attn_sub_norm(attn))); h += o
+    BW_TRY_CUDA(launch_next(
+        st->wo[l], dim, dim, 0, st->attn, g + dim, pin, P, d.eps,
+        rec ? tr->q_o : nullptr, rec ? tr->s_o : nullptr,
+        EpiResid{st->o, st->h, ws + 3, g + 2 * dim, pout}, cs, &grid));
+    flip();
     if (rec) {
-      BW_TRY_CUDA(trace_copy(tr->h_in, st->h, dim * 4, cs));
-      BW_TRY_CUDA(trace_copy(tr->q_attn, st->q, dim, cs));
-      BW_TRY_CUDA(trace_copy(tr->s_attn, st->s, 4, cs));
-    }
-    BW_TRY(gemv_internal(st->q, st->wqkv[l], st->s, ws, b_qkv, 3, 1,
-                         st->qkv_n, dim, reinterpret_cast<bw_bf16 *>(st->qkv),
-                         cs));
-    if (rec) BW_TRY_CUDA(trace_copy(tr->qkv, qkv, st->qkv_n * 2, cs));
-    // attn_sub_norm(one-token attention)
-    BW_TRY_CUDA(launch_norm_quant(
-        AttnLoad{st->qkv, st->v_off, st->hd, st->group}, g + dim, dim, d.eps,
-        nullptr, st->q, st->s, cs));
-    if (rec) {
-      BW_TRY_CUDA(trace_copy(tr->q_o, st->q, dim, cs));
-      BW_TRY_CUDA(trace_copy(tr->s_o, st->s, 4, cs));
-    }
-    BW_TRY(gemv_internal(st->q, st->wo[l], st->s, ws + 3, b_dim, 1, 1, dim,
-                         dim, reinterpret_cast<bw_bf16 *>(st->o), cs));
-    if (rec) BW_TRY_CUDA(trace_copy(tr->o, st->o, dim * 2, cs));
-    // ffn_norm(h + o)
-    BW_TRY_CUDA(launch_norm_quant(ResidualLoad{st->h, st->o}, g + 2 * dim,
-                                  dim, d.eps, st->h, st->q, st->s, cs));
-    if (rec) {
+      BW_TRY_CUDA(trace_copy(tr->o, st->o, dim * 2, cs));
       BW_TRY_CUDA(trace_copy(tr->h_mid, st->h, dim * 4, cs));
-      BW_TRY_CUDA(trace_copy(tr->q_ffn, st->q, dim, cs));
-      BW_TRY_CUDA(trace_copy(tr->s_ffn, st->s, 4, cs));
     }
-    BW_TRY(gemv_internal(st->q, st->w13[l], st->s, ws + 4, b_13, 2, 1,
-                         2 * ffn, dim, reinterpret_cast<bw_bf16 *>(st->gu),
-                         cs));
+    // gu = W2A8(w13, quant(ffn_norm(h))); gated = relu(gate)^2 up
+    BW_TRY_CUDA(launch_next(
+        st->w13[l], 2 * ffn, dim, ffn / kGroupRows, st->h, g + 2 * dim, pin,
+        P, d.eps, rec ? tr->q_ffn : nullptr, rec ? tr->s_ffn : nullptr,
+        EpiGate{st->gu, st->gated, ws + 4, ffn, g + 3 * dim, pout}, cs,
+        &grid));
+    flip();
     if (rec) BW_TRY_CUDA(trace_copy(tr->gu, st->gu, 2 * ffn * 2, cs));
-    // ffn_sub_norm(relu(gate)^2 * up)
-    BW_TRY_CUDA(launch_norm_quant(Relu2Load{st->gu, ffn}, g + 3 * dim, ffn,
-                                  d.eps, nullptr, st->q, st->s, cs));
-    if (rec) {
-      BW_TRY_CUDA(trace_copy(tr->q_down, st->q, ffn, cs));
-      BW_TRY_CUDA(trace_copy(tr->s_down, st->s, 4, cs));
-    }
-    BW_TRY(gemv_internal(st->q, st->w2[l], st->s, ws + 6, b_dim, 1, 1, dim,
-                         ffn, reinterpret_cast<bw_bf16 *>(st->dn), cs));
+    // down = W2A8(w2, quant(ffn_sub_norm(gated))); h += down
+    const float *g_next = last ? nullptr : st->gammas[l + 1];
+    BW_TRY_CUDA(launch_next(
+        st->w2[l], dim, ffn, 0, st->gated, g + 3 * dim, pin, P, d.eps,
+        rec ? tr->q_down : nullptr, rec ? tr->s_down : nullptr,
+        EpiResid{st->dn, st->h, ws + 6, g_next, last ? nullptr : pout}, cs,
+        &grid));
+    flip();
     if (rec) BW_TRY_CUDA(trace_copy(tr->down, st->dn, dim * 2, cs));
   }
-  cudaLaunchAttribute attr[1];
-  cudaLaunchConfig_t cfg = glue_config(cs, attr);
-  BW_TRY_CUDA(cudaLaunchKernelEx(&cfg, residual_kernel, st->h,
-                                 static_cast<const __nv_bfloat16 *>(st->dn),
-                                 dim));
   return BW_OK;
 }
 
@@ -300,8 +530,9 @@ void free_stack(bw_stack *st) {
   if (!st) return;
   if (st->have_graph) cudaGraphExecDestroy(st->exec);
   cudaFree(st->h);
-  cudaFree(st->q);
-  cudaFree(st->s);
+  cudaFree(st->attn);
+  cudaFree(st->gated);
+  cudaFree(st->part);
   cudaFree(st->qkv);
   cudaFree(st->o);
   cudaFree(st->gu);
@@ -322,7 +553,7 @@ bw_status bw_stack_create(const bw_stack_desc *desc, bw_stack **out) {
     return BW_ERR_INVALID_ARG;
   if (d.dim % d.n_heads != 0 || d.n_heads % d.n_kv_heads != 0)
     return BW_ERR_UNSUPPORTED_SHAPE;
-  if (d.dim % 4 != 0 || d.ffn % 4 != 0 || d.dim > kMaxGlueK ||
+  if (d.dim % 4 != 0 || d.ffn % 8 != 0 || d.dim > kMaxGlueK ||
       d.ffn > kMaxGlueK)
     return BW_ERR_UNSUPPORTED_SHAPE;
   if (!d.wqkv || !d.wo || !d.w13 || !d.w2 || !d.ws || !d.gammas)
@@ -336,7 +567,7 @@ bw_status bw_stack_create(const bw_stack_desc *desc, bw_stack **out) {
     };
     if (!a16(d.wqkv[l]) || !a16(d.wo[l]) || !a16(d.w13[l]) || !a16(d.w2[l]) ||
         reinterpret_cast<uintptr_t>(d.ws[l]) % 2 != 0 ||
-        reinterpret_cast<uintptr_t>(d.gammas[l]) % 4 != 0)
+        !a16(d.gammas[l]))
       return BW_ERR_MISALIGNED;
   }
   bw_stack *st = new (std::nothrow) bw_stack();
@@ -355,18 +586,19 @@ bw_status bw_stack_create(const bw_stack_desc *desc, bw_stack **out) {
   st->qkv_n = (d.n_heads + 2 * d.n_kv_heads) * st->hd;
   st->v_off = (d.n_heads + d.n_kv_heads) * st->hd;
   st->group = d.n_heads / d.n_kv_heads;
-  const int qmax = d.dim > d.ffn ? d.dim : d.ffn;
   cudaError_t e = cudaSuccess;
   auto alloc = [&](void **p, size_t bytes) {
     if (e == cudaSuccess) e = cudaMalloc(p, bytes);
   };
   alloc(reinterpret_cast<void **>(&st->h), size_t(d.dim) * 4);
-  alloc(reinterpret_cast<void **>(&st->q), size_t(qmax));
-  alloc(reinterpret_cast<void **>(&st->s), 16);
   alloc(reinterpret_cast<void **>(&st->qkv), size_t(st->qkv_n) * 2);
   alloc(reinterpret_cast<void **>(&st->o), size_t(d.dim) * 2);
   alloc(reinterpret_cast<void **>(&st->gu), size_t(2 * d.ffn) * 2);
   alloc(reinterpret_cast<void **>(&st->dn), size_t(d.dim) * 2);
+  alloc(reinterpret_cast<void **>(&st->attn), size_t(d.dim) * 4);
+  alloc(reinterpret_cast<void **>(&st->gated), size_t(d.ffn) * 4);
+  alloc(reinterpret_cast<void **>(&st->part),
+        size_t(2) * kMaxPartials * sizeof(float2));
   if (e == cudaSuccess) e = cudaMemset(st->h, 0, size_t(d.dim) * 4);
   if (e != cudaSuccess) {
     free_stack(st);

@@ -192,14 +192,21 @@ bw_status bw_gemv_w2a8_acc(const int8_t *x, const uint8_t *packed, int M,
  * i / (n_heads / n_kv_heads) (the softmax of a single score is 1); q and k
  * are computed but do not change the result.  RMSNorm:
  * v * (1/sqrt(mean(v^2) + eps)) * gamma, fp32.  The residual stream h is
- * fp32; GEMV outputs are bf16.
+ * fp32; GEMV outputs are bf16.  Execution: four kernel launches per layer,
+ * one per GEMV.  Each launch's epilogue writes the values the next RMSNorm
+ * reads with per-CTA partial statistics, and the next launch's prologue
+ * finishes the norm and the int8 quantisation; the wo and w2 launches add
+ * their outputs into h (so h += down happens at the end of each layer,
+ * which is the same sum).  The fp32 sums run in a different order than a
+ * sequential loop, so results match a reference within rounding, not bit
+ * for bit.
  * ---------------------------------------------------------------------- */
 typedef struct bw_stack bw_stack;
 
 typedef struct {
     int n_layers;
     int dim;          /* model width (multiple of n_heads and of 4, <= 8192) */
-    int ffn;          /* FFN width (multiple of 4, <= 8192)                  */
+    int ffn;          /* FFN width (multiple of 8, <= 8192)                  */
     int n_heads;      /* query heads                                         */
     int n_kv_heads;   /* KV heads (divides n_heads)                          */
     float eps;        /* RMSNorm epsilon                                     */
@@ -216,8 +223,9 @@ typedef struct {
     /* Host array of n_layers device pointers to 7 bf16 weight scales:
      * q, k, v, o, gate, up, down. */
     const bw_bf16 *const *ws;
-    /* Host array of n_layers device pointers to 3 dim + ffn fp32 gains:
-     * attention_norm, attn_sub_norm, ffn_norm (dim each), ffn_sub_norm. */
+    /* Host array of n_layers device pointers (16-byte aligned) to
+     * 3 dim + ffn fp32 gains: attention_norm, attn_sub_norm, ffn_norm (dim
+     * each), ffn_sub_norm. */
     const float *const *gammas;
 } bw_stack_desc;
 
@@ -239,7 +247,8 @@ typedef struct {
 
 /* Creates a stack: copies the descriptor (the pointer arrays; the weights
  * stay the caller's and must outlive the stack), allocates its device
- * scratch (about 4 dim + 5 ffn bytes of activations) with cudaMalloc,
+ * scratch (about 14 dim + 8 ffn bytes of activations plus 32 KB) with
+ * cudaMalloc,
  * runs one step on zero input and captures one step as a CUDA graph on a
  * private stream.  Synchronising; call it before any stream capture. */
 bw_status bw_stack_create(const bw_stack_desc *desc, bw_stack **stack);

@@ -181,7 +181,10 @@ def test_stack_create_host_validation(lib):
     assert make(dim=250) == SHAPE           # not a multiple of n_heads
     assert make(n_kv_heads=3) == SHAPE      # does not divide n_heads
     assert make(ffn=8196) == SHAPE          # above the glue limit
+    assert make(ffn=1020) == SHAPE          # gate/up pairs need ffn % 8 == 0
     assert make(wo=None) == INVALID
     bad = (P * L)(A16, A16 + 8)             # second layer misaligned
     assert make(w2=ctypes.cast(bad, P)) == MISALIGNED
+    gbad = (P * L)(A4, A4 + 4)              # gains read as float4
+    assert make(gammas=ctypes.cast(gbad, P)) == MISALIGNED
     assert run(None, A4, 1, A4, None, None) == INVALID
