@@ -61,40 +61,69 @@ struct StageInt8 {
   const float *s;  // null in accumulator mode
   int x_ld, K, vec_x;
 
+  struct Pre {};  // every input may come from the preceding kernel
+  __device__ __forceinline__ Pre pre_wait() const { return Pre{}; }
+
   template <int MT>
-  __device__ __forceinline__ void stage(int8_t *xs, uint32_t xrow, int chunks,
-                                        float *s_sm, float *red,
+  __device__ __forceinline__ void stage(const Pre &, const StageCtx &c,
                                         int (&part)[MT]) const {
-    (void)red;
-    if (s && threadIdx.x < MT) s_sm[threadIdx.x] = s[threadIdx.x];
+    // Every load is issued before the first shared-memory store that needs
+    // one (issue is in order): the scale, then up to kBatch vectors per row
+    // and thread at a time.
+    constexpr int kBatch = 4;
+    const float sv = (s && threadIdx.x < MT) ? s[threadIdx.x] : 0.0f;
     const int tid = threadIdx.x, nthreads = blockDim.x;
 #pragma unroll
     for (int m = 0; m < MT; ++m) {
       int p = 0;
-      int8_t *dst = xs + m * xrow;
+      int8_t *dst = c.xs + m * c.xrow;
       if (vec_x) {
         const uint4 *src = reinterpret_cast<const uint4 *>(x + size_t(m) * x_ld);
-        for (int v = tid; v < chunks * 4; v += nthreads) {
-          uint4 x4 = make_uint4(0u, 0u, 0u, 0u);
-          if (16 * v < K) x4 = __ldg(src + v);
-          reinterpret_cast<uint4 *>(dst)[v] = x4;
-          p = dp4a_us(0x01010101u, x4.x, p);
-          p = dp4a_us(0x01010101u, x4.y, p);
-          p = dp4a_us(0x01010101u, x4.z, p);
-          p = dp4a_us(0x01010101u, x4.w, p);
+        const int nv = c.chunks * 4;
+        for (int v0 = tid; v0 < nv; v0 += kBatch * nthreads) {
+          uint4 x4[kBatch];
+#pragma unroll
+          for (int b = 0; b < kBatch; ++b) {
+            const int v = v0 + b * nthreads;
+            x4[b] = (v < nv && 16 * v < K) ? __ldg(src + v)
+                                           : make_uint4(0u, 0u, 0u, 0u);
+          }
+#pragma unroll
+          for (int b = 0; b < kBatch; ++b) {
+            const int v = v0 + b * nthreads;
+            if (v < nv) {
+              reinterpret_cast<uint4 *>(dst)[v] = x4[b];
+              p = dp4a_us(0x01010101u, x4[b].x, p);
+              p = dp4a_us(0x01010101u, x4[b].y, p);
+              p = dp4a_us(0x01010101u, x4[b].z, p);
+              p = dp4a_us(0x01010101u, x4[b].w, p);
+            }
+          }
         }
       } else {
         const unsigned int *src =
             reinterpret_cast<const unsigned int *>(x + size_t(m) * x_ld);
-        for (int wd = tid; wd < chunks * 16; wd += nthreads) {
-          uint32_t v = 0u;
-          if (4 * wd < K) v = __ldg(src + wd);
-          reinterpret_cast<uint32_t *>(dst)[wd] = v;
-          p = dp4a_us(0x01010101u, v, p);
+        const int nw = c.chunks * 16;
+        for (int w0 = tid; w0 < nw; w0 += kBatch * nthreads) {
+          uint32_t xv[kBatch];
+#pragma unroll
+          for (int b = 0; b < kBatch; ++b) {
+            const int wd = w0 + b * nthreads;
+            xv[b] = (wd < nw && 4 * wd < K) ? __ldg(src + wd) : 0u;
+          }
+#pragma unroll
+          for (int b = 0; b < kBatch; ++b) {
+            const int wd = w0 + b * nthreads;
+            if (wd < nw) {
+              reinterpret_cast<uint32_t *>(dst)[wd] = xv[b];
+              p = dp4a_us(0x01010101u, xv[b], p);
+            }
+          }
         }
       }
       part[m] = p;
     }
+    if (s && threadIdx.x < MT) c.s_sm[threadIdx.x] = sv;
   }
 };
 
@@ -107,9 +136,10 @@ struct EpiOut {
   const __nv_bfloat16 *ws;
   WsSegments seg;
 
-  __device__ __forceinline__ void stage_scales(float *ws_sm) const {
-    if (!ACC && int(threadIdx.x) < seg.n_ws)
-      ws_sm[threadIdx.x] = __bfloat162float(ws[threadIdx.x]);
+  __device__ __forceinline__ float scale_value() const {
+    return (!ACC && int(threadIdx.x) < seg.n_ws)
+               ? __bfloat162float(ws[threadIdx.x])
+               : 0.0f;
   }
   __device__ __forceinline__ void store(int n, int m, int total,
                                         const float *s_sm,
@@ -127,16 +157,16 @@ struct EpiOut {
           __float2bfloat16_rn(v);
     }
   }
-  __device__ __forceinline__ float prefetch(const PipeArgs &, int,
-                                            int) const {
-    return 0.0f;
+  __device__ __forceinline__ float2 prefetch(const PipeArgs &, int,
+                                             int) const {
+    return make_float2(0.0f, 0.0f);
   }
   template <int MT>
   __device__ __forceinline__ void finish(const PipeArgs &a, const int *tot,
                                          const int (&sx)[MT], int g_lo,
                                          int n_g, const float *s_sm,
                                          const float *ws_sm, float *red,
-                                         float pre) const {
+                                         float2 pre) const {
     (void)red;
     (void)pre;
     for (int t = threadIdx.x; t < n_g * 8; t += blockDim.x) {

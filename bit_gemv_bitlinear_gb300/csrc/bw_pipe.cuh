@@ -7,21 +7,28 @@
 // (the int8 activations and their scales) and what it writes (bf16 outputs,
 // int32 accumulators, or a residual update) are policies:
 //
-//   Prologue policy, after griddepcontrol.wait, called by every thread:
-//     template <int MT> __device__ void stage(int8_t *xs, uint32_t xrow,
-//         int chunks, float *s_sm, float *red, int (&part)[MT]) const;
-//   stages MT int8 activation rows at xs + m xrow (zero from K up to
-//   64 chunks), their scales in s_sm[m], and returns this thread's share of
-//   sum_k x[m][k] in part[m].  It may use CTA barriers (__syncthreads) and
-//   the 64 floats at `red`.
+//   Prologue policy, called by every thread:
+//     using Pre = ...;                        (state loaded before the wait)
+//     __device__ Pre pre_wait() const;        (static inputs only)
+//     template <int MT> __device__ void stage(const Pre &pre,
+//         const StageCtx &c, int (&part)[MT]) const;  (after the wait)
+//   stages MT int8 activation rows at c.xs + m c.xrow (zero from K up to
+//   64 chunks), their scales in c.s_sm[m], and returns this thread's share
+//   of sum_k x[m][k] in part[m].  It may use CTA barriers (__syncthreads)
+//   and the 64 floats at c.red.  Loads issued right after the wait are
+//   plain loads: a bulk copy here would queue behind the CTA's weight
+//   copies in the TMA unit.
 //
 //   Epilogue policy:
-//     __device__ void stage_scales(float *ws_sm) const;   (after the wait)
-//     __device__ float prefetch(const PipeArgs &a, int g_lo, int n_g) const;
+//     __device__ float scale_value() const;   (after the wait)
+//   scale_value() returns, for thread t < BW_MAX_WS, the t-th weight scale
+//   (fp32) that finish() finds in ws_sm[t]; it is loaded before the
+//   prologue and stored after it, so the two loads overlap.
+//     __device__ float2 prefetch(const PipeArgs &a, int g_lo, int n_g) const;
 //     template <int MT> __device__ void finish(const PipeArgs &a,
 //         const int *tot, const int (&sx)[MT], int g_lo, int n_g,
 //         const float *s_sm, const float *ws_sm, float *red,
-//         float pre) const;
+//         float2 pre) const;
 //   prefetch() runs right after the dependency wait; whatever it returns
 //   reaches finish() of the same thread as `pre` (e.g. a value of the
 //   thread's first output row, loaded early).
@@ -195,7 +202,7 @@ struct PipeLayout {
 
 // sums: [MT] activation scales s, [BW_MAX_WS] weight scales (as fp32),
 // [warps][MT] per-warp activation sums; red: 64 floats of prologue
-// reduction scratch; tot: [k][MT][8] row totals.
+// reduction scratch; tot: [k][MT][8] row totals; bars: the ring barriers.
 __host__ __device__ inline PipeLayout pipe_layout(int mt, int chunks,
                                                   int slot_chunks, int slots,
                                                   int warps, int k) {
@@ -210,6 +217,16 @@ __host__ __device__ inline PipeLayout pipe_layout(int mt, int chunks,
   l.total = l.bars + uint32_t(warps * slots * 8);
   return l;
 }
+
+// What a prologue policy's stage() gets: the activation tile to fill, the
+// scale slots and reduction scratch.
+struct StageCtx {
+  int8_t *xs;
+  uint32_t xrow;
+  int chunks;
+  float *s_sm;
+  float *red;
+};
 
 constexpr int kPipeWarps = 8;
 constexpr int kPipeMaxGroupsPerCta = 256;
@@ -365,12 +382,15 @@ pipe_gemv_kernel(const PipeArgs a, const Pro pro, const Epi epi) {
     for (int s = 0; s < R && iss.u < run_hi; ++s) issue_next(s);
   }
   for (int t = threadIdx.x; t < n_g * MT * 8; t += blockDim.x) tot[t] = 0;
+  const typename Pro::Pre pro_pre = pro.pre_wait();
   pdl_wait();
 
-  epi.stage_scales(ws_sm);
-  const float pre = epi.prefetch(a, g_lo, n_g);
+  const float wsv = epi.scale_value();
+  const float2 pre = epi.prefetch(a, g_lo, n_g);
   int part[MT];
-  pro.template stage<MT>(xs, xrow, C, s_sm, red, part);
+  const StageCtx sc{xs, xrow, C, s_sm, red};
+  pro.template stage<MT>(pro_pre, sc, part);
+  if (threadIdx.x < BW_MAX_WS) ws_sm[threadIdx.x] = wsv;
 #pragma unroll
   for (int m = 0; m < MT; ++m) {
 #pragma unroll

@@ -47,6 +47,8 @@ using namespace pipe;
 
 constexpr int kPrologueThreads = kPipeWarps * 32;
 constexpr int kMaxGlueK = 32 * kPrologueThreads;  // 8192: V <= 32 per thread
+constexpr int kMaxGroup = 8;          // query heads per KV head unrolled
+constexpr int kPartialsPerThread = 2;  // partials loaded at once: 512 per CTA
 
 __device__ __forceinline__ int8_t quant1(float x, float scale) {
   return static_cast<int8_t>(
@@ -68,20 +70,34 @@ struct NormQuantH {
   int8_t *trace_q;
   float *trace_s;
 
+  struct Pre {  // the gains are static: loaded before the wait
+    float gm[V];
+  };
+  __device__ __forceinline__ Pre pre_wait() const {
+    Pre p;
+#pragma unroll
+    for (int i = 0; i < V; ++i) {
+      const int k = threadIdx.x + i * kPrologueThreads;
+      p.gm[i] = k < K ? gamma[k] : 0.0f;
+    }
+    return p;
+  }
+
   template <int MT>
-  __device__ __forceinline__ void stage(int8_t *xs, uint32_t xrow, int chunks,
-                                        float *s_sm, float *red,
+  __device__ __forceinline__ void stage(const Pre &pre, const StageCtx &c,
                                         int (&part)[MT]) const {
     static_assert(MT == 1, "the stack runs one token per step");
-    (void)xrow;
+    int8_t *xs = c.xs;
+    float *s_sm = c.s_sm, *red = c.red;
+    const int chunks = c.chunks;
     const int tid = threadIdx.x;
-    float v[V], gm[V];
+    float v[V];
 #pragma unroll
     for (int i = 0; i < V; ++i) {
       const int k = tid + i * kPrologueThreads;
       v[i] = k < K ? h[k] : 0.0f;
-      gm[i] = k < K ? gamma[k] : 0.0f;
     }
+    const float *gm = pre.gm;
     float ss = 0.0f, unused = 0.0f;
 #pragma unroll
     for (int i = 0; i < V; ++i) ss += v[i] * v[i];
@@ -118,8 +134,8 @@ struct NormQuantH {
 
 // Prologue of every other GEMV: the previous launch wrote the fp32 values
 // v[K] to normalise and, per CTA, the partial statistics (sum of v^2, max
-// of |v * gamma|) over the values it wrote.  Each warp reduces the P
-// partials in the same fixed order, so every CTA gets the same
+// of |v * gamma|) over the values it wrote.  The CTA reduces the P
+// partials in the same fixed order in every CTA, so every CTA gets the same
 //   r = 1 / sqrt(sum / K + eps),  s = 127 / max(max * r, 1e-5),
 // and quantises q = clamp(rint(((v * gamma) * r) * s)).  Rounding is
 // monotone, so max * r is exactly the largest |(v * gamma) * r|.  Four
@@ -134,35 +150,58 @@ struct NormQuantP {
   int8_t *trace_q;
   float *trace_s;
 
+  struct Pre {  // the gains are static: loaded before the wait
+    float4 gm[V4];
+  };
+  __device__ __forceinline__ Pre pre_wait() const {
+    Pre p;
+#pragma unroll
+    for (int i = 0; i < V4; ++i) {
+      const int g = threadIdx.x + i * kPrologueThreads;
+      p.gm[i] = g < (K >> 2)
+                    ? __ldg(reinterpret_cast<const float4 *>(gamma) + g)
+                    : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+    }
+    return p;
+  }
+
   template <int MT>
-  __device__ __forceinline__ void stage(int8_t *xs, uint32_t xrow, int chunks,
-                                        float *s_sm, float *red,
+  __device__ __forceinline__ void stage(const Pre &pre, const StageCtx &c,
                                         int (&part_out)[MT]) const {
     static_assert(MT == 1, "the stack runs one token per step");
-    (void)xrow;
-    (void)red;
-    const int tid = threadIdx.x, lane = tid & 31;
+    int8_t *xs = c.xs;
+    float *s_sm = c.s_sm, *red = c.red;
+    const int chunks = c.chunks;
+    const int tid = threadIdx.x;
     const int groups = K >> 2;  // K is a multiple of 4
-    float4 v[V4], gm[V4];
+    // All loads are issued before the first is used (issue is in order):
+    // the values, then at most kPartialsPerThread partials per thread.
+    float4 v[V4];
 #pragma unroll
     for (int i = 0; i < V4; ++i) {
       const int g = tid + i * kPrologueThreads;
-      if (g < groups) {
-        v[i] = __ldg(reinterpret_cast<const float4 *>(src) + g);
-        gm[i] = __ldg(reinterpret_cast<const float4 *>(gamma) + g);
-      }
+      if (g < groups) v[i] = __ldg(reinterpret_cast<const float4 *>(src) + g);
+    }
+    float2 pv[kPartialsPerThread];
+#pragma unroll
+    for (int j = 0; j < kPartialsPerThread; ++j) {
+      const int i = tid + j * kPrologueThreads;
+      pv[j] = i < P ? part[i] : make_float2(0.0f, 0.0f);
     }
     float ss = 0.0f, mx = 0.0f;
-    for (int i = lane; i < P; i += 32) {
-      const float2 pv = part[i];
-      ss += pv.x;
-      mx = fmaxf(mx, pv.y);
-    }
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      ss += __shfl_xor_sync(0xffffffffu, ss, o);
-      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+    for (int j = 0; j < kPartialsPerThread; ++j) {
+      ss += pv[j].x;
+      mx = fmaxf(mx, pv[j].y);
     }
+    for (int i = tid + kPartialsPerThread * kPrologueThreads; i < P;
+         i += kPrologueThreads) {  // more producer CTAs: rare, sequential
+      const float2 pe = part[i];
+      ss += pe.x;
+      mx = fmaxf(mx, pe.y);
+    }
+    cta_sum_max(ss, mx, red);  // same fixed order in every CTA
+    const float4 *gm = pre.gm;
     const float r = 1.0f / sqrtf(ss / static_cast<float>(K) + eps);
     const float scale = 127.0f / fmaxf(__fmul_rn(mx, r), 1e-5f);
     if (tid == 0) s_sm[0] = scale;
@@ -222,20 +261,20 @@ struct EpiQKV {
   const float *gamma_next;
   float2 *part_out;
 
-  __device__ __forceinline__ void stage_scales(float *ws_sm) const {
-    if (int(threadIdx.x) < seg.n_ws)
-      ws_sm[threadIdx.x] = __bfloat162float(ws[threadIdx.x]);
+  __device__ __forceinline__ float scale_value() const {
+    return int(threadIdx.x) < seg.n_ws ? __bfloat162float(ws[threadIdx.x])
+                                       : 0.0f;
   }
-  __device__ __forceinline__ float prefetch(const PipeArgs &, int,
-                                            int) const {
-    return 0.0f;
+  __device__ __forceinline__ float2 prefetch(const PipeArgs &, int,
+                                             int) const {
+    return make_float2(0.0f, 0.0f);
   }
   template <int MT>
   __device__ __forceinline__ void finish(const PipeArgs &a, const int *tot,
                                          const int (&sx)[MT], int g_lo,
                                          int n_g, const float *s_sm,
                                          const float *ws_sm, float *red,
-                                         float) const {
+                                         float2) const {
     float ss = 0.0f, mx = 0.0f;
     for (int t = threadIdx.x; t < n_g * 8; t += blockDim.x) {
       const int gl = t >> 3, rr = t & 7;
@@ -252,11 +291,23 @@ struct EpiQKV {
         const int j = n - v_off;
         const int kv = j / hd, d = j - kv * hd;
         const float yf = __bfloat162float(yv);
-        for (int h = kv * group; h < (kv + 1) * group; ++h) {
-          const int pos = h * hd + d;
-          attn[pos] = yf;
+        const int base = kv * group * hd + d;  // position of head kv group
+        float gv[kMaxGroup];  // gains loaded together
+#pragma unroll
+        for (int u = 0; u < kMaxGroup; ++u)
+          gv[u] = u < group ? gamma_next[base + u * hd] : 0.0f;
+#pragma unroll
+        for (int u = 0; u < kMaxGroup; ++u) {
+          if (u < group) {
+            attn[base + u * hd] = yf;
+            ss += yf * yf;
+            mx = fmaxf(mx, fabsf(__fmul_rn(yf, gv[u])));
+          }
+        }
+        for (int u = kMaxGroup; u < group; ++u) {  // more heads per KV head
+          attn[base + u * hd] = yf;
           ss += yf * yf;
-          mx = fmaxf(mx, fabsf(__fmul_rn(yf, gamma_next[pos])));
+          mx = fmaxf(mx, fabsf(__fmul_rn(yf, gamma_next[base + u * hd])));
         }
       }
     }
@@ -266,8 +317,8 @@ struct EpiQKV {
 
 // Epilogue of wo and w2: y[n] (bf16, one scale) and the residual update
 // h[n] += y[n] (fp32), with the partial statistics of the new h against the
-// gains of the next RMSNorm (none after the last layer).  h[n] of the
-// thread's first row is loaded right after the dependency wait.
+// gains of the next RMSNorm (none after the last layer).  h[n] and the gain
+// of the thread's first row are loaded right after the dependency wait.
 struct EpiResid {
   __nv_bfloat16 *y;
   float *h;
@@ -275,21 +326,22 @@ struct EpiResid {
   const float *gamma_next;  // or null
   float2 *part_out;         // or null
 
-  __device__ __forceinline__ void stage_scales(float *ws_sm) const {
-    if (threadIdx.x == 0) ws_sm[0] = __bfloat162float(ws[0]);
+  __device__ __forceinline__ float scale_value() const {
+    return threadIdx.x == 0 ? __bfloat162float(ws[0]) : 0.0f;
   }
-  __device__ __forceinline__ float prefetch(const PipeArgs &a, int g_lo,
-                                            int n_g) const {
+  __device__ __forceinline__ float2 prefetch(const PipeArgs &a, int g_lo,
+                                             int n_g) const {
     const int t = threadIdx.x;
     const int n = (g_lo + (t >> 3)) * kGroupRows + (t & 7);
-    return (t < n_g * 8 && n < a.N) ? h[n] : 0.0f;
+    if (t >= n_g * 8 || n >= a.N) return make_float2(0.0f, 0.0f);
+    return make_float2(h[n], gamma_next ? gamma_next[n] : 0.0f);
   }
   template <int MT>
   __device__ __forceinline__ void finish(const PipeArgs &a, const int *tot,
                                          const int (&sx)[MT], int g_lo,
                                          int n_g, const float *s_sm,
                                          const float *ws_sm, float *red,
-                                         float pre) const {
+                                         float2 pre) const {
     float ss = 0.0f, mx = 0.0f;
     for (int t = threadIdx.x; t < n_g * 8; t += blockDim.x) {
       const int gl = t >> 3, rr = t & 7;
@@ -298,12 +350,13 @@ struct EpiResid {
       const __nv_bfloat16 yv =
           scaled_bf16(tot[gl * 8 + rr] - sx[0], s_sm[0], ws_sm[0]);
       y[n] = yv;
-      const float hv = t == int(threadIdx.x) ? pre : h[n];
+      const bool first = t == int(threadIdx.x);  // prefetched row
+      const float hv = first ? pre.x : h[n];
       const float hn = hv + __bfloat162float(yv);
       h[n] = hn;
       if (gamma_next) {
         ss += hn * hn;
-        mx = fmaxf(mx, fabsf(__fmul_rn(hn, gamma_next[n])));
+        mx = fmaxf(mx, fabsf(__fmul_rn(hn, first ? pre.y : gamma_next[n])));
       }
     }
     write_partials(part_out, ss, mx, red);
@@ -322,19 +375,22 @@ struct EpiGate {
   const float *gamma_next;
   float2 *part_out;
 
-  __device__ __forceinline__ void stage_scales(float *ws_sm) const {
-    if (threadIdx.x < 2) ws_sm[threadIdx.x] = __bfloat162float(ws[threadIdx.x]);
+  __device__ __forceinline__ float scale_value() const {
+    return threadIdx.x < 2 ? __bfloat162float(ws[threadIdx.x]) : 0.0f;
   }
-  __device__ __forceinline__ float prefetch(const PipeArgs &, int,
-                                            int) const {
-    return 0.0f;
+  __device__ __forceinline__ float2 prefetch(const PipeArgs &, int g_lo,
+                                             int n_g) const {
+    const int t = threadIdx.x;
+    if (t >= (n_g >> 1) * 8) return make_float2(0.0f, 0.0f);
+    const int f = ((g_lo >> 1) + (t >> 3)) * kGroupRows + (t & 7);
+    return make_float2(gamma_next[f], 0.0f);
   }
   template <int MT>
   __device__ __forceinline__ void finish(const PipeArgs &a, const int *tot,
                                          const int (&sx)[MT], int g_lo,
                                          int n_g, const float *s_sm,
                                          const float *ws_sm, float *red,
-                                         float) const {
+                                         float2 pre) const {
     (void)a;
     float ss = 0.0f, mx = 0.0f;
     // g_lo and n_g are even: the CTA holds whole (gate, up) pairs.
@@ -352,7 +408,8 @@ struct EpiGate {
       const float v = __fmul_rn(__fmul_rn(r, r), __bfloat162float(yu));
       gated[f] = v;
       ss += v * v;
-      mx = fmaxf(mx, fabsf(__fmul_rn(v, gamma_next[f])));
+      const float gn = t == int(threadIdx.x) ? pre.x : gamma_next[f];
+      mx = fmaxf(mx, fabsf(__fmul_rn(v, gn)));
     }
     write_partials(part_out, ss, mx, red);
   }
@@ -385,6 +442,9 @@ cudaError_t launch_first(const uint8_t *w, int N, int K, const float *h,
   if (K <= 8 * kPrologueThreads)
     return launch_one(w, N, K, 0, NormQuantH<8>{h, gamma, K, eps, tq, ts},
                       epi, cs, grid);
+  if (K <= 16 * kPrologueThreads)
+    return launch_one(w, N, K, 0, NormQuantH<16>{h, gamma, K, eps, tq, ts},
+                      epi, cs, grid);
   return launch_one(w, N, K, 0, NormQuantH<32>{h, gamma, K, eps, tq, ts},
                     epi, cs, grid);
 }
@@ -399,6 +459,10 @@ cudaError_t launch_next(const uint8_t *w, int N, int K, int pair_half,
   if (K <= 8 * kPrologueThreads)
     return launch_one(w, N, K, pair_half,
                       NormQuantP<2>{src, gamma, part, P, K, eps, tq, ts}, epi,
+                      cs, grid);
+  if (K <= 16 * kPrologueThreads)
+    return launch_one(w, N, K, pair_half,
+                      NormQuantP<4>{src, gamma, part, P, K, eps, tq, ts}, epi,
                       cs, grid);
   return launch_one(w, N, K, pair_half,
                     NormQuantP<8>{src, gamma, part, P, K, eps, tq, ts}, epi,
