@@ -269,8 +269,9 @@ void bw_stack_destroy(bw_stack *stack);
 /* bw_device_error -- reads and clears the library's device error word.
  * Kernels that wait on an mbarrier bound every wait (about one second); a
  * wait that runs out sets a bit here and the kernel stops early instead of
- * hanging (bit 1: the producer gave up on a free buffer, bit 2: the producer
- * gave up on its own copies, bit 4: a consumer gave up on a full buffer).
+ * hanging (bit 2: a lane gave up waiting for the copies it issued before
+ * leaving, bit 4: a warp gave up waiting for a weight piece; bit 8 is the
+ * self-test's).
  * Returns BW_ERR_TIMEOUT if any bit was set, BW_OK otherwise; *bits receives
  * the word.  SYNCHRONISES `stream`; not for the hot path. */
 bw_status bw_device_error(unsigned int *bits, bw_stream_t stream);
