@@ -1,5 +1,5 @@
 // bw_gemv_mma.cu -- the W2A8 product for batched activations (M >= 8) on
-// tensor cores.
+// tensor cores, streamed like the M = 1 pipe kernel.
 //
 // Same result as the CUDA-core GEMV: acc[m][n] = sum_k w[n][k] x[m][k]
 // exactly, then y = bf16((acc / s[m]) * ws[seg(n)]).  Source: "BitNet GPU
@@ -11,57 +11,39 @@
 // Exactness: ternary weights and int8 activations are exact in fp16, every
 // product is exact, and every fp32 partial sum is an integer of magnitude
 // at most 128 K < 2^21 (K <= 16384), so fp16 MMA with fp32 accumulation
-// gives the exact integer in any order.
+// gives the exact integer in any order; the partial sums of a row group are
+// converted to int32 and added with shared-memory atomics.
 //
-// Design:
-//  * mma.sync m16n8k16 (fp16 in, fp32 accumulate).  A = 16 weight rows x 16
-//    k, B = 16 k x 8 tokens, D = 16 rows x 8 tokens.  A warp owns 16 rows
-//    (two 8-row groups of the device layout) and all tokens of the tile, so
-//    every A fragment is decoded once and used for M/8 MMAs.
-//  * A fragment straight from the packed words in registers: thread (g, t)
-//    needs codes (row g | g+8, k = 2t, 2t+1, 2t+8, 2t+9) of a 16-k word;
+// Design (the streaming is that of bw_pipe.cuh):
+//  * mma.sync m16n8k16 (fp16 in, fp32 accumulate) with A = 16 tokens x 16 k
+//    and B = 16 k x 8 weight rows, i.e. one row group of the device layout:
+//    the pieces a warp streams are the pieces of the M = 1 kernel.
+//  * A CTA owns k consecutive row groups; its 8 warps split the CTA's chunks
+//    into equal runs, each streamed in pieces through the warp's own ring
+//    of bulk copies (the first pieces requested before the dependency wait).
+//  * Activations: a tile of MT = 16 (or 8) tokens is converted once per CTA
+//    to fp16 (x + 128 as the low byte of fp16(1024 + u), minus 1152) into a
+//    shared tile whose rows are 16 bytes longer than 64 k per chunk, so the
+//    ldmatrix.x4 that builds each A fragment is conflict-free.
+//  * B fragment straight from the packed word in shared memory: thread
+//    (g, t) needs codes (row g, k = 2t, 2t+1, 2t+8, 2t+9) of a 16-k word;
 //    with the word interleave of the layout these sit in byte pair 2(t&1)
-//    at slots t/2 and t/2 + 2, so one shift, two masks, a byte permute that
-//    builds fp16(1024 + c) and one fp16 subtract of 1025 give two weights
-//    c - 1 per 32-bit register.
-//  * Activations: the CTA converts each K slice of x (int8) to fp16 once
-//    (x + 128 as the low byte of fp16(1024 + u), minus 1152) into a padded
-//    shared tile, double-buffered; B fragments are conflict-free 32-bit
-//    shared loads.
-//  * The CTA's weight rows are one contiguous run (8 row groups): one bulk
-//    L2 prefetch before the programmatic-launch dependency wait, then
-//    128-bit loads, one slice ahead.
+//    at slots t/2 and t/2 + 2, so one shift and, per two weights, one
+//    mask-or and one byte permute that reads the fp16 high bytes of -1, 0,
+//    +1 from a constant give two weights per 32-bit register (the weights
+//    are signed here: no sum_k x correction).
 #include <cuda_fp16.h>
 
-#include "bw_internal.cuh"
+#include "bw_pipe.cuh"
 
 namespace bw {
 namespace {
 
-constexpr int kMmaWarps = 4;         // 4 warps x 16 rows = 64 rows per CTA
-constexpr int kRowsPerCta = 16 * kMmaWarps;
-constexpr int kSlice = 256;          // k per staged activation slice
-constexpr int kXStride = kSlice + 8; // halves per staged row (+16 bytes)
+using namespace pipe;
 
-__device__ __forceinline__ void pdl_wait() {
-  asm volatile("griddepcontrol.wait;" ::: "memory");
-}
-__device__ __forceinline__ void pdl_trigger() {
-  asm volatile("griddepcontrol.launch_dependents;");
-}
-__device__ __forceinline__ void prefetch_l2(const void *p, uint32_t bytes) {
-  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p),
-               "r"(bytes)
-               : "memory");
-}
-
-__device__ __forceinline__ uint4 ld_weights16(const uint8_t *p) {
-  uint4 v;
-  asm("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
-      : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-      : "l"(p));
-  return v;
-}
+constexpr int kMmaWarps = 16;        // warps per CTA (one CTA per SM)
+constexpr int kMmaSlots = 2;         // ring slots per warp
+constexpr int kMmaPieceChunks = 32;  // 4 KB pieces (2 KB where that fits)
 
 __device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t s) {
   uint32_t d;
@@ -75,10 +57,15 @@ __device__ __forceinline__ uint32_t hsub2(uint32_t a, uint32_t b) {
   return d;
 }
 
-// Two codes (bits 0-1 of bytes 0 and 1 of m) -> fp16x2 of (code - 1).
-__device__ __forceinline__ uint32_t decode_pair(uint32_t m) {
-  // bytes [c0, 0x64, c1, 0x64] = fp16(1024 + c0), fp16(1024 + c1)
-  return hsub2(prmt(m, 0x64646464u, 0x4140u), 0x64016401u);  // - 1025
+// fp16 of a ternary weight has a zero low byte and the high byte 0xBC
+// (-1), 0x00 (0) or 0x3C (+1): byte c of this table for code c = w + 1,
+// byte 3 is the zero low byte.
+constexpr uint32_t kTernaryF16Hi = 0x003C00BCu;
+
+// Two codes at bits 4-5 and 12-13 of sel (other bits ignored) -> fp16x2 of
+// (code - 1): a byte permute whose selector nibbles are 3, c0, 3, c1.
+__device__ __forceinline__ uint32_t decode_pair_hi(uint32_t sel) {
+  return prmt(kTernaryF16Hi, 0u, (sel & 0x3030u) | 0x0303u);
 }
 
 // Four int8 (one 32-bit word) -> two fp16x2 (exact).
@@ -99,189 +86,339 @@ __device__ __forceinline__ void mma16816(float (&d)[4], const uint32_t (&a)[4],
       : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 
-// Stage activation rows [0, 8 NT) x k in [k0, k0 + kSlice) as fp16 (zero
-// beyond K and beyond the tile's rows).
-template <int NT>
-__device__ __forceinline__ void stage_x(const GemvArgs &a, int rows, int k0,
-                                        __half *xs) {
-  constexpr int MT = 8 * NT;
-  constexpr int kWords = kSlice / 4;
-  for (int i = threadIdx.x; i < MT * kWords; i += blockDim.x) {
-    const int m = i / kWords;
-    const int kk = (i % kWords) * 4;
-    const int k = k0 + kk;
-    uint32_t v = 0u;
-    if (m < rows && k < a.K)
-      v = __ldg(reinterpret_cast<const unsigned int *>(a.x + size_t(m) * a.x_ld +
-                                                       k));
-    *reinterpret_cast<uint2 *>(xs + m * kXStride + kk) = int8x4_to_f16(v);
-  }
+__device__ __forceinline__ void ldmatrix_x4(uint32_t (&r)[4], uint32_t addr) {
+  asm volatile(
+      "ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+      : "r"(addr));
 }
 
-template <int NT, bool ACC_OUT>
+// Row stride of the fp16 activation tile in bytes: 64 k per chunk plus 16,
+// so that the 8 rows of an ldmatrix matrix fall in 8 distinct bank groups.
+__host__ __device__ inline uint32_t mma_xrow_bytes(int chunks) {
+  return uint32_t(chunks) * 128u + 16u;
+}
+
+// Shared-memory carve-up: ring [warps][slots][piece], x tile [MT][xrow]
+// (rows past MT are never read: A rows 8..15 of an 8-token tile come from
+// the zero block), zero block (16 bytes), s [16], ws [BW_MAX_WS], row
+// totals [k][16][8] int32, barriers [warps][slots].
+struct MmaLayout {
+  uint32_t ring, xs, zero, s, ws, tot, bars, total;
+};
+
+__host__ __device__ inline MmaLayout mma_layout(int mt, int chunks, int k,
+                                                int piece_chunks) {
+  MmaLayout l;
+  l.ring = 0;
+  l.xs = uint32_t(kMmaWarps * kMmaSlots * piece_chunks) * kGroupChunkBytes;
+  l.zero = l.xs + uint32_t(mt) * mma_xrow_bytes(chunks);
+  l.s = l.zero + 16;
+  l.ws = l.s + 16 * 4;
+  l.tot = l.ws + BW_MAX_WS * 4;
+  l.bars = l.tot + uint32_t(k) * 16 * 8 * 4;
+  l.total = l.bars + uint32_t(kMmaWarps * kMmaSlots * 8);
+  return l;
+}
+
+// One launch: tokens [0, rows) (rows <= MT) of the activations at g.x, all
+// N outputs.  The split fields of `a` are set by the host (launch_tile).
+template <int MT, bool ACC>
 __global__ void __launch_bounds__(kMmaWarps * 32)
-gemv_w2a8_mma_kernel(const GemvArgs a, int rows) {
-  constexpr int MT = 8 * NT;
-  extern __shared__ __align__(16) uint8_t smem[];
-  __half *xs = reinterpret_cast<__half *>(smem);  // [2][MT][kXStride]
+pipe_mma_kernel(const PipeArgs a, const GemvArgs g, int rows) {
+  static_assert(MT == 8 || MT == 16, "token tile of 8 or 16");
+  extern __shared__ __align__(128) uint8_t smem[];
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int g = lane >> 2, t = lane & 3;
-  const int group0 = blockIdx.x * (kRowsPerCta / kGroupRows);
-  const size_t group_bytes = size_t(a.chunks) * kGroupChunkBytes;
+  const int KS = a.slot_chunks;
+  const int R = a.slots;
+  const int C = a.chunks;
+  const int k = a.groups_per_cta;
+  const uint32_t slot_bytes = uint32_t(KS) * kGroupChunkBytes;
+  const uint32_t xrow = mma_xrow_bytes(C);
+  const MmaLayout L = mma_layout(MT, C, k, KS);
+  uint8_t *ring = smem + L.ring + size_t(warp) * R * slot_bytes;
+  uint8_t *xs = smem + L.xs;
+  float *s_sm = reinterpret_cast<float *>(smem + L.s);
+  float *ws_sm = reinterpret_cast<float *>(smem + L.ws);
+  int *tot = reinterpret_cast<int *>(smem + L.tot);  // [k][16][8]
+  uint64_t *full = reinterpret_cast<uint64_t *>(smem + L.bars) + warp * R;
 
-  // The CTA's weight rows are contiguous: ask L2 for them before the wait.
-  if (threadIdx.x == 0) {
-    const int g_end = min(group0 + kRowsPerCta / kGroupRows, a.n_groups);
-    size_t len = size_t(g_end - group0) * group_bytes;
-    const uint8_t *p = a.w + size_t(group0) * group_bytes;
-    for (size_t o = 0; o < len; o += 65536)
-      prefetch_l2(p + o, uint32_t(min(len - o, size_t(65536))));
+  const int g_lo = int(blockIdx.x) * k;
+  const int n_g = max(0, min(k, a.n_groups - g_lo));
+  const int U = n_g * C;
+  const int run_lo = U * warp / kMmaWarps;
+  const int run_hi = U * (warp + 1) / kMmaWarps;
+
+  RunCursor iss;  // next piece to copy (lane 0)
+  iss.u = run_lo;
+  iss.g = run_lo / C;
+  iss.c = run_lo - iss.g * C;
+  RunCursor cur = iss;  // next piece to consume (whole warp)
+  int issued = 0;
+  auto issue_next = [&](int slot) {
+    const int len = iss.piece(KS, C, run_hi);
+    const uint32_t bytes = uint32_t(len) * kGroupChunkBytes;
+    mbar_arrive_expect_tx(&full[slot], bytes);
+    bulk_copy_g2s(ring + size_t(slot) * slot_bytes,
+                  a.w + (size_t(g_lo + iss.g) * C + iss.c) * kGroupChunkBytes,
+                  bytes, &full[slot]);
+    iss.advance(len, C);
+    ++issued;
+  };
+  if (lane == 0) {
+    for (int s = 0; s < R; ++s) mbar_init(&full[s], 1);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    // The weights are static once written: requested before the wait.
+    for (int s = 0; s < R && iss.u < run_hi; ++s) issue_next(s);
   }
+  for (int t = threadIdx.x; t < n_g * 16 * 8; t += blockDim.x) tot[t] = 0;
+  if (threadIdx.x < 4)
+    reinterpret_cast<uint32_t *>(smem + L.zero)[threadIdx.x] = 0u;
   pdl_wait();
+
+  // Scales, then the token tile as fp16 (zero past K and past `rows`); all
+  // loads of a batch are issued before its stores (issue is in order).
+  const float sv = (!ACC && int(threadIdx.x) < rows) ? g.s[threadIdx.x] : 0.0f;
+  const float wv = (!ACC && int(threadIdx.x) < g.seg.n_ws)
+                       ? __bfloat162float(g.ws[threadIdx.x])
+                       : 0.0f;
+  if (g.vec_x) {
+    // 16-byte rows: one 16-byte vector of each of the MT rows per thread
+    // and step, all MT loads in flight before the first store.
+    const int vecs = C * 4;  // 16-byte vectors per row
+    for (int w = threadIdx.x; w < vecs; w += blockDim.x) {
+      uint4 v[MT];
+#pragma unroll
+      for (int m = 0; m < MT; ++m)
+        v[m] = (m < rows && 16 * w < g.K)
+                   ? __ldg(reinterpret_cast<const uint4 *>(
+                               g.x + size_t(m) * g.x_ld) + w)
+                   : make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+      for (int m = 0; m < MT; ++m) {
+        // zero activations stay zero: fp16(1024 + 128) - 1152 = 0
+        const uint2 h0 = int8x4_to_f16(v[m].x), h1 = int8x4_to_f16(v[m].y);
+        const uint2 h2 = int8x4_to_f16(v[m].z), h3 = int8x4_to_f16(v[m].w);
+        uint4 *dst = reinterpret_cast<uint4 *>(xs + m * xrow + w * 32);
+        dst[0] = make_uint4(h0.x, h0.y, h1.x, h1.y);
+        dst[1] = make_uint4(h2.x, h2.y, h3.x, h3.y);
+      }
+    }
+  } else {
+    constexpr int kBatch = 8;
+    const int words = C * 16;  // 4 int8 per word
+    const int total = MT * words;
+    for (int i0 = threadIdx.x; i0 < total; i0 += kBatch * blockDim.x) {
+      uint32_t v[kBatch];
+#pragma unroll
+      for (int b = 0; b < kBatch; ++b) {
+        const int i = i0 + b * blockDim.x;
+        const int m = i / words, w = i - m * words;
+        v[b] = (i < total && m < rows && 4 * w < g.K)
+                   ? __ldg(reinterpret_cast<const unsigned int *>(
+                               g.x + size_t(m) * g.x_ld) + w)
+                   : 0x00000000u;
+      }
+#pragma unroll
+      for (int b = 0; b < kBatch; ++b) {
+        const int i = i0 + b * blockDim.x;
+        if (i < total) {
+          const int m = i / words, w = i - m * words;
+          *reinterpret_cast<uint2 *>(xs + m * xrow + w * 8) =
+              int8x4_to_f16(v[b]);
+        }
+      }
+    }
+  }
+  if (!ACC && int(threadIdx.x) < rows) s_sm[threadIdx.x] = sv;
+  if (threadIdx.x < BW_MAX_WS) ws_sm[threadIdx.x] = wv;
+  __syncthreads();  // tile staged, totals zeroed, barriers set up
   pdl_trigger();
 
-  const int ga = group0 + 2 * warp;  // groups of rows g (ga) and g + 8 (gb)
-  const bool live_a = ga < a.n_groups;
-  const bool live_b = ga + 1 < a.n_groups;
-  const uint8_t *wa = a.w + size_t(ga) * group_bytes + g * kChunkBytes;
-  const uint8_t *wb = wa + group_bytes;
-  const int shift = 16 * (t & 1) + 2 * (t >> 1);
-
-  float acc[NT][4];
+  const int gq = lane >> 2, tq = lane & 3;  // fragment row / column pair
+  const int shift = 16 * (tq & 1) + 2 * (tq >> 1);
+  // ldmatrix.x4 row address of this lane: matrix lane/8 is (tokens 0-7 |
+  // 8-15) x (k 0-7 | 8-15); tokens past MT read the zero block (no advance).
+  const int a_tok = ((lane >> 3) & 1) * 8 + (lane & 7);
+  const bool a_live = a_tok < MT;
+  const uint32_t a_base =
+      a_live ? smem_addr(xs + a_tok * xrow + ((lane >> 4) * 8) * 2)
+             : smem_addr(smem + L.zero);
+  const uint32_t a_step = a_live ? 2u : 0u;  // bytes per k
+  // One accumulator set per 16-k step of a chunk: four independent MMA
+  // chains instead of one (each MMA waits for the previous one on the same
+  // accumulators).  Each set holds an exact integer below 2^21.
+  float d[4][4];
 #pragma unroll
-  for (int j = 0; j < NT; ++j)
+  for (int w4 = 0; w4 < 4; ++w4)
 #pragma unroll
-    for (int i = 0; i < 4; ++i) acc[j][i] = 0.0f;
-
-  const int kpad = a.chunks * kChunkWeights;
-  const int n_slices = (kpad + kSlice - 1) / kSlice;
-  stage_x<NT>(a, rows, 0, xs);
-  __syncthreads();
-
-  for (int sl = 0; sl < n_slices; ++sl) {
-    __half *cur = xs + (sl & 1) * (MT * kXStride);
-    // Weights of this slice: 4 chunks (16 k-steps) of rows g and g + 8.
-    uint4 wra[kSlice / 64], wrb[kSlice / 64];
-#pragma unroll
-    for (int c = 0; c < kSlice / 64; ++c) {
-      const int j = sl * (kSlice / 64) + c;
-      const bool live = j < a.chunks;
-      wra[c] = (live && live_a) ? ld_weights16(wa + size_t(j) * kGroupChunkBytes)
-                                : make_uint4(0x55555555u, 0x55555555u,
-                                             0x55555555u, 0x55555555u);
-      wrb[c] = (live && live_b) ? ld_weights16(wb + size_t(j) * kGroupChunkBytes)
-                                : make_uint4(0x55555555u, 0x55555555u,
-                                             0x55555555u, 0x55555555u);
+    for (int e = 0; e < 4; ++e) d[w4][e] = 0.0f;
+  bool ok = true;
+  int consumed = 0, slot = 0;
+  uint32_t phase = 0;
+  while (cur.u < run_hi) {
+    if (!__all_sync(0xffffffffu, mbar_wait(&full[slot], phase))) {
+      ok = false;
+      break;
     }
-    if (sl + 1 < n_slices)
-      stage_x<NT>(a, rows, (sl + 1) * kSlice,
-                  xs + ((sl + 1) & 1) * (MT * kXStride));
-
-#pragma unroll
-    for (int c = 0; c < kSlice / 64; ++c) {
-      const uint32_t wda[4] = {wra[c].x, wra[c].y, wra[c].z, wra[c].w};
-      const uint32_t wdb[4] = {wrb[c].x, wrb[c].y, wrb[c].z, wrb[c].w};
+    const int len = cur.piece(KS, C, run_hi);
+    const uint8_t *wp = ring + size_t(slot) * slot_bytes + gq * kChunkBytes;
+    uint32_t aa = a_base + a_step * uint32_t(cur.c * kChunkWeights);
+#pragma unroll 2
+    for (int j = 0; j < len; ++j) {
+      const uint4 wv = *reinterpret_cast<const uint4 *>(wp + j * kGroupChunkBytes);
+      const uint32_t wd[4] = {wv.x, wv.y, wv.z, wv.w};
 #pragma unroll
       for (int w4 = 0; w4 < 4; ++w4) {
-        const uint32_t ha = wda[w4] >> shift;
-        const uint32_t hb = wdb[w4] >> shift;
+        const uint32_t h = wd[w4] >> shift;
+        const uint32_t b0 = decode_pair_hi(h << 4);  // k 2t, 2t+1
+        const uint32_t b1 = decode_pair_hi(h);       // k 2t+8, 2t+9
         uint32_t af[4];
-        af[0] = decode_pair(ha & 0x0303u);         // row g,   k 2t, 2t+1
-        af[1] = decode_pair(hb & 0x0303u);         // row g+8, k 2t, 2t+1
-        af[2] = decode_pair((ha >> 4) & 0x0303u);  // row g,   k 2t+8, 2t+9
-        af[3] = decode_pair((hb >> 4) & 0x0303u);  // row g+8, k 2t+8, 2t+9
-        const int kk = c * 64 + w4 * 16;  // k offset inside the slice
+        ldmatrix_x4(af, aa + a_step * uint32_t(16 * w4));
+        mma16816(d[w4], af, b0, b1);
+      }
+      aa += a_step * uint32_t(kChunkWeights);
+    }
+    __syncwarp();
+    if (lane == 0 && iss.u < run_hi) {  // piece consumed + R: this slot
+      fence_proxy_async_smem();
+      issue_next(slot);
+    }
+    const int gl = cur.g;
+    cur.advance(len, C);
+    ++consumed;
+    if (cur.c == 0 || cur.u == run_hi) {  // row group or run finished
+      // D: [0..1] = token gq, rows 2tq, 2tq+1; [2..3] = token gq + 8.
+      int v[4];
 #pragma unroll
-        for (int j = 0; j < NT; ++j) {
-          const __half *xr = cur + (8 * j + g) * kXStride + kk + 2 * t;
-          const uint32_t b0 = *reinterpret_cast<const uint32_t *>(xr);
-          const uint32_t b1 = *reinterpret_cast<const uint32_t *>(xr + 8);
-          mma16816(acc[j], af, b0, b1);
-        }
+      for (int e = 0; e < 4; ++e) {
+        v[e] = __float2int_rn(d[0][e]) + __float2int_rn(d[1][e]) +
+               __float2int_rn(d[2][e]) + __float2int_rn(d[3][e]);
+#pragma unroll
+        for (int w4 = 0; w4 < 4; ++w4) d[w4][e] = 0.0f;
+      }
+      int *tg = tot + gl * 16 * 8;
+      if (gq < MT) {
+        atomicAdd(&tg[gq * 8 + 2 * tq], v[0]);
+        atomicAdd(&tg[gq * 8 + 2 * tq + 1], v[1]);
+      }
+      if (gq + 8 < MT) {
+        atomicAdd(&tg[(gq + 8) * 8 + 2 * tq], v[2]);
+        atomicAdd(&tg[(gq + 8) * 8 + 2 * tq + 1], v[3]);
       }
     }
-    __syncthreads();
+    if (++slot == R) {
+      slot = 0;
+      phase ^= 1u;
+    }
   }
+  if (!ok && lane == 0) {
+    atomicOr(a.err, 4u);
+    for (int i = consumed; i < issued; ++i)
+      if (!mbar_wait(&full[i % R], uint32_t(i / R) & 1u)) atomicOr(a.err, 2u);
+  }
+  __syncthreads();  // every partial sum is in `tot`
 
-  // D fragment: acc[j][0..1] = rows g, tokens 8j + 2t (+1);
-  //             acc[j][2..3] = row g + 8, same tokens.
+  // Outputs: 8 consecutive rows of one token per 8 threads.
+  for (int t = threadIdx.x; t < n_g * MT * 8; t += blockDim.x) {
+    const int rr = t & 7, m = (t >> 3) % MT, gl = (t >> 3) / MT;
+    const int n = (g_lo + gl) * kGroupRows + rr;
+    if (m >= rows || n >= g.N) continue;
+    const int total = tot[(gl * 16 + m) * 8 + rr];
+    if (ACC) {
+      static_cast<int *>(g.out)[size_t(m) * g.out_ld + n] = total;
+    } else {
+      int sg = 0;
 #pragma unroll
-  for (int half = 0; half < 2; ++half) {
-    const int n = (ga + half) * kGroupRows + g;
-    if (n >= a.N) continue;
-    int seg = 0;
-#pragma unroll
-    for (int i = 1; i < BW_MAX_WS; ++i)
-      if (i < a.seg.n_ws && n >= a.seg.bounds[i]) seg = i;
-    const float wsv = ACC_OUT ? 0.0f : __bfloat162float(a.ws[seg]);
-#pragma unroll
-    for (int j = 0; j < NT; ++j) {
-#pragma unroll
-      for (int e = 0; e < 2; ++e) {
-        const int m = 8 * j + 2 * t + e;
-        if (m >= rows) continue;
-        const int total = __float2int_rn(acc[j][2 * half + e]);
-        if (ACC_OUT) {
-          static_cast<int *>(a.out)[size_t(m) * a.out_ld + n] = total;
-        } else {
-          const float scaled = static_cast<float>(total) / a.s[m];
-          static_cast<__nv_bfloat16 *>(a.out)[size_t(m) * a.out_ld + n] =
-              __float2bfloat16_rn(scaled * wsv);
-        }
-      }
+      for (int i = 1; i < BW_MAX_WS; ++i)
+        if (i < g.seg.n_ws && n >= g.seg.bounds[i]) sg = i;
+      const float scaled = static_cast<float>(total) / s_sm[m];
+      static_cast<__nv_bfloat16 *>(g.out)[size_t(m) * g.out_ld + n] =
+          __float2bfloat16_rn(scaled * ws_sm[sg]);
     }
   }
 }
 
-template <int NT, bool ACC>
-cudaError_t launch_nt(const GemvArgs &a, int rows, cudaStream_t stream) {
-  const size_t smem = size_t(2) * (8 * NT) * kXStride * sizeof(__half);
+constexpr int kMmaMaxGroupsPerCta = 32;  // row totals: 16 KB at most
+constexpr uint32_t kSmemLimit = 227u * 1024u;
+
+// Token tile and piece size for K: 16 tokens if the fp16 tile fits beside
+// a ring of 4 KB (else 2 KB) pieces, else 8 tokens likewise; false if
+// neither fits.
+bool mma_config(int K, int *mt, int *piece) {
+  if (K > kMmaMaxK) return false;
+  const int chunks = chunks_per_row(K);
+  for (int t : {16, 8})
+    for (int p : {kMmaPieceChunks, kMmaPieceChunks / 2})
+      if (mma_layout(t, chunks, kMmaMaxGroupsPerCta, p).total <= kSmemLimit) {
+        *mt = t;
+        *piece = p;
+        return true;
+      }
+  return false;
+}
+
+template <int MT, bool ACC>
+cudaError_t launch_tile(const GemvArgs &g, int rows, int piece,
+                        cudaStream_t stream) {
   static bool configured[64];
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return e;
-  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-  if (!configured[dev]) {
-    e = cudaFuncSetAttribute(gemv_w2a8_mma_kernel<NT, ACC>,
-                             cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             int(smem));
+  auto kernel = pipe_mma_kernel<MT, ACC>;
+  PipeArgs a{};
+  a.w = g.w;
+  a.N = g.N;
+  a.chunks = g.chunks;
+  a.n_groups = g.n_groups;
+  a.slots = kMmaSlots;
+  a.slot_chunks = piece;
+  a.err = device_error_word();
+  if (!a.err) return cudaErrorInvalidSymbol;
+  // k groups per CTA from the residency, as for the M = 1 kernel.
+  int64_t k = 1, resident = 0;
+  for (int pass = 0; pass < 2; ++pass) {
+    cudaError_t e = resident_ctas(
+        kernel, configured, kMmaWarps * 32,
+        mma_layout(MT, a.chunks, int(k), a.slot_chunks).total, &resident);
     if (e != cudaSuccess) return e;
-    configured[dev] = true;
+    k = (a.n_groups + resident - 1) / resident;
+    if (k > kMmaMaxGroupsPerCta) k = kMmaMaxGroupsPerCta;
+    if (k < 1) k = 1;
   }
+  const int64_t grid = (a.n_groups + k - 1) / k;
+  const int64_t run = (k * a.chunks + kMmaWarps - 1) / kMmaWarps;
+  if (run < a.slot_chunks) a.slot_chunks = int(run < 1 ? 1 : run);
+  a.groups_per_cta = int(k);
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((a.n_groups * kGroupRows + kRowsPerCta - 1) / kRowsPerCta);
+  cfg.gridDim = dim3(unsigned(grid > 0 ? grid : 1));
   cfg.blockDim = dim3(kMmaWarps * 32);
-  cfg.dynamicSmemBytes = smem;
+  cfg.dynamicSmemBytes =
+      mma_layout(MT, a.chunks, int(k), a.slot_chunks).total;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, gemv_w2a8_mma_kernel<NT, ACC>, a, rows);
+  return cudaLaunchKernelEx(&cfg, kernel, a, g, rows);
 }
 
 }  // namespace
 
-int mma_tile_rows(int left) {
-  return left >= 64 ? 64 : (left > 32 ? 64 : (left > 16 ? 32 : (left > 8 ? 16 : 8)));
+int mma_tile_rows(int K) {
+  int mt = 0, piece = 0;
+  return mma_config(K, &mt, &piece) ? mt : 0;
 }
 
 cudaError_t launch_gemv_mma(const GemvArgs &a, int rows, bool acc_out,
                             cudaStream_t stream) {
-  const int tile = mma_tile_rows(rows);
-  if (tile == 8)
-    return acc_out ? launch_nt<1, true>(a, rows, stream)
-                   : launch_nt<1, false>(a, rows, stream);
-  if (tile == 16)
-    return acc_out ? launch_nt<2, true>(a, rows, stream)
-                   : launch_nt<2, false>(a, rows, stream);
-  if (tile == 32)
-    return acc_out ? launch_nt<4, true>(a, rows, stream)
-                   : launch_nt<4, false>(a, rows, stream);
-  return acc_out ? launch_nt<8, true>(a, rows, stream)
-                 : launch_nt<8, false>(a, rows, stream);
+  int mt = 0, piece = 0;
+  if (!mma_config(a.K, &mt, &piece) || rows < 1 || rows > mt)
+    return cudaErrorInvalidValue;
+  if (mt == 16)
+    return acc_out ? launch_tile<16, true>(a, rows, piece, stream)
+                   : launch_tile<16, false>(a, rows, piece, stream);
+  return acc_out ? launch_tile<8, true>(a, rows, piece, stream)
+                 : launch_tile<8, false>(a, rows, piece, stream);
 }
 
 }  // namespace bw

@@ -66,10 +66,12 @@ cudaError_t launch_selftest_wait(cudaStream_t stream);
 // Reads and clears the device error word (synchronises `stream`).
 cudaError_t read_device_error(cudaStream_t stream, unsigned int *bits);
 
-// Tensor-core GEMV for batched activations (bw_gemv_mma.cu): one launch per
-// tile of up to 64 activation rows (`rows` valid rows at args.x).
+// Tensor-core GEMV for batched activations (bw_gemv_mma.cu): one launch
+// per tile of at most mma_tile_rows(K) activation rows (`rows` valid rows
+// at args.x); mma_tile_rows is 0 where the staged tile does not fit.
 constexpr int kMmaMinRows = 8;      // M at or above this uses tensor cores
 constexpr int kMmaMaxK = 16384;     // fp32 partial sums stay below 2^21
+int mma_tile_rows(int K);
 cudaError_t launch_gemv_mma(const GemvArgs &args, int rows, bool acc_out,
                             cudaStream_t stream);
 
