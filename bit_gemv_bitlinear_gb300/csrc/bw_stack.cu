@@ -50,9 +50,23 @@ constexpr int kMaxGlueK = 32 * kPrologueThreads;  // 8192: V <= 32 per thread
 constexpr int kMaxGroup = 8;          // query heads per KV head unrolled
 constexpr int kPartialsPerThread = 2;  // partials loaded at once: 512 per CTA
 
-__device__ __forceinline__ int8_t quant1(float x, float scale) {
-  return static_cast<int8_t>(
-      static_cast<int>(fminf(fmaxf(rintf(x * scale), -128.0f), 127.0f)));
+// clamp(rint(x * scale), -128, 127): fp32 product, round to nearest even.
+__device__ __forceinline__ int quant1(float x, float scale) {
+  return max(-128, min(127, __float2int_rn(x * scale)));
+}
+
+__device__ __forceinline__ uint32_t byte_perm(uint32_t a, uint32_t b,
+                                              uint32_t sel) {
+  uint32_t d;
+  asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(sel));
+  return d;
+}
+
+// The low bytes of four int32 codes, packed in order into one word.
+__device__ __forceinline__ uint32_t pack4(int a, int b, int c, int d) {
+  const uint32_t ab = byte_perm(uint32_t(a), uint32_t(b), 0x0040u);
+  const uint32_t cd = byte_perm(uint32_t(c), uint32_t(d), 0x0040u);
+  return byte_perm(ab, cd, 0x5410u);
 }
 
 // Prologue of the first GEMV of a step (h comes from the caller, so no
@@ -119,10 +133,10 @@ struct NormQuantH {
     for (int i = 0; i < V; ++i) {
       const int k = tid + i * kPrologueThreads;
       if (k < K) {
-        const int8_t qv = quant1(v[i], scale);
-        xs[k] = qv;
+        const int qv = quant1(v[i], scale);
+        xs[k] = int8_t(qv);
         p += qv;
-        if (tr) trace_q[k] = qv;
+        if (tr) trace_q[k] = int8_t(qv);
       }
     }
     for (int k = K + tid; k < chunks * kChunkWeights; k += kPrologueThreads)
@@ -212,15 +226,15 @@ struct NormQuantP {
     for (int i = 0; i < V4; ++i) {
       const int g = tid + i * kPrologueThreads;
       if (g < groups) {
-        const float e[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
-        const float f[4] = {gm[i].x, gm[i].y, gm[i].z, gm[i].w};
-        uint32_t word = 0;
+        const uint32_t word =
+            pack4(quant1(__fmul_rn(__fmul_rn(v[i].x, gm[i].x), r), scale),
+                  quant1(__fmul_rn(__fmul_rn(v[i].y, gm[i].y), r), scale),
+                  quant1(__fmul_rn(__fmul_rn(v[i].z, gm[i].z), r), scale),
+                  quant1(__fmul_rn(__fmul_rn(v[i].w, gm[i].w), r), scale));
+        if (tr) {
 #pragma unroll
-        for (int b = 0; b < 4; ++b) {
-          const int8_t qv =
-              quant1(__fmul_rn(__fmul_rn(e[b], f[b]), r), scale);
-          word |= uint32_t(uint8_t(qv)) << (8 * b);
-          if (tr) trace_q[4 * g + b] = qv;
+          for (int b = 0; b < 4; ++b)
+            trace_q[4 * g + b] = int8_t(word >> (8 * b));
         }
         xw[g] = word;
         p = dp4a_us(0x01010101u, word, p);
