@@ -157,16 +157,16 @@ struct EpiOut {
           __float2bfloat16_rn(v);
     }
   }
-  __device__ __forceinline__ float2 prefetch(const PipeArgs &, int,
+  __device__ __forceinline__ float4 prefetch(const PipeArgs &, int,
                                              int) const {
-    return make_float2(0.0f, 0.0f);
+    return make_float4(0.0f, 0.0f, 0.0f, 0.0f);
   }
   template <int MT>
   __device__ __forceinline__ void finish(const PipeArgs &a, const int *tot,
                                          const int (&sx)[MT], int g_lo,
                                          int n_g, const float *s_sm,
                                          const float *ws_sm, float *red,
-                                         float2 pre) const {
+                                         float4 pre) const {
     (void)red;
     (void)pre;
     for (int t = threadIdx.x; t < n_g * 8; t += blockDim.x) {

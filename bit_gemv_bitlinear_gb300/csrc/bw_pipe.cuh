@@ -24,14 +24,15 @@
 //   scale_value() returns, for thread t < BW_MAX_WS, the t-th weight scale
 //   (fp32) that finish() finds in ws_sm[t]; it is loaded before the
 //   prologue and stored after it, so the two loads overlap.
-//     __device__ float2 prefetch(const PipeArgs &a, int g_lo, int n_g) const;
+//     __device__ float4 prefetch(const PipeArgs &a, int g_lo, int n_g) const;
 //     template <int MT> __device__ void finish(const PipeArgs &a,
 //         const int *tot, const int (&sx)[MT], int g_lo, int n_g,
 //         const float *s_sm, const float *ws_sm, float *red,
-//         float2 pre) const;
-//   prefetch() runs right after the dependency wait; whatever it returns
-//   reaches finish() of the same thread as `pre` (e.g. a value of the
-//   thread's first output row, loaded early).
+//         float4 pre) const;
+//   prefetch() runs right after the dependency wait, before the prologue;
+//   whatever it returns reaches finish() of the same thread as `pre` (e.g.
+//   a value of the thread's first output row, loaded early).  Issuing it
+//   after the prologue measured 1 % slower on the stack.
 //   finish() is called by every thread once the CTA's row totals are
 //   complete: the exact int32 dot product of output n = 8 G + r (G =
 //   phys_group(a, g_lo + gl)), row m, is tot[(gl MT + m) 8 + r] - sx[m].
@@ -386,7 +387,7 @@ pipe_gemv_kernel(const PipeArgs a, const Pro pro, const Epi epi) {
   pdl_wait();
 
   const float wsv = epi.scale_value();
-  const float2 pre = epi.prefetch(a, g_lo, n_g);
+  const float4 pre = epi.prefetch(a, g_lo, n_g);
   int part[MT];
   const StageCtx sc{xs, xrow, C, s_sm, red};
   pro.template stage<MT>(pro_pre, sc, part);

@@ -279,16 +279,30 @@ struct EpiQKV {
     return int(threadIdx.x) < seg.n_ws ? __bfloat162float(ws[threadIdx.x])
                                        : 0.0f;
   }
-  __device__ __forceinline__ float2 prefetch(const PipeArgs &, int,
-                                             int) const {
-    return make_float2(0.0f, 0.0f);
+  // The gains of the (up to 4) query-head positions of the thread's first
+  // row, if it is a value row: static, so loaded right after the wait.
+  __device__ __forceinline__ float4 prefetch(const PipeArgs &a, int g_lo,
+                                             int n_g) const {
+    const int t = threadIdx.x;
+    const int n = (g_lo + (t >> 3)) * kGroupRows + (t & 7);
+    float4 p = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+    if (t < n_g * 8 && n < a.N && n >= v_off && group <= 4) {
+      const int j = n - v_off;
+      const int kv = j / hd, d = j - kv * hd;
+      const float *gp = gamma_next + kv * group * hd + d;
+      p.x = gp[0];
+      if (group > 1) p.y = gp[hd];
+      if (group > 2) p.z = gp[2 * hd];
+      if (group > 3) p.w = gp[3 * hd];
+    }
+    return p;
   }
   template <int MT>
   __device__ __forceinline__ void finish(const PipeArgs &a, const int *tot,
                                          const int (&sx)[MT], int g_lo,
                                          int n_g, const float *s_sm,
                                          const float *ws_sm, float *red,
-                                         float2) const {
+                                         float4 pre) const {
     float ss = 0.0f, mx = 0.0f;
     for (int t = threadIdx.x; t < n_g * 8; t += blockDim.x) {
       const int gl = t >> 3, rr = t & 7;
@@ -306,10 +320,17 @@ struct EpiQKV {
         const int kv = j / hd, d = j - kv * hd;
         const float yf = __bfloat162float(yv);
         const int base = kv * group * hd + d;  // position of head kv group
-        float gv[kMaxGroup];  // gains loaded together
+        // gains: prefetched for the thread's first row, else loaded together
+        const bool first = t == int(threadIdx.x) && group <= 4;
+        const float pv[4] = {pre.x, pre.y, pre.z, pre.w};
+        float gv[kMaxGroup];
 #pragma unroll
-        for (int u = 0; u < kMaxGroup; ++u)
-          gv[u] = u < group ? gamma_next[base + u * hd] : 0.0f;
+        for (int u = 0; u < kMaxGroup; ++u) {
+          if (first && u < 4)
+            gv[u] = pv[u];
+          else
+            gv[u] = u < group ? gamma_next[base + u * hd] : 0.0f;
+        }
 #pragma unroll
         for (int u = 0; u < kMaxGroup; ++u) {
           if (u < group) {
@@ -343,19 +364,19 @@ struct EpiResid {
   __device__ __forceinline__ float scale_value() const {
     return threadIdx.x == 0 ? __bfloat162float(ws[0]) : 0.0f;
   }
-  __device__ __forceinline__ float2 prefetch(const PipeArgs &a, int g_lo,
+  __device__ __forceinline__ float4 prefetch(const PipeArgs &a, int g_lo,
                                              int n_g) const {
     const int t = threadIdx.x;
     const int n = (g_lo + (t >> 3)) * kGroupRows + (t & 7);
-    if (t >= n_g * 8 || n >= a.N) return make_float2(0.0f, 0.0f);
-    return make_float2(h[n], gamma_next ? gamma_next[n] : 0.0f);
+    if (t >= n_g * 8 || n >= a.N) return make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+    return make_float4(h[n], gamma_next ? gamma_next[n] : 0.0f, 0.0f, 0.0f);
   }
   template <int MT>
   __device__ __forceinline__ void finish(const PipeArgs &a, const int *tot,
                                          const int (&sx)[MT], int g_lo,
                                          int n_g, const float *s_sm,
                                          const float *ws_sm, float *red,
-                                         float2 pre) const {
+                                         float4 pre) const {
     float ss = 0.0f, mx = 0.0f;
     for (int t = threadIdx.x; t < n_g * 8; t += blockDim.x) {
       const int gl = t >> 3, rr = t & 7;
@@ -392,19 +413,19 @@ struct EpiGate {
   __device__ __forceinline__ float scale_value() const {
     return threadIdx.x < 2 ? __bfloat162float(ws[threadIdx.x]) : 0.0f;
   }
-  __device__ __forceinline__ float2 prefetch(const PipeArgs &, int g_lo,
+  __device__ __forceinline__ float4 prefetch(const PipeArgs &, int g_lo,
                                              int n_g) const {
     const int t = threadIdx.x;
-    if (t >= (n_g >> 1) * 8) return make_float2(0.0f, 0.0f);
+    if (t >= (n_g >> 1) * 8) return make_float4(0.0f, 0.0f, 0.0f, 0.0f);
     const int f = ((g_lo >> 1) + (t >> 3)) * kGroupRows + (t & 7);
-    return make_float2(gamma_next[f], 0.0f);
+    return make_float4(gamma_next[f], 0.0f, 0.0f, 0.0f);
   }
   template <int MT>
   __device__ __forceinline__ void finish(const PipeArgs &a, const int *tot,
                                          const int (&sx)[MT], int g_lo,
                                          int n_g, const float *s_sm,
                                          const float *ws_sm, float *red,
-                                         float2 pre) const {
+                                         float4 pre) const {
     (void)a;
     float ss = 0.0f, mx = 0.0f;
     // g_lo and n_g are even: the CTA holds whole (gate, up) pairs.
