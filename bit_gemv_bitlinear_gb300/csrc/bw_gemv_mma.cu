@@ -176,6 +176,7 @@ pipe_mma_kernel(const PipeArgs a, const GemvArgs g, int rows) {
   if (threadIdx.x < 4)
     reinterpret_cast<uint32_t *>(smem + L.zero)[threadIdx.x] = 0u;
   pdl_wait();
+  pdl_trigger();  // as in the pipe kernel: one launch of lookahead
 
   // Scales, then the token tile as fp16 (zero past K and past `rows`); all
   // loads of a batch are issued before its stores (issue is in order).
@@ -234,7 +235,6 @@ pipe_mma_kernel(const PipeArgs a, const GemvArgs g, int rows) {
   if (!ACC && int(threadIdx.x) < rows) s_sm[threadIdx.x] = sv;
   if (threadIdx.x < BW_MAX_WS) ws_sm[threadIdx.x] = wv;
   __syncthreads();  // tile staged, totals zeroed, barriers set up
-  pdl_trigger();
 
   const int gq = lane >> 2, tq = lane & 3;  // fragment row / column pair
   const int shift = 16 * (tq & 1) + 2 * (tq >> 1);
