@@ -263,7 +263,7 @@ struct PipeArgs {
   int chunks;           // C = ceil(K / 64)
   int n_groups;         // ceil(N / 8)
   int slot_chunks;      // chunks per piece (at most)
-  int slots;            // ring slots per warp
+  int slots;            // ring slots per warp (caller's choice; 0: 2)
   int groups_per_cta;   // k
   int pair_half;        // 0, or H: group order 0, H, 1, H + 1, ... (2H groups)
   unsigned int *err;    // device error word (time-out bits)
@@ -491,15 +491,18 @@ cudaError_t resident_ctas(Kernel kernel, bool *configured, int threads,
   return cudaSuccess;
 }
 
-// Pieces of up to 4 KB, two slots per warp: 64 KB of ring per 8-warp CTA,
-// about three CTAs per SM for K <= 8192.
+// Pieces of up to 4 KB.  Ring slots per warp are chosen by the caller
+// (PipeArgs::slots, 2 if unset): 2 slots = 64 KB of ring per 8-warp CTA,
+// about three CTAs per SM for K <= 8192; 3 slots keep more bytes in flight
+// per warp at two CTAs per SM.
 constexpr int kPipeSlotChunks = 32;
-constexpr int kPipeSlots = 2;
+constexpr int kPipeDefaultSlots = 2;
 
 // Shared memory of a launch with k groups per CTA; a launch fits while this
 // is at most 227 KB for k = kPipeMaxGroupsPerCta.
-inline uint32_t pipe_smem_bytes(int mt, int chunks, int slot_chunks, int k) {
-  return pipe_layout(mt, chunks, slot_chunks, kPipeSlots, kPipeWarps, k).total;
+inline uint32_t pipe_smem_bytes(int mt, int chunks, int slot_chunks,
+                                int slots, int k) {
+  return pipe_layout(mt, chunks, slot_chunks, slots, kPipeWarps, k).total;
 }
 
 // Launches the pipe kernel with programmatic dependent launch: k groups per
@@ -514,14 +517,15 @@ cudaError_t launch_pipe(PipeArgs a, const Pro &pro, const Epi &epi,
   static bool configured[64];
   auto kernel = pipe_gemv_kernel<MT, Pro, Epi>;
   a.slot_chunks = kPipeSlotChunks;
-  a.slots = kPipeSlots;
+  if (a.slots < 1) a.slots = kPipeDefaultSlots;
   // k from the residency at k = 1, then once more at that k (the row
   // totals grow with k).
   int64_t k = 1, resident = 0;
   for (int pass = 0; pass < 2; ++pass) {
     cudaError_t e = resident_ctas(
         kernel, configured, kPipeWarps * 32,
-        pipe_smem_bytes(MT, a.chunks, a.slot_chunks, int(k)), &resident);
+        pipe_smem_bytes(MT, a.chunks, a.slot_chunks, a.slots, int(k)),
+        &resident);
     if (e != cudaSuccess) return e;
     k = (a.n_groups + resident - 1) / resident;
     if (k > kPipeMaxGroupsPerCta) k = kPipeMaxGroupsPerCta;
@@ -536,7 +540,8 @@ cudaError_t launch_pipe(PipeArgs a, const Pro &pro, const Epi &epi,
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(unsigned(grid > 0 ? grid : 1));
   cfg.blockDim = dim3(kPipeWarps * 32);
-  cfg.dynamicSmemBytes = pipe_smem_bytes(MT, a.chunks, a.slot_chunks, int(k));
+  cfg.dynamicSmemBytes =
+      pipe_smem_bytes(MT, a.chunks, a.slot_chunks, a.slots, int(k));
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
