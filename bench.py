@@ -53,7 +53,7 @@ FALLBACK_HBM_GBS = 6800.0
 # measured with ncu (dram__bytes_read.sum + dram__bytes_write.sum, median of
 # 4 launches; profiles/bench_m1_sweep_launches.md).  Must be re-measured --
 # or set to None -- whenever the GEMV kernel changes.
-MEASURED_DRAM_BYTES = {"wqkv": 2487296, "wo": 1668224, "w13": 8877056,
+MEASURED_DRAM_BYTES = {"wqkv": 2487168, "wo": 1667840, "w13": 8876928,
                        "w2": 4457728}
 
 
