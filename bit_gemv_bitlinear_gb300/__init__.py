@@ -37,7 +37,8 @@ EXPORTS = ("bw_status_string", "bw_last_cuda_error", "bw_version",
            "bw_quant_act", "bw_repack_bytes", "bw_repack", "bw_unrepack",
            "bw_gemv_w2a8", "bw_gemv_w2a8_acc", "bw_repack_noalloc",
            "bw_device_error", "bw_stack_create", "bw_layer_stack",
-           "bw_stack_destroy", "bw_selftest_wait_timeout")
+           "bw_stack_destroy", "bw_selftest_wait_timeout",
+           "bw_gemv_workspace_bytes")
 
 _P = ctypes.c_void_p
 _I = ctypes.c_int
@@ -47,6 +48,7 @@ _SIGS = {
     "bw_version": (_I, []),
     "bw_quant_act": (_I, [_P, _I, _I, _P, _P, _P]),
     "bw_repack_bytes": (ctypes.c_size_t, [_I, _I]),
+    "bw_gemv_workspace_bytes": (ctypes.c_size_t, [_I, _I, _I]),
     "bw_repack": (_I, [_P, _I, _I, _P, _P]),
     "bw_unrepack": (_I, [_P, _I, _I, _P, _P]),
     "bw_repack_noalloc": (_I, [_P, _I, _I, _P, _P]),
@@ -107,6 +109,11 @@ def status_string(status: int) -> str:
 
 def bw_repack_bytes(N: int, K: int) -> int:
     return int(_lib.bw_repack_bytes(N, K))
+
+
+def bw_gemv_workspace_bytes(M: int, N: int, K: int) -> int:
+    """Device scratch a GEMV of this shape needs from the caller (0)."""
+    return int(_lib.bw_gemv_workspace_bytes(M, N, K))
 
 
 def bw_quant_act(x: torch.Tensor, q: torch.Tensor | None = None,

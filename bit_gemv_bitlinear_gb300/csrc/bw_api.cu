@@ -164,6 +164,13 @@ bw_status bw_quant_act(const float *x, int M, int K, int8_t *q, float *s,
                                       reinterpret_cast<cudaStream_t>(stream)));
 }
 
+size_t bw_gemv_workspace_bytes(int M, int N, int K) {
+  (void)M;
+  (void)N;
+  (void)K;
+  return 0;  // partial sums never leave a CTA's shared memory
+}
+
 size_t bw_repack_bytes(int N, int K) {
   if (N < 1 || K < 4 || N > BW_MAX_N || K > BW_MAX_K) return 0;
   return size_t(padded_rows(N)) * size_t(chunks_per_row(K)) * kChunkBytes;

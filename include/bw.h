@@ -176,6 +176,14 @@ bw_status bw_gemv_w2a8(const int8_t *x, const uint8_t *packed, const float *s,
 bw_status bw_gemv_w2a8_acc(const int8_t *x, const uint8_t *packed, int M,
                            int N, int K, int32_t *acc, bw_stream_t stream);
 
+/* bw_gemv_workspace_bytes -- device scratch a bw_gemv_w2a8 call of this
+ * shape needs from the caller: always 0.  Every kernel reduces its partial
+ * sums in shared memory (int32 atomics per CTA) and no CTA shares a row with
+ * another, so there is no split-K workspace and no cross-CTA reduction
+ * (the pages' kernel has none either: [W2A8] §5.3 reduces inside a block).
+ * Kept so that callers that size a workspace per shape keep working. */
+size_t bw_gemv_workspace_bytes(int M, int N, int K);
+
 /* ------------------------------------------------------------------------
  * Decoder layer stack: chained M=1 W2A8 GEMVs with the fp32 glue between
  * them, in the order of the BitNet b1.58 block ([W2A8] §一 model shape,

@@ -67,6 +67,15 @@ def test_repack_bytes_matches_layout_spec(lib):
     assert lib.bw_repack_bytes(8, 65540) == 0
 
 
+def test_gemv_needs_no_workspace(lib):
+    """No GEMV path reduces across CTAs, so no shape needs scratch."""
+    lib.bw_gemv_workspace_bytes.restype = ctypes.c_size_t
+    lib.bw_gemv_workspace_bytes.argtypes = [ctypes.c_int] * 3
+    for M, N, K in [(1, 2560, 2560), (64, 13824, 2560), (1, 55296, 5120),
+                    (5, 17, 65536)]:
+        assert lib.bw_gemv_workspace_bytes(M, N, K) == 0
+
+
 P = ctypes.c_void_p
 
 
