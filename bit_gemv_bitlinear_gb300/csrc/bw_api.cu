@@ -71,7 +71,21 @@ bw_status gemv_common(const int8_t *x, const uint8_t *packed, const float *s,
   a.seg = seg;
   const size_t out_elem = acc_out ? sizeof(int32_t) : sizeof(bw_bf16);
 
-  // Batched activations: tensor cores, tiles of 16 (or 8) rows.
+  // Batched activations: tcgen05 tensor cores, tiles of up to 64 rows.
+  if (M >= kMmaMinRows && tc_fits(a)) {
+    for (int m0 = 0; m0 < M; m0 += kTcMaxRows) {
+      const int rows = M - m0 < kTcMaxRows ? M - m0 : kTcMaxRows;
+      a.x = x + size_t(m0) * K;
+      a.s = acc_out ? nullptr : s + m0;
+      a.out = static_cast<char *>(out) + size_t(m0) * N * out_elem;
+      cudaError_t e = launch_gemv_tc(a, rows, acc_out, stream);
+      if (e != cudaSuccess) return cuda_status(e);
+    }
+    return BW_OK;
+  }
+
+  // Otherwise (activation rows not 16-byte aligned): mma.sync tiles of 16
+  // (or 8) rows.
   const int tile = (M >= kMmaMinRows && K <= kMmaMaxK) ? mma_tile_rows(K) : 0;
   if (tile) {
     for (int m0 = 0; m0 < M; m0 += tile) {

@@ -1,5 +1,7 @@
 // bw_gemv_mma.cu -- the W2A8 product for batched activations (M >= 8) on
-// tensor cores, streamed like the M = 1 pipe kernel.
+// tensor cores (mma.sync), streamed like the M = 1 pipe kernel.  Used where
+// the activation rows are not 16-byte aligned or K % 16 != 0, which the
+// tcgen05 kernel's tiled copies need (bw_gemv_tc.cu).
 //
 // Same result as the CUDA-core GEMV: acc[m][n] = sum_k w[n][k] x[m][k]
 // exactly, then y = bf16((acc / s[m]) * ws[seg(n)]).  Source: "BitNet GPU

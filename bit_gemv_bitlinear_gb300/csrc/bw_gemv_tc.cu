@@ -1,0 +1,695 @@
+// bw_gemv_tc.cu -- the W2A8 product for batched activations on the
+// fifth-generation tensor cores (tcgen05.mma, accumulators in tensor
+// memory).
+//
+// Same result as the CUDA-core GEMV: acc[m][n] = sum_k w[n][k] x[m][k]
+// exactly, then y = bf16((acc / s[m]) * ws[seg(n)]).  Source: "BitNet GPU
+// 推理框架：从零构建 W2A8 的 2-bit 大模型 CUDA GEMV 内核", §5.3 (product and scale
+// epilogue), §4.2 (weight-scale segments); batching known tokens so that the
+// weights are read once for all of them is the bytes-per-token report's
+// "batched known tokens" item.
+//
+// One CTA owns 128 weight rows (16 row groups of the device layout) and all
+// K, for a tile of T <= 64 tokens; per 256-k stage:
+//  * one producer thread copies each stage's weights (a 2-D tensor-map box:
+//    16 row groups x 512 bytes, issued before the dependency wait since the
+//    weights are static) and tokens (T rows x 320 bytes, the 64 bytes past
+//    the stage unused) into shared-memory rings, one tiled TMA copy each;
+//  * 4 decode warps turn the 2-bit codes into fp16 and store them straight
+//    into tensor memory: thread = weight row = TMEM lane, the MMA's A operand;
+//  * 4 convert warps turn the int8 tokens into fp16 in the 128-byte-swizzled
+//    K-major layout of the MMA's B operand, and sum each token's x;
+//    (decode and convert warps come in two such sets, for the even and the
+//    odd stages);
+//  * one elected thread issues 16 tcgen05.mma (M = 128, N = T, K = 16) per
+//    stage into a 128 x T fp32 accumulator in tensor memory.
+// The decode warps then read the accumulators back (tcgen05.ld) for the
+// epilogue.
+//
+// Weight values.  fp16 bit patterns below 0x0800 are linear in the value
+// (pattern * 2^-24: the subnormals and the first normal binade), so a code
+// c = w + 1 left at bit 2 sl of a half (slot sl of the word interleave) and
+// masked, pattern c 4^sl, is the fp16 c 4^sl 2^-24 exactly: one mask per two
+// weights (plus one shift by 8 per word for the odd bytes), no table.  The
+// token of that column is scaled by 4^-sl (exact in fp16), so every product
+// is c x 2^-24, every partial sum an integer multiple of 2^-24 below 2^-2
+// (|sum| <= 2 * 128 * K <= 2^22 for K <= 16384) and fp32 accumulation exact
+// in any order; acc = 2^24 D - sum_k x (w = c - 1).
+//
+// Pair order.  Column j (0..7) of a 16-k step holds, in its low and high
+// halves, the elements e and e + 2 of the packed word with e = 4 (j & 3) +
+// (j >> 2) (byte j >> 2 and byte (j >> 2) + 2 of the word interleave, slot
+// j & 3): the step's k order is the even elements, then the odd ones.  The
+// token tile uses the same order and the column's scale 4^-(j & 3), so the
+// sum is unchanged.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_fp16.h>
+
+#include "bw_pipe.cuh"
+
+namespace bw {
+namespace {
+
+using namespace pipe;
+
+// Decode and convert warps come in two sets of 4, one for the even stages
+// and one for the odd ones: two stages in flight per role.
+constexpr int kTcSetWarps = 4;
+constexpr int kTcDecodeWarps = 2 * kTcSetWarps;                    // 0..7
+constexpr int kTcConvertWarps = 2 * kTcSetWarps;                   // 8..15
+constexpr int kTcProducerWarp = kTcDecodeWarps + kTcConvertWarps;  // 16
+constexpr int kTcMmaWarp = kTcProducerWarp + 1;                    // 17
+constexpr int kTcThreads = (kTcMmaWarp + 1) * 32;                  // 576
+constexpr int kTcGroups = 16;          // row groups per CTA: 128 rows
+constexpr int kTcStageChunks = 4;      // 256 k per stage
+constexpr int kTcWStages = 6;          // weight stages in flight
+constexpr int kTcXStages = 4;          // token stages in flight
+constexpr int kTcABStages = 3;         // fp16 operand stages (TMEM A, smem B)
+constexpr int kTcMaxTokens = 64;
+constexpr uint32_t kTcWStageBytes = kTcGroups * kTcStageChunks * kGroupChunkBytes;
+// int8 token row of a stage: 256 bytes plus 64, so that the convert warps'
+// 16-byte reads of two adjacent tokens fall in distinct bank groups.
+constexpr uint32_t kTcXRow = 320;
+constexpr uint32_t kTcTmemCols = 512;
+constexpr uint32_t kTcDCol = kTcABStages * 128;  // accumulator columns
+// One CTA per SM: the tensor-memory allocation takes all 512 columns.
+constexpr uint32_t kTcMinSmem = 120u * 1024u;
+
+// Shared-memory carve-up (offsets from a 1024-byte aligned base): weight
+// ring, B ring (1024-aligned: the swizzle pattern is taken from the address),
+// token ring, scales, token sums, TMEM address, barriers.
+struct TcLayout {
+  uint32_t w, b, x, s, ws, sx, tmem, bars, total;
+};
+
+__host__ __device__ inline TcLayout tc_layout(int T) {
+  TcLayout l;
+  l.w = 0;
+  l.b = l.w + kTcWStages * kTcWStageBytes;
+  l.x = l.b + kTcABStages * uint32_t(T) * 512u;
+  l.s = l.x + kTcXStages * uint32_t(T) * kTcXRow;
+  l.ws = l.s + kTcMaxTokens * 4;
+  l.sx = l.ws + BW_MAX_WS * 4;  // [2 sets][kTcMaxTokens]
+  l.tmem = l.sx + 2 * kTcMaxTokens * 4;
+  l.bars = l.tmem + 16;
+  l.total = l.bars + 32 * 8;
+  return l;
+}
+
+// Barrier indices.
+constexpr int kBarFullW = 0;                          // [kTcWStages]
+constexpr int kBarEmptyW = kBarFullW + kTcWStages;    // [kTcWStages]
+constexpr int kBarFullX = kBarEmptyW + kTcWStages;    // [kTcXStages]
+constexpr int kBarEmptyX = kBarFullX + kTcXStages;    // [kTcXStages]
+// A stage stored in TMEM and B stage in smem (decode + convert warps).
+constexpr int kBarFullAB = kBarEmptyX + kTcXStages;   // [kTcABStages]
+constexpr int kBarDone = kBarFullAB + kTcABStages;    // [kTcABStages]
+constexpr int kBarAcc = kBarDone + kTcABStages;       // accumulators final
+constexpr int kBarSums = kBarAcc + 1;                 // token sums stored
+static_assert(kBarSums < 32, "barrier block");
+
+// ---- tcgen05 / proxy helpers -------------------------------------------
+
+__device__ __forceinline__ void tmem_alloc(uint32_t *slot, uint32_t cols) {
+  asm volatile(
+      "tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+          smem_addr(slot)),
+      "r"(cols)
+      : "memory");
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::
+                   : "memory");
+}
+
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t cols) {
+  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(
+                   taddr),
+               "r"(cols)
+               : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+
+__device__ __forceinline__ void tc_fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+// D (tmem) (+)= A (tmem) * B (smem descriptor); M = 128, kind::f16.
+__device__ __forceinline__ void tc_mma(uint32_t d, uint32_t a, uint64_t bdesc,
+                                       uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d),
+      "r"(a), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// Arrives on `bar` once every tcgen05.mma issued so far by this thread is
+// complete.
+__device__ __forceinline__ void tc_commit(uint64_t *bar) {
+  asm volatile(
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 "
+      "[%0];" ::"r"(smem_addr(bar))
+      : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
+  asm volatile(
+      "{\n\t.reg .b64 st;\n\t"
+      "mbarrier.arrive.shared::cta.b64 st, [%0];\n\t}" ::"r"(smem_addr(bar))
+      : "memory");
+}
+
+__device__ __forceinline__ void fence_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// 2-D tiled bulk copy of one box of `map` at element coordinates (c0, c1);
+// completes `bytes` = the box size on `bar` (out-of-range elements are
+// zero-filled and still counted).
+__device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *map,
+                                            int c0, int c1, uint64_t *bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_"
+      "tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(smem_addr(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1),
+      "r"(smem_addr(bar))
+      : "memory");
+}
+
+// True in one lane of the (converged) warp: the lowest active one.
+__device__ __forceinline__ bool elect_one() {
+  uint32_t p;
+  asm volatile(
+      "{\n\t.reg .pred e;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "selp.u32 %0, 1, 0, e;\n\t}"
+      : "=r"(p));
+  return p != 0;
+}
+
+// Warp-uniform bounded wait (all lanes call it).
+__device__ __forceinline__ bool warp_wait(uint64_t *bar, uint32_t parity) {
+  return __all_sync(0xffffffffu, mbar_wait(bar, parity));
+}
+
+// Shared-memory matrix descriptor: K-major rows of 128 bytes with the
+// 128-byte swizzle, 8-row groups 1024 bytes apart.
+__device__ __forceinline__ uint64_t sw128_desc(uint32_t addr) {
+  uint64_t d = uint64_t((addr >> 4) & 0x3FFFu);
+  d |= uint64_t(1) << 16;             // leading byte offset (unused here)
+  d |= uint64_t(1024 >> 4) << 32;     // stride byte offset
+  d |= uint64_t(1) << 46;             // descriptor version
+  d |= uint64_t(2) << 61;             // 128-byte swizzle
+  return d;
+}
+
+// Instruction descriptor, kind::f16: fp16 A and B (K-major), fp32 D,
+// M = 128, N = n.
+__host__ __device__ constexpr uint32_t tc_idesc(int n) {
+  return (1u << 4) | (uint32_t(n >> 3) << 17) | (uint32_t(128 >> 4) << 24);
+}
+
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&v)[32]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
+      "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, "
+      "%17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, "
+      "%31, %32};" ::"r"(taddr),
+      "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]),
+      "r"(v[6]), "r"(v[7]), "r"(v[8]), "r"(v[9]), "r"(v[10]), "r"(v[11]),
+      "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15]), "r"(v[16]), "r"(v[17]),
+      "r"(v[18]), "r"(v[19]), "r"(v[20]), "r"(v[21]), "r"(v[22]), "r"(v[23]),
+      "r"(v[24]), "r"(v[25]), "r"(v[26]), "r"(v[27]), "r"(v[28]), "r"(v[29]),
+      "r"(v[30]), "r"(v[31])
+      : "memory");
+}
+
+__device__ __forceinline__ void tmem_wait_st() {
+  asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void tmem_ld8(uint32_t taddr, float (&v)[8]) {
+  uint32_t r[8];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0, %1, %2, %3, %4, %5, %6, "
+      "%7}, [%8];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]),
+        "=r"(r[6]), "=r"(r[7])
+      : "r"(taddr)
+      : "memory");
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+  for (int i = 0; i < 8; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t s) {
+  uint32_t d;
+  asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(s));
+  return d;
+}
+
+// One packed word (16 weights) -> 8 columns of fp16x2 (c 4^sl 2^-24), in
+// the pair order of the file header: column j = (byte b = j >> 2, slot
+// sl = j & 3), code bits 8 b + 2 sl (+16 for the high half) kept in place
+// (bytes 1 and 3 shifted down by 8).
+__device__ __forceinline__ void decode_word(uint32_t w, uint32_t *col) {
+  const uint32_t v = w >> 8;
+  col[0] = w & 0x00030003u;
+  col[1] = w & 0x000C000Cu;
+  col[2] = w & 0x00300030u;
+  col[3] = w & 0x00C000C0u;
+  col[4] = v & 0x00030003u;
+  col[5] = v & 0x000C000Cu;
+  col[6] = v & 0x00300030u;
+  col[7] = v & 0x00C000C0u;
+}
+
+__device__ __forceinline__ uint32_t hfma2(uint32_t a, uint32_t b, uint32_t c) {
+  uint32_t d;
+  asm("fma.rn.f16x2 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+  return d;
+}
+
+// Column scale 4^-r and -1152 4^-r as fp16x2 (r = slot of the column).
+__device__ __forceinline__ uint32_t col_scale(int r) {
+  return r == 0 ? 0x3C003C00u : r == 1 ? 0x34003400u : r == 2 ? 0x2C002C00u
+                                                               : 0x24002400u;
+}
+__device__ __forceinline__ uint32_t col_bias(int r) {
+  return r == 0 ? 0xE480E480u : r == 1 ? 0xDC80DC80u : r == 2 ? 0xD480D480u
+                                                               : 0xCC80CC80u;
+}
+
+
+// One launch: tokens [0, rows) (rows <= T <= 64, T a multiple of 16) of the
+// activations at g.x (16-byte aligned rows, K % 16 == 0), all N outputs; CTA
+// b owns row groups [16 b, 16 b + 16).
+template <bool ACC>
+__global__ void __launch_bounds__(kTcThreads, 1)
+tc_gemv_kernel(const __grid_constant__ CUtensorMap wmap,
+               const __grid_constant__ CUtensorMap xmap, const GemvArgs g,
+               int rows, int T, unsigned int *err) {
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t *smem = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
+  const TcLayout L = tc_layout(T);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int C = g.chunks;
+  const int n_st = (C + kTcStageChunks - 1) / kTcStageChunks;
+  const int g0 = int(blockIdx.x) * kTcGroups;
+  const int n_grp = min(kTcGroups, g.n_groups - g0);
+  uint64_t *bar = reinterpret_cast<uint64_t *>(smem + L.bars);
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + L.tmem);
+  float *s_sm = reinterpret_cast<float *>(smem + L.s);
+  float *ws_sm = reinterpret_cast<float *>(smem + L.ws);
+  int *sx_sm = reinterpret_cast<int *>(smem + L.sx);
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < kTcWStages; ++i) {
+      mbar_init(&bar[kBarFullW + i], 1);
+      mbar_init(&bar[kBarEmptyW + i], kTcSetWarps);
+    }
+    for (int i = 0; i < kTcXStages; ++i) {
+      mbar_init(&bar[kBarFullX + i], 1);
+      mbar_init(&bar[kBarEmptyX + i], kTcSetWarps);
+    }
+    for (int i = 0; i < kTcABStages; ++i) {
+      mbar_init(&bar[kBarFullAB + i], 2 * kTcSetWarps);
+      mbar_init(&bar[kBarDone + i], 1);
+    }
+    mbar_init(&bar[kBarAcc], 1);
+    mbar_init(&bar[kBarSums], kTcConvertWarps);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  if (warp == kTcMmaWarp) tmem_alloc(tmem_slot, kTcTmemCols);
+  tc_fence_before();
+  __syncthreads();  // barriers set up, tensor memory allocated
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == kTcProducerWarp) {
+    // ---- tiled copies: weight stages (static: before the wait), tokens ----
+    if (lane == 0) {
+      asm volatile("prefetch.tensormap [%0];" ::"l"(
+                       reinterpret_cast<uint64_t>(&wmap))
+                   : "memory");
+      asm volatile("prefetch.tensormap [%0];" ::"l"(
+                       reinterpret_cast<uint64_t>(&xmap))
+                   : "memory");
+    }
+    auto issue_w = [&](int s) {
+      const int slot = s % kTcWStages;
+      mbar_arrive_expect_tx(&bar[kBarFullW + slot], kTcWStageBytes);
+      tma_load_2d(smem + L.w + slot * kTcWStageBytes, &wmap,
+                  s * kTcStageChunks * (kGroupChunkBytes / 8), g0,
+                  &bar[kBarFullW + slot]);
+    };
+    auto issue_x = [&](int s) {
+      const int slot = s % kTcXStages;
+      mbar_arrive_expect_tx(&bar[kBarFullX + slot], uint32_t(T) * kTcXRow);
+      tma_load_2d(smem + L.x + slot * uint32_t(T) * kTcXRow, &xmap,
+                  s * kTcStageChunks * 16, 0, &bar[kBarFullX + slot]);
+    };
+    int sw = 0, sx = 0;
+    if (lane == 0)
+      for (; sw < kTcWStages && sw < n_st; ++sw) issue_w(sw);
+    pdl_wait();
+    pdl_trigger();
+    if (lane == 0) {
+      long long idle_since = clock64();
+      while (sw < n_st || sx < n_st) {
+        bool moved = false;
+        if (sx < n_st &&
+            (sx < kTcXStages ||
+             mbar_try_wait(&bar[kBarEmptyX + sx % kTcXStages],
+                           uint32_t(sx / kTcXStages - 1) & 1u))) {
+          issue_x(sx++);
+          moved = true;
+        }
+        if (sw < n_st &&
+            mbar_try_wait(&bar[kBarEmptyW + sw % kTcWStages],
+                          uint32_t(sw / kTcWStages - 1) & 1u)) {
+          issue_w(sw++);
+          moved = true;
+        }
+        if (moved) {
+          idle_since = clock64();
+        } else if (clock64() - idle_since > kWaitLimitCycles) {
+          atomicOr(err, 4u);
+          break;
+        }
+      }
+      // Copies still in flight land before the CTA exits (their slots' last
+      // phases; normally complete already).
+      for (int s = max(0, sw - kTcWStages); s < sw; ++s)
+        if (!mbar_wait(&bar[kBarFullW + s % kTcWStages],
+                       uint32_t(s / kTcWStages) & 1u))
+          atomicOr(err, 2u);
+      for (int s = max(0, sx - kTcXStages); s < sx; ++s)
+        if (!mbar_wait(&bar[kBarFullX + s % kTcXStages],
+                       uint32_t(s / kTcXStages) & 1u))
+          atomicOr(err, 2u);
+    }
+    __syncwarp();
+  } else if (warp == kTcMmaWarp) {
+    // ---- MMA issue: the warp runs the loop (uniform values), one elected
+    // lane issues and commits ----
+    pdl_wait();
+    pdl_trigger();
+    const uint32_t idesc = tc_idesc(T);
+    const uint32_t b_ring = smem_addr(smem + L.b);
+    const uint32_t slice16 = uint32_t(T) * 128u / 16u;  // slice, 16-byte units
+    bool ok = true;
+    for (int s = 0; s < n_st; ++s) {
+      const int ab = s % kTcABStages;
+      const uint32_t par = uint32_t(s / kTcABStages) & 1u;
+      if (!warp_wait(&bar[kBarFullAB + ab], par)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      // One base descriptor per stage; the 16 k-steps add constants to its
+      // address field (slice ks / 4 of T rows x 128 bytes, 32 bytes per step
+      // within it).
+      const int nks = 4 * min(kTcStageChunks, C - s * kTcStageChunks);
+      const uint64_t bd0 = sw128_desc(b_ring + uint32_t(ab) * uint32_t(T) * 512u);
+      const uint32_t a0 = tmem + uint32_t(ab) * 128u;
+      if (elect_one()) {
+#pragma unroll
+        for (int ks = 0; ks < kTcStageChunks * 4; ++ks) {
+          if (ks < nks)
+            tc_mma(tmem + kTcDCol, a0 + uint32_t(ks) * 8u,
+                   bd0 + uint64_t(uint32_t(ks >> 2) * slice16 + uint32_t(ks & 3) * 2u),
+                   idesc, ks > 0 ? 1u : uint32_t(s > 0));
+        }
+        tc_commit(&bar[kBarDone + ab]);
+      }
+      __syncwarp();
+    }
+    if (!ok && lane == 0) atomicOr(err, 4u);
+    if (elect_one()) tc_commit(&bar[kBarAcc]);  // also on a time-out
+    __syncwarp();
+  } else if (warp >= kTcDecodeWarps) {
+    // ---- convert warps: int8 tokens -> swizzled fp16 B, token sums ----
+    const int cw = (warp - kTcDecodeWarps) & 3;
+    const int set = (warp - kTcDecodeWarps) >> 2;
+    pdl_wait();
+    pdl_trigger();
+    {
+      const int t = threadIdx.x - kTcDecodeWarps * 32;  // 0..255
+      if (!ACC && t < rows) s_sm[t] = g.s[t];
+      if (t < BW_MAX_WS)
+        ws_sm[t] = t < g.seg.n_ws ? __bfloat162float(g.ws[t]) : 0.0f;
+    }
+    // Unit (m, gg): token m, 16 k at 16 gg of the stage.  A phase of 8
+    // lanes covers gg & 3 = 0..3 for two adjacent tokens: conflict-free
+    // reads (rows 320 bytes apart) and swizzled stores.
+    const int gg = (lane & 3) + 4 * (lane >> 3);
+    const int mpar = (lane >> 2) & 1;
+    const int units = T / 8;  // per thread and stage
+    int sum[kTcMaxTokens / 8];
+#pragma unroll
+    for (int i = 0; i < kTcMaxTokens / 8; ++i) sum[i] = 0;
+    bool ok = true;
+    for (int s = set; s < n_st && ok; s += 2) {
+      const int xs = s % kTcXStages, ab = s % kTcABStages;
+      if (!warp_wait(&bar[kBarFullX + xs], uint32_t(s / kTcXStages) & 1u)) {
+        ok = false;
+        break;
+      }
+      const int k = s * kTcStageChunks * 64 + 16 * gg;
+      const uint8_t *xsrc = smem + L.x + xs * uint32_t(T) * kTcXRow + 16 * gg;
+      uint4 v[kTcMaxTokens / 8];
+#pragma unroll
+      for (int i = 0; i < kTcMaxTokens / 8; ++i) {
+        const int m = 2 * (cw + 4 * i) + mpar;
+        v[i] = (i < units && m < rows && k < g.K)
+                   ? *reinterpret_cast<const uint4 *>(xsrc + m * kTcXRow)
+                   : make_uint4(0u, 0u, 0u, 0u);
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bar[kBarEmptyX + xs]);
+      if (s >= kTcABStages &&
+          !warp_wait(&bar[kBarDone + ab], uint32_t(s / kTcABStages - 1) & 1u)) {
+        ok = false;
+        break;
+      }
+      uint8_t *bst = smem + L.b + ab * uint32_t(T) * 512u +
+                     uint32_t(gg >> 2) * uint32_t(T) * 128u;
+#pragma unroll
+      for (int i = 0; i < kTcMaxTokens / 8; ++i) {
+        if (i < units) {
+          const int m = 2 * (cw + 4 * i) + mpar;
+          const uint32_t wv[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
+          uint32_t ev[4], od[4];
+#pragma unroll
+          for (int r = 0; r < 4; ++r) {
+            sum[i] = __dp4a(int(wv[r]), 0x01010101, sum[i]);
+            const uint32_t u = wv[r] ^ 0x80808080u;  // x + 128
+            // (fp16(1024 + u) - 1152) 4^-r = x 4^-r exactly
+            ev[r] = hfma2(prmt(u, 0x64646464u, 0x4240u), col_scale(r), col_bias(r));
+            od[r] = hfma2(prmt(u, 0x64646464u, 0x4341u), col_scale(r), col_bias(r));
+          }
+          const uint32_t phys = uint32_t(2 * (gg & 3)) ^ uint32_t(m & 7);
+          uint8_t *row = bst + m * 128;
+          *reinterpret_cast<uint4 *>(row + phys * 16) =
+              make_uint4(ev[0], ev[1], ev[2], ev[3]);
+          *reinterpret_cast<uint4 *>(row + (phys ^ 1u) * 16) =
+              make_uint4(od[0], od[1], od[2], od[3]);
+        }
+      }
+      fence_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bar[kBarFullAB + ab]);
+    }
+    if (!ok && lane == 0) atomicOr(err, 4u);
+    // Token sums: the 16 lanes of one token parity (lane bits 0, 1, 3, 4).
+#pragma unroll
+    for (int i = 0; i < kTcMaxTokens / 8; ++i) {
+      int v = sum[i];
+      v += __shfl_xor_sync(0xffffffffu, v, 1);
+      v += __shfl_xor_sync(0xffffffffu, v, 2);
+      v += __shfl_xor_sync(0xffffffffu, v, 8);
+      v += __shfl_xor_sync(0xffffffffu, v, 16);
+      const int m = 2 * (cw + 4 * i) + mpar;
+      if (i < units && (lane & ~4) == 0) sx_sm[set * kTcMaxTokens + m] = v;
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&bar[kBarSums]);
+  } else {
+    // ---- decode warps: 2-bit codes -> fp16 A in tensor memory ----
+    pdl_trigger();
+    const int q = warp & 3, h = warp >> 2;  // h: stage set, then column half
+    const int r = 32 * q + lane;  // weight row of the tile = TMEM lane
+    const uint32_t t_lane = tmem + (uint32_t(32 * q) << 16);
+    bool ok = true;
+    for (int s = h; s < n_st && ok; s += 2) {
+      const int ws = s % kTcWStages, ab = s % kTcABStages;
+      if (!warp_wait(&bar[kBarFullW + ws], uint32_t(s / kTcWStages) & 1u)) {
+        ok = false;
+        break;
+      }
+      const int nc = min(kTcStageChunks, C - s * kTcStageChunks);
+      const uint8_t *src = smem + L.w + ws * kTcWStageBytes +
+                           (r >> 3) * (kTcStageChunks * kGroupChunkBytes) +
+                           (r & 7) * kChunkBytes;
+      uint4 wq[kTcStageChunks];
+#pragma unroll
+      for (int c = 0; c < kTcStageChunks; ++c)
+        wq[c] = c < nc ? *reinterpret_cast<const uint4 *>(src + c * kGroupChunkBytes)
+                       : make_uint4(0u, 0u, 0u, 0u);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bar[kBarEmptyW + ws]);
+      if (s >= kTcABStages &&
+          !warp_wait(&bar[kBarDone + ab], uint32_t(s / kTcABStages - 1) & 1u)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+#pragma unroll
+      for (int c = 0; c < kTcStageChunks; ++c) {
+        if (c < nc) {
+          uint32_t col[32];
+          decode_word(wq[c].x, col);
+          decode_word(wq[c].y, col + 8);
+          decode_word(wq[c].z, col + 16);
+          decode_word(wq[c].w, col + 24);
+          tmem_st32(t_lane + uint32_t(ab) * 128u + uint32_t(c) * 32u, col);
+        }
+      }
+      tmem_wait_st();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bar[kBarFullAB + ab]);
+    }
+    if (!ok && lane == 0) atomicOr(err, 4u);
+
+    // ---- epilogue: accumulators -> int32 or bf16 ----
+    pdl_wait();
+    const bool acc_ready = warp_wait(&bar[kBarAcc], 0u);
+    const bool sums_ready = warp_wait(&bar[kBarSums], 0u);
+    tc_fence_after();
+    if (acc_ready && sums_ready && ok) {
+      const int n = (g0 * kGroupRows) + r;
+      int sg = 0;
+#pragma unroll
+      for (int i = 1; i < BW_MAX_WS; ++i)
+        if (i < g.seg.n_ws && n >= g.seg.bounds[i]) sg = i;
+      const float wsv = ws_sm[sg];
+      const int half = T / 2;
+      for (int j0 = h * half; j0 < (h + 1) * half; j0 += 8) {
+        float d[8];
+        tmem_ld8(t_lane + kTcDCol + uint32_t(j0), d);  // whole warp
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          const int m = j0 + e;
+          if (m >= rows || n >= g.N) continue;
+          const int total = __float2int_rn(d[e] * 16777216.0f) - sx_sm[m] -
+                            sx_sm[kTcMaxTokens + m];
+          if (ACC) {
+            static_cast<int *>(g.out)[size_t(m) * g.out_ld + n] = total;
+          } else {
+            const float scaled = static_cast<float>(total) / s_sm[m];
+            static_cast<__nv_bfloat16 *>(g.out)[size_t(m) * g.out_ld + n] =
+                __float2bfloat16_rn(scaled * wsv);
+          }
+        }
+      }
+    } else if (lane == 0) {
+      atomicOr(err, 4u);
+    }
+  }
+  tc_fence_before();
+  __syncthreads();  // every tensor-memory access is done
+  if (warp == kTcMmaWarp) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kTcTmemCols);
+  }
+}
+
+
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (!fn) {
+    void *p = nullptr;
+    cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000,
+                                         cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  }
+  return fn;
+}
+
+// Row-major 2-D tensor: d1 rows of d0 elements, rows `pitch` bytes apart;
+// boxes of b1 rows x b0 elements; out-of-range elements read as zero.
+bool encode_2d(CUtensorMap *map, CUtensorMapDataType type, const void *base,
+               uint64_t d0, uint64_t d1, uint64_t pitch, uint32_t b0,
+               uint32_t b1) {
+  PFN_cuTensorMapEncodeTiled_v12000 fn = tensor_map_encoder();
+  if (!fn) return false;
+  const cuuint64_t dims[2] = {d0, d1};
+  const cuuint64_t strides[1] = {pitch};
+  const cuuint32_t box[2] = {b0, b1};
+  const cuuint32_t elem[2] = {1, 1};
+  return fn(map, type, 2, const_cast<void *>(base), dims, strides, box, elem,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <bool ACC>
+cudaError_t launch_tc(const GemvArgs &g, int rows, int T, cudaStream_t stream) {
+  static bool configured[64];
+  auto kernel = tc_gemv_kernel<ACC>;
+  unsigned int *err = device_error_word();
+  if (!err) return cudaErrorInvalidSymbol;
+  // 1 KB of slack to align the base; at least kTcMinSmem: one CTA per SM.
+  uint32_t smem = tc_layout(T).total + 1024u;
+  if (smem < kTcMinSmem) smem = kTcMinSmem;
+  int64_t resident = 0;
+  cudaError_t e = resident_ctas(kernel, configured, kTcThreads, smem, &resident);
+  if (e != cudaSuccess) return e;
+  // Weights: per row group, C chunks of 128 bytes as 16 C uint64; a box is
+  // one stage of 16 groups.  Tokens: `rows` rows of K / 4 uint32; a box is
+  // 80 uint32 (320 bytes) of T rows (rows past `rows`, k past K: zero).
+  CUtensorMap wmap, xmap;
+  if (!encode_2d(&wmap, CU_TENSOR_MAP_DATA_TYPE_UINT64, g.w,
+                 uint64_t(g.chunks) * (kGroupChunkBytes / 8),
+                 uint64_t(g.n_groups), uint64_t(g.chunks) * kGroupChunkBytes,
+                 kTcStageChunks * (kGroupChunkBytes / 8), kTcGroups) ||
+      !encode_2d(&xmap, CU_TENSOR_MAP_DATA_TYPE_UINT32, g.x, uint64_t(g.K / 4),
+                 uint64_t(rows), uint64_t(g.x_ld), kTcXRow / 4, uint32_t(T)))
+    return cudaErrorInvalidValue;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(unsigned((g.n_groups + kTcGroups - 1) / kTcGroups));
+  cfg.blockDim = dim3(kTcThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, wmap, xmap, g, rows, T, err);
+}
+
+}  // namespace
+
+bool tc_fits(const GemvArgs &a) {
+  return a.vec_x && a.K <= kMmaMaxK &&
+         tc_layout(kTcMaxTokens).total + 1024u <= 227u * 1024u;
+}
+
+cudaError_t launch_gemv_tc(const GemvArgs &a, int rows, bool acc_out,
+                           cudaStream_t stream) {
+  if (!tc_fits(a) || rows < 1 || rows > kTcMaxRows) return cudaErrorInvalidValue;
+  const int T = (rows + 15) / 16 * 16;
+  return acc_out ? launch_tc<true>(a, rows, T, stream)
+                 : launch_tc<false>(a, rows, T, stream);
+}
+
+}  // namespace bw

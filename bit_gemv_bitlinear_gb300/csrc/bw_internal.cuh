@@ -74,6 +74,13 @@ constexpr int kMmaMaxK = 16384;     // fp32 partial sums stay below 2^21
 int mma_tile_rows(int K);
 cudaError_t launch_gemv_mma(const GemvArgs &args, int rows, bool acc_out,
                             cudaStream_t stream);
+// Tensor-core GEMV on tcgen05 (bw_gemv_tc.cu): one launch per tile of at
+// most kTcMaxRows activation rows; needs 16-byte aligned activation rows with
+// K % 16 == 0 (bulk copies) and K <= kMmaMaxK.
+constexpr int kTcMaxRows = 64;
+bool tc_fits(const GemvArgs &args);
+cudaError_t launch_gemv_tc(const GemvArgs &args, int rows, bool acc_out,
+                           cudaStream_t stream);
 
 GemvPlan plan_gemv(int mt, int N, int K, int num_sms);
 cudaError_t launch_gemv(const GemvPlan &plan, const GemvArgs &args,

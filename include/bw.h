@@ -156,9 +156,11 @@ bw_status bw_unrepack(const uint8_t *packed, int N, int K, uint8_t *canon,
  *              q|k|v projection of BitNet-2B: {0, 2560, 3200, 3840}).
  *   y          bf16 [M][N] device, 2-byte aligned (output).
  *   1 <= M <= BW_MAX_M, 1 <= N <= BW_MAX_N, 4 <= K <= BW_MAX_K, K % 4 == 0,
- *   1 <= n_ws <= BW_MAX_WS.  Activation rows are processed in tiles of
- *   4, 2 and 1 on CUDA cores (int dp4a); the weights are streamed once per
- *   tile.
+ *   1 <= n_ws <= BW_MAX_WS.  M < 8: activation rows in tiles of 4, 2 and
+ *   1 on CUDA cores (int dp4a).  M >= 8: tiles of up to 64 rows on the
+ *   tensor cores (tcgen05.mma; mma.sync where x is not 16-byte aligned or
+ *   K % 16 != 0), exact in int32 as well.  The weights are streamed once
+ *   per tile.
  * Ordering: the call is launched with programmatic dependent launch, so it
  * may start while the preceding work on `stream` is still running.  x, s,
  * ws and y are touched only after that work has completed; `packed` may be

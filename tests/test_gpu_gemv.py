@@ -247,10 +247,14 @@ def test_reproducible_and_stream_ordered(bw):
 
 @pytest.mark.parametrize("M,N,K", [
     (8, 8, 64), (9, 100, 300), (17, 1000, 1028), (33, 77, 16384),
-    (65, 513, 2560), (128, 2560, 2560), (200, 64, 68), (8, 40, 20000)])
+    (65, 513, 2560), (128, 2560, 2560), (200, 64, 68), (8, 40, 20000),
+    (24, 300, 1040), (49, 1000, 6928)])
 def test_batched_tensor_core_tiles(bw, M, N, K):
-    """M >= 8 takes the tensor-core path (token tiles of 8..64, padded);
-    K > 16384 goes back to CUDA cores.  int32 exact, bf16 within 1 ulp."""
+    """M >= 8 takes the tensor-core path: tcgen05 tiles of up to 64 tokens
+    (padded to 16) where rows are 16-byte aligned and K % 16 == 0, else
+    mma.sync tiles of 8/16; K > 16384 goes back to CUDA cores.  K = 1040 and
+    6928 end in a partly valid chunk and a one-chunk stage.  int32 exact,
+    bf16 within 1 ulp."""
     case = synth.gemv_case(M, N, K, synth.base_seed(10, M % 16),
                            uniform_x=False, bounds=[0, N // 3 + 1, N])
     q, _ = oracle.quant_act(case["xf"])
