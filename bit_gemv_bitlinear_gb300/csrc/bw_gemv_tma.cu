@@ -66,9 +66,33 @@ struct StageInt8 {
   const int8_t *x;
   const float *s;  // null in accumulator mode
   int x_ld, K, vec_x;
+  int rows;                  // activation rows of this launch
+  const void *ws;            // weight scales (null in accumulator mode)
 
-  struct Pre {};  // every input may come from the preceding kernel
-  __device__ __forceinline__ Pre pre_wait() const { return Pre{}; }
+  // Every input may come from the preceding kernel, so nothing is read
+  // before the dependency wait.  The lines of x, s and ws are only
+  // prefetched into L2 (a hint that returns no data: L2 is the point of
+  // coherence, so the loads after the wait still see the final values),
+  // one line per thread across the grid.
+  struct Pre {};
+  __device__ __forceinline__ Pre pre_wait() const {
+    const char *lo = reinterpret_cast<const char *>(x);
+    const char *hi = lo + size_t(rows - 1) * x_ld + K;  // end of the last row
+    const size_t base = reinterpret_cast<size_t>(lo) & ~size_t(127);
+    const int lines = int((reinterpret_cast<size_t>(hi) - base + 127) / 128);
+    const int stride = gridDim.x * blockDim.x;
+    for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < lines + 2;
+         i += stride) {
+      const void *p = i == lines ? static_cast<const void *>(s)
+                      : i == lines + 1
+                          ? ws
+                          : static_cast<const void *>(
+                                lo + (i == 0 ? 0 : size_t(i) * 128 -
+                                                       (reinterpret_cast<size_t>(lo) - base)));
+      if (p) asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
+    }
+    return Pre{};
+  }
 
   template <int MT>
   __device__ __forceinline__ void stage(const Pre &, const StageCtx &c,
@@ -197,7 +221,8 @@ cudaError_t launch_instance(const GemvArgs &g, cudaStream_t stream) {
   a.slots = kGemvSlots;
   a.err = device_error_word();
   if (!a.err) return cudaErrorInvalidSymbol;
-  const StageInt8 pro{g.x, ACC ? nullptr : g.s, g.x_ld, g.K, g.vec_x};
+  const StageInt8 pro{g.x, ACC ? nullptr : g.s, g.x_ld, g.K, g.vec_x, MT,
+                      ACC ? nullptr : static_cast<const void *>(g.ws)};
   const EpiOut<ACC> epi{g.out, g.out_ld, g.ws, g.seg};
   return launch_pipe<MT>(a, pro, epi, stream);
 }
