@@ -53,8 +53,8 @@ FALLBACK_HBM_GBS = 6800.0
 # measured with ncu (dram__bytes_read.sum + dram__bytes_write.sum, median of
 # 4 launches; profiles/bench_m1_sweep_launches.md).  Must be re-measured --
 # or set to None -- whenever the GEMV kernel changes.
-MEASURED_DRAM_BYTES = {"wqkv": 2487168, "wo": 1667840, "w13": 8876928,
-                       "w2": 4457728}
+MEASURED_DRAM_BYTES = {"wqkv": 2487936, "wo": 1668736, "w13": 8877824,
+                       "w2": 4458880}
 
 
 def parse_args():
@@ -67,6 +67,8 @@ def parse_args():
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-stack", action="store_true",
                    help="skip the layer-stack tok/s measurement")
+    p.add_argument("--no-batched", action="store_true",
+                   help="skip the batched M = 4/16/64 timings")
     p.add_argument("--stack", action="store_true",
                    help="only time the 30-layer decode stack (tok/s)")
     p.add_argument("--stack-layers", type=int, default=None,
@@ -388,6 +390,9 @@ def run_ours(args):
     stack_line = None
     if not args.no_stack:
         stack_line = run_stack_timing(torch, bw, dev)
+    batched_line = None
+    if rank == 0 and not args.no_batched:
+        batched_line = run_batched(torch, bw, dev, peak)
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -442,6 +447,8 @@ def run_ours(args):
         }
         if stack_line is not None:
             line["layer_stack"] = stack_line
+        if batched_line is not None:
+            line["batched"] = batched_line
         if cpu is not None:
             line["cpu_baseline"] = cpu
         print(json.dumps(line), flush=True)
@@ -623,22 +630,16 @@ def run_reference(args):
     print(json.dumps(line), flush=True)
 
 
-def run_single(args):
-    """One shape over rotating weight buffers; also the command the kernel
-    profiles are taken with."""
-    import torch
-    import bit_gemv_bitlinear_gb300 as bw
-
-    dims = [int(v) for v in args.single.split(",")]
-    N, K = dims[0], dims[1]
-    M = dims[2] if len(dims) > 2 else 1
-    dev = torch.device("cuda", 0)
-    torch.cuda.set_device(dev)
+def time_shape(torch, bw, dev, N, K, M, iters=2000, rotate=0, eager=False):
+    """Microseconds per bw_gemv_w2a8 call of one shape, back to back on one
+    stream (a CUDA graph of up to 64 calls unless `eager`), cycling through
+    enough copies of the weights that they exceed L2 (weights, tokens and
+    scales are seeded synthetic data)."""
     seed = synth.base_seed(2, 1)
     canon = synth.canonical_weights(seed, N, K)
     packed0 = bw.bw_repack(torch.from_numpy(canon).to(dev), N, K)
     wb = weight_bytes(N, K)
-    rot = args.rotate or max(2, -(-4 * 126 * 2**20 // wb))
+    rot = rotate or max(2, -(-4 * 126 * 2**20 // wb))
     rot = min(rot, max(2, (8 << 30) // max(wb, 1)))
     packed = [packed0] + [packed0.clone() for _ in range(rot - 1)]
     xf = torch.from_numpy(synth.normal_f32(seed, M * K).reshape(M, K)).to(dev)
@@ -646,7 +647,7 @@ def run_single(args):
     ws = torch.ones(1, device=dev).to(torch.bfloat16)
     y = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
     stream = torch.cuda.Stream(device=dev)
-    per_graph = max(rot, min(args.iters, 64))
+    per_graph = max(rot, min(iters, 64))
 
     def launches():
         for i in range(per_graph):
@@ -656,7 +657,7 @@ def run_single(args):
     with torch.cuda.stream(stream):
         launches()
     stream.synchronize()
-    if args.eager:
+    if eager:
         def run():
             with torch.cuda.stream(stream):
                 launches()
@@ -671,7 +672,7 @@ def run_single(args):
     for _ in range(3):
         run()
     torch.cuda.synchronize()
-    reps = max(1, args.iters // per_graph)
+    reps = max(1, iters // per_graph)
     start = torch.cuda.Event(enable_timing=True)
     end = torch.cuda.Event(enable_timing=True)
     start.record(stream)
@@ -682,11 +683,53 @@ def run_single(args):
     bw.bw_device_error(stream)
     us = start.elapsed_time(end) * 1e3 / (reps * per_graph)
     ab = algorithmic_bytes(N, K, 1) + (M - 1) * (K + 2 * N + 4)
-    print(json.dumps({"single": [N, K, M], "rotate": rot,
-                      "graph": not args.eager, "calls": reps * per_graph,
+    return {"us": us, "rotate": rot, "calls": reps * per_graph,
+            "weight_bytes": wb, "alg_bytes": ab}
+
+
+BATCHED_N, BATCHED_K, BATCHED_M = 13824, 2560, (4, 16, 64)
+
+
+def run_batched(torch, bw, dev, peak_gbs):
+    """The batched known-token GEMM (M = 4, 16, 64 at 13824 x 2560): us per
+    call, weight GB/s, and the fractions of the measured HBM copy peak and
+    of the nominal dense fp16 tensor rate (2.25 PFLOP/s) the call reaches."""
+    out = {"shape": [BATCHED_N, BATCHED_K], "per_m": {}}
+    for M in BATCHED_M:
+        t = time_shape(torch, bw, dev, BATCHED_N, BATCHED_K, M, iters=1024)
+        us = t["us"]
+        flops = 2.0 * M * BATCHED_N * BATCHED_K
+        out["per_m"][str(M)] = {
+            "us_per_call": round(us, 3),
+            "kernel": "tc_gemv_kernel (tcgen05)" if M >= 8
+                      else "gemv_w2a8_pipe_kernel (dp4a)",
+            "weight_GBps": round(t["weight_bytes"] / (us * 1e3), 1),
+            "hbm_frac": round(t["alg_bytes"] / (us * 1e3) / peak_gbs, 4),
+            "tensor_frac_nominal": round(flops / (us * 1e-6) / 2.25e15, 4),
+        }
+    return out
+
+
+def run_single(args):
+    """One shape over rotating weight buffers; also the command the kernel
+    profiles are taken with."""
+    import torch
+    import bit_gemv_bitlinear_gb300 as bw
+
+    dims = [int(v) for v in args.single.split(",")]
+    N, K = dims[0], dims[1]
+    M = dims[2] if len(dims) > 2 else 1
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    t = time_shape(torch, bw, dev, N, K, M, iters=args.iters,
+                   rotate=args.rotate, eager=args.eager)
+    us = t["us"]
+    print(json.dumps({"single": [N, K, M], "rotate": t["rotate"],
+                      "graph": not args.eager, "calls": t["calls"],
                       "us_per_call": round(us, 3),
-                      "weight_GBps": round(wb / (us * 1e3), 1),
-                      "alg_GBps": round(ab / (us * 1e3), 1)}), flush=True)
+                      "weight_GBps": round(t["weight_bytes"] / (us * 1e3), 1),
+                      "alg_GBps": round(t["alg_bytes"] / (us * 1e3), 1)}),
+          flush=True)
 
 
 def main():
