@@ -50,9 +50,12 @@ constexpr int kMaxGlueK = 32 * kPrologueThreads;  // 8192: V <= 32 per thread
 constexpr int kMaxGroup = 8;          // query heads per KV head unrolled
 constexpr int kPartialsPerThread = 2;  // partials loaded at once: 512 per CTA
 
-// clamp(rint(x * scale), -128, 127): fp32 product, round to nearest even.
+// clamp(rint(x * scale), -128, 127): fp32 product, round to nearest even,
+// one saturating convert to s8 (only the low byte of the result is used).
 __device__ __forceinline__ int quant1(float x, float scale) {
-  return max(-128, min(127, __float2int_rn(x * scale)));
+  int q;
+  asm("cvt.rni.sat.s8.f32 %0, %1;" : "=r"(q) : "f"(__fmul_rn(x, scale)));
+  return q;
 }
 
 __device__ __forceinline__ uint32_t byte_perm(uint32_t a, uint32_t b,
@@ -133,7 +136,7 @@ struct NormQuantH {
     for (int i = 0; i < V; ++i) {
       const int k = tid + i * kPrologueThreads;
       if (k < K) {
-        const int qv = quant1(v[i], scale);
+        const int qv = int8_t(quant1(v[i], scale));  // low byte, signed
         xs[k] = int8_t(qv);
         p += qv;
         if (tr) trace_q[k] = int8_t(qv);
