@@ -23,8 +23,8 @@
 //    odd stages);
 //  * one elected thread issues 16 tcgen05.mma (M = 128, N = T, K = 16) per
 //    stage into a 128 x T fp32 accumulator in tensor memory.
-// The decode warps then read the accumulators back (tcgen05.ld) for the
-// epilogue.
+// The decode and convert warps then read the accumulators back (tcgen05.ld)
+// for the epilogue.
 //
 // Weight values.  fp16 bit patterns below 0x0800 are linear in the value
 // (pattern * 2^-24: the subnormals and the first normal binade), so a code
@@ -232,18 +232,19 @@ __device__ __forceinline__ void tmem_wait_st() {
   asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
 
-__device__ __forceinline__ void tmem_ld8(uint32_t taddr, float (&v)[8]) {
-  uint32_t r[8];
+// 4 consecutive accumulator columns of this warp's 32 lanes; the load and
+// its wait are one asm statement, so no use of the values can be scheduled
+// before the wait.
+__device__ __forceinline__ void tmem_ld4(uint32_t taddr, float (&v)[4]) {
+  uint32_t r[4];
   asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0, %1, %2, %3, %4, %5, %6, "
-      "%7}, [%8];"
-      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]),
-        "=r"(r[6]), "=r"(r[7])
+      "tcgen05.ld.sync.aligned.32x32b.x4.b32 {%0, %1, %2, %3}, [%4];\n\t"
+      "tcgen05.wait::ld.sync.aligned;"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
       : "r"(taddr)
       : "memory");
-  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 #pragma unroll
-  for (int i = 0; i < 8; ++i) v[i] = __uint_as_float(r[i]);
+  for (int i = 0; i < 4; ++i) v[i] = __uint_as_float(r[i]);
 }
 
 __device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t s) {
@@ -329,6 +330,46 @@ tc_gemv_kernel(const __grid_constant__ CUtensorMap wmap,
   __syncthreads();  // barriers set up, tensor memory allocated
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+
+  // Epilogue, run by the 8 decode and the 8 convert warps once the last MMA
+  // is complete: warp (lane quarter q, part p of 4) reads accumulator
+  // columns [p T/4, (p + 1) T/4) of weight rows 32 q .. 32 q + 31 and stores
+  // acc = 2^24 D - sum_k x as int32 or as bf16((acc / s[m]) * ws[seg(n)]).
+  auto epilogue = [&](int q, int p) {
+    const bool acc_ready = warp_wait(&bar[kBarAcc], 0u);
+    const bool sums_ready = warp_wait(&bar[kBarSums], 0u);
+    tc_fence_after();
+    if (!(acc_ready && sums_ready)) {
+      if (lane == 0) atomicOr(err, 4u);
+      return;
+    }
+    const uint32_t t_lane = tmem + (uint32_t(32 * q) << 16);
+    const int n = g0 * kGroupRows + 32 * q + lane;
+    int sg = 0;
+#pragma unroll
+    for (int i = 1; i < BW_MAX_WS; ++i)
+      if (i < g.seg.n_ws && n >= g.seg.bounds[i]) sg = i;
+    const float wsv = ws_sm[sg];
+    const int quarter = T / 4;  // a multiple of 4
+    for (int j0 = p * quarter; j0 < (p + 1) * quarter; j0 += 4) {
+      float d[4];
+      tmem_ld4(t_lane + kTcDCol + uint32_t(j0), d);  // whole warp
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int m = j0 + e;
+        if (m >= rows || n >= g.N) continue;
+        const int total = __float2int_rn(d[e] * 16777216.0f) - sx_sm[m] -
+                          sx_sm[kTcMaxTokens + m];
+        if (ACC) {
+          static_cast<int *>(g.out)[size_t(m) * g.out_ld + n] = total;
+        } else {
+          const float scaled = static_cast<float>(total) / s_sm[m];
+          static_cast<__nv_bfloat16 *>(g.out)[size_t(m) * g.out_ld + n] =
+              __float2bfloat16_rn(scaled * wsv);
+        }
+      }
+    }
+  };
 
   if (warp == kTcProducerWarp) {
     // ---- tiled copies: weight stages (static: before the wait), tokens ----
@@ -519,6 +560,7 @@ tc_gemv_kernel(const __grid_constant__ CUtensorMap wmap,
     }
     __syncwarp();
     if (lane == 0) mbar_arrive(&bar[kBarSums]);
+    epilogue(cw, 2 + set);
   } else {
     // ---- decode warps: 2-bit codes -> fp16 A in tensor memory ----
     pdl_trigger();
@@ -566,41 +608,8 @@ tc_gemv_kernel(const __grid_constant__ CUtensorMap wmap,
       if (lane == 0) mbar_arrive(&bar[kBarFullAB + ab]);
     }
     if (!ok && lane == 0) atomicOr(err, 4u);
-
-    // ---- epilogue: accumulators -> int32 or bf16 ----
     pdl_wait();
-    const bool acc_ready = warp_wait(&bar[kBarAcc], 0u);
-    const bool sums_ready = warp_wait(&bar[kBarSums], 0u);
-    tc_fence_after();
-    if (acc_ready && sums_ready && ok) {
-      const int n = (g0 * kGroupRows) + r;
-      int sg = 0;
-#pragma unroll
-      for (int i = 1; i < BW_MAX_WS; ++i)
-        if (i < g.seg.n_ws && n >= g.seg.bounds[i]) sg = i;
-      const float wsv = ws_sm[sg];
-      const int half = T / 2;
-      for (int j0 = h * half; j0 < (h + 1) * half; j0 += 8) {
-        float d[8];
-        tmem_ld8(t_lane + kTcDCol + uint32_t(j0), d);  // whole warp
-#pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          const int m = j0 + e;
-          if (m >= rows || n >= g.N) continue;
-          const int total = __float2int_rn(d[e] * 16777216.0f) - sx_sm[m] -
-                            sx_sm[kTcMaxTokens + m];
-          if (ACC) {
-            static_cast<int *>(g.out)[size_t(m) * g.out_ld + n] = total;
-          } else {
-            const float scaled = static_cast<float>(total) / s_sm[m];
-            static_cast<__nv_bfloat16 *>(g.out)[size_t(m) * g.out_ld + n] =
-                __float2bfloat16_rn(scaled * wsv);
-          }
-        }
-      }
-    } else if (lane == 0) {
-      atomicOr(err, 4u);
-    }
+    epilogue(q, h);
   }
   tc_fence_before();
   __syncthreads();  // every tensor-memory access is done
