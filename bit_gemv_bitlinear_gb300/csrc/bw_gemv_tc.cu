@@ -477,6 +477,21 @@ tc_gemv_kernel(const __grid_constant__ CUtensorMap wmap,
     // ---- convert warps: int8 tokens -> swizzled fp16 B, token sums ----
     const int cw = (warp - kTcDecodeWarps) & 3;
     const int set = (warp - kTcDecodeWarps) >> 2;
+    {
+      // L2 prefetch of the token rows (a hint that returns no data, so it
+      // may precede the dependency wait: the copies after it still see the
+      // final values), one 128-byte line per thread across the grid.
+      const size_t lo = reinterpret_cast<size_t>(g.x);
+      const size_t base = lo & ~size_t(127);
+      const size_t hi = lo + size_t(rows - 1) * g.x_ld + g.K;
+      const int lines = int((hi - base + 127) / 128);
+      const int nt = kTcConvertWarps * 32;
+      for (int i = int(blockIdx.x) * nt + (threadIdx.x - kTcDecodeWarps * 32);
+           i < lines; i += int(gridDim.x) * nt) {
+        const size_t a = i == 0 ? lo : base + size_t(i) * 128;
+        asm volatile("prefetch.global.L2 [%0];" ::"l"(a));
+      }
+    }
     pdl_wait();
     pdl_trigger();
     {
