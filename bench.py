@@ -95,6 +95,22 @@ def dist_env():
     return rank, world, local
 
 
+def job_time_ms(torch, local_ms, world, device):
+    """Whole-job time of a timed region that every rank entered after the
+    same barrier: the maximum over ranks (an all-reduce; no-op at N=1)."""
+    if world == 1:
+        return float(local_ms)
+    t = torch.tensor([float(local_ms)], device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_value(world, bytes_per_rank_step, ms_per_step):
+    """Whole-job GB/s: every rank moves the same bytes per step (replicas),
+    in the whole job's time per step."""
+    return world * bytes_per_rank_step / (ms_per_step * 1e-3) / 1e9
+
+
 def algorithmic_bytes(N, K, n_ws):
     """Packed weights + int8 x + bf16 y + fp32 s + bf16 ws of one call."""
     return N * K // 4 + K + 2 * N + 4 + 2 * n_ws
@@ -332,15 +348,12 @@ def run_ours(args):
     for k in range(K_steps):
         for i, p in enumerate(parts):
             part_ms[p] += evs[k][i].elapsed_time(evs[k][i + 1])
-    if world > 1:
-        t = torch.tensor([total_ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = job_time_ms(torch, total_ms, world, dev)
 
     wbytes_step = R * sum(weight_bytes(shapes[n]["N"], shapes[n]["K"])
                           for n in SHAPES)
     ms_per_step = total_ms / K_steps
-    value = world * wbytes_step / (ms_per_step * 1e-3) / 1e9
+    value = job_value(world, wbytes_step, ms_per_step)
 
     # The GEMV kernel's own time: the events around the GEMV graph of every
     # timed step.
@@ -377,6 +390,8 @@ def run_ours(args):
     for _ in range(args.warmup):
         e2e_step()
     torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
     e_start = torch.cuda.Event(enable_timing=True)
     e_end = torch.cuda.Event(enable_timing=True)
     e_start.record(stream)
@@ -384,8 +399,8 @@ def run_ours(args):
         e2e_step()
     e_end.record(stream)
     torch.cuda.synchronize()
-    e2e_ms = e_start.elapsed_time(e_end) / K_steps
-    e2e_value = world * wbytes_step / (e2e_ms * 1e-3) / 1e9
+    e2e_ms = job_time_ms(torch, e_start.elapsed_time(e_end), world, dev) / K_steps
+    e2e_value = job_value(world, wbytes_step, e2e_ms)
 
     stack_line = None
     if not args.no_stack:
