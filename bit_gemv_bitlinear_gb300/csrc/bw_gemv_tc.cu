@@ -526,6 +526,7 @@ tc_gemv_kernel(const __grid_constant__ CUtensorMap wmap,
                    ? *reinterpret_cast<const uint4 *>(xsrc + m * kTcXRow)
                    : make_uint4(0u, 0u, 0u, 0u);
       }
+      fence_async_smem();  // as for the weight ring: reads done before a refill
       __syncwarp();
       if (lane == 0) mbar_arrive(&bar[kBarEmptyX + xs]);
       if (s >= kTcABStages &&
@@ -598,6 +599,10 @@ tc_gemv_kernel(const __grid_constant__ CUtensorMap wmap,
       for (int c = 0; c < kTcStageChunks; ++c)
         wq[c] = c < nc ? *reinterpret_cast<const uint4 *>(src + c * kGroupChunkBytes)
                        : make_uint4(0u, 0u, 0u, 0u);
+      // The slot is refilled by a bulk copy (async proxy) once released: the
+      // loads above (generic proxy, values not used yet) must be complete and
+      // ordered before that write, so every lane fences before the release.
+      fence_async_smem();
       __syncwarp();
       if (lane == 0) mbar_arrive(&bar[kBarEmptyW + ws]);
       if (s >= kTcABStages &&

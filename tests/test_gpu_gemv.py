@@ -245,6 +245,25 @@ def test_reproducible_and_stream_ordered(bw):
     assert torch.equal(y1, y2)
 
 
+@pytest.mark.parametrize("M,N,K", [(16, 77, 8192), (48, 300, 16384)])
+def test_batched_long_k_repeated(bw, M, N, K):
+    """Long K reuses every ring slot of the tensor-core kernel many times (32
+    and 64 stages of 256 k): repeated back-to-back calls must all be exact.
+    This caught a refill of a weight slot by a bulk copy that overtook the
+    slot's last (generic) loads."""
+    case = synth.gemv_case(M, N, K, synth.base_seed(12, M % 16),
+                           uniform_x=False, bounds=[0, N])
+    q, _ = oracle.quant_act(case["xf"])
+    packed = bw.bw_repack(to_dev(case["canon"]), N, K)
+    x_d = to_dev(q)
+    ref = oracle.gemv_acc(q, case["canon"], N, K)
+    for _ in range(6):
+        acc = bw.bw_gemv_w2a8_acc(x_d, packed, N, K)
+        torch.cuda.synchronize()
+        assert bw.bw_device_error() == 0
+        assert (acc.cpu().numpy() == ref).all()
+
+
 @pytest.mark.parametrize("M,N,K", [
     (8, 8, 64), (9, 100, 300), (17, 1000, 1028), (33, 77, 16384),
     (65, 513, 2560), (128, 2560, 2560), (200, 64, 68), (8, 40, 20000),
