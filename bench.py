@@ -206,20 +206,35 @@ def build_workload(torch, bw, dev, replicas, seed):
     for name in SHAPES:
         K = shapes[name]["K"]
         rows.setdefault(K, []).append(name)
+    # The fp32 rows of all K groups are views of one device buffer, and the
+    # outputs of all calls views of another, so that a step's inputs and
+    # results each move in one host<->device copy.
     act = {}
+    total_in = sum(replicas * len(names) * K for K, names in rows.items())
+    xf_all = torch.empty((total_in,), dtype=torch.float32, device=dev)
+    off = 0
     for K, names in rows.items():
         count = replicas * len(names)
         xf = synth.normal_f32(seed + K, count * K).reshape(count, K)
-        act[K] = dict(names=names, xf=xf,
-                      xf_d=torch.from_numpy(xf).to(dev),
+        xf_d = xf_all[off:off + count * K].view(count, K)
+        xf_d.copy_(torch.from_numpy(xf))
+        off += count * K
+        act[K] = dict(names=names, xf=xf, xf_d=xf_d,
                       q_d=torch.empty((count, K), dtype=torch.int8,
                                       device=dev),
                       s_d=torch.empty((count,), dtype=torch.float32,
                                       device=dev))
-    outs = {name: [torch.empty((1, shapes[name]["N"]), dtype=torch.bfloat16,
-                               device=dev) for _ in range(replicas)]
-            for name in SHAPES}
-    return shapes, act, outs
+    act_all = xf_all
+    total_out = replicas * sum(shapes[n]["N"] for n in SHAPES)
+    out_all = torch.empty((total_out,), dtype=torch.bfloat16, device=dev)
+    outs, off = {}, 0
+    for name in SHAPES:
+        N = shapes[name]["N"]
+        outs[name] = []
+        for _ in range(replicas):
+            outs[name].append(out_all[off:off + N].view(1, N))
+            off += N
+    return shapes, act, outs, act_all, out_all
 
 
 def act_row(act, shapes, name, r):
@@ -268,7 +283,8 @@ def run_ours(args):
 
     R = args.replicas
     seed = synth.base_seed(1)
-    shapes, act, outs = build_workload(torch, bw, dev, R, seed)
+    shapes, act, outs, act_all, out_all = build_workload(torch, bw, dev, R,
+                                                         seed)
     stream = torch.cuda.Stream(device=dev)
 
     def launch_quant():
@@ -368,24 +384,19 @@ def run_ours(args):
     gemv_launches = len(SHAPES) * R
     quant_launches = len(act)
 
-    # End to end: the same step with host buffers -- pinned H2D of the
-    # step's fp32 activation rows, the step, D2H of every output.
-    host_in = {K: torch.from_numpy(a["xf"]).pin_memory()
-               for K, a in act.items()}
-    host_out = {n: [torch.empty_like(o, device="cpu").pin_memory()
-                    for o in outs[n]] for n in SHAPES}
-    h2d = sum(t.numel() * 4 for t in host_in.values())
-    d2h = sum(o.numel() * 2 for n in SHAPES for o in outs[n])
+    # End to end: the same step with host buffers -- one pinned H2D of the
+    # step's fp32 activation rows, the step, one D2H of all its outputs.
+    host_in = act_all.cpu().pin_memory()
+    host_out = torch.empty_like(out_all, device="cpu").pin_memory()
+    h2d = host_in.numel() * 4
+    d2h = host_out.numel() * 2
 
     def e2e_step():
         with torch.cuda.stream(stream):
-            for K, a in act.items():
-                a["xf_d"].copy_(host_in[K], non_blocking=True)
+            act_all.copy_(host_in, non_blocking=True)
             for part in parts:
                 graphs[part].replay()
-            for n in SHAPES:
-                for r in range(R):
-                    host_out[n][r].copy_(outs[n][r], non_blocking=True)
+            host_out.copy_(out_all, non_blocking=True)
 
     for _ in range(args.warmup):
         e2e_step()
