@@ -26,6 +26,11 @@
 // The decode and convert warps then read the accumulators back (tcgen05.ld)
 // for the epilogue.
 //
+// Ring slots.  A shared-memory slot that a bulk copy refills is released only
+// after every reading lane has issued fence.proxy.async: the readers load the
+// stage with ordinary loads and use the values later, and the refill (async
+// proxy) is not otherwise ordered after loads still in flight.
+//
 // Weight values.  fp16 bit patterns below 0x0800 are linear in the value
 // (pattern * 2^-24: the subnormals and the first normal binade), so a code
 // c = w + 1 left at bit 2 sl of a half (slot sl of the word interleave) and
