@@ -75,6 +75,7 @@ def _load():
             "or_attn_one_token": (ctypes.c_int, [P, I64, I64, I64, P]),
             "or_layer": (ctypes.c_int, [P, I64, I64, I64, I64, F,
                                         P, P, P, P, P, P, P]),
+            "or_quant_weight": (ctypes.c_int, [P, I64, I64, P, I64, P, P]),
         }
         for name, (res, args) in sig.items():
             fn = getattr(lib, name)
@@ -161,6 +162,21 @@ def quant_act(x: np.ndarray):
     s = np.empty((M,), np.float32)
     _load().or_quant_act(_ptr(x), M, K, _ptr(q), _ptr(s))
     return q, s
+
+
+def quant_weight(W: np.ndarray, bounds):
+    """Absmean ternarisation: fp32 W [N][K], row segments `bounds` (n_ws + 1
+    values from 0 to N) -> (canonical codes uint8 [N][K/4], bf16 bit
+    patterns of ws uint16 [n_ws])."""
+    W = _c(W, np.float32)
+    N, K = W.shape
+    b = _c(np.asarray(bounds), np.int32)
+    n_ws = len(b) - 1
+    canon = np.empty((N, K // 4), np.uint8)
+    ws = np.empty((n_ws,), np.uint16)
+    _check(_load().or_quant_weight(_ptr(W), N, K, _ptr(b), n_ws, _ptr(canon),
+                                   _ptr(ws)), "quant_weight")
+    return canon, ws
 
 
 def layout_bytes(N: int, K: int) -> int:

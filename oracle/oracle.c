@@ -211,6 +211,49 @@ void or_quant_act(const float *x, int64_t M, int64_t K, int8_t *q, float *s)
     }
 }
 
+/*
+ * Absmean ternarisation of a weight matrix, per weight-scale segment (rows
+ * [bounds[i], bounds[i+1])), as the checkpoint conversion of [W2A8] §4.2
+ * states it: s = 1 / max(mean |W|, 1e-5), w = clamp(round(W * s), -1, 1),
+ * ws = bf16(1 / s).  The page leaves the precision to the framework's dtype;
+ * read here for fp32 weights: |W| summed in fp64 over the segment (rows in
+ * order, k in order), the mean (sum / count in fp64) rounded to fp32; s,
+ * W * s and 1 / s in fp32; round = nearest, ties to even; ws rounded to bf16
+ * (round to nearest even).  Output: canonical pack [N][K/4] (code = w + 1,
+ * element 4j+t at bits 2t of byte j) and the bf16 bit patterns of ws [n_ws].
+ */
+int or_quant_weight(const float *W, int64_t N, int64_t K,
+                    const int32_t *bounds, int64_t n_ws, uint8_t *canon,
+                    uint16_t *ws)
+{
+    if (N < 1 || K < 4 || K % 4 != 0) return OR_BAD_ARG;
+    if (check_bounds(bounds, n_ws, N) != OR_OK) return OR_BAD_ARG;
+    for (int64_t i = 0; i < n_ws; i++) {
+        const int64_t r0 = bounds[i], r1 = bounds[i + 1];
+        double sum = 0.0;
+        for (int64_t n = r0; n < r1; n++)
+            for (int64_t k = 0; k < K; k++)
+                sum += fabs((double)W[n * K + k]);
+        float mean = (float)(sum / (double)((r1 - r0) * K));
+        if (mean < 1e-5f) mean = 1e-5f;
+        const float s = 1.0f / mean;
+        ws[i] = or_bf16_rne(1.0f / s);
+        for (int64_t n = r0; n < r1; n++) {
+            for (int64_t j = 0; j < K / 4; j++) {
+                unsigned byte = 0;
+                for (int t = 0; t < 4; t++) {
+                    float v = nearbyintf(W[n * K + 4 * j + t] * s);
+                    if (v > 1.0f) v = 1.0f;
+                    if (v < -1.0f) v = -1.0f;
+                    byte |= (unsigned)((int)v + 1) << (2 * t);
+                }
+                canon[n * (K / 4) + j] = (uint8_t)byte;
+            }
+        }
+    }
+    return OR_OK;
+}
+
 /* ------------------------------------------------------------------ */
 /* Device weight layout, restated from the boundary header's layout    */
 /* specification (element by element; independent of the CUDA code).  */

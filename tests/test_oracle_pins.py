@@ -395,3 +395,70 @@ def test_layer_matches_stagewise_composition():
                        mats["w13"], mats["w2"], ws, gam)
     assert (out == h2).all()
     assert not (out == h).all()
+
+
+# --------------------------------------------- absmean weight ternarisation
+# [W2A8] §4.2: s = 1 / max(mean|W|, 1e-5), w = clamp(round(W s), -1, 1),
+# ws = bf16(1 / s), one scale per weight-scale segment.
+
+def test_quant_weight_constant_matrices():
+    # W = c everywhere: mean = |c|, W s = sign(c), ws = c for a power of 2.
+    for c, code, ws_bits in [(0.5, 2, 0x3F00), (-0.25, 0, 0x3E80),
+                             (2.0, 2, 0x4000)]:
+        W = np.full((3, 8), c, np.float32)
+        canon, ws = oracle.quant_weight(W, [0, 3])
+        assert (oracle.unpack(canon, 3, 8) == code - 1).all()
+        assert ws.tolist() == [ws_bits]
+
+
+def test_quant_weight_ties_to_even_and_clamp():
+    # mean |W| = 1 exactly, so s = 1: round(0.5) = 0, round(1.5) = 2 -> 1,
+    # round(-0.5) = -0 -> 0, round(-1.5) = -2 -> -1, round(2.5) = 2 -> 1.
+    # sum |W| = 4 + 4 + (2.5 + 0 + 0.5 + 1) = 12 over 12 elements
+    W = np.array([[0.5, 1.5, -0.5, -1.5], [0.5, 1.5, -0.5, -1.5],
+                  [2.5, 0.0, -0.5, -1.0]], np.float32)
+    assert float(np.abs(W).mean()) == 1.0
+    canon, ws = oracle.quant_weight(W, [0, 3])
+    w = oracle.unpack(canon, 3, 4)
+    assert w.tolist() == [[0, 1, 0, -1], [0, 1, 0, -1], [1, 0, 0, -1]]
+    assert ws.tolist() == [0x3F80]   # bf16(1.0)
+
+
+def test_quant_weight_zero_matrix_uses_the_floor():
+    canon, ws = oracle.quant_weight(np.zeros((2, 4), np.float32), [0, 2])
+    assert (oracle.unpack(canon, 2, 4) == 0).all()
+    # ws = 1 / s with s = 1 / 1e-5: 1e-5 within one bf16 step (2^-8 rel.)
+    assert abs(bits_f32(int(ws[0])) - 1e-5) <= 1e-5 * 2.0 ** -8
+
+
+def test_quant_weight_of_a_scaled_ternary_matrix_returns_its_codes():
+    # W = alpha * t (t ternary): mean = alpha (1 - p0), so |W s| = 1/(1-p0)
+    # lies in (1, 2.5) and rounds-and-clamps back to 1; zeros stay zero.
+    N, K, alpha = 40, 256, 0.0371
+    t = synth.canonical_weights(synth.base_seed(13), N, K)
+    t = oracle.unpack(t, N, K).astype(np.float32)
+    W = (alpha * t).astype(np.float32)
+    canon, ws = oracle.quant_weight(W, [0, N])
+    assert (oracle.unpack(canon, N, K) == t).all()
+    mean = float(np.abs(W.astype(np.float64)).mean())
+    assert abs(bits_f32(int(ws[0])) - mean) <= mean * 2.0 ** -8
+
+
+def test_quant_weight_segments_are_independent_and_scale_invariant():
+    rng = np.random.default_rng(7)
+    W = rng.standard_normal((30, 64)).astype(np.float32)
+    W[10:] *= 3.0
+    canon, ws = oracle.quant_weight(W, [0, 10, 30])
+    c0, w0 = oracle.quant_weight(W[:10], [0, 10])
+    c1, w1 = oracle.quant_weight(W[10:], [0, 20])
+    assert (canon[:10] == c0).all() and (canon[10:] == c1).all()
+    assert ws.tolist() == [int(w0[0]), int(w1[0])]
+    # codes of 2^e W equal those of W; the scale moves by 2^e exactly
+    c2, w2 = oracle.quant_weight((W * 8.0).astype(np.float32), [0, 10, 30])
+    assert (c2 == canon).all()
+    assert [bits_f32(int(v)) for v in w2] == \
+        [8.0 * bits_f32(int(v)) for v in ws]
+    # a sign flip of W flips every weight
+    c3, w3 = oracle.quant_weight(-W, [0, 10, 30])
+    assert (oracle.unpack(c3, 30, 64) == -oracle.unpack(canon, 30, 64)).all()
+    assert (w3 == ws).all()
