@@ -38,7 +38,7 @@ EXPORTS = ("bw_status_string", "bw_last_cuda_error", "bw_version",
            "bw_gemv_w2a8", "bw_gemv_w2a8_acc", "bw_repack_noalloc",
            "bw_device_error", "bw_stack_create", "bw_layer_stack",
            "bw_stack_destroy", "bw_selftest_wait_timeout",
-           "bw_gemv_workspace_bytes")
+           "bw_gemv_workspace_bytes", "bw_quant_weight")
 
 _P = ctypes.c_void_p
 _I = ctypes.c_int
@@ -59,6 +59,7 @@ _SIGS = {
     "bw_layer_stack": (_I, [_P, _P, _I, _P, _P, _P]),
     "bw_stack_destroy": (None, [_P]),
     "bw_selftest_wait_timeout": (_I, [_P, _P]),
+    "bw_quant_weight": (_I, [_P, _I, _I, _P, _I, _P, _P, _P]),
 }
 for _name, (_res, _args) in _SIGS.items():
     _fn = getattr(_lib, _name)
@@ -167,6 +168,25 @@ def bw_unrepack(packed: torch.Tensor, N: int, K: int,
                             _dev(canon, torch.uint8, "canon"),
                             _stream(stream)), "bw_unrepack")
     return canon
+
+
+def bw_quant_weight(W: torch.Tensor, ws_bounds, canon: torch.Tensor | None = None,
+                    ws: torch.Tensor | None = None, stream=None):
+    """Absmean ternarisation (synchronising): fp32 W [N][K] (device) and row
+    segments `ws_bounds` -> (canonical codes uint8 [N][K/4], bf16 ws
+    [n_ws]); the codes are the input of bw_repack."""
+    N, K = W.shape
+    n_ws = len(ws_bounds) - 1
+    if canon is None:
+        canon = torch.empty((N, K // 4), dtype=torch.uint8, device=W.device)
+    if ws is None:
+        ws = torch.empty((n_ws,), dtype=torch.bfloat16, device=W.device)
+    _check(_lib.bw_quant_weight(_dev(W, torch.float32, "W"), N, K,
+                                _bounds_array(ws_bounds), n_ws,
+                                _dev(canon, torch.uint8, "canon"),
+                                _dev(ws, torch.bfloat16, "ws"),
+                                _stream(stream)), "bw_quant_weight")
+    return canon, ws
 
 
 def _bounds_array(bounds):

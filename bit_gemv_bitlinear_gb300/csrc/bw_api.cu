@@ -214,6 +214,25 @@ bw_status bw_repack(const uint8_t *canon, int N, int K, uint8_t *packed,
   return bad_host ? BW_ERR_BAD_CODE : BW_OK;
 }
 
+bw_status bw_quant_weight(const float *W, int N, int K, const int *ws_bounds,
+                          int n_ws, uint8_t *canon, bw_bf16 *ws,
+                          bw_stream_t stream) {
+  if (!W || !canon || !ws || !ws_bounds) return BW_ERR_INVALID_ARG;
+  bw_status st = check_mnk(1, N, K);
+  if (st != BW_OK) return st;
+  if (n_ws < 1 || n_ws > BW_MAX_WS) return BW_ERR_INVALID_ARG;
+  if (ws_bounds[0] != 0 || ws_bounds[n_ws] != N) return BW_ERR_INVALID_ARG;
+  for (int i = 0; i < n_ws; ++i)
+    if (ws_bounds[i + 1] <= ws_bounds[i]) return BW_ERR_INVALID_ARG;
+  if (!aligned(W, 16) || !aligned(ws, 2)) return BW_ERR_MISALIGNED;
+  WsSegments seg{};
+  seg.n_ws = n_ws;
+  for (int i = 0; i <= n_ws; ++i) seg.bounds[i] = ws_bounds[i];
+  return cuda_status(launch_quant_weight(
+      W, N, K, seg, canon, reinterpret_cast<__nv_bfloat16 *>(ws),
+      reinterpret_cast<cudaStream_t>(stream)));
+}
+
 bw_status bw_unrepack(const uint8_t *packed, int N, int K, uint8_t *canon,
                       bw_stream_t stream) {
   if (!canon || !packed) return BW_ERR_INVALID_ARG;

@@ -93,6 +93,10 @@ cudaError_t launch_repack(const uint8_t *canon, int N, int K,
                           cudaStream_t stream);
 cudaError_t launch_unrepack(const uint8_t *packed, int N, int K,
                             uint8_t *canon, cudaStream_t stream);
+// Absmean ternarisation (bw_quant_weight.cu): synchronises `stream`.
+cudaError_t launch_quant_weight(const float *W, int N, int K,
+                                const WsSegments &seg, uint8_t *canon,
+                                __nv_bfloat16 *ws, cudaStream_t stream);
 
 int device_sm_count();
 

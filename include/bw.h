@@ -138,6 +138,24 @@ bw_status bw_repack_noalloc(const uint8_t *canon, int N, int K,
 bw_status bw_unrepack(const uint8_t *packed, int N, int K, uint8_t *canon,
                       bw_stream_t stream);
 
+/* bw_quant_weight -- absmean ternarisation of fp32 weights W [N][K] into the
+ * canonical codes [N][K/4] (the input of bw_repack) and one bf16 scale per
+ * weight-scale segment ([W2A8] §4.2, the checkpoint conversion): for the
+ * rows of segment i, s = 1 / max(mean |W|, 1e-5), w = clamp(round(W s), -1,
+ * 1) (nearest, ties to even), ws[i] = bf16(1 / s) (nearest even).  The page
+ * leaves the precision open: |W| is summed in fp64 per segment, the mean
+ * rounded to fp32, and s, W s and 1 / s are fp32.
+ *   W          fp32 [N][K] device, 16-byte aligned.
+ *   ws_bounds  int [n_ws + 1] HOST, as for bw_gemv_w2a8 (1 <= n_ws <=
+ *              BW_MAX_WS).
+ *   canon      uint8 [N][K/4] device (output).
+ *   ws         bf16 [n_ws] device, 2-byte aligned (output).
+ * Same shape limits as bw_repack.  Offline: it takes a few bytes of device
+ * scratch (stream-ordered) and synchronises `stream` before returning. */
+bw_status bw_quant_weight(const float *W, int N, int K, const int *ws_bounds,
+                          int n_ws, uint8_t *canon, bw_bf16 *ws,
+                          bw_stream_t stream);
+
 /* ------------------------------------------------------------------------
  * bw_gemv_w2a8 -- y = bf16( (acc / s[m]) * ws[seg(n)] ),
  *                 acc[m][n] = sum_k w[n][k] * x[m][k]  (exact int32).
