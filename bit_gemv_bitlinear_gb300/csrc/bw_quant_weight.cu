@@ -9,8 +9,8 @@
 // the mean (sum / count, fp64) rounded to fp32, s, W s and 1 / s in fp32,
 // round to nearest even, ws rounded to nearest even bf16.  The fp64 sum is
 // accumulated in a different order than a sequential sum; its rounding can
-// change the fp32 mean only when the fp64 sum lies within about 2^-29 (rel.)
-// of an fp32 rounding boundary.
+// change the fp32 mean only when the mean lies within a few fp64 rounding
+// steps of an fp32 rounding boundary.
 //
 // Offline: two kernels (the segment sums, one fp64 atomic per block; then
 // one thread per output byte), scratch from cudaMallocAsync, and the call
