@@ -10,11 +10,12 @@
 // "batched known tokens" item.
 //
 // One CTA owns 128 weight rows (16 row groups of the device layout) and all
-// K, for a tile of T <= 64 tokens; per 256-k stage:
+// K, for a tile of T <= 128 tokens; per 256-k stage:
 //  * one producer thread copies each stage's weights (a 2-D tensor-map box:
 //    16 row groups x 512 bytes, issued before the dependency wait since the
 //    weights are static) and tokens (T rows x 320 bytes, the 64 bytes past
-//    the stage unused) into shared-memory rings, one tiled TMA copy each;
+//    the stage unused) into shared-memory rings, one tiled TMA copy each
+//    (ring depths: TcCfg);
 //  * 4 decode warps turn the 2-bit codes into fp16 and store them straight
 //    into tensor memory: thread = weight row = TMEM lane, the MMA's A operand;
 //  * 4 convert warps turn the int8 tokens into fp16 in the 128-byte-swizzled
@@ -68,18 +69,41 @@ constexpr int kTcMmaWarp = kTcProducerWarp + 1;                    // 17
 constexpr int kTcThreads = (kTcMmaWarp + 1) * 32;                  // 576
 constexpr int kTcGroups = 16;          // row groups per CTA: 128 rows
 constexpr int kTcStageChunks = 4;      // 256 k per stage
-constexpr int kTcWStages = 6;          // weight stages in flight
-constexpr int kTcXStages = 4;          // token stages in flight
-constexpr int kTcABStages = 3;         // fp16 operand stages (TMEM A, smem B)
-constexpr int kTcMaxTokens = 64;
 constexpr uint32_t kTcWStageBytes = kTcGroups * kTcStageChunks * kGroupChunkBytes;
-// int8 token row of a stage: 256 bytes plus 64, so that the convert warps'
-// 16-byte reads of two adjacent tokens fall in distinct bank groups.
-constexpr uint32_t kTcXRow = 320;
 constexpr uint32_t kTcTmemCols = 512;
-constexpr uint32_t kTcDCol = kTcABStages * 128;  // accumulator columns
 // One CTA per SM: the tensor-memory allocation takes all 512 columns.
 constexpr uint32_t kTcMinSmem = 120u * 1024u;
+
+// Ring depths for a token tile of at most kMaxTokens tokens.  Up to 64
+// tokens: 6 weight, 4 token and 3 operand stages.  Up to 128 tokens (N = 128
+// MMAs): 2 of each, which is what fits in shared memory (two B stages are
+// 128 KB) and in tensor memory (2 A stages + a 128-column accumulator).
+template <int TM, int WS, int XS, int ABS, int XROW>
+struct TcCfg {
+  static constexpr int kMaxTokens = TM;
+  // int8 token row of a stage in shared memory: 256 bytes, plus 64 where it
+  // fits so that the convert warps' 16-byte reads of two adjacent tokens fall
+  // in distinct bank groups.
+  static constexpr uint32_t kXRow = XROW;
+  static constexpr int kWStages = WS;     // weight stages in flight
+  static constexpr int kXStages = XS;     // token stages in flight
+  static constexpr int kABStages = ABS;   // fp16 operand stages (TMEM A, smem B)
+  static constexpr uint32_t kDCol = ABS * 128;  // accumulator columns
+  // Barrier indices.
+  static constexpr int kBarFullW = 0;                        // [WS]
+  static constexpr int kBarEmptyW = kBarFullW + WS;          // [WS]
+  static constexpr int kBarFullX = kBarEmptyW + WS;          // [XS]
+  static constexpr int kBarEmptyX = kBarFullX + XS;          // [XS]
+  // A stage stored in TMEM and B stage in smem (decode + convert warps).
+  static constexpr int kBarFullAB = kBarEmptyX + XS;         // [ABS]
+  static constexpr int kBarDone = kBarFullAB + ABS;          // [ABS]
+  static constexpr int kBarAcc = kBarDone + ABS;             // accumulators final
+  static constexpr int kBarSums = kBarAcc + 1;               // token sums stored
+  static_assert(kBarSums < 32, "barrier block");
+  static_assert(kDCol + TM <= kTcTmemCols, "tensor memory");
+};
+using TcCfg64 = TcCfg<64, 6, 4, 3, 320>;
+using TcCfg128 = TcCfg<128, 2, 2, 2, 320>;
 
 // Shared-memory carve-up (offsets from a 1024-byte aligned base): weight
 // ring, B ring (1024-aligned: the swizzle pattern is taken from the address),
@@ -88,31 +112,20 @@ struct TcLayout {
   uint32_t w, b, x, s, ws, sx, tmem, bars, total;
 };
 
+template <class Cfg>
 __host__ __device__ inline TcLayout tc_layout(int T) {
   TcLayout l;
   l.w = 0;
-  l.b = l.w + kTcWStages * kTcWStageBytes;
-  l.x = l.b + kTcABStages * uint32_t(T) * 512u;
-  l.s = l.x + kTcXStages * uint32_t(T) * kTcXRow;
-  l.ws = l.s + kTcMaxTokens * 4;
-  l.sx = l.ws + BW_MAX_WS * 4;  // [2 sets][kTcMaxTokens]
-  l.tmem = l.sx + 2 * kTcMaxTokens * 4;
+  l.b = l.w + Cfg::kWStages * kTcWStageBytes;
+  l.x = l.b + Cfg::kABStages * uint32_t(T) * 512u;
+  l.s = l.x + Cfg::kXStages * uint32_t(T) * Cfg::kXRow;
+  l.ws = l.s + Cfg::kMaxTokens * 4;
+  l.sx = l.ws + BW_MAX_WS * 4;  // [2 sets][kMaxTokens]
+  l.tmem = l.sx + 2 * Cfg::kMaxTokens * 4;
   l.bars = l.tmem + 16;
   l.total = l.bars + 32 * 8;
   return l;
 }
-
-// Barrier indices.
-constexpr int kBarFullW = 0;                          // [kTcWStages]
-constexpr int kBarEmptyW = kBarFullW + kTcWStages;    // [kTcWStages]
-constexpr int kBarFullX = kBarEmptyW + kTcWStages;    // [kTcXStages]
-constexpr int kBarEmptyX = kBarFullX + kTcXStages;    // [kTcXStages]
-// A stage stored in TMEM and B stage in smem (decode + convert warps).
-constexpr int kBarFullAB = kBarEmptyX + kTcXStages;   // [kTcABStages]
-constexpr int kBarDone = kBarFullAB + kTcABStages;    // [kTcABStages]
-constexpr int kBarAcc = kBarDone + kTcABStages;       // accumulators final
-constexpr int kBarSums = kBarAcc + 1;                 // token sums stored
-static_assert(kBarSums < 32, "barrier block");
 
 // ---- tcgen05 / proxy helpers -------------------------------------------
 
@@ -291,17 +304,27 @@ __device__ __forceinline__ uint32_t col_bias(int r) {
 }
 
 
-// One launch: tokens [0, rows) (rows <= T <= 64, T a multiple of 16) of the
-// activations at g.x (16-byte aligned rows, K % 16 == 0), all N outputs; CTA
-// b owns row groups [16 b, 16 b + 16).
-template <bool ACC>
+// One launch: tokens [0, rows) (rows <= T <= Cfg::kMaxTokens, T a multiple
+// of 16) of the activations at g.x (16-byte aligned rows, K % 16 == 0), all
+// N outputs; CTA b owns row groups [16 b, 16 b + 16).
+template <bool ACC, class Cfg>
 __global__ void __launch_bounds__(kTcThreads, 1)
 tc_gemv_kernel(const __grid_constant__ CUtensorMap wmap,
                const __grid_constant__ CUtensorMap xmap, const GemvArgs g,
                int rows, int T, unsigned int *err) {
+  constexpr int kTcMaxTokens = Cfg::kMaxTokens;
+  constexpr int kTcWStages = Cfg::kWStages;
+  constexpr int kTcXStages = Cfg::kXStages;
+  constexpr int kTcABStages = Cfg::kABStages;
+  constexpr uint32_t kTcDCol = Cfg::kDCol;
+  constexpr uint32_t kTcXRow = Cfg::kXRow;
+  constexpr int kBarFullW = Cfg::kBarFullW, kBarEmptyW = Cfg::kBarEmptyW;
+  constexpr int kBarFullX = Cfg::kBarFullX, kBarEmptyX = Cfg::kBarEmptyX;
+  constexpr int kBarFullAB = Cfg::kBarFullAB, kBarDone = Cfg::kBarDone;
+  constexpr int kBarAcc = Cfg::kBarAcc, kBarSums = Cfg::kBarSums;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t *smem = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
-  const TcLayout L = tc_layout(T);
+  const TcLayout L = tc_layout<Cfg>(T);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int C = g.chunks;
   const int n_st = (C + kTcStageChunks - 1) / kTcStageChunks;
@@ -675,28 +698,28 @@ bool encode_2d(CUtensorMap *map, CUtensorMapDataType type, const void *base,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <bool ACC>
+template <bool ACC, class Cfg>
 cudaError_t launch_tc(const GemvArgs &g, int rows, int T, cudaStream_t stream) {
   static bool configured[64];
-  auto kernel = tc_gemv_kernel<ACC>;
+  auto kernel = tc_gemv_kernel<ACC, Cfg>;
   unsigned int *err = device_error_word();
   if (!err) return cudaErrorInvalidSymbol;
   // 1 KB of slack to align the base; at least kTcMinSmem: one CTA per SM.
-  uint32_t smem = tc_layout(T).total + 1024u;
+  uint32_t smem = tc_layout<Cfg>(T).total + 1024u;
   if (smem < kTcMinSmem) smem = kTcMinSmem;
   int64_t resident = 0;
   cudaError_t e = resident_ctas(kernel, configured, kTcThreads, smem, &resident);
   if (e != cudaSuccess) return e;
   // Weights: per row group, C chunks of 128 bytes as 16 C uint64; a box is
   // one stage of 16 groups.  Tokens: `rows` rows of K / 4 uint32; a box is
-  // 80 uint32 (320 bytes) of T rows (rows past `rows`, k past K: zero).
+  // kXRow / 4 uint32 of T rows (rows past `rows`, k past K: zero).
   CUtensorMap wmap, xmap;
   if (!encode_2d(&wmap, CU_TENSOR_MAP_DATA_TYPE_UINT64, g.w,
                  uint64_t(g.chunks) * (kGroupChunkBytes / 8),
                  uint64_t(g.n_groups), uint64_t(g.chunks) * kGroupChunkBytes,
                  kTcStageChunks * (kGroupChunkBytes / 8), kTcGroups) ||
       !encode_2d(&xmap, CU_TENSOR_MAP_DATA_TYPE_UINT32, g.x, uint64_t(g.K / 4),
-                 uint64_t(rows), uint64_t(g.x_ld), kTcXRow / 4, uint32_t(T)))
+                 uint64_t(rows), uint64_t(g.x_ld), Cfg::kXRow / 4, uint32_t(T)))
     return cudaErrorInvalidValue;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(unsigned((g.n_groups + kTcGroups - 1) / kTcGroups));
@@ -713,17 +736,25 @@ cudaError_t launch_tc(const GemvArgs &g, int rows, int T, cudaStream_t stream) {
 
 }  // namespace
 
+static_assert(TcCfg128::kMaxTokens == kTcMaxRows, "largest token tile");
+
 bool tc_fits(const GemvArgs &a) {
   return a.vec_x && a.K <= kMmaMaxK &&
-         tc_layout(kTcMaxTokens).total + 1024u <= 227u * 1024u;
+         tc_layout<TcCfg64>(TcCfg64::kMaxTokens).total + 1024u <= 227u * 1024u &&
+         tc_layout<TcCfg128>(TcCfg128::kMaxTokens).total + 1024u <= 227u * 1024u;
 }
 
+// Up to 64 tokens: the deep-ring configuration; 65..128: N = 128 MMAs with
+// shallower rings.
 cudaError_t launch_gemv_tc(const GemvArgs &a, int rows, bool acc_out,
                            cudaStream_t stream) {
   if (!tc_fits(a) || rows < 1 || rows > kTcMaxRows) return cudaErrorInvalidValue;
   const int T = (rows + 15) / 16 * 16;
-  return acc_out ? launch_tc<true>(a, rows, T, stream)
-                 : launch_tc<false>(a, rows, T, stream);
+  if (T <= TcCfg64::kMaxTokens)
+    return acc_out ? launch_tc<true, TcCfg64>(a, rows, T, stream)
+                   : launch_tc<false, TcCfg64>(a, rows, T, stream);
+  return acc_out ? launch_tc<true, TcCfg128>(a, rows, T, stream)
+                 : launch_tc<false, TcCfg128>(a, rows, T, stream);
 }
 
 }  // namespace bw

@@ -75,9 +75,10 @@ int mma_tile_rows(int K);
 cudaError_t launch_gemv_mma(const GemvArgs &args, int rows, bool acc_out,
                             cudaStream_t stream);
 // Tensor-core GEMV on tcgen05 (bw_gemv_tc.cu): one launch per tile of at
-// most kTcMaxRows activation rows; needs 16-byte aligned activation rows with
+// most kTcMaxRows activation rows (64-token tiles with deep rings, larger
+// tiles with N = 128 MMAs); needs 16-byte aligned activation rows with
 // K % 16 == 0 (bulk copies) and K <= kMmaMaxK.
-constexpr int kTcMaxRows = 64;
+constexpr int kTcMaxRows = 128;
 bool tc_fits(const GemvArgs &args);
 cudaError_t launch_gemv_tc(const GemvArgs &args, int rows, bool acc_out,
                            cudaStream_t stream);

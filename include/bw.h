@@ -175,7 +175,7 @@ bw_status bw_quant_weight(const float *W, int N, int K, const int *ws_bounds,
  *   y          bf16 [M][N] device, 2-byte aligned (output).
  *   1 <= M <= BW_MAX_M, 1 <= N <= BW_MAX_N, 4 <= K <= BW_MAX_K, K % 4 == 0,
  *   1 <= n_ws <= BW_MAX_WS.  M < 8: activation rows in tiles of 4, 2 and
- *   1 on CUDA cores (int dp4a).  M >= 8: tiles of up to 64 rows on the
+ *   1 on CUDA cores (int dp4a).  M >= 8: tiles of up to 128 rows on the
  *   tensor cores (tcgen05.mma; mma.sync where x is not 16-byte aligned or
  *   K % 16 != 0), exact in int32 as well.  The weights are streamed once
  *   per tile.

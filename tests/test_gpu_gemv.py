@@ -245,7 +245,8 @@ def test_reproducible_and_stream_ordered(bw):
     assert torch.equal(y1, y2)
 
 
-@pytest.mark.parametrize("M,N,K", [(16, 77, 8192), (48, 300, 16384)])
+@pytest.mark.parametrize("M,N,K", [(16, 77, 8192), (48, 300, 16384),
+                                   (128, 77, 8192), (100, 300, 16384)])
 def test_batched_long_k_repeated(bw, M, N, K):
     """Long K reuses every ring slot of the tensor-core kernel many times (32
     and 64 stages of 256 k): repeated back-to-back calls must all be exact.
@@ -267,7 +268,8 @@ def test_batched_long_k_repeated(bw, M, N, K):
 @pytest.mark.parametrize("M,N,K", [
     (8, 8, 64), (9, 100, 300), (17, 1000, 1028), (33, 77, 16384),
     (65, 513, 2560), (128, 2560, 2560), (200, 64, 68), (8, 40, 20000),
-    (24, 300, 1040), (49, 1000, 6928), (256, 1000, 2560)])
+    (24, 300, 1040), (49, 1000, 6928), (256, 1000, 2560), (96, 2560, 6912),
+    (113, 129, 4112)])
 def test_batched_tensor_core_tiles(bw, M, N, K):
     """M >= 8 takes the tensor-core path: tcgen05 tiles of up to 64 tokens
     (padded to 16) where rows are 16-byte aligned and K % 16 == 0, else
