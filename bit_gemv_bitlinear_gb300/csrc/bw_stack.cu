@@ -50,12 +50,18 @@ constexpr int kMaxGlueK = 32 * kPrologueThreads;  // 8192: V <= 32 per thread
 constexpr int kMaxGroup = 8;          // query heads per KV head unrolled
 constexpr int kPartialsPerThread = 2;  // partials loaded at once: 512 per CTA
 
-// clamp(rint(x * scale), -128, 127): fp32 product, round to nearest even,
-// one saturating convert to s8 (only the low byte of the result is used).
+// rint(x * scale) in the low byte of the result: the fp32 product (round to
+// nearest even), then an fp32 add of 1.5 * 2^23, whose result has a unit in
+// the last place of 1, so the add rounds the product to an integer (ties to
+// even) and leaves it, in two's complement, in the low mantissa bits while
+// |x * scale| < 2^22.  Every caller quantises with scale = 127 / max(A,
+// 1e-5) where A is the exact largest |x| of the values it quantises, so
+// |x * scale| <= 127 (1 + 2^-24) and the code is in [-127, 127]: the clamp
+// to [-128, 127] never acts.  Two full-rate fp32 instructions, where a
+// float-to-int convert runs at a fraction of that rate and every CTA
+// quantises the whole vector.
 __device__ __forceinline__ int quant1(float x, float scale) {
-  int q;
-  asm("cvt.rni.sat.s8.f32 %0, %1;" : "=r"(q) : "f"(__fmul_rn(x, scale)));
-  return q;
+  return __float_as_int(__fadd_rn(__fmul_rn(x, scale), 12582912.0f));
 }
 
 __device__ __forceinline__ uint32_t byte_perm(uint32_t a, uint32_t b,
