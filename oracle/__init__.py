@@ -76,6 +76,11 @@ def _load():
             "or_layer": (ctypes.c_int, [P, I64, I64, I64, I64, F,
                                         P, P, P, P, P, P, P]),
             "or_quant_weight": (ctypes.c_int, [P, I64, I64, P, I64, P, P]),
+            "or_bf16_rne_d": (ctypes.c_uint16, [ctypes.c_double]),
+            "or_rope_angle": (F, [I64, I64, I64, F]),
+            "or_rope": (ctypes.c_int, [P, I64, I64, F, P]),
+            "or_attn_decode": (ctypes.c_int, [P, I64, I64, I64, I64, F, P, P,
+                                              I64, P]),
         }
         for name, (res, args) in sig.items():
             fn = getattr(lib, name)
@@ -228,3 +233,38 @@ def layer(h, dim, ffn, n_heads, n_kv, eps, wqkv, wo, w13, w2, ws_bits,
                           _ptr(gammas), _ptr(scratch))
     _check(rc, "layer")
     return h
+
+
+def bf16_rne_d(x: float) -> int:
+    """bf16 bit pattern of a double, rounded to nearest even in one step."""
+    return int(_load().or_bf16_rne_d(float(x)))
+
+
+def rope_angle(p: int, i: int, D: int, theta: float) -> float:
+    """fp32 angle of pair i at position p: fl(p * fl(theta^(-2i/D)))."""
+    return float(_load().or_rope_angle(p, i, D, theta))
+
+
+def rope(x_bits, p: int, theta: float) -> np.ndarray:
+    """RoPE of one head (bf16 bit patterns [D]) at position p, fp64 [D]."""
+    x_bits = _c(x_bits, np.uint16).reshape(-1)
+    out = np.empty((x_bits.size,), np.float64)
+    _check(_load().or_rope(_ptr(x_bits), x_bits.size, p, theta, _ptr(out)),
+           "rope")
+    return out
+
+
+def attn_decode(qkv_bits, H: int, Hkv: int, D: int, p: int, theta: float,
+                kc_bits, vc_bits):
+    """One GQA decode step over a bf16 KV cache [Hkv][S][D].  Returns
+    (out fp64 [H][D], the updated key cache, the updated value cache); the
+    inputs are not modified."""
+    qkv_bits = _c(qkv_bits, np.uint16).reshape(-1)
+    kc = _c(kc_bits, np.uint16).copy()
+    vc = _c(vc_bits, np.uint16).copy()
+    S = kc.size // (Hkv * D)
+    out = np.empty((H, D), np.float64)
+    _check(_load().or_attn_decode(_ptr(qkv_bits), H, Hkv, D, p, theta,
+                                  _ptr(kc), _ptr(vc), S, _ptr(out)),
+           "attn_decode")
+    return out, kc.reshape(Hkv, S, D), vc.reshape(Hkv, S, D)

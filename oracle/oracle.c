@@ -25,18 +25,22 @@
  *     s = 127 / absmax as §六 item 3 defines it;
  *   - an all-zero activation row clamps absmax at 1e-5 (the same floor the
  *     weight quantiser of §4.2 uses), so it quantises to zeros;
- *   - the layer-stack glue (RMSNorm, ReLU^2 gate, one-token attention).
+ *   - the layer-stack glue (RMSNorm, ReLU^2 gate, one-token attention);
+ *   - decode attention: RoPE on adjacent pairs with fp32 angles
+ *     fl(p * fl(theta^(-2i/D))), the new key rounded to bf16 into the
+ *     cache, scores scaled by 1/sqrt(D), softmax over positions 0..p.
  *
  * Precision: integer work is exact (int64 accumulators, checked against the
  * int32 range).  The pages fix fp32 for the quantiser and the epilogue, so
  * those decisions are taken in fp32 (IEEE, no contraction: build with
  * -ffp-contract=off).  RMSNorm statistics, which the pages leave open, are
- * accumulated in fp64.
+ * accumulated in fp64, and so is all of the decode attention.
  */
 #include <stdint.h>
 #include <stddef.h>
 #include <string.h>
 #include <math.h>
+#include <stdlib.h>
 
 enum {
     OR_OK = 0,
@@ -412,5 +416,127 @@ int or_layer(float *h, int64_t dim, int64_t ffn, int64_t n_heads,
                          normed, q, &s, y);
     if (rc) return rc;
     for (int64_t i = 0; i < dim; i++) h[i] = h[i] + or_bf16_value(y[i]);
+    return OR_OK;
+}
+
+/* ------------------------------------------------------------------ */
+/* GQA decode attention over a KV cache ([W2A8] §一: 20 query heads,    */
+/* 5 KV heads, head_dim 128; §4.1: RoPE rotates adjacent pairs of head */
+/* dims; §六 item 2: a preallocated KV cache and flash attention)       */
+/* ------------------------------------------------------------------ */
+
+/* bf16 bit pattern of the double x, rounded to nearest even in one step
+ * (no fp32 intermediate).  |x| = m 2^e with m in [0.5, 1): a normal bf16
+ * keeps 8 significant bits, k = m 2^8 in [128, 256), value k 2^(e-8). */
+uint16_t or_bf16_rne_d(double x)
+{
+    uint16_t sign = signbit(x) ? 0x8000u : 0u;
+    double a = fabs(x);
+    if (isnan(x)) return 0x7fc0u;
+    if (a == 0.0) return sign;
+    int e;
+    double m = frexp(a, &e);
+    int biased = e - 1 + 127;           /* exponent field of a normal */
+    if (biased < 1) {                   /* subnormal: units of 2^-133 */
+        double k = nearbyint(ldexp(a, 133));
+        return (uint16_t)(sign | (uint16_t)k);   /* k = 128 is 0x0080 */
+    }
+    double k = nearbyint(m * 256.0);    /* exact scaling, then RNE */
+    if (k == 256.0) {
+        k = 128.0;
+        biased += 1;
+    }
+    if (biased > 254) return (uint16_t)(sign | 0x7f80u);  /* overflow */
+    return (uint16_t)(sign | (uint16_t)(biased << 7) |
+                      (uint16_t)((int)k - 128));
+}
+
+/* Angle of pair i of a head of D dims at position p.  Reading (the pages
+ * leave the precision open): the frequency f_i = theta^(-2i/D) is taken in
+ * fp64 and rounded to fp32 once, and the angle is the fp32 product
+ * p * f_i (one IEEE rounding; this file is built without contraction). */
+float or_rope_angle(int64_t p, int64_t i, int64_t D, float theta)
+{
+    float f = (float)pow((double)theta, -2.0 * (double)i / (double)D);
+    float pf = (float)p;
+    return pf * f;
+}
+
+/* RoPE of one head vector x (bf16 bits, D values) at position p, in fp64:
+ * pair (x[2i], x[2i+1]) turns by the angle of pair i. */
+int or_rope(const uint16_t *x, int64_t D, int64_t p, float theta,
+            double *out)
+{
+    if (D < 2 || D % 2 != 0 || p < 0) return OR_BAD_ARG;
+    for (int64_t i = 0; i < D / 2; i++) {
+        double phi = (double)or_rope_angle(p, i, D, theta);
+        double c = cos(phi), s = sin(phi);
+        double x0 = or_bf16_value(x[2 * i]), x1 = or_bf16_value(x[2 * i + 1]);
+        out[2 * i] = x0 * c - x1 * s;
+        out[2 * i + 1] = x0 * s + x1 * c;
+    }
+    return OR_OK;
+}
+
+/* One decode step of grouped-query attention for one sequence.
+ *   qkv  bf16 [(H + 2 Hkv) D]: q heads, then k heads, then v heads (the
+ *        fused wqkv output of the layer).
+ *   kc, vc  bf16 [Hkv][S][D]: the cache; positions 0..p-1 hold the earlier
+ *        tokens' rotated keys and values.
+ * Steps: (1) the new key of KV head g is rotated at position p and stored
+ * at kc[g][p] (rounded to bf16, nearest even), the new value is stored at
+ * vc[g][p] as it is; (2) query head h, which reads KV head g = h / (H/Hkv),
+ * is rotated at p; (3) scores s_j = q'.kc[g][j] / sqrt(D) for j = 0..p;
+ * (4) out[h] = sum_j softmax(s)_j vc[g][j].  All arithmetic in fp64; the
+ * softmax subtracts the largest score.  out: fp64 [H][D]. */
+int or_attn_decode(const uint16_t *qkv, int64_t H, int64_t Hkv, int64_t D,
+                   int64_t p, float theta, uint16_t *kc, uint16_t *vc,
+                   int64_t S, double *out)
+{
+    if (H < 1 || Hkv < 1 || H % Hkv != 0 || D < 2 || D % 2 != 0 ||
+        p < 0 || p >= S)
+        return OR_BAD_ARG;
+    int64_t G = H / Hkv;
+    const uint16_t *kn = qkv + H * D, *vn = qkv + (H + Hkv) * D;
+    double *rot = malloc(sizeof(double) * (size_t)D);
+    double *sc = malloc(sizeof(double) * (size_t)(p + 1));
+    if (!rot || !sc) {
+        free(rot);
+        free(sc);
+        return OR_BAD_ARG;
+    }
+    for (int64_t g = 0; g < Hkv; g++) {
+        or_rope(kn + g * D, D, p, theta, rot);
+        for (int64_t d = 0; d < D; d++) {
+            kc[(g * S + p) * D + d] = or_bf16_rne_d(rot[d]);
+            vc[(g * S + p) * D + d] = vn[g * D + d];
+        }
+    }
+    double scale = 1.0 / sqrt((double)D);
+    for (int64_t h = 0; h < H; h++) {
+        int64_t g = h / G;
+        or_rope(qkv + h * D, D, p, theta, rot);
+        double mx = -INFINITY;
+        for (int64_t j = 0; j <= p; j++) {
+            double dot = 0.0;
+            for (int64_t d = 0; d < D; d++)
+                dot += rot[d] * or_bf16_value(kc[(g * S + j) * D + d]);
+            sc[j] = dot * scale;
+            if (sc[j] > mx) mx = sc[j];
+        }
+        double l = 0.0;
+        for (int64_t j = 0; j <= p; j++) {
+            sc[j] = exp(sc[j] - mx);
+            l += sc[j];
+        }
+        for (int64_t d = 0; d < D; d++) {
+            double acc = 0.0;
+            for (int64_t j = 0; j <= p; j++)
+                acc += sc[j] * or_bf16_value(vc[(g * S + j) * D + d]);
+            out[h * D + d] = acc / l;
+        }
+    }
+    free(rot);
+    free(sc);
     return OR_OK;
 }

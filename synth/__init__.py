@@ -36,6 +36,7 @@ _CHUNK = 1 << 22
 # Stream ids: one per kind of quantity, so that changing one size does not
 # shift another quantity's numbers.
 S_WEIGHTS, S_ACT_I8, S_ACT_F32, S_WS, S_GAMMA, S_STEP = 1, 2, 3, 4, 5, 6
+S_ATTN = 7
 
 
 def base_seed(config: int, sub: int = 0) -> int:
@@ -134,6 +135,13 @@ def bf16_bits_to_f32(bits: np.ndarray) -> np.ndarray:
     return (np.asarray(bits, np.uint32) << np.uint32(16)).view(np.float32)
 
 
+def bf16_normal(seed: int, n: int, stream: int = S_ATTN,
+                offset: int = 0) -> np.ndarray:
+    """n bf16 bit patterns of N(0,1) draws: fp32 draw, low 16 bits cut."""
+    v = normal_f32(seed, n, stream, offset)
+    return (v.view(np.uint32) >> np.uint32(16)).astype(np.uint16)
+
+
 # --------------------------------------------------------------------------
 # Workloads
 # --------------------------------------------------------------------------
@@ -210,3 +218,18 @@ def stack_weights(seed: int, n_layers: int, dim: int = 2560,
 def step_inputs(seed: int, steps: int, dim: int) -> np.ndarray:
     """fp32 N(0,1) decoder inputs [steps][dim], one per decode step."""
     return normal_f32(seed, steps * dim, stream=S_STEP).reshape(steps, dim)
+
+
+def attn_case(seed: int, H: int, Hkv: int, D: int, S: int, p: int) -> dict:
+    """One decode-attention step: the fused q | k | v vector of the token
+    (bf16 [(H + 2 Hkv) D]) and a full KV cache (bf16 [Hkv][S][D] each),
+    every value an N(0,1) draw cut to bf16.  Rows p.. of the cache hold
+    draws too: the step must ignore them and overwrite row p only."""
+    nq = (H + 2 * Hkv) * D
+    nc = Hkv * S * D
+    return {
+        "H": H, "Hkv": Hkv, "D": D, "S": S, "p": p, "seed": seed,
+        "qkv": bf16_normal(seed, nq),
+        "kc": bf16_normal(seed, nc, offset=nq).reshape(Hkv, S, D),
+        "vc": bf16_normal(seed, nc, offset=nq + nc).reshape(Hkv, S, D),
+    }

@@ -462,3 +462,160 @@ def test_quant_weight_segments_are_independent_and_scale_invariant():
     c3, w3 = oracle.quant_weight(-W, [0, 10, 30])
     assert (oracle.unpack(c3, 30, 64) == -oracle.unpack(canon, 30, 64)).all()
     assert (w3 == ws).all()
+
+
+# --------------------------------------------------------------------------
+# Decode attention: RoPE, the KV-cache append and grouped-query softmax
+# attention (W2A8 kernel page, §一 head counts, §4.1 adjacent-pair RoPE,
+# §六 item 2 the preallocated KV cache).
+# --------------------------------------------------------------------------
+def _bf16(values):
+    return np.array([oracle.bf16_rne(float(v)) for v in values], np.uint16)
+
+
+def _f(bits):
+    return synth.bf16_bits_to_f32(np.asarray(bits, np.uint16)).astype(
+        np.float64)
+
+
+def test_rope_worked_example_golden():
+    rows = read_golden("rope.txt")
+    assert len(rows) == 2
+    for row in rows:
+        v = [float(t) for t in row.split()]
+        p, theta, q, want = int(v[0]), v[1], v[2:6], np.array(v[6:10])
+        got = oracle.rope(_bf16(q), p, theta)
+        assert np.abs(got - want).max() < 1e-12, (row, got)
+
+
+def test_rope_position_zero_is_identity_and_norms_are_kept():
+    x = synth.bf16_normal(synth.base_seed(20), 128)
+    assert (oracle.rope(x, 0, 10000.0) == _f(x)).all()
+    for p in (1, 7, 1000, 65535):
+        r = oracle.rope(x, p, 500000.0).reshape(-1, 2)
+        n0 = (_f(x).reshape(-1, 2) ** 2).sum(1)
+        assert np.allclose((r ** 2).sum(1), n0, rtol=1e-14, atol=0)
+
+
+def test_rope_scores_depend_on_relative_position():
+    """q'(p1) . k'(p2) depends on p1 - p2 only (up to the fp32 angles)."""
+    q = synth.bf16_normal(synth.base_seed(20, 1), 128)
+    k = synth.bf16_normal(synth.base_seed(20, 2), 128)
+    for p1, p2, t in ((5, 3, 11), (40, 0, 17), (9, 9, 50)):
+        a = oracle.rope(q, p1, 10000.0) @ oracle.rope(k, p2, 10000.0)
+        b = oracle.rope(q, p1 + t, 10000.0) @ oracle.rope(k, p2 + t, 10000.0)
+        assert abs(a - b) < 1e-4 * np.linalg.norm(_f(q)) * np.linalg.norm(_f(k))
+
+
+def test_rope_angles_are_fp32_products():
+    f1 = float(np.float32(10000.0 ** -0.5))
+    assert oracle.rope_angle(1, 1, 4, 10000.0) == f1
+    assert oracle.rope_angle(3, 1, 4, 10000.0) == float(
+        np.float32(np.float32(3.0) * np.float32(f1)))
+    assert oracle.rope_angle(12345, 0, 128, 500000.0) == 12345.0
+
+
+def test_bf16_rne_from_double_is_one_rounding():
+    for v in (1.0, -2.5, 3.140625, 1e-3, 65504.0, 1e-40):
+        assert oracle.bf16_rne_d(v) == oracle.bf16_rne(v)   # exact in fp32
+    assert oracle.bf16_rne_d(1.0 + 2.0 ** -8) == 0x3F80     # tie -> even
+    assert oracle.bf16_rne_d(1.0 + 3 * 2.0 ** -8) == 0x3F82  # tie -> even
+    # just above a tie: an fp32 step first would land on the tie and round
+    # down; one rounding goes up
+    assert oracle.bf16_rne_d(1.0 + 2.0 ** -8 + 2.0 ** -40) == 0x3F81
+    assert oracle.bf16_rne_d(-(1.0 + 2.0 ** -8 + 2.0 ** -40)) == 0xBF81
+    assert oracle.bf16_rne_d(3.5e38) == 0x7F80               # overflow
+    assert oracle.bf16_rne_d(2.0 ** -133) == 0x0001          # subnormal
+
+
+def test_attn_first_position_returns_the_new_value():
+    """p = 0: a single score, weight 1; the rotation at 0 is the identity,
+    so the cached key is the new key itself."""
+    c = synth.attn_case(synth.base_seed(21), 8, 2, 16, 4, 0)
+    out, kc, vc = oracle.attn_decode(c["qkv"], 8, 2, 16, 0, 10000.0,
+                                     c["kc"], c["vc"])
+    qkv = c["qkv"].reshape(-1, 16)
+    for h in range(8):
+        assert (out[h] == _f(qkv[8 + 2 + h // 4])).all()
+    assert (kc[:, 0] == qkv[8:10]).all() and (vc[:, 0] == qkv[10:12]).all()
+
+
+def test_attn_zero_query_averages_the_values_of_its_kv_head():
+    """q = 0: every score is 0, so head h returns the mean of the value rows
+    0..p of KV head h / (H / Hkv) -- pins the grouped head mapping."""
+    H, Hkv, D, S, p = 12, 3, 8, 16, 9
+    c = synth.attn_case(synth.base_seed(21, 1), H, Hkv, D, S, p)
+    qkv = c["qkv"].copy()
+    qkv[:H * D] = 0
+    out, _, vc = oracle.attn_decode(qkv, H, Hkv, D, p, 10000.0, c["kc"],
+                                    c["vc"])
+    for h in range(H):
+        mean = _f(vc[h // (H // Hkv), :p + 1]).mean(axis=0)
+        assert np.allclose(out[h], mean, rtol=0, atol=1e-14)
+
+
+def test_attn_scores_are_scaled_by_inverse_sqrt_head_dim():
+    """D = 4, p = 1: the cached key is 2 ln 3 along q', the new key is 0, so
+    the scores are ln 3 and 0 and the weights 3/4 and 1/4 (up to the bf16
+    rounding of the cached key)."""
+    H, Hkv, D, S, p = 1, 1, 4, 2, 1
+    qkv = _bf16([1, 0, 0, 0, 0, 0, 0, 0, 0.5, -1, 2, 0.25])
+    qr = oracle.rope(qkv[:4], p, 10000.0)
+    k0 = 2 * np.log(3.0) * qr / (qr @ qr)
+    kc = _bf16(k0).reshape(1, 1, 4)
+    kc = np.concatenate([kc, np.zeros((1, 1, 4), np.uint16)], axis=1)
+    vc = np.concatenate([_bf16([1, 2, -4, 8]).reshape(1, 1, 4),
+                         np.zeros((1, 1, 4), np.uint16)], axis=1)
+    out, _, _ = oracle.attn_decode(qkv, H, Hkv, D, p, 10000.0, kc, vc)
+    want = 0.75 * np.array([1, 2, -4, 8]) + 0.25 * np.array([0.5, -1, 2, 0.25])
+    assert np.abs(out[0] - want).max() < 2e-2
+
+
+def test_attn_is_invariant_to_the_order_of_cached_positions():
+    H, Hkv, D, S, p = 4, 2, 16, 32, 20
+    c = synth.attn_case(synth.base_seed(21, 2), H, Hkv, D, S, p)
+    out, _, _ = oracle.attn_decode(c["qkv"], H, Hkv, D, p, 500000.0, c["kc"],
+                                   c["vc"])
+    perm = np.concatenate([np.random.default_rng(3).permutation(p),
+                           np.arange(p, S)])
+    out2, _, _ = oracle.attn_decode(c["qkv"], H, Hkv, D, p, 500000.0,
+                                    c["kc"][:, perm], c["vc"][:, perm])
+    assert np.allclose(out, out2, rtol=0, atol=1e-13)
+
+
+def test_attn_dominant_position_returns_its_value():
+    """One cached key far along q' (a score 40 above the others) takes all
+    of the weight."""
+    H, Hkv, D, S, p = 2, 1, 16, 8, 5
+    c = synth.attn_case(synth.base_seed(21, 3), H, Hkv, D, S, p)
+    qkv = c["qkv"].copy()
+    qkv[D:2 * D] = qkv[:D]                   # both query heads alike
+    kc = np.zeros_like(c["kc"])
+    qkv[H * D:(H + 1) * D] = 0               # the new key: score 0
+    qr = oracle.rope(qkv[:D], p, 10000.0)
+    kc[0, 3] = _bf16(40 * np.sqrt(D) * qr / (qr @ qr))
+    out, _, vc = oracle.attn_decode(qkv, H, Hkv, D, p, 10000.0, kc, c["vc"])
+    assert np.allclose(out[0], _f(vc[0, 3]), rtol=0, atol=1e-12 * 8)
+
+
+def test_attn_appends_only_row_p():
+    H, Hkv, D, S, p = 8, 2, 32, 12, 7
+    c = synth.attn_case(synth.base_seed(21, 4), H, Hkv, D, S, p)
+    _, kc, vc = oracle.attn_decode(c["qkv"], H, Hkv, D, p, 10000.0, c["kc"],
+                                   c["vc"])
+    rows = [j for j in range(S) if j != p]
+    assert (kc[:, rows] == c["kc"][:, rows]).all()
+    assert (vc[:, rows] == c["vc"][:, rows]).all()
+    qkv = c["qkv"].reshape(-1, D)
+    for g in range(Hkv):
+        want = [oracle.bf16_rne_d(v)
+                for v in oracle.rope(qkv[H + g], p, 10000.0)]
+        assert (kc[g, p] == np.array(want, np.uint16)).all()
+        assert (vc[g, p] == qkv[H + Hkv + g]).all()
+
+
+def test_attn_rejects_positions_outside_the_cache():
+    c = synth.attn_case(synth.base_seed(21, 5), 4, 2, 8, 4, 0)
+    for p in (-1, 4):
+        with pytest.raises(oracle.OracleError):
+            oracle.attn_decode(c["qkv"], 4, 2, 8, p, 10000.0, c["kc"], c["vc"])
