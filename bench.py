@@ -69,6 +69,10 @@ def parse_args():
                    help="skip the layer-stack tok/s measurement")
     p.add_argument("--no-batched", action="store_true",
                    help="skip the batched M = 4/16/64 timings")
+    p.add_argument("--no-attn", action="store_true",
+                   help="skip the decode-attention timings")
+    p.add_argument("--attn", action="store_true",
+                   help="only time the decode attention (us/call, KV GB/s)")
     p.add_argument("--stack", action="store_true",
                    help="only time the 30-layer decode stack (tok/s)")
     p.add_argument("--stack-layers", type=int, default=None,
@@ -419,6 +423,9 @@ def run_ours(args):
     batched_line = None
     if rank == 0 and not args.no_batched:
         batched_line = run_batched(torch, bw, dev, peak)
+    attn_line = None
+    if rank == 0 and not args.no_attn:
+        attn_line = run_attn_timing(torch, bw, dev, peak)
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -475,6 +482,8 @@ def run_ours(args):
             line["layer_stack"] = stack_line
         if batched_line is not None:
             line["batched"] = batched_line
+        if attn_line is not None:
+            line["attn_decode"] = attn_line
         if cpu is not None:
             line["cpu_baseline"] = cpu
         print(json.dumps(line), flush=True)
@@ -736,6 +745,84 @@ def run_batched(torch, bw, dev, peak_gbs):
     return out
 
 
+ATTN_H, ATTN_HKV, ATTN_D, ATTN_S = 20, 5, 128, 4096
+ATTN_CONTEXTS = (512, 4096)
+ATTN_THETA = 500000.0
+
+
+def run_attn_timing(torch, bw, dev, peak_gbs, contexts=ATTN_CONTEXTS,
+                    iters=1024):
+    """bw_attn_decode at the BitNet-2B attention shape (20 query heads over
+    5 KV heads of 128, a 4096-position bf16 cache) for contexts of L tokens
+    (the new token at position L - 1): us per call in a graph of calls back
+    to back, each on its own cache so that the keys and values it reads
+    (2 Hkv L D bf16 = 2560 L bytes) come from HBM.  One cache of seeded
+    synthetic N(0,1) values is generated and copied."""
+    H, Hkv, D, S = ATTN_H, ATTN_HKV, ATTN_D, ATTN_S
+    seed = synth.base_seed(5)
+    case = synth.attn_case(seed, H, Hkv, D, S, 0)
+
+    def dev_bf16(bits):
+        return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)) \
+            .to(dev).view(torch.bfloat16)
+
+    qkv = dev_bf16(case["qkv"])
+    kc0, vc0 = dev_bf16(case["kc"]), dev_bf16(case["vc"])
+    ws = torch.zeros((bw.bw_attn_workspace_bytes(H, Hkv, D, S),),
+                     dtype=torch.uint8, device=dev)
+    out = torch.empty((H, D), dtype=torch.float32, device=dev)
+    res = {"heads": H, "kv_heads": Hkv, "head_dim": D, "cache_positions": S,
+           "theta": ATTN_THETA, "kernel": "attn_decode_kernel",
+           "timing": "graph of calls back to back, one cache per call, "
+                     "the caches' read rows over 4x L2",
+           "contexts": {}}
+    stream = torch.cuda.Stream(device=dev)
+    for L in contexts:
+        kv_bytes = 2 * Hkv * L * D * 2
+        rot = max(2, -(-4 * 126 * 2**20 // kv_bytes))
+        kcs = kc0.unsqueeze(0).repeat(rot, 1, 1, 1)
+        vcs = vc0.unsqueeze(0).repeat(rot, 1, 1, 1)
+        pos = torch.tensor([L - 1], dtype=torch.int32, device=dev)
+
+        def launches():
+            for i in range(rot):
+                bw.bw_attn_decode(qkv, pos, H, Hkv, kcs[i], vcs[i],
+                                  theta=ATTN_THETA, out=out, workspace=ws,
+                                  stream=stream)
+
+        with torch.cuda.stream(stream):
+            launches()
+        stream.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            launches()
+        with torch.cuda.stream(stream):
+            for _ in range(3):
+                g.replay()
+        torch.cuda.synchronize()
+        reps = max(1, iters // rot)
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            e0.record(stream)
+            for _ in range(reps):
+                g.replay()
+            e1.record(stream)
+        torch.cuda.synchronize()
+        bw.bw_device_error(stream)
+        us = e0.elapsed_time(e1) * 1e3 / (reps * rot)
+        res["contexts"][str(L)] = {
+            "us_per_call": round(us, 3),
+            "kv_bytes_per_call": kv_bytes,
+            "kv_GBps": round(kv_bytes / (us * 1e3), 1),
+            "hbm_frac": round(kv_bytes / (us * 1e3) / peak_gbs, 4),
+            "caches_rotated": rot,
+        }
+        del kcs, vcs, g
+        torch.cuda.empty_cache()
+    return res
+
+
 def run_single(args):
     """One shape over rotating weight buffers; also the command the kernel
     profiles are taken with."""
@@ -762,6 +849,14 @@ def main():
     args = parse_args()
     if args.single:
         run_single(args)
+    elif args.attn and args.impl != "reference":
+        import torch
+        import bit_gemv_bitlinear_gb300 as bw
+        dev = torch.device("cuda", 0)
+        torch.cuda.set_device(dev)
+        peak, _ = read_peaks()
+        print(json.dumps({"attn_decode": run_attn_timing(torch, bw, dev,
+                                                         peak)}), flush=True)
     elif args.stack and args.impl != "reference":
         import torch
         import bit_gemv_bitlinear_gb300 as bw

@@ -7,7 +7,7 @@ the import fails (build it with ``python -m bit_gemv_bitlinear_gb300.build``
 or ``__graft_entry__.build()``).
 
 Function names follow the C ABI: ``bw_quant_act``, ``bw_repack``,
-``bw_unrepack``, ``bw_gemv_w2a8``, ``bw_gemv_w2a8_acc``.
+``bw_unrepack``, ``bw_gemv_w2a8``, ``bw_gemv_w2a8_acc``, ``bw_attn_decode``.
 """
 from __future__ import annotations
 
@@ -38,7 +38,8 @@ EXPORTS = ("bw_status_string", "bw_last_cuda_error", "bw_version",
            "bw_gemv_w2a8", "bw_gemv_w2a8_acc", "bw_repack_noalloc",
            "bw_device_error", "bw_stack_create", "bw_layer_stack",
            "bw_stack_destroy", "bw_selftest_wait_timeout",
-           "bw_gemv_workspace_bytes", "bw_quant_weight")
+           "bw_gemv_workspace_bytes", "bw_quant_weight",
+           "bw_attn_workspace_bytes", "bw_attn_decode")
 
 _P = ctypes.c_void_p
 _I = ctypes.c_int
@@ -60,6 +61,9 @@ _SIGS = {
     "bw_stack_destroy": (None, [_P]),
     "bw_selftest_wait_timeout": (_I, [_P, _P]),
     "bw_quant_weight": (_I, [_P, _I, _I, _P, _I, _P, _P, _P]),
+    "bw_attn_workspace_bytes": (ctypes.c_size_t, [_I, _I, _I, _I]),
+    "bw_attn_decode": (_I, [_P, _P, _I, _I, _I, _I, ctypes.c_float, _P, _P,
+                            _P, _P, ctypes.c_size_t, _P]),
 }
 for _name, (_res, _args) in _SIGS.items():
     _fn = getattr(_lib, _name)
@@ -229,6 +233,40 @@ def bw_gemv_w2a8_acc(x: torch.Tensor, packed: torch.Tensor, N: int, K: int,
         K, _dev(acc, torch.int32, "acc"), _stream(stream)),
         "bw_gemv_w2a8_acc")
     return acc
+
+
+def bw_attn_workspace_bytes(H: int, Hkv: int, D: int, S: int) -> int:
+    """Device scratch bw_attn_decode needs for this shape (0: unsupported)."""
+    return int(_lib.bw_attn_workspace_bytes(H, Hkv, D, S))
+
+
+def bw_attn_decode(qkv: torch.Tensor, pos: torch.Tensor, H: int, Hkv: int,
+                   k_cache: torch.Tensor, v_cache: torch.Tensor,
+                   theta: float = 500000.0, out: torch.Tensor | None = None,
+                   workspace: torch.Tensor | None = None,
+                   stream=None) -> torch.Tensor:
+    """One grouped-query decode-attention step at position pos[0] (int32
+    device tensor): rotates and appends the new key and value (bf16 qkv
+    [(H + 2 Hkv) D]) to the bf16 caches [Hkv][S][D] and returns fp32 out
+    [H][D].  `workspace` is a uint8 device tensor of at least
+    bw_attn_workspace_bytes bytes, zeroed before its first use; if omitted,
+    a zeroed one is made for this call."""
+    Hkv_, S, D = k_cache.shape
+    if Hkv_ != Hkv or tuple(v_cache.shape) != (Hkv, S, D):
+        raise ValueError("k_cache and v_cache must be [Hkv][S][D]")
+    if out is None:
+        out = torch.empty((H, D), dtype=torch.float32, device=qkv.device)
+    if workspace is None:
+        workspace = torch.zeros((bw_attn_workspace_bytes(H, Hkv, D, S),),
+                                dtype=torch.uint8, device=qkv.device)
+    _check(_lib.bw_attn_decode(
+        _dev(qkv, torch.bfloat16, "qkv"), _dev(pos, torch.int32, "pos"),
+        H, Hkv, D, S, float(theta), _dev(k_cache, torch.bfloat16, "k_cache"),
+        _dev(v_cache, torch.bfloat16, "v_cache"),
+        _dev(out, torch.float32, "out"),
+        _dev(workspace, torch.uint8, "workspace"), workspace.numel(),
+        _stream(stream)), "bw_attn_decode")
+    return out
 
 
 def bw_device_error(stream=None) -> int:

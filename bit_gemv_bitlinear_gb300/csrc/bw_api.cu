@@ -255,7 +255,8 @@ bw_status bw_device_error(unsigned int *bits, bw_stream_t stream) {
   cudaError_t e =
       read_device_error(reinterpret_cast<cudaStream_t>(stream), bits);
   if (e != cudaSuccess) return cuda_status(e);
-  return *bits ? BW_ERR_TIMEOUT : BW_OK;
+  if (*bits & ~16u) return BW_ERR_TIMEOUT;
+  return *bits ? BW_ERR_INVALID_ARG : BW_OK;
 }
 
 bw_status bw_selftest_wait_timeout(unsigned int *bits, bw_stream_t stream) {

@@ -294,14 +294,63 @@ bw_status bw_layer_stack(bw_stack *stack, const float *h_in, int steps,
  * cudaFree).  NULL is accepted. */
 void bw_stack_destroy(bw_stack *stack);
 
+/* ------------------------------------------------------------------------
+ * bw_attn_decode -- one decode step of grouped-query attention for one
+ * sequence over a bf16 KV cache, in the shape of the BitNet-2B decoder
+ * ([W2A8] §一: 20 query heads over 5 KV heads of 128 dims; §4.1: the
+ * model's RoPE turns adjacent pairs of head dims; §六 item 2: the KV cache
+ * is preallocated and attention takes a flash path).  With G = H / Hkv and
+ * p = *pos:
+ *   1. the new key of KV head g (k = qkv[H D + g D ..]) is rotated at
+ *      position p and written to k_cache[g][p] (rounded to bf16, nearest
+ *      even); the new value (qkv[(H + Hkv) D + g D ..]) is written to
+ *      v_cache[g][p] as it is;
+ *   2. query head h (qkv[h D ..]) is rotated at p and reads KV head h / G;
+ *   3. out[h] = sum_j softmax_j(q'.k_cache[h/G][j] / sqrt(D)) v_cache[h/G][j]
+ *      over j = 0..p.
+ * RoPE: pair (x[2i], x[2i+1]) turns by the angle p * f_i, f_i =
+ * theta^(-2i/D); f_i is rounded to fp32 and the angle is the fp32 product
+ * (the pages leave the precision open; BitNet-2B's published configuration
+ * uses theta = 500000).  Scores, softmax and sums are fp32.
+ *   qkv       bf16 [(H + 2 Hkv) D] device, 2-byte aligned: q | k | v, the
+ *             fused wqkv output of the layer.
+ *   pos       int32 [1] device: the position p of the new token; read on the
+ *             device, so a graph replay serves every step.  p outside
+ *             [0, S) writes zeros to out, leaves the cache alone and sets
+ *             bit 16 of the device error word (bw_device_error then returns
+ *             BW_ERR_INVALID_ARG).
+ *   k_cache, v_cache  bf16 [Hkv][S][D] device, 16-byte aligned; rows 0..p-1
+ *             hold the earlier tokens (keys rotated); row p is written.
+ *   out       fp32 [H][D] device, 4-byte aligned.
+ *   workspace device scratch of at least bw_attn_workspace_bytes(H, Hkv, D,
+ *             S) bytes, 16-byte aligned, owned by the caller.  Zero it once
+ *             before its first use: it holds one counter per KV head, and
+ *             every call leaves them at zero again.  Calls sharing a
+ *             workspace must not overlap on the GPU.
+ *   D == 128; G in {1, 2, 4, 8}; 1 <= Hkv <= BW_ATTN_MAX_KV_HEADS;
+ *   1 <= S <= BW_ATTN_MAX_S; theta > 0 (host, fp32).
+ * Ordering: launched with programmatic dependent launch; every input is
+ * read after the preceding work on `stream` has completed.  Asynchronous;
+ * allocates nothing.
+ * ---------------------------------------------------------------------- */
+#define BW_ATTN_MAX_S 65536
+#define BW_ATTN_MAX_KV_HEADS 64
+size_t bw_attn_workspace_bytes(int H, int Hkv, int D, int S);
+bw_status bw_attn_decode(const bw_bf16 *qkv, const int *pos, int H, int Hkv,
+                         int D, int S, float theta, bw_bf16 *k_cache,
+                         bw_bf16 *v_cache, float *out, void *workspace,
+                         size_t workspace_bytes, bw_stream_t stream);
+
 /* bw_device_error -- reads and clears the library's device error word.
  * Kernels that wait on an mbarrier bound every wait (about one second); a
  * wait that runs out sets a bit here and the kernel stops early instead of
  * hanging (bit 2: a lane gave up waiting for the copies it issued before
  * leaving, bit 4: a warp gave up waiting for a weight piece; bit 8 is the
- * self-test's).
- * Returns BW_ERR_TIMEOUT if any bit was set, BW_OK otherwise; *bits receives
- * the word.  SYNCHRONISES `stream`; not for the hot path. */
+ * self-test's).  Bit 16: bw_attn_decode was given a position outside its
+ * cache.
+ * Returns BW_ERR_TIMEOUT if any time-out bit (2, 4, 8) was set, else
+ * BW_ERR_INVALID_ARG if bit 16 was, else BW_OK; *bits receives the word.
+ * SYNCHRONISES `stream`; not for the hot path. */
 bw_status bw_device_error(unsigned int *bits, bw_stream_t stream);
 
 /* bw_selftest_wait_timeout -- failure-detection self-test: launches a

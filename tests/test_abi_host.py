@@ -197,3 +197,42 @@ def test_stack_create_host_validation(lib):
     gbad = (P * L)(A4, A4 + 4)              # gains read as float4
     assert make(gammas=ctypes.cast(gbad, P)) == MISALIGNED
     assert run(None, A4, 1, A4, None, None) == INVALID
+
+
+def test_attn_workspace_and_host_validation(lib):
+    wsb = lib.bw_attn_workspace_bytes
+    wsb.restype = ctypes.c_size_t
+    wsb.argtypes = [ctypes.c_int] * 4
+    # BitNet-2B: 5 KV heads x 4 query heads, 64 splits of a 4096 cache:
+    # [5][64][4][130] floats of partials (256-byte rounded) + 5 counters.
+    assert wsb(20, 5, 128, 4096) == 5 * 64 * 4 * 130 * 4 + 5 * 4
+    assert wsb(20, 5, 128, 65536) == 5 * 128 * 4 * 130 * 4 + 5 * 4
+    assert wsb(20, 5, 128, 10) == (5 * 4 * 130 * 4 + 255) // 256 * 256 + 20
+    assert wsb(20, 5, 64, 4096) == 0          # head dim other than 128
+    assert wsb(12, 4, 128, 4096) == 0         # 3 query heads per KV head
+    assert wsb(20, 5, 128, 65537) == 0
+    ad = lib.bw_attn_decode
+    ad.restype = ctypes.c_int
+    ad.argtypes = [P, P, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                   ctypes.c_int, ctypes.c_float, P, P, P, P, ctypes.c_size_t,
+                   P]
+    need = wsb(20, 5, 128, 4096)
+
+    def call(qkv=A16, pos=A4, H=20, Hkv=5, D=128, S=4096, theta=5e5,
+             kc=A16, vc=A16, out=A4, ws=A16, nb=need):
+        return ad(qkv, pos, H, Hkv, D, S, theta, kc, vc, out, ws, nb, None)
+
+    assert call(qkv=None) == INVALID
+    assert call(ws=None) == INVALID
+    assert call(Hkv=3) == INVALID             # 20 % 3 != 0
+    assert call(H=12, Hkv=4) == SHAPE         # G = 3
+    assert call(D=64) == SHAPE
+    assert call(S=65537) == SHAPE
+    assert call(theta=0.0) == INVALID
+    assert call(theta=float("nan")) == INVALID
+    assert call(nb=need - 1) == INVALID
+    assert call(kc=A16 + 8) == MISALIGNED
+    assert call(vc=A16 + 2) == MISALIGNED
+    assert call(pos=A4 + 2) == MISALIGNED
+    assert call(out=A4 + 1) == MISALIGNED
+    assert call(ws=A16 + 4) == MISALIGNED

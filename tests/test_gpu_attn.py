@@ -1,0 +1,202 @@
+"""Parity of bw_attn_decode (GB300) with the CPU oracle.
+
+One decode step of grouped-query attention over a bf16 KV cache (the W2A8
+kernel page: §一 20 query heads over 5 KV heads of 128 dims, §4.1 RoPE on
+adjacent pairs, §六 item 2 the preallocated cache).  Checked per stage, as
+the layer stack is:
+  * the append: every cache row but p is untouched (bit for bit); the value
+    row p is the new value exactly; the key row p is the rotated new key,
+    within one bf16 ulp of the oracle's (fp32 against fp64 rotation can land
+    on the other side of a bf16 rounding tie), almost always identical;
+  * the attention: against the oracle's attention over the GPU's own cache
+    after the append, |out - ref| <= 2^-13 max |v| of the KV head's rows
+    0..p.  The bound comes from the fp32 arithmetic: scores are 128-term
+    fp32 dot products (relative error ~1e-6 of sum |q k| / sqrt(128)),
+    expf is within 2 ulp and the weighted sums run over at most 512
+    positions per split, all well below 2^-13 of the largest value.
+"""
+import numpy as np
+import pytest
+
+import oracle
+import synth
+
+pytestmark = pytest.mark.gpu
+
+torch = pytest.importorskip("torch")
+
+THETA = 500000.0
+
+
+@pytest.fixture(scope="module")
+def bw():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from conftest import build_lib
+    build_lib()
+    import bit_gemv_bitlinear_gb300 as bw
+    return bw
+
+
+def _dev_bf16(bits):
+    return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)) \
+        .cuda().view(torch.bfloat16)
+
+
+def _bits(t):
+    return t.view(torch.int16).cpu().numpy().view(np.uint16)
+
+
+def _f(bits):
+    return synth.bf16_bits_to_f32(bits).astype(np.float64)
+
+
+class Step:
+    """Device state of one sequence: caches, position, workspace."""
+
+    def __init__(self, bw, case):
+        self.bw = bw
+        self.c = case
+        self.kc = _dev_bf16(case["kc"])
+        self.vc = _dev_bf16(case["vc"])
+        self.pos = torch.tensor([case["p"]], dtype=torch.int32, device="cuda")
+        H, Hkv, D, S = case["H"], case["Hkv"], case["D"], case["S"]
+        self.ws = torch.zeros((bw.bw_attn_workspace_bytes(H, Hkv, D, S),),
+                              dtype=torch.uint8, device="cuda")
+        self.out = torch.empty((H, D), dtype=torch.float32, device="cuda")
+
+    def run(self, qkv_bits, p):
+        c = self.c
+        self.pos.fill_(p)
+        self.bw.bw_attn_decode(_dev_bf16(qkv_bits), self.pos, c["H"], c["Hkv"],
+                               self.kc, self.vc, theta=THETA, out=self.out,
+                               workspace=self.ws)
+        torch.cuda.synchronize()
+        return self.out.cpu().numpy().astype(np.float64)
+
+
+def check_step(case, qkv, p, kc_before, vc_before, out, kc_gpu, vc_gpu):
+    """Checks one step; returns the number of key elements of row p that
+    differ from the oracle's rounding (each by one ulp)."""
+    H, Hkv, D = case["H"], case["Hkv"], case["D"]
+    kref, vref = oracle.attn_append(qkv, H, Hkv, D, p, THETA, kc_before,
+                                    vc_before)
+    rows = [j for j in range(case["S"]) if j != p]
+    assert (kc_gpu[:, rows] == kc_before[:, rows]).all(), "cache rows changed"
+    assert (vc_gpu[:, rows] == vc_before[:, rows]).all(), "cache rows changed"
+    assert (vc_gpu[:, p] == vref[:, p]).all(), "value row p"
+    got, want = _f(kc_gpu[:, p]), _f(kref[:, p])
+    mag = np.maximum(np.abs(want), np.finfo(np.float32).tiny)
+    ulp = np.exp2(np.floor(np.log2(mag)) - 7)
+    assert (np.abs(got - want) <= ulp).all(), "key row p beyond one ulp"
+    flips = int((kc_gpu[:, p] != kref[:, p]).sum())
+    assert flips <= max(2, kc_gpu[:, p].size // 100), flips
+
+    ref = oracle.attn_over_cache(qkv, H, Hkv, D, p, THETA, kc_gpu, vc_gpu)
+    G = H // Hkv
+    for h in range(H):
+        vmax = np.abs(_f(vc_gpu[h // G, :p + 1])).max()
+        err = np.abs(out[h] - ref[h]).max()
+        assert err <= 2.0 ** -13 * vmax, (h, err, vmax)
+    return flips
+
+
+CASES = [
+    # H, Hkv, S, p: BitNet-2B heads (G = 4) over contexts that leave one
+    # split, several, a ragged last split and a full cache; G = 1, 2, 8.
+    (20, 5, 4096, 0),
+    (20, 5, 4096, 1),
+    (20, 5, 4096, 63),
+    (20, 5, 4096, 64),
+    (20, 5, 4096, 1000),
+    (20, 5, 4096, 4095),
+    (8, 8, 300, 299),
+    (16, 8, 1000, 517),
+    (16, 2, 777, 400),
+    (4, 1, 65536, 65535),
+]
+
+
+@pytest.mark.parametrize("H,Hkv,S,p", CASES)
+def test_attn_decode_matches_oracle(bw, H, Hkv, S, p):
+    case = synth.attn_case(synth.base_seed(22, CASES.index((H, Hkv, S, p))),
+                           H, Hkv, 128, S, p)
+    st = Step(bw, case)
+    out = st.run(case["qkv"], p)
+    assert bw.bw_device_error() == 0
+    check_step(case, case["qkv"], p, case["kc"], case["vc"], out,
+               _bits(st.kc), _bits(st.vc))
+
+
+def test_consecutive_steps_share_the_workspace_and_see_the_appended_rows(bw):
+    """Three steps p, p+1, p+2 on one cache and one workspace: every step
+    must find the merge counters at zero and read the rows the previous
+    steps appended."""
+    H, Hkv, D, S, p0 = 20, 5, 128, 512, 190
+    case = synth.attn_case(synth.base_seed(22, 50), H, Hkv, D, S, p0)
+    st = Step(bw, case)
+    kc, vc = case["kc"], case["vc"]
+    for t in range(3):
+        qkv = synth.bf16_normal(synth.base_seed(22, 51 + t),
+                                (H + 2 * Hkv) * D)
+        out = st.run(qkv, p0 + t)
+        kc_gpu, vc_gpu = _bits(st.kc), _bits(st.vc)
+        check_step(case, qkv, p0 + t, kc, vc, out, kc_gpu, vc_gpu)
+        kc, vc = kc_gpu, vc_gpu
+    assert bw.bw_device_error() == 0
+
+
+def test_graph_replay_advances_with_the_device_position(bw):
+    """A CUDA graph captured once serves every step: the position is read
+    on the device."""
+    H, Hkv, D, S, p0 = 20, 5, 128, 256, 100
+    case = synth.attn_case(synth.base_seed(22, 60), H, Hkv, D, S, p0)
+    st = Step(bw, case)
+    qkv_d = _dev_bf16(case["qkv"])
+    stream = torch.cuda.Stream()
+    stream.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(stream):   # warm-up outside the capture
+        bw.bw_attn_decode(qkv_d, st.pos, H, Hkv, st.kc, st.vc, theta=THETA,
+                          out=st.out, workspace=st.ws, stream=stream)
+    stream.synchronize()
+    # restore the cache the warm-up appended to
+    st.kc.copy_(_dev_bf16(case["kc"]))
+    st.vc.copy_(_dev_bf16(case["vc"]))
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        bw.bw_attn_decode(qkv_d, st.pos, H, Hkv, st.kc, st.vc, theta=THETA,
+                          out=st.out, workspace=st.ws, stream=stream)
+    kc, vc = case["kc"], case["vc"]
+    for t in range(3):
+        qkv = synth.bf16_normal(synth.base_seed(22, 61 + t),
+                                (H + 2 * Hkv) * D)
+        qkv_d.copy_(_dev_bf16(qkv))
+        st.pos.fill_(p0 + t)
+        torch.cuda.synchronize()
+        g.replay()
+        torch.cuda.synchronize()
+        out = st.out.cpu().numpy().astype(np.float64)
+        kc_gpu, vc_gpu = _bits(st.kc), _bits(st.vc)
+        check_step(case, qkv, p0 + t, kc, vc, out, kc_gpu, vc_gpu)
+        kc, vc = kc_gpu, vc_gpu
+    assert bw.bw_device_error() == 0
+
+
+def test_position_outside_the_cache_is_reported(bw):
+    H, Hkv, D, S = 20, 5, 128, 128
+    case = synth.attn_case(synth.base_seed(22, 70), H, Hkv, D, S, 0)
+    st = Step(bw, case)
+    st.out.fill_(7.0)
+    for p in (S, -1):
+        out = st.run(case["qkv"], p)
+        assert (out == 0).all()
+        assert (_bits(st.kc) == case["kc"]).all()
+        assert (_bits(st.vc) == case["vc"]).all()
+        with pytest.raises(bw.BwError) as e:
+            bw.bw_device_error()
+        assert e.value.status == 1                 # BW_ERR_INVALID_ARG
+    # the workspace counters are back at zero: a valid step still works
+    out = st.run(case["qkv"], 5)
+    check_step(case, case["qkv"], 5, case["kc"], case["vc"], out,
+               _bits(st.kc), _bits(st.vc))
+    assert bw.bw_device_error() == 0
