@@ -13,22 +13,31 @@
 // at short ones:
 //  * CTA (c, g) takes split c of the positions 0..p for KV head g and all
 //    G = H / Hkv query heads that read it, so every K and V row is loaded
-//    once for the G heads.  The number of splits is fixed at launch from
-//    the cache capacity (at most 128, at least 64 positions each); the
+//    once for the G heads.  The number of splits is fixed at launch: one
+//    CTA per SM over the KV heads where the cache allows (150 CTAs for 5 KV
+//    heads on 152 SMs), never more than 160 positions per split.  The
 //    position p is read on the device, so one launch serves every step of
-//    a graph-replayed decode loop, and splits past the context are empty.
+//    a graph-replayed decode loop: a context of L tokens uses min(splits,
+//    ceil(L / 64)) of them, the others are empty.
+//  * The rows of a split are contiguous in the cache, so two bulk copies
+//    (cp.async.bulk) bring its keys and its values into shared memory, up
+//    to 80 KB in flight per CTA, while the CTA rotates its queries; the
+//    keys complete on their own mbarrier, so the scores start before the
+//    values have landed.  Every wait is bounded.
 //  * A half-warp takes one position: lane l holds head dims 8 (l % 16) ..
-//    8 (l % 16) + 7, one 16-byte load per row; the G dot products are
-//    summed over the half-warp with four shuffles each.
+//    8 (l % 16) + 7 of a 256-byte row; the G dot products are summed over
+//    the half-warp with four shuffles each.
 //  * Inside a CTA the softmax has two passes over the scores in shared
 //    memory (largest score, then exp and sum); the CTA writes its largest
 //    scores m, exp sums l and unnormalised outputs to the workspace.
 //  * The last CTA of KV head g to finish (a fence and an atomic counter;
 //    nothing spins) merges the splits: out = sum_c e^(m_c - M) acc_c /
-//    sum_c e^(m_c - M) l_c, and sets the counter back to zero.
-//  * The CTA whose split holds p rotates the new key, rounds it to bf16,
-//    uses it for the score of p and writes key and value to row p of the
-//    cache; no CTA reads row p from memory.
+//    sum_c e^(m_c - M) l_c.  It loads every m and l at once, keeps the
+//    weights in shared memory, then sums the outputs with 16-byte loads,
+//    the splits shared between the two halves of the CTA; it sets the
+//    counter back to zero.
+//  * The CTA whose split holds p rotates the new key, rounds it to bf16 and
+//    puts key and value into its staged rows and into row p of the cache.
 // Arithmetic: fp32 throughout (fp32 angles p * f_i with f_i =
 // theta^(-2i/D) rounded to fp32 on the host, sincosf, expf), bf16 cache.
 #include "bw_pipe.cuh"
@@ -41,20 +50,21 @@ using pipe::pdl_wait;
 
 constexpr int kAttnD = 128;             // head dim
 constexpr int kAttnPairs = kAttnD / 2;
-constexpr int kAttnThreads = 128;
+constexpr int kAttnThreads = 256;
 constexpr int kAttnWarps = kAttnThreads / 32;
-constexpr int kAttnMinChunk = 64;       // positions per split, at least
-constexpr int kAttnMaxSplits = 128;
-constexpr int kAttnMaxChunk = BW_ATTN_MAX_S / kAttnMaxSplits;  // 512
+constexpr int kAttnChunk = 160;         // positions per split, at most
+constexpr int kAttnMinChunk = 64;       // positions per used split, at least
+// Splits of a cache of S positions: at most ceil(S / 64) (the workspace is
+// sized for that), at least ceil(S / kAttnChunk).
+constexpr int kAttnMaxSplits = (BW_ATTN_MAX_S + kAttnMinChunk - 1) / kAttnMinChunk;
 constexpr unsigned int kAttnErrPosition = 16u;  // device error word bit
-static_assert(kAttnThreads == kAttnD, "thread t owns head dim t in the sums");
 
 struct AttnArgs {
   const __nv_bfloat16 *qkv;  // [(H + 2 Hkv) D]
   const int *pos;            // [1]
   __nv_bfloat16 *kc, *vc;    // [Hkv][S][D]
   float *out;                // [H][D]
-  float *part;               // [Hkv][n_split][G][2 + D]
+  float *part;               // [Hkv][n_split] blocks of G (D + 4) floats
   unsigned int *count;       // [Hkv]
   int H, Hkv, S, n_split;
   float inv_sqrt_d;
@@ -62,24 +72,50 @@ struct AttnArgs {
   unsigned int *err;
 };
 
-__host__ __device__ inline int attn_splits(int S) {
-  const int n = (S + kAttnMinChunk - 1) / kAttnMinChunk;
-  return n < 1 ? 1 : (n > kAttnMaxSplits ? kAttnMaxSplits : n);
+__host__ __device__ inline int max_splits(int S) {
+  return (S + kAttnMinChunk - 1) / kAttnMinChunk;
 }
 
-// Shared memory: pair cos/sin, rotated queries, the new key, scores (later
-// the merge weights), per-warp outputs, reduction scratch.
+// One CTA per SM over the KV heads where the cache is long enough, within
+// [ceil(S / kAttnChunk), ceil(S / kAttnMinChunk)].
+inline int attn_splits(int S, int Hkv, int sms) {
+  const int lo = (S + kAttnChunk - 1) / kAttnChunk;
+  const int hi = max_splits(S);
+  int n = sms / Hkv;
+  if (n > hi) n = hi;
+  if (n < lo) n = lo;
+  return n < 1 ? 1 : n;
+}
+
+// A split's partial: acc [G][D] (16-byte aligned rows), then m [G] and
+// l [G], padded to G (D + 4) floats so that every block stays 16-byte
+// aligned.
+template <int G>
+struct AttnPart {
+  static constexpr int kStride = G * (kAttnD + 4);
+  static constexpr int kM = G * kAttnD;
+  static constexpr int kL = kM + G;
+};
+
+// Shared memory (bytes): staged key and value rows, pair cos/sin, rotated
+// queries, scores (the merge reuses the key rows for its weights),
+// per-warp outputs, reduction scratch.
 template <int G>
 struct AttnSmem {
-  static constexpr int kCs = 0;                              // [64] float2
-  static constexpr int kQ = kCs + 2 * kAttnPairs;            // [G][D]
-  static constexpr int kKn = kQ + G * kAttnD;                // [D]
-  static constexpr int kSc = kKn + kAttnD;                   // [chunk][G]
-  static constexpr int kWacc = kSc + kAttnMaxChunk * G;      // [warps][G][D]
-  static constexpr int kRed = kWacc + kAttnWarps * G * kAttnD;  // [warps][G]
-  static constexpr int kFloats = kRed + kAttnWarps * G;
-  static constexpr size_t kBytes = size_t(kFloats) * 4;
+  static constexpr uint32_t kRowBytes = kAttnD * 2;
+  static constexpr uint32_t kK = 0;
+  static constexpr uint32_t kV = kK + kAttnChunk * kRowBytes;
+  static constexpr uint32_t kCs = kV + kAttnChunk * kRowBytes;  // float2[64]
+  static constexpr uint32_t kQ = kCs + kAttnPairs * 8;          // [G][D]
+  static constexpr uint32_t kSc = kQ + G * kAttnD * 4;          // [chunk][G]
+  static constexpr uint32_t kWacc = kSc + kAttnChunk * G * 4;   // [warps][G][D]
+  static constexpr uint32_t kRed = kWacc + kAttnWarps * G * kAttnD * 4;
+  static constexpr size_t kBytes = kRed + kAttnWarps * G * 4 + 16;
 };
+// The merge keeps [splits][G] weights, [splits][G] exp sums and G totals
+// in the staging rows.
+static_assert((2 * kAttnMaxSplits * 8 + 8) * 4 <= 2 * kAttnChunk * kAttnD * 2,
+              "merge scratch fits in the staging rows");
 
 __device__ __forceinline__ void bf16x8_to_f32(uint4 raw, float (&v)[8]) {
   const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
@@ -120,14 +156,17 @@ __device__ __forceinline__ void cta_reduce(float (&v)[G], float *red) {
 template <int G>
 __global__ void __launch_bounds__(kAttnThreads)
 attn_decode_kernel(const AttnArgs a) {
-  extern __shared__ __align__(16) float sm[];
+  extern __shared__ __align__(128) uint8_t smem[];
   using L = AttnSmem<G>;
-  float2 *cs = reinterpret_cast<float2 *>(sm + L::kCs);
-  float *q_sm = sm + L::kQ;
-  float *kn_sm = sm + L::kKn;
-  float *sc = sm + L::kSc;
-  float *wacc = sm + L::kWacc;
-  float *red = sm + L::kRed;
+  using P = AttnPart<G>;
+  __nv_bfloat16 *kst = reinterpret_cast<__nv_bfloat16 *>(smem + L::kK);
+  __nv_bfloat16 *vst = reinterpret_cast<__nv_bfloat16 *>(smem + L::kV);
+  float2 *cs = reinterpret_cast<float2 *>(smem + L::kCs);
+  float *q_sm = reinterpret_cast<float *>(smem + L::kQ);
+  float *sc = reinterpret_cast<float *>(smem + L::kSc);
+  float *wacc = reinterpret_cast<float *>(smem + L::kWacc);
+  float *red = reinterpret_cast<float *>(smem + L::kRed);
+  __shared__ __align__(8) uint64_t bar[2];  // keys, values
   __shared__ int s_last;
 
   const int c = blockIdx.x, g = blockIdx.y;
@@ -151,18 +190,29 @@ attn_decode_kernel(const AttnArgs a) {
       j1 = int(int64_t(c + 1) * len / n_eff);
     }
   }
-  const int n = j1 - j0;  // positions of this CTA (<= kAttnMaxChunk)
-  float *part = a.part + (size_t(g) * a.n_split + c) * G * (D + 2);
+  const int n = j1 - j0;  // positions of this CTA (<= kAttnChunk)
+  float *part = a.part + (size_t(g) * a.n_split + c) * P::kStride;
   const size_t head_row = size_t(g) * a.S;  // row 0 of KV head g
 
   if (n > 0) {
-    // ---- RoPE: pair angles, rotated queries, the new key (CTA holding p)
+    // ---- the split's key rows and value rows: one bulk copy each ----
+    if (tid == 0) {
+      pipe::mbar_init(&bar[0], 1);
+      pipe::mbar_init(&bar[1], 1);
+      asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+      const uint32_t bytes = uint32_t(n) * L::kRowBytes;
+      pipe::mbar_arrive_expect_tx(&bar[0], bytes);
+      pipe::bulk_copy_g2s(kst, a.kc + (head_row + j0) * D, bytes, &bar[0]);
+      pipe::mbar_arrive_expect_tx(&bar[1], bytes);
+      pipe::bulk_copy_g2s(vst, a.vc + (head_row + j0) * D, bytes, &bar[1]);
+    }
+    // ---- RoPE of the queries meanwhile ----
     if (tid < kAttnPairs) {
       float sn, cn;
       sincosf(__fmul_rn(float(p), a.freq[tid]), &sn, &cn);
       cs[tid] = make_float2(cn, sn);
     }
-    __syncthreads();
+    __syncthreads();  // cos/sin ready; the barriers are initialised
     for (int e = tid; e < G * kAttnPairs; e += kAttnThreads) {
       const int h = e / kAttnPairs, i = e - h * kAttnPairs;
       const __nv_bfloat16 *qh = a.qkv + size_t(g * G + h) * D;
@@ -173,135 +223,155 @@ attn_decode_kernel(const AttnArgs a) {
       q_sm[h * D + 2 * i + 1] = x0 * r.y + x1 * r.x;
     }
     const bool has_p = j0 <= p && p < j1;
-    if (has_p && tid < kAttnPairs) {
-      const int i = tid;
-      const __nv_bfloat16 *kh = a.qkv + size_t(a.H + g) * D;
-      const __nv_bfloat16 *vh = a.qkv + size_t(a.H + a.Hkv + g) * D;
-      const float x0 = __bfloat162float(kh[2 * i]);
-      const float x1 = __bfloat162float(kh[2 * i + 1]);
-      const float2 r = cs[i];
-      const __nv_bfloat16 k0 = __float2bfloat16_rn(x0 * r.x - x1 * r.y);
-      const __nv_bfloat16 k1 = __float2bfloat16_rn(x0 * r.y + x1 * r.x);
-      kn_sm[2 * i] = __bfloat162float(k0);
-      kn_sm[2 * i + 1] = __bfloat162float(k1);
-      __nv_bfloat16 *krow = a.kc + (head_row + p) * D;
-      __nv_bfloat16 *vrow = a.vc + (head_row + p) * D;
-      krow[2 * i] = k0;
-      krow[2 * i + 1] = k1;
-      vrow[2 * i] = vh[2 * i];
-      vrow[2 * i + 1] = vh[2 * i + 1];
-    }
-    __syncthreads();
+    const bool k_in = pipe::mbar_wait(&bar[0], 0u);
+    const bool v_in = k_in && (!has_p || pipe::mbar_wait(&bar[1], 0u));
+    if (!__syncthreads_and(v_in)) {
+      // Never expected: report, let the copies land (bounded) before the
+      // CTA may leave, and contribute no partial.
+      if (tid == 0) {
+        atomicOr(a.err, 4u);
+        if (!pipe::mbar_wait(&bar[0], 0u) || !pipe::mbar_wait(&bar[1], 0u))
+          atomicOr(a.err, 2u);
+      }
+      __syncthreads();
+    } else {
+      // ---- the new token: rotated key and value, staged and appended
+      // (the CTA holding p has waited for both of its copies) ----
+      if (has_p && tid < kAttnPairs) {
+        const int i = tid;
+        const __nv_bfloat16 *kh = a.qkv + size_t(a.H + g) * D;
+        const __nv_bfloat16 *vh = a.qkv + size_t(a.H + a.Hkv + g) * D;
+        const float x0 = __bfloat162float(kh[2 * i]);
+        const float x1 = __bfloat162float(kh[2 * i + 1]);
+        const float2 r = cs[i];
+        const __nv_bfloat162 k2 = __halves2bfloat162(
+            __float2bfloat16_rn(x0 * r.x - x1 * r.y),
+            __float2bfloat16_rn(x0 * r.y + x1 * r.x));
+        const __nv_bfloat162 v2 = __halves2bfloat162(vh[2 * i], vh[2 * i + 1]);
+        const size_t row = size_t(p - j0) * D;
+        reinterpret_cast<__nv_bfloat162 *>(kst + row)[i] = k2;
+        reinterpret_cast<__nv_bfloat162 *>(vst + row)[i] = v2;
+        reinterpret_cast<__nv_bfloat162 *>(a.kc + (head_row + p) * D)[i] = k2;
+        reinterpret_cast<__nv_bfloat162 *>(a.vc + (head_row + p) * D)[i] = v2;
+      }
+      __syncthreads();
 
-    // ---- scores: a half-warp per position, 8 dims per lane ----
-    float qr[G][8];
-#pragma unroll
-    for (int h = 0; h < G; ++h)
-#pragma unroll
-      for (int e = 0; e < 8; ++e) qr[h][e] = q_sm[h * D + 8 * hl + e];
-    for (int jb = 2 * warp; jb < n; jb += 2 * kAttnWarps) {  // warp-uniform
-      const int jj = jb + half;
-      const bool act = jj < n;
-      const int j = j0 + jj;
-      float kv[8];
-      if (act && j == p) {
-#pragma unroll
-        for (int e = 0; e < 8; ++e) kv[e] = kn_sm[8 * hl + e];
-      } else if (act) {
-        bf16x8_to_f32(__ldg(reinterpret_cast<const uint4 *>(
-                          a.kc + (head_row + j) * D + 8 * hl)),
-                      kv);
-      } else {
-#pragma unroll
-        for (int e = 0; e < 8; ++e) kv[e] = 0.0f;
-      }
-      float d[G];
-#pragma unroll
-      for (int h = 0; h < G; ++h) {
-        float t = 0.0f;
-#pragma unroll
-        for (int e = 0; e < 8; ++e) t = fmaf(qr[h][e], kv[e], t);
-        d[h] = t;
-      }
+      // ---- scores: a half-warp per position, 8 dims per lane ----
+      float qr[G][8];
 #pragma unroll
       for (int h = 0; h < G; ++h)
 #pragma unroll
-        for (int o = 8; o > 0; o >>= 1)
-          d[h] += __shfl_xor_sync(0xffffffffu, d[h], o);  // within the half
-      if (act && hl == 0)
+        for (int e = 0; e < 8; ++e) qr[h][e] = q_sm[h * D + 8 * hl + e];
+      // Two positions per half-warp and step: their shuffle chains overlap.
+      for (int jb = 4 * warp; jb < n; jb += 4 * kAttnWarps) {  // warp-uniform
+        float d[2][G];
 #pragma unroll
-        for (int h = 0; h < G; ++h) sc[jj * G + h] = d[h] * a.inv_sqrt_d;
-    }
-    __syncthreads();
-
-    // ---- softmax of the split: largest score, then exp and sum ----
-    float m[G], l[G];
+        for (int r = 0; r < 2; ++r) {
+          const int jj = jb + 2 * r + half;
+          float kv[8];
+          bf16x8_to_f32(jj < n ? *reinterpret_cast<const uint4 *>(
+                                     kst + size_t(jj) * D + 8 * hl)
+                               : make_uint4(0u, 0u, 0u, 0u),
+                        kv);
 #pragma unroll
-    for (int h = 0; h < G; ++h) m[h] = -INFINITY;
-    for (int jj = tid; jj < n; jj += kAttnThreads)
+          for (int h = 0; h < G; ++h) {
+            float t = 0.0f;
 #pragma unroll
-      for (int h = 0; h < G; ++h) m[h] = fmaxf(m[h], sc[jj * G + h]);
-    cta_reduce<G, true>(m, red);
-#pragma unroll
-    for (int h = 0; h < G; ++h) l[h] = 0.0f;
-    for (int jj = tid; jj < n; jj += kAttnThreads)
-#pragma unroll
-      for (int h = 0; h < G; ++h) {
-        const float e = expf(sc[jj * G + h] - m[h]);
-        sc[jj * G + h] = e;
-        l[h] += e;
-      }
-    cta_reduce<G, false>(l, red);  // its barriers also publish sc
-
-    // ---- weighted values ----
-    float acc[G][8];
-#pragma unroll
-    for (int h = 0; h < G; ++h)
-#pragma unroll
-      for (int e = 0; e < 8; ++e) acc[h][e] = 0.0f;
-    for (int jb = 2 * warp; jb < n; jb += 2 * kAttnWarps) {
-      const int jj = jb + half;
-      if (jj < n) {
-        const int j = j0 + jj;
-        float vv[8];
-        if (j == p) {
-          const __nv_bfloat16 *vh = a.qkv + size_t(a.H + a.Hkv + g) * D;
-#pragma unroll
-          for (int e = 0; e < 8; ++e) vv[e] = __bfloat162float(vh[8 * hl + e]);
-        } else {
-          bf16x8_to_f32(__ldg(reinterpret_cast<const uint4 *>(
-                            a.vc + (head_row + j) * D + 8 * hl)),
-                        vv);
+            for (int e = 0; e < 8; ++e) t = fmaf(qr[h][e], kv[e], t);
+            d[r][h] = t;
+          }
         }
+#pragma unroll
+        for (int o = 8; o > 0; o >>= 1)
+#pragma unroll
+          for (int r = 0; r < 2; ++r)
+#pragma unroll
+            for (int h = 0; h < G; ++h)
+              d[r][h] += __shfl_xor_sync(0xffffffffu, d[r][h], o);  // in half
+        if (hl == 0)
+#pragma unroll
+          for (int r = 0; r < 2; ++r) {
+            const int jj = jb + 2 * r + half;
+            if (jj < n)
+#pragma unroll
+              for (int h = 0; h < G; ++h)
+                sc[jj * G + h] = d[r][h] * a.inv_sqrt_d;
+          }
+      }
+      __syncthreads();
+
+      // ---- softmax of the split: largest score, then exp and sum ----
+      float m[G], l[G];
+#pragma unroll
+      for (int h = 0; h < G; ++h) m[h] = -INFINITY;
+      for (int jj = tid; jj < n; jj += kAttnThreads)
+#pragma unroll
+        for (int h = 0; h < G; ++h) m[h] = fmaxf(m[h], sc[jj * G + h]);
+      cta_reduce<G, true>(m, red);
+#pragma unroll
+      for (int h = 0; h < G; ++h) l[h] = 0.0f;
+      for (int jj = tid; jj < n; jj += kAttnThreads)
 #pragma unroll
         for (int h = 0; h < G; ++h) {
-          const float w = sc[jj * G + h];
+          const float e = expf(sc[jj * G + h] - m[h]);
+          sc[jj * G + h] = e;
+          l[h] += e;
+        }
+      cta_reduce<G, false>(l, red);  // its barriers also publish sc
+
+      // ---- weighted values ----
+      if (!has_p && !__syncthreads_and(pipe::mbar_wait(&bar[1], 0u))) {
+        if (tid == 0) {
+          atomicOr(a.err, 4u);
+          if (!pipe::mbar_wait(&bar[1], 0u)) atomicOr(a.err, 2u);
+        }
+        __syncthreads();
+      }
+      float acc[G][8];
 #pragma unroll
-          for (int e = 0; e < 8; ++e) acc[h][e] = fmaf(w, vv[e], acc[h][e]);
+      for (int h = 0; h < G; ++h)
+#pragma unroll
+        for (int e = 0; e < 8; ++e) acc[h][e] = 0.0f;
+      for (int jb = 2 * warp; jb < n; jb += 2 * kAttnWarps) {
+        const int jj = jb + half;
+        if (jj < n) {
+          float vv[8];
+          bf16x8_to_f32(*reinterpret_cast<const uint4 *>(
+                            vst + size_t(jj) * D + 8 * hl),
+                        vv);
+#pragma unroll
+          for (int h = 0; h < G; ++h) {
+            const float w = sc[jj * G + h];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) acc[h][e] = fmaf(w, vv[e], acc[h][e]);
+          }
         }
       }
-    }
-#pragma unroll
-    for (int h = 0; h < G; ++h)
-#pragma unroll
-      for (int e = 0; e < 8; ++e)
-        acc[h][e] += __shfl_xor_sync(0xffffffffu, acc[h][e], 16);
-    if (half == 0)
 #pragma unroll
       for (int h = 0; h < G; ++h)
 #pragma unroll
         for (int e = 0; e < 8; ++e)
-          wacc[(warp * G + h) * D + 8 * hl + e] = acc[h][e];
-    __syncthreads();
+          acc[h][e] += __shfl_xor_sync(0xffffffffu, acc[h][e], 16);
+      if (half == 0)
 #pragma unroll
-    for (int h = 0; h < G; ++h) {  // thread tid: dim tid of every head
-      float t = wacc[h * D + tid];
+        for (int h = 0; h < G; ++h)
 #pragma unroll
-      for (int w = 1; w < kAttnWarps; ++w) t += wacc[(w * G + h) * D + tid];
-      part[h * (D + 2) + 2 + tid] = t;
-      if (tid == h) {
-        part[h * (D + 2)] = m[h];
-        part[h * (D + 2) + 1] = l[h];
+          for (int e = 0; e < 8; ++e)
+            wacc[(warp * G + h) * D + 8 * hl + e] = acc[h][e];
+      __syncthreads();
+      for (int e = tid; e < G * D; e += kAttnThreads) {
+        float t = wacc[e];
+#pragma unroll
+        for (int w = 1; w < kAttnWarps; ++w) t += wacc[w * G * D + e];
+        part[e] = t;  // [h][d]: e = h D + d
+      }
+      if (tid < G) {
+#pragma unroll
+        for (int h = 0; h < G; ++h)
+          if (tid == h) {
+            part[P::kM + h] = m[h];
+            part[P::kL + h] = l[h];
+          }
       }
     }
   }
@@ -319,39 +389,101 @@ attn_decode_kernel(const AttnArgs a) {
   if (tid == 0) a.count[g] = 0u;  // every CTA of this step has counted
   float *o = a.out + size_t(g) * G * D;
   if (!valid) {
-#pragma unroll
-    for (int h = 0; h < G; ++h) o[h * D + tid] = 0.0f;
+    for (int e = tid; e < G * D; e += kAttnThreads) o[e] = 0.0f;
     if (tid == 0) atomicOr(a.err, kAttnErrPosition);
     return;
   }
-  const float *pbase = a.part + size_t(g) * a.n_split * G * (D + 2);
-  float mx[G], ls[G];
+  const float *pbase = a.part + size_t(g) * a.n_split * P::kStride;
+  // Thread (lane s, vec v) sums the splits s, s + kLanesPerVec, ... of
+  // float4 v of the [G][D] block.  Its first 16 splits' outputs are loaded
+  // before the weights are known: they do not depend on them.
+  constexpr int kVec = G * D / 4;
+  constexpr int kLanesPerVec = kAttnThreads / kVec;
+  static_assert(kLanesPerVec * kVec == kAttnThreads, "vec lanes");
+  const int v = tid % kVec, s_lane = tid / kVec;
+  const int hv = v / (D / 4);
+  float4 x[16];
+#pragma unroll
+  for (int u = 0; u < 16; ++u) {
+    const int cc = s_lane + u * kLanesPerVec;
+    x[u] = cc < n_eff ? __ldcg(reinterpret_cast<const float4 *>(
+                                   pbase + size_t(cc) * P::kStride) + v)
+                      : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+  }
+  // Every split's m and l at once; weights w_c = e^(m_c - M) and the sums
+  // sum_c w_c l_c, kept in the staging rows (free now).
+  float *wgt = reinterpret_cast<float *>(smem + L::kK);  // [n_eff][G]
+  float *lbuf = wgt + kAttnMaxSplits * G;                 // [n_eff][G]
+  float *lsum = lbuf + kAttnMaxSplits * G;                // [G]
+  float mx[G];
 #pragma unroll
   for (int h = 0; h < G; ++h) mx[h] = -INFINITY;
-  for (int cc = tid; cc < n_eff; cc += kAttnThreads)
+  for (int e = tid; e < n_eff * G; e += kAttnThreads) {
+    const int cc = e / G, h = e - cc * G;
+    const float *pc = pbase + size_t(cc) * P::kStride;
+    const float mv = __ldcg(pc + P::kM + h);
+    wgt[e] = mv;
+    lbuf[e] = __ldcg(pc + P::kL + h);
 #pragma unroll
-    for (int h = 0; h < G; ++h)
-      mx[h] = fmaxf(mx[h], __ldcg(pbase + (size_t(cc) * G + h) * (D + 2)));
-  cta_reduce<G, true>(mx, red);
-  float *wgt = sc;  // [n_eff][G] merge weights (n_eff <= 128 <= chunk)
+    for (int hh = 0; hh < G; ++hh)
+      if (hh == h) mx[hh] = fmaxf(mx[hh], mv);
+  }
+  cta_reduce<G, true>(mx, red);  // its barriers also publish wgt and lbuf
+  float ls[G];
 #pragma unroll
   for (int h = 0; h < G; ++h) ls[h] = 0.0f;
-  for (int cc = tid; cc < n_eff; cc += kAttnThreads)
+  for (int e = tid; e < n_eff * G; e += kAttnThreads) {
+    const int h = e % G;
+    float w = 0.0f;
 #pragma unroll
-    for (int h = 0; h < G; ++h) {
-      const float *pc = pbase + (size_t(cc) * G + h) * (D + 2);
-      const float w = expf(__ldcg(pc) - mx[h]);
-      wgt[cc * G + h] = w;
-      ls[h] += w * __ldcg(pc + 1);
-    }
+    for (int hh = 0; hh < G; ++hh)
+      if (hh == h) w = expf(wgt[e] - mx[hh]);
+    wgt[e] = w;  // the element this thread read
+#pragma unroll
+    for (int hh = 0; hh < G; ++hh)
+      if (hh == h) ls[hh] = fmaf(w, lbuf[e], ls[hh]);
+  }
   cta_reduce<G, false>(ls, red);  // its barriers also publish wgt
+  if (tid < G) {
 #pragma unroll
-  for (int h = 0; h < G; ++h) {  // thread tid: dim tid of every head
-    float t = 0.0f;
-    for (int cc = 0; cc < n_eff; ++cc)
-      t = fmaf(wgt[cc * G + h],
-               __ldcg(pbase + (size_t(cc) * G + h) * (D + 2) + 2 + tid), t);
-    o[h * D + tid] = t / ls[h];
+    for (int h = 0; h < G; ++h)
+      if (tid == h) lsum[h] = ls[h];
+  }
+  float4 t = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+  for (int c0 = s_lane;; c0 += 16 * kLanesPerVec) {
+#pragma unroll
+    for (int u = 0; u < 16; ++u) {
+      const int cc = c0 + u * kLanesPerVec;
+      const float w = cc < n_eff ? wgt[cc * G + hv] : 0.0f;
+      t.x = fmaf(w, x[u].x, t.x);
+      t.y = fmaf(w, x[u].y, t.y);
+      t.z = fmaf(w, x[u].z, t.z);
+      t.w = fmaf(w, x[u].w, t.w);
+    }
+    if (c0 + 16 * kLanesPerVec >= n_eff) break;
+#pragma unroll
+    for (int u = 0; u < 16; ++u) {  // the next 16 splits of this lane
+      const int cc = c0 + (16 + u) * kLanesPerVec;
+      x[u] = cc < n_eff ? __ldcg(reinterpret_cast<const float4 *>(
+                                     pbase + size_t(cc) * P::kStride) + v)
+                        : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+    }
+  }
+  float4 *mergebuf = reinterpret_cast<float4 *>(wacc);  // [lanes][kVec]
+  mergebuf[s_lane * kVec + v] = t;
+  __syncthreads();
+  if (tid < kVec) {  // output float4 tid: the lanes' sums in order
+    float4 sum = mergebuf[tid];
+    for (int sl = 1; sl < kLanesPerVec; ++sl) {
+      const float4 u = mergebuf[sl * kVec + tid];
+      sum.x += u.x;
+      sum.y += u.y;
+      sum.z += u.z;
+      sum.w += u.w;
+    }
+    const float inv = lsum[tid / (D / 4)];
+    reinterpret_cast<float4 *>(o)[tid] =
+        make_float4(sum.x / inv, sum.y / inv, sum.z / inv, sum.w / inv);
   }
 }
 
@@ -383,9 +515,10 @@ cudaError_t launch_g(const AttnArgs &a, cudaStream_t stream) {
   return cudaLaunchKernelEx(&cfg, kernel, a);
 }
 
+// Partials for the most splits any device uses for this cache.
 size_t part_bytes(int H, int Hkv, int S) {
-  const size_t b = size_t(Hkv) * attn_splits(S) * size_t(H / Hkv) *
-                   (kAttnD + 2) * sizeof(float);
+  const size_t b = size_t(Hkv) * max_splits(S) * size_t(H / Hkv) *
+                   (kAttnD + 4) * sizeof(float);
   return (b + 255) / 256 * 256;
 }
 
@@ -442,7 +575,12 @@ extern "C" bw_status bw_attn_decode(const bw_bf16 *qkv, const int *pos, int H,
   a.H = H;
   a.Hkv = Hkv;
   a.S = S;
-  a.n_split = attn_splits(S);
+  const int sms = device_sm_count();
+  if (sms <= 0) {
+    record_cuda_error(int(cudaErrorNoDevice));
+    return BW_ERR_CUDA;
+  }
+  a.n_split = attn_splits(S, Hkv, sms);
   a.inv_sqrt_d = float(1.0 / sqrt(double(D)));
   for (int i = 0; i < kAttnPairs; ++i)
     a.freq[i] = float(pow(double(theta), -2.0 * i / double(D)));

@@ -203,11 +203,12 @@ def test_attn_workspace_and_host_validation(lib):
     wsb = lib.bw_attn_workspace_bytes
     wsb.restype = ctypes.c_size_t
     wsb.argtypes = [ctypes.c_int] * 4
-    # BitNet-2B: 5 KV heads x 4 query heads, 64 splits of a 4096 cache:
-    # [5][64][4][130] floats of partials (256-byte rounded) + 5 counters.
-    assert wsb(20, 5, 128, 4096) == 5 * 64 * 4 * 130 * 4 + 5 * 4
-    assert wsb(20, 5, 128, 65536) == 5 * 128 * 4 * 130 * 4 + 5 * 4
-    assert wsb(20, 5, 128, 10) == (5 * 4 * 130 * 4 + 255) // 256 * 256 + 20
+    # BitNet-2B: 5 KV heads x 4 query heads; room for the most splits any
+    # device uses, one per 64 positions of a 4096 cache: [5][64] partials
+    # of 4 x (128 + 4) floats (256-byte rounded), then 5 counters.
+    assert wsb(20, 5, 128, 4096) == 5 * 64 * 4 * 132 * 4 + 5 * 4
+    assert wsb(20, 5, 128, 65536) == 5 * 1024 * 4 * 132 * 4 + 5 * 4
+    assert wsb(20, 5, 128, 10) == (5 * 4 * 132 * 4 + 255) // 256 * 256 + 20
     assert wsb(20, 5, 64, 4096) == 0          # head dim other than 128
     assert wsb(12, 4, 128, 4096) == 0         # 3 query heads per KV head
     assert wsb(20, 5, 128, 65537) == 0
