@@ -81,6 +81,10 @@ def _load():
             "or_rope": (ctypes.c_int, [P, I64, I64, F, P]),
             "or_attn_decode": (ctypes.c_int, [P, I64, I64, I64, I64, F, P, P,
                                               I64, P]),
+            "or_attn_append": (ctypes.c_int, [P, I64, I64, I64, I64, F, P, P,
+                                              I64]),
+            "or_attn_over_cache": (ctypes.c_int, [P, I64, I64, I64, I64, F, P,
+                                                  P, I64, P]),
         }
         for name, (res, args) in sig.items():
             fn = getattr(lib, name)
@@ -268,3 +272,31 @@ def attn_decode(qkv_bits, H: int, Hkv: int, D: int, p: int, theta: float,
                                   _ptr(kc), _ptr(vc), S, _ptr(out)),
            "attn_decode")
     return out, kc.reshape(Hkv, S, D), vc.reshape(Hkv, S, D)
+
+
+def attn_append(qkv_bits, H: int, Hkv: int, D: int, p: int, theta: float,
+                kc_bits, vc_bits):
+    """The cache append of a decode step alone: returns updated copies of
+    the key and value caches [Hkv][S][D]."""
+    qkv_bits = _c(qkv_bits, np.uint16).reshape(-1)
+    kc = _c(kc_bits, np.uint16).copy()
+    vc = _c(vc_bits, np.uint16).copy()
+    S = kc.size // (Hkv * D)
+    _check(_load().or_attn_append(_ptr(qkv_bits), H, Hkv, D, p, theta,
+                                  _ptr(kc), _ptr(vc), S), "attn_append")
+    return kc.reshape(Hkv, S, D), vc.reshape(Hkv, S, D)
+
+
+def attn_over_cache(qkv_bits, H: int, Hkv: int, D: int, p: int,
+                    theta: float, kc_bits, vc_bits) -> np.ndarray:
+    """The attention of a decode step over the cache as given (rows 0..p
+    already hold the new token): fp64 out [H][D]."""
+    qkv_bits = _c(qkv_bits, np.uint16).reshape(-1)
+    kc = _c(kc_bits, np.uint16)
+    vc = _c(vc_bits, np.uint16)
+    S = kc.size // (Hkv * D)
+    out = np.empty((H, D), np.float64)
+    _check(_load().or_attn_over_cache(_ptr(qkv_bits), H, Hkv, D, p, theta,
+                                      _ptr(kc), _ptr(vc), S, _ptr(out)),
+           "attn_over_cache")
+    return out

@@ -478,39 +478,50 @@ int or_rope(const uint16_t *x, int64_t D, int64_t p, float theta,
     return OR_OK;
 }
 
-/* One decode step of grouped-query attention for one sequence.
- *   qkv  bf16 [(H + 2 Hkv) D]: q heads, then k heads, then v heads (the
- *        fused wqkv output of the layer).
- *   kc, vc  bf16 [Hkv][S][D]: the cache; positions 0..p-1 hold the earlier
- *        tokens' rotated keys and values.
- * Steps: (1) the new key of KV head g is rotated at position p and stored
- * at kc[g][p] (rounded to bf16, nearest even), the new value is stored at
- * vc[g][p] as it is; (2) query head h, which reads KV head g = h / (H/Hkv),
- * is rotated at p; (3) scores s_j = q'.kc[g][j] / sqrt(D) for j = 0..p;
- * (4) out[h] = sum_j softmax(s)_j vc[g][j].  All arithmetic in fp64; the
- * softmax subtracts the largest score.  out: fp64 [H][D]. */
-int or_attn_decode(const uint16_t *qkv, int64_t H, int64_t Hkv, int64_t D,
+/* The cache append of one decode step: the new key of KV head g (qkv[H D +
+ * g D ..]) is rotated at position p and stored at kc[g][p], rounded to bf16
+ * (nearest even); the new value (qkv[(H + Hkv) D + g D ..]) is stored at
+ * vc[g][p] as it is.  kc, vc: bf16 [Hkv][S][D]. */
+int or_attn_append(const uint16_t *qkv, int64_t H, int64_t Hkv, int64_t D,
                    int64_t p, float theta, uint16_t *kc, uint16_t *vc,
-                   int64_t S, double *out)
+                   int64_t S)
 {
     if (H < 1 || Hkv < 1 || H % Hkv != 0 || D < 2 || D % 2 != 0 ||
         p < 0 || p >= S)
         return OR_BAD_ARG;
-    int64_t G = H / Hkv;
     const uint16_t *kn = qkv + H * D, *vn = qkv + (H + Hkv) * D;
     double *rot = malloc(sizeof(double) * (size_t)D);
-    double *sc = malloc(sizeof(double) * (size_t)(p + 1));
-    if (!rot || !sc) {
-        free(rot);
-        free(sc);
-        return OR_BAD_ARG;
-    }
+    if (!rot) return OR_BAD_ARG;
     for (int64_t g = 0; g < Hkv; g++) {
         or_rope(kn + g * D, D, p, theta, rot);
         for (int64_t d = 0; d < D; d++) {
             kc[(g * S + p) * D + d] = or_bf16_rne_d(rot[d]);
             vc[(g * S + p) * D + d] = vn[g * D + d];
         }
+    }
+    free(rot);
+    return OR_OK;
+}
+
+/* Attention of the step over the cache as it stands (rows 0..p, the new
+ * token's row included): query head h (qkv[h D ..]) is rotated at p and
+ * reads KV head g = h / (H / Hkv); s_j = q'.kc[g][j] / sqrt(D);
+ * out[h] = sum_j softmax(s)_j vc[g][j].  fp64, the softmax subtracting the
+ * largest score.  out: fp64 [H][D]. */
+int or_attn_over_cache(const uint16_t *qkv, int64_t H, int64_t Hkv,
+                       int64_t D, int64_t p, float theta, const uint16_t *kc,
+                       const uint16_t *vc, int64_t S, double *out)
+{
+    if (H < 1 || Hkv < 1 || H % Hkv != 0 || D < 2 || D % 2 != 0 ||
+        p < 0 || p >= S)
+        return OR_BAD_ARG;
+    int64_t G = H / Hkv;
+    double *rot = malloc(sizeof(double) * (size_t)D);
+    double *sc = malloc(sizeof(double) * (size_t)(p + 1));
+    if (!rot || !sc) {
+        free(rot);
+        free(sc);
+        return OR_BAD_ARG;
     }
     double scale = 1.0 / sqrt((double)D);
     for (int64_t h = 0; h < H; h++) {
@@ -539,4 +550,19 @@ int or_attn_decode(const uint16_t *qkv, int64_t H, int64_t Hkv, int64_t D,
     free(rot);
     free(sc);
     return OR_OK;
+}
+
+/* One decode step of grouped-query attention for one sequence: the append,
+ * then the attention over positions 0..p.
+ *   qkv  bf16 [(H + 2 Hkv) D]: q heads, then k heads, then v heads (the
+ *        fused wqkv output of the layer).
+ *   kc, vc  bf16 [Hkv][S][D]: the cache; positions 0..p-1 hold the earlier
+ *        tokens' rotated keys and values; row p is written. */
+int or_attn_decode(const uint16_t *qkv, int64_t H, int64_t Hkv, int64_t D,
+                   int64_t p, float theta, uint16_t *kc, uint16_t *vc,
+                   int64_t S, double *out)
+{
+    int rc = or_attn_append(qkv, H, Hkv, D, p, theta, kc, vc, S);
+    if (rc) return rc;
+    return or_attn_over_cache(qkv, H, Hkv, D, p, theta, kc, vc, S, out);
 }
