@@ -73,6 +73,11 @@ def parse_args():
                    help="skip the decode-attention timings")
     p.add_argument("--attn", action="store_true",
                    help="only time the decode attention (us/call, KV GB/s)")
+    p.add_argument("--attn-contexts", default=None, metavar="L[,L...]",
+                   help="--attn: context lengths (default 512,4096)")
+    p.add_argument("--attn-rotate", type=int, default=0,
+                   help="--attn: caches per graph (0: the read rows of "
+                        "4x L2)")
     p.add_argument("--stack", action="store_true",
                    help="only time the 30-layer decode stack (tok/s)")
     p.add_argument("--stack-layers", type=int, default=None,
@@ -751,7 +756,7 @@ ATTN_THETA = 500000.0
 
 
 def run_attn_timing(torch, bw, dev, peak_gbs, contexts=ATTN_CONTEXTS,
-                    iters=1024):
+                    iters=1024, rotate=0):
     """bw_attn_decode at the BitNet-2B attention shape (20 query heads over
     5 KV heads of 128, a 4096-position bf16 cache) for contexts of L tokens
     (the new token at position L - 1): us per call in a graph of calls back
@@ -779,7 +784,7 @@ def run_attn_timing(torch, bw, dev, peak_gbs, contexts=ATTN_CONTEXTS,
     stream = torch.cuda.Stream(device=dev)
     for L in contexts:
         kv_bytes = 2 * Hkv * L * D * 2
-        rot = max(2, -(-4 * 126 * 2**20 // kv_bytes))
+        rot = rotate or max(2, -(-4 * 126 * 2**20 // kv_bytes))
         kcs = kc0.unsqueeze(0).repeat(rot, 1, 1, 1)
         vcs = vc0.unsqueeze(0).repeat(rot, 1, 1, 1)
         pos = torch.tensor([L - 1], dtype=torch.int32, device=dev)
@@ -855,8 +860,12 @@ def main():
         dev = torch.device("cuda", 0)
         torch.cuda.set_device(dev)
         peak, _ = read_peaks()
-        print(json.dumps({"attn_decode": run_attn_timing(torch, bw, dev,
-                                                         peak)}), flush=True)
+        ctx = (tuple(int(v) for v in args.attn_contexts.split(","))
+               if args.attn_contexts else ATTN_CONTEXTS)
+        print(json.dumps({"attn_decode": run_attn_timing(
+            torch, bw, dev, peak, contexts=ctx,
+            iters=min(args.iters, 1024), rotate=args.attn_rotate)}),
+            flush=True)
     elif args.stack and args.impl != "reference":
         import torch
         import bit_gemv_bitlinear_gb300 as bw

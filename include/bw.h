@@ -310,8 +310,8 @@ void bw_stack_destroy(bw_stack *stack);
  *      over j = 0..p.
  * RoPE: pair (x[2i], x[2i+1]) turns by the angle p * f_i, f_i =
  * theta^(-2i/D); f_i is rounded to fp32 and the angle is the fp32 product
- * (the pages leave the precision open; BitNet-2B's published configuration
- * uses theta = 500000).  Scores, softmax and sums are fp32.
+ * (the pages give neither the base theta nor the precision; theta is an
+ * argument).  Scores, softmax and sums are fp32.
  *   qkv       bf16 [(H + 2 Hkv) D] device, 2-byte aligned: q | k | v, the
  *             fused wqkv output of the layer.
  *   pos       int32 [1] device: the position p of the new token; read on the
