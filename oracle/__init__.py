@@ -85,6 +85,9 @@ def _load():
                                               I64]),
             "or_attn_over_cache": (ctypes.c_int, [P, I64, I64, I64, I64, F, P,
                                                   P, I64, P]),
+            "or_layer_kv": (ctypes.c_int, [P, I64, I64, I64, I64, F,
+                                           P, P, P, P, P, P, P, P, P, I64,
+                                           I64, F]),
         }
         for name, (res, args) in sig.items():
             fn = getattr(lib, name)
@@ -300,3 +303,23 @@ def attn_over_cache(qkv_bits, H: int, Hkv: int, D: int, p: int,
                                       _ptr(kc), _ptr(vc), S, _ptr(out)),
            "attn_over_cache")
     return out
+
+
+def layer_kv(h, dim, ffn, n_heads, n_kv, eps, wqkv, wo, w13, w2, ws_bits,
+             gammas, kc_bits, vc_bits, p: int, theta: float):
+    """One decoder layer with attention over its KV cache at position p:
+    returns (h after the layer, the updated key cache, value cache)."""
+    h = _c(h, np.float32).reshape(-1).copy()
+    ws_bits = _c(ws_bits, np.uint16).reshape(-1)
+    gammas = _c(gammas, np.float32).reshape(-1)
+    mats = [_c(m, np.uint8) for m in (wqkv, wo, w13, w2)]
+    kc = _c(kc_bits, np.uint16).copy()
+    vc = _c(vc_bits, np.uint16).copy()
+    S = kc.size // (n_kv * (dim // n_heads))
+    scratch = np.zeros((4 * ffn,), np.float32)
+    rc = _load().or_layer_kv(_ptr(h), dim, ffn, n_heads, n_kv, eps,
+                             *[_ptr(m) for m in mats], _ptr(ws_bits),
+                             _ptr(gammas), _ptr(scratch), _ptr(kc), _ptr(vc),
+                             S, p, theta)
+    _check(rc, "layer_kv")
+    return h, kc.reshape(kc_bits.shape), vc.reshape(vc_bits.shape)

@@ -361,64 +361,6 @@ static int norm_quant_gemv(const float *x, const float *gamma, int64_t K,
     return or_gemv(q, canon, s, ws, bounds, n_ws, 1, N, K, y);
 }
 
-/*
- * One decoder layer of the stack, M = 1, in the order of the BitNet block:
- *   a = attn_norm(h) -> quant -> wqkv -> one-token attention
- *   b = attn_sub_norm(attn) -> quant -> wo;          h += b
- *   c = ffn_norm(h) -> quant -> w13 -> relu(gate)^2 * up
- *   d = ffn_sub_norm(g) -> quant -> w2;              h += d
- * h (fp32, length dim) is updated in place; residual adds are fp32.
- * gammas: 4 vectors (attn_norm[dim], attn_sub[dim], ffn_norm[dim],
- * ffn_sub[ffn]) concatenated.  ws: wqkv 3 values, wo 1, w13 2, w2 1.
- * scratch must hold 4*ffn floats; the fused qkv width must not exceed 2*ffn.
- */
-int or_layer(float *h, int64_t dim, int64_t ffn, int64_t n_heads,
-             int64_t n_kv, float eps,
-             const uint8_t *wqkv, const uint8_t *wo, const uint8_t *w13,
-             const uint8_t *w2, const uint16_t *ws, const float *gammas,
-             float *scratch)
-{
-    int64_t hd = dim / n_heads;
-    int64_t qkv_n = (n_heads + 2 * n_kv) * hd;
-    int32_t b_qkv[4] = {0, (int32_t)(n_heads * hd),
-                        (int32_t)((n_heads + n_kv) * hd), (int32_t)qkv_n};
-    int32_t b_o[2] = {0, (int32_t)dim};
-    int32_t b_13[3] = {0, (int32_t)ffn, (int32_t)(2 * ffn)};
-    int32_t b_2[2] = {0, (int32_t)dim};
-    const float *g_attn = gammas, *g_asub = gammas + dim;
-    const float *g_ffn = gammas + 2 * dim, *g_fsub = gammas + 3 * dim;
-
-    float *normed = scratch;                 /* up to ffn floats   */
-    float *vec = scratch + ffn;              /* up to ffn floats   */
-    int8_t *q = (int8_t *)(scratch + 2 * ffn);   /* ffn bytes      */
-    uint16_t *y = (uint16_t *)(scratch + 3 * ffn);  /* up to 2 ffn */
-    float s;
-    int rc;
-
-    if (n_heads * hd != dim) return OR_BAD_ARG;
-    if (qkv_n > 2 * ffn || dim > ffn) return OR_BAD_ARG;
-
-    rc = norm_quant_gemv(h, g_attn, dim, eps, wqkv, ws + 0, b_qkv, 3, qkv_n,
-                         normed, q, &s, y);
-    if (rc) return rc;
-    rc = or_attn_one_token(y, n_heads, n_kv, hd, vec);
-    if (rc) return rc;
-    rc = norm_quant_gemv(vec, g_asub, dim, eps, wo, ws + 3, b_o, 1, dim,
-                         normed, q, &s, y);
-    if (rc) return rc;
-    for (int64_t i = 0; i < dim; i++) h[i] = h[i] + or_bf16_value(y[i]);
-
-    rc = norm_quant_gemv(h, g_ffn, dim, eps, w13, ws + 4, b_13, 2, 2 * ffn,
-                         normed, q, &s, y);
-    if (rc) return rc;
-    or_relu2_gate(y, ffn, vec);
-    rc = norm_quant_gemv(vec, g_fsub, ffn, eps, w2, ws + 6, b_2, 1, dim,
-                         normed, q, &s, y);
-    if (rc) return rc;
-    for (int64_t i = 0; i < dim; i++) h[i] = h[i] + or_bf16_value(y[i]);
-    return OR_OK;
-}
-
 /* ------------------------------------------------------------------ */
 /* GQA decode attention over a KV cache ([W2A8] §一: 20 query heads,    */
 /* 5 KV heads, head_dim 128; §4.1: RoPE rotates adjacent pairs of head */
@@ -566,3 +508,107 @@ int or_attn_decode(const uint16_t *qkv, int64_t H, int64_t Hkv, int64_t D,
     if (rc) return rc;
     return or_attn_over_cache(qkv, H, Hkv, D, p, theta, kc, vc, S, out);
 }
+
+/* ------------------------------------------------------------------ */
+/* Decoder layer with attention over a KV cache ([W2A8] §一, §4.1, §六)  */
+/* ------------------------------------------------------------------ */
+
+/*
+ * One decoder layer of the stack, M = 1, in the order of the BitNet block:
+ *   a = attn_norm(h) -> quant -> wqkv -> one-token attention
+ *      (or attention over a KV cache, or_layer_kv)
+ *   b = attn_sub_norm(attn) -> quant -> wo;          h += b
+ *   c = ffn_norm(h) -> quant -> w13 -> relu(gate)^2 * up
+ *   d = ffn_sub_norm(g) -> quant -> w2;              h += d
+ * h (fp32, length dim) is updated in place; residual adds are fp32.
+ * gammas: 4 vectors (attn_norm[dim], attn_sub[dim], ffn_norm[dim],
+ * ffn_sub[ffn]) concatenated.  ws: wqkv 3 values, wo 1, w13 2, w2 1.
+ * scratch must hold 4*ffn floats; the fused qkv width must not exceed 2*ffn.
+ */
+static int layer_impl(float *h, int64_t dim, int64_t ffn, int64_t n_heads,
+                      int64_t n_kv, float eps,
+                      const uint8_t *wqkv, const uint8_t *wo,
+                      const uint8_t *w13, const uint8_t *w2,
+                      const uint16_t *ws, const float *gammas, float *scratch,
+                      uint16_t *kc, uint16_t *vc, int64_t S, int64_t p,
+                      float theta)
+{
+    int64_t hd = dim / n_heads;
+    int64_t qkv_n = (n_heads + 2 * n_kv) * hd;
+    int32_t b_qkv[4] = {0, (int32_t)(n_heads * hd),
+                        (int32_t)((n_heads + n_kv) * hd), (int32_t)qkv_n};
+    int32_t b_o[2] = {0, (int32_t)dim};
+    int32_t b_13[3] = {0, (int32_t)ffn, (int32_t)(2 * ffn)};
+    int32_t b_2[2] = {0, (int32_t)dim};
+    const float *g_attn = gammas, *g_asub = gammas + dim;
+    const float *g_ffn = gammas + 2 * dim, *g_fsub = gammas + 3 * dim;
+
+    float *normed = scratch;                 /* up to ffn floats   */
+    float *vec = scratch + ffn;              /* up to ffn floats   */
+    int8_t *q = (int8_t *)(scratch + 2 * ffn);   /* ffn bytes      */
+    uint16_t *y = (uint16_t *)(scratch + 3 * ffn);  /* up to 2 ffn */
+    float s;
+    int rc;
+
+    if (n_heads * hd != dim) return OR_BAD_ARG;
+    if (qkv_n > 2 * ffn || dim > ffn) return OR_BAD_ARG;
+
+    rc = norm_quant_gemv(h, g_attn, dim, eps, wqkv, ws + 0, b_qkv, 3, qkv_n,
+                         normed, q, &s, y);
+    if (rc) return rc;
+    if (!kc) {
+        rc = or_attn_one_token(y, n_heads, n_kv, hd, vec);
+    } else {
+        double *att = malloc(sizeof(double) * (size_t)dim);
+        if (!att) return OR_BAD_ARG;
+        rc = or_attn_decode(y, n_heads, n_kv, hd, p, theta, kc, vc, S, att);
+        for (int64_t i = 0; i < dim && rc == OR_OK; i++)
+            vec[i] = (float)att[i];
+        free(att);
+    }
+    if (rc) return rc;
+    rc = norm_quant_gemv(vec, g_asub, dim, eps, wo, ws + 3, b_o, 1, dim,
+                         normed, q, &s, y);
+    if (rc) return rc;
+    for (int64_t i = 0; i < dim; i++) h[i] = h[i] + or_bf16_value(y[i]);
+
+    rc = norm_quant_gemv(h, g_ffn, dim, eps, w13, ws + 4, b_13, 2, 2 * ffn,
+                         normed, q, &s, y);
+    if (rc) return rc;
+    or_relu2_gate(y, ffn, vec);
+    rc = norm_quant_gemv(vec, g_fsub, ffn, eps, w2, ws + 6, b_2, 1, dim,
+                         normed, q, &s, y);
+    if (rc) return rc;
+    for (int64_t i = 0; i < dim; i++) h[i] = h[i] + or_bf16_value(y[i]);
+    return OR_OK;
+}
+
+
+int or_layer(float *h, int64_t dim, int64_t ffn, int64_t n_heads,
+             int64_t n_kv, float eps,
+             const uint8_t *wqkv, const uint8_t *wo, const uint8_t *w13,
+             const uint8_t *w2, const uint16_t *ws, const float *gammas,
+             float *scratch)
+{
+    return layer_impl(h, dim, ffn, n_heads, n_kv, eps, wqkv, wo, w13, w2, ws,
+                      gammas, scratch, NULL, NULL, 0, 0, 0.0f);
+}
+
+/* The same layer with grouped-query attention over the layer's KV cache
+ * (kc, vc: bf16 [n_kv][S][hd]) at position p in place of the one-token
+ * attention: the decode step of or_attn_decode on the bf16 wqkv output,
+ * its fp64 result rounded to fp32 as the input of attn_sub_norm.  At p = 0
+ * the attention returns the value heads exactly, so the layer equals
+ * or_layer. */
+int or_layer_kv(float *h, int64_t dim, int64_t ffn, int64_t n_heads,
+                int64_t n_kv, float eps,
+                const uint8_t *wqkv, const uint8_t *wo, const uint8_t *w13,
+                const uint8_t *w2, const uint16_t *ws, const float *gammas,
+                float *scratch, uint16_t *kc, uint16_t *vc, int64_t S,
+                int64_t p, float theta)
+{
+    if (!kc || !vc) return OR_BAD_ARG;
+    return layer_impl(h, dim, ffn, n_heads, n_kv, eps, wqkv, wo, w13, w2, ws,
+                      gammas, scratch, kc, vc, S, p, theta);
+}
+

@@ -397,6 +397,75 @@ def test_layer_matches_stagewise_composition():
     assert not (out == h).all()
 
 
+def _tiny_cache(seed, nkv, S, hd):
+    c = synth.attn_case(seed, 1, 1, hd, S * nkv, 0)
+    return (c["kc"].reshape(nkv, S, hd).copy(),
+            c["vc"].reshape(nkv, S, hd).copy())
+
+
+def test_layer_kv_at_position_zero_is_the_one_token_layer():
+    """At p = 0 the attention over the cache returns the value heads
+    exactly, so the layer equals the one-token layer bit for bit."""
+    dim, ffn, nh, nkv, mats, ws, gam = _tiny_stack(zero=False)
+    h = synth.normal_f32(6, dim)
+    kc, vc = _tiny_cache(synth.base_seed(23), nkv, 8, dim // nh)
+    want = oracle.layer(h, dim, ffn, nh, nkv, 1e-5, mats["wqkv"], mats["wo"],
+                        mats["w13"], mats["w2"], ws, gam)
+    got, kc2, vc2 = oracle.layer_kv(h, dim, ffn, nh, nkv, 1e-5, mats["wqkv"],
+                                    mats["wo"], mats["w13"], mats["w2"], ws,
+                                    gam, kc, vc, 0, 10000.0)
+    assert (got == want).all()
+    assert (kc2[:, 1:] == kc[:, 1:]).all() and (vc2[:, 1:] == vc[:, 1:]).all()
+
+
+def test_layer_kv_matches_stagewise_composition():
+    """The layer with a cache equals its stages run one by one, with the
+    decode attention (append + attention over rows 0..p) after wqkv."""
+    dim, ffn, nh, nkv, mats, ws, gam = _tiny_stack(zero=False)
+    hd = dim // nh
+    qkv_n = (nh + 2 * nkv) * hd
+    h = synth.normal_f32(7, dim)
+    kc, vc = _tiny_cache(synth.base_seed(23, 1), nkv, 8, hd)
+    p, theta = 5, 500000.0
+    one = np.ones(max(dim, ffn), np.float32)
+
+    def nqg(v, canon, n_out, k, w_bits, bounds):
+        normed = oracle.rmsnorm(v, one[:k], 1e-5)
+        q, s = oracle.quant_act(normed)
+        return oracle.gemv(q, canon, s, w_bits, bounds, n_out, k)[0]
+
+    y = nqg(h, mats["wqkv"], qkv_n, dim, ws[0:3],
+            [0, nh * hd, (nh + nkv) * hd, qkv_n])
+    att, kc_s, vc_s = oracle.attn_decode(y, nh, nkv, hd, p, theta, kc, vc)
+    att = att.reshape(-1).astype(np.float32)
+    o = nqg(att, mats["wo"], dim, dim, ws[3:4], [0, dim])
+    h1 = (h + synth.bf16_bits_to_f32(o)).astype(np.float32)
+    gu = nqg(h1, mats["w13"], 2 * ffn, dim, ws[4:6], [0, ffn, 2 * ffn])
+    g = oracle.relu2_gate(gu)
+    d = nqg(g, mats["w2"], dim, ffn, ws[6:7], [0, dim])
+    h2 = (h1 + synth.bf16_bits_to_f32(d)).astype(np.float32)
+    out, kc2, vc2 = oracle.layer_kv(h, dim, ffn, nh, nkv, 1e-5, mats["wqkv"],
+                                    mats["wo"], mats["w13"], mats["w2"], ws,
+                                    gam, kc, vc, p, theta)
+    assert (out == h2).all()
+    assert (kc2 == kc_s).all() and (vc2 == vc_s).all()
+
+
+def test_layer_kv_ignores_rows_past_p():
+    dim, ffn, nh, nkv, mats, ws, gam = _tiny_stack(zero=False)
+    hd = dim // nh
+    h = synth.normal_f32(8, dim)
+    kc, vc = _tiny_cache(synth.base_seed(23, 2), nkv, 8, hd)
+    args = (dim, ffn, nh, nkv, 1e-5, mats["wqkv"], mats["wo"], mats["w13"],
+            mats["w2"], ws, gam)
+    base, _, _ = oracle.layer_kv(h, *args, kc, vc, 3, 10000.0)
+    kc_late, vc_late = kc.copy(), vc.copy()
+    kc_late[:, 4:] ^= 0x1234                 # rows past p: ignored
+    vc_late[:, 4:] ^= 0x0101
+    late, _, _ = oracle.layer_kv(h, *args, kc_late, vc_late, 3, 10000.0)
+    assert (late == base).all()
+
+
 # --------------------------------------------- absmean weight ternarisation
 # [W2A8] §4.2: s = 1 / max(mean|W|, 1e-5), w = clamp(round(W s), -1, 1),
 # ws = bf16(1 / s), one scale per weight-scale segment.
