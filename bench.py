@@ -84,6 +84,9 @@ def parse_args():
                    help="--stack: layers (default 30)")
     p.add_argument("--stack-steps", type=int, default=None,
                    help="--stack: decode steps per run (default 256)")
+    p.add_argument("--stack-kv", type=int, default=0, metavar="S",
+                   help="--stack: attend over a KV cache of S positions "
+                        "(the steps are tokens 0.. of one sequence)")
     p.add_argument("--cpu-seconds", type=float, default=12.0,
                    help="bounded CPU work for the oracle baseline")
     p.add_argument("--single", default=None, metavar="N,K[,M]",
@@ -422,9 +425,11 @@ def run_ours(args):
     e2e_ms = job_time_ms(torch, e_start.elapsed_time(e_end), world, dev) / K_steps
     e2e_value = job_value(world, wbytes_step, e2e_ms)
 
-    stack_line = None
+    stack_line = stack_kv_line = None
     if not args.no_stack:
         stack_line = run_stack_timing(torch, bw, dev)
+        stack_kv_line = run_stack_timing(torch, bw, dev,
+                                         kv_positions=ATTN_S)
     batched_line = None
     if rank == 0 and not args.no_batched:
         batched_line = run_batched(torch, bw, dev, peak)
@@ -485,6 +490,8 @@ def run_ours(args):
         }
         if stack_line is not None:
             line["layer_stack"] = stack_line
+        if stack_kv_line is not None:
+            line["layer_stack_kv"] = stack_kv_line
         if batched_line is not None:
             line["batched"] = batched_line
         if attn_line is not None:
@@ -500,12 +507,15 @@ STACK_LAYERS, STACK_STEPS = 30, 256
 
 
 def run_stack_timing(torch, bw, dev, n_layers=STACK_LAYERS,
-                     steps=STACK_STEPS, reps=3):
+                     steps=STACK_STEPS, reps=3, kv_positions=0):
     """The BitNet-2B-shaped decode layer stack (dim 2560, ffn 6912, 20/5
-    heads): `steps` independent decode steps through `n_layers` layers.
-    One layer's random ternary weights are generated and copied into
-    n_layers distinct device buffers (521 MB for 30 layers, so every step
-    streams all weights from HBM).  Returns tok/s and the derived figures."""
+    heads): `steps` decode steps through `n_layers` layers.  One layer's
+    random ternary weights are generated and copied into n_layers distinct
+    device buffers (521 MB for 30 layers, so every step streams all weights
+    from HBM).  kv_positions = 0: independent steps with the one-token
+    attention; > 0: a stack with a KV cache of that many positions, the
+    steps being tokens 0 .. steps - 1 of one sequence (the cache reset
+    before every timed run).  Returns tok/s and the derived figures."""
     dim, ffn, nh, nkv = 2560, 6912, 20, 5
     seed = synth.base_seed(4)
     w = synth.stack_weights(seed, 1, dim, ffn, nh, nkv)
@@ -519,7 +529,8 @@ def run_stack_timing(torch, bw, dev, n_layers=STACK_LAYERS,
     gam = torch.from_numpy(L0["gammas"]).to(dev)
     layers = [{k: (v if i == 0 else v.clone()) for k, v in base.items()}
               | {"ws": ws, "gammas": gam} for i in range(n_layers)]
-    stack = bw.Stack(layers, dim, ffn, nh, nkv, w["eps"])
+    stack = bw.Stack(layers, dim, ffn, nh, nkv, w["eps"],
+                     max_positions=kv_positions, theta=ATTN_THETA)
     h_in = torch.from_numpy(synth.step_inputs(seed, steps, dim)).to(dev)
     h_out = torch.empty_like(h_in)
     stream = torch.cuda.Stream(device=dev)
@@ -531,6 +542,8 @@ def run_stack_timing(torch, bw, dev, n_layers=STACK_LAYERS,
         e0 = torch.cuda.Event(enable_timing=True)
         e1 = torch.cuda.Event(enable_timing=True)
         with torch.cuda.stream(stream):
+            if kv_positions:
+                stack.reset_kv(stream=stream)
             e0.record(stream)
             stack.run(h_in, h_out, stream=stream)
             e1.record(stream)
@@ -541,12 +554,19 @@ def run_stack_timing(torch, bw, dev, n_layers=STACK_LAYERS,
     stack.close()
     layer_bytes = sum(int(base[k].numel()) for k in base)
     us_tok = best * 1e3 / steps
-    return {"layers": n_layers, "steps": steps, "tok_s": round(steps / (best * 1e-3), 1),
-            "us_per_token": round(us_tok, 2),
-            "weight_bytes_per_token": layer_bytes * n_layers,
-            "weight_GBps": round(layer_bytes * n_layers / (us_tok * 1e3), 1),
-            "launches_per_token": 4 * n_layers,
-            "timing": f"best of {reps} runs of {steps} steps, CUDA events"}
+    res = {"layers": n_layers, "steps": steps,
+           "tok_s": round(steps / (best * 1e-3), 1),
+           "us_per_token": round(us_tok, 2),
+           "weight_bytes_per_token": layer_bytes * n_layers,
+           "weight_GBps": round(layer_bytes * n_layers / (us_tok * 1e3), 1),
+           "launches_per_token": (5 if kv_positions else 4) * n_layers,
+           "timing": f"best of {reps} runs of {steps} steps, CUDA events"}
+    if kv_positions:
+        res["attention"] = (f"KV cache of {kv_positions} positions; tokens "
+                            f"0..{steps - 1} of one sequence per run")
+    else:
+        res["attention"] = "one-token context (independent steps)"
+    return res
 
 
 def per_shape_times(torch, bw, shapes, act, outs, R, stream, reps=50):
@@ -873,7 +893,8 @@ def main():
         torch.cuda.set_device(dev)
         print(json.dumps({"layer_stack": run_stack_timing(
             torch, bw, dev, args.stack_layers or STACK_LAYERS,
-            args.stack_steps or STACK_STEPS)}),
+            args.stack_steps or STACK_STEPS,
+            kv_positions=args.stack_kv)}),
               flush=True)
     elif args.impl == "reference":
         run_reference(args)

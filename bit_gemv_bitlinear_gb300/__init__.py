@@ -39,7 +39,8 @@ EXPORTS = ("bw_status_string", "bw_last_cuda_error", "bw_version",
            "bw_device_error", "bw_stack_create", "bw_layer_stack",
            "bw_stack_destroy", "bw_selftest_wait_timeout",
            "bw_gemv_workspace_bytes", "bw_quant_weight",
-           "bw_attn_workspace_bytes", "bw_attn_decode")
+           "bw_attn_workspace_bytes", "bw_attn_decode", "bw_stack_create_kv",
+           "bw_stack_read_kv", "bw_stack_reset_kv")
 
 _P = ctypes.c_void_p
 _I = ctypes.c_int
@@ -62,6 +63,9 @@ _SIGS = {
     "bw_selftest_wait_timeout": (_I, [_P, _P]),
     "bw_quant_weight": (_I, [_P, _I, _I, _P, _I, _P, _P, _P]),
     "bw_attn_workspace_bytes": (ctypes.c_size_t, [_I, _I, _I, _I]),
+    "bw_stack_create_kv": (_I, [_P, _I, ctypes.c_float, _P]),
+    "bw_stack_read_kv": (_I, [_P, _I, _P, _P, _P]),
+    "bw_stack_reset_kv": (_I, [_P, _P]),
     "bw_attn_decode": (_I, [_P, _P, _I, _I, _I, _I, ctypes.c_float, _P, _P,
                             _P, _P, ctypes.c_size_t, _P]),
 }
@@ -298,11 +302,16 @@ class Stack:
 
     layers: list of dicts with device tensors 'wqkv', 'wo', 'w13', 'w2'
     (uint8 device layouts from bw_repack), 'ws' (bf16 [7]) and 'gammas'
-    (fp32 [3 dim + ffn]).  The tensors must outlive the stack."""
+    (fp32 [3 dim + ffn]).  The tensors must outlive the stack.
+    max_positions > 0 makes a stack with a KV cache of that many positions
+    (bw_stack_create_kv, RoPE base theta): consecutive steps are then
+    consecutive tokens of one sequence."""
 
-    def __init__(self, layers, dim, ffn, n_heads, n_kv_heads, eps=1e-5):
+    def __init__(self, layers, dim, ffn, n_heads, n_kv_heads, eps=1e-5,
+                 max_positions=0, theta=500000.0):
         self.dim, self.ffn = dim, ffn
         self.n_heads, self.n_kv_heads = n_heads, n_kv_heads
+        self.max_positions = max_positions
         self._keep = layers
         L = len(layers)
         arr = lambda key, dt: (_P * L)(*[_dev(l[key], dt, key)
@@ -313,9 +322,31 @@ class Stack:
         desc = _StackDesc(L, dim, ffn, n_heads, n_kv_heads, eps,
                           *[ctypes.cast(a, _P) for a in self._arrays])
         handle = _P()
-        _check(_lib.bw_stack_create(ctypes.byref(desc), ctypes.byref(handle)),
-               "bw_stack_create")
+        if max_positions > 0:
+            _check(_lib.bw_stack_create_kv(ctypes.byref(desc), max_positions,
+                                           float(theta),
+                                           ctypes.byref(handle)),
+                   "bw_stack_create_kv")
+        else:
+            _check(_lib.bw_stack_create(ctypes.byref(desc),
+                                        ctypes.byref(handle)),
+                   "bw_stack_create")
         self._h = handle
+
+    def read_kv(self, layer: int, stream=None):
+        """(keys, values) of one layer's cache: bf16 [Hkv][S][128] copies."""
+        shape = (self.n_kv_heads, self.max_positions, 128)
+        k = torch.empty(shape, dtype=torch.bfloat16, device="cuda")
+        v = torch.empty(shape, dtype=torch.bfloat16, device="cuda")
+        _check(_lib.bw_stack_read_kv(self._h, layer, k.data_ptr(),
+                                     v.data_ptr(), _stream(stream)),
+               "bw_stack_read_kv")
+        return k, v
+
+    def reset_kv(self, stream=None):
+        """Start a new sequence at position 0."""
+        _check(_lib.bw_stack_reset_kv(self._h, _stream(stream)),
+               "bw_stack_reset_kv")
 
     def run(self, h_in: torch.Tensor, h_out: torch.Tensor | None = None,
             trace: dict | None = None, stream=None) -> torch.Tensor:

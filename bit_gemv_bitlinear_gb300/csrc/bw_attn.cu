@@ -70,6 +70,10 @@ struct AttnArgs {
   float inv_sqrt_d;
   float freq[kAttnPairs];    // f_i = theta^(-2i/D), fp32
   unsigned int *err;
+  // Optional (layer stack): statistics of the output for the next RMSNorm,
+  // one entry per KV head: (sum of out^2, max |out * norm_gamma|).
+  const float *norm_gamma;   // [H][D] or null
+  float2 *norm_part;         // [Hkv] or null
 };
 
 __host__ __device__ inline int max_splits(int S) {
@@ -390,7 +394,10 @@ attn_decode_kernel(const AttnArgs a) {
   float *o = a.out + size_t(g) * G * D;
   if (!valid) {
     for (int e = tid; e < G * D; e += kAttnThreads) o[e] = 0.0f;
-    if (tid == 0) atomicOr(a.err, kAttnErrPosition);
+    if (tid == 0) {
+      atomicOr(a.err, kAttnErrPosition);
+      if (a.norm_part) a.norm_part[g] = make_float2(0.0f, 0.0f);
+    }
     return;
   }
   const float *pbase = a.part + size_t(g) * a.n_split * P::kStride;
@@ -485,6 +492,23 @@ attn_decode_kernel(const AttnArgs a) {
     reinterpret_cast<float4 *>(o)[tid] =
         make_float4(sum.x / inv, sum.y / inv, sum.z / inv, sum.w / inv);
   }
+  if (a.norm_part) {
+    // The next RMSNorm's partial statistics over this head's G D outputs
+    // (each thread re-reads what it stored), in a fixed order.
+    float ss = 0.0f, amx = 0.0f;
+    if (tid < kVec) {
+      const float4 y = reinterpret_cast<const float4 *>(o)[tid];
+      const float4 gm = reinterpret_cast<const float4 *>(
+          a.norm_gamma + size_t(g) * G * D)[tid];
+      ss = y.x * y.x + y.y * y.y + y.z * y.z + y.w * y.w;
+      amx = fmaxf(fmaxf(fabsf(__fmul_rn(y.x, gm.x)), fabsf(__fmul_rn(y.y, gm.y))),
+                  fmaxf(fabsf(__fmul_rn(y.z, gm.z)), fabsf(__fmul_rn(y.w, gm.w))));
+    }
+    float v1[1] = {ss}, v2[1] = {amx};
+    cta_reduce<1, false>(v1, red);
+    cta_reduce<1, true>(v2, red);
+    if (tid == 0) a.norm_part[g] = make_float2(v1[0], v2[0]);
+  }
 }
 
 template <int G>
@@ -537,13 +561,53 @@ bw_status check_attn_shape(int H, int Hkv, int D, int S) {
 }
 
 }  // namespace
+
+size_t attn_workspace_bytes(int H, int Hkv, int D, int S) {
+  if (check_attn_shape(H, Hkv, D, S) != BW_OK) return 0;
+  return part_bytes(H, Hkv, S) + size_t(Hkv) * sizeof(unsigned int);
+}
+
+cudaError_t launch_attn(const AttnLaunch &l, cudaStream_t stream) {
+  const int sms = device_sm_count();
+  if (sms <= 0) return cudaErrorNoDevice;
+  AttnArgs a{};
+  a.qkv = l.qkv;
+  a.pos = l.pos;
+  a.kc = l.kc;
+  a.vc = l.vc;
+  a.out = l.out;
+  a.part = static_cast<float *>(l.workspace);
+  a.count = reinterpret_cast<unsigned int *>(
+      static_cast<uint8_t *>(l.workspace) + part_bytes(l.H, l.Hkv, l.S));
+  a.H = l.H;
+  a.Hkv = l.Hkv;
+  a.S = l.S;
+  a.n_split = attn_splits(l.S, l.Hkv, sms);
+  a.inv_sqrt_d = float(1.0 / sqrt(double(kAttnD)));
+  for (int i = 0; i < kAttnPairs; ++i)
+    a.freq[i] = float(pow(double(l.theta), -2.0 * i / double(kAttnD)));
+  a.err = device_error_word();
+  if (!a.err) return cudaErrorInvalidSymbol;
+  a.norm_gamma = l.norm_gamma;
+  a.norm_part = l.norm_part;
+  switch (l.H / l.Hkv) {
+    case 1: return launch_g<1>(a, stream);
+    case 2: return launch_g<2>(a, stream);
+    case 4: return launch_g<4>(a, stream);
+    default: return launch_g<8>(a, stream);
+  }
+}
+
+bw_status check_attn(int H, int Hkv, int D, int S) {
+  return check_attn_shape(H, Hkv, D, S);
+}
+
 }  // namespace bw
 
 using namespace bw;
 
 extern "C" size_t bw_attn_workspace_bytes(int H, int Hkv, int D, int S) {
-  if (check_attn_shape(H, Hkv, D, S) != BW_OK) return 0;
-  return part_bytes(H, Hkv, S) + size_t(Hkv) * sizeof(unsigned int);
+  return attn_workspace_bytes(H, Hkv, D, S);
 }
 
 extern "C" bw_status bw_attn_decode(const bw_bf16 *qkv, const int *pos, int H,
@@ -557,46 +621,24 @@ extern "C" bw_status bw_attn_decode(const bw_bf16 *qkv, const int *pos, int H,
   bw_status st = check_attn_shape(H, Hkv, D, S);
   if (st != BW_OK) return st;
   if (!(theta > 0.0f) || !(theta < 3.0e38f)) return BW_ERR_INVALID_ARG;
-  if (workspace_bytes < bw_attn_workspace_bytes(H, Hkv, D, S))
+  if (workspace_bytes < attn_workspace_bytes(H, Hkv, D, S))
     return BW_ERR_INVALID_ARG;
   if (!aligned(qkv, 2) || !aligned(pos, 4) || !aligned(k_cache, 16) ||
       !aligned(v_cache, 16) || !aligned(out, 4) || !aligned(workspace, 16))
     return BW_ERR_MISALIGNED;
-
-  AttnArgs a{};
-  a.qkv = reinterpret_cast<const __nv_bfloat16 *>(qkv);
-  a.pos = pos;
-  a.kc = reinterpret_cast<__nv_bfloat16 *>(k_cache);
-  a.vc = reinterpret_cast<__nv_bfloat16 *>(v_cache);
-  a.out = out;
-  a.part = static_cast<float *>(workspace);
-  a.count = reinterpret_cast<unsigned int *>(
-      static_cast<uint8_t *>(workspace) + part_bytes(H, Hkv, S));
-  a.H = H;
-  a.Hkv = Hkv;
-  a.S = S;
-  const int sms = device_sm_count();
-  if (sms <= 0) {
-    record_cuda_error(int(cudaErrorNoDevice));
-    return BW_ERR_CUDA;
-  }
-  a.n_split = attn_splits(S, Hkv, sms);
-  a.inv_sqrt_d = float(1.0 / sqrt(double(D)));
-  for (int i = 0; i < kAttnPairs; ++i)
-    a.freq[i] = float(pow(double(theta), -2.0 * i / double(D)));
-  a.err = device_error_word();
-  if (!a.err) {
-    record_cuda_error(int(cudaErrorInvalidSymbol));
-    return BW_ERR_CUDA;
-  }
-  cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
-  cudaError_t e = cudaSuccess;
-  switch (H / Hkv) {
-    case 1: e = launch_g<1>(a, cs); break;
-    case 2: e = launch_g<2>(a, cs); break;
-    case 4: e = launch_g<4>(a, cs); break;
-    default: e = launch_g<8>(a, cs); break;
-  }
+  AttnLaunch l{};
+  l.qkv = reinterpret_cast<const __nv_bfloat16 *>(qkv);
+  l.pos = pos;
+  l.kc = reinterpret_cast<__nv_bfloat16 *>(k_cache);
+  l.vc = reinterpret_cast<__nv_bfloat16 *>(v_cache);
+  l.out = out;
+  l.workspace = workspace;
+  l.H = H;
+  l.Hkv = Hkv;
+  l.S = S;
+  l.theta = theta;
+  const cudaError_t e =
+      launch_attn(l, reinterpret_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) {
     record_cuda_error(int(e));
     return BW_ERR_CUDA;

@@ -101,6 +101,24 @@ cudaError_t launch_quant_weight(const float *W, int N, int K,
 
 int device_sm_count();
 
+// Decode attention (bw_attn.cu) for library-internal callers: the checks of
+// bw_attn_decode are the caller's; norm_gamma / norm_part (or null) ask for
+// the next RMSNorm's per-KV-head statistics of the output.
+struct AttnLaunch {
+  const __nv_bfloat16 *qkv;
+  const int *pos;
+  __nv_bfloat16 *kc, *vc;
+  float *out;
+  void *workspace;  // attn_workspace_bytes, zeroed before its first use
+  int H, Hkv, S;
+  float theta;
+  const float *norm_gamma;
+  float2 *norm_part;
+};
+size_t attn_workspace_bytes(int H, int Hkv, int D, int S);  // 0: unsupported
+bw_status check_attn(int H, int Hkv, int D, int S);
+cudaError_t launch_attn(const AttnLaunch &l, cudaStream_t stream);
+
 // Remembers a CUDA error for bw_last_cuda_error() (calling thread).
 void record_cuda_error(int err);
 

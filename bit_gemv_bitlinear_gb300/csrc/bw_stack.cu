@@ -18,6 +18,10 @@
 //   h <- h + down
 // attn() is attention over a one-token context: the softmax of one score is
 // 1, so query head h returns the value vector of KV head h / (heads / kv).
+// A stack made with bw_stack_create_kv attends over a KV cache instead: one
+// more launch per layer (bw_attn.cu) rotates and appends the token's key
+// and value at the current position and attends over positions 0..p; the
+// last launch of a step advances the position.
 //
 // Each GEMV is ONE launch of the pipe GEMV kernel (bw_pipe.cuh); the glue
 // is split between launches so that every value is computed once:
@@ -274,7 +278,9 @@ __device__ __forceinline__ void write_partials(float2 *out, float ss, float mx,
 // Epilogue of wqkv: qkv[n] (bf16, scales q | k | v), and for the value rows
 // the one-token attention output attn[h hd + d] = v[kv hd + d] for the
 // `group` query heads h of KV head kv (fp32), with the partial statistics
-// of attn against the attn_sub_norm gains.
+// of attn against the attn_sub_norm gains.  With attn null (a stack with a
+// KV cache) it writes qkv only: the attention launch that follows produces
+// attn and its statistics.
 struct EpiQKV {
   __nv_bfloat16 *qkv;
   float *attn;
@@ -295,7 +301,7 @@ struct EpiQKV {
     const int t = threadIdx.x;
     const int n = (g_lo + (t >> 3)) * kGroupRows + (t & 7);
     float4 p = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
-    if (t < n_g * 8 && n < a.N && n >= v_off && group <= 4) {
+    if (attn && t < n_g * 8 && n < a.N && n >= v_off && group <= 4) {
       const int j = n - v_off;
       const int kv = j / hd, d = j - kv * hd;
       const float *gp = gamma_next + kv * group * hd + d;
@@ -324,7 +330,7 @@ struct EpiQKV {
       const __nv_bfloat16 yv =
           scaled_bf16(tot[gl * 8 + rr] - sx[0], s_sm[0], ws_sm[sg]);
       qkv[n] = yv;
-      if (n >= v_off) {
+      if (attn && n >= v_off) {
         const int j = n - v_off;
         const int kv = j / hd, d = j - kv * hd;
         const float yf = __bfloat162float(yv);
@@ -369,6 +375,7 @@ struct EpiResid {
   const __nv_bfloat16 *ws;
   const float *gamma_next;  // or null
   float2 *part_out;         // or null
+  int *pos_advance;         // or null: the KV position, advanced once
 
   __device__ __forceinline__ float scale_value() const {
     return threadIdx.x == 0 ? __bfloat162float(ws[0]) : 0.0f;
@@ -404,6 +411,10 @@ struct EpiResid {
       }
     }
     write_partials(part_out, ss, mx, red);
+    // The last launch of a step: every attention launch of the step has
+    // completed (each launch waits for the one before it), so the next
+    // token's position can be published.
+    if (pos_advance && blockIdx.x == 0 && threadIdx.x == 0) *pos_advance += 1;
   }
 };
 
@@ -536,6 +547,14 @@ struct bw_stack {
   __nv_bfloat16 *qkv, *o, *gu, *dn;   // GEMV outputs
   float *attn, *gated;                // inputs of attn_sub_norm, ffn_sub_norm
   float2 *part;                       // [2][kMaxPartials] partial statistics
+  // KV cache (kv_S > 0): [n_layers][Hkv][kv_S][hd] bf16 keys and values,
+  // the position of the next token, the attention workspace.
+  int kv_S;
+  float theta;
+  __nv_bfloat16 *kc, *vc;
+  int *pos;
+  void *attn_ws;
+  size_t kv_layer_elems;
   cudaGraphExec_t exec;
   bool have_graph;
 };
@@ -590,9 +609,12 @@ bw_status run_step(bw_stack *st, cudaStream_t cs, const bw_stack_trace *tr) {
     const bool last = l == d.n_layers - 1;
     const bool rec = tr && tr->layer == l;
     if (rec) BW_TRY_CUDA(trace_copy(tr->h_in, st->h, dim * 4, cs));
-    // qkv = W2A8(wqkv, quant(attention_norm(h))); attn = value heads
-    const EpiQKV e_qkv{st->qkv, st->attn,    ws,     seg_qkv, st->v_off,
-                       st->hd,  st->group,   g + dim, pout};
+    // qkv = W2A8(wqkv, quant(attention_norm(h))); attn = value heads (one
+    // token) or the attention over the cache (next launch)
+    const bool kv = st->kv_S > 0;
+    const EpiQKV e_qkv{st->qkv,    kv ? nullptr : st->attn, ws,
+                       seg_qkv,    st->v_off,               st->hd,
+                       st->group,  kv ? nullptr : g + dim,  kv ? nullptr : pout};
     if (l == 0)
       BW_TRY_CUDA(launch_first(st->wqkv[l], st->qkv_n, dim, st->h, g, d.eps,
                                rec ? tr->q_attn : nullptr,
@@ -603,6 +625,27 @@ bw_status run_step(bw_stack *st, cudaStream_t cs, const bw_stack_trace *tr) {
                               rec ? tr->s_attn : nullptr, e_qkv, cs, &grid));
     flip();
     if (rec) BW_TRY_CUDA(trace_copy(tr->qkv, st->qkv, st->qkv_n * 2, cs));
+    if (kv) {
+      // attn = attention of the step's token over layer l's cache (the key
+      // and value appended at the current position), with the statistics
+      // of attn_sub_norm per KV head
+      AttnLaunch al{};
+      al.qkv = st->qkv;
+      al.pos = st->pos;
+      al.kc = st->kc + size_t(l) * st->kv_layer_elems;
+      al.vc = st->vc + size_t(l) * st->kv_layer_elems;
+      al.out = st->attn;
+      al.workspace = st->attn_ws;
+      al.H = d.n_heads;
+      al.Hkv = d.n_kv_heads;
+      al.S = st->kv_S;
+      al.theta = st->theta;
+      al.norm_gamma = g + dim;
+      al.norm_part = pout;
+      BW_TRY_CUDA(launch_attn(al, cs));
+      grid = d.n_kv_heads;
+      flip();
+    }
     // o = W2A8(wo, quant(attn_sub_norm(attn))); h += o
     BW_TRY_CUDA(launch_next(
         st->wo[l], dim, dim, 0, st->attn, g + dim, pin, P, d.eps,
@@ -626,8 +669,9 @@ bw_status run_step(bw_stack *st, cudaStream_t cs, const bw_stack_trace *tr) {
     BW_TRY_CUDA(launch_next(
         st->w2[l], dim, ffn, 0, st->gated, g + 3 * dim, pin, P, d.eps,
         rec ? tr->q_down : nullptr, rec ? tr->s_down : nullptr,
-        EpiResid{st->dn, st->h, ws + 6, g_next, last ? nullptr : pout}, cs,
-        &grid));
+        EpiResid{st->dn, st->h, ws + 6, g_next, last ? nullptr : pout,
+                 last && st->kv_S > 0 ? st->pos : nullptr},
+        cs, &grid));
     flip();
     if (rec) BW_TRY_CUDA(trace_copy(tr->down, st->dn, dim * 2, cs));
   }
@@ -645,14 +689,15 @@ void free_stack(bw_stack *st) {
   cudaFree(st->o);
   cudaFree(st->gu);
   cudaFree(st->dn);
+  cudaFree(st->kc);
+  cudaFree(st->vc);
+  cudaFree(st->pos);
+  cudaFree(st->attn_ws);
   delete st;
 }
 
-}  // namespace
-
-extern "C" {
-
-bw_status bw_stack_create(const bw_stack_desc *desc, bw_stack **out) {
+bw_status stack_create(const bw_stack_desc *desc, int kv_S, float theta,
+                       bw_stack **out) {
   if (!desc || !out) return BW_ERR_INVALID_ARG;
   *out = nullptr;
   const bw_stack_desc &d = *desc;
@@ -677,6 +722,13 @@ bw_status bw_stack_create(const bw_stack_desc *desc, bw_stack **out) {
         reinterpret_cast<uintptr_t>(d.ws[l]) % 2 != 0 ||
         !a16(d.gammas[l]))
       return BW_ERR_MISALIGNED;
+  }
+  if (kv_S > 0) {
+    bw_status ks = check_attn(d.n_heads, d.n_kv_heads, d.dim / d.n_heads, kv_S);
+    if (ks != BW_OK) return ks;
+    if (!(theta > 0.0f) || !(theta < 3.0e38f)) return BW_ERR_INVALID_ARG;
+  } else if (kv_S < 0) {
+    return BW_ERR_INVALID_ARG;
   }
   bw_stack *st = new (std::nothrow) bw_stack();
   if (!st) return BW_ERR_INVALID_ARG;
@@ -708,6 +760,22 @@ bw_status bw_stack_create(const bw_stack_desc *desc, bw_stack **out) {
   alloc(reinterpret_cast<void **>(&st->part),
         size_t(2) * kMaxPartials * sizeof(float2));
   if (e == cudaSuccess) e = cudaMemset(st->h, 0, size_t(d.dim) * 4);
+  size_t ws_bytes = 0;
+  if (kv_S > 0) {
+    st->kv_S = kv_S;
+    st->theta = theta;
+    st->kv_layer_elems = size_t(d.n_kv_heads) * kv_S * st->hd;
+    const size_t cache = size_t(d.n_layers) * st->kv_layer_elems * 2;
+    ws_bytes = attn_workspace_bytes(d.n_heads, d.n_kv_heads, st->hd, kv_S);
+    alloc(reinterpret_cast<void **>(&st->kc), cache);
+    alloc(reinterpret_cast<void **>(&st->vc), cache);
+    alloc(reinterpret_cast<void **>(&st->pos), sizeof(int));
+    alloc(&st->attn_ws, ws_bytes);
+    if (e == cudaSuccess) e = cudaMemset(st->kc, 0, cache);
+    if (e == cudaSuccess) e = cudaMemset(st->vc, 0, cache);
+    if (e == cudaSuccess) e = cudaMemset(st->pos, 0, sizeof(int));
+    if (e == cudaSuccess) e = cudaMemset(st->attn_ws, 0, ws_bytes);
+  }
   if (e != cudaSuccess) {
     free_stack(st);
     return cuda_err(e);
@@ -736,8 +804,56 @@ bw_status bw_stack_create(const bw_stack_desc *desc, bw_stack **out) {
     free_stack(st);
     return bs;
   }
+  if (kv_S > 0) {
+    // The set-up step advanced the position and wrote row 0: start the
+    // sequence at position 0 (rows at and past the position are never read).
+    e = cudaMemset(st->pos, 0, sizeof(int));
+    if (e == cudaSuccess) e = cudaDeviceSynchronize();
+    if (e != cudaSuccess) {
+      free_stack(st);
+      return cuda_err(e);
+    }
+  }
   *out = st;
   return BW_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+bw_status bw_stack_create(const bw_stack_desc *desc, bw_stack **out) {
+  return stack_create(desc, 0, 0.0f, out);
+}
+
+bw_status bw_stack_create_kv(const bw_stack_desc *desc, int max_positions,
+                             float theta, bw_stack **out) {
+  if (max_positions < 1) return BW_ERR_INVALID_ARG;
+  return stack_create(desc, max_positions, theta, out);
+}
+
+bw_status bw_stack_read_kv(const bw_stack *st, int layer, bw_bf16 *k_out,
+                           bw_bf16 *v_out, bw_stream_t stream) {
+  if (!st || st->kv_S < 1 || layer < 0 || layer >= st->d.n_layers ||
+      !k_out || !v_out)
+    return BW_ERR_INVALID_ARG;
+  if (reinterpret_cast<uintptr_t>(k_out) % 2 != 0 ||
+      reinterpret_cast<uintptr_t>(v_out) % 2 != 0)
+    return BW_ERR_MISALIGNED;
+  cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+  const size_t bytes = st->kv_layer_elems * 2;
+  const size_t off = size_t(layer) * st->kv_layer_elems;
+  BW_TRY_CUDA(cudaMemcpyAsync(k_out, st->kc + off, bytes,
+                              cudaMemcpyDeviceToDevice, cs));
+  BW_TRY_CUDA(cudaMemcpyAsync(v_out, st->vc + off, bytes,
+                              cudaMemcpyDeviceToDevice, cs));
+  return BW_OK;
+}
+
+bw_status bw_stack_reset_kv(bw_stack *st, bw_stream_t stream) {
+  if (!st || st->kv_S < 1) return BW_ERR_INVALID_ARG;
+  return cuda_err(cudaMemsetAsync(st->pos, 0, sizeof(int),
+                                  reinterpret_cast<cudaStream_t>(stream)));
 }
 
 bw_status bw_layer_stack(bw_stack *st, const float *h_in, int steps,

@@ -281,8 +281,39 @@ typedef struct {
  * private stream.  Synchronising; call it before any stream capture. */
 bw_status bw_stack_create(const bw_stack_desc *desc, bw_stack **stack);
 
+/* bw_stack_create_kv -- the same stack with grouped-query attention over a
+ * KV cache in place of the one-token attention: per layer, after the wqkv
+ * launch, one bw_attn_decode-style launch rotates the token's new key and
+ * query heads (RoPE base theta), appends key and value at the current
+ * position p of the layer's bf16 cache and attends over positions 0..p
+ * ([W2A8] §一 head counts, §4.1 RoPE on adjacent pairs, §六 item 2 the
+ * preallocated cache).  Five launches per layer.  The position starts at 0
+ * and advances by one per decode step, so consecutive bw_layer_stack steps
+ * (and calls) are consecutive tokens of one sequence; a step at position
+ * max_positions or beyond sets bit 16 of the device error word and gives
+ * zero attention.  Needs dim / n_heads == 128, n_heads / n_kv_heads in {1,
+ * 2, 4, 8}, 1 <= max_positions <= BW_ATTN_MAX_S, theta > 0.  Allocates
+ * 2 n_layers n_kv_heads max_positions 128 bf16 of cache with cudaMalloc
+ * (zeroed) besides the scratch of bw_stack_create.  Synchronising; call it
+ * before any stream capture. */
+bw_status bw_stack_create_kv(const bw_stack_desc *desc, int max_positions,
+                             float theta, bw_stack **stack);
+
+/* Copies layer `layer`'s key and value caches (bf16 [n_kv_heads]
+ * [max_positions][128] each) into k_out and v_out (device, 2-byte aligned),
+ * asynchronously on `stream`.  Only for stacks made by bw_stack_create_kv. */
+bw_status bw_stack_read_kv(const bw_stack *stack, int layer, bw_bf16 *k_out,
+                           bw_bf16 *v_out, bw_stream_t stream);
+
+/* Sets the position of a KV stack back to 0 (a new sequence), on `stream`.
+ * The cache rows are not cleared: rows at and past the position are never
+ * read. */
+bw_status bw_stack_reset_kv(bw_stack *stack, bw_stream_t stream);
+
 /* Runs `steps` decode steps: h_out[t] = stack(h_in[t]) (fp32 [steps][dim],
- * device).  Steps are independent (no KV cache).  Asynchronous on `stream`.
+ * device).  Steps are independent (no KV cache) for a stack made by
+ * bw_stack_create; for one made by bw_stack_create_kv they are consecutive
+ * tokens of one sequence.  Asynchronous on `stream`.
  * `trace` (may be NULL) records the stages of trace->layer in the last
  * step.  Calls on the same stack must not overlap (they share its scratch);
  * use one stack per concurrent stream. */
