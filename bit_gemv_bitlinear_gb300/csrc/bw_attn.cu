@@ -18,7 +18,9 @@
 //    heads on 152 SMs), never more than 160 positions per split.  The
 //    position p is read on the device, so one launch serves every step of
 //    a graph-replayed decode loop: a context of L tokens uses min(splits,
-//    ceil(L / 64)) of them, the others are empty.
+//    ceil(L / 64)) of them, the others are empty.  A context of at most 128
+//    tokens takes one split, finished by that CTA alone straight from its
+//    shared memory: no partial, fence, counter or merge.
 //  * The rows of a split are contiguous in the cache, so two bulk copies
 //    (cp.async.bulk) bring its keys and its values into shared memory, up
 //    to 80 KB in flight per CTA, while the CTA rotates its queries; the
@@ -54,6 +56,7 @@ constexpr int kAttnThreads = 256;
 constexpr int kAttnWarps = kAttnThreads / 32;
 constexpr int kAttnChunk = 160;         // positions per split, at most
 constexpr int kAttnMinChunk = 64;       // positions per used split, at least
+constexpr int kAttnSoloMax = 128;       // contexts one CTA per head finishes
 // Splits of a cache of S positions: at most ceil(S / 64) (the workspace is
 // sized for that), at least ceil(S / kAttnChunk).
 constexpr int kAttnMaxSplits = (BW_ATTN_MAX_S + kAttnMinChunk - 1) / kAttnMinChunk;
@@ -188,7 +191,9 @@ attn_decode_kernel(const AttnArgs a) {
   int n_eff = 0, j0 = 0, j1 = 0;
   if (valid) {
     const int len = p + 1;
-    n_eff = min(a.n_split, (len + kAttnMinChunk - 1) / kAttnMinChunk);
+    n_eff = len <= kAttnSoloMax
+                ? 1
+                : min(a.n_split, (len + kAttnMinChunk - 1) / kAttnMinChunk);
     if (c < n_eff) {
       j0 = int(int64_t(c) * len / n_eff);
       j1 = int(int64_t(c + 1) * len / n_eff);
@@ -363,6 +368,37 @@ attn_decode_kernel(const AttnArgs a) {
           for (int e = 0; e < 8; ++e)
             wacc[(warp * G + h) * D + 8 * hl + e] = acc[h][e];
       __syncthreads();
+      if (n_eff == 1) {
+        // One split holds the whole context: its sums are final.  Write
+        // the outputs (and the next RMSNorm's statistics) directly; no
+        // partial, fence, counter or merge.
+        float *o = a.out + size_t(g) * G * D;
+        float ss = 0.0f, amx = 0.0f;
+        for (int e = tid; e < G * D; e += kAttnThreads) {
+          float t = wacc[e];
+#pragma unroll
+          for (int w = 1; w < kAttnWarps; ++w) t += wacc[w * G * D + e];
+          const int h = e / D;
+          float lh = l[0];
+#pragma unroll
+          for (int hh = 1; hh < G; ++hh)
+            if (hh == h) lh = l[hh];
+          const float y = t / lh;
+          o[e] = y;
+          if (a.norm_part) {
+            ss += y * y;
+            amx = fmaxf(amx, fabsf(__fmul_rn(
+                                 y, a.norm_gamma[size_t(g) * G * D + e])));
+          }
+        }
+        if (a.norm_part) {
+          float v1[1] = {ss}, v2[1] = {amx};
+          cta_reduce<1, false>(v1, red);
+          cta_reduce<1, true>(v2, red);
+          if (tid == 0) a.norm_part[g] = make_float2(v1[0], v2[0]);
+        }
+        return;
+      }
       for (int e = tid; e < G * D; e += kAttnThreads) {
         float t = wacc[e];
 #pragma unroll
@@ -379,6 +415,8 @@ attn_decode_kernel(const AttnArgs a) {
       }
     }
   }
+  // A single split finished the head above; the other CTAs have no work.
+  if (valid && n_eff == 1) return;
 
   // ---- the last CTA of KV head g merges the splits ----
   __threadfence();
