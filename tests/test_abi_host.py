@@ -237,3 +237,37 @@ def test_attn_workspace_and_host_validation(lib):
     assert call(pos=A4 + 2) == MISALIGNED
     assert call(out=A4 + 1) == MISALIGNED
     assert call(ws=A16 + 4) == MISALIGNED
+
+
+def test_stack_create_kv_host_validation(lib):
+    create = lib.bw_stack_create_kv
+    create.argtypes = [P, ctypes.c_int, ctypes.c_float, P]
+    handle = P()
+    L = 1
+    w16 = (P * L)(A16)
+    ws = (P * L)(A2)
+    gam = (P * L)(A4)
+
+    def make(S=64, theta=5e5, **kw):
+        base = dict(n_layers=L, dim=512, ffn=1024, n_heads=4, n_kv_heads=2,
+                    eps=1e-5, wqkv=ctypes.cast(w16, P), wo=ctypes.cast(w16, P),
+                    w13=ctypes.cast(w16, P), w2=ctypes.cast(w16, P),
+                    ws=ctypes.cast(ws, P), gammas=ctypes.cast(gam, P))
+        base.update(kw)
+        return create(ctypes.byref(_Desc(**base)), S, theta,
+                      ctypes.byref(handle))
+
+    assert make(S=0) == INVALID
+    assert make(S=-3) == INVALID
+    assert make(S=65537) == SHAPE           # beyond BW_ATTN_MAX_S
+    assert make(dim=256) == SHAPE           # head dim 64, attention needs 128
+    assert make(n_heads=3, dim=384, n_kv_heads=1) == SHAPE   # 3 heads per KV
+    assert make(theta=0.0) == INVALID
+    assert make(theta=float("inf")) == INVALID
+    assert make(wo=None) == INVALID
+    reset = lib.bw_stack_reset_kv
+    reset.argtypes = [P, P]
+    assert reset(None, None) == INVALID
+    read = lib.bw_stack_read_kv
+    read.argtypes = [P, ctypes.c_int, P, P, P]
+    assert read(None, 0, A2, A2, None) == INVALID
