@@ -102,17 +102,24 @@ def check_step(case, qkv, p, kc_before, vc_before, out, kc_gpu, vc_gpu):
 
 
 CASES = [
-    # H, Hkv, S, p: BitNet-2B heads (G = 4) over contexts that leave one
-    # split, several, a ragged last split and a full cache; G = 1, 2, 8.
+    # H, Hkv, S, p: BitNet-2B heads (G = 4) over contexts finished by one
+    # CTA per head (up to 128 positions), the first split context (129),
+    # several splits, a ragged last split and a full cache; G = 1, 2, 8,
+    # each on both paths.
     (20, 5, 4096, 0),
     (20, 5, 4096, 1),
     (20, 5, 4096, 63),
     (20, 5, 4096, 64),
+    (20, 5, 4096, 127),
+    (20, 5, 4096, 128),
     (20, 5, 4096, 1000),
     (20, 5, 4096, 4095),
     (8, 8, 300, 299),
+    (8, 8, 300, 50),
     (16, 8, 1000, 517),
+    (16, 8, 1000, 128),
     (16, 2, 777, 400),
+    (16, 2, 777, 100),
     (4, 1, 65536, 65535),
 ]
 
