@@ -31,6 +31,7 @@ import os
 import statistics
 import subprocess
 import sys
+import tempfile
 import time
 
 import numpy as np
@@ -155,8 +156,8 @@ class ClockSampler:
     def __init__(self, index: int):
         self.index = index
         self.proc = None
-        self.path = os.path.join(ROOT, "gpurun_out",
-                                 f"clocks_rank{index}.csv")
+        self.path = os.path.join(tempfile.gettempdir(),
+                                 f"bw_bench_clocks_rank{index}.csv")
 
     def start(self):
         try:
