@@ -117,7 +117,7 @@ struct AttnSmem {
   static constexpr uint32_t kSc = kQ + G * kAttnD * 4;          // [chunk][G]
   static constexpr uint32_t kWacc = kSc + kAttnChunk * G * 4;   // [warps][G][D]
   static constexpr uint32_t kRed = kWacc + kAttnWarps * G * kAttnD * 4;
-  static constexpr size_t kBytes = kRed + kAttnWarps * G * 4 + 16;
+  static constexpr size_t kBytes = kRed + kAttnWarps * (G < 2 ? 2 : G) * 4 + 16;
 };
 // The merge keeps [splits][G] weights, [splits][G] exp sums and G totals
 // in the staging rows.
@@ -134,7 +134,8 @@ __device__ __forceinline__ void bf16x8_to_f32(uint4 raw, float (&v)[8]) {
 }
 
 // Max (kMax) or sum over the CTA of G values per thread, in a fixed order;
-// every thread receives the results.  `red` holds kAttnWarps * G floats.
+// every thread receives the results.  `red` holds kAttnWarps * max(G, 2)
+// floats.
 template <int G, bool kMax>
 __device__ __forceinline__ void cta_reduce(float (&v)[G], float *red) {
 #pragma unroll
@@ -157,7 +158,31 @@ __device__ __forceinline__ void cta_reduce(float (&v)[G], float *red) {
       t = kMax ? fmaxf(t, red[w * G + h]) : t + red[w * G + h];
     v[h] = t;
   }
-  __syncthreads();  // red may be reused at once
+  // No trailing barrier: the next writer of `red` is the next reduction,
+  // whose first barrier comes after every thread has read these values.
+}
+
+// Sum and max of one value per thread over the CTA in one exchange (the
+// next RMSNorm's statistics); `red` holds 2 kAttnWarps floats.
+__device__ __forceinline__ void cta_sum_max(float &ss, float &mx, float *red) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    ss += __shfl_xor_sync(0xffffffffu, ss, o);
+    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+  }
+  __syncthreads();
+  if ((threadIdx.x & 31) == 0) {
+    red[threadIdx.x >> 5] = ss;
+    red[kAttnWarps + (threadIdx.x >> 5)] = mx;
+  }
+  __syncthreads();
+  ss = red[0];
+  mx = red[kAttnWarps];
+#pragma unroll
+  for (int w = 1; w < kAttnWarps; ++w) {
+    ss += red[w];
+    mx = fmaxf(mx, red[kAttnWarps + w]);
+  }
 }
 
 template <int G>
@@ -232,9 +257,7 @@ attn_decode_kernel(const AttnArgs a) {
       q_sm[h * D + 2 * i + 1] = x0 * r.y + x1 * r.x;
     }
     const bool has_p = j0 <= p && p < j1;
-    const bool k_in = pipe::mbar_wait(&bar[0], 0u);
-    const bool v_in = k_in && (!has_p || pipe::mbar_wait(&bar[1], 0u));
-    if (!__syncthreads_and(v_in)) {
+    if (!__syncthreads_and(pipe::mbar_wait(&bar[0], 0u))) {
       // Never expected: report, let the copies land (bounded) before the
       // CTA may leave, and contribute no partial.
       if (tid == 0) {
@@ -244,24 +267,19 @@ attn_decode_kernel(const AttnArgs a) {
       }
       __syncthreads();
     } else {
-      // ---- the new token: rotated key and value, staged and appended
-      // (the CTA holding p has waited for both of its copies) ----
+      // ---- the new token's rotated key: staged and appended (the key
+      // copy has landed, so neither write can be overwritten or read by it)
       if (has_p && tid < kAttnPairs) {
         const int i = tid;
         const __nv_bfloat16 *kh = a.qkv + size_t(a.H + g) * D;
-        const __nv_bfloat16 *vh = a.qkv + size_t(a.H + a.Hkv + g) * D;
         const float x0 = __bfloat162float(kh[2 * i]);
         const float x1 = __bfloat162float(kh[2 * i + 1]);
         const float2 r = cs[i];
         const __nv_bfloat162 k2 = __halves2bfloat162(
             __float2bfloat16_rn(x0 * r.x - x1 * r.y),
             __float2bfloat16_rn(x0 * r.y + x1 * r.x));
-        const __nv_bfloat162 v2 = __halves2bfloat162(vh[2 * i], vh[2 * i + 1]);
-        const size_t row = size_t(p - j0) * D;
-        reinterpret_cast<__nv_bfloat162 *>(kst + row)[i] = k2;
-        reinterpret_cast<__nv_bfloat162 *>(vst + row)[i] = v2;
+        reinterpret_cast<__nv_bfloat162 *>(kst + size_t(p - j0) * D)[i] = k2;
         reinterpret_cast<__nv_bfloat162 *>(a.kc + (head_row + p) * D)[i] = k2;
-        reinterpret_cast<__nv_bfloat162 *>(a.vc + (head_row + p) * D)[i] = v2;
       }
       __syncthreads();
 
@@ -328,14 +346,22 @@ attn_decode_kernel(const AttnArgs a) {
         }
       cta_reduce<G, false>(l, red);  // its barriers also publish sc
 
-      // ---- weighted values ----
-      if (!has_p && !__syncthreads_and(pipe::mbar_wait(&bar[1], 0u))) {
+      // ---- weighted values (the value copy landed during the scores) ----
+      if (!__syncthreads_and(pipe::mbar_wait(&bar[1], 0u))) {
         if (tid == 0) {
           atomicOr(a.err, 4u);
           if (!pipe::mbar_wait(&bar[1], 0u)) atomicOr(a.err, 2u);
         }
         __syncthreads();
       }
+      if (has_p && tid < kAttnPairs) {  // the new token's value
+        const int i = tid;
+        const __nv_bfloat16 *vh = a.qkv + size_t(a.H + a.Hkv + g) * D;
+        const __nv_bfloat162 v2 = __halves2bfloat162(vh[2 * i], vh[2 * i + 1]);
+        reinterpret_cast<__nv_bfloat162 *>(vst + size_t(p - j0) * D)[i] = v2;
+        reinterpret_cast<__nv_bfloat162 *>(a.vc + (head_row + p) * D)[i] = v2;
+      }
+      __syncthreads();
       float acc[G][8];
 #pragma unroll
       for (int h = 0; h < G; ++h)
@@ -392,10 +418,8 @@ attn_decode_kernel(const AttnArgs a) {
           }
         }
         if (a.norm_part) {
-          float v1[1] = {ss}, v2[1] = {amx};
-          cta_reduce<1, false>(v1, red);
-          cta_reduce<1, true>(v2, red);
-          if (tid == 0) a.norm_part[g] = make_float2(v1[0], v2[0]);
+          cta_sum_max(ss, amx, red);
+          if (tid == 0) a.norm_part[g] = make_float2(ss, amx);
         }
         return;
       }
@@ -542,10 +566,8 @@ attn_decode_kernel(const AttnArgs a) {
       amx = fmaxf(fmaxf(fabsf(__fmul_rn(y.x, gm.x)), fabsf(__fmul_rn(y.y, gm.y))),
                   fmaxf(fabsf(__fmul_rn(y.z, gm.z)), fabsf(__fmul_rn(y.w, gm.w))));
     }
-    float v1[1] = {ss}, v2[1] = {amx};
-    cta_reduce<1, false>(v1, red);
-    cta_reduce<1, true>(v2, red);
-    if (tid == 0) a.norm_part[g] = make_float2(v1[0], v2[0]);
+    cta_sum_max(ss, amx, red);
+    if (tid == 0) a.norm_part[g] = make_float2(ss, amx);
   }
 }
 
