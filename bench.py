@@ -98,6 +98,9 @@ def parse_args():
                    help="--single: weight buffers (0: enough for 4x L2)")
     p.add_argument("--eager", action="store_true",
                    help="--single: launch eagerly instead of a CUDA graph")
+    p.add_argument("--cold", action="store_true",
+                   help="--single: isolated calls, L2 flushed before each "
+                        "(median of --iters, at most 200), launch included")
     return p.parse_args()
 
 
@@ -849,6 +852,38 @@ def run_attn_timing(torch, bw, dev, peak_gbs, contexts=ATTN_CONTEXTS,
     return res
 
 
+def time_cold(torch, bw, dev, N, K, M, reps=50):
+    """Microseconds of one isolated bw_gemv_w2a8 call: a 512 MB buffer is
+    written first (L2 holds no weights), then events bracket the call alone
+    on an otherwise idle stream, so the launch latency is included (the
+    way the pages time their kernel).  Median of `reps`."""
+    seed = synth.base_seed(2, 2)
+    canon = synth.canonical_weights(seed, N, K)
+    packed = bw.bw_repack(torch.from_numpy(canon).to(dev), N, K)
+    xf = torch.from_numpy(synth.normal_f32(seed, M * K).reshape(M, K)).to(dev)
+    q, s_ = bw.bw_quant_act(xf)
+    ws = torch.ones(1, device=dev).to(torch.bfloat16)
+    y = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+    flush = torch.empty((512 << 20,), dtype=torch.uint8, device=dev)
+    stream = torch.cuda.Stream(device=dev)
+    times = []
+    with torch.cuda.stream(stream):
+        for i in range(reps + 3):
+            flush.fill_(i & 0xFF)
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            stream.synchronize()
+            e0.record(stream)
+            bw.bw_gemv_w2a8(q, packed, s_, ws, [0, N], N, K, y=y,
+                            stream=stream)
+            e1.record(stream)
+            stream.synchronize()
+            if i >= 3:
+                times.append(e0.elapsed_time(e1) * 1e3)
+    bw.bw_device_error(stream)
+    return statistics.median(times)
+
+
 def run_single(args):
     """One shape over rotating weight buffers; also the command the kernel
     profiles are taken with."""
@@ -860,6 +895,17 @@ def run_single(args):
     M = dims[2] if len(dims) > 2 else 1
     dev = torch.device("cuda", 0)
     torch.cuda.set_device(dev)
+    if args.cold:
+        reps = max(1, min(args.iters, 200))
+        us = time_cold(torch, bw, dev, N, K, M, reps=reps)
+        print(json.dumps({"single": [N, K, M], "cold": True, "calls": reps,
+                          "us_per_call": round(us, 3),
+                          "weight_GBps": round(weight_bytes(N, K)
+                                               / (us * 1e3), 1),
+                          "timing": "median of isolated calls after a "
+                                    "512 MB write, launch included"}),
+              flush=True)
+        return
     t = time_shape(torch, bw, dev, N, K, M, iters=args.iters,
                    rotate=args.rotate, eager=args.eager)
     us = t["us"]
