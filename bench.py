@@ -52,8 +52,8 @@ FALLBACK_HBM_GBS = 6800.0
 
 # DRAM bytes (read + write) per launch of the current TMA GEMV kernel,
 # measured with ncu (dram__bytes_read.sum + dram__bytes_write.sum, median of
-# 4 launches; profiles/bench_m1_sweep_launches.md).  Must be re-measured --
-# or set to None -- whenever the GEMV kernel changes.
+# 4 launches of the bench's own sweep).  Must be re-measured -- or set to
+# None -- whenever the GEMV kernel changes.
 MEASURED_DRAM_BYTES = {"wqkv": 2487936, "wo": 1668736, "w13": 8877824,
                        "w2": 4458880}
 

@@ -108,6 +108,13 @@ def _dev(t: torch.Tensor, dtype, name: str) -> int:
     return t.data_ptr()
 
 
+def _need(t: torch.Tensor, count: int, name: str):
+    """Rejects a buffer with fewer than `count` elements before any kernel
+    can read or write past its end."""
+    if t.numel() < count:
+        raise ValueError(f"{name} holds {t.numel()} elements, needs {count}")
+
+
 def version() -> int:
     return _lib.bw_version()
 
@@ -134,6 +141,8 @@ def bw_quant_act(x: torch.Tensor, q: torch.Tensor | None = None,
         q = torch.empty((M, K), dtype=torch.int8, device=x.device)
     if s is None:
         s = torch.empty((M,), dtype=torch.float32, device=x.device)
+    _need(q, M * K, "q")
+    _need(s, M, "s")
     _check(_lib.bw_quant_act(_dev(x2, torch.float32, "x"), M, K,
                              _dev(q, torch.int8, "q"),
                              _dev(s, torch.float32, "s"), _stream(stream)),
@@ -141,14 +150,23 @@ def bw_quant_act(x: torch.Tensor, q: torch.Tensor | None = None,
     return q, s
 
 
+def _repack_sizes(canon: torch.Tensor, N: int, K: int) -> int:
+    """Checks that `canon` holds N * K / 4 bytes; returns the size of the
+    device layout."""
+    size = bw_repack_bytes(N, K)
+    if size == 0 or K % 4:
+        raise BwError(2, "bw_repack_bytes")
+    _need(canon, N * (K // 4), "canon")
+    return size
+
+
 def bw_repack(canon: torch.Tensor, N: int, K: int,
               packed: torch.Tensor | None = None, stream=None) -> torch.Tensor:
     """Canonical bytes uint8 [N][K/4] -> device layout (synchronising)."""
+    size = _repack_sizes(canon, N, K)
     if packed is None:
-        size = bw_repack_bytes(N, K)
-        if size == 0:
-            raise BwError(2, "bw_repack_bytes")
         packed = torch.empty((size,), dtype=torch.uint8, device=canon.device)
+    _need(packed, size, "packed")
     _check(_lib.bw_repack(_dev(canon, torch.uint8, "canon"), N, K,
                           _dev(packed, torch.uint8, "packed"),
                           _stream(stream)), "bw_repack")
@@ -161,6 +179,7 @@ def bw_repack_noalloc(canon: torch.Tensor, N: int, K: int,
     supplies `packed` (bw_repack_bytes(N, K) bytes) and the library uses a
     fixed internal scratch word instead of allocating one (synchronising;
     overlapping calls race on that word)."""
+    _need(packed, _repack_sizes(canon, N, K), "packed")
     _check(_lib.bw_repack_noalloc(_dev(canon, torch.uint8, "canon"), N, K,
                                   _dev(packed, torch.uint8, "packed"),
                                   _stream(stream)), "bw_repack_noalloc")
@@ -172,6 +191,7 @@ def bw_unrepack(packed: torch.Tensor, N: int, K: int,
     if canon is None:
         canon = torch.empty((N, K // 4), dtype=torch.uint8,
                             device=packed.device)
+    _need(packed, _repack_sizes(canon, N, K), "packed")
     _check(_lib.bw_unrepack(_dev(packed, torch.uint8, "packed"), N, K,
                             _dev(canon, torch.uint8, "canon"),
                             _stream(stream)), "bw_unrepack")
@@ -189,6 +209,8 @@ def bw_quant_weight(W: torch.Tensor, ws_bounds, canon: torch.Tensor | None = Non
         canon = torch.empty((N, K // 4), dtype=torch.uint8, device=W.device)
     if ws is None:
         ws = torch.empty((n_ws,), dtype=torch.bfloat16, device=W.device)
+    _need(canon, N * (K // 4), "canon")
+    _need(ws, n_ws, "ws")
     _check(_lib.bw_quant_weight(_dev(W, torch.float32, "W"), N, K,
                                 _bounds_array(ws_bounds), n_ws,
                                 _dev(canon, torch.uint8, "canon"),
@@ -213,6 +235,10 @@ def bw_gemv_w2a8(x: torch.Tensor, packed: torch.Tensor, s: torch.Tensor,
         raise ValueError("x has the wrong K")
     if y is None:
         y = torch.empty((M, N), dtype=torch.bfloat16, device=x.device)
+    _need(packed, bw_repack_bytes(N, K), "packed")
+    _need(s, M, "s")
+    _need(ws, len(ws_bounds) - 1, "ws")
+    _need(y, M * N, "y")
     b = _bounds_array(ws_bounds)
     _check(_lib.bw_gemv_w2a8(
         _dev(x2, torch.int8, "x"), _dev(packed, torch.uint8, "packed"),
@@ -232,6 +258,8 @@ def bw_gemv_w2a8_acc(x: torch.Tensor, packed: torch.Tensor, N: int, K: int,
         raise ValueError("x has the wrong K")
     if acc is None:
         acc = torch.empty((M, N), dtype=torch.int32, device=x.device)
+    _need(packed, bw_repack_bytes(N, K), "packed")
+    _need(acc, M * N, "acc")
     _check(_lib.bw_gemv_w2a8_acc(
         _dev(x2, torch.int8, "x"), _dev(packed, torch.uint8, "packed"), M, N,
         K, _dev(acc, torch.int32, "acc"), _stream(stream)),
@@ -263,6 +291,9 @@ def bw_attn_decode(qkv: torch.Tensor, pos: torch.Tensor, H: int, Hkv: int,
     if workspace is None:
         workspace = torch.zeros((bw_attn_workspace_bytes(H, Hkv, D, S),),
                                 dtype=torch.uint8, device=qkv.device)
+    _need(qkv, (H + 2 * Hkv) * D, "qkv")
+    _need(pos, 1, "pos")
+    _need(out, H * D, "out")
     _check(_lib.bw_attn_decode(
         _dev(qkv, torch.bfloat16, "qkv"), _dev(pos, torch.int32, "pos"),
         H, Hkv, D, S, float(theta), _dev(k_cache, torch.bfloat16, "k_cache"),
@@ -294,7 +325,7 @@ class _StackDesc(ctypes.Structure):
 class _StackTrace(ctypes.Structure):
     _fields_ = [("layer", _I)] + [(n, _P) for n in (
         "h_in", "q_attn", "s_attn", "qkv", "q_o", "s_o", "o", "h_mid",
-        "q_ffn", "s_ffn", "gu", "q_down", "s_down", "down")]
+        "q_ffn", "s_ffn", "gu", "q_down", "s_down", "down", "attn")]
 
 
 class Stack:
@@ -314,6 +345,21 @@ class Stack:
         self.max_positions = max_positions
         self._keep = layers
         L = len(layers)
+        self.head_dim = dim // n_heads
+        qkv_n = (n_heads + 2 * n_kv_heads) * self.head_dim
+        need = {"wqkv": bw_repack_bytes(qkv_n, dim),
+                "wo": bw_repack_bytes(dim, dim),
+                "w13": bw_repack_bytes(2 * ffn, dim),
+                "w2": bw_repack_bytes(dim, ffn), "ws": 7,
+                "gammas": 3 * dim + ffn}
+        for i, layer in enumerate(layers):
+            for key, count in need.items():
+                _need(layer[key], count, f"layers[{i}]['{key}']")
+        self._trace_sizes = {
+            "h_in": dim, "q_attn": dim, "s_attn": 1, "qkv": qkv_n,
+            "q_o": dim, "s_o": 1, "o": dim, "h_mid": dim, "q_ffn": dim,
+            "s_ffn": 1, "gu": 2 * ffn, "q_down": ffn, "s_down": 1,
+            "down": dim, "attn": dim}
         arr = lambda key, dt: (_P * L)(*[_dev(l[key], dt, key)
                                          for l in layers])
         self._arrays = [arr("wqkv", torch.uint8), arr("wo", torch.uint8),
@@ -334,8 +380,9 @@ class Stack:
         self._h = handle
 
     def read_kv(self, layer: int, stream=None):
-        """(keys, values) of one layer's cache: bf16 [Hkv][S][128] copies."""
-        shape = (self.n_kv_heads, self.max_positions, 128)
+        """(keys, values) of one layer's cache: bf16 [Hkv][S][head_dim]
+        copies."""
+        shape = (self.n_kv_heads, self.max_positions, self.head_dim)
         k = torch.empty(shape, dtype=torch.bfloat16, device="cuda")
         v = torch.empty(shape, dtype=torch.bfloat16, device="cuda")
         _check(_lib.bw_stack_read_kv(self._h, layer, k.data_ptr(),
@@ -354,13 +401,21 @@ class Stack:
         with 'layer' and device tensors named as bw_stack_trace's fields."""
         h2 = h_in if h_in.dim() == 2 else h_in.reshape(1, -1)
         steps = h2.shape[0]
+        if h2.shape[1] != self.dim:
+            raise ValueError("h_in has the wrong width")
         if h_out is None:
             h_out = torch.empty_like(h2)
+        _need(h_out, steps * self.dim, "h_out")
         tr_ptr = None
         if trace is not None:
             tr = _StackTrace(int(trace["layer"]))
             for name, _ in _StackTrace._fields_[1:]:
                 t = trace.get(name)
+                if t is not None:
+                    if not t.is_cuda or not t.is_contiguous():
+                        raise ValueError(f"trace['{name}'] must be a "
+                                         "contiguous CUDA tensor")
+                    _need(t, self._trace_sizes[name], f"trace['{name}']")
                 setattr(tr, name, t.data_ptr() if t is not None else None)
             tr_ptr = ctypes.byref(tr)
         _check(_lib.bw_layer_stack(self._h, _dev(h2, torch.float32, "h_in"),

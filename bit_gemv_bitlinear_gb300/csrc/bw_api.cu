@@ -71,7 +71,8 @@ bw_status gemv_common(const int8_t *x, const uint8_t *packed, const float *s,
   a.seg = seg;
   const size_t out_elem = acc_out ? sizeof(int32_t) : sizeof(bw_bf16);
 
-  // Batched activations: tcgen05 tensor cores, tiles of up to 64 rows.
+  // Batched activations: tcgen05 tensor cores, tiles of up to kTcMaxRows
+  // (128) rows.
   if (M >= kMmaMinRows && tc_fits(a)) {
     for (int m0 = 0; m0 < M; m0 += kTcMaxRows) {
       const int rows = M - m0 < kTcMaxRows ? M - m0 : kTcMaxRows;

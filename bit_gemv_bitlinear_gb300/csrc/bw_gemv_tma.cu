@@ -31,6 +31,8 @@
 //  * Programmatic dependent launch: the first pieces are requested before
 //    griddepcontrol.wait (the packed weights are static once bw_repack has
 //    returned); activations, scales and outputs are touched after it.
+#include <atomic>
+
 #include "bw_pipe.cuh"
 
 namespace bw {
@@ -229,17 +231,24 @@ cudaError_t launch_instance(const GemvArgs &g, cudaStream_t stream) {
 
 }  // namespace
 
+// Cached per device: every launch needs the address and the lookup costs a
+// runtime call.  Threads racing on the first lookup store the same value, so
+// the cache is a relaxed atomic.  Like the other per-device state of the
+// library (SM counts, kernel attributes), it assumes the device is not reset
+// with cudaDeviceReset while the library is loaded (bw.h says so).
 unsigned int *device_error_word() {
-  static unsigned int *word[64];
+  static std::atomic<unsigned int *> word[64];
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64)
     return nullptr;
-  if (!word[dev]) {
+  unsigned int *w = word[dev].load(std::memory_order_relaxed);
+  if (!w) {
     void *p = nullptr;
     if (cudaGetSymbolAddress(&p, g_device_error) != cudaSuccess) return nullptr;
-    word[dev] = static_cast<unsigned int *>(p);
+    w = static_cast<unsigned int *>(p);
+    word[dev].store(w, std::memory_order_relaxed);
   }
-  return word[dev];
+  return w;
 }
 
 bool pipe_fits(int mt, int K) {
@@ -265,8 +274,10 @@ cudaError_t launch_gemv_pipe(const GemvArgs &a, int mt, bool acc_out,
 }
 
 cudaError_t launch_selftest_wait(cudaStream_t stream) {
-  int khz = 0;
-  cudaError_t e = cudaDeviceGetAttribute(&khz, cudaDevAttrClockRate, 0);
+  int dev = 0, khz = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e == cudaSuccess)
+    e = cudaDeviceGetAttribute(&khz, cudaDevAttrClockRate, dev);
   if (e != cudaSuccess) return e;
   const long long limit = (long long)(khz > 0 ? khz : 2000000) * 10;  // ~10 ms
   selftest_wait_kernel<<<1, 32, 0, stream>>>(limit);

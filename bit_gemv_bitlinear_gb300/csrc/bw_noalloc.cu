@@ -21,24 +21,18 @@ namespace {
 constexpr int kScratchWords = 64;
 static __device__ __align__(256) unsigned int g_noalloc_scratch[kScratchWords];
 
-// Device address of the array, looked up once per device.  In host code the
+// Device address of the array on the current device.  In host code the
 // name g_noalloc_scratch is only a host-side stand-in for the symbol; a
-// kernel must be given the address that cudaGetSymbolAddress returns.
-constexpr int kDevices = 64;
-unsigned int *g_scratch_addr[kDevices];
-
+// kernel must be given the address that cudaGetSymbolAddress returns.  It is
+// looked up on every call rather than cached: the module can load at another
+// address after a cudaDeviceReset or in another context on the same device,
+// and a per-call lookup also leaves no shared host state between threads.
+// The call is cheap next to the synchronising repack.
 cudaError_t scratch_address(unsigned int **out) {
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
+  void *p = nullptr;
+  cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
   if (e != cudaSuccess) return e;
-  if (dev < 0 || dev >= kDevices) return cudaErrorInvalidDevice;
-  if (g_scratch_addr[dev] == nullptr) {
-    void *p = nullptr;
-    e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
-    if (e != cudaSuccess) return e;
-    g_scratch_addr[dev] = static_cast<unsigned int *>(p);
-  }
-  *out = g_scratch_addr[dev];
+  *out = static_cast<unsigned int *>(p);
   return cudaSuccess;
 }
 

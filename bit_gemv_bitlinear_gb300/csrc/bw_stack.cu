@@ -646,6 +646,7 @@ bw_status run_step(bw_stack *st, cudaStream_t cs, const bw_stack_trace *tr) {
       grid = d.n_kv_heads;
       flip();
     }
+    if (rec) BW_TRY_CUDA(trace_copy(tr->attn, st->attn, dim * 4, cs));
     // o = W2A8(wo, quant(attn_sub_norm(attn))); h += o
     BW_TRY_CUDA(launch_next(
         st->wo[l], dim, dim, 0, st->attn, g + dim, pin, P, d.eps,

@@ -25,6 +25,10 @@
  *   - bf16 values are passed as their 16-bit patterns (the upper half of an
  *     IEEE fp32 pattern), type bw_bf16; __nv_bfloat16 has the same layout.
  *   - Matrices are row-major.  Sizes are element counts.
+ *   - The library keeps per-device state for the life of the process (SM
+ *     counts, kernel attributes, the address of its device error word):
+ *     resetting a device with cudaDeviceReset while the library is loaded
+ *     is not supported.
  *
  * Canonical weight format (input of bw_repack, output of bw_unrepack):
  *   N rows of K/4 bytes; weight w[n][k] in {-1, 0, +1} is stored as the code
@@ -122,13 +126,14 @@ bw_status bw_repack(const uint8_t *canon, int N, int K, uint8_t *packed,
  *   Scratch: instead of allocating its 4-byte bad-code flag, the call uses
  *   a fixed 256-byte array inside the library (every GPU that loads the
  *   library holds it until the process exits; the repack needs one word of
- *   it whatever N and K are).  The first call on each device looks up that
- *   array's device address with the device current; make that first call
- *   before any stream capture.  Every call shares the array and clears the
- *   flag before use, so calls that overlap on the GPU (on different streams
- *   or from different threads) race on it and may report each other's bad
- *   codes: serialise them.  Calls no cudaMalloc, cudaFree or other
- *   allocating routine.  SYNCHRONISES `stream` before returning. */
+ *   it whatever N and K are).  Each call looks up that array's device
+ *   address on the current device.  Every call shares the array and clears
+ *   the flag before use, so calls that overlap on the GPU (on different
+ *   streams or from different threads) race on it and may report each
+ *   other's bad codes: serialise them.  Calls no cudaMalloc, cudaFree or
+ *   other allocating routine.  SYNCHRONISES `stream` before returning (it
+ *   copies the flag to the host and waits for it), so it must not be called
+ *   while `stream` is being captured into a graph. */
 bw_status bw_repack_noalloc(const uint8_t *canon, int N, int K,
                             uint8_t *packed, bw_stream_t stream);
 
@@ -271,6 +276,8 @@ typedef struct {
     bw_bf16 *gu;                     /* [2 ffn]                            */
     int8_t *q_down; float *s_down;   /* [ffn], [1]                         */
     bw_bf16 *down;                   /* [dim]                              */
+    float *attn;                     /* [dim] attention output: the fp32
+                                        input of attn_sub_norm             */
 } bw_stack_trace;
 
 /* Creates a stack: copies the descriptor (the pointer arrays; the weights

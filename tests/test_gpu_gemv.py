@@ -284,3 +284,20 @@ def test_batched_tensor_core_tiles(bw, M, N, K):
     case["q"][M // 2, ::3] = -128
     case["q"][M // 2, 1::3] = 127
     run_case(bw, case)
+
+
+@pytest.mark.parametrize("M", [512, 1024, 2048])
+def test_prefill_sizes(bw, M):
+    """Prompt-sized batches (the W2A8 page's §一 splits prefill from decode):
+    M = 512 .. 2048 tokens of absmax-quantised N(0,1) rows against the w13
+    shape, int32 exact and bf16 within one ulp on sampled output rows (all
+    M tokens of each), including both ends and the gate/up boundary."""
+    N, K = 13824, 2560
+    case = synth.gemv_case(M, N, K, synth.base_seed(11, M // 512),
+                           uniform_x=False, bounds=[0, 6912, N])
+    q, _ = oracle.quant_act(case["xf"])
+    case["q"] = q
+    rows = np.unique(np.concatenate([
+        np.arange(0, 16), np.arange(6904, 6920), np.arange(N - 16, N),
+        (synth.u64(13, M, 160) % np.uint64(N)).astype(np.int64)]))
+    run_case(bw, case, rows=rows)

@@ -106,7 +106,7 @@ def trace_buffers(dim, ffn, qkv_n, layer):
             "qkv": b16(qkv_n), "q_o": i8(dim), "s_o": f(1), "o": b16(dim),
             "h_mid": f(dim), "q_ffn": i8(dim), "s_ffn": f(1),
             "gu": b16(2 * ffn), "q_down": i8(ffn), "s_down": f(1),
-            "down": b16(dim)}
+            "down": b16(dim), "attn": f(dim)}
 
 
 def test_zero_weights_layer_is_identity(bw):
@@ -133,13 +133,15 @@ def test_graph_steps_equal_eager_steps(bw):
     stack.close()
 
 
-@pytest.mark.parametrize("layer", [0, 1])
-def test_bitnet_stack_per_stage_parity(bw, layer):
+@pytest.mark.parametrize("layer,steps", [(0, 2), (1, 2), (1, 256)])
+def test_bitnet_stack_per_stage_parity(bw, layer, steps):
+    """The trace is of the last step of the call: steps 1 and 255 (the
+    bench's runs are 256 steps long)."""
     dim, ffn, nh, nkv = 2560, 6912, 20, 5
     hd = dim // nh
     qkv_n = (nh + 2 * nkv) * hd
     stack, w = make_stack(bw, 2, dim, ffn, nh, nkv, 33, gamma_one=False)
-    h0 = synth.step_inputs(7, 2, dim)
+    h0 = synth.step_inputs(7, steps, dim)
     tr = trace_buffers(dim, ffn, qkv_n, layer)
     out = stack.run(to_dev(h0), trace=tr)
     assert bw.bw_device_error() == 0
@@ -149,8 +151,9 @@ def test_bitnet_stack_per_stage_parity(bw, layer):
     g = L["gammas"]
     eps = w["eps"]
     B = w["bounds"]
+    p = steps - 1
     if layer == 0:
-        assert (T["h_in"] == h0[1]).all()
+        assert (T["h_in"] == h0[p]).all()
     flips = 0
     # attention_norm + quant -> wqkv
     flips += check_norm_quant(T["h_in"], g[:dim], eps, T["q_attn"],
@@ -160,6 +163,7 @@ def test_bitnet_stack_per_stage_parity(bw, layer):
     assert_bf16_within_ulp(T["qkv"], ref, "wqkv")
     # one-token attention + attn_sub_norm + quant -> wo
     att = oracle.attn_one_token(T["qkv"], nh, nkv, hd)
+    assert (T["attn"] == att).all()          # bf16 values copied exactly
     flips += check_norm_quant(att, g[dim:2 * dim], eps, T["q_o"],
                               float(T["s_o"][0]), "attn_sub_norm")
     ref = oracle.gemv(T["q_o"], L["wo"], T["s_o"], L["ws"][3:4], B["wo"],
@@ -184,7 +188,7 @@ def test_bitnet_stack_per_stage_parity(bw, layer):
     if layer == 1:
         h_out = (T["h_mid"] + synth.bf16_bits_to_f32(T["down"])).astype(
             np.float32)
-        assert (out[1].cpu().numpy() == h_out).all()
+        assert (out[p].cpu().numpy() == h_out).all()
     stack.close()
 
 

@@ -8,9 +8,11 @@ plain stack, parity is per stage, teacher-forced from the GPU's own trace
 and, for the attention, from the GPU's own cache:
 * the appended row of the traced step within one bf16 ulp of the oracle's
   append of the traced q|k|v (values exact), rows past it untouched;
-* attn_sub_norm + quantisation from the oracle's attention over the GPU's
-  cache: the GPU attention is within 2^-13 of the largest value, so codes
-  may differ by one within 0.1 of a rounding tie and the scale by 2^-12;
+* the traced fp32 attention output against the oracle's attention over the
+  GPU's own cache, within 2^-13 of the largest value of the KV head (the
+  bound of the attention's own tests), then attn_sub_norm + quantisation
+  from that traced output at the plain stack's bar (scale within 1e-5,
+  codes equal except within 1e-3 of a rounding tie);
 * every GEMV and residual as in the plain stack's test.
 End to end over a few tokens it stays within 1 % of the oracle's layers.
 """
@@ -50,32 +52,21 @@ def make_kv_stack(bw, n_layers, dim, ffn, nh, nkv, seed, S,
     return stack, w
 
 
-def check_norm_quant_loose(x, gamma, eps, q_gpu, s_gpu, what):
-    normed = oracle.rmsnorm(x, gamma, eps)
-    q_ref, s_ref = oracle.quant_act(normed)
-    q_ref, s_ref = q_ref[0], float(s_ref[0])
-    assert abs(s_gpu - s_ref) <= 2.0 ** -12 * abs(s_ref), (what, s_gpu, s_ref)
-    diff = np.nonzero(q_gpu.astype(np.int32) != q_ref.astype(np.int32))[0]
-    if diff.size:
-        prod = normed[diff].astype(np.float64) * s_ref
-        frac = np.abs(prod - np.floor(prod) - 0.5)
-        assert (frac < 0.1).all(), (what, diff[:8], prod[:8])
-        assert (np.abs(q_gpu[diff].astype(np.int32)
-                       - q_ref[diff].astype(np.int32)) <= 1).all(), what
-        assert diff.size <= max(2, x.size // 100), (what, diff.size)
-
-
-@pytest.mark.parametrize("layer", [0, 1])
-def test_kv_stack_per_stage_parity(bw, layer):
-    dim, ffn, nh, nkv, S = 2560, 6912, 20, 5, 64
+@pytest.mark.parametrize("layer,steps,S", [(0, 3, 64), (1, 3, 64),
+                                           (1, 200, 256)])
+def test_kv_stack_per_stage_parity(bw, layer, steps, S):
+    """The trace is of the last token of the call: position 2 (a context the
+    attention finishes in one CTA per KV head) and position 199 (200
+    positions in four splits merged across CTAs, the path the bench's
+    256-token runs take past position 127)."""
+    dim, ffn, nh, nkv = 2560, 6912, 20, 5
     hd = dim // nh
     qkv_n = (nh + 2 * nkv) * hd
     stack, w = make_kv_stack(bw, 2, dim, ffn, nh, nkv, 41, S,
                              gamma_one=False)
-    steps = 3
     h0 = synth.step_inputs(9, steps, dim)
     tr = trace_buffers(dim, ffn, qkv_n, layer)
-    out = stack.run(to_dev(h0), trace=tr)        # positions 0, 1, 2
+    out = stack.run(to_dev(h0), trace=tr)        # positions 0 .. steps - 1
     kc_d, vc_d = stack.read_kv(layer)
     torch.cuda.synchronize()
     assert bw.bw_device_error() == 0
@@ -100,11 +91,17 @@ def test_kv_stack_per_stage_parity(bw, layer):
                            "appended key row")
     assert (kc[:, p + 1:] == 0).all() and (vc[:, p + 1:] == 0).all()
     assert (kc[:, :p] != 0).any() and (vc[:, :p] != 0).any()
-    # attention over the GPU's own cache -> attn_sub_norm -> wo
+    # attention over the GPU's own cache, then attn_sub_norm from the traced
+    # attention output -> wo
     att = oracle.attn_over_cache(T["qkv"], nh, nkv, hd, p, THETA, kc, vc)
-    att = att.reshape(-1).astype(np.float32)
-    check_norm_quant_loose(att, g[dim:2 * dim], eps, T["q_o"],
-                           float(T["s_o"][0]), "attn_sub_norm")
+    G = nh // nkv
+    got = T["attn"].reshape(nh, hd).astype(np.float64)
+    for h in range(nh):
+        vmax = np.abs(synth.bf16_bits_to_f32(vc[h // G, :p + 1])).max()
+        err = np.abs(got[h] - att[h]).max()
+        assert err <= 2.0 ** -13 * vmax, (h, err, vmax)
+    check_norm_quant(T["attn"], g[dim:2 * dim], eps, T["q_o"],
+                     float(T["s_o"][0]), "attn_sub_norm")
     ref = oracle.gemv(T["q_o"], L["wo"], T["s_o"], L["ws"][3:4], B["wo"],
                       dim, dim)[0]
     assert_bf16_within_ulp(T["o"], ref, "wo")

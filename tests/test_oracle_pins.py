@@ -466,6 +466,110 @@ def test_layer_kv_ignores_rows_past_p():
     assert (late == base).all()
 
 
+def _hand_layer():
+    """The hand-worked layer of tests/golden/layer_hand.txt as a dict of
+    float arrays (matrices as [rows][cols] lists of weights)."""
+    out = {}
+    for line in read_golden("layer_hand.txt"):
+        key, val = (t.strip() for t in line.split("=", 1))
+        if "|" in val:
+            out[key] = np.array([[float(v) for v in row.split()]
+                                 for row in val.split("|")])
+        else:
+            out[key] = np.array([float(v) for v in val.split()])
+    return out
+
+
+def _exact_bf16(values):
+    """bf16 bit patterns of values that bf16 holds exactly (the pattern is
+    the high half of the fp32 pattern; checked, no rounding involved)."""
+    f = np.asarray(values, np.float32)
+    u = f.view(np.uint32)
+    assert ((u & 0xFFFF) == 0).all(), values
+    return (u >> 16).astype(np.uint16)
+
+
+def _hand_args(G, case):
+    dim, ffn, nh, nkv = (int(v) for v in G[case + ".shape"])
+    mats = [oracle.pack(G[case.replace("B", "A") + "." + name]
+                        .astype(np.int8))
+            for name in ("wqkv", "wo", "w13", "w2")]
+    ws = _exact_bf16(G["A.ws"])
+    gam = G["A.gammas"].astype(np.float32)
+    return dim, ffn, nh, nkv, mats, ws, gam
+
+
+def test_layer_hand_worked_one_token():
+    """h_out of the hand-worked layer (one-token attention), exactly; the
+    golden file derives every stage from the block order of the W2A8 page's
+    §4.1.  A swapped gain slice, weight-scale offset, query-to-KV head map
+    or a dropped residual changes the result."""
+    G = _hand_layer()
+    dim, ffn, nh, nkv, mats, ws, gam = _hand_args(G, "A")
+    h = G["A.h"].astype(np.float32)
+    out = oracle.layer(h, dim, ffn, nh, nkv, float(G["A.eps"][0]), *mats, ws,
+                       gam)
+    assert (out == G["A.h_out"].astype(np.float32)).all(), out
+
+
+def test_layer_hand_worked_stages():
+    """The stage functions reproduce each hand-derived intermediate of the
+    golden layer from the previous one (teacher forced)."""
+    G = _hand_layer()
+    dim, ffn, nh, nkv, mats, ws, gam = _hand_args(G, "A")
+    eps = float(G["A.eps"][0])
+    hd = dim // nh
+    qkv_n = (nh + 2 * nkv) * hd
+
+    def nqg(v, g, canon, n_out, k, w_bits, bounds):
+        q, s = oracle.quant_act(oracle.rmsnorm(v, g, eps))
+        return oracle.gemv(q, canon, s, w_bits, bounds, n_out, k)[0]
+
+    f = lambda bits: synth.bf16_bits_to_f32(bits)
+    qkv = nqg(G["A.h"], gam[:dim], mats[0], qkv_n, dim, ws[0:3],
+              [0, nh * hd, (nh + nkv) * hd, qkv_n])
+    assert (f(qkv) == [0, 0, 0, 0, 0, 0, -1.5, 1.5]).all(), f(qkv)
+    att = oracle.attn_one_token(qkv, nh, nkv, hd)
+    assert (att == G["A.attn"]).all()
+    o = nqg(G["A.attn"], gam[dim:2 * dim], mats[1], dim, dim, ws[3:4],
+            [0, dim])
+    assert (f(o) == G["A.o"]).all()
+    gu = nqg(G["A.h_mid"], gam[2 * dim:3 * dim], mats[2], 2 * ffn, dim,
+             ws[4:6], [0, ffn, 2 * ffn])
+    assert (oracle.relu2_gate(gu) == G["A.gated"]).all()
+    d = nqg(G["A.gated"], gam[3 * dim:], mats[3], dim, ffn, ws[6:7],
+            [0, dim])
+    assert (f(d) == G["A.down"]).all()
+
+
+def test_layer_kv_hand_worked():
+    """The hand-worked layer with attention over a KV cache at p = 1: the
+    queries are zero, so the softmax over rows 0..1 is uniform; the new
+    token's value and (rotated, zero) key are appended at row 1 and rows 2
+    and 3, past the context, are neither read nor written."""
+    G = _hand_layer()
+    dim, ffn, nh, nkv, mats, ws, gam = _hand_args(G, "B")
+    hd = dim // nh
+    S, p = int(G["B.S"][0]), int(G["B.p"][0])
+    kc = _exact_bf16(G["B.k_cache"]).reshape(nkv, S, hd)
+    vc = _exact_bf16(G["B.v_cache"]).reshape(nkv, S, hd)
+    h = G["B.h"].astype(np.float32)
+    out, kc2, vc2 = oracle.layer_kv(h, dim, ffn, nh, nkv,
+                                    float(G["B.eps"][0]), *mats, ws, gam,
+                                    kc, vc, p, float(G["B.theta"][0]))
+    assert (out == G["B.h_out"].astype(np.float32)).all(), out
+    assert (synth.bf16_bits_to_f32(kc2[0, p]) == G["B.k_row1"]).all()
+    assert (vc2[0, p] == _exact_bf16(G["B.v_row1"])).all()
+    rows = [j for j in range(S) if j != p]
+    assert (kc2[:, rows] == kc[:, rows]).all()
+    assert (vc2[:, rows] == vc[:, rows]).all()
+    # the attention stage alone on the appended cache
+    qkv = _exact_bf16([0, 0, 0, 0, 0, 0, -1.5, 1.5])
+    att = oracle.attn_over_cache(qkv, nh, nkv, hd, p, float(G["B.theta"][0]),
+                                 kc2, vc2)
+    assert (att.reshape(-1) == G["B.attn"]).all()
+
+
 # --------------------------------------------- absmean weight ternarisation
 # [W2A8] §4.2: s = 1 / max(mean|W|, 1e-5), w = clamp(round(W s), -1, 1),
 # ws = bf16(1 / s), one scale per weight-scale segment.

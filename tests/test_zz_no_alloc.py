@@ -6,10 +6,15 @@ not call cudaMalloc (or the stream-ordered allocator) behind its back; for
 them the library offers a repack whose scratch word lives in a fixed array
 inside the library.  Its output must be identical to bw_repack's (packed
 bytes are compared exactly, the bar for byte work), on two calls in a row,
-since every call reuses the same scratch and must clear it first.  This file
-is collected last and also passes when run alone in a fresh process.
+since every call reuses the same scratch and must clear it first.  It must
+also allocate nothing: the device's default memory pool (which the
+stream-ordered allocator behind bw_repack draws from) sees no use, and the
+device's free memory does not move, while bw_repack, the control, does draw
+from the pool.  This file is collected last and also passes when run alone in
+a fresh process.
 """
 import ctypes
+import os
 
 import numpy as np
 import pytest
@@ -77,3 +82,71 @@ def test_noalloc_rejects_sizes_beyond_the_limits(lib):
     assert f(dummy.data_ptr(), 8, 65540, dummy.data_ptr(), None) == SHAPE
     assert f(dummy.data_ptr(), (1 << 24) + 1, 64, dummy.data_ptr(),
              None) == SHAPE
+
+
+# cudaMemPoolAttr values from the CUDA runtime's driver_types.h.
+USED_MEM_CURRENT, USED_MEM_HIGH = 0x7, 0x8
+
+
+def _cudart():
+    """The CUDA runtime as a shared library (the library under test links
+    its own copy statically; both see the same device memory pool)."""
+    home = os.environ.get("CUDA_HOME", "/usr/local/cuda")
+    for name in (os.path.join(home, "lib64", "libcudart.so"),
+                 os.path.join(home, "lib64", "libcudart.so.13"),
+                 "libcudart.so.13", "libcudart.so"):
+        try:
+            rt = ctypes.CDLL(name)
+        except OSError:
+            continue
+        rt.cudaDeviceGetDefaultMemPool.argtypes = [ctypes.POINTER(P),
+                                                   ctypes.c_int]
+        rt.cudaMemPoolGetAttribute.argtypes = [P, ctypes.c_int, P]
+        rt.cudaMemPoolSetAttribute.argtypes = [P, ctypes.c_int, P]
+        return rt
+    pytest.skip("no shared CUDA runtime library to query the memory pool")
+
+
+def test_noalloc_allocates_nothing(lib):
+    rt = _cudart()
+    pool = P()
+    assert rt.cudaDeviceGetDefaultMemPool(
+        ctypes.byref(pool), torch.cuda.current_device()) == 0
+
+    def attr(which):
+        v = ctypes.c_uint64(0)
+        assert rt.cudaMemPoolGetAttribute(pool, which, ctypes.byref(v)) == 0
+        return v.value
+
+    def reset_high():
+        zero = ctypes.c_uint64(0)
+        assert rt.cudaMemPoolSetAttribute(pool, USED_MEM_HIGH,
+                                          ctypes.byref(zero)) == 0
+
+    N, K = 2560, 2560
+    canon = synth.canonical_weights(synth.base_seed(12, 6), N, K)
+    canon_d = torch.from_numpy(canon).cuda()
+    out = torch.empty((lib.bw_repack_bytes(N, K),), dtype=torch.uint8,
+                      device="cuda")
+    stream = torch.cuda.current_stream().cuda_stream
+
+    def call(fn):
+        rc = getattr(lib, fn)(canon_d.data_ptr(), N, K, out.data_ptr(),
+                              stream)
+        torch.cuda.synchronize()
+        assert rc == OK
+
+    # A first call may load the library's code onto the device (lazy module
+    # loading), which the driver backs with device memory of its own.
+    call("bw_repack_noalloc")
+    used = attr(USED_MEM_CURRENT)
+    free_before = torch.cuda.mem_get_info()[0]
+    reset_high()
+    for _ in range(2):
+        call("bw_repack_noalloc")
+    assert attr(USED_MEM_HIGH) <= used            # nothing drawn from the pool
+    assert torch.cuda.mem_get_info()[0] == free_before
+    # the control: bw_repack's stream-ordered scratch word shows in the pool
+    reset_high()
+    call("bw_repack")
+    assert attr(USED_MEM_HIGH) > used
