@@ -18,8 +18,9 @@ CUDA events between the two give the GEMV kernel's own time inside the
 timed region.
 
 value = packed weight bytes per step / step time (GB/s, all GPUs).
-The reference arm (--impl reference) times the CPU oracle, single-threaded,
-on a bounded sample of the same workload, in the same unit.
+The reference arm (--impl reference) times the CPU oracle, its output rows
+split over every host core, on a bounded sample of the same workload, in
+the same unit.
 Multi-GPU: replicas only (the path has no exchange step); each rank runs the
 same workload on its own GPU.
 """
@@ -50,12 +51,35 @@ SHAPES = ["wqkv", "wo", "w13", "w2"]
 REPLICAS = 16
 FALLBACK_HBM_GBS = 6800.0
 
-# DRAM bytes (read + write) per launch of the current TMA GEMV kernel,
-# measured with ncu (dram__bytes_read.sum + dram__bytes_write.sum, median of
-# 4 launches of the bench's own sweep).  Must be re-measured -- or set to
-# None -- whenever the GEMV kernel changes.
-MEASURED_DRAM_BYTES = {"wqkv": 2487936, "wo": 1668736, "w13": 8877824,
-                       "w2": 4458880}
+# DRAM bytes (read + write) per launch of the TMA GEMV kernel, measured with
+# ncu (dram__bytes_read.sum + dram__bytes_write.sum, median of the captured
+# launches of the bench's own sweep), with the SHA-256 of the kernel's
+# source files at the time.  The bench reports them only while those files
+# are unchanged, so a changed kernel reports null until it is re-measured.
+TRAFFIC_SOURCES = ("bit_gemv_bitlinear_gb300/csrc/bw_pipe.cuh",
+                   "bit_gemv_bitlinear_gb300/csrc/bw_gemv_tma.cu")
+MEASURED_DRAM = {
+    "sha256": "0ed513557a113e3a4390ad8bb2caea50937b91abb59256fbe9fceabdfa61732b",
+    "bytes": {"wqkv": 2488064, "wo": 1668480, "w13": 8877824, "w2": 4458496}}
+
+
+def traffic_sources_sha() -> str:
+    import hashlib
+    h = hashlib.sha256()
+    for rel in TRAFFIC_SOURCES:
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()
+
+
+def measured_traffic():
+    """ncu DRAM bytes per GEMV launch (mean over the 4 shapes), or None if
+    the kernel changed since they were taken."""
+    if (not MEASURED_DRAM["bytes"]
+            or MEASURED_DRAM["sha256"] != traffic_sources_sha()):
+        return None
+    b = MEASURED_DRAM["bytes"]
+    return round(sum(b[n] for n in SHAPES) / len(SHAPES))
 
 
 def parse_args():
@@ -70,6 +94,9 @@ def parse_args():
                    help="skip the layer-stack tok/s measurement")
     p.add_argument("--no-batched", action="store_true",
                    help="skip the batched M = 4/16/64 timings")
+    p.add_argument("--no-configs", action="store_true",
+                   help="skip the single-shape timings of the 2560x2560 "
+                        "and large-shape configurations")
     p.add_argument("--no-attn", action="store_true",
                    help="skip the decode-attention timings")
     p.add_argument("--attn", action="store_true",
@@ -429,6 +456,10 @@ def run_ours(args):
     e2e_ms = job_time_ms(torch, e_start.elapsed_time(e_end), world, dev) / K_steps
     e2e_value = job_value(world, wbytes_step, e2e_ms)
 
+    configs_line = None
+    if rank == 0 and not args.no_configs:
+        configs_line = run_config_shapes(torch, bw, dev, peak)
+
     stack_line = stack_kv_line = None
     if not args.no_stack:
         stack_line = run_stack_timing(torch, bw, dev)
@@ -479,9 +510,7 @@ def run_ours(args):
                 "peak_kind": peak_kind,
                 "unit": "GB/s",
                 "frac": round(achieved / peak, 4),
-                "traffic": (round(sum(MEASURED_DRAM_BYTES[n] for n in SHAPES)
-                                  / len(SHAPES))
-                            if MEASURED_DRAM_BYTES else None),
+                "traffic": measured_traffic(),
                 "traffic_unit": "bytes per GEMV launch (ncu)",
                 "alg_bytes_per_launch": round(alg_total / (K_steps * R
                                                            * len(SHAPES))),
@@ -492,6 +521,8 @@ def run_ours(args):
             "gpu_launches": (gemv_launches + quant_launches) * K_steps,
             "clocks": clocks,
         }
+        if configs_line is not None:
+            line["configs"] = configs_line
         if stack_line is not None:
             line["layer_stack"] = stack_line
         if stack_kv_line is not None:
@@ -604,31 +635,79 @@ def per_shape_times(torch, bw, shapes, act, outs, R, stream, reps=50):
     return res
 
 
+def oracle_gemv_threads(oracle, q, canon, s, ws, bounds, N, K, threads):
+    """The oracle's GEMV over `threads` contiguous slices of output rows, run
+    on a thread pool: each slice is one call of the unmodified oracle (its C
+    code releases the GIL), with the weight-scale segments cut to the slice.
+    Rows are independent, so the result equals one call over all rows."""
+    import concurrent.futures as cf
+    cuts = [N * i // threads for i in range(threads + 1)]
+    bounds = np.asarray(bounds)
+
+    def part(i):
+        lo, hi = cuts[i], cuts[i + 1]
+        if hi <= lo:
+            return np.empty((q.shape[0] if q.ndim == 2 else 1, 0), np.uint16)
+        seg_lo = int(np.searchsorted(bounds, lo, side="right") - 1)
+        seg_hi = int(np.searchsorted(bounds, hi - 1, side="right") - 1)
+        b = [lo] + [int(v) for v in bounds[seg_lo + 1:seg_hi + 1]] + [hi]
+        b = [v - lo for v in b]
+        return oracle.gemv(q, canon[lo:hi], s, ws[seg_lo:seg_hi + 1], b,
+                           hi - lo, K)
+
+    with cf.ThreadPoolExecutor(max_workers=threads) as ex:
+        return np.concatenate(list(ex.map(part, range(threads))), axis=1)
+
+
+def oracle_step(oracle, shapes, act, threads):
+    """One replica's step through the oracle: the quantisation of its rows,
+    then the 4 decode-shape GEMVs; returns the packed weight bytes."""
+    wb = 0
+    for K, a in act.items():
+        oracle.quant_act(a["xf"][: len(a["names"])])
+    for name in SHAPES:
+        sh = shapes[name]
+        K = sh["K"]
+        a = act[K]
+        q, s = oracle.quant_act(a["xf"][a["names"].index(name)])
+        if threads == 1:
+            oracle.gemv(q, sh["canon"], s, sh["ws"], sh["bounds"], sh["N"], K)
+        else:
+            oracle_gemv_threads(oracle, q, sh["canon"], s, sh["ws"],
+                                sh["bounds"], sh["N"], K, threads)
+        wb += weight_bytes(sh["N"], K)
+    return wb
+
+
 def cpu_baseline(shapes, act, seconds):
-    """The oracle as it stands, single-threaded, on whole steps of the
-    workload restricted to one replica, repeated for a bounded time."""
+    """The oracle as it stands on whole steps of the workload restricted to
+    one replica, repeated for a bounded time: on every host core (output
+    rows split over a thread pool), and on one core."""
     import oracle
     oracle.build()
-    t0 = time.perf_counter()
-    reps, wbytes = 0, 0
-    while True:
-        for K, a in act.items():
-            oracle.quant_act(a["xf"][: len(a["names"])])
-        for name in SHAPES:
-            sh = shapes[name]
-            K = sh["K"]
-            a = act[K]
-            q, s = oracle.quant_act(a["xf"][a["names"].index(name)])
-            oracle.gemv(q, sh["canon"], s, sh["ws"], sh["bounds"], sh["N"], K)
-            wbytes += weight_bytes(sh["N"], K)
-        reps += 1
-        if time.perf_counter() - t0 >= seconds:
-            break
-    dt = time.perf_counter() - t0
-    return {"value": round(wbytes / dt / 1e9, 4), "unit": "GB/s", "cores": 1,
+    cores = os.cpu_count() or 1
+    res = {}
+    for threads in (cores, 1):
+        t0 = time.perf_counter()
+        reps, wbytes = 0, 0
+        while True:
+            wbytes += oracle_step(oracle, shapes, act, threads)
+            reps += 1
+            if time.perf_counter() - t0 >= seconds / 2:
+                break
+        dt = time.perf_counter() - t0
+        res[threads] = (wbytes / dt / 1e9, reps, dt)
+    v, reps, dt = res[cores]
+    v1, reps1, dt1 = res[1]
+    return {"value": round(v, 4), "unit": "GB/s", "cores": cores,
             "kind": "oracle",
             "sample": f"{reps} pass(es) of quant + the 4 decode-shape GEMVs "
-                      f"(one replica), {dt:.1f} s on 1 host core"}
+                      f"(one replica), {dt:.1f} s, output rows split over "
+                      f"{cores} threads",
+            "single_core": {"value": round(v1, 4), "unit": "GB/s",
+                            "cores": 1,
+                            "sample": f"{reps1} pass(es), {dt1:.1f} s on one "
+                                      f"thread"}}
 
 
 def run_reference(args):
@@ -653,18 +732,10 @@ def run_reference(args):
     import oracle
     oracle.build()
 
+    cores = os.cpu_count() or 1
+
     def one_step():
-        wb = 0
-        for K, a in act.items():
-            oracle.quant_act(a["xf"])
-        for name in SHAPES:
-            sh = shapes[name]
-            a = act[sh["K"]]
-            q, s = oracle.quant_act(a["xf"][a["names"].index(name)])
-            oracle.gemv(q, sh["canon"], s, sh["ws"], sh["bounds"], sh["N"],
-                        sh["K"])
-            wb += weight_bytes(sh["N"], sh["K"])
-        return wb
+        return oracle_step(oracle, shapes, act, cores)
 
     for _ in range(args.warmup):
         one_step()
@@ -676,7 +747,7 @@ def run_reference(args):
     value = wb / dt / 1e9
     sample = (f"each step: quant + the 4 decode-shape GEMVs of one replica "
               f"(1/{REPLICAS} of a GPU step); {args.steps} steps in "
-              f"{dt:.1f} s on 1 host core")
+              f"{dt:.1f} s, output rows split over {cores} host threads")
     line = {
         "impl": "reference",
         "metric": METRIC, "value": round(value, 4), "unit": "GB/s",
@@ -685,9 +756,10 @@ def run_reference(args):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "int8", "data": "synthetic",
         "config": {"workload": WORKLOAD, "replicas": 1,
-                   "implementation": "CPU oracle (plain C, single thread)"},
+                   "implementation": "CPU oracle (plain C; output rows "
+                                     f"split over {cores} threads)"},
         "cpu_baseline": {"value": round(value, 4), "unit": "GB/s",
-                         "cores": 1, "kind": "oracle", "sample": sample},
+                         "cores": cores, "kind": "oracle", "sample": sample},
         "e2e": {"value": round(value, 4), "unit": "GB/s",
                 "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
@@ -749,6 +821,33 @@ def time_shape(torch, bw, dev, N, K, M, iters=2000, rotate=0, eager=False):
     ab = algorithmic_bytes(N, K, 1) + (M - 1) * (K + 2 * N + 4)
     return {"us": us, "rotate": rot, "calls": reps * per_graph,
             "weight_bytes": wb, "alg_bytes": ab}
+
+
+# The single-call configurations: one 2560 x 2560 GEMV with one weight scale,
+# and the large M = 1 shapes whose weights (70.8 and 17.7 MB) far exceed L2.
+CONFIG_SHAPES = (("single_2560x2560", 2560, 2560),
+                 ("large_55296x5120", 55296, 5120),
+                 ("large_13824x5120", 13824, 5120))
+
+
+def run_config_shapes(torch, bw, dev, peak_gbs):
+    """us per call of each single-call configuration, back to back in a CUDA
+    graph over rotating weight buffers (their total over 4x L2), with the
+    weight GB/s and the fraction of the measured HBM copy peak on the
+    algorithmic bytes (weights + x + y + scales)."""
+    out = {"timing": "graph of calls back to back over rotating weight "
+                     "buffers (over 4x L2), CUDA events",
+           "kernel": "gemv_w2a8_pipe_kernel"}
+    for name, N, K in CONFIG_SHAPES:
+        t = time_shape(torch, bw, dev, N, K, 1, iters=1024)
+        us = t["us"]
+        out[name] = {"N": N, "K": K, "us_per_call": round(us, 3),
+                     "weight_GBps": round(t["weight_bytes"] / (us * 1e3), 1),
+                     "alg_GBps": round(t["alg_bytes"] / (us * 1e3), 1),
+                     "hbm_frac": round(t["alg_bytes"] / (us * 1e3) / peak_gbs,
+                                       4),
+                     "weight_buffers": t["rotate"]}
+    return out
 
 
 BATCHED_N, BATCHED_K, BATCHED_M = 13824, 2560, (4, 16, 64)

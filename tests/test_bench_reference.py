@@ -30,8 +30,29 @@ def test_reference_arm_prints_one_contract_line():
     assert d["value"] > 0 and d["ms_per_step"] > 0
     assert d["config"]["workload"] == bench.WORKLOAD
     cb = d["cpu_baseline"]
-    assert cb["kind"] == "oracle" and cb["cores"] == 1 and cb["sample"]
+    assert cb["kind"] == "oracle" and cb["cores"] == (os.cpu_count() or 1)
+    assert cb["sample"]
     assert cb["value"] == d["value"]
     e = d["e2e"]
     assert e["value"] == d["value"] and e["unit"] == d["unit"]
     assert e["h2d_bytes_per_step"] == 0 and e["d2h_bytes_per_step"] == 0
+
+
+def test_row_split_oracle_equals_one_call():
+    """The all-core baseline splits a GEMV's output rows over threads, each
+    slice an unmodified oracle call with its own weight-scale segments: the
+    result is the single call's, bit for bit (the wqkv segments are cut)."""
+    import numpy as np
+
+    import bench
+    import oracle
+    import synth
+    N, K, bounds = synth.DECODE_SHAPES["wqkv"]
+    case = synth.gemv_case(1, N, K, synth.base_seed(1, 9), bounds=bounds)
+    q, s = oracle.quant_act(case["xf"])
+    want = oracle.gemv(q, case["canon"], s, case["ws"], case["bounds"], N, K)
+    for threads in (1, 3, 7, 16):
+        got = bench.oracle_gemv_threads(oracle, q, case["canon"], s,
+                                        case["ws"], case["bounds"], N, K,
+                                        threads)
+        assert (got == want).all(), threads
