@@ -264,6 +264,7 @@ bw_status bw_selftest_wait_timeout(unsigned int *bits, bw_stream_t stream) {
   if (!bits) return BW_ERR_INVALID_ARG;
   cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
   cudaError_t e = launch_selftest_wait(cs);
+  if (e == cudaSuccess) e = launch_selftest_poll(cs);
   if (e == cudaSuccess) e = read_device_error(cs, bits);
   if (e != cudaSuccess) return cuda_status(e);
   return *bits ? BW_ERR_TIMEOUT : BW_OK;

@@ -119,6 +119,34 @@ size_t attn_workspace_bytes(int H, int Hkv, int D, int S);  // 0: unsupported
 bw_status check_attn(int H, int Hkv, int D, int S);
 cudaError_t launch_attn(const AttnLaunch &l, cudaStream_t stream);
 
+// The layer stack as one persistent kernel (bw_decoder.cu) for stacks
+// without a KV cache.  The table holds the per-layer pointers
+// (decoder_upload_table); the exchange buffers (decoder_xch_bytes) are
+// zeroed once and the 4 control words set to {1, 0, 0, 0} once, at creation.
+struct DecoderLaunch {
+  const void *table;
+  int n_layers, steps, dim, ffn, n_heads, n_kv;
+  float eps;
+  const float *h_in;   // [steps][dim]
+  float *h_out;        // [steps][dim]
+  void *xch;
+  unsigned int *ctl;
+  const bw_stack_trace *trace;  // or null
+};
+size_t decoder_xch_bytes(int dim, int ffn);
+size_t decoder_table_bytes(int n_layers);
+bool decoder_fits(int dim, int ffn, int n_heads, int n_kv, int n_layers);
+cudaError_t decoder_upload_table(void *table, int n_layers,
+                                 const uint8_t *const *wqkv,
+                                 const uint8_t *const *wo,
+                                 const uint8_t *const *w13,
+                                 const uint8_t *const *w2,
+                                 const bw_bf16 *const *ws,
+                                 const float *const *gammas);
+cudaError_t launch_decoder(const DecoderLaunch &l, cudaStream_t stream);
+// Self-test of the decoder's bounded exchange poll (sets bit 64 in ~10 ms).
+cudaError_t launch_selftest_poll(cudaStream_t stream);
+
 // Remembers a CUDA error for bw_last_cuda_error() (calling thread).
 void record_cuda_error(int err);
 

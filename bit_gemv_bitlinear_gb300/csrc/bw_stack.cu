@@ -557,6 +557,13 @@ struct bw_stack {
   size_t kv_layer_elems;
   cudaGraphExec_t exec;
   bool have_graph;
+  // Stacks without a KV cache run as one persistent kernel per call
+  // (bw_decoder.cu): its per-layer pointer table, exchange buffers and
+  // control words.
+  bool persistent;
+  void *dec_table;
+  void *dec_xch;
+  unsigned int *dec_ctl;
 };
 
 namespace {
@@ -679,8 +686,32 @@ bw_status run_step(bw_stack *st, cudaStream_t cs, const bw_stack_trace *tr) {
   return BW_OK;
 }
 
+// One persistent-kernel launch over `steps` steps (stacks without a cache).
+bw_status run_decoder(bw_stack *st, const float *h_in, int steps,
+                      float *h_out, const bw_stack_trace *tr,
+                      cudaStream_t cs) {
+  DecoderLaunch dl{};
+  dl.table = st->dec_table;
+  dl.n_layers = st->d.n_layers;
+  dl.steps = steps;
+  dl.dim = st->d.dim;
+  dl.ffn = st->d.ffn;
+  dl.n_heads = st->d.n_heads;
+  dl.n_kv = st->d.n_kv_heads;
+  dl.eps = st->d.eps;
+  dl.h_in = h_in;
+  dl.h_out = h_out;
+  dl.xch = st->dec_xch;
+  dl.ctl = st->dec_ctl;
+  dl.trace = tr;
+  return cuda_err(launch_decoder(dl, cs));
+}
+
 void free_stack(bw_stack *st) {
   if (!st) return;
+  cudaFree(st->dec_table);
+  cudaFree(st->dec_xch);
+  cudaFree(st->dec_ctl);
   if (st->have_graph) cudaGraphExecDestroy(st->exec);
   cudaFree(st->h);
   cudaFree(st->attn);
@@ -781,6 +812,37 @@ bw_status stack_create(const bw_stack_desc *desc, int kv_S, float theta,
     free_stack(st);
     return cuda_err(e);
   }
+  if (kv_S == 0 &&
+      decoder_fits(d.dim, d.ffn, d.n_heads, d.n_kv_heads, d.n_layers)) {
+    // One persistent kernel per call: the pointer table, the exchange
+    // buffers (zeroed: epoch 0 is never used) and the control words.
+    st->persistent = true;
+    const unsigned int ctl0[4] = {1u, 0u, 0u, 0u};
+    alloc(&st->dec_table, decoder_table_bytes(d.n_layers));
+    alloc(&st->dec_xch, decoder_xch_bytes(d.dim, d.ffn));
+    alloc(reinterpret_cast<void **>(&st->dec_ctl), sizeof(ctl0));
+    if (e == cudaSuccess)
+      e = decoder_upload_table(st->dec_table, d.n_layers, st->wqkv.data(),
+                               st->wo.data(), st->w13.data(), st->w2.data(),
+                               st->ws.data(), st->gammas.data());
+    if (e == cudaSuccess)
+      e = cudaMemset(st->dec_xch, 0, decoder_xch_bytes(d.dim, d.ffn));
+    if (e == cudaSuccess)
+      e = cudaMemcpy(st->dec_ctl, ctl0, sizeof(ctl0), cudaMemcpyHostToDevice);
+    if (e != cudaSuccess) {
+      free_stack(st);
+      return cuda_err(e);
+    }
+    // One step on zero input performs every one-time set-up.
+    bw_status bs = run_decoder(st, st->h, 1, st->attn, nullptr, nullptr);
+    if (bs == BW_OK) bs = cuda_err(cudaDeviceSynchronize());
+    if (bs != BW_OK) {
+      free_stack(st);
+      return bs;
+    }
+    *out = st;
+    return BW_OK;
+  }
   // Capture one decode step as a graph on a private stream (after one eager
   // run on zero input, which also performs every one-time set-up).
   cudaStream_t cap = nullptr;
@@ -867,6 +929,7 @@ bw_status bw_layer_stack(bw_stack *st, const float *h_in, int steps,
   if (trace && (trace->layer < 0 || trace->layer >= st->d.n_layers))
     return BW_ERR_INVALID_ARG;
   cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+  if (st->persistent) return run_decoder(st, h_in, steps, h_out, trace, cs);
   const size_t row = size_t(st->d.dim) * 4;
   for (int t = 0; t < steps; ++t) {
     BW_TRY_CUDA(cudaMemcpyAsync(st->h, h_in + size_t(t) * st->d.dim, row,

@@ -225,14 +225,20 @@ size_t bw_gemv_workspace_bytes(int M, int N, int K);
  * i / (n_heads / n_kv_heads) (the softmax of a single score is 1); q and k
  * are computed but do not change the result.  RMSNorm:
  * v * (1/sqrt(mean(v^2) + eps)) * gamma, fp32.  The residual stream h is
- * fp32; GEMV outputs are bf16.  Execution: four kernel launches per layer,
- * one per GEMV.  Each launch's epilogue writes the values the next RMSNorm
- * reads with per-CTA partial statistics, and the next launch's prologue
- * finishes the norm and the int8 quantisation; the wo and w2 launches add
- * their outputs into h (so h += down happens at the end of each layer,
- * which is the same sum).  The fp32 sums run in a different order than a
- * sequential loop, so results match a reference within rounding, not bit
- * for bit.
+ * fp32; GEMV outputs are bf16.  The wo and w2 GEMVs add their outputs into
+ * h (so h += down happens at the end of each layer, which is the same sum).
+ * Execution of a stack without a KV cache (bw_stack_create): ONE persistent
+ * cooperative kernel per bw_layer_stack call runs every step, with one CTA
+ * per SM; each CTA streams its share of every GEMV's weights ahead of time
+ * and receives each GEMV's input from the other CTAs through exchange
+ * buffers polled with bounded waits (bw_device_error bit 32 if one runs
+ * out).  It needs n_layers <= 128 and the shapes to fit one CTA per SM
+ * (every BitNet-2B-sized shape does); a stack that does not fit, and a
+ * stack with a KV cache, run as one kernel launch per GEMV (and one per
+ * attention) instead, each step replayed from a CUDA graph.  In both, every
+ * CTA reduces the norm statistics in a fixed order, so every CTA gets the
+ * same codes.  The fp32 sums run in a different order than a sequential
+ * loop, so results match a reference within rounding, not bit for bit.
  * ---------------------------------------------------------------------- */
 typedef struct bw_stack bw_stack;
 
@@ -320,7 +326,9 @@ bw_status bw_stack_reset_kv(bw_stack *stack, bw_stream_t stream);
 /* Runs `steps` decode steps: h_out[t] = stack(h_in[t]) (fp32 [steps][dim],
  * device).  Steps are independent (no KV cache) for a stack made by
  * bw_stack_create; for one made by bw_stack_create_kv they are consecutive
- * tokens of one sequence.  Asynchronous on `stream`.
+ * tokens of one sequence.  Asynchronous on `stream`.  For a stack without a
+ * KV cache the call is one kernel launch, which may be captured in a CUDA
+ * graph and replayed (its exchange epochs live in device memory).
  * `trace` (may be NULL) records the stages of trace->layer in the last
  * step.  Calls on the same stack must not overlap (they share its scratch);
  * use one stack per concurrent stream. */
@@ -380,24 +388,28 @@ bw_status bw_attn_decode(const bw_bf16 *qkv, const int *pos, int H, int Hkv,
                          size_t workspace_bytes, bw_stream_t stream);
 
 /* bw_device_error -- reads and clears the library's device error word.
- * Kernels that wait on an mbarrier bound every wait (about one second); a
- * wait that runs out sets a bit here and the kernel stops early instead of
- * hanging (bit 2: a lane gave up waiting for the copies it issued before
- * leaving, bit 4: a warp gave up waiting for a weight piece; bit 8 is the
- * self-test's).  Bit 16: bw_attn_decode was given a position outside its
- * cache.
- * Returns BW_ERR_TIMEOUT if any time-out bit (2, 4, 8) was set, else
+ * Kernels that wait on an mbarrier or poll for another CTA's data bound
+ * every wait (about one second); a wait that runs out sets a bit here and
+ * the kernel stops early instead of hanging (bit 2: a lane gave up waiting
+ * for the copies it issued before leaving; bit 4: a warp gave up waiting
+ * for a weight piece; bit 32: a CTA of the persistent decoder stack gave
+ * up waiting for another CTA's output, or saw another CTA give up; bits 8
+ * and 64 are the self-test's).  Bit 16: bw_attn_decode was given a position
+ * outside its cache.
+ * Returns BW_ERR_TIMEOUT if any bit other than 16 was set, else
  * BW_ERR_INVALID_ARG if bit 16 was, else BW_OK; *bits receives the word.
  * SYNCHRONISES `stream`; not for the hot path. */
 bw_status bw_device_error(unsigned int *bits, bw_stream_t stream);
 
-/* bw_selftest_wait_timeout -- failure-detection self-test: launches a
- * one-thread kernel whose mbarrier wait cannot complete (it expects two
- * arrivals and receives one) with a limit of about 10 ms.  The wait runs
- * out, the kernel sets bit 8 of the device error word and returns; this
- * call then reads and clears the word like bw_device_error and returns
- * BW_ERR_TIMEOUT (with *bits = 8) -- the expected outcome.  The context
- * stays usable.  SYNCHRONISES `stream`. */
+/* bw_selftest_wait_timeout -- failure-detection self-test of both kinds of
+ * bounded wait.  It launches (1) a one-thread kernel whose mbarrier wait
+ * cannot complete (it expects two arrivals and receives one) and (2) a
+ * kernel that polls, with the persistent decoder's poll routine, exchange
+ * entries that nothing writes; each has a limit of about 10 ms.  Both waits
+ * run out; the kernels set bits 8 and 64 of the device error word and
+ * return; this call then reads and clears the word like bw_device_error and
+ * returns BW_ERR_TIMEOUT (with *bits = 8 | 64) -- the expected outcome.  The
+ * context stays usable.  SYNCHRONISES `stream`. */
 bw_status bw_selftest_wait_timeout(unsigned int *bits, bw_stream_t stream);
 
 #ifdef __cplusplus

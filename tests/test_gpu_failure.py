@@ -2,9 +2,11 @@
 
 Every mbarrier wait in the library's pipelines is bounded; when one runs out
 the kernel sets a bit in the device error word and returns instead of
-hanging, and the host reads BW_ERR_TIMEOUT.  The self-test kernel makes a
-wait run out on purpose (an arrival that never comes, ~10 ms limit); the
-context must stay usable afterwards.
+hanging, and the host reads BW_ERR_TIMEOUT.  The same holds for the
+persistent decoder's polls for another CTA's output.  The self-test makes
+one wait of each kind run out on purpose (an arrival that never comes, and
+exchange entries that nothing writes; ~10 ms limits); the context must stay
+usable afterwards.
 """
 import numpy as np
 import pytest
@@ -29,7 +31,7 @@ def bw():
 def test_bounded_wait_reports_timeout_and_context_survives(bw):
     assert bw.bw_device_error() == 0          # nothing pending
     status, bits = bw.bw_selftest_wait_timeout()
-    assert status == 6 and bits == 8          # BW_ERR_TIMEOUT, self-test bit
+    assert status == 6 and bits == 8 | 64     # BW_ERR_TIMEOUT, self-test bits
     assert bw.bw_device_error() == 0          # the word was cleared
     # the context still runs the real path correctly
     N, K = 64, 256

@@ -208,3 +208,26 @@ def test_tiny_stack_end_to_end_close_to_oracle(bw):
         rel = np.linalg.norm(out[t] - h) / np.linalg.norm(h)
         assert rel < 1e-2, rel
     stack.close()
+
+
+def test_call_replayed_from_a_graph_equals_eager(bw):
+    """A stack without a KV cache runs a call as one persistent kernel whose
+    exchange epochs live in device memory, so a captured call replays
+    correctly: two replays give the eager result bit for bit."""
+    dim, ffn, nh, nkv = 512, 1024, 8, 2
+    stack, _ = make_stack(bw, 3, dim, ffn, nh, nkv, 35)
+    h = to_dev(synth.step_inputs(13, 5, dim))
+    want = stack.run(h).clone()
+    out = torch.empty_like(h)
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        stack.run(h, out, stream=s)
+    for _ in range(2):
+        out.zero_()
+        g.replay()
+        torch.cuda.synchronize()
+        assert torch.equal(out, want)
+    assert bw.bw_device_error() == 0
+    stack.close()
