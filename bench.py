@@ -125,6 +125,11 @@ def parse_args():
                    help="--single: weight buffers (0: enough for 4x L2)")
     p.add_argument("--eager", action="store_true",
                    help="--single: launch eagerly instead of a CUDA graph")
+    p.add_argument("--lut", action="store_true",
+                   help="--single: time the pair-table (LUT) variant "
+                        "bw_gemv_w2a8_lut instead of the dp4a GEMV")
+    p.add_argument("--no-lut", action="store_true",
+                   help="skip the LUT-variant comparison")
     p.add_argument("--cold", action="store_true",
                    help="--single: isolated calls, L2 flushed before each "
                         "(median of --iters, at most 200), launch included")
@@ -161,6 +166,14 @@ def algorithmic_bytes(N, K, n_ws):
 
 def weight_bytes(N, K):
     return N * K // 4
+
+
+def read_all_peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return json.load(f)
+    except (OSError, ValueError):
+        return {}
 
 
 def read_peaks():
@@ -456,6 +469,9 @@ def run_ours(args):
     e2e_ms = job_time_ms(torch, e_start.elapsed_time(e_end), world, dev) / K_steps
     e2e_value = job_value(world, wbytes_step, e2e_ms)
 
+    lut_line = None
+    if rank == 0 and not args.no_lut:
+        lut_line = run_lut_comparison(torch, bw, dev)
     configs_line = None
     if rank == 0 and not args.no_configs:
         configs_line = run_config_shapes(torch, bw, dev, peak)
@@ -465,9 +481,10 @@ def run_ours(args):
         stack_line = run_stack_timing(torch, bw, dev)
         stack_kv_line = run_stack_timing(torch, bw, dev,
                                          kv_positions=ATTN_S)
-    batched_line = None
+    batched_line = prefill_line = None
     if rank == 0 and not args.no_batched:
         batched_line = run_batched(torch, bw, dev, peak)
+        prefill_line = run_prefill(torch, bw, dev, read_all_peaks())
     attn_line = None
     if rank == 0 and not args.no_attn:
         attn_line = run_attn_timing(torch, bw, dev, peak)
@@ -523,12 +540,16 @@ def run_ours(args):
         }
         if configs_line is not None:
             line["configs"] = configs_line
+        if lut_line is not None:
+            line["lut_variant"] = lut_line
         if stack_line is not None:
             line["layer_stack"] = stack_line
         if stack_kv_line is not None:
             line["layer_stack_kv"] = stack_kv_line
         if batched_line is not None:
             line["batched"] = batched_line
+        if prefill_line is not None:
+            line["prefill"] = prefill_line
         if attn_line is not None:
             line["attn_decode"] = attn_line
         if cpu is not None:
@@ -766,7 +787,8 @@ def run_reference(args):
     print(json.dumps(line), flush=True)
 
 
-def time_shape(torch, bw, dev, N, K, M, iters=2000, rotate=0, eager=False):
+def time_shape(torch, bw, dev, N, K, M, iters=2000, rotate=0, eager=False,
+               lut=False):
     """Microseconds per bw_gemv_w2a8 call of one shape, back to back on one
     stream (a CUDA graph of up to 64 calls unless `eager`), cycling through
     enough copies of the weights that they exceed L2 (weights, tokens and
@@ -784,11 +806,11 @@ def time_shape(torch, bw, dev, N, K, M, iters=2000, rotate=0, eager=False):
     y = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
     stream = torch.cuda.Stream(device=dev)
     per_graph = max(rot, min(iters, 64))
+    gemv = bw.bw_gemv_w2a8_lut if lut else bw.bw_gemv_w2a8
 
     def launches():
         for i in range(per_graph):
-            bw.bw_gemv_w2a8(q, packed[i % rot], s_, ws, [0, N], N, K, y=y,
-                            stream=stream)
+            gemv(q, packed[i % rot], s_, ws, [0, N], N, K, y=y, stream=stream)
 
     with torch.cuda.stream(stream):
         launches()
@@ -850,7 +872,47 @@ def run_config_shapes(torch, bw, dev, peak_gbs):
     return out
 
 
+# The pair-table (LUT) variant against the dp4a decode, same kernel template.
+LUT_CASES = ((1, 2560, 2560), (1, 13824, 2560), (4, 13824, 2560))
+
+
+def run_lut_comparison(torch, bw, dev):
+    """us per call of bw_gemv_w2a8_lut and bw_gemv_w2a8 at M = 1 and 4 (graph
+    of calls over rotating weight buffers), and their ratio."""
+    out = {"timing": "graph of calls back to back over rotating weight "
+                     "buffers (over 4x L2), CUDA events", "cases": {}}
+    for M, N, K in LUT_CASES:
+        d = time_shape(torch, bw, dev, N, K, M, iters=1024)
+        lt = time_shape(torch, bw, dev, N, K, M, iters=1024, lut=True)
+        out["cases"][f"M{M}_{N}x{K}"] = {
+            "dp4a_us": round(d["us"], 3), "lut_us": round(lt["us"], 3),
+            "lut_over_dp4a": round(lt["us"] / d["us"], 3)}
+    return out
+
+
 BATCHED_N, BATCHED_K, BATCHED_M = 13824, 2560, (4, 16, 64)
+PREFILL_M = (128, 512, 1024, 2048)
+
+
+def run_prefill(torch, bw, dev, peaks):
+    """Prompt-sized W2A8 GEMMs (the W2A8 page's §一 prefill) on the tcgen05
+    path at 13824 x 2560: us per call (graph of calls over rotating weight
+    buffers) and TFLOP/s (2 M N K per call) against the measured dense bf16
+    rate -- the path runs kind::f16 MMAs, whose nominal rate equals bf16's."""
+    out = {"shape": [BATCHED_N, BATCHED_K], "kernel": "tc_gemv_kernel "
+           "(tcgen05, 128-token tiles)", "per_m": {}}
+    for M in PREFILL_M:
+        t = time_shape(torch, bw, dev, BATCHED_N, BATCHED_K, M,
+                       iters=max(8, 8192 // M))
+        us = t["us"]
+        tflops = 2.0 * M * BATCHED_N * BATCHED_K / (us * 1e-6) / 1e12
+        out["per_m"][str(M)] = {
+            "us_per_call": round(us, 2), "tflops": round(tflops, 1),
+            "frac_of_measured_bf16_sustained":
+                round(tflops / peaks["bf16_tflops_sustained"], 4)
+                if peaks.get("bf16_tflops_sustained") else None,
+            "frac_of_nominal_dense_fp16": round(tflops / 2250.0, 4)}
+    return out
 
 
 def run_batched(torch, bw, dev, peak_gbs):
@@ -1006,9 +1068,10 @@ def run_single(args):
               flush=True)
         return
     t = time_shape(torch, bw, dev, N, K, M, iters=args.iters,
-                   rotate=args.rotate, eager=args.eager)
+                   rotate=args.rotate, eager=args.eager, lut=args.lut)
     us = t["us"]
     print(json.dumps({"single": [N, K, M], "rotate": t["rotate"],
+                      "kernel": "pair-table (LUT)" if args.lut else "dp4a",
                       "graph": not args.eager, "calls": t["calls"],
                       "us_per_call": round(us, 3),
                       "weight_GBps": round(t["weight_bytes"] / (us * 1e3), 1),

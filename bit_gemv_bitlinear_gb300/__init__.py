@@ -40,7 +40,8 @@ EXPORTS = ("bw_status_string", "bw_last_cuda_error", "bw_version",
            "bw_stack_destroy", "bw_selftest_wait_timeout",
            "bw_gemv_workspace_bytes", "bw_quant_weight",
            "bw_attn_workspace_bytes", "bw_attn_decode", "bw_stack_create_kv",
-           "bw_stack_read_kv", "bw_stack_reset_kv")
+           "bw_stack_read_kv", "bw_stack_reset_kv", "bw_gemv_w2a8_lut",
+           "bw_gemv_w2a8_lut_acc")
 
 _P = ctypes.c_void_p
 _I = ctypes.c_int
@@ -56,6 +57,8 @@ _SIGS = {
     "bw_repack_noalloc": (_I, [_P, _I, _I, _P, _P]),
     "bw_gemv_w2a8": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _P, _P]),
     "bw_gemv_w2a8_acc": (_I, [_P, _P, _I, _I, _I, _P, _P]),
+    "bw_gemv_w2a8_lut": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _P, _P]),
+    "bw_gemv_w2a8_lut_acc": (_I, [_P, _P, _I, _I, _I, _P, _P]),
     "bw_device_error": (_I, [_P, _P]),
     "bw_stack_create": (_I, [_P, _P]),
     "bw_layer_stack": (_I, [_P, _P, _I, _P, _P, _P]),
@@ -246,6 +249,48 @@ def bw_gemv_w2a8(x: torch.Tensor, packed: torch.Tensor, s: torch.Tensor,
         ctypes.cast(b, _P), len(ws_bounds) - 1, M, N, K,
         _dev(y, torch.bfloat16, "y"), _stream(stream)), "bw_gemv_w2a8")
     return y
+
+
+def bw_gemv_w2a8_lut(x: torch.Tensor, packed: torch.Tensor, s: torch.Tensor,
+                     ws: torch.Tensor, ws_bounds, N: int, K: int,
+                     y: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """bw_gemv_w2a8 computed with pre-summed pair tables (same result)."""
+    x2 = x if x.dim() == 2 else x.reshape(1, -1)
+    M = x2.shape[0]
+    if x2.shape[1] != K:
+        raise ValueError("x has the wrong K")
+    if y is None:
+        y = torch.empty((M, N), dtype=torch.bfloat16, device=x.device)
+    _need(packed, bw_repack_bytes(N, K), "packed")
+    _need(s, M, "s")
+    _need(ws, len(ws_bounds) - 1, "ws")
+    _need(y, M * N, "y")
+    b = _bounds_array(ws_bounds)
+    _check(_lib.bw_gemv_w2a8_lut(
+        _dev(x2, torch.int8, "x"), _dev(packed, torch.uint8, "packed"),
+        _dev(s, torch.float32, "s"), _dev(ws, torch.bfloat16, "ws"),
+        ctypes.cast(b, _P), len(ws_bounds) - 1, M, N, K,
+        _dev(y, torch.bfloat16, "y"), _stream(stream)), "bw_gemv_w2a8_lut")
+    return y
+
+
+def bw_gemv_w2a8_lut_acc(x: torch.Tensor, packed: torch.Tensor, N: int,
+                         K: int, acc: torch.Tensor | None = None,
+                         stream=None) -> torch.Tensor:
+    """Exact int32 acc [M][N] through the pair-table kernel."""
+    x2 = x if x.dim() == 2 else x.reshape(1, -1)
+    M = x2.shape[0]
+    if x2.shape[1] != K:
+        raise ValueError("x has the wrong K")
+    if acc is None:
+        acc = torch.empty((M, N), dtype=torch.int32, device=x.device)
+    _need(packed, bw_repack_bytes(N, K), "packed")
+    _need(acc, M * N, "acc")
+    _check(_lib.bw_gemv_w2a8_lut_acc(
+        _dev(x2, torch.int8, "x"), _dev(packed, torch.uint8, "packed"), M, N,
+        K, _dev(acc, torch.int32, "acc"), _stream(stream)),
+        "bw_gemv_w2a8_lut_acc")
+    return acc
 
 
 def bw_gemv_w2a8_acc(x: torch.Tensor, packed: torch.Tensor, N: int, K: int,

@@ -122,6 +122,60 @@ bw_status gemv_common(const int8_t *x, const uint8_t *packed, const float *s,
   return BW_OK;
 }
 
+// The pair-table variant: the same validation, then M-tiles of 4, 2 and 1
+// rows, all checked to fit before the first launch.
+bw_status gemv_lut_common(const int8_t *x, const uint8_t *packed,
+                          const float *s, const bw_bf16 *ws,
+                          const int *ws_bounds, int n_ws, int M, int N, int K,
+                          void *out, bool acc_out, cudaStream_t stream) {
+  if (!x || !packed || !out) return BW_ERR_INVALID_ARG;
+  bw_status st = check_mnk(M, N, K);
+  if (st != BW_OK) return st;
+  WsSegments seg{};
+  if (!acc_out) {
+    if (!s || !ws || !ws_bounds) return BW_ERR_INVALID_ARG;
+    if (n_ws < 1 || n_ws > BW_MAX_WS) return BW_ERR_INVALID_ARG;
+    if (ws_bounds[0] != 0 || ws_bounds[n_ws] != N) return BW_ERR_INVALID_ARG;
+    for (int i = 0; i < n_ws; ++i)
+      if (ws_bounds[i + 1] <= ws_bounds[i]) return BW_ERR_INVALID_ARG;
+    seg.n_ws = n_ws;
+    for (int i = 0; i <= n_ws; ++i) seg.bounds[i] = ws_bounds[i];
+    if (!aligned(s, 4) || !aligned(ws, 2) || !aligned(out, 2))
+      return BW_ERR_MISALIGNED;
+  } else if (!aligned(out, 4)) {
+    return BW_ERR_MISALIGNED;
+  }
+  if (!aligned(x, 4) || !aligned(packed, 16)) return BW_ERR_MISALIGNED;
+  if (device_sm_count() <= 0) return cuda_status(cudaErrorNoDevice);
+  for (int left = M; left > 0;) {
+    const int mt = left >= 4 ? 4 : (left >= 2 ? 2 : 1);
+    if (!lut_fits(mt, N, K)) return BW_ERR_UNSUPPORTED_SHAPE;
+    left -= mt;
+  }
+  GemvArgs a{};
+  a.w = packed;
+  a.ws = reinterpret_cast<const __nv_bfloat16 *>(ws);
+  a.K = K;
+  a.N = N;
+  a.x_ld = K;
+  a.out_ld = N;
+  a.chunks = chunks_per_row(K);
+  a.n_groups = int(padded_rows(N) / kGroupRows);
+  a.seg = seg;
+  const size_t out_elem = acc_out ? sizeof(int32_t) : sizeof(bw_bf16);
+  for (int m0 = 0; m0 < M;) {
+    const int left = M - m0;
+    const int mt = left >= 4 ? 4 : (left >= 2 ? 2 : 1);
+    a.x = x + size_t(m0) * K;
+    a.s = acc_out ? nullptr : s + m0;
+    a.out = static_cast<char *>(out) + size_t(m0) * N * out_elem;
+    cudaError_t e = launch_gemv_lut(a, mt, acc_out, stream);
+    if (e != cudaSuccess) return cuda_status(e);
+    m0 += mt;
+  }
+  return BW_OK;
+}
+
 }  // namespace
 
 int device_sm_count() {
@@ -274,6 +328,21 @@ bw_status bw_gemv_w2a8_acc(const int8_t *x, const uint8_t *packed, int M,
                            int N, int K, int32_t *acc, bw_stream_t stream) {
   return gemv_common(x, packed, nullptr, nullptr, nullptr, 0, M, N, K, acc,
                      true, reinterpret_cast<cudaStream_t>(stream));
+}
+
+bw_status bw_gemv_w2a8_lut(const int8_t *x, const uint8_t *packed,
+                           const float *s, const bw_bf16 *ws,
+                           const int *ws_bounds, int n_ws, int M, int N, int K,
+                           bw_bf16 *y, bw_stream_t stream) {
+  return gemv_lut_common(x, packed, s, ws, ws_bounds, n_ws, M, N, K, y, false,
+                         reinterpret_cast<cudaStream_t>(stream));
+}
+
+bw_status bw_gemv_w2a8_lut_acc(const int8_t *x, const uint8_t *packed, int M,
+                               int N, int K, int32_t *acc,
+                               bw_stream_t stream) {
+  return gemv_lut_common(x, packed, nullptr, nullptr, nullptr, 0, M, N, K,
+                         acc, true, reinterpret_cast<cudaStream_t>(stream));
 }
 
 }  // extern "C"

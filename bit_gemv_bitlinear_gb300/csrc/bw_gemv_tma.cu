@@ -159,60 +159,6 @@ struct StageInt8 {
   }
 };
 
-// Epilogue: y[m][n] = bf16((acc / s[m]) * ws[seg(n)]) (IEEE fp32, round to
-// nearest even), or the int32 accumulator itself.
-template <bool ACC>
-struct EpiOut {
-  void *out;  // bf16 or int32 [m][out_ld]
-  int out_ld;
-  const __nv_bfloat16 *ws;
-  WsSegments seg;
-
-  __device__ __forceinline__ float scale_value() const {
-    return (!ACC && int(threadIdx.x) < seg.n_ws)
-               ? __bfloat162float(ws[threadIdx.x])
-               : 0.0f;
-  }
-  __device__ __forceinline__ void store(int n, int m, int total,
-                                        const float *s_sm,
-                                        const float *ws_sm) const {
-    if (ACC) {
-      static_cast<int *>(out)[size_t(m) * out_ld + n] = total;
-    } else {
-      int sg = 0;
-#pragma unroll
-      for (int i = 1; i < BW_MAX_WS; ++i)
-        if (i < seg.n_ws && n >= seg.bounds[i]) sg = i;
-      const float scaled = static_cast<float>(total) / s_sm[m];
-      const float v = scaled * ws_sm[sg];
-      static_cast<__nv_bfloat16 *>(out)[size_t(m) * out_ld + n] =
-          __float2bfloat16_rn(v);
-    }
-  }
-  __device__ __forceinline__ float4 prefetch(const PipeArgs &, int,
-                                             int) const {
-    return make_float4(0.0f, 0.0f, 0.0f, 0.0f);
-  }
-  template <int MT>
-  __device__ __forceinline__ void finish(const PipeArgs &a, const int *tot,
-                                         const int (&sx)[MT], int g_lo,
-                                         int n_g, const float *s_sm,
-                                         const float *ws_sm, float *red,
-                                         float4 pre) const {
-    (void)red;
-    (void)pre;
-    for (int t = threadIdx.x; t < n_g * 8; t += blockDim.x) {
-      const int gl = t >> 3, rr = t & 7;
-      const int n = (g_lo + gl) * kGroupRows + rr;  // no row pairing here
-      if (n < a.N) {
-#pragma unroll
-        for (int m = 0; m < MT; ++m)
-          store(n, m, tot[(gl * MT + m) * 8 + rr] - sx[m], s_sm, ws_sm);
-      }
-    }
-  }
-};
-
 template <int MT, bool ACC>
 cudaError_t launch_instance(const GemvArgs &g, cudaStream_t stream) {
   PipeArgs a{};

@@ -83,6 +83,12 @@ bool tc_fits(const GemvArgs &args);
 cudaError_t launch_gemv_tc(const GemvArgs &args, int rows, bool acc_out,
                            cudaStream_t stream);
 
+// Pair-table (LUT) GEMV (bw_gemv_lut.cu) for M-tiles of mt = 1, 2 or 4
+// rows; lut_fits() is false where the tables do not fit in shared memory.
+bool lut_fits(int mt, int N, int K);
+cudaError_t launch_gemv_lut(const GemvArgs &args, int mt, bool acc_out,
+                            cudaStream_t stream);
+
 GemvPlan plan_gemv(int mt, int N, int K, int num_sms);
 cudaError_t launch_gemv(const GemvPlan &plan, const GemvArgs &args,
                         bool acc_out, cudaStream_t stream);

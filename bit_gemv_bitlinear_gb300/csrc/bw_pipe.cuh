@@ -180,6 +180,25 @@ __device__ __forceinline__ int fold_row(const int (&a)[4]) {
   return v;
 }
 
+// The default dot-product policy of the pipe kernel: unsigned codes masked
+// in place and fed to dp4a against the int8 activations staged in shared
+// memory (xs_chunk_bytes: shared-memory bytes per chunk of K and activation
+// row; run: the products of a run of chunks; fold: a lane's partial sums to
+// its share of the row value, summed over the row's 4 chunk lanes).
+struct DotDp4a {
+  static constexpr uint32_t kXsChunkBytes = 64;  // per activation row
+  template <int MT>
+  __device__ __forceinline__ static void run(const uint8_t *wbase,
+                                             const int8_t *xs, uint32_t xrow,
+                                             int c0, int chunks, int q, int r,
+                                             int (&acc)[MT][4]) {
+    dot_row_group<MT>(wbase, xs, xrow, c0, chunks, q, r, acc);
+  }
+  __device__ __forceinline__ static int fold(const int (&a)[4]) {
+    return fold_row(a);
+  }
+};
+
 // ---------------------------------------------------------------------------
 // Balanced per-warp pipelines (pipe mode).
 //
@@ -204,13 +223,13 @@ struct PipeLayout {
 // sums: [MT] activation scales s, [BW_MAX_WS] weight scales (as fp32),
 // [warps][MT] per-warp activation sums; red: 64 floats of prologue
 // reduction scratch; tot: [k][MT][8] row totals; bars: the ring barriers.
-__host__ __device__ inline PipeLayout pipe_layout(int mt, int chunks,
-                                                  int slot_chunks, int slots,
-                                                  int warps, int k) {
+__host__ __device__ inline PipeLayout pipe_layout(
+    int mt, int chunks, int slot_chunks, int slots, int warps, int k,
+    uint32_t xs_chunk_bytes = DotDp4a::kXsChunkBytes) {
   PipeLayout l;
   l.ring = 0;
   l.xs = uint32_t(warps * slots * slot_chunks) * kGroupChunkBytes;
-  l.sums = l.xs + uint32_t(mt) * xs_row_bytes(chunks);
+  l.sums = l.xs + uint32_t(mt) * uint32_t(chunks) * xs_chunk_bytes;
   const uint32_t sums_bytes = uint32_t((mt + BW_MAX_WS + warps * mt) * 4);
   l.red = (l.sums + sums_bytes + 15) / 16 * 16;
   l.tot = l.red + 64 * 4;
@@ -330,7 +349,7 @@ __device__ __forceinline__ float cta_max(float v, float *red) {
   return t;
 }
 
-template <int MT, class Pro, class Epi>
+template <int MT, class Pro, class Epi, class Dot = DotDp4a>
 __global__ void __launch_bounds__(kPipeWarps * 32)
 pipe_gemv_kernel(const PipeArgs a, const Pro pro, const Epi epi) {
   extern __shared__ __align__(128) uint8_t smem[];
@@ -342,7 +361,8 @@ pipe_gemv_kernel(const PipeArgs a, const Pro pro, const Epi epi) {
   const int k = a.groups_per_cta;
   const uint32_t slot_bytes = uint32_t(KS) * kGroupChunkBytes;
   const uint32_t xrow = xs_row_bytes(C);
-  const PipeLayout L = pipe_layout(MT, C, KS, R, kPipeWarps, k);
+  const PipeLayout L =
+      pipe_layout(MT, C, KS, R, kPipeWarps, k, Dot::kXsChunkBytes);
   uint8_t *ring = smem + L.ring + size_t(warp) * R * slot_bytes;
   int8_t *xs = reinterpret_cast<int8_t *>(smem + L.xs);
   float *s_sm = reinterpret_cast<float *>(smem + L.sums);
@@ -424,8 +444,8 @@ pipe_gemv_kernel(const PipeArgs a, const Pro pro, const Epi epi) {
       break;
     }
     const int len = cur.piece(KS, C, run_hi);
-    dot_row_group<MT>(ring + size_t(slot) * slot_bytes, xs, xrow, cur.c, len,
-                      q, r, acc);
+    Dot::template run<MT>(ring + size_t(slot) * slot_bytes, xs, xrow, cur.c,
+                          len, q, r, acc);
     __syncwarp();
     if (lane == 0 && iss.u < run_hi) {  // piece consumed + R: this slot
       fence_proxy_async_smem();
@@ -437,7 +457,7 @@ pipe_gemv_kernel(const PipeArgs a, const Pro pro, const Epi epi) {
     if (cur.c == 0 || cur.u == run_hi) {  // row group or run finished
 #pragma unroll
       for (int m = 0; m < MT; ++m) {
-        const int v = fold_row(acc[m]);
+        const int v = Dot::fold(acc[m]);
         if (q == 0) atomicAdd(&tot[(g * MT + m) * 8 + r], v);
 #pragma unroll
         for (int t = 0; t < 4; ++t) acc[m][t] = 0;
@@ -465,6 +485,60 @@ pipe_gemv_kernel(const PipeArgs a, const Pro pro, const Epi epi) {
   }
   epi.template finish<MT>(a, tot, sx, g_lo, n_g, s_sm, ws_sm, red, pre);
 }
+
+// Epilogue: y[m][n] = bf16((acc / s[m]) * ws[seg(n)]) (IEEE fp32, round to
+// nearest even), or the int32 accumulator itself.
+template <bool ACC>
+struct EpiOut {
+  void *out;  // bf16 or int32 [m][out_ld]
+  int out_ld;
+  const __nv_bfloat16 *ws;
+  WsSegments seg;
+
+  __device__ __forceinline__ float scale_value() const {
+    return (!ACC && int(threadIdx.x) < seg.n_ws)
+               ? __bfloat162float(ws[threadIdx.x])
+               : 0.0f;
+  }
+  __device__ __forceinline__ void store(int n, int m, int total,
+                                        const float *s_sm,
+                                        const float *ws_sm) const {
+    if (ACC) {
+      static_cast<int *>(out)[size_t(m) * out_ld + n] = total;
+    } else {
+      int sg = 0;
+#pragma unroll
+      for (int i = 1; i < BW_MAX_WS; ++i)
+        if (i < seg.n_ws && n >= seg.bounds[i]) sg = i;
+      const float scaled = static_cast<float>(total) / s_sm[m];
+      const float v = scaled * ws_sm[sg];
+      static_cast<__nv_bfloat16 *>(out)[size_t(m) * out_ld + n] =
+          __float2bfloat16_rn(v);
+    }
+  }
+  __device__ __forceinline__ float4 prefetch(const PipeArgs &, int,
+                                             int) const {
+    return make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+  }
+  template <int MT>
+  __device__ __forceinline__ void finish(const PipeArgs &a, const int *tot,
+                                         const int (&sx)[MT], int g_lo,
+                                         int n_g, const float *s_sm,
+                                         const float *ws_sm, float *red,
+                                         float4 pre) const {
+    (void)red;
+    (void)pre;
+    for (int t = threadIdx.x; t < n_g * 8; t += blockDim.x) {
+      const int gl = t >> 3, rr = t & 7;
+      const int n = (g_lo + gl) * kGroupRows + rr;  // no row pairing here
+      if (n < a.N) {
+#pragma unroll
+        for (int m = 0; m < MT; ++m)
+          store(n, m, tot[(gl * MT + m) * 8 + rr] - sx[m], s_sm, ws_sm);
+      }
+    }
+  }
+};
 
 // Sets the opt-in shared-memory size once per device and returns how many
 // CTAs of `kernel` are resident on the device at once (at least one).
@@ -501,8 +575,11 @@ constexpr int kPipeDefaultSlots = 2;
 // Shared memory of a launch with k groups per CTA; a launch fits while this
 // is at most 227 KB for k = kPipeMaxGroupsPerCta.
 inline uint32_t pipe_smem_bytes(int mt, int chunks, int slot_chunks,
-                                int slots, int k) {
-  return pipe_layout(mt, chunks, slot_chunks, slots, kPipeWarps, k).total;
+                                int slots, int k,
+                                uint32_t xs_chunk_bytes = DotDp4a::kXsChunkBytes) {
+  return pipe_layout(mt, chunks, slot_chunks, slots, kPipeWarps, k,
+                     xs_chunk_bytes)
+      .total;
 }
 
 // Launches the pipe kernel with programmatic dependent launch: k groups per
@@ -511,11 +588,11 @@ inline uint32_t pipe_smem_bytes(int mt, int chunks, int slot_chunks,
 // runs in waves; even with pair_half), and pieces no longer than a warp's
 // run.  Fills in the split fields of `a`; *grid_out (if set) receives the
 // number of CTAs.
-template <int MT, class Pro, class Epi>
+template <int MT, class Pro, class Epi, class Dot = DotDp4a>
 cudaError_t launch_pipe(PipeArgs a, const Pro &pro, const Epi &epi,
                         cudaStream_t stream, int *grid_out = nullptr) {
   static bool configured[64];
-  auto kernel = pipe_gemv_kernel<MT, Pro, Epi>;
+  auto kernel = pipe_gemv_kernel<MT, Pro, Epi, Dot>;
   a.slot_chunks = kPipeSlotChunks;
   if (a.slots < 1) a.slots = kPipeDefaultSlots;
   // k from the residency at k = 1, then once more at that k (the row
@@ -524,7 +601,8 @@ cudaError_t launch_pipe(PipeArgs a, const Pro &pro, const Epi &epi,
   for (int pass = 0; pass < 2; ++pass) {
     cudaError_t e = resident_ctas(
         kernel, configured, kPipeWarps * 32,
-        pipe_smem_bytes(MT, a.chunks, a.slot_chunks, a.slots, int(k)),
+        pipe_smem_bytes(MT, a.chunks, a.slot_chunks, a.slots, int(k),
+                        Dot::kXsChunkBytes),
         &resident);
     if (e != cudaSuccess) return e;
     k = (a.n_groups + resident - 1) / resident;
@@ -540,8 +618,8 @@ cudaError_t launch_pipe(PipeArgs a, const Pro &pro, const Epi &epi,
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(unsigned(grid > 0 ? grid : 1));
   cfg.blockDim = dim3(kPipeWarps * 32);
-  cfg.dynamicSmemBytes =
-      pipe_smem_bytes(MT, a.chunks, a.slot_chunks, a.slots, int(k));
+  cfg.dynamicSmemBytes = pipe_smem_bytes(MT, a.chunks, a.slot_chunks,
+                                         a.slots, int(k), Dot::kXsChunkBytes);
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;

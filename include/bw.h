@@ -201,6 +201,29 @@ bw_status bw_gemv_w2a8(const int8_t *x, const uint8_t *packed, const float *s,
 bw_status bw_gemv_w2a8_acc(const int8_t *x, const uint8_t *packed, int M,
                            int N, int K, int32_t *acc, bw_stream_t stream);
 
+/* bw_gemv_w2a8_lut, bw_gemv_w2a8_lut_acc -- the same products as
+ * bw_gemv_w2a8 and bw_gemv_w2a8_acc (identical int32 accumulators, identical
+ * bf16 outputs), computed with pre-summed activation tables instead of the
+ * dp4a decode: the GPU restatement of the table-lookup kernels of "BitNet на
+ * микроконтроллерах: как устроен запуск 1.58-битной LLM на кластере
+ * ESP32-S3" (sections "LUT-компиляция" and "Ядро qgemm_lut").  For every pair
+ * of activations whose weights share a 4-bit nibble of the device layout,
+ * the kernel first builds the 16 sums (c0 - 1) x0 + (c1 - 1) x1 over the
+ * codes, then adds one table entry per nibble.  Same arguments, layouts,
+ * ordering and limits as bw_gemv_w2a8, except that the tables of one
+ * activation row take K bytes x 16 of shared memory: rows are taken in tiles
+ * of 4, 2 and 1, and a tile whose tables do not fit (K above about 10000 at
+ * one row, about 2600 at four) returns BW_ERR_UNSUPPORTED_SHAPE before any
+ * launch.  Provided to compare the table method with the dp4a decode; the
+ * dp4a path is faster on this GPU at every measured M. */
+bw_status bw_gemv_w2a8_lut(const int8_t *x, const uint8_t *packed,
+                           const float *s, const bw_bf16 *ws,
+                           const int *ws_bounds, int n_ws, int M, int N, int K,
+                           bw_bf16 *y, bw_stream_t stream);
+bw_status bw_gemv_w2a8_lut_acc(const int8_t *x, const uint8_t *packed, int M,
+                               int N, int K, int32_t *acc,
+                               bw_stream_t stream);
+
 /* bw_gemv_workspace_bytes -- device scratch a bw_gemv_w2a8 call of this
  * shape needs from the caller: always 0.  Every kernel reduces its partial
  * sums in shared memory (int32 atomics per CTA) and no CTA shares a row with

@@ -79,8 +79,8 @@ def test_gemv_needs_no_workspace(lib):
 P = ctypes.c_void_p
 
 
-def gemv(lib, x, w, s, ws, bounds, n_ws, M, N, K, y):
-    f = lib.bw_gemv_w2a8
+def gemv(lib, x, w, s, ws, bounds, n_ws, M, N, K, y, fn="bw_gemv_w2a8"):
+    f = getattr(lib, fn)
     f.restype = ctypes.c_int
     f.argtypes = [P, P, P, P, P, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                   ctypes.c_int, P, P]
@@ -93,7 +93,8 @@ def gemv(lib, x, w, s, ws, bounds, n_ws, M, N, K, y):
 A16, A4, A2 = 0x10000, 0x20000, 0x30000
 
 
-def test_gemv_host_validation(lib):
+@pytest.mark.parametrize("fn", ["bw_gemv_w2a8", "bw_gemv_w2a8_lut"])
+def test_gemv_host_validation(lib, fn):
     good = dict(x=A16, w=A16, s=A4, ws=A2, bounds=[0, 64], n_ws=1, M=1,
                 N=64, K=256, y=A2)
 
@@ -101,7 +102,7 @@ def test_gemv_host_validation(lib):
         a = dict(good)
         a.update(kw)
         return gemv(lib, a["x"], a["w"], a["s"], a["ws"], a["bounds"],
-                    a["n_ws"], a["M"], a["N"], a["K"], a["y"])
+                    a["n_ws"], a["M"], a["N"], a["K"], a["y"], fn)
 
     assert call(x=None) == INVALID
     assert call(w=None) == INVALID
@@ -146,6 +147,11 @@ def test_other_entry_points_host_validation(lib):
     ga.argtypes = [P, P, ctypes.c_int, ctypes.c_int, ctypes.c_int, P, P]
     assert ga(A16, A16, 1, 64, 256, A4 + 2, None) == MISALIGNED
     assert ga(A16, A16, 1, 64, 6, A4, None) == SHAPE
+    la = lib.bw_gemv_w2a8_lut_acc
+    la.argtypes = [P, P, ctypes.c_int, ctypes.c_int, ctypes.c_int, P, P]
+    assert la(A16, A16, 1, 64, 256, A4 + 2, None) == MISALIGNED
+    assert la(A16, A16, 1, 64, 6, A4, None) == SHAPE
+    assert la(None, A16, 1, 64, 256, A4, None) == INVALID
 
 
 def test_product_path_never_touches_the_oracle():

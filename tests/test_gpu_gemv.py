@@ -301,3 +301,56 @@ def test_prefill_sizes(bw, M):
         np.arange(0, 16), np.arange(6904, 6920), np.arange(N - 16, N),
         (synth.u64(13, M, 160) % np.uint64(N)).astype(np.int64)]))
     run_case(bw, case, rows=rows)
+
+
+# ------------------------------------------------- pair-table (LUT) variant
+@pytest.mark.parametrize("M,N,K", [
+    (1, 2560, 2560), (1, 3840, 2560), (1, 2560, 6912), (1, 13824, 2560),
+    (2, 1000, 300), (3, 77, 1028), (4, 13824, 2560), (5, 129, 68),
+    (4, 8, 64), (1, 5, 4)])
+def test_lut_variant_parity(bw, M, N, K):
+    """bw_gemv_w2a8_lut (the TL pages' lut_ctor / qgemm_lut restated): int32
+    exact against the oracle and bit-identical to the dp4a path, bf16
+    within one ulp; ragged N and K, 1 to 5 rows (tiles of 4, 2 and 1)."""
+    bounds = [0, N] if N < 3 else [0, N // 3 + 1, N]
+    case = synth.gemv_case(M, N, K, synth.base_seed(14, M * 7 + K % 5),
+                           uniform_x=False, bounds=bounds)
+    q, s_ref = oracle.quant_act(case["xf"])
+    case["q"] = q
+    q[0, ::5] = -128                          # extremes of the int8 range
+    q[M - 1, 1::7] = 127
+    canon = case["canon"]
+    packed = bw.bw_repack(to_dev(canon), N, K)
+    x_d = to_dev(q)
+    acc = bw.bw_gemv_w2a8_lut_acc(x_d, packed, N, K)
+    acc_dp4a = bw.bw_gemv_w2a8_acc(x_d, packed, N, K)
+    s_d = to_dev(s_ref)
+    ws_d = bf16_dev(case["ws"])
+    y = bw.bw_gemv_w2a8_lut(x_d, packed, s_d, ws_d, case["bounds"].tolist(),
+                            N, K)
+    y_dp4a = bw.bw_gemv_w2a8(x_d, packed, s_d, ws_d, case["bounds"].tolist(),
+                             N, K)
+    torch.cuda.synchronize()
+    assert bw.bw_device_error() == 0
+    sel = np.arange(N) if N <= 4000 else np.unique(np.concatenate([
+        np.arange(0, 64), np.arange(N - 64, N),
+        (synth.u64(14, N, 400) % np.uint64(N)).astype(np.int64)]))
+    acc_ref = oracle.gemv_acc(q, np.ascontiguousarray(canon[sel]), len(sel), K)
+    assert (acc.cpu().numpy()[:, sel] == acc_ref).all()
+    assert torch.equal(acc, acc_dp4a)
+    assert torch.equal(y.view(torch.int16), y_dp4a.view(torch.int16))
+    if N <= 4000:
+        y_ref = oracle.gemv(q, canon, s_ref, case["ws"], case["bounds"], N, K)
+        assert_bf16_within_ulp(bits_of(y), y_ref)
+
+
+def test_lut_variant_rejects_tables_that_do_not_fit(bw):
+    """Four rows at K = 6912 need 4 x 6912 x 16 bytes of tables: rejected
+    before any launch."""
+    N, K = 64, 6912
+    x = torch.zeros((4, K), dtype=torch.int8, device=DEV)
+    packed = torch.zeros((bw.bw_repack_bytes(N, K),), dtype=torch.uint8,
+                         device=DEV)
+    with pytest.raises(bw.BwError) as e:
+        bw.bw_gemv_w2a8_lut_acc(x, packed, N, K)
+    assert e.value.status == 2
