@@ -962,7 +962,9 @@ def run_attn_timing(torch, bw, dev, peak_gbs, contexts=ATTN_CONTEXTS,
                      dtype=torch.uint8, device=dev)
     out = torch.empty((H, D), dtype=torch.float32, device=dev)
     res = {"heads": H, "kv_heads": Hkv, "head_dim": D, "cache_positions": S,
-           "theta": ATTN_THETA, "kernel": "attn_decode_kernel",
+           "theta": ATTN_THETA,
+           "kernel": "attn_cluster_kernel (one cluster of up to 16 CTAs per "
+                     "KV head, merge in distributed shared memory)",
            "timing": "graph of calls back to back, one cache per call, "
                      "the caches' read rows over 4x L2",
            "contexts": {}}

@@ -10,7 +10,12 @@
 //
 // Design for sm_103a.  The step reads 2 Hkv (p + 1) D bf16 values of cache
 // and little else, so it is bound by HBM at long contexts and by latency
-// at short ones:
+// at short ones.  Two kernels share the per-split work (attend_split):
+//  * Caches of at most 4096 positions: one thread-block cluster of up to 16
+//    CTAs per KV head (attn_cluster_kernel, described at its definition):
+//    the splits merge through distributed shared memory.
+//  * Longer caches: the kernel below, whose splits merge through the
+//    caller's workspace:
 //  * CTA (c, g) takes split c of the positions 0..p for KV head g and all
 //    G = H / Hkv query heads that read it, so every K and V row is loaded
 //    once for the G heads.  The number of splits is fixed at launch: one
@@ -107,15 +112,15 @@ struct AttnPart {
 // Shared memory (bytes): staged key and value rows, pair cos/sin, rotated
 // queries, scores (the merge reuses the key rows for its weights),
 // per-warp outputs, reduction scratch.
-template <int G>
+template <int G, int kChunk = kAttnChunk>
 struct AttnSmem {
   static constexpr uint32_t kRowBytes = kAttnD * 2;
   static constexpr uint32_t kK = 0;
-  static constexpr uint32_t kV = kK + kAttnChunk * kRowBytes;
-  static constexpr uint32_t kCs = kV + kAttnChunk * kRowBytes;  // float2[64]
+  static constexpr uint32_t kV = kK + kChunk * kRowBytes;
+  static constexpr uint32_t kCs = kV + kChunk * kRowBytes;      // float2[64]
   static constexpr uint32_t kQ = kCs + kAttnPairs * 8;          // [G][D]
   static constexpr uint32_t kSc = kQ + G * kAttnD * 4;          // [chunk][G]
-  static constexpr uint32_t kWacc = kSc + kAttnChunk * G * 4;   // [warps][G][D]
+  static constexpr uint32_t kWacc = kSc + kChunk * G * 4;       // [warps][G][D]
   static constexpr uint32_t kRed = kWacc + kAttnWarps * G * kAttnD * 4;
   static constexpr size_t kBytes = kRed + kAttnWarps * (G < 2 ? 2 : G) * 4 + 16;
 };
@@ -185,6 +190,201 @@ __device__ __forceinline__ void cta_sum_max(float &ss, float &mx, float *red) {
   }
 }
 
+// The partial of one split, positions j0 .. j0 + n - 1 of KV head g (n >= 1,
+// n <= kChunk): the two bulk copies of its key and value rows, the rotated
+// queries, the append of the new token when the split holds p, the scores,
+// the split's softmax (largest score m and exp sum l per query head, the
+// same in every thread) and the unnormalised output per warp in the wacc
+// rows of the layout (summed over warps by the caller after the final
+// barrier here).  bar: the split's two mbarriers.  Returns false if the
+// key copy did not land (the CTA then has no partial).
+template <int G, int kChunk>
+__device__ __forceinline__ bool attend_split(const AttnArgs &a, int g, int p,
+                                             int j0, int n, uint8_t *smem,
+                                             uint64_t *bar, float (&m)[G],
+                                             float (&l)[G]) {
+  using L = AttnSmem<G, kChunk>;
+  __nv_bfloat16 *kst = reinterpret_cast<__nv_bfloat16 *>(smem + L::kK);
+  __nv_bfloat16 *vst = reinterpret_cast<__nv_bfloat16 *>(smem + L::kV);
+  float2 *cs = reinterpret_cast<float2 *>(smem + L::kCs);
+  float *q_sm = reinterpret_cast<float *>(smem + L::kQ);
+  float *sc = reinterpret_cast<float *>(smem + L::kSc);
+  float *wacc = reinterpret_cast<float *>(smem + L::kWacc);
+  float *red = reinterpret_cast<float *>(smem + L::kRed);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int hl = lane & 15, half = lane >> 4;
+  constexpr int D = kAttnD;
+  const size_t head_row = size_t(g) * a.S;  // row 0 of KV head g
+    // ---- the split's key rows and value rows: one bulk copy each ----
+  if (tid == 0) {
+    pipe::mbar_init(&bar[0], 1);
+    pipe::mbar_init(&bar[1], 1);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    const uint32_t bytes = uint32_t(n) * L::kRowBytes;
+    pipe::mbar_arrive_expect_tx(&bar[0], bytes);
+    pipe::bulk_copy_g2s(kst, a.kc + (head_row + j0) * D, bytes, &bar[0]);
+    pipe::mbar_arrive_expect_tx(&bar[1], bytes);
+    pipe::bulk_copy_g2s(vst, a.vc + (head_row + j0) * D, bytes, &bar[1]);
+  }
+  // ---- RoPE of the queries meanwhile ----
+  if (tid < kAttnPairs) {
+    float sn, cn;
+    sincosf(__fmul_rn(float(p), a.freq[tid]), &sn, &cn);
+    cs[tid] = make_float2(cn, sn);
+  }
+  __syncthreads();  // cos/sin ready; the barriers are initialised
+  for (int e = tid; e < G * kAttnPairs; e += kAttnThreads) {
+    const int h = e / kAttnPairs, i = e - h * kAttnPairs;
+    const __nv_bfloat16 *qh = a.qkv + size_t(g * G + h) * D;
+    const float x0 = __bfloat162float(qh[2 * i]);
+    const float x1 = __bfloat162float(qh[2 * i + 1]);
+    const float2 r = cs[i];
+    q_sm[h * D + 2 * i] = x0 * r.x - x1 * r.y;
+    q_sm[h * D + 2 * i + 1] = x0 * r.y + x1 * r.x;
+  }
+  const bool has_p = j0 <= p && p < j0 + n;
+  if (!__syncthreads_and(pipe::mbar_wait(&bar[0], 0u))) {
+    // Never expected: report, let the copies land (bounded) before the
+    // CTA may leave, and contribute no partial.
+    if (tid == 0) {
+      atomicOr(a.err, 4u);
+      if (!pipe::mbar_wait(&bar[0], 0u) || !pipe::mbar_wait(&bar[1], 0u))
+        atomicOr(a.err, 2u);
+    }
+    __syncthreads();
+    return false;
+  }
+  {
+    // ---- the new token's rotated key: staged and appended (the key
+    // copy has landed, so neither write can be overwritten or read by it)
+    if (has_p && tid < kAttnPairs) {
+      const int i = tid;
+      const __nv_bfloat16 *kh = a.qkv + size_t(a.H + g) * D;
+      const float x0 = __bfloat162float(kh[2 * i]);
+      const float x1 = __bfloat162float(kh[2 * i + 1]);
+      const float2 r = cs[i];
+      const __nv_bfloat162 k2 = __halves2bfloat162(
+          __float2bfloat16_rn(x0 * r.x - x1 * r.y),
+          __float2bfloat16_rn(x0 * r.y + x1 * r.x));
+      reinterpret_cast<__nv_bfloat162 *>(kst + size_t(p - j0) * D)[i] = k2;
+      reinterpret_cast<__nv_bfloat162 *>(a.kc + (head_row + p) * D)[i] = k2;
+    }
+    __syncthreads();
+
+    // ---- scores: a half-warp per position, 8 dims per lane ----
+    float qr[G][8];
+#pragma unroll
+    for (int h = 0; h < G; ++h)
+#pragma unroll
+      for (int e = 0; e < 8; ++e) qr[h][e] = q_sm[h * D + 8 * hl + e];
+    // Two positions per half-warp and step: their shuffle chains overlap.
+    for (int jb = 4 * warp; jb < n; jb += 4 * kAttnWarps) {  // warp-uniform
+      float d[2][G];
+#pragma unroll
+      for (int r = 0; r < 2; ++r) {
+        const int jj = jb + 2 * r + half;
+        float kv[8];
+        bf16x8_to_f32(jj < n ? *reinterpret_cast<const uint4 *>(
+                                   kst + size_t(jj) * D + 8 * hl)
+                             : make_uint4(0u, 0u, 0u, 0u),
+                      kv);
+#pragma unroll
+        for (int h = 0; h < G; ++h) {
+          float t = 0.0f;
+#pragma unroll
+          for (int e = 0; e < 8; ++e) t = fmaf(qr[h][e], kv[e], t);
+          d[r][h] = t;
+        }
+      }
+#pragma unroll
+      for (int o = 8; o > 0; o >>= 1)
+#pragma unroll
+        for (int r = 0; r < 2; ++r)
+#pragma unroll
+          for (int h = 0; h < G; ++h)
+            d[r][h] += __shfl_xor_sync(0xffffffffu, d[r][h], o);  // in half
+      if (hl == 0)
+#pragma unroll
+        for (int r = 0; r < 2; ++r) {
+          const int jj = jb + 2 * r + half;
+          if (jj < n)
+#pragma unroll
+            for (int h = 0; h < G; ++h)
+              sc[jj * G + h] = d[r][h] * a.inv_sqrt_d;
+        }
+    }
+    __syncthreads();
+
+    // ---- softmax of the split: largest score, then exp and sum ----
+#pragma unroll
+    for (int h = 0; h < G; ++h) m[h] = -INFINITY;
+    for (int jj = tid; jj < n; jj += kAttnThreads)
+#pragma unroll
+      for (int h = 0; h < G; ++h) m[h] = fmaxf(m[h], sc[jj * G + h]);
+    cta_reduce<G, true>(m, red);
+#pragma unroll
+    for (int h = 0; h < G; ++h) l[h] = 0.0f;
+    for (int jj = tid; jj < n; jj += kAttnThreads)
+#pragma unroll
+      for (int h = 0; h < G; ++h) {
+        const float e = expf(sc[jj * G + h] - m[h]);
+        sc[jj * G + h] = e;
+        l[h] += e;
+      }
+    cta_reduce<G, false>(l, red);  // its barriers also publish sc
+
+    // ---- weighted values (the value copy landed during the scores) ----
+    if (!__syncthreads_and(pipe::mbar_wait(&bar[1], 0u))) {
+      if (tid == 0) {
+        atomicOr(a.err, 4u);
+        if (!pipe::mbar_wait(&bar[1], 0u)) atomicOr(a.err, 2u);
+      }
+      __syncthreads();
+    }
+    if (has_p && tid < kAttnPairs) {  // the new token's value
+      const int i = tid;
+      const __nv_bfloat16 *vh = a.qkv + size_t(a.H + a.Hkv + g) * D;
+      const __nv_bfloat162 v2 = __halves2bfloat162(vh[2 * i], vh[2 * i + 1]);
+      reinterpret_cast<__nv_bfloat162 *>(vst + size_t(p - j0) * D)[i] = v2;
+      reinterpret_cast<__nv_bfloat162 *>(a.vc + (head_row + p) * D)[i] = v2;
+    }
+    __syncthreads();
+    float acc[G][8];
+#pragma unroll
+    for (int h = 0; h < G; ++h)
+#pragma unroll
+      for (int e = 0; e < 8; ++e) acc[h][e] = 0.0f;
+    for (int jb = 2 * warp; jb < n; jb += 2 * kAttnWarps) {
+      const int jj = jb + half;
+      if (jj < n) {
+        float vv[8];
+        bf16x8_to_f32(*reinterpret_cast<const uint4 *>(
+                          vst + size_t(jj) * D + 8 * hl),
+                      vv);
+#pragma unroll
+        for (int h = 0; h < G; ++h) {
+          const float w = sc[jj * G + h];
+#pragma unroll
+          for (int e = 0; e < 8; ++e) acc[h][e] = fmaf(w, vv[e], acc[h][e]);
+        }
+      }
+    }
+#pragma unroll
+    for (int h = 0; h < G; ++h)
+#pragma unroll
+      for (int e = 0; e < 8; ++e)
+        acc[h][e] += __shfl_xor_sync(0xffffffffu, acc[h][e], 16);
+    if (half == 0)
+#pragma unroll
+      for (int h = 0; h < G; ++h)
+#pragma unroll
+        for (int e = 0; e < 8; ++e)
+          wacc[(warp * G + h) * D + 8 * hl + e] = acc[h][e];
+    __syncthreads();
+  }
+  return true;
+}
+
 template <int G>
 __global__ void __launch_bounds__(kAttnThreads)
 attn_decode_kernel(const AttnArgs a) {
@@ -202,8 +402,7 @@ attn_decode_kernel(const AttnArgs a) {
   __shared__ int s_last;
 
   const int c = blockIdx.x, g = blockIdx.y;
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int hl = lane & 15, half = lane >> 4;
+  const int tid = threadIdx.x;
   constexpr int D = kAttnD;
 
   // Every input may come from the preceding kernel (the q|k|v GEMV, an
@@ -226,174 +425,10 @@ attn_decode_kernel(const AttnArgs a) {
   }
   const int n = j1 - j0;  // positions of this CTA (<= kAttnChunk)
   float *part = a.part + (size_t(g) * a.n_split + c) * P::kStride;
-  const size_t head_row = size_t(g) * a.S;  // row 0 of KV head g
 
   if (n > 0) {
-    // ---- the split's key rows and value rows: one bulk copy each ----
-    if (tid == 0) {
-      pipe::mbar_init(&bar[0], 1);
-      pipe::mbar_init(&bar[1], 1);
-      asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-      const uint32_t bytes = uint32_t(n) * L::kRowBytes;
-      pipe::mbar_arrive_expect_tx(&bar[0], bytes);
-      pipe::bulk_copy_g2s(kst, a.kc + (head_row + j0) * D, bytes, &bar[0]);
-      pipe::mbar_arrive_expect_tx(&bar[1], bytes);
-      pipe::bulk_copy_g2s(vst, a.vc + (head_row + j0) * D, bytes, &bar[1]);
-    }
-    // ---- RoPE of the queries meanwhile ----
-    if (tid < kAttnPairs) {
-      float sn, cn;
-      sincosf(__fmul_rn(float(p), a.freq[tid]), &sn, &cn);
-      cs[tid] = make_float2(cn, sn);
-    }
-    __syncthreads();  // cos/sin ready; the barriers are initialised
-    for (int e = tid; e < G * kAttnPairs; e += kAttnThreads) {
-      const int h = e / kAttnPairs, i = e - h * kAttnPairs;
-      const __nv_bfloat16 *qh = a.qkv + size_t(g * G + h) * D;
-      const float x0 = __bfloat162float(qh[2 * i]);
-      const float x1 = __bfloat162float(qh[2 * i + 1]);
-      const float2 r = cs[i];
-      q_sm[h * D + 2 * i] = x0 * r.x - x1 * r.y;
-      q_sm[h * D + 2 * i + 1] = x0 * r.y + x1 * r.x;
-    }
-    const bool has_p = j0 <= p && p < j1;
-    if (!__syncthreads_and(pipe::mbar_wait(&bar[0], 0u))) {
-      // Never expected: report, let the copies land (bounded) before the
-      // CTA may leave, and contribute no partial.
-      if (tid == 0) {
-        atomicOr(a.err, 4u);
-        if (!pipe::mbar_wait(&bar[0], 0u) || !pipe::mbar_wait(&bar[1], 0u))
-          atomicOr(a.err, 2u);
-      }
-      __syncthreads();
-    } else {
-      // ---- the new token's rotated key: staged and appended (the key
-      // copy has landed, so neither write can be overwritten or read by it)
-      if (has_p && tid < kAttnPairs) {
-        const int i = tid;
-        const __nv_bfloat16 *kh = a.qkv + size_t(a.H + g) * D;
-        const float x0 = __bfloat162float(kh[2 * i]);
-        const float x1 = __bfloat162float(kh[2 * i + 1]);
-        const float2 r = cs[i];
-        const __nv_bfloat162 k2 = __halves2bfloat162(
-            __float2bfloat16_rn(x0 * r.x - x1 * r.y),
-            __float2bfloat16_rn(x0 * r.y + x1 * r.x));
-        reinterpret_cast<__nv_bfloat162 *>(kst + size_t(p - j0) * D)[i] = k2;
-        reinterpret_cast<__nv_bfloat162 *>(a.kc + (head_row + p) * D)[i] = k2;
-      }
-      __syncthreads();
-
-      // ---- scores: a half-warp per position, 8 dims per lane ----
-      float qr[G][8];
-#pragma unroll
-      for (int h = 0; h < G; ++h)
-#pragma unroll
-        for (int e = 0; e < 8; ++e) qr[h][e] = q_sm[h * D + 8 * hl + e];
-      // Two positions per half-warp and step: their shuffle chains overlap.
-      for (int jb = 4 * warp; jb < n; jb += 4 * kAttnWarps) {  // warp-uniform
-        float d[2][G];
-#pragma unroll
-        for (int r = 0; r < 2; ++r) {
-          const int jj = jb + 2 * r + half;
-          float kv[8];
-          bf16x8_to_f32(jj < n ? *reinterpret_cast<const uint4 *>(
-                                     kst + size_t(jj) * D + 8 * hl)
-                               : make_uint4(0u, 0u, 0u, 0u),
-                        kv);
-#pragma unroll
-          for (int h = 0; h < G; ++h) {
-            float t = 0.0f;
-#pragma unroll
-            for (int e = 0; e < 8; ++e) t = fmaf(qr[h][e], kv[e], t);
-            d[r][h] = t;
-          }
-        }
-#pragma unroll
-        for (int o = 8; o > 0; o >>= 1)
-#pragma unroll
-          for (int r = 0; r < 2; ++r)
-#pragma unroll
-            for (int h = 0; h < G; ++h)
-              d[r][h] += __shfl_xor_sync(0xffffffffu, d[r][h], o);  // in half
-        if (hl == 0)
-#pragma unroll
-          for (int r = 0; r < 2; ++r) {
-            const int jj = jb + 2 * r + half;
-            if (jj < n)
-#pragma unroll
-              for (int h = 0; h < G; ++h)
-                sc[jj * G + h] = d[r][h] * a.inv_sqrt_d;
-          }
-      }
-      __syncthreads();
-
-      // ---- softmax of the split: largest score, then exp and sum ----
-      float m[G], l[G];
-#pragma unroll
-      for (int h = 0; h < G; ++h) m[h] = -INFINITY;
-      for (int jj = tid; jj < n; jj += kAttnThreads)
-#pragma unroll
-        for (int h = 0; h < G; ++h) m[h] = fmaxf(m[h], sc[jj * G + h]);
-      cta_reduce<G, true>(m, red);
-#pragma unroll
-      for (int h = 0; h < G; ++h) l[h] = 0.0f;
-      for (int jj = tid; jj < n; jj += kAttnThreads)
-#pragma unroll
-        for (int h = 0; h < G; ++h) {
-          const float e = expf(sc[jj * G + h] - m[h]);
-          sc[jj * G + h] = e;
-          l[h] += e;
-        }
-      cta_reduce<G, false>(l, red);  // its barriers also publish sc
-
-      // ---- weighted values (the value copy landed during the scores) ----
-      if (!__syncthreads_and(pipe::mbar_wait(&bar[1], 0u))) {
-        if (tid == 0) {
-          atomicOr(a.err, 4u);
-          if (!pipe::mbar_wait(&bar[1], 0u)) atomicOr(a.err, 2u);
-        }
-        __syncthreads();
-      }
-      if (has_p && tid < kAttnPairs) {  // the new token's value
-        const int i = tid;
-        const __nv_bfloat16 *vh = a.qkv + size_t(a.H + a.Hkv + g) * D;
-        const __nv_bfloat162 v2 = __halves2bfloat162(vh[2 * i], vh[2 * i + 1]);
-        reinterpret_cast<__nv_bfloat162 *>(vst + size_t(p - j0) * D)[i] = v2;
-        reinterpret_cast<__nv_bfloat162 *>(a.vc + (head_row + p) * D)[i] = v2;
-      }
-      __syncthreads();
-      float acc[G][8];
-#pragma unroll
-      for (int h = 0; h < G; ++h)
-#pragma unroll
-        for (int e = 0; e < 8; ++e) acc[h][e] = 0.0f;
-      for (int jb = 2 * warp; jb < n; jb += 2 * kAttnWarps) {
-        const int jj = jb + half;
-        if (jj < n) {
-          float vv[8];
-          bf16x8_to_f32(*reinterpret_cast<const uint4 *>(
-                            vst + size_t(jj) * D + 8 * hl),
-                        vv);
-#pragma unroll
-          for (int h = 0; h < G; ++h) {
-            const float w = sc[jj * G + h];
-#pragma unroll
-            for (int e = 0; e < 8; ++e) acc[h][e] = fmaf(w, vv[e], acc[h][e]);
-          }
-        }
-      }
-#pragma unroll
-      for (int h = 0; h < G; ++h)
-#pragma unroll
-        for (int e = 0; e < 8; ++e)
-          acc[h][e] += __shfl_xor_sync(0xffffffffu, acc[h][e], 16);
-      if (half == 0)
-#pragma unroll
-        for (int h = 0; h < G; ++h)
-#pragma unroll
-          for (int e = 0; e < 8; ++e)
-            wacc[(warp * G + h) * D + 8 * hl + e] = acc[h][e];
-      __syncthreads();
+    float m[G], l[G];
+    if (attend_split<G, kAttnChunk>(a, g, p, j0, n, smem, bar, m, l)) {
       if (n_eff == 1) {
         // One split holds the whole context: its sums are final.  Write
         // the outputs (and the next RMSNorm's statistics) directly; no
@@ -571,6 +606,275 @@ attn_decode_kernel(const AttnArgs a) {
   }
 }
 
+// ---------------------------------------------------------------------------
+// Caches of at most kClMaxS positions: one thread-block cluster per KV head.
+// Its CTAs take consecutive splits of positions 0..p (at least kClMinChunk
+// each), keep their partials (m, l and the unnormalised output) in their own
+// shared memory, and after a cluster barrier each CTA merges a slice of the
+// head's G D outputs by reading every partial through distributed shared
+// memory; each CTA then stores its share of the next RMSNorm's statistics
+// into CTA 0's shared memory, and after a second barrier CTA 0 sums them in
+// order.  No workspace, fence or counter, and no partial leaves the chip.
+// A context of at most kClSoloMax positions (and an invalid position) is
+// finished by CTA 0 alone, straight from its shared memory, with no cluster
+// barrier: the other CTAs leave at once.  Every CTA reads the same position,
+// so the choice is the same in the whole cluster, and otherwise every CTA
+// executes both cluster barriers on every path: a barrier never waits for a
+// CTA that has left.
+constexpr int kClMaxCtas = 16;                  // CTAs per KV head
+constexpr int kClChunk = 256;                   // positions per CTA, at most
+constexpr int kClMinChunk = 16;                 // positions per used CTA
+constexpr int kClSoloMax = 64;                  // contexts CTA 0 finishes alone
+constexpr int kClMaxS = kClMaxCtas * kClChunk;  // 4096
+
+// CTAs per KV head for a cache of S <= kClMaxS positions.
+inline int cl_ctas(int S) {
+  const int n = (S + kClMinChunk - 1) / kClMinChunk;
+  return n < 1 ? 1 : (n > kClMaxCtas ? kClMaxCtas : n);
+}
+
+// The partial and merge scratch after the split's layout.
+template <int G>
+struct ClSmem {
+  using L = AttnSmem<G, kClChunk>;
+  static constexpr uint32_t kAcc = uint32_t((L::kBytes + 15) / 16 * 16);
+  static constexpr uint32_t kM = kAcc + G * kAttnD * 4;           // [G]
+  static constexpr uint32_t kL = kM + G * 4;                      // [G]
+  static constexpr uint32_t kStats = (kL + G * 4 + 7) / 8 * 8;    // float2[16]
+  static constexpr uint32_t kMm = kStats + kClMaxCtas * 8;        // [16][G]
+  static constexpr uint32_t kLl = kMm + kClMaxCtas * G * 4;       // [16][G]
+  static constexpr size_t kBytes = kLl + kClMaxCtas * G * 4;
+};
+
+__device__ __forceinline__ uint32_t cl_map(const void *p, int rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;"
+               : "=r"(r)
+               : "r"(pipe::smem_addr(p)), "r"(rank));
+  return r;
+}
+__device__ __forceinline__ float cl_ld(uint32_t addr) {
+  float v;
+  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(addr)
+               : "memory");
+  return v;
+}
+__device__ __forceinline__ void cl_st2(uint32_t addr, float a, float b) {
+  asm volatile("st.shared::cluster.v2.f32 [%0], {%1, %2};" ::"r"(addr),
+               "f"(a), "f"(b)
+               : "memory");
+}
+__device__ __forceinline__ void cluster_sync_all() {
+  asm volatile(
+      "barrier.cluster.arrive.release.aligned;\n\t"
+      "barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+template <int G>
+__global__ void __launch_bounds__(kAttnThreads)
+attn_cluster_kernel(const AttnArgs a) {
+  extern __shared__ __align__(128) uint8_t smem[];
+  using L = AttnSmem<G, kClChunk>;
+  using CS = ClSmem<G>;
+  float *wacc = reinterpret_cast<float *>(smem + L::kWacc);
+  float *red = reinterpret_cast<float *>(smem + L::kRed);
+  float *pacc = reinterpret_cast<float *>(smem + CS::kAcc);
+  float *pm = reinterpret_cast<float *>(smem + CS::kM);
+  float *pl = reinterpret_cast<float *>(smem + CS::kL);
+  float2 *stats = reinterpret_cast<float2 *>(smem + CS::kStats);
+  float *mm = reinterpret_cast<float *>(smem + CS::kMm);
+  float *ll = reinterpret_cast<float *>(smem + CS::kLl);
+  __shared__ __align__(8) uint64_t bar[2];  // keys, values
+  constexpr int D = kAttnD;
+  const int c = blockIdx.x, g = blockIdx.y, cl = gridDim.x;  // c = rank
+  const int tid = threadIdx.x;
+
+  // Every input may come from the preceding kernel.
+  pdl_wait();
+  pdl_trigger();
+
+  const int p = *a.pos;
+  const bool valid = p >= 0 && p < a.S;
+  float m[G], l[G];
+#pragma unroll
+  for (int h = 0; h < G; ++h) {
+    m[h] = -INFINITY;
+    l[h] = 0.0f;
+  }
+  if (!valid || p + 1 <= kClSoloMax) {
+    // ---- CTA 0 alone: the whole context, or zeros for a bad position ----
+    if (c != 0) return;
+    const bool have =
+        valid && attend_split<G, kClChunk>(a, g, p, 0, p + 1, smem, bar, m, l);
+    float *o = a.out + size_t(g) * G * D;
+    float ss = 0.0f, amx = 0.0f;
+    for (int e = tid; e < G * D; e += kAttnThreads) {
+      float y = 0.0f;
+      if (have) {
+        float t = wacc[e];
+#pragma unroll
+        for (int w = 1; w < kAttnWarps; ++w) t += wacc[w * G * D + e];
+        const int h = e / D;
+        float lh = l[0];
+#pragma unroll
+        for (int hh = 1; hh < G; ++hh)
+          if (hh == h) lh = l[hh];
+        y = t / lh;
+      }
+      o[e] = y;
+      if (a.norm_part) {
+        ss += y * y;
+        amx = fmaxf(amx,
+                    fabsf(__fmul_rn(y, a.norm_gamma[size_t(g) * G * D + e])));
+      }
+    }
+    if (a.norm_part) {
+      cta_sum_max(ss, amx, red);
+      if (tid == 0) a.norm_part[g] = make_float2(ss, amx);
+    }
+    if (!valid && tid == 0) atomicOr(a.err, kAttnErrPosition);
+    return;
+  }
+  int n_eff = 0, j0 = 0, n = 0;
+  {
+    const int len = p + 1;
+    n_eff = min(cl, (len + kClMinChunk - 1) / kClMinChunk);
+    if (c < n_eff) {
+      j0 = int(int64_t(c) * len / n_eff);
+      n = int(int64_t(c + 1) * len / n_eff) - j0;
+    }
+  }
+  // ---- this CTA's partial, in its own shared memory ----
+  bool have = false;
+  if (n > 0) have = attend_split<G, kClChunk>(a, g, p, j0, n, smem, bar, m, l);
+  for (int e = tid; e < G * D; e += kAttnThreads) {
+    float t = 0.0f;
+    if (have) {
+      t = wacc[e];
+#pragma unroll
+      for (int w = 1; w < kAttnWarps; ++w) t += wacc[w * G * D + e];
+    }
+    pacc[e] = t;
+  }
+  if (tid < G) {
+#pragma unroll
+    for (int h = 0; h < G; ++h)
+      if (tid == h) {
+        pm[h] = have ? m[h] : -INFINITY;
+        pl[h] = have ? l[h] : 0.0f;
+      }
+  }
+  cluster_sync_all();  // every partial of the head is complete
+
+  // ---- merge: this CTA's slice of the head's G D outputs ----
+  for (int t = tid; t < kClMaxCtas * G; t += kAttnThreads) {
+    const int cc = t / G, h = t - cc * G;
+    float mv = -INFINITY, lv = 0.0f;
+    if (cc < n_eff) {
+      mv = cl_ld(cl_map(pm + h, cc));
+      lv = cl_ld(cl_map(pl + h, cc));
+    }
+    mm[t] = mv;
+    ll[t] = lv;
+  }
+  __syncthreads();
+  const int per = (G * D + cl - 1) / cl;
+  const int e_lo = c * per, e_hi = min(G * D, e_lo + per);
+  float *o = a.out + size_t(g) * G * D;
+  float ss = 0.0f, amx = 0.0f;
+  for (int e = e_lo + tid; e < e_hi; e += kAttnThreads) {
+    float y = 0.0f;
+    {
+      const int h = e / D;
+      float mx = -INFINITY;
+      for (int cc = 0; cc < n_eff; ++cc) mx = fmaxf(mx, mm[cc * G + h]);
+      float lsum = 0.0f, acc = 0.0f;
+      for (int cc = 0; cc < n_eff; ++cc) {
+        const float w = expf(mm[cc * G + h] - mx);
+        lsum = fmaf(w, ll[cc * G + h], lsum);
+        acc = fmaf(w, cl_ld(cl_map(pacc + e, cc)), acc);
+      }
+      y = acc / lsum;
+    }
+    o[e] = y;
+    if (a.norm_part) {
+      ss += y * y;
+      amx = fmaxf(amx, fabsf(__fmul_rn(y, a.norm_gamma[size_t(g) * G * D + e])));
+    }
+  }
+  if (a.norm_part) {
+    cta_sum_max(ss, amx, red);
+    if (tid == 0) cl_st2(cl_map(stats + c, 0), ss, amx);
+  }
+  cluster_sync_all();  // the peers' partials are no longer read
+  if (c == 0 && tid == 0) {
+    if (a.norm_part) {
+      float ts = 0.0f, tm = 0.0f;
+      for (int cc = 0; cc < cl; ++cc) {
+        ts += stats[cc].x;
+        tm = fmaxf(tm, stats[cc].y);
+      }
+      a.norm_part[g] = make_float2(ts, tm);
+    }
+  }
+}
+
+// Whether clusters of kClMaxCtas CTAs of this kernel can be resident (once
+// per device).
+template <int G>
+bool cluster_ok(int dev) {
+  static int state[64];  // 0 unknown, 1 yes, 2 no
+  if (state[dev] == 0) {
+    auto kernel = attn_cluster_kernel<G>;
+    bool ok =
+        cudaFuncSetAttribute(kernel,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             int(ClSmem<G>::kBytes)) == cudaSuccess &&
+        cudaFuncSetAttribute(kernel,
+                             cudaFuncAttributeNonPortableClusterSizeAllowed,
+                             1) == cudaSuccess;
+    if (ok) {
+      cudaLaunchConfig_t cfg = {};
+      cfg.gridDim = dim3(kClMaxCtas, 1);
+      cfg.blockDim = dim3(kAttnThreads);
+      cfg.dynamicSmemBytes = ClSmem<G>::kBytes;
+      cudaLaunchAttribute attr[1];
+      attr[0].id = cudaLaunchAttributeClusterDimension;
+      attr[0].val.clusterDim.x = kClMaxCtas;
+      attr[0].val.clusterDim.y = 1;
+      attr[0].val.clusterDim.z = 1;
+      cfg.attrs = attr;
+      cfg.numAttrs = 1;
+      int clusters = 0;
+      ok = cudaOccupancyMaxActiveClusters(&clusters, kernel, &cfg) ==
+               cudaSuccess &&
+           clusters >= 1;
+    }
+    cudaGetLastError();  // a refused query is not an error of the call
+    state[dev] = ok ? 1 : 2;
+  }
+  return state[dev] == 1;
+}
+
+template <int G>
+cudaError_t launch_cluster_g(const AttnArgs &a, int cl, cudaStream_t stream) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(unsigned(cl), unsigned(a.Hkv));
+  cfg.blockDim = dim3(kAttnThreads);
+  cfg.dynamicSmemBytes = ClSmem<G>::kBytes;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = unsigned(cl);
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 2;
+  return cudaLaunchKernelEx(&cfg, attn_cluster_kernel<G>, a);
+}
+
 template <int G>
 cudaError_t launch_g(const AttnArgs &a, cudaStream_t stream) {
   static bool configured[64];
@@ -650,7 +954,31 @@ cudaError_t launch_attn(const AttnLaunch &l, cudaStream_t stream) {
   if (!a.err) return cudaErrorInvalidSymbol;
   a.norm_gamma = l.norm_gamma;
   a.norm_part = l.norm_part;
-  switch (l.H / l.Hkv) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  const int G = l.H / l.Hkv;
+  if (l.S <= kClMaxS) {  // one cluster per KV head, merged on chip
+    const int cl = cl_ctas(l.S);
+    a.n_split = cl;
+    switch (G) {
+      case 1:
+        if (cluster_ok<1>(dev)) return launch_cluster_g<1>(a, cl, stream);
+        break;
+      case 2:
+        if (cluster_ok<2>(dev)) return launch_cluster_g<2>(a, cl, stream);
+        break;
+      case 4:
+        if (cluster_ok<4>(dev)) return launch_cluster_g<4>(a, cl, stream);
+        break;
+      default:
+        if (cluster_ok<8>(dev)) return launch_cluster_g<8>(a, cl, stream);
+        break;
+    }
+    a.n_split = attn_splits(l.S, l.Hkv, sms);
+  }
+  switch (G) {
     case 1: return launch_g<1>(a, stream);
     case 2: return launch_g<2>(a, stream);
     case 4: return launch_g<4>(a, stream);

@@ -53,7 +53,7 @@ constexpr uint32_t lut_pad() {
 // Prologue: the pair tables of the MT activation rows (zero beyond K) and
 // their scales.  The tables already hold signed weights, so the code-sum
 // correction of the dp4a path is zero.
-template <uint32_t kChunkBytes>
+template <uint32_t kTabBytes>
 struct StageLut {
   const int8_t *x;
   const float *s;  // null in accumulator mode
@@ -68,7 +68,7 @@ struct StageLut {
     const float sv = (s && threadIdx.x < MT) ? s[threadIdx.x] : 0.0f;
     const int pairs = c.chunks * 32;
     uint4 *tab = reinterpret_cast<uint4 *>(c.xs);
-    constexpr int kChunkVecs = int(kChunkBytes) * MT / 16;
+    constexpr int kChunkVecs = int(kTabBytes) * MT / 16;
     for (int pi = threadIdx.x; pi < pairs; pi += blockDim.x) {
       // pair pi = (chunk j, word t, nibble p): elements e0 = b + 8h and
       // e0 + 4 of word t, b = p mod 4, h = p div 4
@@ -111,9 +111,9 @@ struct StageLut {
 
 // The table-lookup dot product.  acc[m][0] collects row m's sum (the other
 // three accumulators of the dp4a layout stay zero).
-template <uint32_t kChunkBytes>
+template <uint32_t kTabBytes>
 struct DotLut {
-  static constexpr uint32_t kXsChunkBytes = kChunkBytes;
+  static constexpr uint32_t kXsChunkBytes = kTabBytes;
 
   template <int MT>
   __device__ __forceinline__ static void chunk(const uint8_t *wp,
@@ -172,13 +172,13 @@ struct DotLut {
                                              int (&acc)[MT][4]) {
     const uint8_t *wp = wbase + q * kGroupChunkBytes + r * kChunkBytes;
     const uint8_t *tc = reinterpret_cast<const uint8_t *>(xs) +
-                        size_t(c0 + q) * kChunkBytes * MT;
+                        size_t(c0 + q) * kTabBytes * MT;
     const int quads = chunks >> 2;
 #pragma unroll 1
     for (int pq = 0; pq < quads; ++pq) {
       chunk<MT>(wp, tc, acc);
       wp += 4 * kGroupChunkBytes;
-      tc += 4 * kChunkBytes * MT;
+      tc += 4 * kTabBytes * MT;
     }
     if (q < (chunks & 3)) chunk<MT>(wp, tc, acc);
   }

@@ -395,7 +395,10 @@ void bw_stack_destroy(bw_stack *stack);
  *             S) bytes, 16-byte aligned, owned by the caller.  Zero it once
  *             before its first use: it holds one counter per KV head, and
  *             every call leaves them at zero again.  Calls sharing a
- *             workspace must not overlap on the GPU.
+ *             workspace must not overlap on the GPU.  For S <= 4096 the
+ *             splits of a KV head run as one thread-block cluster and merge
+ *             through distributed shared memory, leaving the workspace
+ *             untouched; it is required all the same.
  *   D == 128; G in {1, 2, 4, 8}; 1 <= Hkv <= BW_ATTN_MAX_KV_HEADS;
  *   1 <= S <= BW_ATTN_MAX_S; theta > 0 (host, fp32).
  * Ordering: launched with programmatic dependent launch; every input is
