@@ -615,8 +615,15 @@ def run_stack_timing(torch, bw, dev, n_layers=STACK_LAYERS,
            "us_per_token": round(us_tok, 2),
            "weight_bytes_per_token": layer_bytes * n_layers,
            "weight_GBps": round(layer_bytes * n_layers / (us_tok * 1e3), 1),
-           "launches_per_token": (5 if kv_positions else 4) * n_layers,
            "timing": f"best of {reps} runs of {steps} steps, CUDA events"}
+    if kv_positions:
+        res["launches_per_token"] = 5 * n_layers
+        res["execution"] = ("one launch per GEMV and one per attention, each "
+                            "step replayed from a CUDA graph")
+    else:
+        res["launches_per_call"] = 1
+        res["execution"] = ("one persistent cooperative kernel per call "
+                            f"({steps} steps x {n_layers} layers x 4 GEMVs)")
     if kv_positions:
         res["attention"] = (f"KV cache of {kv_positions} positions; tokens "
                             f"0..{steps - 1} of one sequence per run")
@@ -700,10 +707,35 @@ def oracle_step(oracle, shapes, act, threads):
     return wb
 
 
+def oracle_stack_token(oracle, seconds):
+    """The oracle's decoder layers at the BitNet-2B shape (dim 2560, ffn 6912,
+    20/5 heads, one-token attention, the bench stack's seeded weights): one
+    token through as many of the 30 layers as a bounded time allows, one
+    core; returns tok/s for the 30-layer stack."""
+    dim, ffn, nh, nkv = 2560, 6912, 20, 5
+    seed = synth.base_seed(4)
+    w = synth.stack_weights(seed, 1, dim, ffn, nh, nkv)
+    L0 = w["layers"][0]
+    h = synth.step_inputs(seed, 1, dim)[0]
+    t0 = time.perf_counter()
+    layers = 0
+    while layers < STACK_LAYERS:
+        h = oracle.layer(h, dim, ffn, nh, nkv, w["eps"], L0["wqkv"], L0["wo"],
+                         L0["w13"], L0["w2"], L0["ws"], L0["gammas"])
+        layers += 1
+        if time.perf_counter() - t0 >= seconds:
+            break
+    dt = time.perf_counter() - t0
+    return {"tok_s": round(layers / (dt * STACK_LAYERS), 4), "cores": 1,
+            "sample": f"{layers} layer(s) of one token in {dt:.1f} s on one "
+                      f"thread, scaled to {STACK_LAYERS} layers"}
+
+
 def cpu_baseline(shapes, act, seconds):
     """The oracle as it stands on whole steps of the workload restricted to
     one replica, repeated for a bounded time: on every host core (output
-    rows split over a thread pool), and on one core."""
+    rows split over a thread pool), and on one core.  Beside it, the oracle's
+    decoder layers in tok/s."""
     import oracle
     oracle.build()
     cores = os.cpu_count() or 1
@@ -728,7 +760,8 @@ def cpu_baseline(shapes, act, seconds):
             "single_core": {"value": round(v1, 4), "unit": "GB/s",
                             "cores": 1,
                             "sample": f"{reps1} pass(es), {dt1:.1f} s on one "
-                                      f"thread"}}
+                                      f"thread"},
+            "layer_stack": oracle_stack_token(oracle, seconds / 2)}
 
 
 def run_reference(args):
