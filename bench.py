@@ -59,8 +59,8 @@ FALLBACK_HBM_GBS = 6800.0
 TRAFFIC_SOURCES = ("bit_gemv_bitlinear_gb300/csrc/bw_pipe.cuh",
                    "bit_gemv_bitlinear_gb300/csrc/bw_gemv_tma.cu")
 MEASURED_DRAM = {
-    "sha256": "0ed513557a113e3a4390ad8bb2caea50937b91abb59256fbe9fceabdfa61732b",
-    "bytes": {"wqkv": 2488064, "wo": 1668480, "w13": 8877824, "w2": 4458496}}
+    "sha256": "a7e0b88bbde98c4391974ba1bcdc58049f614aac80f6b731bfd96d79183afe79",
+    "bytes": {"wqkv": 2487936, "wo": 1668608, "w13": 8877568, "w2": 4457728}}
 
 
 def traffic_sources_sha() -> str:
