@@ -167,6 +167,35 @@ __device__ __forceinline__ void cta_reduce(float (&v)[G], float *red) {
   // whose first barrier comes after every thread has read these values.
 }
 
+// Sums V values per lane (V a power of 2, at most 16) over each half-warp,
+// in the butterfly order of xor offsets 8, 4, 2, 1, spreading the results
+// over the lanes: in a round with two or more values left, a lane keeps one
+// half of them and adds the partner's copy of that half (the partner keeps
+// the other half), so the V sums cost V - 1 shuffles instead of 4 V.  Every
+// sum is the same pairwise tree as the plain butterfly's, so the results are
+// bit-identical to it.  On return v[0] holds sum `idx`, the same in the
+// lanes that differ only in the bits below 16 / V.
+template <int N, int V, int O>
+__device__ __forceinline__ void spread_sum(float (&v)[N], int hl, int &idx) {
+  if constexpr (O >= 1) {
+    if constexpr (V >= 2) {
+      constexpr int kHalf = V / 2;
+      const bool up = (hl & O) != 0;
+#pragma unroll
+      for (int i = 0; i < kHalf; ++i) {
+        const float keep = up ? v[i + kHalf] : v[i];
+        const float send = up ? v[i] : v[i + kHalf];
+        v[i] = keep + __shfl_xor_sync(0xffffffffu, send, O);
+      }
+      if (up) idx += kHalf;
+      spread_sum<N, kHalf, O / 2>(v, hl, idx);
+    } else {
+      v[0] += __shfl_xor_sync(0xffffffffu, v[0], O);
+      spread_sum<N, 1, O / 2>(v, hl, idx);
+    }
+  }
+}
+
 // Sum and max of one value per thread over the CTA in one exchange (the
 // next RMSNorm's statistics); `red` holds 2 kAttnWarps floats.
 __device__ __forceinline__ void cta_sum_max(float &ss, float &mx, float *red) {
@@ -190,19 +219,55 @@ __device__ __forceinline__ void cta_sum_max(float &ss, float &mx, float *red) {
   }
 }
 
+// What a CTA of KV head g reads from the q|k|v vector: the query pairs it
+// rotates (pair e = h D / 2 + i of the G heads, e = tid + u kAttnThreads)
+// and, for tid < D / 2, pair tid of the new key and value.  Loaded right
+// after the dependency wait together with the position, which they do not
+// depend on, so the three loads overlap.  The vector is only 2-byte aligned:
+// scalar loads.
+template <int G>
+struct QkvPre {
+  static constexpr int kQ = (G * kAttnPairs + kAttnThreads - 1) / kAttnThreads;
+  __nv_bfloat16 q[kQ][2];
+  __nv_bfloat16 k[2], v[2];
+
+  __device__ __forceinline__ void load(const AttnArgs &a, int g) {
+    const int tid = threadIdx.x;
+    const __nv_bfloat16 *qg = a.qkv + size_t(g) * G * kAttnD;
+#pragma unroll
+    for (int u = 0; u < kQ; ++u) {
+      const int e = tid + u * kAttnThreads;
+      const bool in = e < G * kAttnPairs;
+      q[u][0] = in ? qg[2 * e] : __float2bfloat16_rn(0.0f);
+      q[u][1] = in ? qg[2 * e + 1] : __float2bfloat16_rn(0.0f);
+    }
+    k[0] = k[1] = v[0] = v[1] = __float2bfloat16_rn(0.0f);
+    if (tid < kAttnPairs) {
+      const __nv_bfloat16 *kh = a.qkv + size_t(a.H + g) * kAttnD;
+      const __nv_bfloat16 *vh = a.qkv + size_t(a.H + a.Hkv + g) * kAttnD;
+      k[0] = kh[2 * tid];
+      k[1] = kh[2 * tid + 1];
+      v[0] = vh[2 * tid];
+      v[1] = vh[2 * tid + 1];
+    }
+  }
+};
+
 // The partial of one split, positions j0 .. j0 + n - 1 of KV head g (n >= 1,
 // n <= kChunk): the two bulk copies of its key and value rows, the rotated
 // queries, the append of the new token when the split holds p, the scores,
 // the split's softmax (largest score m and exp sum l per query head, the
 // same in every thread) and the unnormalised output per warp in the wacc
 // rows of the layout (summed over warps by the caller after the final
-// barrier here).  bar: the split's two mbarriers.  Returns false if the
-// key copy did not land (the CTA then has no partial).
+// barrier here).  pre: this thread's loads of the q|k|v vector.  bar: the
+// split's two mbarriers.  Returns false if the key copy did not land (the
+// CTA then has no partial).
 template <int G, int kChunk>
-__device__ __forceinline__ bool attend_split(const AttnArgs &a, int g, int p,
-                                             int j0, int n, uint8_t *smem,
-                                             uint64_t *bar, float (&m)[G],
-                                             float (&l)[G]) {
+__device__ __forceinline__ bool attend_split(const AttnArgs &a,
+                                             const QkvPre<G> &pre, int g,
+                                             int p, int j0, int n,
+                                             uint8_t *smem, uint64_t *bar,
+                                             float (&m)[G], float (&l)[G]) {
   using L = AttnSmem<G, kChunk>;
   __nv_bfloat16 *kst = reinterpret_cast<__nv_bfloat16 *>(smem + L::kK);
   __nv_bfloat16 *vst = reinterpret_cast<__nv_bfloat16 *>(smem + L::kV);
@@ -233,14 +298,17 @@ __device__ __forceinline__ bool attend_split(const AttnArgs &a, int g, int p,
     cs[tid] = make_float2(cn, sn);
   }
   __syncthreads();  // cos/sin ready; the barriers are initialised
-  for (int e = tid; e < G * kAttnPairs; e += kAttnThreads) {
-    const int h = e / kAttnPairs, i = e - h * kAttnPairs;
-    const __nv_bfloat16 *qh = a.qkv + size_t(g * G + h) * D;
-    const float x0 = __bfloat162float(qh[2 * i]);
-    const float x1 = __bfloat162float(qh[2 * i + 1]);
-    const float2 r = cs[i];
-    q_sm[h * D + 2 * i] = x0 * r.x - x1 * r.y;
-    q_sm[h * D + 2 * i + 1] = x0 * r.y + x1 * r.x;
+#pragma unroll
+  for (int u = 0; u < QkvPre<G>::kQ; ++u) {
+    const int e = tid + u * kAttnThreads;
+    if (e < G * kAttnPairs) {
+      const int h = e / kAttnPairs, i = e - h * kAttnPairs;
+      const float x0 = __bfloat162float(pre.q[u][0]);
+      const float x1 = __bfloat162float(pre.q[u][1]);
+      const float2 r = cs[i];
+      q_sm[h * D + 2 * i] = x0 * r.x - x1 * r.y;
+      q_sm[h * D + 2 * i + 1] = x0 * r.y + x1 * r.x;
+    }
   }
   const bool has_p = j0 <= p && p < j0 + n;
   if (!__syncthreads_and(pipe::mbar_wait(&bar[0], 0u))) {
@@ -259,9 +327,8 @@ __device__ __forceinline__ bool attend_split(const AttnArgs &a, int g, int p,
     // copy has landed, so neither write can be overwritten or read by it)
     if (has_p && tid < kAttnPairs) {
       const int i = tid;
-      const __nv_bfloat16 *kh = a.qkv + size_t(a.H + g) * D;
-      const float x0 = __bfloat162float(kh[2 * i]);
-      const float x1 = __bfloat162float(kh[2 * i + 1]);
+      const float x0 = __bfloat162float(pre.k[0]);
+      const float x1 = __bfloat162float(pre.k[1]);
       const float2 r = cs[i];
       const __nv_bfloat162 k2 = __halves2bfloat162(
           __float2bfloat16_rn(x0 * r.x - x1 * r.y),
@@ -343,8 +410,7 @@ __device__ __forceinline__ bool attend_split(const AttnArgs &a, int g, int p,
     }
     if (has_p && tid < kAttnPairs) {  // the new token's value
       const int i = tid;
-      const __nv_bfloat16 *vh = a.qkv + size_t(a.H + a.Hkv + g) * D;
-      const __nv_bfloat162 v2 = __halves2bfloat162(vh[2 * i], vh[2 * i + 1]);
+      const __nv_bfloat162 v2 = __halves2bfloat162(pre.v[0], pre.v[1]);
       reinterpret_cast<__nv_bfloat162 *>(vst + size_t(p - j0) * D)[i] = v2;
       reinterpret_cast<__nv_bfloat162 *>(a.vc + (head_row + p) * D)[i] = v2;
     }
@@ -410,6 +476,8 @@ attn_decode_kernel(const AttnArgs a) {
   pdl_wait();
   pdl_trigger();
 
+  QkvPre<G> pre;
+  pre.load(a, g);
   const int p = *a.pos;
   const bool valid = p >= 0 && p < a.S;
   int n_eff = 0, j0 = 0, j1 = 0;
@@ -428,7 +496,7 @@ attn_decode_kernel(const AttnArgs a) {
 
   if (n > 0) {
     float m[G], l[G];
-    if (attend_split<G, kAttnChunk>(a, g, p, j0, n, smem, bar, m, l)) {
+    if (attend_split<G, kAttnChunk>(a, pre, g, p, j0, n, smem, bar, m, l)) {
       if (n_eff == 1) {
         // One split holds the whole context: its sums are final.  Write
         // the outputs (and the next RMSNorm's statistics) directly; no
@@ -608,18 +676,23 @@ attn_decode_kernel(const AttnArgs a) {
 
 // ---------------------------------------------------------------------------
 // Caches of at most kClMaxS positions: one thread-block cluster per KV head.
-// Its CTAs take consecutive splits of positions 0..p (at least kClMinChunk
-// each), keep their partials (m, l and the unnormalised output) in their own
-// shared memory, and after a cluster barrier each CTA merges a slice of the
-// head's G D outputs by reading every partial through distributed shared
-// memory; each CTA then stores its share of the next RMSNorm's statistics
-// into CTA 0's shared memory, and after a second barrier CTA 0 sums them in
-// order.  No workspace, fence or counter, and no partial leaves the chip.
+// CTA c owns slice c of the head's G D outputs (per outputs, a multiple of
+// 4).  The CTAs take consecutive splits of positions 0..p (at least
+// kClMinChunk each); as soon as its split is done a CTA pushes it through
+// distributed shared memory: its m and l to every CTA, and each slice of its
+// unnormalised output to the slice's owner.  After one cluster barrier every
+// CTA merges its slice from its own shared memory.  With the layer stack's
+// RMSNorm statistics, each CTA then stores its share into CTA 0's shared
+// memory, and after a second barrier CTA 0 sums them in order.  No
+// workspace, fence or counter, and no partial leaves the chip.  A barrier
+// phase that every CTA arrives at before its split (and waits for before
+// its first push) guarantees that all CTAs of the cluster have started
+// before any shared memory of another is written.
 // A context of at most kClSoloMax positions (and an invalid position) is
 // finished by CTA 0 alone, straight from its shared memory, with no cluster
 // barrier: the other CTAs leave at once.  Every CTA reads the same position,
 // so the choice is the same in the whole cluster, and otherwise every CTA
-// executes both cluster barriers on every path: a barrier never waits for a
+// executes every cluster barrier on every path: a barrier never waits for a
 // CTA that has left.
 constexpr int kClMaxCtas = 16;                  // CTAs per KV head
 constexpr int kClChunk = 256;                   // positions per CTA, at most
@@ -633,17 +706,22 @@ inline int cl_ctas(int S) {
   return n < 1 ? 1 : (n > kClMaxCtas ? kClMaxCtas : n);
 }
 
-// The partial and merge scratch after the split's layout.
+// Outputs per slice for a cluster of cl CTAs: ceil(G D / cl) rounded up to
+// a multiple of 4 (so that slices move as 16-byte vectors).
+template <int G>
+__device__ __forceinline__ int cl_slice(int cl) {
+  return ((G * kAttnD + cl - 1) / cl + 3) & ~3;
+}
+
+// The pushed partials after the split's layout: [cl][slice] outputs
+// (cl * slice <= G D + 4 cl), [16][G] (m, l) pairs, [16] statistics.
 template <int G>
 struct ClSmem {
   using L = AttnSmem<G, kClChunk>;
-  static constexpr uint32_t kAcc = uint32_t((L::kBytes + 15) / 16 * 16);
-  static constexpr uint32_t kM = kAcc + G * kAttnD * 4;           // [G]
-  static constexpr uint32_t kL = kM + G * 4;                      // [G]
-  static constexpr uint32_t kStats = (kL + G * 4 + 7) / 8 * 8;    // float2[16]
-  static constexpr uint32_t kMm = kStats + kClMaxCtas * 8;        // [16][G]
-  static constexpr uint32_t kLl = kMm + kClMaxCtas * G * 4;       // [16][G]
-  static constexpr size_t kBytes = kLl + kClMaxCtas * G * 4;
+  static constexpr uint32_t kRecv = uint32_t((L::kBytes + 15) / 16 * 16);
+  static constexpr uint32_t kMl = kRecv + (G * kAttnD + 4 * kClMaxCtas) * 4;
+  static constexpr uint32_t kStats = kMl + kClMaxCtas * G * 8;
+  static constexpr size_t kBytes = kStats + kClMaxCtas * 8;
 };
 
 __device__ __forceinline__ uint32_t cl_map(const void *p, int rank) {
@@ -653,16 +731,21 @@ __device__ __forceinline__ uint32_t cl_map(const void *p, int rank) {
                : "r"(pipe::smem_addr(p)), "r"(rank));
   return r;
 }
-__device__ __forceinline__ float cl_ld(uint32_t addr) {
-  float v;
-  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(addr)
-               : "memory");
-  return v;
-}
 __device__ __forceinline__ void cl_st2(uint32_t addr, float a, float b) {
   asm volatile("st.shared::cluster.v2.f32 [%0], {%1, %2};" ::"r"(addr),
                "f"(a), "f"(b)
                : "memory");
+}
+__device__ __forceinline__ void cl_st4(uint32_t addr, float4 v) {
+  asm volatile("st.shared::cluster.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(addr),
+               "f"(v.x), "f"(v.y), "f"(v.z), "f"(v.w)
+               : "memory");
+}
+__device__ __forceinline__ void cluster_arrive_relaxed() {
+  asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait() {
+  asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 __device__ __forceinline__ void cluster_sync_all() {
   asm volatile(
@@ -678,12 +761,9 @@ attn_cluster_kernel(const AttnArgs a) {
   using CS = ClSmem<G>;
   float *wacc = reinterpret_cast<float *>(smem + L::kWacc);
   float *red = reinterpret_cast<float *>(smem + L::kRed);
-  float *pacc = reinterpret_cast<float *>(smem + CS::kAcc);
-  float *pm = reinterpret_cast<float *>(smem + CS::kM);
-  float *pl = reinterpret_cast<float *>(smem + CS::kL);
+  float *recv = reinterpret_cast<float *>(smem + CS::kRecv);
+  float2 *ml = reinterpret_cast<float2 *>(smem + CS::kMl);
   float2 *stats = reinterpret_cast<float2 *>(smem + CS::kStats);
-  float *mm = reinterpret_cast<float *>(smem + CS::kMm);
-  float *ll = reinterpret_cast<float *>(smem + CS::kLl);
   __shared__ __align__(8) uint64_t bar[2];  // keys, values
   constexpr int D = kAttnD;
   const int c = blockIdx.x, g = blockIdx.y, cl = gridDim.x;  // c = rank
@@ -693,6 +773,8 @@ attn_cluster_kernel(const AttnArgs a) {
   pdl_wait();
   pdl_trigger();
 
+  QkvPre<G> pre;
+  pre.load(a, g);
   const int p = *a.pos;
   const bool valid = p >= 0 && p < a.S;
   float m[G], l[G];
@@ -704,8 +786,9 @@ attn_cluster_kernel(const AttnArgs a) {
   if (!valid || p + 1 <= kClSoloMax) {
     // ---- CTA 0 alone: the whole context, or zeros for a bad position ----
     if (c != 0) return;
-    const bool have =
-        valid && attend_split<G, kClChunk>(a, g, p, 0, p + 1, smem, bar, m, l);
+    const bool have = valid && attend_split<G, kClChunk>(a, pre, g, p, 0,
+                                                         p + 1, smem, bar, m,
+                                                         l);
     float *o = a.out + size_t(g) * G * D;
     float ss = 0.0f, amx = 0.0f;
     for (int e = tid; e < G * D; e += kAttnThreads) {
@@ -735,6 +818,7 @@ attn_cluster_kernel(const AttnArgs a) {
     if (!valid && tid == 0) atomicOr(a.err, kAttnErrPosition);
     return;
   }
+  cluster_arrive_relaxed();  // this CTA has started
   int n_eff = 0, j0 = 0, n = 0;
   {
     const int len = p + 1;
@@ -744,71 +828,73 @@ attn_cluster_kernel(const AttnArgs a) {
       n = int(int64_t(c + 1) * len / n_eff) - j0;
     }
   }
-  // ---- this CTA's partial, in its own shared memory ----
+  const int per = cl_slice<G>(cl);
+  // ---- this CTA's partial ----
   bool have = false;
-  if (n > 0) have = attend_split<G, kClChunk>(a, g, p, j0, n, smem, bar, m, l);
-  for (int e = tid; e < G * D; e += kAttnThreads) {
-    float t = 0.0f;
-    if (have) {
-      t = wacc[e];
+  if (n > 0)
+    have = attend_split<G, kClChunk>(a, pre, g, p, j0, n, smem, bar, m, l);
+  cluster_wait();  // every CTA has started: its shared memory may be written
+  if (c < n_eff) {
+    // ---- pushed to the owners: output slices, then m and l to every CTA
+    for (int e = 4 * tid; e < G * D; e += 4 * kAttnThreads) {
+      float4 t = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+      if (have) {
+        t = *reinterpret_cast<const float4 *>(wacc + e);
 #pragma unroll
-      for (int w = 1; w < kAttnWarps; ++w) t += wacc[w * G * D + e];
-    }
-    pacc[e] = t;
-  }
-  if (tid < G) {
-#pragma unroll
-    for (int h = 0; h < G; ++h)
-      if (tid == h) {
-        pm[h] = have ? m[h] : -INFINITY;
-        pl[h] = have ? l[h] : 0.0f;
+        for (int w = 1; w < kAttnWarps; ++w) {
+          const float4 u =
+              *reinterpret_cast<const float4 *>(wacc + w * G * D + e);
+          t.x += u.x;
+          t.y += u.y;
+          t.z += u.z;
+          t.w += u.w;
+        }
       }
-  }
-  cluster_sync_all();  // every partial of the head is complete
-
-  // ---- merge: this CTA's slice of the head's G D outputs ----
-  for (int t = tid; t < kClMaxCtas * G; t += kAttnThreads) {
-    const int cc = t / G, h = t - cc * G;
-    float mv = -INFINITY, lv = 0.0f;
-    if (cc < n_eff) {
-      mv = cl_ld(cl_map(pm + h, cc));
-      lv = cl_ld(cl_map(pl + h, cc));
+      const int own = e / per;  // < cl: G D <= cl per
+      cl_st4(cl_map(recv + c * per + (e - own * per), own), t);
     }
-    mm[t] = mv;
-    ll[t] = lv;
+    if (tid < cl * G) {
+      const int dst = tid / G, h = tid - dst * G;
+      float mv = -INFINITY, lv = 0.0f;
+      if (have)
+#pragma unroll
+        for (int hh = 0; hh < G; ++hh)
+          if (hh == h) {
+            mv = m[hh];
+            lv = l[hh];
+          }
+      cl_st2(cl_map(ml + c * G + h, dst), mv, lv);
+    }
   }
-  __syncthreads();
-  const int per = (G * D + cl - 1) / cl;
+  cluster_sync_all();  // every partial of the head has been pushed
+
+  // ---- merge: this CTA's slice, from its own shared memory ----
   const int e_lo = c * per, e_hi = min(G * D, e_lo + per);
   float *o = a.out + size_t(g) * G * D;
   float ss = 0.0f, amx = 0.0f;
   for (int e = e_lo + tid; e < e_hi; e += kAttnThreads) {
-    float y = 0.0f;
-    {
-      const int h = e / D;
-      float mx = -INFINITY;
-      for (int cc = 0; cc < n_eff; ++cc) mx = fmaxf(mx, mm[cc * G + h]);
-      float lsum = 0.0f, acc = 0.0f;
-      for (int cc = 0; cc < n_eff; ++cc) {
-        const float w = expf(mm[cc * G + h] - mx);
-        lsum = fmaf(w, ll[cc * G + h], lsum);
-        acc = fmaf(w, cl_ld(cl_map(pacc + e, cc)), acc);
-      }
-      y = acc / lsum;
+    const int h = e / D;
+    float mx = -INFINITY;
+    for (int cc = 0; cc < n_eff; ++cc) mx = fmaxf(mx, ml[cc * G + h].x);
+    float lsum = 0.0f, acc = 0.0f;
+    for (int cc = 0; cc < n_eff; ++cc) {
+      const float2 v = ml[cc * G + h];
+      const float w = expf(v.x - mx);
+      lsum = fmaf(w, v.y, lsum);
+      acc = fmaf(w, recv[cc * per + (e - e_lo)], acc);
     }
+    const float y = acc / lsum;
     o[e] = y;
     if (a.norm_part) {
       ss += y * y;
       amx = fmaxf(amx, fabsf(__fmul_rn(y, a.norm_gamma[size_t(g) * G * D + e])));
     }
   }
-  if (a.norm_part) {
+  if (a.norm_part) {  // the same for every CTA of the launch
     cta_sum_max(ss, amx, red);
     if (tid == 0) cl_st2(cl_map(stats + c, 0), ss, amx);
-  }
-  cluster_sync_all();  // the peers' partials are no longer read
-  if (c == 0 && tid == 0) {
-    if (a.norm_part) {
+    cluster_sync_all();  // every share is in CTA 0
+    if (c == 0 && tid == 0) {
       float ts = 0.0f, tm = 0.0f;
       for (int cc = 0; cc < cl; ++cc) {
         ts += stats[cc].x;
