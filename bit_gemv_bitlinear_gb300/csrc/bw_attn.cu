@@ -344,9 +344,13 @@ __device__ __forceinline__ bool attend_split(const AttnArgs &a,
     for (int h = 0; h < G; ++h)
 #pragma unroll
       for (int e = 0; e < 8; ++e) qr[h][e] = q_sm[h * D + 8 * hl + e];
-    // Two positions per half-warp and step: their shuffle chains overlap.
+    // Two positions per half-warp and step; the 2 G dot products of a lane
+    // are summed over the half-warp together (spread_sum), and the lane
+    // that holds sum (r, h) stores it.
+    constexpr int kV = 2 * G;
+    constexpr int kLow = 16 / kV - 1;  // lanes below this hold copies
     for (int jb = 4 * warp; jb < n; jb += 4 * kAttnWarps) {  // warp-uniform
-      float d[2][G];
+      float d[kV];
 #pragma unroll
       for (int r = 0; r < 2; ++r) {
         const int jj = jb + 2 * r + half;
@@ -360,25 +364,13 @@ __device__ __forceinline__ bool attend_split(const AttnArgs &a,
           float t = 0.0f;
 #pragma unroll
           for (int e = 0; e < 8; ++e) t = fmaf(qr[h][e], kv[e], t);
-          d[r][h] = t;
+          d[r * G + h] = t;
         }
       }
-#pragma unroll
-      for (int o = 8; o > 0; o >>= 1)
-#pragma unroll
-        for (int r = 0; r < 2; ++r)
-#pragma unroll
-          for (int h = 0; h < G; ++h)
-            d[r][h] += __shfl_xor_sync(0xffffffffu, d[r][h], o);  // in half
-      if (hl == 0)
-#pragma unroll
-        for (int r = 0; r < 2; ++r) {
-          const int jj = jb + 2 * r + half;
-          if (jj < n)
-#pragma unroll
-            for (int h = 0; h < G; ++h)
-              sc[jj * G + h] = d[r][h] * a.inv_sqrt_d;
-        }
+      int idx = 0;
+      spread_sum<kV, kV, 8>(d, hl, idx);  // in half
+      const int jj = jb + 2 * (idx / G) + half;
+      if ((hl & kLow) == 0 && jj < n) sc[jj * G + idx % G] = d[0] * a.inv_sqrt_d;
     }
     __syncthreads();
 
