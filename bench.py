@@ -128,6 +128,9 @@ def parse_args():
     p.add_argument("--lut", action="store_true",
                    help="--single: time the pair-table (LUT) variant "
                         "bw_gemv_w2a8_lut instead of the dp4a GEMV")
+    p.add_argument("--gemm", action="store_true",
+                   help="--single: time the prefill call bw_gemm_w2a8 "
+                        "(256-token tensor-core tiles)")
     p.add_argument("--no-lut", action="store_true",
                    help="skip the LUT-variant comparison")
     p.add_argument("--cold", action="store_true",
@@ -821,11 +824,12 @@ def run_reference(args):
 
 
 def time_shape(torch, bw, dev, N, K, M, iters=2000, rotate=0, eager=False,
-               lut=False):
-    """Microseconds per bw_gemv_w2a8 call of one shape, back to back on one
-    stream (a CUDA graph of up to 64 calls unless `eager`), cycling through
-    enough copies of the weights that they exceed L2 (weights, tokens and
-    scales are seeded synthetic data)."""
+               lut=False, gemm=False):
+    """Microseconds per bw_gemv_w2a8 call of one shape (bw_gemv_w2a8_lut
+    with `lut`, the prefill call bw_gemm_w2a8 with `gemm`), back to back on
+    one stream (a CUDA graph of up to 64 calls unless `eager`), cycling
+    through enough copies of the weights that they exceed L2 (weights,
+    tokens and scales are seeded synthetic data)."""
     seed = synth.base_seed(2, 1)
     canon = synth.canonical_weights(seed, N, K)
     packed0 = bw.bw_repack(torch.from_numpy(canon).to(dev), N, K)
@@ -840,10 +844,17 @@ def time_shape(torch, bw, dev, N, K, M, iters=2000, rotate=0, eager=False,
     stream = torch.cuda.Stream(device=dev)
     per_graph = max(rot, min(iters, 64))
     gemv = bw.bw_gemv_w2a8_lut if lut else bw.bw_gemv_w2a8
+    work = (torch.empty((bw.bw_gemm_workspace_bytes(M, K),),
+                        dtype=torch.uint8, device=dev) if gemm else None)
 
     def launches():
         for i in range(per_graph):
-            gemv(q, packed[i % rot], s_, ws, [0, N], N, K, y=y, stream=stream)
+            if gemm:
+                bw.bw_gemm_w2a8(q, packed[i % rot], s_, ws, [0, N], N, K, y=y,
+                                workspace=work, stream=stream)
+            else:
+                gemv(q, packed[i % rot], s_, ws, [0, N], N, K, y=y,
+                     stream=stream)
 
     with torch.cuda.stream(stream):
         launches()
@@ -924,19 +935,25 @@ def run_lut_comparison(torch, bw, dev):
 
 
 BATCHED_N, BATCHED_K, BATCHED_M = 13824, 2560, (4, 16, 64)
-PREFILL_M = (128, 512, 1024, 2048)
+PREFILL_M = (256, 512, 1024, 2048)
 
 
 def run_prefill(torch, bw, dev, peaks):
-    """Prompt-sized W2A8 GEMMs (the W2A8 page's §一 prefill) on the tcgen05
-    path at 13824 x 2560: us per call (graph of calls over rotating weight
-    buffers) and TFLOP/s (2 M N K per call) against the measured dense bf16
-    rate -- the path runs kind::f16 MMAs, whose nominal rate equals bf16's."""
-    out = {"shape": [BATCHED_N, BATCHED_K], "kernel": "tc_gemv_kernel "
-           "(tcgen05, 128-token tiles)", "per_m": {}}
+    """Prompt-sized W2A8 GEMMs (the W2A8 page's §一 prefill) at 13824 x 2560
+    through bw_gemm_w2a8 (the token conversion plus 256-token tcgen05 tiles):
+    us per call (graph of calls over rotating weight buffers) and TFLOP/s
+    (2 M N K per call) against the measured dense bf16 rate -- the path runs
+    kind::f16 MMAs, whose nominal rate equals bf16's.  Beside it, the same
+    product through bw_gemv_w2a8's 128-token tiles."""
+    out = {"shape": [BATCHED_N, BATCHED_K],
+           "kernel": "tok_fp16_kernel + gemm_kernel (tcgen05, 128 weight "
+                     "rows x 256 tokens per CTA)",
+           "per_m": {}}
     for M in PREFILL_M:
         t = time_shape(torch, bw, dev, BATCHED_N, BATCHED_K, M,
-                       iters=max(8, 8192 // M))
+                       iters=max(8, 8192 // M), gemm=True)
+        t128 = time_shape(torch, bw, dev, BATCHED_N, BATCHED_K, M,
+                          iters=max(8, 8192 // M))
         us = t["us"]
         tflops = 2.0 * M * BATCHED_N * BATCHED_K / (us * 1e-6) / 1e12
         out["per_m"][str(M)] = {
@@ -944,7 +961,8 @@ def run_prefill(torch, bw, dev, peaks):
             "frac_of_measured_bf16_sustained":
                 round(tflops / peaks["bf16_tflops_sustained"], 4)
                 if peaks.get("bf16_tflops_sustained") else None,
-            "frac_of_nominal_dense_fp16": round(tflops / 2250.0, 4)}
+            "frac_of_nominal_dense_fp16": round(tflops / 2250.0, 4),
+            "gemv_128_token_tiles_us": round(t128["us"], 2)}
     return out
 
 
@@ -1103,10 +1121,14 @@ def run_single(args):
               flush=True)
         return
     t = time_shape(torch, bw, dev, N, K, M, iters=args.iters,
-                   rotate=args.rotate, eager=args.eager, lut=args.lut)
+                   rotate=args.rotate, eager=args.eager, lut=args.lut,
+                   gemm=args.gemm)
     us = t["us"]
+    kernel = ("pair-table (LUT)" if args.lut else
+              "prefill (bw_gemm_w2a8)" if args.gemm else "bw_gemv_w2a8")
     print(json.dumps({"single": [N, K, M], "rotate": t["rotate"],
-                      "kernel": "pair-table (LUT)" if args.lut else "dp4a",
+                      "kernel": kernel,
+                      "tflops": round(2.0 * M * N * K / (us * 1e-6) / 1e12, 1),
                       "graph": not args.eager, "calls": t["calls"],
                       "us_per_call": round(us, 3),
                       "weight_GBps": round(t["weight_bytes"] / (us * 1e3), 1),

@@ -7,7 +7,8 @@ the import fails (build it with ``python -m bit_gemv_bitlinear_gb300.build``
 or ``__graft_entry__.build()``).
 
 Function names follow the C ABI: ``bw_quant_act``, ``bw_repack``,
-``bw_unrepack``, ``bw_gemv_w2a8``, ``bw_gemv_w2a8_acc``, ``bw_attn_decode``.
+``bw_unrepack``, ``bw_gemv_w2a8``, ``bw_gemv_w2a8_acc``, ``bw_gemm_w2a8``,
+``bw_gemm_w2a8_acc``, ``bw_attn_decode``.
 """
 from __future__ import annotations
 
@@ -41,7 +42,8 @@ EXPORTS = ("bw_status_string", "bw_last_cuda_error", "bw_version",
            "bw_gemv_workspace_bytes", "bw_quant_weight",
            "bw_attn_workspace_bytes", "bw_attn_decode", "bw_stack_create_kv",
            "bw_stack_read_kv", "bw_stack_reset_kv", "bw_gemv_w2a8_lut",
-           "bw_gemv_w2a8_lut_acc")
+           "bw_gemv_w2a8_lut_acc", "bw_gemm_workspace_bytes", "bw_gemm_w2a8",
+           "bw_gemm_w2a8_acc")
 
 _P = ctypes.c_void_p
 _I = ctypes.c_int
@@ -59,6 +61,11 @@ _SIGS = {
     "bw_gemv_w2a8_acc": (_I, [_P, _P, _I, _I, _I, _P, _P]),
     "bw_gemv_w2a8_lut": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _P, _P]),
     "bw_gemv_w2a8_lut_acc": (_I, [_P, _P, _I, _I, _I, _P, _P]),
+    "bw_gemm_workspace_bytes": (ctypes.c_size_t, [_I, _I]),
+    "bw_gemm_w2a8": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _P, _P,
+                          ctypes.c_size_t, _P]),
+    "bw_gemm_w2a8_acc": (_I, [_P, _P, _I, _I, _I, _P, _P, ctypes.c_size_t,
+                              _P]),
     "bw_device_error": (_I, [_P, _P]),
     "bw_stack_create": (_I, [_P, _P]),
     "bw_layer_stack": (_I, [_P, _P, _I, _P, _P, _P]),
@@ -309,6 +316,71 @@ def bw_gemv_w2a8_acc(x: torch.Tensor, packed: torch.Tensor, N: int, K: int,
         _dev(x2, torch.int8, "x"), _dev(packed, torch.uint8, "packed"), M, N,
         K, _dev(acc, torch.int32, "acc"), _stream(stream)),
         "bw_gemv_w2a8_acc")
+    return acc
+
+
+def bw_gemm_workspace_bytes(M: int, K: int) -> int:
+    """Device scratch a prefill product of M tokens needs (0: unsupported)."""
+    return int(_lib.bw_gemm_workspace_bytes(M, K))
+
+
+def _gemm_workspace(workspace, M: int, K: int, device):
+    need = bw_gemm_workspace_bytes(M, K)
+    if workspace is None:
+        workspace = torch.empty((max(need, 1),), dtype=torch.uint8,
+                                device=device)
+    _need(workspace, need, "workspace")
+    return workspace
+
+
+def bw_gemm_w2a8(x: torch.Tensor, packed: torch.Tensor, s: torch.Tensor,
+                 ws: torch.Tensor, ws_bounds, N: int, K: int,
+                 y: torch.Tensor | None = None,
+                 workspace: torch.Tensor | None = None,
+                 stream=None) -> torch.Tensor:
+    """The prefill product: the same bf16 y [M][N] as bw_gemv_w2a8, through
+    256-token tensor-core tiles; workspace is a uint8 device tensor of at
+    least bw_gemm_workspace_bytes(M, K) bytes (allocated if None)."""
+    x2 = x if x.dim() == 2 else x.reshape(1, -1)
+    M = x2.shape[0]
+    if x2.shape[1] != K:
+        raise ValueError("x has the wrong K")
+    if y is None:
+        y = torch.empty((M, N), dtype=torch.bfloat16, device=x.device)
+    _need(packed, bw_repack_bytes(N, K), "packed")
+    _need(s, M, "s")
+    _need(ws, len(ws_bounds) - 1, "ws")
+    _need(y, M * N, "y")
+    workspace = _gemm_workspace(workspace, M, K, x.device)
+    b = _bounds_array(ws_bounds)
+    _check(_lib.bw_gemm_w2a8(
+        _dev(x2, torch.int8, "x"), _dev(packed, torch.uint8, "packed"),
+        _dev(s, torch.float32, "s"), _dev(ws, torch.bfloat16, "ws"),
+        ctypes.cast(b, _P), len(ws_bounds) - 1, M, N, K,
+        _dev(y, torch.bfloat16, "y"), _dev(workspace, torch.uint8, "workspace"),
+        workspace.numel(), _stream(stream)), "bw_gemm_w2a8")
+    return y
+
+
+def bw_gemm_w2a8_acc(x: torch.Tensor, packed: torch.Tensor, N: int, K: int,
+                     acc: torch.Tensor | None = None,
+                     workspace: torch.Tensor | None = None,
+                     stream=None) -> torch.Tensor:
+    """Exact int32 acc [M][N] through the prefill tiles."""
+    x2 = x if x.dim() == 2 else x.reshape(1, -1)
+    M = x2.shape[0]
+    if x2.shape[1] != K:
+        raise ValueError("x has the wrong K")
+    if acc is None:
+        acc = torch.empty((M, N), dtype=torch.int32, device=x.device)
+    _need(packed, bw_repack_bytes(N, K), "packed")
+    _need(acc, M * N, "acc")
+    workspace = _gemm_workspace(workspace, M, K, x.device)
+    _check(_lib.bw_gemm_w2a8_acc(
+        _dev(x2, torch.int8, "x"), _dev(packed, torch.uint8, "packed"), M, N,
+        K, _dev(acc, torch.int32, "acc"),
+        _dev(workspace, torch.uint8, "workspace"), workspace.numel(),
+        _stream(stream)), "bw_gemm_w2a8_acc")
     return acc
 
 

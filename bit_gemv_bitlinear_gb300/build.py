@@ -17,8 +17,9 @@ ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libbw.so")
-HEADERS = [os.path.join(ROOT, "include", "bw.h"),
-           os.path.join(CSRC, "bw_internal.cuh")]
+# Every header: a change to any of them rebuilds every object.
+HEADERS = [os.path.join(ROOT, "include", "bw.h")] + sorted(
+    os.path.join(CSRC, f) for f in os.listdir(CSRC) if f.endswith(".cuh"))
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC",
@@ -54,6 +55,8 @@ def _compile(src: str, extra) -> str:
         if r.stderr.strip():
             with open(obj + ".log", "w") as f:
                 f.write(r.stderr)
+        elif os.path.exists(obj + ".log"):
+            os.remove(obj + ".log")
     return obj
 
 

@@ -31,29 +31,42 @@ bw_status check_mnk(int M, int N, int K) {
 constexpr int kMaxDevices = 64;
 int g_sm_count[kMaxDevices];
 
-// Shared validation and launch of both GEMV entry points.
-bw_status gemv_common(const int8_t *x, const uint8_t *packed, const float *s,
-                      const bw_bf16 *ws, const int *ws_bounds, int n_ws,
-                      int M, int N, int K, void *out, bool acc_out,
-                      cudaStream_t stream) {
+// The checks every product entry point makes (pointers, shape, scale
+// segments, alignment); fills the segments.
+bw_status check_product(const int8_t *x, const uint8_t *packed,
+                        const float *s, const bw_bf16 *ws,
+                        const int *ws_bounds, int n_ws, int M, int N, int K,
+                        const void *out, bool acc_out, WsSegments *seg) {
   if (!x || !packed || !out) return BW_ERR_INVALID_ARG;
   bw_status st = check_mnk(M, N, K);
   if (st != BW_OK) return st;
-  WsSegments seg{};
+  *seg = WsSegments{};
   if (!acc_out) {
     if (!s || !ws || !ws_bounds) return BW_ERR_INVALID_ARG;
     if (n_ws < 1 || n_ws > BW_MAX_WS) return BW_ERR_INVALID_ARG;
     if (ws_bounds[0] != 0 || ws_bounds[n_ws] != N) return BW_ERR_INVALID_ARG;
     for (int i = 0; i < n_ws; ++i)
       if (ws_bounds[i + 1] <= ws_bounds[i]) return BW_ERR_INVALID_ARG;
-    seg.n_ws = n_ws;
-    for (int i = 0; i <= n_ws; ++i) seg.bounds[i] = ws_bounds[i];
+    seg->n_ws = n_ws;
+    for (int i = 0; i <= n_ws; ++i) seg->bounds[i] = ws_bounds[i];
     if (!aligned(s, 4) || !aligned(ws, 2) || !aligned(out, 2))
       return BW_ERR_MISALIGNED;
   } else if (!aligned(out, 4)) {
     return BW_ERR_MISALIGNED;
   }
   if (!aligned(x, 4) || !aligned(packed, 16)) return BW_ERR_MISALIGNED;
+  return BW_OK;
+}
+
+// Shared validation and launch of both GEMV entry points.
+bw_status gemv_common(const int8_t *x, const uint8_t *packed, const float *s,
+                      const bw_bf16 *ws, const int *ws_bounds, int n_ws,
+                      int M, int N, int K, void *out, bool acc_out,
+                      cudaStream_t stream) {
+  WsSegments seg;
+  bw_status st = check_product(x, packed, s, ws, ws_bounds, n_ws, M, N, K, out,
+                               acc_out, &seg);
+  if (st != BW_OK) return st;
 
   const int sms = device_sm_count();
   if (sms <= 0) return cuda_status(cudaErrorNoDevice);
@@ -128,24 +141,10 @@ bw_status gemv_lut_common(const int8_t *x, const uint8_t *packed,
                           const float *s, const bw_bf16 *ws,
                           const int *ws_bounds, int n_ws, int M, int N, int K,
                           void *out, bool acc_out, cudaStream_t stream) {
-  if (!x || !packed || !out) return BW_ERR_INVALID_ARG;
-  bw_status st = check_mnk(M, N, K);
+  WsSegments seg;
+  bw_status st = check_product(x, packed, s, ws, ws_bounds, n_ws, M, N, K, out,
+                               acc_out, &seg);
   if (st != BW_OK) return st;
-  WsSegments seg{};
-  if (!acc_out) {
-    if (!s || !ws || !ws_bounds) return BW_ERR_INVALID_ARG;
-    if (n_ws < 1 || n_ws > BW_MAX_WS) return BW_ERR_INVALID_ARG;
-    if (ws_bounds[0] != 0 || ws_bounds[n_ws] != N) return BW_ERR_INVALID_ARG;
-    for (int i = 0; i < n_ws; ++i)
-      if (ws_bounds[i + 1] <= ws_bounds[i]) return BW_ERR_INVALID_ARG;
-    seg.n_ws = n_ws;
-    for (int i = 0; i <= n_ws; ++i) seg.bounds[i] = ws_bounds[i];
-    if (!aligned(s, 4) || !aligned(ws, 2) || !aligned(out, 2))
-      return BW_ERR_MISALIGNED;
-  } else if (!aligned(out, 4)) {
-    return BW_ERR_MISALIGNED;
-  }
-  if (!aligned(x, 4) || !aligned(packed, 16)) return BW_ERR_MISALIGNED;
   if (device_sm_count() <= 0) return cuda_status(cudaErrorNoDevice);
   for (int left = M; left > 0;) {
     const int mt = left >= 4 ? 4 : (left >= 2 ? 2 : 1);
@@ -174,6 +173,38 @@ bw_status gemv_lut_common(const int8_t *x, const uint8_t *packed,
     m0 += mt;
   }
   return BW_OK;
+}
+
+// The prefill product: validation, then the token conversion and the
+// 256-token tensor-core tiles (two launches).
+bw_status gemm_common(const int8_t *x, const uint8_t *packed, const float *s,
+                      const bw_bf16 *ws, const int *ws_bounds, int n_ws,
+                      int M, int N, int K, void *out, bool acc_out,
+                      void *workspace, size_t workspace_bytes,
+                      cudaStream_t stream) {
+  WsSegments seg;
+  bw_status st = check_product(x, packed, s, ws, ws_bounds, n_ws, M, N, K, out,
+                               acc_out, &seg);
+  if (st != BW_OK) return st;
+  if (K > kMmaMaxK) return BW_ERR_UNSUPPORTED_SHAPE;
+  if (!workspace || workspace_bytes < gemm_workspace_bytes(M, K))
+    return BW_ERR_INVALID_ARG;
+  if (!aligned(workspace, 256)) return BW_ERR_MISALIGNED;
+  if (device_sm_count() <= 0) return cuda_status(cudaErrorNoDevice);
+  GemvArgs a{};
+  a.x = x;
+  a.w = packed;
+  a.s = acc_out ? nullptr : s;
+  a.ws = reinterpret_cast<const __nv_bfloat16 *>(ws);
+  a.out = out;
+  a.K = K;
+  a.N = N;
+  a.x_ld = K;
+  a.out_ld = N;
+  a.chunks = chunks_per_row(K);
+  a.n_groups = int(padded_rows(N) / kGroupRows);
+  a.seg = seg;
+  return cuda_status(launch_gemm(a, M, acc_out, workspace, stream));
 }
 
 }  // namespace
@@ -343,6 +374,28 @@ bw_status bw_gemv_w2a8_lut_acc(const int8_t *x, const uint8_t *packed, int M,
                                bw_stream_t stream) {
   return gemv_lut_common(x, packed, nullptr, nullptr, nullptr, 0, M, N, K,
                          acc, true, reinterpret_cast<cudaStream_t>(stream));
+}
+
+size_t bw_gemm_workspace_bytes(int M, int K) {
+  if (M < 1 || M > BW_MAX_M || K < 4 || K % 4 != 0 || K > kMmaMaxK) return 0;
+  return gemm_workspace_bytes(M, K);
+}
+
+bw_status bw_gemm_w2a8(const int8_t *x, const uint8_t *packed, const float *s,
+                       const bw_bf16 *ws, const int *ws_bounds, int n_ws,
+                       int M, int N, int K, bw_bf16 *y, void *workspace,
+                       size_t workspace_bytes, bw_stream_t stream) {
+  return gemm_common(x, packed, s, ws, ws_bounds, n_ws, M, N, K, y, false,
+                     workspace, workspace_bytes,
+                     reinterpret_cast<cudaStream_t>(stream));
+}
+
+bw_status bw_gemm_w2a8_acc(const int8_t *x, const uint8_t *packed, int M,
+                           int N, int K, int32_t *acc, void *workspace,
+                           size_t workspace_bytes, bw_stream_t stream) {
+  return gemm_common(x, packed, nullptr, nullptr, nullptr, 0, M, N, K, acc,
+                     true, workspace, workspace_bytes,
+                     reinterpret_cast<cudaStream_t>(stream));
 }
 
 }  // extern "C"

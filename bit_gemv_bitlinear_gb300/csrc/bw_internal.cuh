@@ -83,6 +83,13 @@ bool tc_fits(const GemvArgs &args);
 cudaError_t launch_gemv_tc(const GemvArgs &args, int rows, bool acc_out,
                            cudaStream_t stream);
 
+// Prefill-sized products (bw_gemm.cu): the tokens converted once to fp16
+// in the caller's workspace, then 256-token tcgen05 tiles of 128 weight
+// rows; needs K <= kMmaMaxK.
+size_t gemm_workspace_bytes(int M, int K);
+cudaError_t launch_gemm(const GemvArgs &args, int M, bool acc_out,
+                        void *workspace, cudaStream_t stream);
+
 // Pair-table (LUT) GEMV (bw_gemv_lut.cu) for M-tiles of mt = 1, 2 or 4
 // rows; lut_fits() is false where the tables do not fit in shared memory.
 bool lut_fits(int mt, int N, int K);

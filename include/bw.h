@@ -233,6 +233,41 @@ bw_status bw_gemv_w2a8_lut_acc(const int8_t *x, const uint8_t *packed, int M,
 size_t bw_gemv_workspace_bytes(int M, int N, int K);
 
 /* ------------------------------------------------------------------------
+ * bw_gemm_w2a8, bw_gemm_w2a8_acc -- the same products as bw_gemv_w2a8 and
+ * bw_gemv_w2a8_acc (identical int32 accumulators, identical bf16 outputs)
+ * for prefill-sized batches of tokens.  [W2A8] §一 runs prefill and decode
+ * as separate paths (the page's prefill is a BF16 matmul); this is the
+ * prefill product in W2A8, with the §5.3 exact int32 accumulation and
+ * epilogue and the §4.2 weight-scale segments.
+ * Two launches on `stream`: the tokens are first written once into
+ * `workspace` as the tensor cores' fp16 operand (plus their sums), then
+ * each CTA multiplies 128 weight rows by 256 tokens over all K (tcgen05.mma,
+ * M = 128, N = 256, fp32 accumulators exact by construction), so every
+ * decoded weight serves 256 tokens.
+ *   x, packed, s, ws, ws_bounds, n_ws, M, N, K, y, acc: as for
+ *              bw_gemv_w2a8 / bw_gemv_w2a8_acc (same layouts, alignment,
+ *              limits), and K <= 16384.
+ *   workspace  device scratch of at least bw_gemm_workspace_bytes(M, K)
+ *              bytes, 256-byte aligned, owned by the caller; overwritten.
+ *              It must not be in use by work still in flight elsewhere.
+ * Any M >= 1 is accepted; it pays off from a few hundred tokens (for fewer,
+ * bw_gemv_w2a8 takes 64- or 128-token tiles).  Errors: BW_ERR_INVALID_ARG
+ * (null pointer, bad segments, workspace too small), BW_ERR_MISALIGNED,
+ * BW_ERR_UNSUPPORTED_SHAPE (K % 4 != 0, K > 16384, M, N beyond the limits),
+ * BW_ERR_CUDA; nothing is launched on an error.  Ordering as for
+ * bw_gemv_w2a8 (programmatic dependent launch; `packed` may be read before
+ * the preceding work on `stream` completes).
+ * ---------------------------------------------------------------------- */
+size_t bw_gemm_workspace_bytes(int M, int K);
+bw_status bw_gemm_w2a8(const int8_t *x, const uint8_t *packed, const float *s,
+                       const bw_bf16 *ws, const int *ws_bounds, int n_ws,
+                       int M, int N, int K, bw_bf16 *y, void *workspace,
+                       size_t workspace_bytes, bw_stream_t stream);
+bw_status bw_gemm_w2a8_acc(const int8_t *x, const uint8_t *packed, int M,
+                           int N, int K, int32_t *acc, void *workspace,
+                           size_t workspace_bytes, bw_stream_t stream);
+
+/* ------------------------------------------------------------------------
  * Decoder layer stack: chained M=1 W2A8 GEMVs with the fp32 glue between
  * them, in the order of the BitNet b1.58 block ([W2A8] §一 model shape,
  * §4.1 fused projections and the four RMSNorms, §六 item 3 the per-token

@@ -154,6 +154,61 @@ def test_other_entry_points_host_validation(lib):
     assert la(None, A16, 1, 64, 256, A4, None) == INVALID
 
 
+def test_gemm_workspace_and_host_validation(lib):
+    """The prefill product (bw_gemm_w2a8): its workspace size (fp16 tokens
+    of 64 C columns plus the token sums, each rounded to 256 bytes), and
+    every argument check before any CUDA call."""
+    wb = lib.bw_gemm_workspace_bytes
+    wb.restype = ctypes.c_size_t
+    wb.argtypes = [ctypes.c_int, ctypes.c_int]
+    r256 = lambda b: (b + 255) // 256 * 256
+    for M, K in [(1, 4), (256, 2560), (1024, 2560), (77, 300), (4096, 16384)]:
+        C = (K + 63) // 64
+        assert wb(M, K) == r256(M * C * 64 * 2) + r256(M * 4)
+    assert wb(0, 2560) == 0 and wb(4097, 2560) == 0
+    assert wb(256, 6) == 0 and wb(256, 16388) == 0
+
+    f = lib.bw_gemm_w2a8
+    f.restype = ctypes.c_int
+    f.argtypes = [P, P, P, P, P, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                  ctypes.c_int, P, P, ctypes.c_size_t, P]
+    W256 = 0x100000  # fake, 256-byte aligned
+    good = dict(x=A16, w=A16, s=A4, ws=A2, bounds=[0, 64], n_ws=1, M=300,
+                N=64, K=2560, y=A2, work=W256, wbytes=wb(300, 2560))
+
+    def call(**kw):
+        a = dict(good)
+        a.update(kw)
+        b = (None if a["bounds"] is None else
+             (ctypes.c_int * len(a["bounds"]))(*a["bounds"]))
+        return f(a["x"], a["w"], a["s"], a["ws"],
+                 ctypes.cast(b, P) if b is not None else None, a["n_ws"],
+                 a["M"], a["N"], a["K"], a["y"], a["work"], a["wbytes"], None)
+
+    assert call(x=None) == INVALID
+    assert call(y=None) == INVALID
+    assert call(s=None) == INVALID
+    assert call(bounds=[0, 63]) == INVALID
+    assert call(M=0) == INVALID
+    assert call(K=258) == SHAPE
+    assert call(K=16388, wbytes=1 << 40) == SHAPE   # above the fp32-exact K
+    assert call(M=4097) == SHAPE
+    assert call(work=None) == INVALID
+    assert call(wbytes=wb(300, 2560) - 1) == INVALID
+    assert call(work=W256 + 128) == MISALIGNED
+    assert call(x=A4 + 1) == MISALIGNED
+    assert call(w=A16 + 4) == MISALIGNED
+    fa = lib.bw_gemm_w2a8_acc
+    fa.restype = ctypes.c_int
+    fa.argtypes = [P, P, ctypes.c_int, ctypes.c_int, ctypes.c_int, P, P,
+                   ctypes.c_size_t, P]
+    assert fa(A16, A16, 300, 64, 2560, A4 + 2, W256, wb(300, 2560),
+              None) == MISALIGNED
+    assert fa(A16, A16, 300, 64, 2560, A4, W256, 16, None) == INVALID
+    assert fa(None, A16, 300, 64, 2560, A4, W256, wb(300, 2560),
+              None) == INVALID
+
+
 def test_product_path_never_touches_the_oracle():
     """The package and its sources must not reference the oracle."""
     pkg = os.path.join(ROOT, "bit_gemv_bitlinear_gb300")
