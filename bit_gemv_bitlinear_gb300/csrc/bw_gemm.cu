@@ -28,7 +28,9 @@
 //       per stage into a 128 x 256 fp32 accumulator in tensor memory;
 //       columns 0..255 hold it, 4 A stages of 64 columns the rest of 512;
 //     - the decode warps then read the accumulator back (tcgen05.ld) and
-//       store acc = 2^24 D - sum_k x as int32, or the bf16 output.
+//       store acc = 2^24 D - sum_k x as int32, or the bf16 output; the
+//       division by s is a product with 1 / s corrected to the IEEE
+//       quotient (div_by_recip), so the outputs equal bw_gemv_w2a8's.
 // Values (as in bw_gemv_tc.cu): a code c = w + 1 left in place at bit
 // 2 sl of an fp16 half is the value c 4^sl 2^-24 (fp16 patterns below 0x0800
 // are linear), the token of that k is x 4^-sl, so every product is
@@ -79,7 +81,8 @@ constexpr int kGmBars = kBarAcc + 1;
 constexpr uint32_t kSmB = 0;
 constexpr uint32_t kSmW = kSmB + kGmBStages * kGmBStageBytes;
 constexpr uint32_t kSmS = kSmW + kGmWStages * kGmWStageBytes;  // fp32 [256]
-constexpr uint32_t kSmSx = kSmS + kGmTokens * 4;               // int [256]
+constexpr uint32_t kSmR = kSmS + kGmTokens * 4;                // fp32 [256]
+constexpr uint32_t kSmSx = kSmR + kGmTokens * 4;               // fp32 [256]
 constexpr uint32_t kSmWs = kSmSx + kGmTokens * 4;              // fp32 [8]
 constexpr uint32_t kSmTmem = kSmWs + BW_MAX_WS * 4;
 constexpr uint32_t kSmBars = (kSmTmem + 16 + 7) / 8 * 8;
@@ -105,6 +108,31 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
         "=r"(r[30]), "=r"(r[31])
       : "r"(taddr)
       : "memory");
+}
+
+// a / s rounded to nearest even, from r = RN(1 / s): two correction steps
+// of the product a r by its exact residual (fma).  The first brings the
+// quotient within one ulp of a / s, so the second residual is exact and,
+// by P. Markstein's theorem on the final step of division (IBM J. Res.
+// Dev. 34(1), 1990), the second correction is the correctly rounded
+// quotient.  Valid for an integer |a| <= 2^24 and s, r in [2^-60, 2^60]
+// (no intermediate leaves the normal range); the caller divides otherwise.
+// Five FMA-pipe instructions instead of a division per output.
+__device__ __forceinline__ float div_by_recip(float a, float s, float r) {
+  const float q0 = a * r;
+  const float q1 = fmaf(fmaf(-q0, s, a), r, q0);
+  return fmaf(fmaf(-q1, s, a), r, q1);
+}
+
+// 16 bytes of shared memory.  Volatile (kept in order with the barriers and
+// tensor-memory loads around it) but without a memory clobber, so that the
+// compiler need not order it against the epilogue's global stores.
+__device__ __forceinline__ float4 lds4(const void *p) {
+  float4 v;
+  asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
+               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+               : "r"(smem_addr(p)));
+  return v;
 }
 
 // Barrier among the 8 decode warps only (named barrier 1).
@@ -177,7 +205,8 @@ gemm_kernel(const __grid_constant__ CUtensorMap wmap,
   uint64_t *bar = reinterpret_cast<uint64_t *>(smem + kSmBars);
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + kSmTmem);
   float *s_sm = reinterpret_cast<float *>(smem + kSmS);
-  int *sx_sm = reinterpret_cast<int *>(smem + kSmSx);
+  float *r_sm = reinterpret_cast<float *>(smem + kSmR);
+  float *nsx_sm = reinterpret_cast<float *>(smem + kSmSx);
   float *ws_sm = reinterpret_cast<float *>(smem + kSmWs);
 
   if (threadIdx.x == 0) {
@@ -364,10 +393,19 @@ gemm_kernel(const __grid_constant__ CUtensorMap wmap,
     // 128) (tokens) of weight rows 32 q .. 32 q + 31 ----
     pdl_wait();
     {
+      // Per token: -sum_k x (as fp32, exact: |sum| < 2^22; +0 for a zero
+      // sum), s and r = 1 / s (0 where s is outside [2^-60, 2^60]).
       const int t = threadIdx.x;  // 0..255
+      nsx_sm[t] = 0.0f;  // tokens past M: computed in pairs, never stored
+      s_sm[t] = 1.0f;
+      r_sm[t] = 1.0f;
       if (m0 + t < M) {
-        sx_sm[t] = sx[m0 + t];
-        if (!ACC) s_sm[t] = g.s[m0 + t];
+        nsx_sm[t] = static_cast<float>(-sx[m0 + t]);
+        if (!ACC) {
+          const float sv = g.s[m0 + t];
+          s_sm[t] = sv;
+          r_sm[t] = (sv >= 0x1p-60f && sv <= 0x1p60f) ? 1.0f / sv : 0.0f;
+        }
       }
       if (t < BW_MAX_WS)
         ws_sm[t] = t < g.seg.n_ws ? __bfloat162float(g.ws[t]) : 0.0f;
@@ -388,18 +426,51 @@ gemm_kernel(const __grid_constant__ CUtensorMap wmap,
         if (m0 + j0 >= M) break;  // warp-uniform
         uint32_t d[32];
         tmem_ld32(t_lane + uint32_t(j0), d);  // whole warp
+        if (n < g.N) {  // the collective load above is the whole warp's
+          // acc = 2^24 D - sum_k x, exact in fp32 (an integer below 2^24),
+          // in two halves of 16 tokens: their per-token values are loaded
+          // first, then the outputs go out in pairs of tokens (one
+          // conversion to bf16 per pair).
 #pragma unroll
-        for (int e = 0; e < 32; ++e) {
-          const int j = j0 + e, m = m0 + j;
-          if (m >= M || n >= g.N) continue;
-          const int total =
-              __float2int_rn(__uint_as_float(d[e]) * 16777216.0f) - sx_sm[j];
-          if (ACC) {
-            static_cast<int *>(g.out)[size_t(m) * g.out_ld + n] = total;
-          } else {
-            const float scaled = static_cast<float>(total) / s_sm[j];
-            static_cast<__nv_bfloat16 *>(g.out)[size_t(m) * g.out_ld + n] =
-                __float2bfloat16_rn(scaled * wsv);
+          for (int hb = 0; hb < 32; hb += 16) {
+            float nsx[16], sv[16], rv[16];
+#pragma unroll
+            for (int i = 0; i < 16; i += 4) {
+              const float4 a = lds4(nsx_sm + j0 + hb + i);
+              nsx[i] = a.x; nsx[i + 1] = a.y; nsx[i + 2] = a.z; nsx[i + 3] = a.w;
+              if (!ACC) {
+                const float4 b = lds4(s_sm + j0 + hb + i);
+                const float4 c = lds4(r_sm + j0 + hb + i);
+                sv[i] = b.x; sv[i + 1] = b.y; sv[i + 2] = b.z; sv[i + 3] = b.w;
+                rv[i] = c.x; rv[i + 1] = c.y; rv[i + 2] = c.z; rv[i + 3] = c.w;
+              }
+            }
+#pragma unroll
+            for (int e = 0; e < 16; e += 2) {
+              const int m = m0 + j0 + hb + e;
+              if (m >= M) break;
+              const float a0 =
+                  fmaf(__uint_as_float(d[hb + e]), 16777216.0f, nsx[e]);
+              const float a1 =
+                  fmaf(__uint_as_float(d[hb + e + 1]), 16777216.0f, nsx[e + 1]);
+              if (ACC) {
+                int *o = static_cast<int *>(g.out) + size_t(m) * g.out_ld + n;
+                o[0] = __float2int_rn(a0);
+                if (m + 1 < M) o[g.out_ld] = __float2int_rn(a1);
+              } else {
+                const float q0 = rv[e] != 0.0f ? div_by_recip(a0, sv[e], rv[e])
+                                               : a0 / sv[e];
+                const float q1 = rv[e + 1] != 0.0f
+                                     ? div_by_recip(a1, sv[e + 1], rv[e + 1])
+                                     : a1 / sv[e + 1];
+                const __nv_bfloat162 y2 =
+                    __floats2bfloat162_rn(q0 * wsv, q1 * wsv);
+                __nv_bfloat16 *o = static_cast<__nv_bfloat16 *>(g.out) +
+                                   size_t(m) * g.out_ld + n;
+                o[0] = y2.x;
+                if (m + 1 < M) o[g.out_ld] = y2.y;
+              }
+            }
           }
         }
       }

@@ -86,11 +86,27 @@ def test_gemm_prompt_sizes(bw, M, N, K):
 
 def test_gemm_equals_gemv_and_repeats(bw):
     """The prefill tiles and the GEMV's 128-token tiles compute the same
-    exact accumulators and the same bf16 outputs; repeated calls with one
-    workspace give identical results."""
+    exact accumulators and bit-identical bf16 outputs (the GEMV divides by
+    s; the prefill epilogue multiplies by 1 / s and corrects the product to
+    the IEEE quotient, or divides where s is outside [2^-60, 2^60]: the row
+    scaled by 1e25 takes that path; the row scaled by 1e-20 meets the
+    quantiser's floor on absmax); repeated calls with one workspace give
+    identical results."""
     M, N, K = 384, 1000, 2560
     q, packed, acc, y = check(bw, M, N, K, synth.base_seed(17, 0))
     x_d = to_dev(q)
+    xf = synth.normal_f32(synth.base_seed(17, 1), M * K).reshape(M, K)
+    xf[3] *= np.float32(1e-20)
+    xf[200] *= np.float32(1e25)
+    q_d, s_d = bw.bw_quant_act(to_dev(xf))
+    ws_d = bf16_dev(synth.bf16_uniform(synth.base_seed(17, 2), 2))
+    bounds = [0, 333, N]
+    y_gemm = bw.bw_gemm_w2a8(q_d, packed, s_d, ws_d, bounds, N, K)
+    y_gemv = bw.bw_gemv_w2a8(q_d, packed, s_d, ws_d, bounds, N, K)
+    torch.cuda.synchronize()
+    s_h = s_d.cpu().numpy()
+    assert s_h[200] < 2.0**-60
+    assert torch.equal(y_gemm.view(torch.int16), y_gemv.view(torch.int16))
     acc_gemv = bw.bw_gemv_w2a8_acc(x_d, packed, N, K)
     work = torch.empty((bw.bw_gemm_workspace_bytes(M, K),), dtype=torch.uint8,
                        device="cuda")
