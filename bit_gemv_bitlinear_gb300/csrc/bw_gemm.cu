@@ -445,6 +445,12 @@ gemm_kernel(const __grid_constant__ CUtensorMap wmap,
                 rv[i] = c.x; rv[i + 1] = c.y; rv[i + 2] = c.z; rv[i + 3] = c.w;
               }
             }
+            // Every token of the half on the corrected-product path, or
+            // (never for quantised activations of ordinary range) all of
+            // them divided: one branch per half, the same in every lane.
+            bool fast = true;
+#pragma unroll
+            for (int i = 0; i < 16; ++i) fast = fast && rv[i] != 0.0f;
 #pragma unroll
             for (int e = 0; e < 16; e += 2) {
               const int m = m0 + j0 + hb + e;
@@ -458,11 +464,17 @@ gemm_kernel(const __grid_constant__ CUtensorMap wmap,
                 o[0] = __float2int_rn(a0);
                 if (m + 1 < M) o[g.out_ld] = __float2int_rn(a1);
               } else {
-                const float q0 = rv[e] != 0.0f ? div_by_recip(a0, sv[e], rv[e])
-                                               : a0 / sv[e];
-                const float q1 = rv[e + 1] != 0.0f
-                                     ? div_by_recip(a1, sv[e + 1], rv[e + 1])
-                                     : a1 / sv[e + 1];
+                float q0, q1;
+                if (fast) {
+                  q0 = div_by_recip(a0, sv[e], rv[e]);
+                  q1 = div_by_recip(a1, sv[e + 1], rv[e + 1]);
+                } else {
+                  q0 = rv[e] != 0.0f ? div_by_recip(a0, sv[e], rv[e])
+                                     : a0 / sv[e];
+                  q1 = rv[e + 1] != 0.0f
+                           ? div_by_recip(a1, sv[e + 1], rv[e + 1])
+                           : a1 / sv[e + 1];
+                }
                 const __nv_bfloat162 y2 =
                     __floats2bfloat162_rn(q0 * wsv, q1 * wsv);
                 __nv_bfloat16 *o = static_cast<__nv_bfloat16 *>(g.out) +
