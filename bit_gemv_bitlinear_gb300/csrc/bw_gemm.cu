@@ -1,6 +1,7 @@
 // bw_gemm.cu -- the W2A8 product for prefill-sized batches of tokens (a few
 // hundred to a few thousand) on the fifth-generation tensor cores, with
-// 256-token tiles so that every decoded weight serves 256 tokens.
+// 256-token tiles so that every decoded weight serves 256 tokens (and
+// 64- or 128-token tiles for smaller batches).
 //
 // Source: "BitNet GPU 推理框架：从零构建 W2A8 的 2-bit 大模型 CUDA GEMV 内核",
 // §一 (the model runs prefill and decode as separate paths; this is the
@@ -15,18 +16,19 @@
 //    the weight decode, each scaled by 4^-slot (below), and the token sums
 //    sum_k x.
 //  * gemm_kernel: CTA (b, t) owns weight rows [128 b, 128 b + 128) and
-//    tokens [256 t, 256 t + 256), over all K in stages of 128 k:
+//    tokens [T t, T t + T), over all K in stages of 128 k; T = 256 tokens
+//    (64 or 128 for calls of at most 64 or 128 tokens):
 //     - one producer thread streams each stage's weights (one 2-D box of 16
 //       row groups x 256 bytes, issued before the dependency wait since the
-//       weights are static) and tokens (two boxes of 64 k x 256 tokens,
+//       weights are static) and tokens (two boxes of 64 k x T tokens,
 //       128-byte swizzled by the copy itself: the layout the MMA reads) into
 //       shared-memory rings with tiled TMA;
 //     - 8 decode warps, two sets of 4 for the even and the odd stages
 //       (thread = weight row = tensor-memory lane), turn the 2-bit codes into
 //       fp16 and store them in tensor memory: the MMA's A operand;
-//     - one elected thread issues 8 tcgen05.mma (M = 128, N = 256, K = 16)
-//       per stage into a 128 x 256 fp32 accumulator in tensor memory;
-//       columns 0..255 hold it, 4 A stages of 64 columns the rest of 512;
+//     - one elected thread issues 8 tcgen05.mma (M = 128, N = T, K = 16)
+//       per stage into a 128 x T fp32 accumulator in tensor memory;
+//       columns 0..T-1 hold it, then 4 A stages of 64 columns;
 //     - the decode warps then read the accumulator back (tcgen05.ld) and
 //       store acc = 2^24 D - sum_k x as int32, or the bf16 output; the
 //       division by s is a product with 1 / s corrected to the IEEE
@@ -44,51 +46,60 @@ namespace bw {
 namespace {
 
 constexpr int kGmRowGroups = 16;                 // 128 weight rows per CTA
-constexpr int kGmTokens = 256;                   // tokens per CTA (MMA N)
 constexpr int kGmStageChunks = 2;                // 128 k per stage
 constexpr uint32_t kGmWStageBytes =
     kGmRowGroups * kGmStageChunks * kGroupChunkBytes;  // 4 KB
-constexpr uint32_t kGmSliceBytes = kGmTokens * 128;    // 64 k x 256 tokens
-constexpr uint32_t kGmBStageBytes = kGmStageChunks * kGmSliceBytes;  // 64 KB
-constexpr int kGmWStages = 4;
-constexpr int kGmBStages = 3;
 constexpr int kGmAStages = 4;
 constexpr uint32_t kGmACols = kGmStageChunks * 32;  // fp16 pairs of a stage
-constexpr uint32_t kGmAccCols = kGmTokens;          // fp32, from column 0
 constexpr uint32_t kGmTmemCols = 512;
-static_assert(kGmAccCols + kGmAStages * kGmACols <= kGmTmemCols, "tensor memory");
 // A and W slots are each used by one stage parity (one decode set).
-static_assert(kGmAStages % 2 == 0 && kGmWStages % 2 == 0, "stage sets");
+static_assert(kGmAStages % 2 == 0, "stage sets");
 
 constexpr int kGmSetWarps = 4;
 constexpr int kGmDecodeWarps = 2 * kGmSetWarps;   // warps 0..7
 constexpr int kGmProducerWarp = kGmDecodeWarps;   // 8
 constexpr int kGmMmaWarp = kGmProducerWarp + 1;   // 9
 constexpr int kGmThreads = (kGmMmaWarp + 1) * 32; // 320
+constexpr int kGmMaxTokens = 256;                 // per-token arrays
 
-// Barrier indices.
-constexpr int kBarFullW = 0;
-constexpr int kBarEmptyW = kBarFullW + kGmWStages;
-constexpr int kBarFullB = kBarEmptyW + kGmWStages;
-constexpr int kBarEmptyB = kBarFullB + kGmBStages;
-constexpr int kBarFullA = kBarEmptyB + kGmBStages;
-constexpr int kBarDoneA = kBarFullA + kGmAStages;
-constexpr int kBarAcc = kBarDoneA + kGmAStages;
-constexpr int kGmBars = kBarAcc + 1;
-
-// Shared memory (offsets from a 1024-byte aligned base; the token stages
-// first, 1024-aligned as the swizzle requires).
-constexpr uint32_t kSmB = 0;
-constexpr uint32_t kSmW = kSmB + kGmBStages * kGmBStageBytes;
-constexpr uint32_t kSmS = kSmW + kGmWStages * kGmWStageBytes;  // fp32 [256]
-constexpr uint32_t kSmR = kSmS + kGmTokens * 4;                // fp32 [256]
-constexpr uint32_t kSmSx = kSmR + kGmTokens * 4;               // fp32 [256]
-constexpr uint32_t kSmWs = kSmSx + kGmTokens * 4;              // fp32 [8]
-constexpr uint32_t kSmTmem = kSmWs + BW_MAX_WS * 4;
-constexpr uint32_t kSmBars = (kSmTmem + 16 + 7) / 8 * 8;
-constexpr uint32_t kSmTotal = kSmBars + kGmBars * 8;
-constexpr uint32_t kGmSmem = kSmTotal + 1024;  // slack to align the base
-static_assert(kGmSmem <= 227u * 1024u, "shared memory");
+// Per token tile: T tokens per CTA (the MMA's N: 64, 128 or 256), the ring
+// depths, barrier indices and shared memory.  Small tiles finish a stage's
+// MMAs quickly, so their weight ring is deeper: the weights come from HBM,
+// and the bytes in flight per SM must cover its latency.
+template <int T>
+struct GmCfg {
+  static constexpr uint32_t kSliceBytes = T * 128;  // 64 k x T tokens
+  static constexpr uint32_t kBStageBytes = kGmStageChunks * kSliceBytes;
+  static constexpr int kBStages = T == 256 ? 3 : (T == 128 ? 5 : 6);
+  static constexpr int kWStages = T == 256 ? 6 : (T == 128 ? 8 : 16);
+  static_assert(kWStages % 2 == 0, "stage sets");
+  static constexpr uint32_t kAccCols = T;  // fp32, from column 0
+  static_assert(T == 64 || T == 128 || T == 256, "token tile");
+  static_assert(kAccCols + kGmAStages * kGmACols <= kGmTmemCols,
+                "tensor memory");
+  // Barrier indices.
+  static constexpr int kBarFullW = 0;
+  static constexpr int kBarEmptyW = kBarFullW + kWStages;
+  static constexpr int kBarFullB = kBarEmptyW + kWStages;
+  static constexpr int kBarEmptyB = kBarFullB + kBStages;
+  static constexpr int kBarFullA = kBarEmptyB + kBStages;
+  static constexpr int kBarDoneA = kBarFullA + kGmAStages;
+  static constexpr int kBarAcc = kBarDoneA + kGmAStages;
+  static constexpr int kBars = kBarAcc + 1;
+  // Shared memory (offsets from a 1024-byte aligned base; the token
+  // stages first, 1024-aligned as the swizzle requires).
+  static constexpr uint32_t kSmB = 0;
+  static constexpr uint32_t kSmW = kSmB + kBStages * kBStageBytes;
+  static constexpr uint32_t kSmS = kSmW + kWStages * kGmWStageBytes;  // fp32 [256]
+  static constexpr uint32_t kSmR = kSmS + kGmMaxTokens * 4;             // fp32 [256]
+  static constexpr uint32_t kSmSx = kSmR + kGmMaxTokens * 4;            // fp32 [256]
+  static constexpr uint32_t kSmWs = kSmSx + kGmMaxTokens * 4;           // fp32 [8]
+  static constexpr uint32_t kSmTmem = kSmWs + BW_MAX_WS * 4;
+  static constexpr uint32_t kSmBars = (kSmTmem + 16 + 7) / 8 * 8;
+  static constexpr uint32_t kSmTotal = kSmBars + kBars * 8;
+  static constexpr uint32_t kSmem = kSmTotal + 1024;  // slack for the base
+  static_assert(kSmem <= 227u * 1024u, "shared memory");
+};
 
 // 32 consecutive accumulator columns of this warp's 32 lanes, loaded and
 // waited for in one asm statement.
@@ -190,11 +201,25 @@ tok_fp16_kernel(const int8_t *x, int x_ld, int K, int Kp, __half *xb,
 // [128 b, 128 b + 128) of the M x N product (rows past M or N are not
 // stored).  wmap: the device weight layout; bmap: the fp16 tokens
 // (tok_fp16_kernel), Kp = 64 C columns; sx: the token sums.
-template <bool ACC>
+template <bool ACC, int T>
 __global__ void __launch_bounds__(kGmThreads, 1)
 gemm_kernel(const __grid_constant__ CUtensorMap wmap,
             const __grid_constant__ CUtensorMap bmap, const GemvArgs g,
             const int *sx, int M, unsigned int *err) {
+  using Cfg = GmCfg<T>;
+  constexpr int kGmTokens = T;
+  constexpr uint32_t kGmSliceBytes = Cfg::kSliceBytes;
+  constexpr uint32_t kGmBStageBytes = Cfg::kBStageBytes;
+  constexpr int kGmBStages = Cfg::kBStages;
+  constexpr int kGmWStages = Cfg::kWStages;
+  constexpr uint32_t kGmAccCols = Cfg::kAccCols;
+  constexpr int kBarFullW = Cfg::kBarFullW, kBarEmptyW = Cfg::kBarEmptyW;
+  constexpr int kBarFullB = Cfg::kBarFullB, kBarEmptyB = Cfg::kBarEmptyB;
+  constexpr int kBarFullA = Cfg::kBarFullA, kBarDoneA = Cfg::kBarDoneA;
+  constexpr int kBarAcc = Cfg::kBarAcc;
+  constexpr uint32_t kSmB = Cfg::kSmB, kSmW = Cfg::kSmW, kSmS = Cfg::kSmS;
+  constexpr uint32_t kSmR = Cfg::kSmR, kSmSx = Cfg::kSmSx, kSmWs = Cfg::kSmWs;
+  constexpr uint32_t kSmTmem = Cfg::kSmTmem, kSmBars = Cfg::kSmBars;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t *smem = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -389,8 +414,8 @@ gemm_kernel(const __grid_constant__ CUtensorMap wmap,
     }
     if (!ok && lane == 0) atomicOr(err, 4u);
 
-    // ---- epilogue: warp (q, h) takes accumulator columns [128 h, 128 h +
-    // 128) (tokens) of weight rows 32 q .. 32 q + 31 ----
+    // ---- epilogue: warp (q, h) takes accumulator columns [T/2 h,
+    // T/2 (h + 1)) (tokens) of weight rows 32 q .. 32 q + 31 ----
     pdl_wait();
     {
       // Per token: -sum_k x (as fp32, exact: |sum| < 2^22; +0 for a zero
@@ -422,7 +447,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap wmap,
       for (int i = 1; i < BW_MAX_WS; ++i)
         if (i < g.seg.n_ws && n >= g.seg.bounds[i]) sg = i;
       const float wsv = ws_sm[sg];
-      for (int j0 = 128 * h; j0 < 128 * h + 128; j0 += 32) {
+      for (int j0 = (T / 2) * h; j0 < (T / 2) * (h + 1); j0 += 32) {
         if (m0 + j0 >= M) break;  // warp-uniform
         uint32_t d[32];
         tmem_ld32(t_lane + uint32_t(j0), d);  // whole warp
@@ -498,10 +523,11 @@ gemm_kernel(const __grid_constant__ CUtensorMap wmap,
 
 size_t align256(size_t b) { return (b + 255) / 256 * 256; }
 
-template <bool ACC>
+template <bool ACC, int T>
 cudaError_t launch_gemm_t(const GemvArgs &g, int M, void *workspace,
                           cudaStream_t stream) {
   static bool configured[64];
+  using Cfg = GmCfg<T>;
   unsigned int *err = device_error_word();
   if (!err) return cudaErrorInvalidSymbol;
   const int Kp = g.chunks * 64;
@@ -522,27 +548,27 @@ cudaError_t launch_gemm_t(const GemvArgs &g, int M, void *workspace,
                                      Kp, xb, sx);
   if (e != cudaSuccess) return e;
 
-  auto kernel = gemm_kernel<ACC>;
+  auto kernel = gemm_kernel<ACC, T>;
   int64_t resident = 0;
-  e = resident_ctas(kernel, configured, kGmThreads, kGmSmem, &resident);
+  e = resident_ctas(kernel, configured, kGmThreads, Cfg::kSmem, &resident);
   if (e != cudaSuccess) return e;
   // Weights: per row group, C chunks of 128 bytes as 16 C uint64; a box is
   // one stage of 16 groups.  Tokens: M rows of Kp fp16; a box is 64 k (128
-  // bytes, swizzled) of 256 rows (rows past M read as zero).
+  // bytes, swizzled) of T rows (rows past M read as zero).
   CUtensorMap wmap, bmap;
   if (!encode_2d(&wmap, CU_TENSOR_MAP_DATA_TYPE_UINT64, g.w,
                  uint64_t(g.chunks) * (kGroupChunkBytes / 8),
                  uint64_t(g.n_groups), uint64_t(g.chunks) * kGroupChunkBytes,
                  kGmStageChunks * (kGroupChunkBytes / 8), kGmRowGroups) ||
       !encode_2d(&bmap, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, xb, uint64_t(Kp),
-                 uint64_t(M), uint64_t(Kp) * 2, 64, kGmTokens,
+                 uint64_t(M), uint64_t(Kp) * 2, 64, T,
                  CU_TENSOR_MAP_SWIZZLE_128B))
     return cudaErrorInvalidValue;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(unsigned((g.n_groups + kGmRowGroups - 1) / kGmRowGroups),
-                     unsigned((M + kGmTokens - 1) / kGmTokens));
+                     unsigned((M + T - 1) / T));
   cfg.blockDim = dim3(kGmThreads);
-  cfg.dynamicSmemBytes = kGmSmem;
+  cfg.dynamicSmemBytes = Cfg::kSmem;
   cfg.stream = stream;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
@@ -556,10 +582,17 @@ size_t gemm_workspace_bytes(int M, int K) {
          align256(size_t(M) * sizeof(int));
 }
 
+// Token tiles of 64 up to 64 tokens, of 128 up to 128, else of 256.
 cudaError_t launch_gemm(const GemvArgs &a, int M, bool acc_out,
                         void *workspace, cudaStream_t stream) {
-  return acc_out ? launch_gemm_t<true>(a, M, workspace, stream)
-                 : launch_gemm_t<false>(a, M, workspace, stream);
+  if (M <= 64)
+    return acc_out ? launch_gemm_t<true, 64>(a, M, workspace, stream)
+                   : launch_gemm_t<false, 64>(a, M, workspace, stream);
+  if (M <= 128)
+    return acc_out ? launch_gemm_t<true, 128>(a, M, workspace, stream)
+                   : launch_gemm_t<false, 128>(a, M, workspace, stream);
+  return acc_out ? launch_gemm_t<true, 256>(a, M, workspace, stream)
+                 : launch_gemm_t<false, 256>(a, M, workspace, stream);
 }
 
 }  // namespace bw

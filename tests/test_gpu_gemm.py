@@ -63,12 +63,14 @@ def check(bw, M, N, K, seed, rows=None, extremes=True):
 
 @pytest.mark.parametrize("M,N,K", [
     (1, 8, 64), (7, 100, 300), (129, 1000, 1028), (256, 2560, 2560),
-    (257, 77, 2564), (300, 130, 16384), (511, 513, 640), (64, 2560, 6912)])
+    (257, 77, 2564), (300, 130, 16384), (511, 513, 640), (64, 2560, 6912),
+    (16, 1000, 2560), (100, 777, 1028), (128, 300, 4112)])
 def test_gemm_full_parity(bw, M, N, K):
-    """Every output: one to three 256-token tiles (ragged last tile), ragged
-    weight-row tiles (N not a multiple of 128), K ending in a one-chunk
-    stage (1028, 2564, 300) or in a partly valid chunk (300, 2564), the
-    largest K (16384: 128 stages through the rings)."""
+    """Every output: 64-token tiles (M <= 64), 128-token tiles (M <= 128),
+    one to three 256-token tiles (ragged last tile), ragged weight-row tiles
+    (N not a multiple of 128), K ending in a one-chunk stage (1028, 2564,
+    300, 4112) or in a partly valid chunk (300, 2564), the largest K (16384:
+    128 stages through the rings)."""
     check(bw, M, N, K, synth.base_seed(15, M % 64 + K % 7))
 
 
