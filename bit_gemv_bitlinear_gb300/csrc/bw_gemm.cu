@@ -63,9 +63,9 @@ constexpr int kGmThreads = (kGmMmaWarp + 1) * 32; // 320
 constexpr int kGmMaxTokens = 256;                 // per-token arrays
 
 // Per token tile: T tokens per CTA (the MMA's N: 64, 128 or 256), the ring
-// depths, barrier indices and shared memory.  Small tiles finish a stage's
-// MMAs quickly, so their weight ring is deeper: the weights come from HBM,
-// and the bytes in flight per SM must cover its latency.
+// depths, barrier indices and shared memory.  The smaller token stages of
+// the small tiles leave room for deeper rings (more weight bytes in flight
+// against HBM latency).
 template <int T>
 struct GmCfg {
   static constexpr uint32_t kSliceBytes = T * 128;  // 64 k x T tokens
