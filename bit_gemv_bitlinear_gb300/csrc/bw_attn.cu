@@ -26,14 +26,16 @@
 //    ceil(L / 64)) of them, the others are empty.  A context of at most 128
 //    tokens takes one split, finished by that CTA alone straight from its
 //    shared memory: no partial, fence, counter or merge.
-//  * The rows of a split are contiguous in the cache, so two bulk copies
-//    (cp.async.bulk) bring its keys and its values into shared memory, up
-//    to 80 KB in flight per CTA, while the CTA rotates its queries; the
-//    keys complete on their own mbarrier, so the scores start before the
-//    values have landed.  Every wait is bounded.
-//  * A half-warp takes one position: lane l holds head dims 8 (l % 16) ..
-//    8 (l % 16) + 7 of a 256-byte row; the G dot products are summed over
-//    the half-warp with four shuffles each.
+//  * The rows of a split are contiguous in the cache: tiled copies (TMA, one
+//    box per 32 rows and 64 dims, 128-byte swizzled) bring its keys and its
+//    values into shared memory while the CTA rotates its queries; the keys
+//    complete on their own mbarrier, so the scores start before the values
+//    have landed.  Every wait is bounded.
+//  * Scores and weighted values run on the tensor cores (mma.sync, bf16
+//    operands from ldmatrix, fp32 accumulation): S = K q^T per 16-position
+//    tile with the fp32 queries as a bf16 pair q_hi + q_lo, and out^T =
+//    V^T P with the fp32 exp weights as a bf16 pair likewise, so both
+//    products keep about 16 bits beyond one bf16 rounding.
 //  * Inside a CTA the softmax has two passes over the scores in shared
 //    memory (largest score, then exp and sum); the CTA writes its largest
 //    scores m, exp sums l and unnormalised outputs to the workspace.
@@ -45,9 +47,13 @@
 //    counter back to zero.
 //  * The CTA whose split holds p rotates the new key, rounds it to bf16 and
 //    puts key and value into its staged rows and into row p of the cache.
-// Arithmetic: fp32 throughout (fp32 angles p * f_i with f_i =
-// theta^(-2i/D) rounded to fp32 on the host, sincosf, expf), bf16 cache.
-#include "bw_pipe.cuh"
+// Arithmetic: fp32 (fp32 angles p * f_i with f_i = theta^(-2i/D) rounded
+// to fp32 on the host, sincosf, expf, the softmax and the merges), bf16
+// cache; the two contractions on the tensor cores take their fp32 operand
+// (queries, exp weights) as a sum of two bf16 values and accumulate in fp32.
+// The caches are read through tensor maps (encoded per launch: 2-D, Hkv S
+// rows of D bf16).
+#include "bw_tc.cuh"
 
 namespace bw {
 namespace {
@@ -129,13 +135,48 @@ struct AttnSmem {
 static_assert((2 * kAttnMaxSplits * 8 + 8) * 4 <= 2 * kAttnChunk * kAttnD * 2,
               "merge scratch fits in the staging rows");
 
-__device__ __forceinline__ void bf16x8_to_f32(uint4 raw, float (&v)[8]) {
-  const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    v[2 * i] = __uint_as_float(w[i] << 16);
-    v[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
-  }
+// Staged key and value rows: blocks of 32 rows, each two boxes (dims 0..63,
+// 64..127) of 32 rows x 128 bytes in the 128-byte swizzle of the tiled copy:
+// the 16-byte piece c of row r of a box is stored at piece c ^ (r mod 8).
+constexpr int kAttnBlockRows = 32;
+constexpr uint32_t kAttnBlockBytes = kAttnBlockRows * kAttnD * 2;  // 8 KB
+__device__ __forceinline__ uint32_t staged_offset(int row, int dim) {
+  const int r = row & (kAttnBlockRows - 1);
+  return uint32_t(row / kAttnBlockRows) * kAttnBlockBytes +
+         uint32_t(dim >> 6) * (kAttnBlockBytes / 2) + uint32_t(r) * 128u +
+         ((uint32_t((dim & 63) >> 3) ^ uint32_t(r & 7)) << 4) +
+         uint32_t(dim & 7) * 2u;
+}
+
+// Four 8x8 bf16 matrices from shared memory (lane l gives the row address
+// of matrix l / 8), as mma fragments; .trans: transposed.
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t (&r)[4]) {
+  asm volatile(
+      "ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+      : "r"(addr)
+      : "memory");
+}
+__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t (&r)[4]) {
+  asm volatile(
+      "ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+      : "r"(addr)
+      : "memory");
+}
+
+// C (16 x 8, fp32) += A (16 x 16, bf16, row-major) B (16 x 8, bf16).
+__device__ __forceinline__ void mma_bf16(float (&c)[4], const uint32_t (&a)[4],
+                                         uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 "
+      "{%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
+      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ uint32_t bf162_bits(__nv_bfloat162 v) {
+  return *reinterpret_cast<const uint32_t *>(&v);
 }
 
 // Max (kMax) or sum over the CTA of G values per thread, in a fixed order;
@@ -165,35 +206,6 @@ __device__ __forceinline__ void cta_reduce(float (&v)[G], float *red) {
   }
   // No trailing barrier: the next writer of `red` is the next reduction,
   // whose first barrier comes after every thread has read these values.
-}
-
-// Sums V values per lane (V a power of 2, at most 16) over each half-warp,
-// in the butterfly order of xor offsets 8, 4, 2, 1, spreading the results
-// over the lanes: in a round with two or more values left, a lane keeps one
-// half of them and adds the partner's copy of that half (the partner keeps
-// the other half), so the V sums cost V - 1 shuffles instead of 4 V.  Every
-// sum is the same pairwise tree as the plain butterfly's, so the results are
-// bit-identical to it.  On return v[0] holds sum `idx`, the same in the
-// lanes that differ only in the bits below 16 / V.
-template <int N, int V, int O>
-__device__ __forceinline__ void spread_sum(float (&v)[N], int hl, int &idx) {
-  if constexpr (O >= 1) {
-    if constexpr (V >= 2) {
-      constexpr int kHalf = V / 2;
-      const bool up = (hl & O) != 0;
-#pragma unroll
-      for (int i = 0; i < kHalf; ++i) {
-        const float keep = up ? v[i + kHalf] : v[i];
-        const float send = up ? v[i] : v[i + kHalf];
-        v[i] = keep + __shfl_xor_sync(0xffffffffu, send, O);
-      }
-      if (up) idx += kHalf;
-      spread_sum<N, kHalf, O / 2>(v, hl, idx);
-    } else {
-      v[0] += __shfl_xor_sync(0xffffffffu, v[0], O);
-      spread_sum<N, 1, O / 2>(v, hl, idx);
-    }
-  }
 }
 
 // Sum and max of one value per thread over the CTA in one exchange (the
@@ -254,7 +266,7 @@ struct QkvPre {
 };
 
 // The partial of one split, positions j0 .. j0 + n - 1 of KV head g (n >= 1,
-// n <= kChunk): the two bulk copies of its key and value rows, the rotated
+// n <= kChunk): the tiled copies of its key and value rows, the rotated
 // queries, the append of the new token when the split holds p, the scores,
 // the split's softmax (largest score m and exp sum l per query head, the
 // same in every thread) and the unnormalised output per warp in the wacc
@@ -264,32 +276,42 @@ struct QkvPre {
 // CTA then has no partial).
 template <int G, int kChunk>
 __device__ __forceinline__ bool attend_split(const AttnArgs &a,
+                                             const CUtensorMap *kmap,
+                                             const CUtensorMap *vmap,
                                              const QkvPre<G> &pre, int g,
                                              int p, int j0, int n,
                                              uint8_t *smem, uint64_t *bar,
                                              float (&m)[G], float (&l)[G]) {
   using L = AttnSmem<G, kChunk>;
-  __nv_bfloat16 *kst = reinterpret_cast<__nv_bfloat16 *>(smem + L::kK);
-  __nv_bfloat16 *vst = reinterpret_cast<__nv_bfloat16 *>(smem + L::kV);
+  uint8_t *kst = smem + L::kK;
+  uint8_t *vst = smem + L::kV;
   float2 *cs = reinterpret_cast<float2 *>(smem + L::kCs);
   float *q_sm = reinterpret_cast<float *>(smem + L::kQ);
   float *sc = reinterpret_cast<float *>(smem + L::kSc);
   float *wacc = reinterpret_cast<float *>(smem + L::kWacc);
   float *red = reinterpret_cast<float *>(smem + L::kRed);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int hl = lane & 15, half = lane >> 4;
   constexpr int D = kAttnD;
   const size_t head_row = size_t(g) * a.S;  // row 0 of KV head g
-    // ---- the split's key rows and value rows: one bulk copy each ----
+  const int nb = (n + kAttnBlockRows - 1) / kAttnBlockRows;
+  const int n_mt = (n + 15) / 16;           // 16-position tiles
+  // ---- the split's key rows and value rows: 32-row blocks of two swizzled
+  // boxes of 64 dims each (tiled TMA) ----
   if (tid == 0) {
     pipe::mbar_init(&bar[0], 1);
     pipe::mbar_init(&bar[1], 1);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-    const uint32_t bytes = uint32_t(n) * L::kRowBytes;
-    pipe::mbar_arrive_expect_tx(&bar[0], bytes);
-    pipe::bulk_copy_g2s(kst, a.kc + (head_row + j0) * D, bytes, &bar[0]);
-    pipe::mbar_arrive_expect_tx(&bar[1], bytes);
-    pipe::bulk_copy_g2s(vst, a.vc + (head_row + j0) * D, bytes, &bar[1]);
+    pipe::mbar_arrive_expect_tx(&bar[0], uint32_t(nb) * kAttnBlockBytes);
+    pipe::mbar_arrive_expect_tx(&bar[1], uint32_t(nb) * kAttnBlockBytes);
+    for (int b = 0; b < nb; ++b)
+#pragma unroll
+      for (int hh = 0; hh < 2; ++hh) {
+        const int row = int(head_row) + j0 + b * kAttnBlockRows;
+        tma_load_2d(kst + b * kAttnBlockBytes + hh * (kAttnBlockBytes / 2),
+                    kmap, hh * 64, row, &bar[0]);
+        tma_load_2d(vst + b * kAttnBlockBytes + hh * (kAttnBlockBytes / 2),
+                    vmap, hh * 64, row, &bar[1]);
+      }
   }
   // ---- RoPE of the queries meanwhile ----
   if (tid < kAttnPairs) {
@@ -322,131 +344,160 @@ __device__ __forceinline__ bool attend_split(const AttnArgs &a,
     __syncthreads();
     return false;
   }
+  // ---- the new token's rotated key: staged and appended (the key copy has
+  // landed, so neither write can be overwritten or read by it) ----
+  if (has_p && tid < kAttnPairs) {
+    const int i = tid;
+    const float x0 = __bfloat162float(pre.k[0]);
+    const float x1 = __bfloat162float(pre.k[1]);
+    const float2 r = cs[i];
+    const __nv_bfloat162 k2 = __halves2bfloat162(
+        __float2bfloat16_rn(x0 * r.x - x1 * r.y),
+        __float2bfloat16_rn(x0 * r.y + x1 * r.x));
+    *reinterpret_cast<__nv_bfloat162 *>(kst + staged_offset(p - j0, 2 * i)) = k2;
+    reinterpret_cast<__nv_bfloat162 *>(a.kc + (head_row + p) * D)[i] = k2;
+  }
+  __syncthreads();
+
+  // ---- scores ----
   {
-    // ---- the new token's rotated key: staged and appended (the key
-    // copy has landed, so neither write can be overwritten or read by it)
-    if (has_p && tid < kAttnPairs) {
-      const int i = tid;
-      const float x0 = __bfloat162float(pre.k[0]);
-      const float x1 = __bfloat162float(pre.k[1]);
-      const float2 r = cs[i];
-      const __nv_bfloat162 k2 = __halves2bfloat162(
-          __float2bfloat16_rn(x0 * r.x - x1 * r.y),
-          __float2bfloat16_rn(x0 * r.y + x1 * r.x));
-      reinterpret_cast<__nv_bfloat162 *>(kst + size_t(p - j0) * D)[i] = k2;
-      reinterpret_cast<__nv_bfloat162 *>(a.kc + (head_row + p) * D)[i] = k2;
-    }
-    __syncthreads();
-
-    // ---- scores: a half-warp per position, 8 dims per lane ----
-    float qr[G][8];
+    // Tensor cores: S = K q^T per 16-position tile (the A operand, ldmatrix
+    // from the swizzled rows) against the G rotated queries (the B operand,
+    // heads padded to 8), bf16 with fp32 accumulation; the fp32 queries
+    // enter as q_hi + q_lo (two bf16), so the products keep ~16 more bits
+    // than q rounded once.
+    const int fg = lane >> 2, ft = lane & 3;  // fragment row / column pair
+    uint32_t qh[8][2], ql[8][2];
 #pragma unroll
-    for (int h = 0; h < G; ++h)
+    for (int kk = 0; kk < 8; ++kk)
 #pragma unroll
-      for (int e = 0; e < 8; ++e) qr[h][e] = q_sm[h * D + 8 * hl + e];
-    // Two positions per half-warp and step; the 2 G dot products of a lane
-    // are summed over the half-warp together (spread_sum), and the lane
-    // that holds sum (r, h) stores it.
-    constexpr int kV = 2 * G;
-    constexpr int kLow = 16 / kV - 1;  // lanes below this hold copies
-    for (int jb = 4 * warp; jb < n; jb += 4 * kAttnWarps) {  // warp-uniform
-      float d[kV];
-#pragma unroll
-      for (int r = 0; r < 2; ++r) {
-        const int jj = jb + 2 * r + half;
-        float kv[8];
-        bf16x8_to_f32(jj < n ? *reinterpret_cast<const uint4 *>(
-                                   kst + size_t(jj) * D + 8 * hl)
-                             : make_uint4(0u, 0u, 0u, 0u),
-                      kv);
-#pragma unroll
-        for (int h = 0; h < G; ++h) {
-          float t = 0.0f;
-#pragma unroll
-          for (int e = 0; e < 8; ++e) t = fmaf(qr[h][e], kv[e], t);
-          d[r * G + h] = t;
+      for (int u = 0; u < 2; ++u) {
+        float x0 = 0.0f, x1 = 0.0f;
+        if (fg < G) {
+          const int d = 16 * kk + 2 * ft + 8 * u;
+          x0 = q_sm[fg * D + d];
+          x1 = q_sm[fg * D + d + 1];
         }
+        const __nv_bfloat162 hi = __floats2bfloat162_rn(x0, x1);
+        const __nv_bfloat162 lo = __floats2bfloat162_rn(
+            x0 - __low2float(hi), x1 - __high2float(hi));
+        qh[kk][u] = bf162_bits(hi);
+        ql[kk][u] = bf162_bits(lo);
       }
-      int idx = 0;
-      spread_sum<kV, kV, 8>(d, hl, idx);  // in half
-      const int jj = jb + 2 * (idx / G) + half;
-      if ((hl & kLow) == 0 && jj < n) sc[jj * G + idx % G] = d[0] * a.inv_sqrt_d;
+    for (int mt = warp; mt < n_mt; mt += kAttnWarps) {
+      // four independent accumulators (q_hi / q_lo, even / odd k-steps),
+      // summed at the end: short dependency chains
+      float c[4][4] = {};
+      const int row = 16 * mt + (lane & 15);
+#pragma unroll
+      for (int kk = 0; kk < 8; ++kk) {
+        uint32_t fa[4];
+        ldsm_x4(pipe::smem_addr(kst + staged_offset(row, 16 * kk + 8 * (lane >> 4))),
+                fa);
+        mma_bf16(c[kk & 1], fa, qh[kk][0], qh[kk][1]);
+        mma_bf16(c[2 + (kk & 1)], fa, ql[kk][0], ql[kk][1]);
+      }
+      // c0, c1: position 16 mt + fg, heads 2 ft, 2 ft + 1; c2, c3: + 8
+#pragma unroll
+      for (int v = 0; v < 4; ++v) {
+        const int jj = 16 * mt + fg + 8 * (v >> 1), h = 2 * ft + (v & 1);
+        const float t = (c[0][v] + c[1][v]) + (c[2][v] + c[3][v]);
+        if (h < G && jj < n) sc[jj * G + h] = t * a.inv_sqrt_d;
+      }
     }
-    __syncthreads();
+  }
+  __syncthreads();
 
-    // ---- softmax of the split: largest score, then exp and sum ----
+  // ---- softmax of the split: largest score, then exp and sum ----
 #pragma unroll
-    for (int h = 0; h < G; ++h) m[h] = -INFINITY;
-    for (int jj = tid; jj < n; jj += kAttnThreads)
+  for (int h = 0; h < G; ++h) m[h] = -INFINITY;
+  for (int jj = tid; jj < n; jj += kAttnThreads)
 #pragma unroll
-      for (int h = 0; h < G; ++h) m[h] = fmaxf(m[h], sc[jj * G + h]);
-    cta_reduce<G, true>(m, red);
+    for (int h = 0; h < G; ++h) m[h] = fmaxf(m[h], sc[jj * G + h]);
+  cta_reduce<G, true>(m, red);
 #pragma unroll
-    for (int h = 0; h < G; ++h) l[h] = 0.0f;
-    for (int jj = tid; jj < n; jj += kAttnThreads)
+  for (int h = 0; h < G; ++h) l[h] = 0.0f;
+  for (int jj = tid; jj < n; jj += kAttnThreads)
 #pragma unroll
-      for (int h = 0; h < G; ++h) {
-        const float e = expf(sc[jj * G + h] - m[h]);
-        sc[jj * G + h] = e;
-        l[h] += e;
-      }
-    cta_reduce<G, false>(l, red);  // its barriers also publish sc
+    for (int h = 0; h < G; ++h) {
+      const float e = expf(sc[jj * G + h] - m[h]);
+      sc[jj * G + h] = e;
+      l[h] += e;
+    }
+  cta_reduce<G, false>(l, red);  // its barriers also publish sc
 
-    // ---- weighted values (the value copy landed during the scores) ----
-    if (!__syncthreads_and(pipe::mbar_wait(&bar[1], 0u))) {
-      if (tid == 0) {
-        atomicOr(a.err, 4u);
-        if (!pipe::mbar_wait(&bar[1], 0u)) atomicOr(a.err, 2u);
-      }
-      __syncthreads();
+  // ---- weighted values (the value copy landed during the scores) ----
+  if (!__syncthreads_and(pipe::mbar_wait(&bar[1], 0u))) {
+    if (tid == 0) {
+      atomicOr(a.err, 4u);
+      if (!pipe::mbar_wait(&bar[1], 0u)) atomicOr(a.err, 2u);
     }
-    if (has_p && tid < kAttnPairs) {  // the new token's value
-      const int i = tid;
-      const __nv_bfloat162 v2 = __halves2bfloat162(pre.v[0], pre.v[1]);
-      reinterpret_cast<__nv_bfloat162 *>(vst + size_t(p - j0) * D)[i] = v2;
-      reinterpret_cast<__nv_bfloat162 *>(a.vc + (head_row + p) * D)[i] = v2;
-    }
-    __syncthreads();
-    float acc[G][8];
-#pragma unroll
-    for (int h = 0; h < G; ++h)
-#pragma unroll
-      for (int e = 0; e < 8; ++e) acc[h][e] = 0.0f;
-    for (int jb = 2 * warp; jb < n; jb += 2 * kAttnWarps) {
-      const int jj = jb + half;
-      if (jj < n) {
-        float vv[8];
-        bf16x8_to_f32(*reinterpret_cast<const uint4 *>(
-                          vst + size_t(jj) * D + 8 * hl),
-                      vv);
-#pragma unroll
-        for (int h = 0; h < G; ++h) {
-          const float w = sc[jj * G + h];
-#pragma unroll
-          for (int e = 0; e < 8; ++e) acc[h][e] = fmaf(w, vv[e], acc[h][e]);
-        }
-      }
-    }
-#pragma unroll
-    for (int h = 0; h < G; ++h)
-#pragma unroll
-      for (int e = 0; e < 8; ++e)
-        acc[h][e] += __shfl_xor_sync(0xffffffffu, acc[h][e], 16);
-    if (half == 0)
-#pragma unroll
-      for (int h = 0; h < G; ++h)
-#pragma unroll
-        for (int e = 0; e < 8; ++e)
-          wacc[(warp * G + h) * D + 8 * hl + e] = acc[h][e];
     __syncthreads();
   }
+  // Rows n .. 16 ceil(n / 16) - 1 enter the products with weight 0; they
+  // hold other positions (or rows not yet written), so they are zeroed: a
+  // non-finite value there would not vanish.
+  for (int e = tid; e < (16 * n_mt - n) * 16; e += kAttnThreads) {
+    const int row = n + e / 16, q16 = e & 15;  // 16-byte pieces of the row
+    *reinterpret_cast<uint4 *>(vst + staged_offset(row, 8 * q16)) =
+        make_uint4(0u, 0u, 0u, 0u);
+  }
+  if (has_p && tid < kAttnPairs) {  // the new token's value
+    const int i = tid;
+    const __nv_bfloat162 v2 = __halves2bfloat162(pre.v[0], pre.v[1]);
+    *reinterpret_cast<__nv_bfloat162 *>(vst + staged_offset(p - j0, 2 * i)) = v2;
+    reinterpret_cast<__nv_bfloat162 *>(a.vc + (head_row + p) * D)[i] = v2;
+  }
+  __syncthreads();
+  {
+    // Tensor cores: out^T = V^T P.  Warp w owns dims 16 w .. 16 w + 15 (the
+    // A operand: V^T, ldmatrix.trans from the swizzled rows) over all
+    // positions, 16 per step (the B operand: the exp weights, heads padded
+    // to 8, as p_hi + p_lo); the result is the split's whole output for its
+    // dims, written to the first wacc row (no sum over warps).
+    const int fg = lane >> 2, ft = lane & 3;
+    const int d0 = 16 * warp;
+    float c[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+    float cl[4] = {0.0f, 0.0f, 0.0f, 0.0f};  // the p_lo products
+    for (int ks = 0; ks < n_mt; ++ks) {
+      uint32_t fa[4];
+      ldsm_x4_t(pipe::smem_addr(vst + staged_offset(
+                    16 * ks + ((lane >> 4) << 3) + (lane & 7),
+                    d0 + (((lane >> 3) & 1) << 3))),
+                fa);
+      float w[4];
+#pragma unroll
+      for (int v = 0; v < 4; ++v) {  // P[16 ks + 2 ft + (v & 1) + 8 (v >> 1)][fg]
+        const int jj = 16 * ks + 2 * ft + (v & 1) + 8 * (v >> 1);
+        w[v] = (fg < G && jj < n) ? sc[jj * G + fg] : 0.0f;
+      }
+      const __nv_bfloat162 h01 = __floats2bfloat162_rn(w[0], w[1]);
+      const __nv_bfloat162 h23 = __floats2bfloat162_rn(w[2], w[3]);
+      const __nv_bfloat162 l01 = __floats2bfloat162_rn(
+          w[0] - __low2float(h01), w[1] - __high2float(h01));
+      const __nv_bfloat162 l23 = __floats2bfloat162_rn(
+          w[2] - __low2float(h23), w[3] - __high2float(h23));
+      mma_bf16(c, fa, bf162_bits(h01), bf162_bits(h23));
+      mma_bf16(cl, fa, bf162_bits(l01), bf162_bits(l23));
+    }
+    // c0, c1: dim d0 + fg, heads 2 ft, 2 ft + 1; c2, c3: dim + 8
+#pragma unroll
+    for (int v = 0; v < 4; ++v) {
+      const int h = 2 * ft + (v & 1), d = d0 + fg + 8 * (v >> 1);
+      if (h < G) wacc[h * D + d] = c[v] + cl[v];
+    }
+  }
+  __syncthreads();
   return true;
 }
 
 template <int G>
 __global__ void __launch_bounds__(kAttnThreads)
-attn_decode_kernel(const AttnArgs a) {
-  extern __shared__ __align__(128) uint8_t smem[];
+attn_decode_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap kmap,
+                   const __grid_constant__ CUtensorMap vmap) {
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  // the swizzled staging wants a 1024-byte aligned base
+  uint8_t *smem = smem_raw + ((1024u - (pipe::smem_addr(smem_raw) & 1023u)) & 1023u);
   using L = AttnSmem<G>;
   using P = AttnPart<G>;
   __nv_bfloat16 *kst = reinterpret_cast<__nv_bfloat16 *>(smem + L::kK);
@@ -463,6 +514,12 @@ attn_decode_kernel(const AttnArgs a) {
   const int tid = threadIdx.x;
   constexpr int D = kAttnD;
 
+  if (tid == 0) {  // the copies' descriptors, while the wait lasts
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&kmap))
+                 : "memory");
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&vmap))
+                 : "memory");
+  }
   // Every input may come from the preceding kernel (the q|k|v GEMV, an
   // update of the position, the previous step's append).
   pdl_wait();
@@ -488,7 +545,8 @@ attn_decode_kernel(const AttnArgs a) {
 
   if (n > 0) {
     float m[G], l[G];
-    if (attend_split<G, kAttnChunk>(a, pre, g, p, j0, n, smem, bar, m, l)) {
+    if (attend_split<G, kAttnChunk>(a, &kmap, &vmap, pre, g, p, j0, n, smem,
+                                    bar, m, l)) {
       if (n_eff == 1) {
         // One split holds the whole context: its sums are final.  Write
         // the outputs (and the next RMSNorm's statistics) directly; no
@@ -496,9 +554,7 @@ attn_decode_kernel(const AttnArgs a) {
         float *o = a.out + size_t(g) * G * D;
         float ss = 0.0f, amx = 0.0f;
         for (int e = tid; e < G * D; e += kAttnThreads) {
-          float t = wacc[e];
-#pragma unroll
-          for (int w = 1; w < kAttnWarps; ++w) t += wacc[w * G * D + e];
+          const float t = wacc[e];
           const int h = e / D;
           float lh = l[0];
 #pragma unroll
@@ -518,12 +574,8 @@ attn_decode_kernel(const AttnArgs a) {
         }
         return;
       }
-      for (int e = tid; e < G * D; e += kAttnThreads) {
-        float t = wacc[e];
-#pragma unroll
-        for (int w = 1; w < kAttnWarps; ++w) t += wacc[w * G * D + e];
-        part[e] = t;  // [h][d]: e = h D + d
-      }
+      for (int e = tid; e < G * D; e += kAttnThreads)
+        part[e] = wacc[e];  // [h][d]: e = h D + d
       if (tid < G) {
 #pragma unroll
         for (int h = 0; h < G; ++h)
@@ -688,8 +740,8 @@ attn_decode_kernel(const AttnArgs a) {
 // CTA that has left.
 constexpr int kClMaxCtas = 16;                  // CTAs per KV head
 constexpr int kClChunk = 256;                   // positions per CTA, at most
-constexpr int kClMinChunk = 16;                 // positions per used CTA
-constexpr int kClSoloMax = 64;                  // contexts CTA 0 finishes alone
+constexpr int kClMinChunk = 32;                 // positions per used CTA
+constexpr int kClSoloMax = 128;                 // contexts CTA 0 finishes alone
 constexpr int kClMaxS = kClMaxCtas * kClChunk;  // 4096
 
 // CTAs per KV head for a cache of S <= kClMaxS positions.
@@ -747,8 +799,12 @@ __device__ __forceinline__ void cluster_sync_all() {
 
 template <int G>
 __global__ void __launch_bounds__(kAttnThreads)
-attn_cluster_kernel(const AttnArgs a) {
-  extern __shared__ __align__(128) uint8_t smem[];
+attn_cluster_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap kmap,
+                    const __grid_constant__ CUtensorMap vmap) {
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  // the swizzled staging wants a 1024-byte aligned base (the same offset in
+  // every CTA, so distributed shared memory addresses still match)
+  uint8_t *smem = smem_raw + ((1024u - (pipe::smem_addr(smem_raw) & 1023u)) & 1023u);
   using L = AttnSmem<G, kClChunk>;
   using CS = ClSmem<G>;
   float *wacc = reinterpret_cast<float *>(smem + L::kWacc);
@@ -761,6 +817,12 @@ attn_cluster_kernel(const AttnArgs a) {
   const int c = blockIdx.x, g = blockIdx.y, cl = gridDim.x;  // c = rank
   const int tid = threadIdx.x;
 
+  if (tid == 0) {  // the copies' descriptors, while the wait lasts
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&kmap))
+                 : "memory");
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&vmap))
+                 : "memory");
+  }
   // Every input may come from the preceding kernel.
   pdl_wait();
   pdl_trigger();
@@ -778,17 +840,15 @@ attn_cluster_kernel(const AttnArgs a) {
   if (!valid || p + 1 <= kClSoloMax) {
     // ---- CTA 0 alone: the whole context, or zeros for a bad position ----
     if (c != 0) return;
-    const bool have = valid && attend_split<G, kClChunk>(a, pre, g, p, 0,
-                                                         p + 1, smem, bar, m,
-                                                         l);
+    const bool have =
+        valid && attend_split<G, kClChunk>(a, &kmap, &vmap, pre, g, p, 0,
+                                           p + 1, smem, bar, m, l);
     float *o = a.out + size_t(g) * G * D;
     float ss = 0.0f, amx = 0.0f;
     for (int e = tid; e < G * D; e += kAttnThreads) {
       float y = 0.0f;
       if (have) {
-        float t = wacc[e];
-#pragma unroll
-        for (int w = 1; w < kAttnWarps; ++w) t += wacc[w * G * D + e];
+        const float t = wacc[e];
         const int h = e / D;
         float lh = l[0];
 #pragma unroll
@@ -824,24 +884,14 @@ attn_cluster_kernel(const AttnArgs a) {
   // ---- this CTA's partial ----
   bool have = false;
   if (n > 0)
-    have = attend_split<G, kClChunk>(a, pre, g, p, j0, n, smem, bar, m, l);
+    have = attend_split<G, kClChunk>(a, &kmap, &vmap, pre, g, p, j0, n, smem,
+                                     bar, m, l);
   cluster_wait();  // every CTA has started: its shared memory may be written
   if (c < n_eff) {
     // ---- pushed to the owners: output slices, then m and l to every CTA
     for (int e = 4 * tid; e < G * D; e += 4 * kAttnThreads) {
       float4 t = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
-      if (have) {
-        t = *reinterpret_cast<const float4 *>(wacc + e);
-#pragma unroll
-        for (int w = 1; w < kAttnWarps; ++w) {
-          const float4 u =
-              *reinterpret_cast<const float4 *>(wacc + w * G * D + e);
-          t.x += u.x;
-          t.y += u.y;
-          t.z += u.z;
-          t.w += u.w;
-        }
-      }
+      if (have) t = *reinterpret_cast<const float4 *>(wacc + e);
       const int own = e / per;  // < cl: G D <= cl per
       cl_st4(cl_map(recv + c * per + (e - own * per), own), t);
     }
@@ -907,7 +957,7 @@ bool cluster_ok(int dev) {
     bool ok =
         cudaFuncSetAttribute(kernel,
                              cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             int(ClSmem<G>::kBytes)) == cudaSuccess &&
+                             int(ClSmem<G>::kBytes + 1024)) == cudaSuccess &&
         cudaFuncSetAttribute(kernel,
                              cudaFuncAttributeNonPortableClusterSizeAllowed,
                              1) == cudaSuccess;
@@ -915,7 +965,7 @@ bool cluster_ok(int dev) {
       cudaLaunchConfig_t cfg = {};
       cfg.gridDim = dim3(kClMaxCtas, 1);
       cfg.blockDim = dim3(kAttnThreads);
-      cfg.dynamicSmemBytes = ClSmem<G>::kBytes;
+      cfg.dynamicSmemBytes = ClSmem<G>::kBytes + 1024;
       cudaLaunchAttribute attr[1];
       attr[0].id = cudaLaunchAttributeClusterDimension;
       attr[0].val.clusterDim.x = kClMaxCtas;
@@ -935,11 +985,13 @@ bool cluster_ok(int dev) {
 }
 
 template <int G>
-cudaError_t launch_cluster_g(const AttnArgs &a, int cl, cudaStream_t stream) {
+cudaError_t launch_cluster_g(const AttnArgs &a, const CUtensorMap &kmap,
+                             const CUtensorMap &vmap, int cl,
+                             cudaStream_t stream) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(unsigned(cl), unsigned(a.Hkv));
   cfg.blockDim = dim3(kAttnThreads);
-  cfg.dynamicSmemBytes = ClSmem<G>::kBytes;
+  cfg.dynamicSmemBytes = ClSmem<G>::kBytes + 1024;  // base alignment
   cfg.stream = stream;
   cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -950,11 +1002,12 @@ cudaError_t launch_cluster_g(const AttnArgs &a, int cl, cudaStream_t stream) {
   attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 2;
-  return cudaLaunchKernelEx(&cfg, attn_cluster_kernel<G>, a);
+  return cudaLaunchKernelEx(&cfg, attn_cluster_kernel<G>, a, kmap, vmap);
 }
 
 template <int G>
-cudaError_t launch_g(const AttnArgs &a, cudaStream_t stream) {
+cudaError_t launch_g(const AttnArgs &a, const CUtensorMap &kmap,
+                     const CUtensorMap &vmap, cudaStream_t stream) {
   static bool configured[64];
   auto kernel = attn_decode_kernel<G>;
   int dev = 0;
@@ -964,21 +1017,21 @@ cudaError_t launch_g(const AttnArgs &a, cudaStream_t stream) {
   if (!configured[dev]) {
     e = cudaFuncSetAttribute(kernel,
                              cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             int(AttnSmem<G>::kBytes));
+                             int(AttnSmem<G>::kBytes + 1024));
     if (e != cudaSuccess) return e;
     configured[dev] = true;
   }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(unsigned(a.n_split), unsigned(a.Hkv));
   cfg.blockDim = dim3(kAttnThreads);
-  cfg.dynamicSmemBytes = AttnSmem<G>::kBytes;
+  cfg.dynamicSmemBytes = AttnSmem<G>::kBytes + 1024;  // base alignment
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, kernel, a);
+  return cudaLaunchKernelEx(&cfg, kernel, a, kmap, vmap);
 }
 
 // Partials for the most splits any device uses for this cache.
@@ -1037,30 +1090,44 @@ cudaError_t launch_attn(const AttnLaunch &l, cudaStream_t stream) {
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
   const int G = l.H / l.Hkv;
+  // The caches as 2-D tensors of Hkv S rows of D bf16, boxes of 32 rows x 64
+  // dims in the 128-byte swizzle (rows past the end read as zero).
+  CUtensorMap kmap, vmap;
+  if (!encode_2d(&kmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, l.kc, kAttnD,
+                 uint64_t(l.Hkv) * uint64_t(l.S), kAttnD * 2, 64,
+                 kAttnBlockRows, CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !encode_2d(&vmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, l.vc, kAttnD,
+                 uint64_t(l.Hkv) * uint64_t(l.S), kAttnD * 2, 64,
+                 kAttnBlockRows, CU_TENSOR_MAP_SWIZZLE_128B))
+    return cudaErrorInvalidValue;
   if (l.S <= kClMaxS) {  // one cluster per KV head, merged on chip
     const int cl = cl_ctas(l.S);
     a.n_split = cl;
     switch (G) {
       case 1:
-        if (cluster_ok<1>(dev)) return launch_cluster_g<1>(a, cl, stream);
+        if (cluster_ok<1>(dev))
+          return launch_cluster_g<1>(a, kmap, vmap, cl, stream);
         break;
       case 2:
-        if (cluster_ok<2>(dev)) return launch_cluster_g<2>(a, cl, stream);
+        if (cluster_ok<2>(dev))
+          return launch_cluster_g<2>(a, kmap, vmap, cl, stream);
         break;
       case 4:
-        if (cluster_ok<4>(dev)) return launch_cluster_g<4>(a, cl, stream);
+        if (cluster_ok<4>(dev))
+          return launch_cluster_g<4>(a, kmap, vmap, cl, stream);
         break;
       default:
-        if (cluster_ok<8>(dev)) return launch_cluster_g<8>(a, cl, stream);
+        if (cluster_ok<8>(dev))
+          return launch_cluster_g<8>(a, kmap, vmap, cl, stream);
         break;
     }
     a.n_split = attn_splits(l.S, l.Hkv, sms);
   }
   switch (G) {
-    case 1: return launch_g<1>(a, stream);
-    case 2: return launch_g<2>(a, stream);
-    case 4: return launch_g<4>(a, stream);
-    default: return launch_g<8>(a, stream);
+    case 1: return launch_g<1>(a, kmap, vmap, stream);
+    case 2: return launch_g<2>(a, kmap, vmap, stream);
+    case 4: return launch_g<4>(a, kmap, vmap, stream);
+    default: return launch_g<8>(a, kmap, vmap, stream);
   }
 }
 

@@ -103,9 +103,9 @@ def check_step(case, qkv, p, kc_before, vc_before, out, kc_gpu, vc_gpu):
 
 CASES = [
     # H, Hkv, S, p: BitNet-2B heads (G = 4) over contexts finished by one
-    # CTA per head (up to 128 positions), the first split context (129),
-    # several splits, a ragged last split and a full cache; G = 1, 2, 8,
-    # each on both paths.
+    # CTA per head (up to 64 positions), the first split contexts, several
+    # splits, a ragged last split and a full cache; G = 1, 2, 8, each on
+    # both paths.
     (20, 5, 4096, 0),
     (20, 5, 4096, 1),
     (20, 5, 4096, 63),
@@ -121,6 +121,12 @@ CASES = [
     (16, 2, 777, 400),
     (16, 2, 777, 100),
     (4, 1, 65536, 65535),
+    # splits of at least 48 positions per CTA take the tensor-core scores
+    # and values: G = 2, 8 and 1 on the cluster path and G = 8 alone
+    (16, 8, 1000, 999),
+    (16, 2, 2048, 2047),
+    (16, 2, 777, 60),
+    (8, 8, 3000, 2999),
 ]
 
 
