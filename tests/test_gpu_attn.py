@@ -127,6 +127,10 @@ CASES = [
     (16, 2, 2048, 2047),
     (16, 2, 777, 60),
     (8, 8, 3000, 2999),
+    # caches over 4096 positions: the workspace kernel's splits, G = 1, 2, 8
+    (8, 8, 4500, 4499),
+    (16, 8, 4200, 3000),
+    (16, 2, 5000, 4999),
 ]
 
 
