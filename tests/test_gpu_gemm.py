@@ -75,11 +75,11 @@ def test_gemm_full_parity(bw, M, N, K):
 
 
 @pytest.mark.parametrize("M,N,K", [(1024, 13824, 2560), (2048, 2560, 6912),
-                                   (768, 3840, 2560)])
+                                   (768, 3840, 2560), (4096, 1000, 2560)])
 def test_gemm_prompt_sizes(bw, M, N, K):
-    """Prompt-sized batches at the BitNet-2B shapes, sampled weight rows
-    (all tokens of each): both ends, a row tile boundary and 160 seeded
-    rows."""
+    """Prompt-sized batches at the BitNet-2B shapes and the largest M
+    (4096 tokens: 16 token tiles), sampled weight rows (all tokens of each):
+    both ends, a row tile boundary and 160 seeded rows."""
     rows = np.unique(np.concatenate([
         np.arange(0, 16), np.arange(120, 136), np.arange(N - 16, N),
         (synth.u64(16, M, 160) % np.uint64(N)).astype(np.int64)]))
