@@ -998,7 +998,11 @@ def run_attn_timing(torch, bw, dev, peak_gbs, contexts=ATTN_CONTEXTS,
     (the new token at position L - 1): us per call in a graph of calls back
     to back, each on its own cache so that the keys and values it reads
     (2 Hkv L D bf16 = 2560 L bytes) come from HBM.  One cache of seeded
-    synthetic N(0,1) values is generated and copied."""
+    synthetic N(0,1) values is generated and copied.  Timed twice: as
+    bw_attn_decode (every input read after the preceding call) and with
+    BW_ATTN_PAST_READY (the position and the rows before it read and copied
+    before the dependency wait, which this chain allows: no call writes the
+    position or another call's cache), as the KV stack runs it."""
     H, Hkv, D, S = ATTN_H, ATTN_HKV, ATTN_D, ATTN_S
     seed = synth.base_seed(5)
     case = synth.attn_case(seed, H, Hkv, D, S, 0)
@@ -1026,42 +1030,50 @@ def run_attn_timing(torch, bw, dev, peak_gbs, contexts=ATTN_CONTEXTS,
         kcs = kc0.unsqueeze(0).repeat(rot, 1, 1, 1)
         vcs = vc0.unsqueeze(0).repeat(rot, 1, 1, 1)
         pos = torch.tensor([L - 1], dtype=torch.int32, device=dev)
+        times = {}
+        for flags in (0, bw.BW_ATTN_PAST_READY):
+            def launches():
+                for i in range(rot):
+                    bw.bw_attn_decode_ex(qkv, pos, H, Hkv, kcs[i], vcs[i],
+                                         theta=ATTN_THETA, out=out,
+                                         workspace=ws, flags=flags,
+                                         stream=stream)
 
-        def launches():
-            for i in range(rot):
-                bw.bw_attn_decode(qkv, pos, H, Hkv, kcs[i], vcs[i],
-                                  theta=ATTN_THETA, out=out, workspace=ws,
-                                  stream=stream)
-
-        with torch.cuda.stream(stream):
-            launches()
-        stream.synchronize()
-        g = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g, stream=stream):
-            launches()
-        with torch.cuda.stream(stream):
-            for _ in range(3):
-                g.replay()
-        torch.cuda.synchronize()
-        reps = max(1, iters // rot)
-        e0 = torch.cuda.Event(enable_timing=True)
-        e1 = torch.cuda.Event(enable_timing=True)
-        with torch.cuda.stream(stream):
-            e0.record(stream)
-            for _ in range(reps):
-                g.replay()
-            e1.record(stream)
-        torch.cuda.synchronize()
-        bw.bw_device_error(stream)
-        us = e0.elapsed_time(e1) * 1e3 / (reps * rot)
+            with torch.cuda.stream(stream):
+                launches()
+            stream.synchronize()
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                launches()
+            with torch.cuda.stream(stream):
+                for _ in range(3):
+                    g.replay()
+            torch.cuda.synchronize()
+            reps = max(1, iters // rot)
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            with torch.cuda.stream(stream):
+                e0.record(stream)
+                for _ in range(reps):
+                    g.replay()
+                e1.record(stream)
+            torch.cuda.synchronize()
+            bw.bw_device_error(stream)
+            times[flags] = e0.elapsed_time(e1) * 1e3 / (reps * rot)
+            del g
+        us, us_pr = times[0], times[bw.BW_ATTN_PAST_READY]
         res["contexts"][str(L)] = {
             "us_per_call": round(us, 3),
             "kv_bytes_per_call": kv_bytes,
             "kv_GBps": round(kv_bytes / (us * 1e3), 1),
             "hbm_frac": round(kv_bytes / (us * 1e3) / peak_gbs, 4),
             "caches_rotated": rot,
+            "past_ready": {
+                "us_per_call": round(us_pr, 3),
+                "kv_GBps": round(kv_bytes / (us_pr * 1e3), 1),
+                "hbm_frac": round(kv_bytes / (us_pr * 1e3) / peak_gbs, 4)},
         }
-        del kcs, vcs, g
+        del kcs, vcs
         torch.cuda.empty_cache()
     return res
 

@@ -8,7 +8,7 @@ or ``__graft_entry__.build()``).
 
 Function names follow the C ABI: ``bw_quant_act``, ``bw_repack``,
 ``bw_unrepack``, ``bw_gemv_w2a8``, ``bw_gemv_w2a8_acc``, ``bw_gemm_w2a8``,
-``bw_gemm_w2a8_acc``, ``bw_attn_decode``.
+``bw_gemm_w2a8_acc``, ``bw_attn_decode``, ``bw_attn_decode_ex``.
 """
 from __future__ import annotations
 
@@ -32,6 +32,7 @@ STATUS_NAMES = {0: "BW_OK", 1: "BW_ERR_INVALID_ARG",
                 2: "BW_ERR_UNSUPPORTED_SHAPE", 3: "BW_ERR_MISALIGNED",
                 4: "BW_ERR_BAD_CODE", 5: "BW_ERR_CUDA", 6: "BW_ERR_TIMEOUT"}
 MAX_K, MAX_N, MAX_M, MAX_WS = 65536, 1 << 24, 4096, 8
+BW_ATTN_PAST_READY = 1
 
 # Every symbol the C ABI declares (checked by the tests without a GPU).
 EXPORTS = ("bw_status_string", "bw_last_cuda_error", "bw_version",
@@ -40,7 +41,8 @@ EXPORTS = ("bw_status_string", "bw_last_cuda_error", "bw_version",
            "bw_device_error", "bw_stack_create", "bw_layer_stack",
            "bw_stack_destroy", "bw_selftest_wait_timeout",
            "bw_gemv_workspace_bytes", "bw_quant_weight",
-           "bw_attn_workspace_bytes", "bw_attn_decode", "bw_stack_create_kv",
+           "bw_attn_workspace_bytes", "bw_attn_decode", "bw_attn_decode_ex",
+           "bw_stack_create_kv",
            "bw_stack_read_kv", "bw_stack_reset_kv", "bw_gemv_w2a8_lut",
            "bw_gemv_w2a8_lut_acc", "bw_gemm_workspace_bytes", "bw_gemm_w2a8",
            "bw_gemm_w2a8_acc")
@@ -78,6 +80,9 @@ _SIGS = {
     "bw_stack_reset_kv": (_I, [_P, _P]),
     "bw_attn_decode": (_I, [_P, _P, _I, _I, _I, _I, ctypes.c_float, _P, _P,
                             _P, _P, ctypes.c_size_t, _P]),
+    "bw_attn_decode_ex": (_I, [_P, _P, _I, _I, _I, _I, ctypes.c_float, _P,
+                               _P, _P, _P, ctypes.c_size_t, ctypes.c_uint,
+                               _P]),
 }
 for _name, (_res, _args) in _SIGS.items():
     _fn = getattr(_lib, _name)
@@ -400,6 +405,20 @@ def bw_attn_decode(qkv: torch.Tensor, pos: torch.Tensor, H: int, Hkv: int,
     [H][D].  `workspace` is a uint8 device tensor of at least
     bw_attn_workspace_bytes bytes, zeroed before its first use; if omitted,
     a zeroed one is made for this call."""
+    return bw_attn_decode_ex(qkv, pos, H, Hkv, k_cache, v_cache, theta, out,
+                             workspace, 0, stream)
+
+
+def bw_attn_decode_ex(qkv: torch.Tensor, pos: torch.Tensor, H: int,
+                      Hkv: int, k_cache: torch.Tensor, v_cache: torch.Tensor,
+                      theta: float = 500000.0,
+                      out: torch.Tensor | None = None,
+                      workspace: torch.Tensor | None = None, flags: int = 0,
+                      stream=None) -> torch.Tensor:
+    """bw_attn_decode with flags (BW_ATTN_PAST_READY: pos and the cache
+    rows before it are final before the preceding launch on the stream
+    starts, so the call reads and copies them before its dependency
+    wait)."""
     Hkv_, S, D = k_cache.shape
     if Hkv_ != Hkv or tuple(v_cache.shape) != (Hkv, S, D):
         raise ValueError("k_cache and v_cache must be [Hkv][S][D]")
@@ -411,13 +430,13 @@ def bw_attn_decode(qkv: torch.Tensor, pos: torch.Tensor, H: int, Hkv: int,
     _need(qkv, (H + 2 * Hkv) * D, "qkv")
     _need(pos, 1, "pos")
     _need(out, H * D, "out")
-    _check(_lib.bw_attn_decode(
+    _check(_lib.bw_attn_decode_ex(
         _dev(qkv, torch.bfloat16, "qkv"), _dev(pos, torch.int32, "pos"),
         H, Hkv, D, S, float(theta), _dev(k_cache, torch.bfloat16, "k_cache"),
         _dev(v_cache, torch.bfloat16, "v_cache"),
         _dev(out, torch.float32, "out"),
         _dev(workspace, torch.uint8, "workspace"), workspace.numel(),
-        _stream(stream)), "bw_attn_decode")
+        int(flags), _stream(stream)), "bw_attn_decode_ex")
     return out
 
 

@@ -341,7 +341,7 @@ bw_status bw_device_error(unsigned int *bits, bw_stream_t stream) {
   cudaError_t e =
       read_device_error(reinterpret_cast<cudaStream_t>(stream), bits);
   if (e != cudaSuccess) return cuda_status(e);
-  if (*bits & ~16u) return BW_ERR_TIMEOUT;
+  if (*bits & ~(16u | 128u)) return BW_ERR_TIMEOUT;  // caller errors: 16, 128
   return *bits ? BW_ERR_INVALID_ARG : BW_OK;
 }
 

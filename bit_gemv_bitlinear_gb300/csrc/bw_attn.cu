@@ -88,6 +88,9 @@ struct AttnArgs {
   // one entry per KV head: (sum of out^2, max |out * norm_gamma|).
   const float *norm_gamma;   // [H][D] or null
   float2 *norm_part;         // [Hkv] or null
+  // Nonzero: *pos and the cache rows before it are final before the
+  // preceding kernel on the stream starts (BW_ATTN_PAST_READY).
+  int past_ready;
 };
 
 __host__ __device__ inline int max_splits(int S) {
@@ -103,6 +106,69 @@ inline int attn_splits(int S, int Hkv, int sms) {
   if (n > hi) n = hi;
   if (n < lo) n = lo;
   return n < 1 ? 1 : n;
+}
+
+// A CTA's share of positions 0..p: n_eff splits in use, positions
+// [j0, j0 + n) for this CTA (n = 0: none); valid: p lies in the cache; solo:
+// (cluster kernel) CTA 0 finishes the context alone.
+struct SplitPlan {
+  bool valid, solo;
+  int n_eff, j0, n;
+};
+
+// Split c of the workspace kernel's n_split: a context of at most
+// kAttnSoloMax positions is one split, longer ones take
+// min(n_split, ceil(len / kAttnMinChunk)) equal shares.
+__host__ __device__ inline SplitPlan ws_plan(int p, int S, int n_split, int c) {
+  SplitPlan r{p >= 0 && p < S, false, 0, 0, 0};
+  if (r.valid) {
+    const int len = p + 1;
+    const int want = (len + kAttnMinChunk - 1) / kAttnMinChunk;
+    r.n_eff = len <= kAttnSoloMax ? 1 : (want < n_split ? want : n_split);
+    if (c < r.n_eff) {
+      r.j0 = int(int64_t(c) * len / r.n_eff);
+      r.n = int(int64_t(c + 1) * len / r.n_eff) - r.j0;
+    }
+  }
+  return r;
+}
+
+// BW_ATTN_PAST_READY: a position read after the dependency wait that
+// differs from the one read before it means the caller's promise was
+// broken (device error word bit).
+constexpr unsigned int kAttnErrPastReady = 128u;
+
+// With past_ready, after the dependency wait: early = {j0, n} of the plan
+// thread 0 made from the position it read before the wait (its copies
+// started when n > 0), pl the plan of the position read after it, which
+// decides everything that follows.  If this CTA's rows differ, the early
+// copies are of other rows: they are let land (bounded), the split's
+// barriers invalidated, the broken promise reported, and the split copies
+// its own rows as usual; if they do not land, the CTA gets no rows
+// (pl.n = 0).  Returns whether the CTA's copies are in flight already.
+// Every thread of the CTA calls it, after a barrier that publishes early.
+__device__ __forceinline__ bool settle_early(const AttnArgs &a,
+                                             const int *early, SplitPlan &pl,
+                                             uint64_t *bar) {
+  if (early[1] == 0) return false;
+  if (early[0] == pl.j0 && early[1] == pl.n) return true;
+  __shared__ int s_landed;
+  if (threadIdx.x == 0) {
+    const bool ok = pipe::mbar_wait(&bar[0], 0u) && pipe::mbar_wait(&bar[1], 0u);
+    if (ok) {
+      asm volatile("mbarrier.inval.shared::cta.b64 [%0];" ::"r"(
+                       pipe::smem_addr(&bar[0]))
+                   : "memory");
+      asm volatile("mbarrier.inval.shared::cta.b64 [%0];" ::"r"(
+                       pipe::smem_addr(&bar[1]))
+                   : "memory");
+    }
+    atomicOr(a.err, ok ? kAttnErrPastReady : kAttnErrPastReady | 2u);
+    s_landed = ok;
+  }
+  __syncthreads();
+  if (!s_landed) pl.n = 0;
+  return false;
 }
 
 // A split's partial: acc [G][D] (16-byte aligned rows), then m [G] and
@@ -265,13 +331,43 @@ struct QkvPre {
   }
 };
 
+// The copies of a split's n key rows and n value rows from cache row row0
+// on (thread 0 only): 32-row blocks of two swizzled boxes of 64 dims each
+// (tiled TMA), the keys on bar[0] and the values on bar[1], which it
+// initialises.  Rows past the split (up to the end of its last block) come
+// along; the split never uses them.
+template <int G, int kChunk>
+__device__ __forceinline__ void split_copies(const CUtensorMap *kmap,
+                                             const CUtensorMap *vmap,
+                                             int row0, int n, uint8_t *smem,
+                                             uint64_t *bar) {
+  using L = AttnSmem<G, kChunk>;
+  uint8_t *kst = smem + L::kK;
+  uint8_t *vst = smem + L::kV;
+  const int nb = (n + kAttnBlockRows - 1) / kAttnBlockRows;
+  pipe::mbar_init(&bar[0], 1);
+  pipe::mbar_init(&bar[1], 1);
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  pipe::mbar_arrive_expect_tx(&bar[0], uint32_t(nb) * kAttnBlockBytes);
+  pipe::mbar_arrive_expect_tx(&bar[1], uint32_t(nb) * kAttnBlockBytes);
+  for (int b = 0; b < nb; ++b)
+#pragma unroll
+    for (int hh = 0; hh < 2; ++hh) {
+      const int row = row0 + b * kAttnBlockRows;
+      tma_load_2d(kst + b * kAttnBlockBytes + hh * (kAttnBlockBytes / 2),
+                  kmap, hh * 64, row, &bar[0]);
+      tma_load_2d(vst + b * kAttnBlockBytes + hh * (kAttnBlockBytes / 2),
+                  vmap, hh * 64, row, &bar[1]);
+    }
+}
+
 // The partial of one split, positions j0 .. j0 + n - 1 of KV head g (n >= 1,
-// n <= kChunk): the tiled copies of its key and value rows, the rotated
+// n <= kChunk): the tiled copies of its key and value rows (unless `issued`:
+// thread 0 started them already, before the dependency wait), the rotated
 // queries, the append of the new token when the split holds p, the scores,
 // the split's softmax (largest score m and exp sum l per query head, the
-// same in every thread) and the unnormalised output per warp in the wacc
-// rows of the layout (summed over warps by the caller after the final
-// barrier here).  pre: this thread's loads of the q|k|v vector.  bar: the
+// same in every thread) and its unnormalised output in the first wacc row
+// of the layout.  pre: this thread's loads of the q|k|v vector.  bar: the
 // split's two mbarriers.  Returns false if the key copy did not land (the
 // CTA then has no partial).
 template <int G, int kChunk>
@@ -280,8 +376,9 @@ __device__ __forceinline__ bool attend_split(const AttnArgs &a,
                                              const CUtensorMap *vmap,
                                              const QkvPre<G> &pre, int g,
                                              int p, int j0, int n,
-                                             uint8_t *smem, uint64_t *bar,
-                                             float (&m)[G], float (&l)[G]) {
+                                             bool issued, uint8_t *smem,
+                                             uint64_t *bar, float (&m)[G],
+                                             float (&l)[G]) {
   using L = AttnSmem<G, kChunk>;
   uint8_t *kst = smem + L::kK;
   uint8_t *vst = smem + L::kV;
@@ -293,26 +390,10 @@ __device__ __forceinline__ bool attend_split(const AttnArgs &a,
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   constexpr int D = kAttnD;
   const size_t head_row = size_t(g) * a.S;  // row 0 of KV head g
-  const int nb = (n + kAttnBlockRows - 1) / kAttnBlockRows;
   const int n_mt = (n + 15) / 16;           // 16-position tiles
-  // ---- the split's key rows and value rows: 32-row blocks of two swizzled
-  // boxes of 64 dims each (tiled TMA) ----
-  if (tid == 0) {
-    pipe::mbar_init(&bar[0], 1);
-    pipe::mbar_init(&bar[1], 1);
-    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-    pipe::mbar_arrive_expect_tx(&bar[0], uint32_t(nb) * kAttnBlockBytes);
-    pipe::mbar_arrive_expect_tx(&bar[1], uint32_t(nb) * kAttnBlockBytes);
-    for (int b = 0; b < nb; ++b)
-#pragma unroll
-      for (int hh = 0; hh < 2; ++hh) {
-        const int row = int(head_row) + j0 + b * kAttnBlockRows;
-        tma_load_2d(kst + b * kAttnBlockBytes + hh * (kAttnBlockBytes / 2),
-                    kmap, hh * 64, row, &bar[0]);
-        tma_load_2d(vst + b * kAttnBlockBytes + hh * (kAttnBlockBytes / 2),
-                    vmap, hh * 64, row, &bar[1]);
-      }
-  }
+  // ---- the split's key rows and value rows ----
+  if (tid == 0 && !issued)
+    split_copies<G, kChunk>(kmap, vmap, int(head_row) + j0, n, smem, bar);
   // ---- RoPE of the queries meanwhile ----
   if (tid < kAttnPairs) {
     float sn, cn;
@@ -520,33 +601,40 @@ attn_decode_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap kmap,
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&vmap))
                  : "memory");
   }
-  // Every input may come from the preceding kernel (the q|k|v GEMV, an
-  // update of the position, the previous step's append).
+  // With past_ready the position and the cache rows before it are final
+  // before the preceding kernel started: read the position and start the
+  // split's copies while the dependency wait lasts.  Otherwise every input
+  // may come from the preceding kernel (the q|k|v GEMV, an update of the
+  // position, the previous step's append).
+  __shared__ int s_early[2];  // thread 0's early plan: j0, n
+  if (a.past_ready && tid == 0) {
+    const SplitPlan e = ws_plan(__ldcg(a.pos), a.S, a.n_split, c);
+    s_early[0] = e.j0;
+    s_early[1] = e.n;
+    if (e.n > 0)
+      split_copies<G, kAttnChunk>(&kmap, &vmap, g * a.S + e.j0, e.n, smem, bar);
+  }
   pdl_wait();
   pdl_trigger();
 
   QkvPre<G> pre;
   pre.load(a, g);
-  const int p = *a.pos;
-  const bool valid = p >= 0 && p < a.S;
-  int n_eff = 0, j0 = 0, j1 = 0;
-  if (valid) {
-    const int len = p + 1;
-    n_eff = len <= kAttnSoloMax
-                ? 1
-                : min(a.n_split, (len + kAttnMinChunk - 1) / kAttnMinChunk);
-    if (c < n_eff) {
-      j0 = int(int64_t(c) * len / n_eff);
-      j1 = int(int64_t(c + 1) * len / n_eff);
-    }
+  const int p = __ldcg(a.pos);  // final now: the same plan in every CTA
+  SplitPlan pl = ws_plan(p, a.S, a.n_split, c);
+  bool issued = false;
+  if (a.past_ready) {
+    __syncthreads();  // s_early
+    issued = settle_early(a, s_early, pl, bar);
   }
-  const int n = j1 - j0;  // positions of this CTA (<= kAttnChunk)
+  const bool valid = pl.valid;
+  const int n_eff = pl.n_eff, j0 = pl.j0;
+  const int n = pl.n;  // positions of this CTA (<= kAttnChunk)
   float *part = a.part + (size_t(g) * a.n_split + c) * P::kStride;
 
   if (n > 0) {
     float m[G], l[G];
-    if (attend_split<G, kAttnChunk>(a, &kmap, &vmap, pre, g, p, j0, n, smem,
-                                    bar, m, l)) {
+    if (attend_split<G, kAttnChunk>(a, &kmap, &vmap, pre, g, p, j0, n,
+                                    issued, smem, bar, m, l)) {
       if (n_eff == 1) {
         // One split holds the whole context: its sums are final.  Write
         // the outputs (and the next RMSNorm's statistics) directly; no
@@ -750,6 +838,28 @@ inline int cl_ctas(int S) {
   return n < 1 ? 1 : (n > kClMaxCtas ? kClMaxCtas : n);
 }
 
+// CTA c of a cluster of cl: a context of at most kClSoloMax positions, and
+// an invalid position, are CTA 0's alone (solo); longer contexts take
+// min(cl, ceil(len / kClMinChunk)) equal shares.  Every CTA of the cluster
+// reads the same position, so solo is the same in all of them.
+__host__ __device__ inline SplitPlan cl_plan(int p, int S, int cl, int c) {
+  SplitPlan r{p >= 0 && p < S, false, 0, 0, 0};
+  r.solo = !r.valid || p < kClSoloMax;
+  if (r.solo) {
+    r.n_eff = 1;
+    r.n = (r.valid && c == 0) ? p + 1 : 0;
+    return r;
+  }
+  const int len = p + 1;
+  const int want = (len + kClMinChunk - 1) / kClMinChunk;
+  r.n_eff = want < cl ? want : cl;
+  if (c < r.n_eff) {
+    r.j0 = int(int64_t(c) * len / r.n_eff);
+    r.n = int(int64_t(c + 1) * len / r.n_eff) - r.j0;
+  }
+  return r;
+}
+
 // Outputs per slice for a cluster of cl CTAs: ceil(G D / cl) rounded up to
 // a multiple of 4 (so that slices move as 16-byte vectors).
 template <int G>
@@ -823,26 +933,44 @@ attn_cluster_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap kmap,
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&vmap))
                  : "memory");
   }
-  // Every input may come from the preceding kernel.
+  // With past_ready the position and the cache rows before it are final
+  // before the preceding kernel started: read the position and start the
+  // split's copies while the dependency wait lasts.  Otherwise every input
+  // may come from the preceding kernel.
+  __shared__ int s_early[2];  // thread 0's early plan: j0, n
+  if (a.past_ready && tid == 0) {
+    const SplitPlan e = cl_plan(__ldcg(a.pos), a.S, cl, c);
+    s_early[0] = e.j0;
+    s_early[1] = e.n;
+    if (e.n > 0)
+      split_copies<G, kClChunk>(&kmap, &vmap, g * a.S + e.j0, e.n, smem, bar);
+  }
   pdl_wait();
   pdl_trigger();
 
   QkvPre<G> pre;
   pre.load(a, g);
-  const int p = *a.pos;
-  const bool valid = p >= 0 && p < a.S;
+  // final now: the same plan in every CTA of the cluster
+  const int p = __ldcg(a.pos);
+  SplitPlan pl = cl_plan(p, a.S, cl, c);
+  bool issued = false;
+  if (a.past_ready) {
+    __syncthreads();  // s_early
+    issued = settle_early(a, s_early, pl, bar);
+  }
+  const bool valid = pl.valid;
   float m[G], l[G];
 #pragma unroll
   for (int h = 0; h < G; ++h) {
     m[h] = -INFINITY;
     l[h] = 0.0f;
   }
-  if (!valid || p + 1 <= kClSoloMax) {
+  if (pl.solo) {
     // ---- CTA 0 alone: the whole context, or zeros for a bad position ----
     if (c != 0) return;
     const bool have =
-        valid && attend_split<G, kClChunk>(a, &kmap, &vmap, pre, g, p, 0,
-                                           p + 1, smem, bar, m, l);
+        pl.n > 0 && attend_split<G, kClChunk>(a, &kmap, &vmap, pre, g, p, 0,
+                                              pl.n, issued, smem, bar, m, l);
     float *o = a.out + size_t(g) * G * D;
     float ss = 0.0f, amx = 0.0f;
     for (int e = tid; e < G * D; e += kAttnThreads) {
@@ -871,21 +999,13 @@ attn_cluster_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap kmap,
     return;
   }
   cluster_arrive_relaxed();  // this CTA has started
-  int n_eff = 0, j0 = 0, n = 0;
-  {
-    const int len = p + 1;
-    n_eff = min(cl, (len + kClMinChunk - 1) / kClMinChunk);
-    if (c < n_eff) {
-      j0 = int(int64_t(c) * len / n_eff);
-      n = int(int64_t(c + 1) * len / n_eff) - j0;
-    }
-  }
+  const int n_eff = pl.n_eff, j0 = pl.j0, n = pl.n;
   const int per = cl_slice<G>(cl);
   // ---- this CTA's partial ----
   bool have = false;
   if (n > 0)
-    have = attend_split<G, kClChunk>(a, &kmap, &vmap, pre, g, p, j0, n, smem,
-                                     bar, m, l);
+    have = attend_split<G, kClChunk>(a, &kmap, &vmap, pre, g, p, j0, n,
+                                     issued, smem, bar, m, l);
   cluster_wait();  // every CTA has started: its shared memory may be written
   if (c < n_eff) {
     // ---- pushed to the owners: output slices, then m and l to every CTA
@@ -1085,6 +1205,7 @@ cudaError_t launch_attn(const AttnLaunch &l, cudaStream_t stream) {
   if (!a.err) return cudaErrorInvalidSymbol;
   a.norm_gamma = l.norm_gamma;
   a.norm_part = l.norm_part;
+  a.past_ready = l.past_ready ? 1 : 0;
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
@@ -1143,14 +1264,16 @@ extern "C" size_t bw_attn_workspace_bytes(int H, int Hkv, int D, int S) {
   return attn_workspace_bytes(H, Hkv, D, S);
 }
 
-extern "C" bw_status bw_attn_decode(const bw_bf16 *qkv, const int *pos, int H,
-                                    int Hkv, int D, int S, float theta,
-                                    bw_bf16 *k_cache, bw_bf16 *v_cache,
-                                    float *out, void *workspace,
-                                    size_t workspace_bytes,
-                                    bw_stream_t stream) {
+extern "C" bw_status bw_attn_decode_ex(const bw_bf16 *qkv, const int *pos,
+                                       int H, int Hkv, int D, int S,
+                                       float theta, bw_bf16 *k_cache,
+                                       bw_bf16 *v_cache, float *out,
+                                       void *workspace, size_t workspace_bytes,
+                                       unsigned int flags,
+                                       bw_stream_t stream) {
   if (!qkv || !pos || !k_cache || !v_cache || !out || !workspace)
     return BW_ERR_INVALID_ARG;
+  if (flags & ~unsigned(BW_ATTN_PAST_READY)) return BW_ERR_INVALID_ARG;
   bw_status st = check_attn_shape(H, Hkv, D, S);
   if (st != BW_OK) return st;
   if (!(theta > 0.0f) || !(theta < 3.0e38f)) return BW_ERR_INVALID_ARG;
@@ -1170,6 +1293,7 @@ extern "C" bw_status bw_attn_decode(const bw_bf16 *qkv, const int *pos, int H,
   l.Hkv = Hkv;
   l.S = S;
   l.theta = theta;
+  l.past_ready = (flags & BW_ATTN_PAST_READY) ? 1 : 0;
   const cudaError_t e =
       launch_attn(l, reinterpret_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) {
@@ -1177,4 +1301,14 @@ extern "C" bw_status bw_attn_decode(const bw_bf16 *qkv, const int *pos, int H,
     return BW_ERR_CUDA;
   }
   return BW_OK;
+}
+
+extern "C" bw_status bw_attn_decode(const bw_bf16 *qkv, const int *pos, int H,
+                                    int Hkv, int D, int S, float theta,
+                                    bw_bf16 *k_cache, bw_bf16 *v_cache,
+                                    float *out, void *workspace,
+                                    size_t workspace_bytes,
+                                    bw_stream_t stream) {
+  return bw_attn_decode_ex(qkv, pos, H, Hkv, D, S, theta, k_cache, v_cache,
+                           out, workspace, workspace_bytes, 0u, stream);
 }

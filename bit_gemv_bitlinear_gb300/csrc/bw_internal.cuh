@@ -127,6 +127,7 @@ struct AttnLaunch {
   float theta;
   const float *norm_gamma;
   float2 *norm_part;
+  int past_ready;  // BW_ATTN_PAST_READY: *pos and rows < *pos final earlier
 };
 size_t attn_workspace_bytes(int H, int Hkv, int D, int S);  // 0: unsupported
 bw_status check_attn(int H, int Hkv, int D, int S);

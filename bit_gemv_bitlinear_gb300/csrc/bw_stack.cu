@@ -649,6 +649,12 @@ bw_status run_step(bw_stack *st, cudaStream_t cs, const bw_stack_trace *tr) {
       al.theta = st->theta;
       al.norm_gamma = g + dim;
       al.norm_part = pout;
+      // The position is advanced by the last launch of the previous step
+      // and rows before it were appended by earlier steps; the launch
+      // before this one (the wqkv GEMV) released its dependents only after
+      // its own dependency wait, so all of that has completed when this
+      // launch starts: its copies may start before its wait.
+      al.past_ready = 1;
       BW_TRY_CUDA(launch_attn(al, cs));
       grid = d.n_kv_heads;
       flip();

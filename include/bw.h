@@ -448,6 +448,31 @@ bw_status bw_attn_decode(const bw_bf16 *qkv, const int *pos, int H, int Hkv,
                          bw_bf16 *v_cache, float *out, void *workspace,
                          size_t workspace_bytes, bw_stream_t stream);
 
+/* bw_attn_decode_ex -- bw_attn_decode with flags; flags 0 is bw_attn_decode.
+ *   BW_ATTN_PAST_READY: the caller promises that *pos and rows 0..p-1 of
+ *     both caches are final before the launch immediately preceding this
+ *     one on `stream` starts: no work still running when that launch may
+ *     start writes them.  The call then reads the position and starts
+ *     copying those rows before it waits for the preceding launch (the
+ *     layer's past is static during a decode step, like the weights); q|k|v
+ *     and everything the call writes keep the ordering above.  A decoder
+ *     meets it when the position and the earlier rows are written by the
+ *     previous step and the launch before the attention releases its
+ *     dependents only after its own dependency wait, as the M = 1 q|k|v
+ *     GEMV (bw_gemv_w2a8) and this call do.  The position is read again
+ *     after the wait and decides the result; if this CTA's rows differ, the
+ *     early copies are discarded, the rows copied again and bit 128 of the
+ *     device error word set.  A broken promise about the rows gives the
+ *     attention over stale rows, never an access outside the caches.
+ * Unknown flag bits return BW_ERR_INVALID_ARG.  Otherwise as
+ * bw_attn_decode. */
+#define BW_ATTN_PAST_READY 1u
+bw_status bw_attn_decode_ex(const bw_bf16 *qkv, const int *pos, int H,
+                            int Hkv, int D, int S, float theta,
+                            bw_bf16 *k_cache, bw_bf16 *v_cache, float *out,
+                            void *workspace, size_t workspace_bytes,
+                            unsigned int flags, bw_stream_t stream);
+
 /* bw_device_error -- reads and clears the library's device error word.
  * Kernels that wait on an mbarrier or poll for another CTA's data bound
  * every wait (about one second); a wait that runs out sets a bit here and
@@ -456,9 +481,12 @@ bw_status bw_attn_decode(const bw_bf16 *qkv, const int *pos, int H, int Hkv,
  * for a weight piece; bit 32: a CTA of the persistent decoder stack gave
  * up waiting for another CTA's output, or saw another CTA give up; bits 8
  * and 64 are the self-test's).  Bit 16: bw_attn_decode was given a position
- * outside its cache.
- * Returns BW_ERR_TIMEOUT if any bit other than 16 was set, else
- * BW_ERR_INVALID_ARG if bit 16 was, else BW_OK; *bits receives the word.
+ * outside its cache.  Bit 128: bw_attn_decode_ex with BW_ATTN_PAST_READY
+ * read a different position after its dependency wait than before it (the
+ * promise was broken; the call used the later one).
+ * Returns BW_ERR_TIMEOUT if any bit other than 16 and 128 was set, else
+ * BW_ERR_INVALID_ARG if bit 16 or 128 was, else BW_OK; *bits receives the
+ * word.
  * SYNCHRONISES `stream`; not for the hot path. */
 bw_status bw_device_error(unsigned int *bits, bw_stream_t stream);
 

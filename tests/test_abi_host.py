@@ -298,6 +298,23 @@ def test_attn_workspace_and_host_validation(lib):
     assert call(pos=A4 + 2) == MISALIGNED
     assert call(out=A4 + 1) == MISALIGNED
     assert call(ws=A16 + 4) == MISALIGNED
+    # The flagged form validates the same way, and refuses unknown flags
+    # before any launch.
+    ax = lib.bw_attn_decode_ex
+    ax.restype = ctypes.c_int
+    ax.argtypes = [P, P, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                   ctypes.c_int, ctypes.c_float, P, P, P, P, ctypes.c_size_t,
+                   ctypes.c_uint, P]
+
+    def call_ex(flags, qkv=A16, nb=need, D=128):
+        return ax(qkv, A4, 20, 5, D, 4096, 5e5, A16, A16, A4, A16, nb, flags,
+                  None)
+
+    assert call_ex(2) == INVALID
+    assert call_ex(0x80000000) == INVALID
+    assert call_ex(1, qkv=None) == INVALID
+    assert call_ex(1, nb=need - 1) == INVALID
+    assert call_ex(1, D=64) == SHAPE
 
 
 def test_stack_create_kv_host_validation(lib):

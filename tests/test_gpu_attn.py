@@ -65,12 +65,17 @@ class Step:
                               dtype=torch.uint8, device="cuda")
         self.out = torch.empty((H, D), dtype=torch.float32, device="cuda")
 
-    def run(self, qkv_bits, p):
+    def run(self, qkv_bits, p, flags=0):
         c = self.c
         self.pos.fill_(p)
-        self.bw.bw_attn_decode(_dev_bf16(qkv_bits), self.pos, c["H"], c["Hkv"],
-                               self.kc, self.vc, theta=THETA, out=self.out,
-                               workspace=self.ws)
+        qkv = _dev_bf16(qkv_bits)
+        if flags & self.bw.BW_ATTN_PAST_READY:
+            # the promise: nothing in flight writes the position or the
+            # cache when the call is launched
+            torch.cuda.synchronize()
+        self.bw.bw_attn_decode_ex(qkv, self.pos, c["H"], c["Hkv"], self.kc,
+                                  self.vc, theta=THETA, out=self.out,
+                                  workspace=self.ws, flags=flags)
         torch.cuda.synchronize()
         return self.out.cpu().numpy().astype(np.float64)
 
@@ -145,7 +150,79 @@ def test_attn_decode_matches_oracle(bw, H, Hkv, S, p):
                _bits(st.kc), _bits(st.vc))
 
 
-def test_consecutive_steps_share_the_workspace_and_see_the_appended_rows(bw):
+# BW_ATTN_PAST_READY: the position and the earlier rows are read and copied
+# before the dependency wait.  Both kernels; CTA 0 alone, the cluster splits
+# and the workspace splits; the first and the last position of a cache.
+PAST_READY_CASES = [
+    (20, 5, 4096, 0),
+    (20, 5, 4096, 127),
+    (20, 5, 4096, 128),
+    (20, 5, 4096, 1000),
+    (20, 5, 4096, 4095),
+    (8, 8, 300, 50),
+    (16, 8, 1000, 999),
+    (16, 2, 777, 60),
+    (8, 8, 4500, 4499),
+    (16, 8, 4200, 3000),
+    (16, 2, 5000, 64),
+    (4, 1, 65536, 65535),
+]
+
+
+@pytest.mark.parametrize("H,Hkv,S,p", PAST_READY_CASES)
+def test_past_ready_matches_oracle(bw, H, Hkv, S, p):
+    case = synth.attn_case(
+        synth.base_seed(22, 100 + PAST_READY_CASES.index((H, Hkv, S, p))),
+        H, Hkv, 128, S, p)
+    st = Step(bw, case)
+    out = st.run(case["qkv"], p, flags=bw.BW_ATTN_PAST_READY)
+    assert bw.bw_device_error() == 0
+    check_step(case, case["qkv"], p, case["kc"], case["vc"], out,
+               _bits(st.kc), _bits(st.vc))
+
+
+def test_past_ready_chain_of_calls_in_a_graph(bw):
+    """Flagged calls back to back in one graph, each on its own cache at
+    the same position: every call's predecessor is the previous call, which
+    writes neither the position nor this call's cache, so each may start
+    its copies early.  Every call matches the oracle."""
+    H, Hkv, D, S, p = 20, 5, 128, 4096, 700
+    n = 4
+    cases = [synth.attn_case(synth.base_seed(22, 120 + i), H, Hkv, D, S, p)
+             for i in range(n)]
+    steps = [Step(bw, c) for c in cases]
+    qkvs = [_dev_bf16(c["qkv"]) for c in cases]
+    stream = torch.cuda.Stream()
+    stream.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(stream):   # warm-up outside the capture
+        bw.bw_attn_decode_ex(qkvs[0], steps[0].pos, H, Hkv, steps[0].kc,
+                             steps[0].vc, theta=THETA, out=steps[0].out,
+                             workspace=steps[0].ws, stream=stream)
+    stream.synchronize()
+    steps[0].kc.copy_(_dev_bf16(cases[0]["kc"]))
+    steps[0].vc.copy_(_dev_bf16(cases[0]["vc"]))
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        for i in range(n):
+            bw.bw_attn_decode_ex(qkvs[i], steps[i].pos, H, Hkv, steps[i].kc,
+                                 steps[i].vc, theta=THETA, out=steps[i].out,
+                                 workspace=steps[i].ws,
+                                 flags=bw.BW_ATTN_PAST_READY, stream=stream)
+    torch.cuda.synchronize()
+    g.replay()
+    torch.cuda.synchronize()
+    assert bw.bw_device_error() == 0
+    for i in range(n):
+        out = steps[i].out.cpu().numpy().astype(np.float64)
+        check_step(cases[i], cases[i]["qkv"], p, cases[i]["kc"],
+                   cases[i]["vc"], out, _bits(steps[i].kc),
+                   _bits(steps[i].vc))
+
+
+@pytest.mark.parametrize("flags", [0, 1])
+def test_consecutive_steps_share_the_workspace_and_see_the_appended_rows(
+        bw, flags):
     """Three steps p, p+1, p+2 on one cache and one workspace: every step
     must find the merge counters at zero and read the rows the previous
     steps appended."""
@@ -156,7 +233,7 @@ def test_consecutive_steps_share_the_workspace_and_see_the_appended_rows(bw):
     for t in range(3):
         qkv = synth.bf16_normal(synth.base_seed(22, 51 + t),
                                 (H + 2 * Hkv) * D)
-        out = st.run(qkv, p0 + t)
+        out = st.run(qkv, p0 + t, flags=flags)
         kc_gpu, vc_gpu = _bits(st.kc), _bits(st.vc)
         check_step(case, qkv, p0 + t, kc, vc, out, kc_gpu, vc_gpu)
         kc, vc = kc_gpu, vc_gpu
@@ -199,13 +276,14 @@ def test_graph_replay_advances_with_the_device_position(bw):
     assert bw.bw_device_error() == 0
 
 
-def test_position_outside_the_cache_is_reported(bw):
+@pytest.mark.parametrize("flags", [0, 1])
+def test_position_outside_the_cache_is_reported(bw, flags):
     H, Hkv, D, S = 20, 5, 128, 128
     case = synth.attn_case(synth.base_seed(22, 70), H, Hkv, D, S, 0)
     st = Step(bw, case)
     st.out.fill_(7.0)
     for p in (S, -1):
-        out = st.run(case["qkv"], p)
+        out = st.run(case["qkv"], p, flags=flags)
         assert (out == 0).all()
         assert (_bits(st.kc) == case["kc"]).all()
         assert (_bits(st.vc) == case["vc"]).all()
@@ -213,7 +291,7 @@ def test_position_outside_the_cache_is_reported(bw):
             bw.bw_device_error()
         assert e.value.status == 1                 # BW_ERR_INVALID_ARG
     # the workspace counters are back at zero: a valid step still works
-    out = st.run(case["qkv"], 5)
+    out = st.run(case["qkv"], 5, flags=flags)
     check_step(case, case["qkv"], 5, case["kc"], case["vc"], out,
                _bits(st.kc), _bits(st.vc))
     assert bw.bw_device_error() == 0
