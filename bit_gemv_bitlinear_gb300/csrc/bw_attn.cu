@@ -192,8 +192,11 @@ struct AttnSmem {
   static constexpr uint32_t kCs = kV + kChunk * kRowBytes;      // float2[64]
   static constexpr uint32_t kQ = kCs + kAttnPairs * 8;          // [G][D]
   static constexpr uint32_t kSc = kQ + G * kAttnD * 4;          // [chunk][G]
-  static constexpr uint32_t kWacc = kSc + kChunk * G * 4;       // [warps][G][D]
-  static constexpr uint32_t kRed = kWacc + kAttnWarps * G * kAttnD * 4;
+  // the split's output [G][D]; the workspace merge's [threads] float4 sums
+  static constexpr uint32_t kWacc = kSc + kChunk * G * 4;
+  static constexpr uint32_t kWaccBytes =
+      G * kAttnD * 4 > kAttnThreads * 16 ? G * kAttnD * 4 : kAttnThreads * 16;
+  static constexpr uint32_t kRed = kWacc + kWaccBytes;
   static constexpr size_t kBytes = kRed + kAttnWarps * (G < 2 ? 2 : G) * 4 + 16;
 };
 // The merge keeps [splits][G] weights, [splits][G] exp sums and G totals
@@ -826,11 +829,18 @@ attn_decode_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap kmap,
 // so the choice is the same in the whole cluster, and otherwise every CTA
 // executes every cluster barrier on every path: a barrier never waits for a
 // CTA that has left.
+// The kernel comes in two sizes of a CTA's staging, kClChunk positions
+// (caches of up to kClMaxS) and kClChunkSmall (a launch that serves short
+// contexts only: less shared memory, so its CTAs fit beside other kernels'
+// on an SM); a launch of cl CTAs per KV head serves contexts of at most
+// cl * chunk positions.
 constexpr int kClMaxCtas = 16;                  // CTAs per KV head
 constexpr int kClChunk = 256;                   // positions per CTA, at most
+constexpr int kClChunkSmall = 128;
 constexpr int kClMinChunk = 32;                 // positions per used CTA
 constexpr int kClSoloMax = 128;                 // contexts CTA 0 finishes alone
 constexpr int kClMaxS = kClMaxCtas * kClChunk;  // 4096
+static_assert(kClSoloMax <= kClChunkSmall, "CTA 0 stages a solo context");
 
 // CTAs per KV head for a cache of S <= kClMaxS positions.
 inline int cl_ctas(int S) {
@@ -840,10 +850,13 @@ inline int cl_ctas(int S) {
 
 // CTA c of a cluster of cl: a context of at most kClSoloMax positions, and
 // an invalid position, are CTA 0's alone (solo); longer contexts take
-// min(cl, ceil(len / kClMinChunk)) equal shares.  Every CTA of the cluster
+// min(cl, ceil(len / kClMinChunk)) equal shares.  A position is invalid
+// outside the cache and past the launch's cap = cl * chunk contexts (which
+// keeps every share within a CTA's staging).  Every CTA of the cluster
 // reads the same position, so solo is the same in all of them.
-__host__ __device__ inline SplitPlan cl_plan(int p, int S, int cl, int c) {
-  SplitPlan r{p >= 0 && p < S, false, 0, 0, 0};
+__host__ __device__ inline SplitPlan cl_plan(int p, int S, int cl, int c,
+                                             int cap) {
+  SplitPlan r{p >= 0 && p < S && p < cap, false, 0, 0, 0};
   r.solo = !r.valid || p < kClSoloMax;
   if (r.solo) {
     r.n_eff = 1;
@@ -869,9 +882,9 @@ __device__ __forceinline__ int cl_slice(int cl) {
 
 // The pushed partials after the split's layout: [cl][slice] outputs
 // (cl * slice <= G D + 4 cl), [16][G] (m, l) pairs, [16] statistics.
-template <int G>
+template <int G, int kChunk>
 struct ClSmem {
-  using L = AttnSmem<G, kClChunk>;
+  using L = AttnSmem<G, kChunk>;
   static constexpr uint32_t kRecv = uint32_t((L::kBytes + 15) / 16 * 16);
   static constexpr uint32_t kMl = kRecv + (G * kAttnD + 4 * kClMaxCtas) * 4;
   static constexpr uint32_t kStats = kMl + kClMaxCtas * G * 8;
@@ -907,7 +920,7 @@ __device__ __forceinline__ void cluster_sync_all() {
       "barrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
-template <int G>
+template <int G, int kChunk>
 __global__ void __launch_bounds__(kAttnThreads)
 attn_cluster_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap kmap,
                     const __grid_constant__ CUtensorMap vmap) {
@@ -915,8 +928,8 @@ attn_cluster_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap kmap,
   // the swizzled staging wants a 1024-byte aligned base (the same offset in
   // every CTA, so distributed shared memory addresses still match)
   uint8_t *smem = smem_raw + ((1024u - (pipe::smem_addr(smem_raw) & 1023u)) & 1023u);
-  using L = AttnSmem<G, kClChunk>;
-  using CS = ClSmem<G>;
+  using L = AttnSmem<G, kChunk>;
+  using CS = ClSmem<G, kChunk>;
   float *wacc = reinterpret_cast<float *>(smem + L::kWacc);
   float *red = reinterpret_cast<float *>(smem + L::kRed);
   float *recv = reinterpret_cast<float *>(smem + CS::kRecv);
@@ -939,11 +952,11 @@ attn_cluster_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap kmap,
   // may come from the preceding kernel.
   __shared__ int s_early[2];  // thread 0's early plan: j0, n
   if (a.past_ready && tid == 0) {
-    const SplitPlan e = cl_plan(__ldcg(a.pos), a.S, cl, c);
+    const SplitPlan e = cl_plan(__ldcg(a.pos), a.S, cl, c, cl * kChunk);
     s_early[0] = e.j0;
     s_early[1] = e.n;
     if (e.n > 0)
-      split_copies<G, kClChunk>(&kmap, &vmap, g * a.S + e.j0, e.n, smem, bar);
+      split_copies<G, kChunk>(&kmap, &vmap, g * a.S + e.j0, e.n, smem, bar);
   }
   pdl_wait();
   pdl_trigger();
@@ -952,7 +965,7 @@ attn_cluster_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap kmap,
   pre.load(a, g);
   // final now: the same plan in every CTA of the cluster
   const int p = __ldcg(a.pos);
-  SplitPlan pl = cl_plan(p, a.S, cl, c);
+  SplitPlan pl = cl_plan(p, a.S, cl, c, cl * kChunk);
   bool issued = false;
   if (a.past_ready) {
     __syncthreads();  // s_early
@@ -969,7 +982,7 @@ attn_cluster_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap kmap,
     // ---- CTA 0 alone: the whole context, or zeros for a bad position ----
     if (c != 0) return;
     const bool have =
-        pl.n > 0 && attend_split<G, kClChunk>(a, &kmap, &vmap, pre, g, p, 0,
+        pl.n > 0 && attend_split<G, kChunk>(a, &kmap, &vmap, pre, g, p, 0,
                                               pl.n, issued, smem, bar, m, l);
     float *o = a.out + size_t(g) * G * D;
     float ss = 0.0f, amx = 0.0f;
@@ -1004,7 +1017,7 @@ attn_cluster_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap kmap,
   // ---- this CTA's partial ----
   bool have = false;
   if (n > 0)
-    have = attend_split<G, kClChunk>(a, &kmap, &vmap, pre, g, p, j0, n,
+    have = attend_split<G, kChunk>(a, &kmap, &vmap, pre, g, p, j0, n,
                                      issued, smem, bar, m, l);
   cluster_wait();  // every CTA has started: its shared memory may be written
   if (c < n_eff) {
@@ -1068,16 +1081,17 @@ attn_cluster_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap kmap,
 }
 
 // Whether clusters of kClMaxCtas CTAs of this kernel can be resident (once
-// per device).
-template <int G>
+// per device and size).
+template <int G, int kChunk>
 bool cluster_ok(int dev) {
   static int state[64];  // 0 unknown, 1 yes, 2 no
   if (state[dev] == 0) {
-    auto kernel = attn_cluster_kernel<G>;
+    auto kernel = attn_cluster_kernel<G, kChunk>;
+    constexpr size_t kSmem = ClSmem<G, kChunk>::kBytes + 1024;
     bool ok =
         cudaFuncSetAttribute(kernel,
                              cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             int(ClSmem<G>::kBytes + 1024)) == cudaSuccess &&
+                             int(kSmem)) == cudaSuccess &&
         cudaFuncSetAttribute(kernel,
                              cudaFuncAttributeNonPortableClusterSizeAllowed,
                              1) == cudaSuccess;
@@ -1085,7 +1099,7 @@ bool cluster_ok(int dev) {
       cudaLaunchConfig_t cfg = {};
       cfg.gridDim = dim3(kClMaxCtas, 1);
       cfg.blockDim = dim3(kAttnThreads);
-      cfg.dynamicSmemBytes = ClSmem<G>::kBytes + 1024;
+      cfg.dynamicSmemBytes = kSmem;
       cudaLaunchAttribute attr[1];
       attr[0].id = cudaLaunchAttributeClusterDimension;
       attr[0].val.clusterDim.x = kClMaxCtas;
@@ -1104,14 +1118,14 @@ bool cluster_ok(int dev) {
   return state[dev] == 1;
 }
 
-template <int G>
+template <int G, int kChunk>
 cudaError_t launch_cluster_g(const AttnArgs &a, const CUtensorMap &kmap,
                              const CUtensorMap &vmap, int cl,
                              cudaStream_t stream) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(unsigned(cl), unsigned(a.Hkv));
   cfg.blockDim = dim3(kAttnThreads);
-  cfg.dynamicSmemBytes = ClSmem<G>::kBytes + 1024;  // base alignment
+  cfg.dynamicSmemBytes = ClSmem<G, kChunk>::kBytes + 1024;  // base alignment
   cfg.stream = stream;
   cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -1122,7 +1136,33 @@ cudaError_t launch_cluster_g(const AttnArgs &a, const CUtensorMap &kmap,
   attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 2;
-  return cudaLaunchKernelEx(&cfg, attn_cluster_kernel<G>, a, kmap, vmap);
+  return cudaLaunchKernelEx(&cfg, attn_cluster_kernel<G, kChunk>, a, kmap,
+                            vmap);
+}
+
+// The cluster kernel of staging kChunk for G, if its clusters fit.
+template <int kChunk>
+bool try_cluster(int G, int dev, const AttnArgs &a, const CUtensorMap &kmap,
+                 const CUtensorMap &vmap, int cl, cudaStream_t stream,
+                 cudaError_t *e) {
+  switch (G) {
+    case 1:
+      if (!cluster_ok<1, kChunk>(dev)) return false;
+      *e = launch_cluster_g<1, kChunk>(a, kmap, vmap, cl, stream);
+      return true;
+    case 2:
+      if (!cluster_ok<2, kChunk>(dev)) return false;
+      *e = launch_cluster_g<2, kChunk>(a, kmap, vmap, cl, stream);
+      return true;
+    case 4:
+      if (!cluster_ok<4, kChunk>(dev)) return false;
+      *e = launch_cluster_g<4, kChunk>(a, kmap, vmap, cl, stream);
+      return true;
+    default:
+      if (!cluster_ok<8, kChunk>(dev)) return false;
+      *e = launch_cluster_g<8, kChunk>(a, kmap, vmap, cl, stream);
+      return true;
+  }
 }
 
 template <int G>
@@ -1221,27 +1261,22 @@ cudaError_t launch_attn(const AttnLaunch &l, cudaStream_t stream) {
                  uint64_t(l.Hkv) * uint64_t(l.S), kAttnD * 2, 64,
                  kAttnBlockRows, CU_TENSOR_MAP_SWIZZLE_128B))
     return cudaErrorInvalidValue;
-  if (l.S <= kClMaxS) {  // one cluster per KV head, merged on chip
-    const int cl = cl_ctas(l.S);
-    a.n_split = cl;
-    switch (G) {
-      case 1:
-        if (cluster_ok<1>(dev))
-          return launch_cluster_g<1>(a, kmap, vmap, cl, stream);
-        break;
-      case 2:
-        if (cluster_ok<2>(dev))
-          return launch_cluster_g<2>(a, kmap, vmap, cl, stream);
-        break;
-      case 4:
-        if (cluster_ok<4>(dev))
-          return launch_cluster_g<4>(a, kmap, vmap, cl, stream);
-        break;
-      default:
-        if (cluster_ok<8>(dev))
-          return launch_cluster_g<8>(a, kmap, vmap, cl, stream);
-        break;
+  // The contexts this launch serves: every context of the cache, or (the
+  // layer stack's short-context launches) at most l.max_len positions.
+  const int max_len = (l.max_len > 0 && l.max_len < l.S) ? l.max_len : l.S;
+  if (max_len <= kClMaxS) {  // one cluster per KV head, merged on chip
+    cudaError_t le = cudaSuccess;
+    if (max_len <= kClMaxCtas * kClChunkSmall && max_len < l.S) {
+      // the smaller staging: CTAs of half the shared memory
+      const int cl = (max_len + kClChunkSmall - 1) / kClChunkSmall;
+      a.n_split = cl;
+      if (try_cluster<kClChunkSmall>(G, dev, a, kmap, vmap, cl, stream, &le))
+        return le;
     }
+    const int cl = cl_ctas(max_len);
+    a.n_split = cl;
+    if (try_cluster<kClChunk>(G, dev, a, kmap, vmap, cl, stream, &le))
+      return le;
     a.n_split = attn_splits(l.S, l.Hkv, sms);
   }
   switch (G) {

@@ -128,6 +128,10 @@ struct AttnLaunch {
   const float *norm_gamma;
   float2 *norm_part;
   int past_ready;  // BW_ATTN_PAST_READY: *pos and rows < *pos final earlier
+  // 0, or the longest context (p + 1) the launch must serve; a shorter one
+  // lets a launch of fewer, smaller CTAs serve it (a longer position then
+  // reads as outside the cache: zeros and device error bit 16).
+  int max_len;
 };
 size_t attn_workspace_bytes(int H, int Hkv, int D, int S);  // 0: unsupported
 bw_status check_attn(int H, int Hkv, int D, int S);

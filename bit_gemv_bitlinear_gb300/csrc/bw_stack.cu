@@ -555,8 +555,15 @@ struct bw_stack {
   int *pos;
   void *attn_ws;
   size_t kv_layer_elems;
-  cudaGraphExec_t exec;
-  bool have_graph;
+  // One captured step per context bucket: graph b serves the tokens whose
+  // context (position + 1) is at most graph_len[b] (0: any), its attention
+  // launches sized for that; host_pos counts the tokens since the last reset
+  // and picks the graph (the kernels read the position on the device).
+  static constexpr int kMaxGraphs = 3;
+  int n_graphs;
+  int graph_len[kMaxGraphs];
+  cudaGraphExec_t exec[kMaxGraphs];
+  long long host_pos;
   // Stacks without a KV cache run as one persistent kernel per call
   // (bw_decoder.cu): its per-layer pointer table, exchange buffers and
   // control words.
@@ -567,6 +574,11 @@ struct bw_stack {
 };
 
 namespace {
+
+// Context buckets of a stack with a KV cache (positions + 1), below the
+// cache size; a last bucket takes every context.
+constexpr int kStackBuckets[2] = {128, 1024};
+static_assert(2 + 1 <= bw_stack::kMaxGraphs, "one graph per bucket");
 
 bw_status cuda_err(cudaError_t e) {
   if (e == cudaSuccess) return BW_OK;
@@ -593,7 +605,8 @@ cudaError_t trace_copy(void *dst, const void *src, size_t bytes,
 // values the next launch normalises, with per-CTA partial statistics in one
 // of two alternating buffers (a launch reads the previous launch's buffer
 // and writes the other).
-bw_status run_step(bw_stack *st, cudaStream_t cs, const bw_stack_trace *tr) {
+bw_status run_step(bw_stack *st, cudaStream_t cs, const bw_stack_trace *tr,
+                   int max_len) {
   const bw_stack_desc &d = st->d;
   const int dim = d.dim, ffn = d.ffn;
   const int b_qkv[4] = {0, d.n_heads * st->hd,
@@ -655,6 +668,7 @@ bw_status run_step(bw_stack *st, cudaStream_t cs, const bw_stack_trace *tr) {
       // its own dependency wait, so all of that has completed when this
       // launch starts: its copies may start before its wait.
       al.past_ready = 1;
+      al.max_len = max_len;
       BW_TRY_CUDA(launch_attn(al, cs));
       grid = d.n_kv_heads;
       flip();
@@ -718,7 +732,7 @@ void free_stack(bw_stack *st) {
   cudaFree(st->dec_table);
   cudaFree(st->dec_xch);
   cudaFree(st->dec_ctl);
-  if (st->have_graph) cudaGraphExecDestroy(st->exec);
+  for (int b = 0; b < st->n_graphs; ++b) cudaGraphExecDestroy(st->exec[b]);
   cudaFree(st->h);
   cudaFree(st->attn);
   cudaFree(st->gated);
@@ -850,23 +864,40 @@ bw_status stack_create(const bw_stack_desc *desc, int kv_S, float theta,
     return BW_OK;
   }
   // Capture one decode step as a graph on a private stream (after one eager
-  // run on zero input, which also performs every one-time set-up).
+  // run on zero input, which also performs every one-time set-up); with a
+  // cache, one graph per context bucket (up to 128 and 1024 positions, then
+  // any), so that short contexts run attention launches of fewer, smaller
+  // CTAs.
+  int lens[bw_stack::kMaxGraphs];
+  int n_lens = 0;
+  if (kv_S > 0)
+    for (int b : kStackBuckets)
+      if (b < kv_S) lens[n_lens++] = b;
+  lens[n_lens++] = 0;
   cudaStream_t cap = nullptr;
   e = cudaStreamCreateWithFlags(&cap, cudaStreamNonBlocking);
-  bw_status bs = e == cudaSuccess ? run_step(st, cap, nullptr) : cuda_err(e);
+  bw_status bs = e == cudaSuccess ? run_step(st, cap, nullptr, 0) : cuda_err(e);
   if (bs == BW_OK) e = cudaStreamSynchronize(cap);
-  if (bs == BW_OK && e == cudaSuccess) {
+  for (int b = 0; b < n_lens && bs == BW_OK && e == cudaSuccess; ++b) {
     cudaGraph_t graph = nullptr;
-    e = cudaStreamBeginCapture(cap, cudaStreamCaptureModeRelaxed);
-    if (e == cudaSuccess) {
-      bw_status rs = run_step(st, cap, nullptr);
+    bool ok = false;
+    if (cudaStreamBeginCapture(cap, cudaStreamCaptureModeRelaxed) ==
+        cudaSuccess) {
+      bw_status rs = run_step(st, cap, nullptr, lens[b]);
       cudaError_t ee = cudaStreamEndCapture(cap, &graph);
-      if (rs == BW_OK && ee == cudaSuccess &&
-          cudaGraphInstantiate(&st->exec, graph, 0) == cudaSuccess)
-        st->have_graph = true;
+      ok = rs == BW_OK && ee == cudaSuccess &&
+           cudaGraphInstantiate(&st->exec[st->n_graphs], graph, 0) ==
+               cudaSuccess;
       if (graph) cudaGraphDestroy(graph);
     }
     cudaGetLastError();  // a failed capture leaves eager launches
+    if (!ok) break;
+    st->graph_len[st->n_graphs++] = lens[b];
+  }
+  // Without every graph the steps run eagerly (still sized per bucket).
+  if (st->n_graphs != n_lens) {
+    for (int b = 0; b < st->n_graphs; ++b) cudaGraphExecDestroy(st->exec[b]);
+    st->n_graphs = 0;
   }
   if (cap) cudaStreamDestroy(cap);
   if (bs != BW_OK) {
@@ -921,8 +952,10 @@ bw_status bw_stack_read_kv(const bw_stack *st, int layer, bw_bf16 *k_out,
 
 bw_status bw_stack_reset_kv(bw_stack *st, bw_stream_t stream) {
   if (!st || st->kv_S < 1) return BW_ERR_INVALID_ARG;
-  return cuda_err(cudaMemsetAsync(st->pos, 0, sizeof(int),
-                                  reinterpret_cast<cudaStream_t>(stream)));
+  BW_TRY_CUDA(cudaMemsetAsync(st->pos, 0, sizeof(int),
+                              reinterpret_cast<cudaStream_t>(stream)));
+  st->host_pos = 0;
+  return BW_OK;
 }
 
 bw_status bw_layer_stack(bw_stack *st, const float *h_in, int steps,
@@ -938,14 +971,27 @@ bw_status bw_layer_stack(bw_stack *st, const float *h_in, int steps,
   if (st->persistent) return run_decoder(st, h_in, steps, h_out, trace, cs);
   const size_t row = size_t(st->d.dim) * 4;
   for (int t = 0; t < steps; ++t) {
+    // the step's bucket: the first whose contexts include this token's
+    int len = 0;
+    int b = 0;
+    if (st->kv_S > 0) {
+      const long long want = st->host_pos + 1;
+      for (int lb : kStackBuckets)
+        if (lb < st->kv_S && want <= lb) {
+          len = lb;
+          break;
+        }
+      while (b + 1 < st->n_graphs && st->graph_len[b] != len) ++b;
+    }
     BW_TRY_CUDA(cudaMemcpyAsync(st->h, h_in + size_t(t) * st->d.dim, row,
                                 cudaMemcpyDeviceToDevice, cs));
-    if ((trace && t == steps - 1) || !st->have_graph)
-      BW_TRY(run_step(st, cs, t == steps - 1 ? trace : nullptr));
+    if ((trace && t == steps - 1) || st->n_graphs == 0)
+      BW_TRY(run_step(st, cs, t == steps - 1 ? trace : nullptr, len));
     else
-      BW_TRY_CUDA(cudaGraphLaunch(st->exec, cs));
+      BW_TRY_CUDA(cudaGraphLaunch(st->exec[b], cs));
     BW_TRY_CUDA(cudaMemcpyAsync(h_out + size_t(t) * st->d.dim, st->h, row,
                                 cudaMemcpyDeviceToDevice, cs));
+    ++st->host_pos;
   }
   return BW_OK;
 }

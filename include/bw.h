@@ -365,8 +365,13 @@ bw_status bw_stack_create(const bw_stack_desc *desc, bw_stack **stack);
  * zero attention.  Needs dim / n_heads == 128, n_heads / n_kv_heads in {1,
  * 2, 4, 8}, 1 <= max_positions <= BW_ATTN_MAX_S, theta > 0.  Allocates
  * 2 n_layers n_kv_heads max_positions 128 bf16 of cache with cudaMalloc
- * (zeroed) besides the scratch of bw_stack_create.  Synchronising; call it
- * before any stream capture. */
+ * (zeroed) besides the scratch of bw_stack_create.  It captures one step per
+ * context bucket (contexts up to 128 and up to 1024 positions where the
+ * cache is longer, then any); the stack counts its tokens on the host (reset
+ * by bw_stack_reset_kv) and replays the graph of the token's bucket, whose
+ * attention launches have fewer and smaller CTAs for short contexts.  The
+ * kernels read the position from device memory: write it only through this
+ * API.  Synchronising; call it before any stream capture. */
 bw_status bw_stack_create_kv(const bw_stack_desc *desc, int max_positions,
                              float theta, bw_stack **stack);
 
@@ -394,7 +399,7 @@ bw_status bw_layer_stack(bw_stack *stack, const float *h_in, int steps,
                          float *h_out, const bw_stack_trace *trace,
                          bw_stream_t stream);
 
-/* Frees the scratch and the graph (synchronises the device through
+/* Frees the scratch and the graphs (synchronises the device through
  * cudaFree).  NULL is accepted. */
 void bw_stack_destroy(bw_stack *stack);
 

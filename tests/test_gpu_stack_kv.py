@@ -53,12 +53,16 @@ def make_kv_stack(bw, n_layers, dim, ffn, nh, nkv, seed, S,
 
 
 @pytest.mark.parametrize("layer,steps,S", [(0, 3, 64), (1, 3, 64),
-                                           (1, 200, 256)])
+                                           (1, 200, 256), (0, 3, 4096),
+                                           (1, 200, 4096)])
 def test_kv_stack_per_stage_parity(bw, layer, steps, S):
     """The trace is of the last token of the call: position 2 (a context the
     attention finishes in one CTA per KV head) and position 199 (200
-    positions in four splits merged across CTAs, the path the bench's
-    256-token runs take past position 127)."""
+    positions in splits merged across CTAs, the path the bench's 256-token
+    runs take past position 127).  With the 4096-position cache the stack
+    replays its short-context graphs: position 2 in a launch of one small
+    CTA per KV head, position 199 in clusters of 8 small CTAs, after 128
+    tokens of the first and 71 of the second."""
     dim, ffn, nh, nkv = 2560, 6912, 20, 5
     hd = dim // nh
     qkv_n = (nh + 2 * nkv) * hd
