@@ -129,6 +129,32 @@ def test_kv_stack_per_stage_parity(bw, layer, steps, S):
     stack.close()
 
 
+def test_kv_stack_short_context_graphs_equal_the_full_cache_launch(bw):
+    """Tokens 0..255 through two stacks with the same weights.  With a
+    4096-position cache the stack replays its short-context graphs: to
+    position 127 one 128-row CTA per KV head, then clusters of 8 CTAs of
+    128 rows (the switch between the two inside one call).  With a
+    256-position cache it replays its own short graph to position 127, then
+    its full-cache graph: clusters of 8 CTAs of the 256-row staging.  Past
+    position 127 both split the positions over the same CTAs and merge them
+    alike, so the outputs and the caches are bit-identical."""
+    dim, ffn, nh, nkv = 2560, 6912, 20, 5
+    steps = 256
+    h = to_dev(synth.step_inputs(13, steps, dim))
+    outs, caches = [], []
+    for S in (4096, 256):
+        stack, _ = make_kv_stack(bw, 2, dim, ffn, nh, nkv, 45, S,
+                                 gamma_one=False)
+        outs.append(stack.run(h).clone())
+        assert bw.bw_device_error() == 0
+        k, v = stack.read_kv(1)
+        caches.append((k[:, :steps].clone(), v[:, :steps].clone()))
+        stack.close()
+    assert torch.equal(outs[0], outs[1])
+    assert torch.equal(caches[0][0], caches[1][0])
+    assert torch.equal(caches[0][1], caches[1][1])
+
+
 def test_kv_stack_graph_steps_equal_eager_and_reset_restarts(bw):
     dim, ffn, nh, nkv, S = 512, 1024, 4, 1, 16
     qkv_n = (nh + 2 * nkv) * (dim // nh)
