@@ -476,36 +476,66 @@ gemm_kernel(const __grid_constant__ CUtensorMap wmap,
             bool fast = true;
 #pragma unroll
             for (int i = 0; i < 16; ++i) fast = fast && rv[i] != 0.0f;
+            // All 16 results first, as independent straight-line chains
+            // (tokens past M have s = r = 1 and no token sum, and are never
+            // stored), then the stores, in pairs of tokens.
+            float yv[16];
+            if (ACC) {
 #pragma unroll
-            for (int e = 0; e < 16; e += 2) {
-              const int m = m0 + j0 + hb + e;
-              if (m >= M) break;
-              const float a0 =
-                  fmaf(__uint_as_float(d[hb + e]), 16777216.0f, nsx[e]);
-              const float a1 =
-                  fmaf(__uint_as_float(d[hb + e + 1]), 16777216.0f, nsx[e + 1]);
+              for (int e = 0; e < 16; ++e)
+                yv[e] = fmaf(__uint_as_float(d[hb + e]), 16777216.0f, nsx[e]);
+            } else if (fast) {
+#pragma unroll
+              for (int e = 0; e < 16; ++e)
+                yv[e] = div_by_recip(fmaf(__uint_as_float(d[hb + e]),
+                                          16777216.0f, nsx[e]),
+                                     sv[e], rv[e]) *
+                        wsv;
+            } else {
+#pragma unroll
+              for (int e = 0; e < 16; ++e) {
+                const float a =
+                    fmaf(__uint_as_float(d[hb + e]), 16777216.0f, nsx[e]);
+                yv[e] = (rv[e] != 0.0f ? div_by_recip(a, sv[e], rv[e])
+                                       : a / sv[e]) *
+                        wsv;
+              }
+            }
+            const int mh = m0 + j0 + hb;  // the half's first token
+            const size_t ld = size_t(g.out_ld);
+            if (mh + 16 <= M) {  // warp-uniform: the whole half is stored
               if (ACC) {
-                int *o = static_cast<int *>(g.out) + size_t(m) * g.out_ld + n;
-                o[0] = __float2int_rn(a0);
-                if (m + 1 < M) o[g.out_ld] = __float2int_rn(a1);
+                int *o = static_cast<int *>(g.out) + size_t(mh) * ld + n;
+#pragma unroll
+                for (int e = 0; e < 16; ++e) o[e * ld] = __float2int_rn(yv[e]);
               } else {
-                float q0, q1;
-                if (fast) {
-                  q0 = div_by_recip(a0, sv[e], rv[e]);
-                  q1 = div_by_recip(a1, sv[e + 1], rv[e + 1]);
-                } else {
-                  q0 = rv[e] != 0.0f ? div_by_recip(a0, sv[e], rv[e])
-                                     : a0 / sv[e];
-                  q1 = rv[e + 1] != 0.0f
-                           ? div_by_recip(a1, sv[e + 1], rv[e + 1])
-                           : a1 / sv[e + 1];
+                __nv_bfloat16 *o =
+                    static_cast<__nv_bfloat16 *>(g.out) + size_t(mh) * ld + n;
+#pragma unroll
+                for (int e = 0; e < 16; e += 2) {
+                  const __nv_bfloat162 y2 =
+                      __floats2bfloat162_rn(yv[e], yv[e + 1]);
+                  o[e * ld] = y2.x;
+                  o[(e + 1) * ld] = y2.y;
                 }
-                const __nv_bfloat162 y2 =
-                    __floats2bfloat162_rn(q0 * wsv, q1 * wsv);
-                __nv_bfloat16 *o = static_cast<__nv_bfloat16 *>(g.out) +
-                                   size_t(m) * g.out_ld + n;
-                o[0] = y2.x;
-                if (m + 1 < M) o[g.out_ld] = y2.y;
+              }
+            } else {
+#pragma unroll
+              for (int e = 0; e < 16; e += 2) {
+                const int m = mh + e;
+                if (m >= M) break;
+                if (ACC) {
+                  int *o = static_cast<int *>(g.out) + size_t(m) * ld + n;
+                  o[0] = __float2int_rn(yv[e]);
+                  if (m + 1 < M) o[ld] = __float2int_rn(yv[e + 1]);
+                } else {
+                  const __nv_bfloat162 y2 =
+                      __floats2bfloat162_rn(yv[e], yv[e + 1]);
+                  __nv_bfloat16 *o = static_cast<__nv_bfloat16 *>(g.out) +
+                                     size_t(m) * ld + n;
+                  o[0] = y2.x;
+                  if (m + 1 < M) o[ld] = y2.y;
+                }
               }
             }
           }
