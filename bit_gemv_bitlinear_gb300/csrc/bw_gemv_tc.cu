@@ -201,19 +201,27 @@ tc_gemv_kernel(const __grid_constant__ CUtensorMap wmap,
     for (int j0 = p * quarter; j0 < (p + 1) * quarter; j0 += 4) {
       float d[4];
       tmem_ld4(t_lane + kTcDCol + uint32_t(j0), d);  // whole warp
+      if (n >= g.N) continue;
+      // the 4 results first (a token past `rows` reads row rows - 1's
+      // values and is not stored), then the stores
+      int tv[4];
+      float yv[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int m = min(j0 + e, rows - 1);
+        tv[e] = __float2int_rn(d[e] * 16777216.0f) - sx_sm[m] -
+                sx_sm[kTcMaxTokens + m];
+        if (!ACC) yv[e] = (static_cast<float>(tv[e]) / s_sm[m]) * wsv;
+      }
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
         const int m = j0 + e;
-        if (m >= rows || n >= g.N) continue;
-        const int total = __float2int_rn(d[e] * 16777216.0f) - sx_sm[m] -
-                          sx_sm[kTcMaxTokens + m];
-        if (ACC) {
-          static_cast<int *>(g.out)[size_t(m) * g.out_ld + n] = total;
-        } else {
-          const float scaled = static_cast<float>(total) / s_sm[m];
+        if (m >= rows) break;
+        if (ACC)
+          static_cast<int *>(g.out)[size_t(m) * g.out_ld + n] = tv[e];
+        else
           static_cast<__nv_bfloat16 *>(g.out)[size_t(m) * g.out_ld + n] =
-              __float2bfloat16_rn(scaled * wsv);
-        }
+              __float2bfloat16_rn(yv[e]);
       }
     }
   };
