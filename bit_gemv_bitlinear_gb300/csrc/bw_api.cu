@@ -29,7 +29,7 @@ bw_status check_mnk(int M, int N, int K) {
 }
 
 constexpr int kMaxDevices = 64;
-int g_sm_count[kMaxDevices];
+std::atomic<int> g_sm_count[kMaxDevices];  // 0: not queried yet
 
 // The checks every product entry point makes (pointers, shape, scale
 // segments, alignment); fills the segments.
@@ -213,14 +213,14 @@ int device_sm_count() {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices)
     return 0;
-  if (g_sm_count[dev] == 0) {
-    int n = 0;
+  int n = g_sm_count[dev].load(std::memory_order_relaxed);
+  if (n == 0) {
     if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) !=
         cudaSuccess)
       return 0;
-    g_sm_count[dev] = n;
+    g_sm_count[dev].store(n, std::memory_order_relaxed);
   }
-  return g_sm_count[dev];
+  return n;
 }
 
 void record_cuda_error(int err) { g_last_cuda_error = err; }

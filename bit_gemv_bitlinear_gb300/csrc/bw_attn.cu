@@ -1084,8 +1084,8 @@ attn_cluster_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap kmap,
 // per device and size).
 template <int G, int kChunk>
 bool cluster_ok(int dev) {
-  static int state[64];  // 0 unknown, 1 yes, 2 no
-  if (state[dev] == 0) {
+  static std::atomic<int> state[64];  // 0 unknown, 1 yes, 2 no
+  if (state[dev].load(std::memory_order_relaxed) == 0) {
     auto kernel = attn_cluster_kernel<G, kChunk>;
     constexpr size_t kSmem = ClSmem<G, kChunk>::kBytes + 1024;
     bool ok =
@@ -1113,9 +1113,9 @@ bool cluster_ok(int dev) {
            clusters >= 1;
     }
     cudaGetLastError();  // a refused query is not an error of the call
-    state[dev] = ok ? 1 : 2;
+    state[dev].store(ok ? 1 : 2, std::memory_order_relaxed);
   }
-  return state[dev] == 1;
+  return state[dev].load(std::memory_order_relaxed) == 1;
 }
 
 template <int G, int kChunk>
@@ -1168,18 +1168,18 @@ bool try_cluster(int G, int dev, const AttnArgs &a, const CUtensorMap &kmap,
 template <int G>
 cudaError_t launch_g(const AttnArgs &a, const CUtensorMap &kmap,
                      const CUtensorMap &vmap, cudaStream_t stream) {
-  static bool configured[64];
+  static std::atomic<bool> configured[64];
   auto kernel = attn_decode_kernel<G>;
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-  if (!configured[dev]) {
+  if (!configured[dev].load(std::memory_order_relaxed)) {
     e = cudaFuncSetAttribute(kernel,
                              cudaFuncAttributeMaxDynamicSharedMemorySize,
                              int(AttnSmem<G>::kBytes + 1024));
     if (e != cudaSuccess) return e;
-    configured[dev] = true;
+    configured[dev].store(true, std::memory_order_relaxed);
   }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(unsigned(a.n_split), unsigned(a.Hkv));

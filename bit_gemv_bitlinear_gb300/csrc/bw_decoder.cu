@@ -816,7 +816,7 @@ cudaError_t launch_selftest_poll(cudaStream_t stream) {
 }
 
 cudaError_t launch_decoder(const DecoderLaunch &l, cudaStream_t stream) {
-  static bool configured[64];
+  static std::atomic<bool> configured[64];
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
@@ -825,12 +825,12 @@ cudaError_t launch_decoder(const DecoderLaunch &l, cudaStream_t stream) {
   if (sms <= 0) return cudaErrorNoDevice;
   const DecShape d =
       decoder_shape(l.dim, l.ffn, l.n_heads, l.n_kv, l.n_layers, sms);
-  if (!configured[dev]) {
+  if (!configured[dev].load(std::memory_order_relaxed)) {
     e = cudaFuncSetAttribute(decoder_kernel,
                              cudaFuncAttributeMaxDynamicSharedMemorySize,
                              227 * 1024);
     if (e != cudaSuccess) return e;
-    configured[dev] = true;
+    configured[dev].store(true, std::memory_order_relaxed);
   }
   int per_sm = 0;
   e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, decoder_kernel,

@@ -556,7 +556,7 @@ size_t align256(size_t b) { return (b + 255) / 256 * 256; }
 template <bool ACC, int T>
 cudaError_t launch_gemm_t(const GemvArgs &g, int M, void *workspace,
                           cudaStream_t stream) {
-  static bool configured[64];
+  static std::atomic<bool> configured[64];
   using Cfg = GmCfg<T>;
   unsigned int *err = device_error_word();
   if (!err) return cudaErrorInvalidSymbol;

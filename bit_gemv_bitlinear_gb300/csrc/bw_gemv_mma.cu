@@ -364,7 +364,7 @@ bool mma_config(int K, int *mt, int *piece) {
 template <int MT, bool ACC>
 cudaError_t launch_tile(const GemvArgs &g, int rows, int piece,
                         cudaStream_t stream) {
-  static bool configured[64];
+  static std::atomic<bool> configured[64];
   auto kernel = pipe_mma_kernel<MT, ACC>;
   PipeArgs a{};
   a.w = g.w;

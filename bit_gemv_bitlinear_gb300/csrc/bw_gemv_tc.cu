@@ -498,7 +498,7 @@ tc_gemv_kernel(const __grid_constant__ CUtensorMap wmap,
 
 template <bool ACC, class Cfg>
 cudaError_t launch_tc(const GemvArgs &g, int rows, int T, cudaStream_t stream) {
-  static bool configured[64];
+  static std::atomic<bool> configured[64];
   auto kernel = tc_gemv_kernel<ACC, Cfg>;
   unsigned int *err = device_error_word();
   if (!err) return cudaErrorInvalidSymbol;

@@ -2,6 +2,8 @@
 // Nothing here is visible through the C ABI (include/bw.h).
 #pragma once
 
+#include <atomic>
+
 #include <cuda_runtime.h>
 #include <cuda_bf16.h>
 #include <stdint.h>

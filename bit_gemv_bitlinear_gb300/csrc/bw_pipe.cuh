@@ -542,19 +542,22 @@ struct EpiOut {
 
 // Sets the opt-in shared-memory size once per device and returns how many
 // CTAs of `kernel` are resident on the device at once (at least one).
+// configured: the caller's per-device flags for this kernel (host threads
+// may race on them; setting the attribute twice is harmless).
 template <class Kernel>
-cudaError_t resident_ctas(Kernel kernel, bool *configured, int threads,
+cudaError_t resident_ctas(Kernel kernel, std::atomic<bool> *configured,
+                          int threads,
                           uint32_t smem, int64_t *resident) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-  if (!configured[dev]) {
+  if (!configured[dev].load(std::memory_order_relaxed)) {
     e = cudaFuncSetAttribute(kernel,
                              cudaFuncAttributeMaxDynamicSharedMemorySize,
                              227 * 1024);
     if (e != cudaSuccess) return e;
-    configured[dev] = true;
+    configured[dev].store(true, std::memory_order_relaxed);
   }
   int per_sm = 0;
   if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, threads,
@@ -591,7 +594,7 @@ inline uint32_t pipe_smem_bytes(int mt, int chunks, int slot_chunks,
 template <int MT, class Pro, class Epi, class Dot = DotDp4a>
 cudaError_t launch_pipe(PipeArgs a, const Pro &pro, const Epi &epi,
                         cudaStream_t stream, int *grid_out = nullptr) {
-  static bool configured[64];
+  static std::atomic<bool> configured[64];
   auto kernel = pipe_gemv_kernel<MT, Pro, Epi, Dot>;
   a.slot_chunks = kPipeSlotChunks;
   if (a.slots < 1) a.slots = kPipeDefaultSlots;
