@@ -39,6 +39,8 @@
 //   It may use CTA barriers and the 64 floats at `red`.
 #pragma once
 
+#include <type_traits>
+
 #include "bw_internal.cuh"
 
 namespace bw {
@@ -220,16 +222,26 @@ struct PipeLayout {
   uint32_t ring, xs, sums, red, tot, bars, total;
 };
 
+// Chunks of the longest warp run of a CTA with k groups of `chunks` chunks.
+__host__ __device__ inline int max_run_chunks(int k, int chunks, int warps) {
+  return (k * chunks + warps - 1) / warps;
+}
+
+// xs: the staged activations, [MT][chunks] chunks for the CTA, or (per-warp
+// staging) [warps][MT][max run] chunks, each warp its own run's;
 // sums: [MT] activation scales s, [BW_MAX_WS] weight scales (as fp32),
 // [warps][MT] per-warp activation sums; red: 64 floats of prologue
 // reduction scratch; tot: [k][MT][8] row totals; bars: the ring barriers.
 __host__ __device__ inline PipeLayout pipe_layout(
     int mt, int chunks, int slot_chunks, int slots, int warps, int k,
-    uint32_t xs_chunk_bytes = DotDp4a::kXsChunkBytes) {
+    uint32_t xs_chunk_bytes = DotDp4a::kXsChunkBytes, int per_warp_x = 0) {
   PipeLayout l;
   l.ring = 0;
   l.xs = uint32_t(warps * slots * slot_chunks) * kGroupChunkBytes;
-  l.sums = l.xs + uint32_t(mt) * uint32_t(chunks) * xs_chunk_bytes;
+  const uint32_t xs_chunks =
+      per_warp_x ? uint32_t(warps) * uint32_t(max_run_chunks(k, chunks, warps))
+                 : uint32_t(chunks);
+  l.sums = l.xs + uint32_t(mt) * xs_chunks * xs_chunk_bytes;
   const uint32_t sums_bytes = uint32_t((mt + BW_MAX_WS + warps * mt) * 4);
   l.red = (l.sums + sums_bytes + 15) / 16 * 16;
   l.tot = l.red + 64 * 4;
@@ -286,7 +298,30 @@ struct PipeArgs {
   int groups_per_cta;   // k
   int pair_half;        // 0, or H: group order 0, H, 1, H + 1, ... (2H groups)
   unsigned int *err;    // device error word (time-out bits)
+  // 1: each warp stages only the activations of its own run, which lies in
+  // one row group of every CTA (launch_pipe decides; prologues with
+  // kPerWarpX only)
+  int per_warp_x;
 };
+
+// Whether each of the 8 warp runs of a CTA with n_g groups of `chunks`
+// chunks lies within a single row group (empty runs do).
+__host__ __device__ inline bool runs_in_one_group(int n_g, int chunks,
+                                                  int warps) {
+  const int U = n_g * chunks;
+  for (int w = 0; w < warps; ++w) {
+    const int lo = U * w / warps, hi = U * (w + 1) / warps;
+    if (hi > lo && lo / chunks != (hi - 1) / chunks) return false;
+  }
+  return true;
+}
+
+// Prologue policies that can stage per warp declare kPerWarpX = true.
+template <class P, class = void>
+struct has_per_warp_x : std::false_type {};
+template <class P>
+struct has_per_warp_x<P, std::void_t<decltype(P::kPerWarpX)>>
+    : std::integral_constant<bool, P::kPerWarpX> {};
 
 // Physical row group of the g-th group in streaming order.  With pair_half
 // H the two halves of the rows are interleaved group by group, so that a
@@ -349,7 +384,10 @@ __device__ __forceinline__ float cta_max(float v, float *red) {
   return t;
 }
 
-template <int MT, class Pro, class Epi, class Dot = DotDp4a>
+// kPW: the per-warp activation staging (a.per_warp_x set; prologues with
+// kPerWarpX only), a kernel of its own so that the CTA-wide form keeps its
+// registers.
+template <int MT, class Pro, class Epi, class Dot = DotDp4a, bool kPW = false>
 __global__ void __launch_bounds__(kPipeWarps * 32)
 pipe_gemv_kernel(const PipeArgs a, const Pro pro, const Epi epi) {
   extern __shared__ __align__(128) uint8_t smem[];
@@ -361,8 +399,10 @@ pipe_gemv_kernel(const PipeArgs a, const Pro pro, const Epi epi) {
   const int k = a.groups_per_cta;
   const uint32_t slot_bytes = uint32_t(KS) * kGroupChunkBytes;
   const uint32_t xrow = xs_row_bytes(C);
-  const PipeLayout L =
-      pipe_layout(MT, C, KS, R, kPipeWarps, k, Dot::kXsChunkBytes);
+  constexpr bool kCanPerWarp = kPW && has_per_warp_x<Pro>::value;
+  constexpr bool per_warp = kCanPerWarp;
+  const PipeLayout L = pipe_layout(MT, C, KS, R, kPipeWarps, k,
+                                   Dot::kXsChunkBytes, per_warp ? 1 : 0);
   uint8_t *ring = smem + L.ring + size_t(warp) * R * slot_bytes;
   int8_t *xs = reinterpret_cast<int8_t *>(smem + L.xs);
   float *s_sm = reinterpret_cast<float *>(smem + L.sums);
@@ -403,6 +443,15 @@ pipe_gemv_kernel(const PipeArgs a, const Pro pro, const Epi epi) {
     for (int s = 0; s < R && iss.u < run_hi; ++s) issue_next(s);
   }
   for (int t = threadIdx.x; t < n_g * MT * 8; t += blockDim.x) tot[t] = 0;
+  // Per-warp staging: this warp's run lies in one row group, chunks
+  // [xc_lo, xc_lo + run length) of it; the warp stages those activations in
+  // its own region and needs no CTA barrier after the dependency wait, so
+  // the zeroed totals are published before it.
+  const int xc_lo = run_lo - (run_lo / C) * C;
+  const int max_run = max_run_chunks(k, C, kPipeWarps);
+  const uint32_t xrow_w = uint32_t(max_run) * Dot::kXsChunkBytes;
+  int8_t *xs_w = xs + size_t(warp) * MT * xrow_w;
+  if (per_warp) __syncthreads();
   const typename Pro::Pre pro_pre = pro.pre_wait();
   pdl_wait();
   // Dependents may start their pre-wait part (their own weight requests)
@@ -415,17 +464,27 @@ pipe_gemv_kernel(const PipeArgs a, const Pro pro, const Epi epi) {
   const float wsv = epi.scale_value();
   const float4 pre = epi.prefetch(a, g_lo, n_g);
   int part[MT];
-  const StageCtx sc{xs, xrow, C, s_sm, red};
-  pro.template stage<MT>(pro_pre, sc, part);
-  if (threadIdx.x < BW_MAX_WS) ws_sm[threadIdx.x] = wsv;
+  int xsum[MT];  // per-warp staging: sum of the staged activations per row
 #pragma unroll
-  for (int m = 0; m < MT; ++m) {
+  for (int m = 0; m < MT; ++m) xsum[m] = 0;
+  if constexpr (kCanPerWarp) {
+    pro.template stage_warp<MT>(pro_pre, xs_w, xrow_w, xc_lo,
+                                xc_lo + (run_hi - run_lo), s_sm, xsum);
+    if (threadIdx.x < BW_MAX_WS) ws_sm[threadIdx.x] = wsv;
+    __syncwarp();  // the warp's activations staged, its barriers set up
+  } else {
+    const StageCtx sc{xs, xrow, C, s_sm, red};
+    pro.template stage<MT>(pro_pre, sc, part);
+    if (threadIdx.x < BW_MAX_WS) ws_sm[threadIdx.x] = wsv;
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1)
-      part[m] += __shfl_xor_sync(0xffffffffu, part[m], o);
-    if (lane == 0) sx_part[warp * MT + m] = part[m];
+    for (int m = 0; m < MT; ++m) {
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1)
+        part[m] += __shfl_xor_sync(0xffffffffu, part[m], o);
+      if (lane == 0) sx_part[warp * MT + m] = part[m];
+    }
+    __syncthreads();  // activations staged, totals zeroed, barriers set up
   }
-  __syncthreads();  // activations staged, totals zeroed, barriers set up
 
   const int q = lane >> 3;  // chunk residue (relative to the piece) mod 4
   const int r = lane & 7;   // row inside the group
@@ -444,8 +503,12 @@ pipe_gemv_kernel(const PipeArgs a, const Pro pro, const Epi epi) {
       break;
     }
     const int len = cur.piece(KS, C, run_hi);
-    Dot::template run<MT>(ring + size_t(slot) * slot_bytes, xs, xrow, cur.c,
-                          len, q, r, acc);
+    if (per_warp)
+      Dot::template run<MT>(ring + size_t(slot) * slot_bytes, xs_w, xrow_w,
+                            cur.c - xc_lo, len, q, r, acc);
+    else
+      Dot::template run<MT>(ring + size_t(slot) * slot_bytes, xs, xrow, cur.c,
+                            len, q, r, acc);
     __syncwarp();
     if (lane == 0 && iss.u < run_hi) {  // piece consumed + R: this slot
       fence_proxy_async_smem();
@@ -457,7 +520,9 @@ pipe_gemv_kernel(const PipeArgs a, const Pro pro, const Epi epi) {
     if (cur.c == 0 || cur.u == run_hi) {  // row group or run finished
 #pragma unroll
       for (int m = 0; m < MT; ++m) {
-        const int v = Dot::fold(acc[m]);
+        // per-warp staging: the run is this group's only fold, and the sum
+        // of the activations it covered comes off here
+        const int v = Dot::fold(acc[m]) - xsum[m];
         if (q == 0) atomicAdd(&tot[(g * MT + m) * 8 + r], v);
 #pragma unroll
         for (int t = 0; t < 4; ++t) acc[m][t] = 0;
@@ -476,12 +541,13 @@ pipe_gemv_kernel(const PipeArgs a, const Pro pro, const Epi epi) {
   }
   __syncthreads();  // every partial sum is in `tot`
 
-  int sx[MT];  // sum_k x[m][k] over the whole row
+  int sx[MT];  // sum_k x[m][k] over the whole row (per-warp: already off)
 #pragma unroll
   for (int m = 0; m < MT; ++m) {
     sx[m] = 0;
+    if (!per_warp)
 #pragma unroll
-    for (int w = 0; w < kPipeWarps; ++w) sx[m] += sx_part[w * MT + m];
+      for (int w = 0; w < kPipeWarps; ++w) sx[m] += sx_part[w * MT + m];
   }
   epi.template finish<MT>(a, tot, sx, g_lo, n_g, s_sm, ws_sm, red, pre);
 }
@@ -579,9 +645,10 @@ constexpr int kPipeDefaultSlots = 2;
 // is at most 227 KB for k = kPipeMaxGroupsPerCta.
 inline uint32_t pipe_smem_bytes(int mt, int chunks, int slot_chunks,
                                 int slots, int k,
-                                uint32_t xs_chunk_bytes = DotDp4a::kXsChunkBytes) {
+                                uint32_t xs_chunk_bytes = DotDp4a::kXsChunkBytes,
+                                int per_warp_x = 0) {
   return pipe_layout(mt, chunks, slot_chunks, slots, kPipeWarps, k,
-                     xs_chunk_bytes)
+                     xs_chunk_bytes, per_warp_x)
       .total;
 }
 
@@ -591,11 +658,17 @@ inline uint32_t pipe_smem_bytes(int mt, int chunks, int slot_chunks,
 // runs in waves; even with pair_half), and pieces no longer than a warp's
 // run.  Fills in the split fields of `a`; *grid_out (if set) receives the
 // number of CTAs.
+// Per-warp staging is taken where every run of every CTA lies in one row
+// group, the per-warp activation regions stay small (at most 16 KB a CTA)
+// and the CTAs resident per SM do not drop.
+constexpr uint32_t kPipeMaxPerWarpXs = 16u * 1024u;
+
 template <int MT, class Pro, class Epi, class Dot = DotDp4a>
 cudaError_t launch_pipe(PipeArgs a, const Pro &pro, const Epi &epi,
                         cudaStream_t stream, int *grid_out = nullptr) {
   static std::atomic<bool> configured[64];
-  auto kernel = pipe_gemv_kernel<MT, Pro, Epi, Dot>;
+  static std::atomic<bool> configured_pw[64];
+  auto kernel = pipe_gemv_kernel<MT, Pro, Epi, Dot, false>;
   a.slot_chunks = kPipeSlotChunks;
   if (a.slots < 1) a.slots = kPipeDefaultSlots;
   // k from the residency at k = 1, then once more at that k (the row
@@ -618,17 +691,48 @@ cudaError_t launch_pipe(PipeArgs a, const Pro &pro, const Epi &epi,
   if (run < a.slot_chunks) a.slot_chunks = int(run < 1 ? 1 : run);
   a.groups_per_cta = int(k);
   if (grid_out) *grid_out = int(grid);
+  a.per_warp_x = 0;
+  if constexpr (has_per_warp_x<Pro>::value) {
+    const int last_groups = int(a.n_groups - (grid - 1) * k);
+    const uint32_t pw_xs = uint32_t(kPipeWarps) * uint32_t(MT) *
+                           uint32_t(max_run_chunks(int(k), a.chunks, kPipeWarps)) *
+                           Dot::kXsChunkBytes;
+    if (pro.per_warp_capable() && pw_xs <= kPipeMaxPerWarpXs &&
+        runs_in_one_group(int(k), a.chunks, kPipeWarps) &&
+        runs_in_one_group(last_groups, a.chunks, kPipeWarps)) {
+      auto kernel_pw = pipe_gemv_kernel<MT, Pro, Epi, Dot, true>;
+      int64_t resident_pw = 0;
+      const cudaError_t e = resident_ctas(
+          kernel_pw, configured_pw, kPipeWarps * 32,
+          pipe_smem_bytes(MT, a.chunks, a.slot_chunks, a.slots, int(k),
+                          Dot::kXsChunkBytes, 1),
+          &resident_pw);
+      if (e != cudaSuccess) return e;
+      int64_t resident_now = 0;
+      const cudaError_t e2 = resident_ctas(
+          kernel, configured, kPipeWarps * 32,
+          pipe_smem_bytes(MT, a.chunks, a.slot_chunks, a.slots, int(k),
+                          Dot::kXsChunkBytes),
+          &resident_now);
+      if (e2 != cudaSuccess) return e2;
+      if (resident_pw >= resident_now) a.per_warp_x = 1;
+    }
+  }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(unsigned(grid > 0 ? grid : 1));
   cfg.blockDim = dim3(kPipeWarps * 32);
-  cfg.dynamicSmemBytes = pipe_smem_bytes(MT, a.chunks, a.slot_chunks,
-                                         a.slots, int(k), Dot::kXsChunkBytes);
+  cfg.dynamicSmemBytes =
+      pipe_smem_bytes(MT, a.chunks, a.slot_chunks, a.slots, int(k),
+                      Dot::kXsChunkBytes, a.per_warp_x);
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
+  if (a.per_warp_x)
+    return cudaLaunchKernelEx(&cfg, pipe_gemv_kernel<MT, Pro, Epi, Dot, true>,
+                              a, pro, epi);
   return cudaLaunchKernelEx(&cfg, kernel, a, pro, epi);
 }
 
