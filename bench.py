@@ -59,8 +59,8 @@ FALLBACK_HBM_GBS = 6800.0
 TRAFFIC_SOURCES = ("bit_gemv_bitlinear_gb300/csrc/bw_pipe.cuh",
                    "bit_gemv_bitlinear_gb300/csrc/bw_gemv_tma.cu")
 MEASURED_DRAM = {
-    "sha256": "a7e0b88bbde98c4391974ba1bcdc58049f614aac80f6b731bfd96d79183afe79",
-    "bytes": {"wqkv": 2487936, "wo": 1668608, "w13": 8877568, "w2": 4457728}}
+    "sha256": "5783881dfa787d5380204c05f2ffdecfb531f6daa0f40159afb8219ce53fb4a2",
+    "bytes": {"wqkv": 2482560, "wo": 1663360, "w13": 8877568, "w2": 4452992}}
 
 
 def traffic_sources_sha() -> str:
