@@ -97,49 +97,61 @@ struct StageInt8 {
   }
 
   // Per-warp staging (PipeArgs::per_warp_x): a warp loads only the chunks
-  // [c_lo, c_hi) its run covers, into its own region (row stride xrow_w),
-  // and returns their sum per row; it needs 16-byte aligned rows.
+  // its run covers -- [a_lo, a_lo + len_a) of a row, then [0, len_b) (the
+  // start of the next row group's) -- into its own region (row stride
+  // xrow_w), in that order, and returns the two segments' sums per row; it
+  // needs 16-byte aligned rows.
   static constexpr bool kPerWarpX = true;
   __host__ __device__ bool per_warp_capable() const { return vec_x != 0; }
   template <int MT>
   __device__ __forceinline__ void stage_warp(const Pre &, int8_t *xw,
-                                             uint32_t xrow_w, int c_lo,
-                                             int c_hi, float *s_sm,
-                                             int (&xsum)[MT]) const {
+                                             uint32_t xrow_w, int a_lo,
+                                             int len_a, int len_b,
+                                             float *s_sm, int (&xsum_a)[MT],
+                                             int (&xsum_b)[MT]) const {
     constexpr int kBatch = 4;
     const int lane = threadIdx.x & 31;
     const float sv = (s && threadIdx.x < MT) ? s[threadIdx.x] : 0.0f;
-    const int nv = (c_hi - c_lo) * 4;  // 16-byte vectors of a row
+    const int nv = (len_a + len_b) * 4;  // 16-byte vectors of a row
+    const int va = len_a * 4;            // of them in the first segment
+    const int kv = K / 16;               // vectors inside K (K % 16 == 0)
 #pragma unroll
     for (int m = 0; m < MT; ++m) {
-      const uint4 *src =
-          reinterpret_cast<const uint4 *>(x + size_t(m) * x_ld) + c_lo * 4;
+      const uint4 *src = reinterpret_cast<const uint4 *>(x + size_t(m) * x_ld);
       uint4 *dst = reinterpret_cast<uint4 *>(xw + m * xrow_w);
-      const int v_end = K / 16 - c_lo * 4;  // vectors inside K (K % 16 == 0)
-      int p = 0;
+      int pa = 0, pb = 0;
       for (int v0 = lane; v0 < nv; v0 += kBatch * 32) {
         uint4 x4[kBatch];
 #pragma unroll
         for (int b = 0; b < kBatch; ++b) {
           const int v = v0 + b * 32;
-          x4[b] = (v < nv && v < v_end) ? __ldg(src + v)
-                                        : make_uint4(0u, 0u, 0u, 0u);
+          const int gv = v < va ? a_lo * 4 + v : v - va;  // vector of the row
+          x4[b] = (v < nv && gv < kv) ? __ldg(src + gv)
+                                      : make_uint4(0u, 0u, 0u, 0u);
         }
 #pragma unroll
         for (int b = 0; b < kBatch; ++b) {
           const int v = v0 + b * 32;
           if (v < nv) {
             dst[v] = x4[b];
-            p = dp4a_us(0x01010101u, x4[b].x, p);
-            p = dp4a_us(0x01010101u, x4[b].y, p);
-            p = dp4a_us(0x01010101u, x4[b].z, p);
-            p = dp4a_us(0x01010101u, x4[b].w, p);
+            int t = dp4a_us(0x01010101u, x4[b].x, 0);
+            t = dp4a_us(0x01010101u, x4[b].y, t);
+            t = dp4a_us(0x01010101u, x4[b].z, t);
+            t = dp4a_us(0x01010101u, x4[b].w, t);
+            if (v < va)
+              pa += t;
+            else
+              pb += t;
           }
         }
       }
 #pragma unroll
-      for (int o = 16; o > 0; o >>= 1) p += __shfl_xor_sync(0xffffffffu, p, o);
-      xsum[m] = p;
+      for (int o = 16; o > 0; o >>= 1) {
+        pa += __shfl_xor_sync(0xffffffffu, pa, o);
+        pb += __shfl_xor_sync(0xffffffffu, pb, o);
+      }
+      xsum_a[m] = pa;
+      xsum_b[m] = pb;
     }
     if (s && threadIdx.x < MT) s_sm[threadIdx.x] = sv;
   }

@@ -298,21 +298,20 @@ struct PipeArgs {
   int groups_per_cta;   // k
   int pair_half;        // 0, or H: group order 0, H, 1, H + 1, ... (2H groups)
   unsigned int *err;    // device error word (time-out bits)
-  // 1: each warp stages only the activations of its own run, which lies in
-  // one row group of every CTA (launch_pipe decides; prologues with
+  // 1: each warp stages only the activations of its own run, which touches
+  // at most two row groups of every CTA (launch_pipe decides; prologues with
   // kPerWarpX only)
   int per_warp_x;
 };
 
 // Whether each of the 8 warp runs of a CTA with n_g groups of `chunks`
-// chunks lies within a single row group (empty runs do).
-__host__ __device__ inline bool runs_in_one_group(int n_g, int chunks,
-                                                  int warps) {
+// chunks is at most one row long, so that it touches at most two row groups
+// (the end of one and the start of the next).
+__host__ __device__ inline bool runs_in_two_groups(int n_g, int chunks,
+                                                   int warps) {
   const int U = n_g * chunks;
-  for (int w = 0; w < warps; ++w) {
-    const int lo = U * w / warps, hi = U * (w + 1) / warps;
-    if (hi > lo && lo / chunks != (hi - 1) / chunks) return false;
-  }
+  for (int w = 0; w < warps; ++w)
+    if (U * (w + 1) / warps - U * w / warps > chunks) return false;
   return true;
 }
 
@@ -443,11 +442,15 @@ pipe_gemv_kernel(const PipeArgs a, const Pro pro, const Epi epi) {
     for (int s = 0; s < R && iss.u < run_hi; ++s) issue_next(s);
   }
   for (int t = threadIdx.x; t < n_g * MT * 8; t += blockDim.x) tot[t] = 0;
-  // Per-warp staging: this warp's run lies in one row group, chunks
-  // [xc_lo, xc_lo + run length) of it; the warp stages those activations in
-  // its own region and needs no CTA barrier after the dependency wait, so
-  // the zeroed totals are published before it.
-  const int xc_lo = run_lo - (run_lo / C) * C;
+  // Per-warp staging: this warp's run covers chunks [xa_lo, xa_lo + len_a)
+  // of the CTA's group g_a and chunks [0, len_b) of the next one; the warp
+  // stages those activations in its own region, in that order, and needs no
+  // CTA barrier after the dependency wait, so the zeroed totals are
+  // published before it.
+  const int g_a = run_lo / C;
+  const int xa_lo = run_lo - g_a * C;
+  const int len_a = min(run_hi - run_lo, C - xa_lo);
+  const int len_b = (run_hi - run_lo) - len_a;
   const int max_run = max_run_chunks(k, C, kPipeWarps);
   const uint32_t xrow_w = uint32_t(max_run) * Dot::kXsChunkBytes;
   int8_t *xs_w = xs + size_t(warp) * MT * xrow_w;
@@ -464,12 +467,14 @@ pipe_gemv_kernel(const PipeArgs a, const Pro pro, const Epi epi) {
   const float wsv = epi.scale_value();
   const float4 pre = epi.prefetch(a, g_lo, n_g);
   int part[MT];
-  int xsum[MT];  // per-warp staging: sum of the staged activations per row
+  // per-warp staging: the sums of the staged activations per row, of the
+  // first group's segment and of the next group's
+  int xsum_a[MT], xsum_b[MT];
 #pragma unroll
-  for (int m = 0; m < MT; ++m) xsum[m] = 0;
+  for (int m = 0; m < MT; ++m) xsum_a[m] = xsum_b[m] = 0;
   if constexpr (kCanPerWarp) {
-    pro.template stage_warp<MT>(pro_pre, xs_w, xrow_w, xc_lo,
-                                xc_lo + (run_hi - run_lo), s_sm, xsum);
+    pro.template stage_warp<MT>(pro_pre, xs_w, xrow_w, xa_lo, len_a, len_b,
+                                s_sm, xsum_a, xsum_b);
     if (threadIdx.x < BW_MAX_WS) ws_sm[threadIdx.x] = wsv;
     __syncwarp();  // the warp's activations staged, its barriers set up
   } else {
@@ -505,7 +510,8 @@ pipe_gemv_kernel(const PipeArgs a, const Pro pro, const Epi epi) {
     const int len = cur.piece(KS, C, run_hi);
     if (per_warp)
       Dot::template run<MT>(ring + size_t(slot) * slot_bytes, xs_w, xrow_w,
-                            cur.c - xc_lo, len, q, r, acc);
+                            cur.g == g_a ? cur.c - xa_lo : len_a + cur.c, len,
+                            q, r, acc);
     else
       Dot::template run<MT>(ring + size_t(slot) * slot_bytes, xs, xrow, cur.c,
                             len, q, r, acc);
@@ -520,9 +526,9 @@ pipe_gemv_kernel(const PipeArgs a, const Pro pro, const Epi epi) {
     if (cur.c == 0 || cur.u == run_hi) {  // row group or run finished
 #pragma unroll
       for (int m = 0; m < MT; ++m) {
-        // per-warp staging: the run is this group's only fold, and the sum
-        // of the activations it covered comes off here
-        const int v = Dot::fold(acc[m]) - xsum[m];
+        // per-warp staging: the warp folds each of its (at most two) groups
+        // once, and the sum of the activations it covered there comes off
+        const int v = Dot::fold(acc[m]) - (g == g_a ? xsum_a[m] : xsum_b[m]);
         if (q == 0) atomicAdd(&tot[(g * MT + m) * 8 + r], v);
 #pragma unroll
         for (int t = 0; t < 4; ++t) acc[m][t] = 0;
@@ -658,8 +664,8 @@ inline uint32_t pipe_smem_bytes(int mt, int chunks, int slot_chunks,
 // runs in waves; even with pair_half), and pieces no longer than a warp's
 // run.  Fills in the split fields of `a`; *grid_out (if set) receives the
 // number of CTAs.
-// Per-warp staging is taken where every run of every CTA lies in one row
-// group, the per-warp activation regions stay small (at most 16 KB a CTA)
+// Per-warp staging is taken where every run of every CTA touches at most two
+// row groups, the per-warp activation regions stay small (at most 16 KB a CTA)
 // and the CTAs resident per SM do not drop.
 constexpr uint32_t kPipeMaxPerWarpXs = 16u * 1024u;
 
@@ -698,8 +704,8 @@ cudaError_t launch_pipe(PipeArgs a, const Pro &pro, const Epi &epi,
                            uint32_t(max_run_chunks(int(k), a.chunks, kPipeWarps)) *
                            Dot::kXsChunkBytes;
     if (pro.per_warp_capable() && pw_xs <= kPipeMaxPerWarpXs &&
-        runs_in_one_group(int(k), a.chunks, kPipeWarps) &&
-        runs_in_one_group(last_groups, a.chunks, kPipeWarps)) {
+        runs_in_two_groups(int(k), a.chunks, kPipeWarps) &&
+        runs_in_two_groups(last_groups, a.chunks, kPipeWarps)) {
       auto kernel_pw = pipe_gemv_kernel<MT, Pro, Epi, Dot, true>;
       int64_t resident_pw = 0;
       const cudaError_t e = resident_ctas(
