@@ -59,8 +59,8 @@ FALLBACK_HBM_GBS = 6800.0
 TRAFFIC_SOURCES = ("bit_gemv_bitlinear_gb300/csrc/bw_pipe.cuh",
                    "bit_gemv_bitlinear_gb300/csrc/bw_gemv_tma.cu")
 MEASURED_DRAM = {
-    "sha256": "5783881dfa787d5380204c05f2ffdecfb531f6daa0f40159afb8219ce53fb4a2",
-    "bytes": {"wqkv": 2482560, "wo": 1663360, "w13": 8877568, "w2": 4452992}}
+    "sha256": "c60f34eb1ab76f874b6780efd221acbb02b1c931647fa1f2da4f1543d793331d",
+    "bytes": {"wqkv": 2478848, "wo": 1660032, "w13": 8868736, "w2": 4449536}}
 
 
 def traffic_sources_sha() -> str:
