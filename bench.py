@@ -59,8 +59,8 @@ FALLBACK_HBM_GBS = 6800.0
 TRAFFIC_SOURCES = ("bit_gemv_bitlinear_gb300/csrc/bw_pipe.cuh",
                    "bit_gemv_bitlinear_gb300/csrc/bw_gemv_tma.cu")
 MEASURED_DRAM = {
-    "sha256": "c60f34eb1ab76f874b6780efd221acbb02b1c931647fa1f2da4f1543d793331d",
-    "bytes": {"wqkv": 2478848, "wo": 1660032, "w13": 8868736, "w2": 4449536}}
+    "sha256": "3c98a6960de8fbbe9072a9dc07d6e568f97d69fc9be013c5cd0f8eceb8620333",
+    "bytes": {"wqkv": 2479232, "wo": 1659648, "w13": 8868736, "w2": 4449408}}
 
 
 def traffic_sources_sha() -> str:

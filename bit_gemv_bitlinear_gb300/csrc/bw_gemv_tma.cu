@@ -20,8 +20,11 @@
 //    any order); one epilogue per CTA scales and stores the rows.
 //  * Lane (q, r): row r of the group, chunks j = q (mod 4).  One 128-bit
 //    shared load gives 64 codes (a contiguous 512-byte warp access, no bank
-//    conflict); the int8 activations, staged once in shared memory, come as
-//    four 128-bit broadcast loads per chunk.  Decode = one AND per 4 codes
+//    conflict); the int8 activations, staged in shared memory, come as
+//    four 128-bit broadcast loads per chunk.  Where each warp's run is at
+//    most one row long, every warp stages only the activations of its own
+//    run (stage_warp) and no CTA barrier follows the dependency wait;
+//    otherwise the CTA stages the whole row once (stage).  Decode = one AND per 4 codes
 //    (unsigned codes c = w + 1 masked in place, unsigned x signed dp4a); the
 //    4^i slot factor and the sum_k x offset are removed once per row.
 //  * Every mbarrier wait is bounded (clock64); on time-out the kernel sets
