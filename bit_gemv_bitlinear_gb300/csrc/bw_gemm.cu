@@ -121,31 +121,6 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
       : "memory");
 }
 
-// a / s rounded to nearest even, from r = RN(1 / s): two correction steps
-// of the product a r by its exact residual (fma).  The first brings the
-// quotient within one ulp of a / s, so the second residual is exact and,
-// by P. Markstein's theorem on the final step of division (IBM J. Res.
-// Dev. 34(1), 1990), the second correction is the correctly rounded
-// quotient.  Valid for an integer |a| <= 2^24 and s, r in [2^-60, 2^60]
-// (no intermediate leaves the normal range); the caller divides otherwise.
-// Five FMA-pipe instructions instead of a division per output.
-__device__ __forceinline__ float div_by_recip(float a, float s, float r) {
-  const float q0 = a * r;
-  const float q1 = fmaf(fmaf(-q0, s, a), r, q0);
-  return fmaf(fmaf(-q1, s, a), r, q1);
-}
-
-// 16 bytes of shared memory.  Volatile (kept in order with the barriers and
-// tensor-memory loads around it) but without a memory clobber, so that the
-// compiler need not order it against the epilogue's global stores.
-__device__ __forceinline__ float4 lds4(const void *p) {
-  float4 v;
-  asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
-               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
-               : "r"(smem_addr(p)));
-  return v;
-}
-
 // Barrier among the 8 decode warps only (named barrier 1).
 __device__ __forceinline__ void decode_warps_sync() {
   asm volatile("bar.sync 1, %0;" ::"n"(kGmDecodeWarps * 32) : "memory");

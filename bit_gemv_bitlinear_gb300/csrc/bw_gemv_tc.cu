@@ -103,9 +103,10 @@ using TcCfg128 = TcCfg<128, 2, 2, 2, 320>;
 
 // Shared-memory carve-up (offsets from a 1024-byte aligned base): weight
 // ring, B ring (1024-aligned: the swizzle pattern is taken from the address),
-// token ring, scales, token sums, TMEM address, barriers.
+// token ring, activation scales and their reciprocals, weight scales, token
+// sums, TMEM address, barriers.
 struct TcLayout {
-  uint32_t w, b, x, s, ws, sx, tmem, bars, total;
+  uint32_t w, b, x, s, r, ws, sx, tmem, bars, total;
 };
 
 template <class Cfg>
@@ -114,10 +115,11 @@ __host__ __device__ inline TcLayout tc_layout(int T) {
   l.w = 0;
   l.b = l.w + Cfg::kWStages * kTcWStageBytes;
   l.x = l.b + Cfg::kABStages * uint32_t(T) * 512u;
-  l.s = l.x + Cfg::kXStages * uint32_t(T) * Cfg::kXRow;
-  l.ws = l.s + Cfg::kMaxTokens * 4;
-  l.sx = l.ws + BW_MAX_WS * 4;  // [2 sets][kMaxTokens]
-  l.tmem = l.sx + 2 * Cfg::kMaxTokens * 4;
+  l.s = l.x + Cfg::kXStages * uint32_t(T) * Cfg::kXRow;  // fp32 s[m]
+  l.r = l.s + Cfg::kMaxTokens * 4;                       // fp32 RN(1 / s[m])
+  l.ws = l.r + Cfg::kMaxTokens * 4;
+  l.sx = l.ws + BW_MAX_WS * 4;  // fp32 -sum_k x[m] (both stage sets)
+  l.tmem = l.sx + Cfg::kMaxTokens * 4;
   l.bars = l.tmem + 16;
   l.total = l.bars + 32 * 8;
   return l;
@@ -152,8 +154,9 @@ tc_gemv_kernel(const __grid_constant__ CUtensorMap wmap,
   uint64_t *bar = reinterpret_cast<uint64_t *>(smem + L.bars);
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + L.tmem);
   float *s_sm = reinterpret_cast<float *>(smem + L.s);
+  float *r_sm = reinterpret_cast<float *>(smem + L.r);
   float *ws_sm = reinterpret_cast<float *>(smem + L.ws);
-  int *sx_sm = reinterpret_cast<int *>(smem + L.sx);
+  float *nsx_sm = reinterpret_cast<float *>(smem + L.sx);
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < kTcWStages; ++i) {
@@ -172,6 +175,9 @@ tc_gemv_kernel(const __grid_constant__ CUtensorMap wmap,
     mbar_init(&bar[kBarSums], kTcConvertWarps);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
+  // The two convert sets add their token sums here (before the barrier
+  // below, so that every addition comes after the zero).
+  if (threadIdx.x < kTcMaxTokens) nsx_sm[threadIdx.x] = 0.0f;
   if (warp == kTcMmaWarp) tmem_alloc(tmem_slot, kTcTmemCols);
   tc_fence_before();
   __syncthreads();  // barriers set up, tensor memory allocated
@@ -182,6 +188,9 @@ tc_gemv_kernel(const __grid_constant__ CUtensorMap wmap,
   // is complete: warp (lane quarter q, part p of 4) reads accumulator
   // columns [p T/4, (p + 1) T/4) of weight rows 32 q .. 32 q + 31 and stores
   // acc = 2^24 D - sum_k x as int32 or as bf16((acc / s[m]) * ws[seg(n)]).
+  // acc is exact in fp32 (an integer below 2^23); the quotient is the
+  // correctly rounded one, from the token's reciprocal (div_by_recip) where
+  // s is in its range, else by division.
   auto epilogue = [&](int q, int p) {
     const bool acc_ready = warp_wait(&bar[kBarAcc], 0u);
     const bool sums_ready = warp_wait(&bar[kBarSums], 0u);
@@ -202,16 +211,33 @@ tc_gemv_kernel(const __grid_constant__ CUtensorMap wmap,
       float d[4];
       tmem_ld4(t_lane + kTcDCol + uint32_t(j0), d);  // whole warp
       if (n >= g.N) continue;
-      // the 4 results first (a token past `rows` reads row rows - 1's
-      // values and is not stored), then the stores
+      // the 4 results first (a token past `rows` has s = r = 1 and no token
+      // sum, and is not stored), then the stores
+      const float4 nx = lds4(nsx_sm + j0);
+      const float a[4] = {fmaf(d[0], 16777216.0f, nx.x),
+                          fmaf(d[1], 16777216.0f, nx.y),
+                          fmaf(d[2], 16777216.0f, nx.z),
+                          fmaf(d[3], 16777216.0f, nx.w)};
       int tv[4];
       float yv[4];
+      if (ACC) {
 #pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const int m = min(j0 + e, rows - 1);
-        tv[e] = __float2int_rn(d[e] * 16777216.0f) - sx_sm[m] -
-                sx_sm[kTcMaxTokens + m];
-        if (!ACC) yv[e] = (static_cast<float>(tv[e]) / s_sm[m]) * wsv;
+        for (int e = 0; e < 4; ++e) tv[e] = __float2int_rn(a[e]);
+      } else {
+        const float4 s4 = lds4(s_sm + j0), r4 = lds4(r_sm + j0);
+        const float sv[4] = {s4.x, s4.y, s4.z, s4.w};
+        const float rv[4] = {r4.x, r4.y, r4.z, r4.w};
+        // one branch per 4 tokens, the same in every lane
+        if (rv[0] != 0.0f && rv[1] != 0.0f && rv[2] != 0.0f && rv[3] != 0.0f) {
+#pragma unroll
+          for (int e = 0; e < 4; ++e) yv[e] = div_by_recip(a[e], sv[e], rv[e]) * wsv;
+        } else {
+#pragma unroll
+          for (int e = 0; e < 4; ++e)
+            yv[e] = (rv[e] != 0.0f ? div_by_recip(a[e], sv[e], rv[e])
+                                   : a[e] / sv[e]) *
+                    wsv;
+        }
       }
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
@@ -351,7 +377,11 @@ tc_gemv_kernel(const __grid_constant__ CUtensorMap wmap,
     pdl_trigger();
     {
       const int t = threadIdx.x - kTcDecodeWarps * 32;  // 0..255
-      if (!ACC && t < rows) s_sm[t] = g.s[t];
+      if (!ACC && t < kTcMaxTokens) {
+        const float sv = t < rows ? g.s[t] : 1.0f;
+        s_sm[t] = sv;
+        r_sm[t] = (sv >= 0x1p-60f && sv <= 0x1p60f) ? 1.0f / sv : 0.0f;
+      }
       if (t < BW_MAX_WS)
         ws_sm[t] = t < g.seg.n_ws ? __bfloat162float(g.ws[t]) : 0.0f;
     }
@@ -427,7 +457,8 @@ tc_gemv_kernel(const __grid_constant__ CUtensorMap wmap,
       v += __shfl_xor_sync(0xffffffffu, v, 8);
       v += __shfl_xor_sync(0xffffffffu, v, 16);
       const int m = 2 * (cw + 4 * i) + mpar;
-      if (i < units && (lane & ~4) == 0) sx_sm[set * kTcMaxTokens + m] = v;
+      if (i < units && (lane & ~4) == 0)
+        atomicAdd(&nsx_sm[m], -static_cast<float>(v));  // exact: |v| < 2^22
     }
     __syncwarp();
     if (lane == 0) mbar_arrive(&bar[kBarSums]);

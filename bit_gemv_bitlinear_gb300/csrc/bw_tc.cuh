@@ -2,7 +2,8 @@
 // (bw_gemv_tc.cu, bw_gemm.cu): tensor-memory allocation, MMA issue and
 // commit, tiled TMA loads, shared-memory matrix and instruction
 // descriptors, tensor-memory loads and stores, the 2-bit weight decode into
-// fp16 operands, and the host-side tensor-map encoder.
+// fp16 operands, the epilogues' corrected-reciprocal division and 16-byte
+// shared-memory load, and the host-side tensor-map encoder.
 #pragma once
 
 #include <cuda.h>
@@ -152,6 +153,31 @@ __device__ __forceinline__ void tmem_ld4(uint32_t taddr, float (&v)[4]) {
       : "memory");
 #pragma unroll
   for (int i = 0; i < 4; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+// a / s rounded to nearest even, from r = RN(1 / s): two correction steps
+// of the product a r by its exact residual (fma).  The first brings the
+// quotient within one ulp of a / s, so the second residual is exact and,
+// by P. Markstein's theorem on the final step of division (IBM J. Res.
+// Dev. 34(1), 1990), the second correction is the correctly rounded
+// quotient.  Valid for an integer |a| <= 2^24 and s, r in [2^-60, 2^60]
+// (no intermediate leaves the normal range); the caller divides otherwise.
+// Five FMA-pipe instructions instead of a division per output.
+__device__ __forceinline__ float div_by_recip(float a, float s, float r) {
+  const float q0 = a * r;
+  const float q1 = fmaf(fmaf(-q0, s, a), r, q0);
+  return fmaf(fmaf(-q1, s, a), r, q1);
+}
+
+// 16 bytes of shared memory.  Volatile (kept in order with the barriers and
+// tensor-memory loads around it) but without a memory clobber, so that the
+// compiler need not order it against the epilogue's global stores.
+__device__ __forceinline__ float4 lds4(const void *p) {
+  float4 v;
+  asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
+               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+               : "r"(smem_addr(p)));
+  return v;
 }
 
 __device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t s) {
