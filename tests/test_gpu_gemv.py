@@ -286,6 +286,37 @@ def test_batched_tensor_core_tiles(bw, M, N, K):
     run_case(bw, case)
 
 
+def test_batched_tensor_core_scale_out_of_range(bw):
+    """The tensor-core epilogue multiplies by a stored RN(1 / s) and corrects
+    the product to the IEEE quotient. A token whose s is outside
+    [2^-60, 2^60] is divided instead: row 5, scaled by 1e25. It shares
+    tokens 4..7's group of 4 with three tokens on the corrected path, so
+    both forms run in one group. Row 17, scaled by 1e-20, meets the
+    quantiser's floor on absmax. Within 1 ulp of the oracle, and bit-equal
+    to M = 1 calls on the same rows (the CUDA-core kernel, which divides)."""
+    M, N, K = 24, 1000, 2560
+    canon = synth.canonical_weights(synth.base_seed(24, 0), N, K)
+    packed = bw.bw_repack(to_dev(canon), N, K)
+    xf = synth.normal_f32(synth.base_seed(24, 1), M * K).reshape(M, K)
+    xf[5] *= np.float32(1e25)
+    xf[17] *= np.float32(1e-20)
+    ws = synth.bf16_uniform(synth.base_seed(24, 2), 2)
+    bounds = [0, 333, N]
+    q_d, s_d = bw.bw_quant_act(to_dev(xf))
+    y = bw.bw_gemv_w2a8(q_d, packed, s_d, bf16_dev(ws), bounds, N, K)
+    torch.cuda.synchronize()
+    assert bw.bw_device_error() == 0
+    assert s_d.cpu().numpy()[5] < 2.0**-60
+    q_ref, s_ref = oracle.quant_act(xf)
+    y_ref = oracle.gemv(q_ref, canon, s_ref, ws, bounds, N, K)
+    assert_bf16_within_ulp(bits_of(y), y_ref)
+    for m in (4, 5, 6, 17):
+        y1 = bw.bw_gemv_w2a8(q_d[m:m + 1], packed, s_d[m:m + 1], bf16_dev(ws),
+                             bounds, N, K)
+        torch.cuda.synchronize()
+        assert torch.equal(y1.view(torch.int16), y[m:m + 1].view(torch.int16))
+
+
 @pytest.mark.parametrize("M", [512, 1024, 2048])
 def test_prefill_sizes(bw, M):
     """Prompt-sized batches (the W2A8 page's §一 splits prefill from decode):
