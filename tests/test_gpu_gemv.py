@@ -2,8 +2,9 @@
 
 Bars: packed bytes and int8 codes bit-exact; int32 accumulators bit-exact;
 activation scales bit-exact (same fp32 operations); bf16 outputs within one
-bf16 ulp of the oracle (relative 2^-8), the tolerance the benchmark spec fixes for the
-epilogue.  Shapes cover several tiles with ragged tails, the BitNet-2B decode
+bf16 ulp of the oracle (relative 2^-8); both sides round acc / s and then
+its product by ws in fp32 before the one bf16 rounding, so the bar is a
+margin.  Shapes cover several tiles with ragged tails, the BitNet-2B decode
 shapes at full size, the large shapes, batched M, and the edge cases
 (smallest sizes, ragged N and K, unaligned activations, the maximum K,
 eight scale segments, zero and all-ones weights, extreme activations).

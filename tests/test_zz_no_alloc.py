@@ -137,7 +137,7 @@ def test_noalloc_allocates_nothing(lib):
         assert rc == OK
 
     # A first call may load the library's code onto the device (lazy module
-    # loading), which the driver backs with device memory of its own.
+    # loading), which the CUDA driver backs with device memory of its own.
     call("bw_repack_noalloc")
     used = attr(USED_MEM_CURRENT)
     free_before = torch.cuda.mem_get_info()[0]
