@@ -94,7 +94,7 @@ struct TcCfg {
   static constexpr int kBarFullAB = kBarEmptyX + XS;         // [ABS]
   static constexpr int kBarDone = kBarFullAB + ABS;          // [ABS]
   static constexpr int kBarAcc = kBarDone + ABS;             // accumulators final
-  static constexpr int kBarSums = kBarAcc + 1;               // token sums stored
+  static constexpr int kBarSums = kBarAcc + 1;  // token sums added, scales stored
   static_assert(kBarSums < 32, "barrier block");
   static_assert(kDCol + TM <= kTcTmemCols, "tensor memory");
 };
@@ -230,7 +230,8 @@ tc_gemv_kernel(const __grid_constant__ CUtensorMap wmap,
         // one branch per 4 tokens, the same in every lane
         if (rv[0] != 0.0f && rv[1] != 0.0f && rv[2] != 0.0f && rv[3] != 0.0f) {
 #pragma unroll
-          for (int e = 0; e < 4; ++e) yv[e] = div_by_recip(a[e], sv[e], rv[e]) * wsv;
+          for (int e = 0; e < 4; ++e)
+            yv[e] = div_by_recip(a[e], sv[e], rv[e]) * wsv;
         } else {
 #pragma unroll
           for (int e = 0; e < 4; ++e)
