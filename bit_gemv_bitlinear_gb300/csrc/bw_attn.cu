@@ -15,7 +15,7 @@
 //    CTAs per KV head (attn_cluster_kernel, described at its definition):
 //    the splits merge through distributed shared memory.
 //  * Longer caches: the kernel below, whose splits merge through the
-//    caller's workspace:
+//    caller's workspace (both kernels' split plans: bw_attn_plan.cuh):
 //  * CTA (c, g) takes split c of the positions 0..p for KV head g and all
 //    G = H / Hkv query heads that read it, so every K and V row is loaded
 //    once for the G heads.  The number of splits is fixed at launch: one
@@ -53,6 +53,7 @@
 // (queries, exp weights) as a sum of two bf16 values and accumulate in fp32.
 // The caches are read through tensor maps (encoded per launch: 2-D, Hkv S
 // rows of D bf16).
+#include "bw_attn_plan.cuh"
 #include "bw_tc.cuh"
 
 namespace bw {
@@ -65,9 +66,6 @@ constexpr int kAttnD = 128;             // head dim
 constexpr int kAttnPairs = kAttnD / 2;
 constexpr int kAttnThreads = 256;
 constexpr int kAttnWarps = kAttnThreads / 32;
-constexpr int kAttnChunk = 160;         // positions per split, at most
-constexpr int kAttnMinChunk = 64;       // positions per used split, at least
-constexpr int kAttnSoloMax = 128;       // contexts one CTA per head finishes
 // Splits of a cache of S positions: at most ceil(S / 64) (the workspace is
 // sized for that), at least ceil(S / kAttnChunk).
 constexpr int kAttnMaxSplits = (BW_ATTN_MAX_S + kAttnMinChunk - 1) / kAttnMinChunk;
@@ -92,46 +90,6 @@ struct AttnArgs {
   // preceding kernel on the stream starts (BW_ATTN_PAST_READY).
   int past_ready;
 };
-
-__host__ __device__ inline int max_splits(int S) {
-  return (S + kAttnMinChunk - 1) / kAttnMinChunk;
-}
-
-// One CTA per SM over the KV heads where the cache is long enough, within
-// [ceil(S / kAttnChunk), ceil(S / kAttnMinChunk)].
-inline int attn_splits(int S, int Hkv, int sms) {
-  const int lo = (S + kAttnChunk - 1) / kAttnChunk;
-  const int hi = max_splits(S);
-  int n = sms / Hkv;
-  if (n > hi) n = hi;
-  if (n < lo) n = lo;
-  return n < 1 ? 1 : n;
-}
-
-// A CTA's share of positions 0..p: n_eff splits in use, positions
-// [j0, j0 + n) for this CTA (n = 0: none); valid: p lies in the cache; solo:
-// (cluster kernel) CTA 0 finishes the context alone.
-struct SplitPlan {
-  bool valid, solo;
-  int n_eff, j0, n;
-};
-
-// Split c of the workspace kernel's n_split: a context of at most
-// kAttnSoloMax positions is one split, longer ones take
-// min(n_split, ceil(len / kAttnMinChunk)) equal shares.
-__host__ __device__ inline SplitPlan ws_plan(int p, int S, int n_split, int c) {
-  SplitPlan r{p >= 0 && p < S, false, 0, 0, 0};
-  if (r.valid) {
-    const int len = p + 1;
-    const int want = (len + kAttnMinChunk - 1) / kAttnMinChunk;
-    r.n_eff = len <= kAttnSoloMax ? 1 : (want < n_split ? want : n_split);
-    if (c < r.n_eff) {
-      r.j0 = int(int64_t(c) * len / r.n_eff);
-      r.n = int(int64_t(c + 1) * len / r.n_eff) - r.j0;
-    }
-  }
-  return r;
-}
 
 // BW_ATTN_PAST_READY: a position read after the dependency wait that
 // differs from the one read before it means the caller's promise was
@@ -822,56 +780,8 @@ attn_decode_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap kmap,
 // workspace, fence or counter, and no partial leaves the chip.  A barrier
 // phase that every CTA arrives at before its split (and waits for before
 // its first push) guarantees that all CTAs of the cluster have started
-// before any shared memory of another is written.
-// A context of at most kClSoloMax positions (and an invalid position) is
-// finished by CTA 0 alone, straight from its shared memory, with no cluster
-// barrier: the other CTAs leave at once.  Every CTA reads the same position,
-// so the choice is the same in the whole cluster, and otherwise every CTA
-// executes every cluster barrier on every path: a barrier never waits for a
-// CTA that has left.
-// The kernel comes in two sizes of a CTA's staging, kClChunk positions
-// (caches of up to kClMaxS) and kClChunkSmall (a launch that serves short
-// contexts only: less shared memory, so its CTAs fit beside other kernels'
-// on an SM); a launch of cl CTAs per KV head serves contexts of at most
-// cl * chunk positions.
-constexpr int kClMaxCtas = 16;                  // CTAs per KV head
-constexpr int kClChunk = 256;                   // positions per CTA, at most
-constexpr int kClChunkSmall = 128;
-constexpr int kClMinChunk = 32;                 // positions per used CTA
-constexpr int kClSoloMax = 128;                 // contexts CTA 0 finishes alone
-constexpr int kClMaxS = kClMaxCtas * kClChunk;  // 4096
-static_assert(kClSoloMax <= kClChunkSmall, "CTA 0 stages a solo context");
-
-// CTAs per KV head for a cache of S <= kClMaxS positions.
-inline int cl_ctas(int S) {
-  const int n = (S + kClMinChunk - 1) / kClMinChunk;
-  return n < 1 ? 1 : (n > kClMaxCtas ? kClMaxCtas : n);
-}
-
-// CTA c of a cluster of cl: a context of at most kClSoloMax positions, and
-// an invalid position, are CTA 0's alone (solo); longer contexts take
-// min(cl, ceil(len / kClMinChunk)) equal shares.  A position is invalid
-// outside the cache and past the launch's cap = cl * chunk contexts (which
-// keeps every share within a CTA's staging).  Every CTA of the cluster
-// reads the same position, so solo is the same in all of them.
-__host__ __device__ inline SplitPlan cl_plan(int p, int S, int cl, int c,
-                                             int cap) {
-  SplitPlan r{p >= 0 && p < S && p < cap, false, 0, 0, 0};
-  r.solo = !r.valid || p < kClSoloMax;
-  if (r.solo) {
-    r.n_eff = 1;
-    r.n = (r.valid && c == 0) ? p + 1 : 0;
-    return r;
-  }
-  const int len = p + 1;
-  const int want = (len + kClMinChunk - 1) / kClMinChunk;
-  r.n_eff = want < cl ? want : cl;
-  if (c < r.n_eff) {
-    r.j0 = int(int64_t(c) * len / r.n_eff);
-    r.n = int(int64_t(c + 1) * len / r.n_eff) - r.j0;
-  }
-  return r;
-}
+// before any shared memory of another is written.  Which positions each CTA
+// takes (cl_plan) and how many CTAs a launch uses are in bw_attn_plan.cuh.
 
 // Outputs per slice for a cluster of cl CTAs: ceil(G D / cl) rounded up to
 // a multiple of 4 (so that slices move as 16-byte vectors).
@@ -1268,7 +1178,7 @@ cudaError_t launch_attn(const AttnLaunch &l, cudaStream_t stream) {
     cudaError_t le = cudaSuccess;
     if (max_len <= kClMaxCtas * kClChunkSmall && max_len < l.S) {
       // the smaller staging: CTAs of half the shared memory
-      const int cl = (max_len + kClChunkSmall - 1) / kClChunkSmall;
+      const int cl = cl_ctas_small(max_len);
       a.n_split = cl;
       if (try_cluster<kClChunkSmall>(G, dev, a, kmap, vmap, cl, stream, &le))
         return le;
