@@ -169,7 +169,10 @@ bw_status bw_quant_weight(const float *W, int N, int K, const int *ws_bounds,
  * weight scale per fused sub-projection).  The page's kernel multiplies by
  * s; with s = 127/absmax (§六 item 3) the dimensionally consistent reading
  * divides, which is what this call does.  Every fp32 step is IEEE (no fast
- * math) and there is a single rounding to bf16, to nearest even.
+ * math) and there is a single rounding to bf16, to nearest even.  The
+ * tensor-core tiles get the correctly rounded quotient acc / s from a stored
+ * RN(1 / s) and a corrected product (Markstein's final step of division),
+ * and divide where s lies outside [2^-60, 2^60]; the result is the same.
  *   x          int8 [M][K] device, 4-byte aligned.
  *   packed     device weight layout from bw_repack(N, K), 16-byte aligned.
  *   s          fp32 [M] device: activation scales (as bw_quant_act writes).
